@@ -1,0 +1,279 @@
+// fno_api.cu -- the C ABI: argument validation, plans, dispatch, errors.
+//
+// The boundary follows §4.3 of the TurboFNO article (gsyq.cn/news/457482): a
+// C function in a shared library that receives raw device pointers and runs
+// the fused layer on a stream, bypassing any framework dispatch.  Nothing here
+// allocates in the forward call, so a forward is capturable in a CUDA graph
+// (the article's §2.3 / §3.3 point about a compile-time output size).
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "fno_internal.cuh"
+#include "fno_fused.cuh"
+
+using namespace fno;
+
+namespace {
+
+constexpr int kVersion = 10000;   // 1.0.0
+constexpr int64_t kMaxN = 1024;
+
+// Host-side fault injection for the failure-path tests: FNO_FAULT_INJECT names
+// one site ("plan_alloc" or "launch") at which the library behaves as if the
+// CUDA call there had failed.  No device fault is involved.
+bool inject(const char *site) {
+    const char *v = std::getenv("FNO_FAULT_INJECT");
+    return v && std::strcmp(v, site) == 0;
+}
+
+bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
+
+fno_status_t make_geom(Geom *g, int ndim, const int64_t *n, const int32_t *modes) {
+    if (ndim < 1 || ndim > FNO_MAX_NDIM || !n || !modes) return FNO_ERR_INVALID_ARG;
+    std::memset(g, 0, sizeof(*g));
+    g->d = ndim;
+    g->nkept = g->npix = g->nblk = g->mblk = 1;
+    for (int a = 0; a < ndim; ++a) {
+        if (!is_pow2(n[a]) || n[a] < 2) return FNO_ERR_INVALID_ARG;
+        if (n[a] > kMaxN) return FNO_ERR_UNSUPPORTED;
+        const int64_t m = modes[a];
+        if (m < 1) return FNO_ERR_INVALID_ARG;
+        if (a < ndim - 1) {
+            if (2 * m > n[a]) return FNO_ERR_INVALID_ARG;   // corner blocks may not overlap
+            g->kdim[a] = 2 * m;
+            g->nblk *= 2;
+        } else {
+            if (m > n[a] / 2 + 1) return FNO_ERR_INVALID_ARG;
+            g->kdim[a] = m;
+        }
+        g->n[a] = n[a];
+        g->m[a] = (int32_t)m;
+        g->nkept *= g->kdim[a];
+        g->npix *= n[a];
+        g->mblk *= m;
+    }
+    return FNO_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fno_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? FNO_OK : FNO_ERR_CUDA; }
+
+size_t elem_bytes(fno_dtype_t t) { return t == FNO_F16 ? 2 : 4; }
+
+// Which kernel sequence a valid description runs on.
+int choose_path(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout,
+                uint32_t flags) {
+    if (flags & FNO_PLAN_UNFUSED) return kPathUnfused;
+    if (fused_supported(g, dtype, batch, cin, cout)) return kPathFused2D;
+    return kPathUnfused;
+}
+
+struct Sizes {
+    size_t workspace, weight;
+    int path, kernels;
+};
+
+fno_status_t describe(int ndim, const int64_t *n, const int32_t *modes, int64_t batch,
+                      int32_t cin, int32_t cout, fno_dtype_t dtype, uint32_t flags,
+                      Geom *g, Sizes *sz) {
+    fno_status_t st = make_geom(g, ndim, n, modes);
+    if (st != FNO_OK) return st;
+    if (batch < 1 || cin < 1 || cout < 1) return FNO_ERR_INVALID_ARG;
+    if (dtype != FNO_F32 && dtype != FNO_F16) return FNO_ERR_INVALID_ARG;
+    if (flags & ~FNO_PLAN_UNFUSED) return FNO_ERR_INVALID_ARG;
+    // int64 element counts must not overflow and a tensor must stay addressable
+    const double xe = (double)batch * cin * g->npix, ye = (double)batch * cout * g->npix;
+    if (xe > 4.0e12 || ye > 4.0e12) return FNO_ERR_UNSUPPORTED;
+    sz->path = choose_path(*g, dtype, batch, cin, cout, flags);
+    if (sz->path == kPathUnfused) {
+        sz->workspace = unfused_workspace_bytes(*g, batch, cin, cout);
+        sz->kernels = unfused_kernel_count(*g);
+    } else {
+        sz->workspace = fused_workspace_bytes(*g, dtype, batch, cin, cout);
+        sz->kernels = fused_kernel_count(*g, dtype, batch, cin, cout);
+    }
+    sz->weight = (size_t)g->nblk * cin * cout * g->mblk * 2 * elem_bytes(dtype);
+    return FNO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *fno_status_string(fno_status_t s) {
+    switch (s) {
+        case FNO_OK: return "FNO_OK";
+        case FNO_ERR_INVALID_ARG: return "FNO_ERR_INVALID_ARG: invalid argument";
+        case FNO_ERR_UNSUPPORTED: return "FNO_ERR_UNSUPPORTED: shape not supported";
+        case FNO_ERR_MISALIGNED: return "FNO_ERR_MISALIGNED: pointer not 16-byte aligned";
+        case FNO_ERR_OUT_OF_MEMORY: return "FNO_ERR_OUT_OF_MEMORY: allocation failed";
+        case FNO_ERR_CUDA: return "FNO_ERR_CUDA: CUDA call or launch failed";
+        case FNO_ERR_DEVICE_TIMEOUT: return "FNO_ERR_DEVICE_TIMEOUT: device wait gave up";
+        case FNO_ERR_DEVICE_BOUNDS: return "FNO_ERR_DEVICE_BOUNDS: device index check failed";
+        case FNO_ERR_ALIASING: return "FNO_ERR_ALIASING: output overlaps an input";
+    }
+    return "FNO_ERR_UNKNOWN: not a status code";
+}
+
+int fno_version(void) { return kVersion; }
+
+fno_status_t fno_spectral_conv_query(int ndim, const int64_t *n, const int32_t *modes,
+                                     int64_t batch, int32_t cin, int32_t cout,
+                                     fno_dtype_t dtype, uint32_t flags,
+                                     size_t *workspace_bytes, size_t *weight_bytes) {
+    Geom g;
+    Sizes sz;
+    fno_status_t st = describe(ndim, n, modes, batch, cin, cout, dtype, flags, &g, &sz);
+    if (st != FNO_OK) return st;
+    if (workspace_bytes) *workspace_bytes = sz.workspace;
+    if (weight_bytes) *weight_bytes = sz.weight;
+    return FNO_OK;
+}
+
+fno_status_t fno_spectral_conv_plan(fno_plan_t *out, int ndim, const int64_t *n,
+                                    const int32_t *modes, int64_t batch, int32_t cin,
+                                    int32_t cout, fno_dtype_t dtype, uint32_t flags) {
+    if (!out) return FNO_ERR_INVALID_ARG;
+    *out = nullptr;
+    Geom g;
+    Sizes sz;
+    fno_status_t st = describe(ndim, n, modes, batch, cin, cout, dtype, flags, &g, &sz);
+    if (st != FNO_OK) return st;
+    if (inject("plan_alloc")) return FNO_ERR_OUT_OF_MEMORY;
+
+    Plan *p = new (std::nothrow) Plan();
+    if (!p) return FNO_ERR_OUT_OF_MEMORY;
+    p->g = g;
+    p->batch = batch;
+    p->cin = cin;
+    p->cout = cout;
+    p->dtype = dtype;
+    p->flags = flags;
+    p->path = sz.path;
+    p->kernels_per_forward = sz.kernels;
+    p->workspace_bytes = sz.workspace;
+    p->weight_bytes = sz.weight;
+
+    if (cudaGetDevice(&p->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        delete p;
+        return FNO_ERR_CUDA;
+    }
+
+    // Twiddle tables, one per axis: tw[a][j] = exp(-2 pi i j / N_a), computed
+    // in double and rounded once to float; then the device error word.
+    size_t off[FNO_MAX_NDIM + 1];
+    size_t total = 0;
+    for (int a = 0; a < g.d; ++a) {
+        off[a] = total;
+        total += ((size_t)g.n[a] * sizeof(float2) + 255) & ~size_t(255);
+    }
+    off[g.d] = total;
+    total += 256;
+    std::vector<unsigned char> host(total, 0);
+    for (int a = 0; a < g.d; ++a) {
+        float2 *t = reinterpret_cast<float2 *>(host.data() + off[a]);
+        for (int64_t j = 0; j < g.n[a]; ++j) {
+            const double ang = -2.0 * M_PI * (double)j / (double)g.n[a];
+            t[j] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+        }
+    }
+    if (cudaMalloc(&p->dev_tables, total) != cudaSuccess) {
+        cudaGetLastError();
+        delete p;
+        return FNO_ERR_OUT_OF_MEMORY;
+    }
+    p->dev_tables_bytes = total;
+    unsigned char *base = static_cast<unsigned char *>(p->dev_tables);
+    for (int a = 0; a < FNO_MAX_NDIM; ++a)
+        p->tw[a] = a < g.d ? reinterpret_cast<float2 *>(base + off[a]) : nullptr;
+    p->dev_err = reinterpret_cast<int *>(base + off[g.d]);
+    cudaError_t e = cudaMemcpy(p->dev_tables, host.data(), total, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && p->path != kPathUnfused) e = fused_plan_init(*p);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(p->dev_tables);
+        delete p;
+        return FNO_ERR_CUDA;
+    }
+    *out = reinterpret_cast<fno_plan_t>(p);
+    return FNO_OK;
+}
+
+fno_status_t fno_spectral_conv_workspace_size(fno_plan_t plan, size_t *bytes) {
+    if (!plan || !bytes) return FNO_ERR_INVALID_ARG;
+    *bytes = reinterpret_cast<Plan *>(plan)->workspace_bytes;
+    return FNO_OK;
+}
+
+fno_status_t fno_spectral_conv_kernel_count(fno_plan_t plan, int *count) {
+    if (!plan || !count) return FNO_ERR_INVALID_ARG;
+    *count = reinterpret_cast<Plan *>(plan)->kernels_per_forward;
+    return FNO_OK;
+}
+
+static bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || !na || !nb) return false;
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+fno_status_t fno_spectral_conv_forward(fno_plan_t plan, const void *x, const void *w,
+                                       void *y, void *workspace, fno_stream_t stream) {
+    if (!plan || !x || !w || !y) return FNO_ERR_INVALID_ARG;
+    const Plan &p = *reinterpret_cast<Plan *>(plan);
+    if (p.workspace_bytes && !workspace) return FNO_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || !aligned16(workspace))
+        return FNO_ERR_MISALIGNED;
+    const size_t eb = elem_bytes(p.dtype);
+    const size_t xb = (size_t)p.batch * p.cin * p.g.npix * eb;
+    const size_t yb = (size_t)p.batch * p.cout * p.g.npix * eb;
+    if (overlaps(y, yb, x, xb) || overlaps(y, yb, w, p.weight_bytes) ||
+        overlaps(y, yb, workspace, p.workspace_bytes))
+        return FNO_ERR_ALIASING;
+    if (inject("launch")) return FNO_ERR_CUDA;
+    Buffers b{x, w, y, workspace};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = p.path == kPathUnfused ? unfused_forward(p, b, s) : fused_forward(p, b, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return FNO_ERR_CUDA;
+    }
+    return FNO_OK;
+}
+
+fno_status_t fno_plan_get_device_error(fno_plan_t plan, fno_stream_t stream) {
+    if (!plan) return FNO_ERR_INVALID_ARG;
+    const Plan &p = *reinterpret_cast<Plan *>(plan);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int v = 0;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemcpy(&v, p.dev_err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(p.dev_err, 0, sizeof(int));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return FNO_ERR_CUDA;
+    }
+    if (v == kDevTimeout) return FNO_ERR_DEVICE_TIMEOUT;
+    if (v == kDevBounds) return FNO_ERR_DEVICE_BOUNDS;
+    return FNO_OK;
+}
+
+fno_status_t fno_plan_destroy(fno_plan_t plan) {
+    if (!plan) return FNO_OK;
+    Plan *p = reinterpret_cast<Plan *>(plan);
+    cudaError_t e = cudaSuccess;
+    if (p->path != kPathUnfused) fused_plan_release(*p);
+    if (p->dev_tables) e = cudaFree(p->dev_tables);
+    delete p;
+    return from_cuda(e);
+}
+
+}  // extern "C"

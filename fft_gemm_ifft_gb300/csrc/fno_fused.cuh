@@ -1,0 +1,18 @@
+// fno_fused.cuh -- host-side entry points of the fused layer kernels.
+#pragma once
+
+#include "fno_internal.cuh"
+
+namespace fno {
+
+// True when the fused path handles this description.
+bool fused_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout);
+size_t fused_workspace_bytes(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin,
+                             int cout);
+int fused_kernel_count(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout);
+// Plan-time set-up (tables, attributes); called once from plan creation.
+cudaError_t fused_plan_init(Plan &p);
+void fused_plan_release(Plan &p);
+cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s);
+
+}  // namespace fno

@@ -1,0 +1,106 @@
+// fno_internal.cuh -- shared definitions of the CUDA library (not installed).
+//
+// Geometry of the layer (TurboFNO article, gsyq.cn/news/457482, §2.1-§2.3):
+// x (B, Cin, N_0..N_{d-1}) real -> kept modes X (B, Cin, K_0..K_{d-1}) complex,
+// K_a = 2 m_a on full axes (low rows then high rows), K_{d-1} = m_{d-1};
+// Y[b,o,k] = sum_i X[b,i,k] W[blk(k), i, o, local(k)]; y = inverse(Y).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fno.h"
+
+namespace fno {
+
+// Device error word codes (plan-owned int, first error wins).
+enum : int { kDevOk = 0, kDevTimeout = 1, kDevBounds = 2 };
+
+struct Geom {
+    int d;
+    int64_t n[FNO_MAX_NDIM];
+    int32_t m[FNO_MAX_NDIM];
+    int64_t kdim[FNO_MAX_NDIM];   // kept extent per axis
+    int64_t nkept;                // |K|
+    int64_t npix;                 // prod N
+    int64_t nblk;                 // weight blocks 2^(d-1)
+    int64_t mblk;                 // modes per block prod m
+};
+
+// Host-side plan state.
+struct Plan {
+    Geom g;
+    int64_t batch;
+    int32_t cin, cout;
+    fno_dtype_t dtype;
+    uint32_t flags;
+    int device;
+    int path;                     // which kernel sequence runs (kPath*)
+    int kernels_per_forward;
+    size_t workspace_bytes;
+    size_t weight_bytes;
+    // plan-owned device memory
+    float2 *tw[FNO_MAX_NDIM];     // tw[a][j] = exp(-2 pi i j / N_a), j < N_a
+    int *dev_err;                 // device error word
+    void *dev_tables;             // single allocation holding the above
+    size_t dev_tables_bytes;
+    int num_sms;
+};
+
+enum { kPathUnfused = 0, kPathFused2D = 1, kPathFused1D = 2 };
+
+// --------------------------------------------------------------------------
+// Small device helpers
+// --------------------------------------------------------------------------
+__device__ __forceinline__ float2 cmul(float2 a, float2 b) {
+    return make_float2(a.x * b.x - a.y * b.y, a.x * b.y + a.y * b.x);
+}
+// a * conj(b)
+__device__ __forceinline__ float2 cmulc(float2 a, float2 b) {
+    return make_float2(a.x * b.x + a.y * b.y, a.y * b.x - a.x * b.y);
+}
+__device__ __forceinline__ void cfma(float2 &acc, float2 a, float2 b) {
+    acc.x = fmaf(a.x, b.x, acc.x);
+    acc.x = fmaf(-a.y, b.y, acc.x);
+    acc.y = fmaf(a.x, b.y, acc.y);
+    acc.y = fmaf(a.y, b.x, acc.y);
+}
+
+template <typename T> struct Storage;
+template <> struct Storage<float> {
+    static __device__ __forceinline__ float load(const float *p) { return *p; }
+    static __device__ __forceinline__ void store(float *p, float v) { *p = v; }
+    static __device__ __forceinline__ float2 load2(const float *p) {
+        return *reinterpret_cast<const float2 *>(p);
+    }
+};
+template <> struct Storage<__half> {
+    static __device__ __forceinline__ float load(const __half *p) { return __half2float(*p); }
+    static __device__ __forceinline__ void store(__half *p, float v) { *p = __float2half_rn(v); }
+    static __device__ __forceinline__ float2 load2(const __half *p) {
+        return __half22float2(*reinterpret_cast<const __half2 *>(p));
+    }
+};
+
+// Sets the device error word once (first error wins).
+__device__ __forceinline__ void raise_dev_error(int *err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// --------------------------------------------------------------------------
+// Host-side entry points of the kernel translation units
+// --------------------------------------------------------------------------
+struct Buffers {
+    const void *x;
+    const void *w;
+    void *y;
+    void *ws;
+};
+
+// Unfused per-axis path (fno_unfused.cu).
+size_t unfused_workspace_bytes(const Geom &g, int64_t batch, int cin, int cout);
+int unfused_kernel_count(const Geom &g);
+cudaError_t unfused_forward(const Plan &p, const Buffers &b, cudaStream_t s);
+
+}  // namespace fno

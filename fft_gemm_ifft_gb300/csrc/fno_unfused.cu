@@ -1,0 +1,261 @@
+// fno_unfused.cu -- the layer as separate kernels, one per transform axis,
+// one for the mixing, through the workspace.
+//
+// This is the "separate kernels" arrangement that the TurboFNO article
+// (gsyq.cn/news/457482) measures against its fused kernel (§5.2 note): each
+// step of §2.1-§2.3 is its own launch and the intermediates round-trip
+// through device memory.  Every axis pass is a direct (dense) DFT over the
+// kept frequencies only, so it is exact up to float rounding for any
+// power-of-two extent; it serves as the ablation baseline and covers shapes
+// the fused kernels are not specialised for.
+#include <algorithm>
+
+#include "fno_internal.cuh"
+
+namespace fno {
+namespace {
+
+constexpr int kThreads = 256;
+
+struct KeptGeom {            // by-value kernel argument
+    int d;
+    int64_t kdim[FNO_MAX_NDIM];
+    int32_t m[FNO_MAX_NDIM];
+    int64_t nkept, mblk;
+};
+
+// Frequency of kept row r on a full axis: low rows 0..m-1, then high rows
+// N-m..N-1 (TurboFNO §2.2 keeps the low-frequency modes; the high rows are
+// the negative frequencies -m..-1 of the two-sided full axis).
+__device__ __forceinline__ int kept_freq(int r, int m, int n) {
+    return r < m ? r : n - 2 * m + r;
+}
+
+// Step a1, last axis: out[line][k] = sum_n x[line][n] e^{-2 pi i k n / N}, k < M.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+k_fwd_last(const T *__restrict__ x, float2 *__restrict__ out, int64_t nlines, int N,
+           int M, const float2 *__restrict__ tw) {
+    const int64_t total = nlines * M;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t line = idx / M;
+        const int k = (int)(idx - line * M);
+        const T *src = x + line * N;
+        float2 acc = make_float2(0.f, 0.f);
+        for (int n = 0; n < N; ++n) {
+            const float v = Storage<T>::load(src + n);
+            const float2 w = tw[(k * n) & (N - 1)];
+            acc.x = fmaf(v, w.x, acc.x);
+            acc.y = fmaf(v, w.y, acc.y);
+        }
+        out[idx] = acc;
+    }
+}
+
+// Step a1, one full axis: out[o][r][q] = sum_n in[o][n][q] e^{-2 pi i f(r) n / N}.
+__global__ void __launch_bounds__(kThreads)
+k_fwd_full(const float2 *__restrict__ in, float2 *__restrict__ out, int64_t outer, int N,
+           int64_t inner, int m, const float2 *__restrict__ tw) {
+    const int K = 2 * m;
+    const int64_t total = outer * K * inner;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t q = idx % inner;
+        const int64_t t = idx / inner;
+        const int r = (int)(t % K);
+        const int64_t o = t / K;
+        const int f = kept_freq(r, m, N);
+        const float2 *src = in + o * N * inner + q;
+        float2 acc = make_float2(0.f, 0.f);
+        for (int n = 0; n < N; ++n) cfma(acc, src[n * inner], tw[(f * n) & (N - 1)]);
+        out[idx] = acc;
+    }
+}
+
+// Step a2: Y[b][o][k] = sum_i X[b][i][k] W[blk(k)][i][o][local(k)].
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+k_mix(const float2 *__restrict__ X, const T *__restrict__ w, float2 *__restrict__ Y,
+      int64_t batch, int cin, int cout, KeptGeom g) {
+    const int64_t total = batch * cout * g.nkept;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t kk = idx % g.nkept;
+        const int64_t t = idx / g.nkept;
+        const int o = (int)(t % cout);
+        const int64_t b = t / cout;
+        int64_t rem = kk, local = 0, stride = 1;
+        int blk = 0;
+        for (int a = g.d - 1; a >= 0; --a) {
+            const int64_t r = rem % g.kdim[a];
+            rem /= g.kdim[a];
+            int64_t l = r;
+            if (a < g.d - 1 && r >= g.m[a]) {
+                l = r - g.m[a];
+                blk |= 1 << a;
+            }
+            local += l * stride;
+            stride *= g.m[a];
+        }
+        const float2 *xs = X + b * cin * g.nkept + kk;
+        const T *ws = w + ((((int64_t)blk * cin) * cout + o) * g.mblk + local) * 2;
+        const int64_t wstride = (int64_t)cout * g.mblk * 2;
+        float2 acc = make_float2(0.f, 0.f);
+        for (int i = 0; i < cin; ++i)
+            cfma(acc, xs[(int64_t)i * g.nkept], Storage<T>::load2(ws + i * wstride));
+        Y[idx] = acc;
+    }
+}
+
+// Step a3, one full axis: out[o][n][q] = sum_r in[o][r][q] e^{+2 pi i f(r) n / N}.
+__global__ void __launch_bounds__(kThreads)
+k_inv_full(const float2 *__restrict__ in, float2 *__restrict__ out, int64_t outer, int N,
+           int64_t inner, int m, const float2 *__restrict__ tw) {
+    const int K = 2 * m;
+    const int64_t total = outer * N * inner;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t q = idx % inner;
+        const int64_t t = idx / inner;
+        const int n = (int)(t % N);
+        const int64_t o = t / N;
+        const float2 *src = in + o * K * inner + q;
+        float2 acc = make_float2(0.f, 0.f);
+        for (int r = 0; r < K; ++r) {
+            const float2 w = tw[(kept_freq(r, m, N) * n) & (N - 1)];
+            cfma(acc, src[r * inner], make_float2(w.x, -w.y));   // conjugate twiddle
+        }
+        out[idx] = acc;
+    }
+}
+
+// Step a3, last axis: y[line][n] = scale * sum_{k<M} c(k) Re(Y[k] e^{+2 pi i k n/N}),
+// c(0) = c(N/2) = 1, c = 2 otherwise.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+k_inv_last(const float2 *__restrict__ in, T *__restrict__ y, int64_t nlines, int N, int M,
+           const float2 *__restrict__ tw, float scale) {
+    const int64_t total = nlines * N;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t line = idx / N;
+        const int n = (int)(idx - line * N);
+        const float2 *src = in + line * M;
+        float acc = 0.f;
+        for (int k = 0; k < M; ++k) {
+            const float c = (k == 0 || 2 * k == N) ? 1.f : 2.f;
+            const float2 v = src[k];
+            const float2 w = tw[(k * n) & (N - 1)];
+            // Re(v * conj(w)) with w = e^{-i theta}
+            acc = fmaf(c, fmaf(v.x, w.x, v.y * w.y), acc);
+        }
+        Storage<T>::store(y + idx, acc * scale);
+    }
+}
+
+int grid_for(int64_t total, int num_sms) {
+    const int64_t blocks = (total + kThreads - 1) / kThreads;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)num_sms * 16));
+}
+
+// Complex-element counts of every intermediate of the sequence.
+void stage_sizes(const Geom &g, int64_t batch, int cin, int cout, int64_t *max_elems) {
+    const int d = g.d;
+    const int64_t ml = g.m[d - 1];
+    int64_t best = 0;
+    // forward: after the last axis, then after each full axis from d-2 down to 0
+    int64_t s0 = batch * cin * ml;
+    for (int j = 0; j < d - 1; ++j) s0 *= g.n[j];
+    best = std::max(best, s0);
+    for (int a = d - 2; a >= 0; --a) {
+        int64_t s = batch * cin * ml;
+        for (int j = 0; j < d - 1; ++j) s *= (j < a) ? g.n[j] : g.kdim[j];
+        best = std::max(best, s);
+    }
+    best = std::max(best, batch * cin * g.nkept);
+    best = std::max(best, batch * cout * g.nkept);
+    // inverse: after expanding full axis a = 0..d-2
+    for (int a = 0; a < d - 1; ++a) {
+        int64_t s = batch * cout * ml;
+        for (int j = 0; j < d - 1; ++j) s *= (j <= a) ? g.n[j] : g.kdim[j];
+        best = std::max(best, s);
+    }
+    *max_elems = best;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+}  // namespace
+
+size_t unfused_workspace_bytes(const Geom &g, int64_t batch, int cin, int cout) {
+    int64_t e = 0;
+    stage_sizes(g, batch, cin, cout, &e);
+    return 2 * align256((size_t)e * sizeof(float2));
+}
+
+int unfused_kernel_count(const Geom &g) { return 2 * g.d + 1; }
+
+template <typename T>
+static cudaError_t unfused_forward_t(const Plan &p, const Buffers &bf, cudaStream_t s) {
+    const Geom &g = p.g;
+    const int d = g.d;
+    const int64_t ml = g.m[d - 1];
+    int64_t e = 0;
+    stage_sizes(g, p.batch, p.cin, p.cout, &e);
+    float2 *bufA = reinterpret_cast<float2 *>(bf.ws);
+    float2 *bufB = reinterpret_cast<float2 *>(reinterpret_cast<char *>(bf.ws) +
+                                              align256((size_t)e * sizeof(float2)));
+    const int sms = p.num_sms;
+
+    // a1, last axis (real -> half spectrum, truncated)
+    int64_t lines = p.batch * p.cin;
+    for (int j = 0; j < d - 1; ++j) lines *= g.n[j];
+    k_fwd_last<T><<<grid_for(lines * ml, sms), kThreads, 0, s>>>(
+        reinterpret_cast<const T *>(bf.x), bufA, lines, (int)g.n[d - 1], (int)ml, p.tw[d - 1]);
+    float2 *cur = bufA, *nxt = bufB;
+    // a1, full axes from d-2 down to 0
+    for (int a = d - 2; a >= 0; --a) {
+        int64_t outer = p.batch * p.cin, inner = ml;
+        for (int j = 0; j < a; ++j) outer *= g.n[j];
+        for (int j = a + 1; j < d - 1; ++j) inner *= g.kdim[j];
+        k_fwd_full<<<grid_for(outer * g.kdim[a] * inner, sms), kThreads, 0, s>>>(
+            cur, nxt, outer, (int)g.n[a], inner, g.m[a], p.tw[a]);
+        std::swap(cur, nxt);
+    }
+    // a2, mixing
+    KeptGeom kg;
+    kg.d = d;
+    for (int a = 0; a < FNO_MAX_NDIM; ++a) {
+        kg.kdim[a] = a < d ? g.kdim[a] : 1;
+        kg.m[a] = a < d ? g.m[a] : 1;
+    }
+    kg.nkept = g.nkept;
+    kg.mblk = g.mblk;
+    k_mix<T><<<grid_for(p.batch * p.cout * g.nkept, sms), kThreads, 0, s>>>(
+        cur, reinterpret_cast<const T *>(bf.w), nxt, p.batch, p.cin, p.cout, kg);
+    std::swap(cur, nxt);
+    // a3, full axes 0..d-2
+    for (int a = 0; a < d - 1; ++a) {
+        int64_t outer = p.batch * p.cout, inner = ml;
+        for (int j = 0; j < a; ++j) outer *= g.n[j];
+        for (int j = a + 1; j < d - 1; ++j) inner *= g.kdim[j];
+        k_inv_full<<<grid_for(outer * g.n[a] * inner, sms), kThreads, 0, s>>>(
+            cur, nxt, outer, (int)g.n[a], inner, g.m[a], p.tw[a]);
+        std::swap(cur, nxt);
+    }
+    // a3, last axis (half spectrum -> real), scale 1/prod(N)
+    lines = p.batch * p.cout;
+    for (int j = 0; j < d - 1; ++j) lines *= g.n[j];
+    k_inv_last<T><<<grid_for(lines * g.n[d - 1], sms), kThreads, 0, s>>>(
+        cur, reinterpret_cast<T *>(bf.y), lines, (int)g.n[d - 1], (int)ml, p.tw[d - 1],
+        (float)(1.0 / (double)g.npix));
+    return cudaGetLastError();
+}
+
+cudaError_t unfused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
+    return p.dtype == FNO_F32 ? unfused_forward_t<float>(p, b, s)
+                              : unfused_forward_t<__half>(p, b, s);
+}
+
+}  // namespace fno

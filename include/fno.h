@@ -1,0 +1,212 @@
+/*
+ * fno.h -- C ABI of the GB300 (sm_103a) Fourier Neural Operator library.
+ *
+ * The library computes the FNO spectral-convolution layer described in the
+ * TurboFNO article (gsyq.cn/news/457482):
+ *   §2.1  a real forward FFT over the spatial axes of a channels-first real
+ *         tensor (unnormalised, kernel e^{-2 pi i k.n/N});
+ *   §2.2  truncation to the retained low-frequency modes and a per-mode
+ *         complex contraction over the input channels with a learned complex
+ *         weight per mode (plain complex product, no conjugation);
+ *   §2.3  zero-padding of the discarded modes and an inverse real FFT back to
+ *         the grid (scale 1/prod(N)),
+ * fused on the device so that the intermediates stay on chip or in L2 (§3.4).
+ * §4.3 of the article exposes the fused layer as a C function of a shared
+ * library taking raw device pointers; this header is that boundary.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - No entry point throws, aborts or prints; each returns fno_status_t.
+ *  - Device pointers are caller-owned.  The library never frees them and never
+ *    keeps them beyond the call.
+ *  - fno_stream_t is a cudaStream_t (NULL = the legacy default stream).  All
+ *    device work is enqueued asynchronously on that stream.
+ *  - Tensors are dense, row-major (last axis contiguous), with no padding.
+ *  - Complex values are interleaved (re, im) pairs of the storage type.
+ *
+ * Kept modes (the "corner blocks").  For spatial extents N_0..N_{d-1} and
+ * per-block modes m_0..m_{d-1}:
+ *  - on each full axis a < d-1 the kept rows are the low rows 0..m_a-1 and
+ *    the high rows N_a-m_a..N_a-1 (negative frequencies -m_a..-1);
+ *  - on the last (half-spectrum) axis the kept bins are 0..m_{d-1}-1.
+ * A weight block is one choice of low/high per full axis; block
+ * beta = sum_a hi_a * 2^a (axis 0 varies fastest): 1 block in 1-D, 2 in 2-D
+ * (low rows, high rows), 4 in 3-D ((lo,lo), (hi,lo), (lo,hi), (hi,hi)).
+ * In the inverse, bins 0 and N_{d-1}/2 of the half axis carry weight 1 and
+ * every other bin weight 2, and the real part is taken (the convention of a
+ * real inverse FFT applied to a zero-filled half spectrum).
+ */
+#ifndef FNO_H_
+#define FNO_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FNO_MAX_NDIM 3
+
+typedef enum fno_status_e {
+    FNO_OK = 0,
+    FNO_ERR_INVALID_ARG = 1,     /* a null pointer, a bad rank/extent/modes/channels     */
+    FNO_ERR_UNSUPPORTED = 2,     /* valid shape this build does not handle               */
+    FNO_ERR_MISALIGNED = 3,      /* a device pointer is not 16-byte aligned              */
+    FNO_ERR_OUT_OF_MEMORY = 4,   /* plan-owned device or host memory could not be had    */
+    FNO_ERR_CUDA = 5,            /* a CUDA runtime call or kernel launch failed          */
+    FNO_ERR_DEVICE_TIMEOUT = 6,  /* a bounded device-side wait gave up                   */
+    FNO_ERR_DEVICE_BOUNDS = 7,   /* a device-side index check failed (debug builds)      */
+    FNO_ERR_ALIASING = 8         /* the output overlaps an input or the workspace        */
+} fno_status_t;
+
+typedef enum fno_dtype_e {
+    FNO_F32 = 0,   /* float32 storage, float32 arithmetic                                 */
+    FNO_F16 = 1    /* IEEE half storage (x, w, y), float32 accumulation                   */
+} fno_dtype_t;
+
+typedef void *fno_stream_t;                 /* a cudaStream_t                            */
+typedef struct fno_plan_s *fno_plan_t;      /* opaque spectral-convolution plan          */
+typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan                     */
+
+/* Plan flags. */
+#define FNO_PLAN_DEFAULT 0u
+/* Run the layer as separate per-axis transform, mixing and inverse kernels
+ * through the workspace instead of the fused path (the "separate kernels"
+ * ablation of the article's §5.2 note).  Results agree with the fused path
+ * within rounding.                                                           */
+#define FNO_PLAN_UNFUSED 1u
+
+/* Human-readable name of a status code; never NULL. */
+const char *fno_status_string(fno_status_t status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int fno_version(void);
+
+/* -------------------------------------------------------------------------
+ * Spectral convolution (one layer).
+ * ------------------------------------------------------------------------- */
+
+/* Validate a layer description and report its memory needs without touching
+ * the GPU (no CUDA call is made).
+ *   ndim          1, 2 or 3
+ *   n[ndim]       spatial extents; each a power of two, 2 <= N <= 256
+ *   modes[ndim]   per-block modes; 1 <= m_a and 2 m_a <= N_a on full axes,
+ *                 1 <= m_{d-1} <= N_{d-1}/2 + 1 on the last axis
+ *   batch, cin, cout  >= 1
+ *   dtype         FNO_F32 or FNO_F16
+ *   flags         FNO_PLAN_* bits
+ * Outputs (each may be NULL):
+ *   workspace_bytes  device scratch the forward call needs (caller-owned)
+ *   weight_bytes     size of w: nblk*cin*cout*prod(m)*2*sizeof(storage)
+ * Returns FNO_OK, FNO_ERR_INVALID_ARG or FNO_ERR_UNSUPPORTED.             */
+fno_status_t fno_spectral_conv_query(int ndim, const int64_t *n, const int32_t *modes,
+                                     int64_t batch, int32_t cin, int32_t cout,
+                                     fno_dtype_t dtype, uint32_t flags,
+                                     size_t *workspace_bytes, size_t *weight_bytes);
+
+/* Create a plan on the current CUDA device.  Arguments as in
+ * fno_spectral_conv_query.  The plan computes its twiddle tables on the host
+ * in double precision, rounds them once to float and copies them to
+ * plan-owned device memory; it synchronises the device once, here, and is
+ * immutable afterwards.  *plan is set to NULL on failure.
+ * Errors: INVALID_ARG, UNSUPPORTED, OUT_OF_MEMORY, CUDA.                  */
+fno_status_t fno_spectral_conv_plan(fno_plan_t *plan, int ndim, const int64_t *n,
+                                    const int32_t *modes, int64_t batch, int32_t cin,
+                                    int32_t cout, fno_dtype_t dtype, uint32_t flags);
+
+/* Bytes of device workspace fno_spectral_conv_forward needs for this plan. */
+fno_status_t fno_spectral_conv_workspace_size(fno_plan_t plan, size_t *bytes);
+
+/* Number of kernels one forward call launches for this plan. */
+fno_status_t fno_spectral_conv_kernel_count(fno_plan_t plan, int *count);
+
+/* y = SpectralConv(x; w), enqueued on `stream`.
+ *   x          device, (batch, cin, N_0..N_{d-1}) storage dtype
+ *   w          device, (nblk, cin, cout, m_0..m_{d-1}) complex storage dtype,
+ *              block order as described at the top of this header
+ *   y          device, (batch, cout, N_0..N_{d-1}) storage dtype; fully
+ *              overwritten; must not overlap x, w or the workspace
+ *   workspace  device, at least fno_spectral_conv_workspace_size bytes, or
+ *              NULL when that size is 0; its contents on entry are ignored
+ *              and on exit are unspecified.  Two calls that run at the same
+ *              time need two workspaces.
+ * Every pointer must be 16-byte aligned (FNO_ERR_MISALIGNED otherwise).
+ * The call makes no allocation and no host synchronisation, so it may be
+ * captured in a CUDA graph.  Launch failures return FNO_ERR_CUDA; faults
+ * detected inside kernels are reported by fno_plan_get_device_error.        */
+fno_status_t fno_spectral_conv_forward(fno_plan_t plan, const void *x, const void *w,
+                                       void *y, void *workspace, fno_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the plan's device error word.
+ * Returns FNO_OK, FNO_ERR_DEVICE_TIMEOUT, FNO_ERR_DEVICE_BOUNDS or CUDA.   */
+fno_status_t fno_plan_get_device_error(fno_plan_t plan, fno_stream_t stream);
+
+/* Release the plan and its device memory.  NULL is accepted (no-op).  The
+ * caller must make sure no work that uses the plan is still running.       */
+fno_status_t fno_plan_destroy(fno_plan_t plan);
+
+/* -------------------------------------------------------------------------
+ * FNO forward stack (2-D grid), the workload of the article's §5 tasks:
+ *   a_0     = Lift x + lift_b                         (1x1, cin_lift -> width)
+ *   t_l     = SpectralConv_l(a_l) + Pw_l a_l + pw_b_l (l = 0 .. nlayers-1)
+ *   a_{l+1} = GELU(t_l) for l < nlayers-1, t_l for the last layer
+ *   out     = Proj2 GELU(Proj1 a_L + proj1_b) + proj2_b
+ * GELU is the exact form v/2 (1 + erf(v / sqrt 2)).  1x1 linear weights are
+ * (out, in) row-major float32.
+ * ------------------------------------------------------------------------- */
+typedef struct fno_model_desc_s {
+    int64_t batch;       /* B                                                   */
+    int32_t cin_lift;    /* input channels (3: field + two coordinates)         */
+    int32_t width;       /* hidden channels of the spectral layers              */
+    int32_t nlayers;     /* number of spectral layers                           */
+    int32_t hidden;      /* projection hidden width                             */
+    int32_t cout;        /* output channels                                     */
+    int64_t h, w;        /* grid                                                */
+    int32_t modes[2];    /* per-block modes (rows, half-axis bins)              */
+    fno_dtype_t dtype;   /* FNO_F32 only in this version                        */
+    uint32_t flags;      /* FNO_PLAN_* bits, applied to every spectral layer    */
+} fno_model_desc_t;
+
+typedef struct fno_model_params_s {
+    const float *lift_w;   /* (width, cin_lift)                                  */
+    const float *lift_b;   /* (width)                                            */
+    const float *spec_w;   /* nlayers x (2, width, width, m0, m1) complex        */
+    const float *pw_w;     /* nlayers x (width, width)                           */
+    const float *pw_b;     /* nlayers x (width)                                  */
+    const float *proj1_w;  /* (hidden, width)                                    */
+    const float *proj1_b;  /* (hidden)                                           */
+    const float *proj2_w;  /* (cout, hidden)                                     */
+    const float *proj2_b;  /* (cout)                                             */
+} fno_model_params_t;
+
+/* Validate the description and create the stack's plan (one spectral plan
+ * shared by the layers).  Errors as for fno_spectral_conv_plan.            */
+fno_status_t fno_model_plan(fno_model_t *model, const fno_model_desc_t *desc);
+
+/* Device workspace bytes fno_forward needs (activations + layer scratch).  */
+fno_status_t fno_model_workspace_size(fno_model_t model, size_t *bytes);
+
+/* Number of kernels one fno_forward call launches. */
+fno_status_t fno_model_kernel_count(fno_model_t model, int *count);
+
+/* out = FNO(x), enqueued on `stream`.
+ *   x    device, (batch, cin_lift, h, w) float32
+ *   p    host struct of device pointers (all 16-byte aligned)
+ *   out  device, (batch, cout, h, w) float32; must not overlap the inputs
+ *   workspace  device, fno_model_workspace_size bytes
+ * No allocation, no host synchronisation (graph-capturable).               */
+fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_params_t *p,
+                         void *out, void *workspace, fno_stream_t stream);
+
+/* Synchronise `stream`, read and clear the device error word of the stack. */
+fno_status_t fno_model_get_device_error(fno_model_t model, fno_stream_t stream);
+
+/* Release the stack's plan; NULL is accepted. */
+fno_status_t fno_model_destroy(fno_model_t model);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FNO_H_ */

@@ -1,0 +1,48 @@
+"""GPU parity of the FNO forward stack (fno_forward) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fft_gemm_ifft_gb300 import FnoModel, workloads
+from parity_util import assert_close, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(fno, oracle_mod):
+    yield
+
+
+def run_model(case, x, params, batch):
+    m = FnoModel(batch, case.h, case.w, case.modes, case.cin_lift, case.width, case.nlayers,
+                 case.hidden, case.cout)
+    dev = {k: to_dev(v) for k, v in params.items()}
+    y = m(to_dev(x), dev)
+    torch.cuda.synchronize()
+    assert m.device_error() == 0
+    kernels = m.kernel_count
+    m.close()
+    return y.cpu().numpy(), kernels
+
+
+def test_small_stack_matches_oracle():
+    case = workloads.FnoCase("small", batch=2, width=8, nlayers=2, h=32, w=32, modes=(4, 4),
+                             hidden=16, cout=2)
+    x = workloads.make_fno_inputs(case)
+    p = workloads.make_fno_params(case)
+    got, _ = run_model(case, x, p, case.batch)
+    ref = oracle.fno_forward(x, workloads.fno_params_for_oracle(p), case.modes)
+    assert_close(got, ref, "f32", "small FNO stack")
+
+
+def test_full_stack_sampled():
+    case = workloads.FNO_CASE
+    x = workloads.make_fno_inputs(case)
+    p = workloads.make_fno_params(case)
+    got, _ = run_model(case, x, p, case.batch)
+    q = workloads.fno_params_for_oracle(p)
+    for b in (0, case.batch - 1):
+        ref = oracle.fno_forward(x[b:b + 1], q, case.modes)
+        assert_close(got[b:b + 1], ref, "f32", f"FNO b={b}")

@@ -1,0 +1,177 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle on
+the same seeded inputs (element by element), plus edge cases and the error
+paths of the forward call."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fft_gemm_ifft_gb300 import FNO_PLAN_UNFUSED, FnoError, SpectralConv, capi, workloads
+from parity_util import assert_close, run_gpu, run_oracle, to_dev
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    # (n, modes, batch, cin, cout, dtype)
+    ((256,), (16,), 4, 16, 16, "f32"),
+    ((16,), (9,), 2, 3, 5, "f32"),
+    ((8,), (5,), 1, 1, 1, "f32"),
+    ((128, 128), (16, 16), 3, 32, 32, "f32"),
+    ((128, 128), (16, 16), 1, 5, 7, "f32"),
+    ((128, 128), (1, 1), 2, 4, 4, "f32"),
+    ((16, 32), (3, 7), 3, 5, 3, "f32"),
+    ((32, 16), (16, 9), 2, 2, 3, "f32"),
+    ((64, 64), (16, 16), 2, 8, 8, "f32"),
+    ((256, 256), (32, 32), 1, 8, 8, "f16"),
+    ((256, 256), (32, 32), 2, 3, 5, "f16"),
+    ((64, 64), (8, 8), 2, 4, 6, "f16"),
+    ((64, 64, 64), (16, 16, 16), 1, 4, 4, "f32"),
+    ((8, 8, 8), (2, 3, 4), 2, 3, 2, "f32"),
+    ((4, 8, 16), (2, 4, 9), 2, 2, 2, "f32"),
+    ((32, 32, 32), (8, 8, 8), 2, 3, 4, "f16"),
+]
+
+
+def case_id(c):
+    n, m, b, ci, co, dt = c
+    return f"{'x'.join(map(str, n))}_m{'x'.join(map(str, m))}_b{b}_{ci}to{co}_{dt}"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(fno, oracle_mod):
+    yield
+
+
+@pytest.mark.parametrize("flags", [0, FNO_PLAN_UNFUSED], ids=["default", "unfused"])
+@pytest.mark.parametrize("spec", SMALL, ids=[case_id(c) for c in SMALL])
+def test_small_cases_match_oracle(spec, flags):
+    n, modes, b, ci, co, dt = spec
+    case = workloads.small_case(n, modes, b, ci, co, dt, index=7)
+    x = workloads.make_x(case, seed=100 + sum(n))
+    w = workloads.make_w(case, seed=200 + sum(modes))
+    # a random weight with negative parts too, so sign errors cannot cancel
+    w = (w * case.cin * case.cout * 2 - 1).astype(case.np_dtype) / np.float32(case.cin)
+    w = w.astype(case.np_dtype)
+    got, _ = run_gpu(case, x, w, flags)
+    ref = run_oracle(case, x, w)
+    assert_close(got, ref, dt, case_id(spec))
+
+
+@pytest.mark.parametrize("n", [(8,), (16,), (8, 8), (16, 32), (4, 4, 8), (8, 4, 16)])
+def test_all_modes_identity_reproduces_input(n):
+    modes = tuple(v // 2 for v in n[:-1]) + (n[-1] // 2 + 1,)
+    cin = 3
+    case = workloads.small_case(n, modes, 2, cin, cin, "f32")
+    x = workloads.make_x(case, seed=5)
+    w = np.zeros(case.weight_shape + (2,), dtype=np.float32)
+    for i in range(cin):
+        w[:, i, i, ..., 0] = 1.0
+    got, _ = run_gpu(case, x, w)
+    assert np.max(np.abs(got - x)) < 1e-5 * np.max(np.abs(x))
+
+
+def test_single_hot_mode_each_block_3d():
+    # one block's weight at a time: every other block must contribute nothing
+    case = workloads.small_case((16, 16, 16), (4, 4, 4), 1, 2, 2, "f32")
+    x = workloads.make_x(case, seed=11)
+    for blk in range(4):
+        w = np.zeros(case.weight_shape + (2,), dtype=np.float32)
+        w[blk, :, :, 1, 2, 3, 0] = 0.5
+        w[blk, :, :, 1, 2, 3, 1] = -0.25
+        got, _ = run_gpu(case, x, w)
+        ref = run_oracle(case, x, w)
+        assert_close(got, ref, "f32", f"block {blk}")
+
+
+@pytest.mark.parametrize("name", ["1d_f32", "2d_f32"])
+def test_full_size_workload_full_compare(name):
+    case = workloads.CASES[name]
+    x, w = workloads.make_x(case), workloads.make_w(case)
+    got, _ = run_gpu(case, x, w)
+    ref = run_oracle(case, x, w)
+    assert_close(got, ref, case.dtype, name)
+
+
+@pytest.mark.parametrize("name,samples", [("2d_f16", (0, 31)), ("3d_f32", (0, 3))])
+def test_full_size_workload_sampled(name, samples):
+    # the GPU runs the whole batch; the oracle checks whole samples of it
+    # (each sample's output depends only on that sample's input)
+    case = workloads.CASES[name]
+    x, w = workloads.make_x(case), workloads.make_w(case)
+    got, _ = run_gpu(case, x, w)
+    for b in samples:
+        ref = run_oracle(case, x[b:b + 1], w)
+        assert_close(got[b:b + 1], ref, case.dtype, f"{name}[b={b}]")
+
+
+def test_fused_and_unfused_agree_and_are_deterministic():
+    case = workloads.CASES["2d_f32"]
+    x, w = workloads.make_x(case), workloads.make_w(case)
+    a, _ = run_gpu(case, x, w)
+    b, _ = run_gpu(case, x, w)
+    c, _ = run_gpu(case, x, w, FNO_PLAN_UNFUSED)
+    assert np.array_equal(a, b), "two runs of the same plan differ"
+    assert_close(a, c.astype(np.float64), "f32", "fused vs unfused")
+
+
+def test_output_red_zones_untouched():
+    case = workloads.small_case((64, 64), (8, 8), 2, 3, 4, "f32")
+    x, w = workloads.make_x(case, seed=3), workloads.make_w(case, seed=4)
+    conv = SpectralConv(case.n, case.modes, 2, 3, 4)
+    guard = 1024
+    ny = int(np.prod(case.y_shape))
+    buf = torch.full((ny + 2 * guard,), 12345.0, device="cuda")
+    y = buf[guard:guard + ny].view(case.y_shape)
+    conv(to_dev(x), to_dev(w), y)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:guard] == 12345.0) and torch.all(buf[guard + ny:] == 12345.0)
+    assert_close(y.cpu().numpy(), run_oracle(case, x, w), "f32", "red zone case")
+    conv.close()
+
+
+def test_forward_error_paths():
+    case = workloads.small_case((32, 32), (4, 4), 1, 2, 2, "f32")
+    conv = SpectralConv(case.n, case.modes, 1, 2, 2)
+    x = to_dev(workloads.make_x(case, seed=1))
+    w = to_dev(workloads.make_w(case, seed=2))
+    y = torch.empty(case.y_shape, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    ws = conv.workspace.data_ptr() if conv.workspace is not None else None
+    st = capi.fno_spectral_conv_forward(conv.handle, x.data_ptr() + 4, w.data_ptr(),
+                                        y.data_ptr(), ws, s)
+    assert st == capi.FNO_ERR_MISALIGNED
+    st = capi.fno_spectral_conv_forward(conv.handle, x.data_ptr(), w.data_ptr(),
+                                        x.data_ptr(), ws, s)
+    assert st == capi.FNO_ERR_ALIASING
+    st = capi.fno_spectral_conv_forward(conv.handle, 0, w.data_ptr(), y.data_ptr(), ws, s)
+    assert st == capi.FNO_ERR_INVALID_ARG
+    with pytest.raises(TypeError):
+        conv(x.double(), w)
+    conv.close()
+
+
+def test_injected_launch_failure_reports_and_recovers(monkeypatch):
+    case = workloads.small_case((32, 32), (4, 4), 1, 2, 2, "f32")
+    x, w = workloads.make_x(case, seed=1), workloads.make_w(case, seed=2)
+    conv = SpectralConv(case.n, case.modes, 1, 2, 2)
+    monkeypatch.setenv("FNO_FAULT_INJECT", "launch")
+    with pytest.raises(FnoError) as ei:
+        conv(to_dev(x), to_dev(w))
+    assert ei.value.status == capi.FNO_ERR_CUDA
+    monkeypatch.delenv("FNO_FAULT_INJECT")
+    y = conv(to_dev(x), to_dev(w))
+    torch.cuda.synchronize()
+    assert conv.device_error() == capi.FNO_OK
+    assert_close(y.cpu().numpy(), run_oracle(case, x, w), "f32", "after recovery")
+    conv.close()
+
+
+def test_plan_create_destroy_many_times_no_leak():
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(50):
+        st, h = capi.fno_spectral_conv_plan(2, [128, 128], [16, 16], 8, 32, 32, capi.FNO_F32)
+        assert st == capi.FNO_OK
+        assert capi.fno_plan_destroy(h) == capi.FNO_OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free0 - free1 < 8 << 20
