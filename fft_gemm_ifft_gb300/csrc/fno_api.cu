@@ -175,7 +175,7 @@ fno_status_t fno_spectral_conv_plan(fno_plan_t *out, int ndim, const int64_t *n,
         total += ((size_t)g.n[a] * sizeof(float2) + 255) & ~size_t(255);
     }
     off[g.d] = total;
-    total += 256;
+    total += 512;                 // device error word, then the fused-path counters
     std::vector<unsigned char> host(total, 0);
     for (int a = 0; a < g.d; ++a) {
         float2 *t = reinterpret_cast<float2 *>(host.data() + off[a]);
@@ -194,6 +194,7 @@ fno_status_t fno_spectral_conv_plan(fno_plan_t *out, int ndim, const int64_t *n,
     for (int a = 0; a < FNO_MAX_NDIM; ++a)
         p->tw[a] = a < g.d ? reinterpret_cast<float2 *>(base + off[a]) : nullptr;
     p->dev_err = reinterpret_cast<int *>(base + off[g.d]);
+    p->sync = base + off[g.d] + 256;
     cudaError_t e = cudaMemcpy(p->dev_tables, host.data(), total, cudaMemcpyHostToDevice);
     if (e == cudaSuccess && p->path != kPathUnfused) e = fused_plan_init(*p);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();

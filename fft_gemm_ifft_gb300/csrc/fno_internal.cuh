@@ -43,9 +43,14 @@ struct Plan {
     // plan-owned device memory
     float2 *tw[FNO_MAX_NDIM];     // tw[a][j] = exp(-2 pi i j / N_a), j < N_a
     int *dev_err;                 // device error word
+    void *sync;                   // fused-path queue counters (256 bytes, zero between launches)
     void *dev_tables;             // single allocation holding the above
     size_t dev_tables_bytes;
     int num_sms;
+    // fused path launch shape (set by fused_plan_init)
+    int fused_grid;
+    size_t fused_smem;
+    int fused_ob;
 };
 
 enum { kPathUnfused = 0, kPathFused2D = 1, kPathFused1D = 2 };

@@ -90,7 +90,7 @@ int fno_version(void);
 /* Validate a layer description and report its memory needs without touching
  * the GPU (no CUDA call is made).
  *   ndim          1, 2 or 3
- *   n[ndim]       spatial extents; each a power of two, 2 <= N <= 256
+ *   n[ndim]       spatial extents; each a power of two, 2 <= N <= 1024
  *   modes[ndim]   per-block modes; 1 <= m_a and 2 m_a <= N_a on full axes,
  *                 1 <= m_{d-1} <= N_{d-1}/2 + 1 on the last axis
  *   batch, cin, cout  >= 1
@@ -129,8 +129,11 @@ fno_status_t fno_spectral_conv_kernel_count(fno_plan_t plan, int *count);
  *              overwritten; must not overlap x, w or the workspace
  *   workspace  device, at least fno_spectral_conv_workspace_size bytes, or
  *              NULL when that size is 0; its contents on entry are ignored
- *              and on exit are unspecified.  Two calls that run at the same
- *              time need two workspaces.
+ *              and on exit are unspecified.
+ * Calls that may run at the same time on the GPU (different streams) need
+ * their own plan and their own workspace: the fused kernel keeps its work-
+ * queue counters in plan-owned device memory and resets them at the end of
+ * every call.  Calls on one stream, or stream-ordered, may share both.
  * Every pointer must be 16-byte aligned (FNO_ERR_MISALIGNED otherwise).
  * The call makes no allocation and no host synchronisation, so it may be
  * captured in a CUDA graph.  Launch failures return FNO_ERR_CUDA; faults

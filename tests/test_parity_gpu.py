@@ -19,6 +19,10 @@ SMALL = [
     ((128, 128), (16, 16), 3, 32, 32, "f32"),
     ((128, 128), (16, 16), 1, 5, 7, "f32"),
     ((128, 128), (1, 1), 2, 4, 4, "f32"),
+    ((128, 128), (16, 16), 2, 6, 5, "f16"),
+    ((128, 128), (16, 16), 2, 64, 64, "f32"),
+    ((128, 128), (16, 16), 1, 64, 37, "f32"),
+    ((128, 128), (16, 16), 9, 3, 2, "f32"),
     ((16, 32), (3, 7), 3, 5, 3, "f32"),
     ((32, 16), (16, 9), 2, 2, 3, "f32"),
     ((64, 64), (16, 16), 2, 8, 8, "f32"),
