@@ -8,9 +8,9 @@
 // all-to-all dependencies.  This kernel resolves them inside one launch with
 // a ticket-ordered work queue:
 //
-//   phase A  (image, row chunk)   x rows  -> partial kept modes   (HBM read)
-//   phase B  (mode group, o blk)  sum partials, mix with W -> Y   (L2 + W read)
-//   phase C  (image, row chunk)   Y -> output rows                (HBM write)
+//   phase A  (image, row chunk)           x rows -> partial kept modes   (HBM read)
+//   phase B  (mode pair, o block, b block) sum partials, mix with W -> Y (L2 + W)
+//   phase C  (image, row chunk)           Y -> output rows              (HBM write)
 //
 // Every CTA takes the next ticket from an atomic counter; tickets are ordered
 // A, then B, then C, and a B (C) item waits -- with a bounded spin -- until
@@ -29,7 +29,11 @@
 // RC = A*B2 with B2-point register FFTs.  The inverse runs the same steps
 // backwards with conjugate twiddles, applies the half-spectrum weights
 // c(0) = 1, c(k) = 2 and the 1/(N0*N1) scale, and stores the rows.
-#include <cstdio>
+//
+// Shared-memory layouts are chosen so that the 32 lanes of a warp touch 32
+// distinct banks (padded row strides, bin index fastest); loads of the
+// mixing and inverse phases are issued as cp.async copies all at once, and
+// the weights of a mixing item are fetched before it waits for phase A.
 #include <type_traits>
 
 #include "fno_fft.cuh"
@@ -39,15 +43,16 @@ namespace fno {
 namespace {
 
 using fft::cadd;
-using fft::cconj;
 using fft::cmac;
 using fft::cmul;
 using fft::cmulc;
 using fft::cscale;
-using fft::csub;
 
-constexpr int kNT = 128;                       // threads per CTA
-constexpr long long kWaitTimeoutNs = 500000000; // bounded device waits: 0.5 s
+constexpr int kNT = 128;                        // threads per CTA
+constexpr long long kWaitTimeoutNs = 500000000;  // bounded device waits: 0.5 s
+constexpr int kG = 2;                           // kept modes per phase-B item
+constexpr size_t kWsBudget = 16u << 10;         // phase-B weight slab (bytes)
+constexpr size_t kXpBudget = 24u << 10;         // phase-B partial modes (bytes)
 
 // Counters shared by the CTAs of one launch (plan-owned, zero between launches).
 struct SyncBlock {
@@ -69,7 +74,9 @@ struct Cfg {
     static constexpr int P = N1 / Q;             // row partial sums per bin
     static constexpr int B2 = B2_;               // column FFT length
     static constexpr int A = RC / B2;            // column partial sums
-    static constexpr int XS = N1 + 8;            // padded smem row stride (floats)
+    static constexpr int XS = N1 + 8;            // x row stride in smem (floats)
+    static constexpr int ZS = M1 + 4;            // Z row stride in smem (float2)
+    static constexpr int TS = M1 + 1;            // per-lane twiddle row stride (float2)
     static constexpr int PAIRS = RC * P / 2;     // row-FFT work units (2 rows each)
     static constexpr int KB = P / 2;             // bins per reduce-scatter block
     static_assert(N0 % RC == 0 && N1 % Q == 0 && RC % B2 == 0, "tiling");
@@ -77,10 +84,15 @@ struct Cfg {
     static_assert(M1 <= Q, "row FFT must cover the kept bins");
     static_assert(P >= 2 && P <= 32 && (32 % P) == 0, "P lanes share a row");
     static_assert(M1 % KB == 0, "bins split into reduce-scatter blocks");
-    static_assert(PAIRS % 128 == 0, "whole CTAs in the row pass (warp shuffles)");
-    // smem floats for each phase
-    static constexpr int kSmemA = RC * XS + 2 * RC * M1 + 2 * A * M1 * B2;
-    static constexpr int kSmemC = 4 * RC * M1 + 2 * A * M1 * B2;
+    static_assert(PAIRS % kNT == 0, "whole CTAs in the row pass (warp shuffles)");
+    static_assert((RC * N1 / 4) % kNT == 0, "whole load rounds");
+    static_assert(NK % kG == 0 && M1 % kG == 0, "mode pairs stay in one kept row");
+    // bytes of each phase's shared memory
+    static constexpr size_t kSmemA =
+        RC * XS * 4 + RC * ZS * 8 + (size_t)A * B2 * M1 * 8;
+    static constexpr size_t kSmemC =
+        NK * 8 + RC * M1 * 8 + (size_t)A * B2 * M1 * 8 + RC * ZS * 8;
+    static constexpr size_t kSmemTw = ((N0 + P * TS) * 8 + 15) / 16 * 16;
 };
 
 // Frequency of kept row j on axis 0: low rows 0..M0-1, then N0-M0..N0-1.
@@ -91,33 +103,29 @@ __device__ __forceinline__ int kept_freq(int j) {
 
 template <typename T> struct Io;
 template <> struct Io<float> {
-    // 8 consecutive values -> float
-    static __device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
-        const float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
-        const float4 b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    }
-    static __device__ __forceinline__ float2 w2(const float *p) {
-        return *reinterpret_cast<const float2 *>(p);
+    using W2 = float4;                               // two complex weights
+    static __device__ __forceinline__ float4 load4(const float *p) {
+        return __ldcs(reinterpret_cast<const float4 *>(p));
     }
     static __device__ __forceinline__ void store(float *p, float v) { __stcs(p, v); }
+    static __device__ __forceinline__ float2 wget(const float4 &w, int g) {
+        return g == 0 ? make_float2(w.x, w.y) : make_float2(w.z, w.w);
+    }
 };
 template <> struct Io<__half> {
-    static __device__ __forceinline__ void load8(const __half *p, float (&v)[8]) {
-        const uint4 a = __ldcs(reinterpret_cast<const uint4 *>(p));
-        const __half2 *h = reinterpret_cast<const __half2 *>(&a);
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __half22float2(h[i]);
-            v[2 * i] = f.x;
-            v[2 * i + 1] = f.y;
-        }
-    }
-    static __device__ __forceinline__ float2 w2(const __half *p) {
-        return __half22float2(*reinterpret_cast<const __half2 *>(p));
+    using W2 = uint2;                                // two complex weights (4 halves)
+    static __device__ __forceinline__ float4 load4(const __half *p) {
+        const uint2 a = __ldcs(reinterpret_cast<const uint2 *>(p));
+        const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&a.x));
+        const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&a.y));
+        return make_float4(lo.x, lo.y, hi.x, hi.y);
     }
     static __device__ __forceinline__ void store(__half *p, float v) {
         *p = __float2half_rn(v);
+    }
+    static __device__ __forceinline__ float2 wget(const uint2 &w, int g) {
+        const unsigned u = g == 0 ? w.x : w.y;
+        return __half22float2(*reinterpret_cast<const __half2 *>(&u));
     }
 };
 
@@ -131,6 +139,25 @@ __device__ __forceinline__ long long globaltimer() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+__device__ __forceinline__ unsigned smem_addr(const void *p) {
+    return (unsigned)__cvta_generic_to_shared(p);
+}
+// 16-byte asynchronous copy global -> shared through L2 only (data written by
+// other CTAs of this launch must not be served from a stale L1 line)
+__device__ __forceinline__ void cp_async16(void *s, const void *g) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(s)), "l"(g)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async8(void *s, const void *g) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(s)), "l"(g)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
 
 // Thread 0 waits until *ctr >= target; gives up (sets the error word) after
 // kWaitTimeoutNs or as soon as another CTA has reported an error.
@@ -143,7 +170,7 @@ __device__ bool wait_count(const int *ctr, int target, int *err) {
             return true;
         }
         if (*reinterpret_cast<volatile int *>(err) != 0) return false;
-        __nanosleep(64);
+        __nanosleep(32);
         if ((spin & 255u) == 255u && globaltimer() - t0 > kWaitTimeoutNs) {
             raise_dev_error(err, kDevTimeout);
             return false;
@@ -151,37 +178,41 @@ __device__ bool wait_count(const int *ctr, int target, int *err) {
     }
 }
 
+struct Tw {
+    const float2 *t0;   // [N0]      W_N0^e
+    const float2 *t1;   // [P][TS]   W_N1^{n1 k}
+};
+
 // ---------------------------------------------------------------------------
 // Phase A: one chunk of rows of one input image -> partial kept modes
 // ---------------------------------------------------------------------------
 template <class Cf, typename T>
 __device__ void phase_a(const T *__restrict__ x, float2 *__restrict__ part, int nimg, int img,
-                        int c, float *smem, const float2 *tw0, const float2 *tw1) {
-    constexpr int N1 = Cf::N1, RC = Cf::RC, C = Cf::C, P = Cf::P, Q = Cf::Q, M1 = Cf::M1;
-    constexpr int XS = Cf::XS, A = Cf::A, B2 = Cf::B2, K0 = Cf::K0, NK = Cf::NK;
-    float *xs = smem;                                             // [RC][XS]
-    float2 *zs = reinterpret_cast<float2 *>(smem + RC * XS);      // [RC][M1]
-    float2 *ss = zs + RC * M1;                                    // [A][M1][B2]
+                        int c, char *smem, Tw tw) {
+    constexpr int N0 = Cf::N0, N1 = Cf::N1, RC = Cf::RC, C = Cf::C, P = Cf::P, Q = Cf::Q;
+    constexpr int M1 = Cf::M1, XS = Cf::XS, ZS = Cf::ZS, A = Cf::A, B2 = Cf::B2;
+    constexpr int NK = Cf::NK, KB = Cf::KB;
+    float *xs = reinterpret_cast<float *>(smem);                         // [RC][XS]
+    float2 *zs = reinterpret_cast<float2 *>(smem + RC * XS * 4);         // [RC][ZS]
+    float2 *ss = zs + RC * ZS;                                           // [A][B2][M1]
     const int tid = threadIdx.x;
 
-    // 1. rows c, c+C, c+2C, ... of the image into shared memory (as float)
-    const T *src = x + (size_t)img * Cf::N0 * N1;
-    constexpr int kLoads = RC * (N1 / 8) / kNT;
-    static_assert(RC * (N1 / 8) % kNT == 0, "whole load rounds");
-    float v[kLoads][8];
+    // 1. rows c, c+C, c+2C, ... of the image into shared memory (as float);
+    //    every load of the chunk is in flight before the first store
+    const T *src = x + (size_t)img * N0 * N1;
+    constexpr int kLoads = RC * N1 / 4 / kNT;
+    float4 v[kLoads];
 #pragma unroll
-    for (int r = 0; r < kLoads; ++r) {          // all loads in flight before any store
+    for (int r = 0; r < kLoads; ++r) {
         const int e = tid + r * kNT;
-        const int t = e / (N1 / 8), s = e % (N1 / 8);
-        Io<T>::load8(src + (size_t)(c + C * t) * N1 + 8 * s, v[r]);
+        const int t = e / (N1 / 4), s = e % (N1 / 4);
+        v[r] = Io<T>::load4(src + (size_t)(c + C * t) * N1 + 4 * s);
     }
 #pragma unroll
     for (int r = 0; r < kLoads; ++r) {
         const int e = tid + r * kNT;
-        const int t = e / (N1 / 8), s = e % (N1 / 8);
-        float4 *dst = reinterpret_cast<float4 *>(xs + t * XS + 8 * s);
-        dst[0] = make_float4(v[r][0], v[r][1], v[r][2], v[r][3]);
-        dst[1] = make_float4(v[r][4], v[r][5], v[r][6], v[r][7]);
+        const int t = e / (N1 / 4), s = e % (N1 / 4);
+        *reinterpret_cast<float4 *>(xs + t * XS + 4 * s) = v[r];
     }
     __syncthreads();
 
@@ -194,35 +225,35 @@ __device__ void phase_a(const T *__restrict__ x, float2 *__restrict__ part, int 
         for (int n2 = 0; n2 < Q; ++n2)
             z[n2] = make_float2(xs[t * XS + n1 + P * n2], xs[t2 * XS + n1 + P * n2]);
         fft::fft_dif<Q, -1>(z);
-        const int lane_in_group = n1;   // == lane % P
-        fft::unroll<0, M1 / Cf::KB>([&](auto kbi) {
+        const float2 *twl = tw.t1 + n1 * Cf::TS;
+        fft::unroll<0, M1 / KB>([&](auto kbi) {
             constexpr int kb = decltype(kbi)::value;
             // contributions of this lane for bins kb*KB .. kb*KB+KB-1 of both rows
-            float2 v[2 * Cf::KB];
-            fft::unroll<0, Cf::KB>([&](auto qi) {
-                constexpr int k = kb * Cf::KB + decltype(qi)::value;
+            float2 vv[2 * KB];
+            fft::unroll<0, KB>([&](auto qi) {
+                constexpr int q = decltype(qi)::value;
+                constexpr int k = kb * KB + q;
                 float2 a, b;
                 fft::split_real_pair<Q, k % Q>(z, a, b);
-                const float2 w = tw1[(n1 * k) & (N1 - 1)];
-                v[decltype(qi)::value] = cmul(a, w);
-                v[Cf::KB + decltype(qi)::value] = cmul(b, w);
+                const float2 w = twl[k];
+                vv[q] = cmul(a, w);
+                vv[KB + q] = cmul(b, w);
             });
-            // reduce-scatter over the P lanes: lane l ends with element l of v
+            // reduce-scatter over the P lanes: lane l ends with element l of vv
             fft::unroll<0, fft::ilog2(P)>([&](auto ri) {
                 constexpr int half = P >> (decltype(ri)::value + 1);
-                const bool upper = (lane_in_group & half) != 0;
+                const bool upper = (n1 & half) != 0;
 #pragma unroll
                 for (int i = 0; i < half; ++i) {
-                    const float2 send = upper ? v[i] : v[i + half];
-                    float2 keep = upper ? v[i + half] : v[i];
+                    const float2 send = upper ? vv[i] : vv[i + half];
+                    float2 keep = upper ? vv[i + half] : vv[i];
                     keep.x += __shfl_xor_sync(0xffffffffu, send.x, half);
                     keep.y += __shfl_xor_sync(0xffffffffu, send.y, half);
-                    v[i] = keep;
+                    vv[i] = keep;
                 }
             });
-            const int row = lane_in_group < Cf::KB ? t : t2;
-            const int k = kb * Cf::KB + (lane_in_group % Cf::KB);
-            zs[row * M1 + k] = v[0];
+            const int row = n1 < KB ? t : t2;
+            zs[row * ZS + kb * KB + (n1 % KB)] = vv[0];
         });
     }
     __syncthreads();
@@ -232,77 +263,110 @@ __device__ void phase_a(const T *__restrict__ x, float2 *__restrict__ part, int 
         const int t1 = u / M1, k = u % M1;
         float2 z[B2];
 #pragma unroll
-        for (int i = 0; i < B2; ++i) z[i] = zs[(t1 + A * i) * M1 + k];
+        for (int i = 0; i < B2; ++i) z[i] = zs[(t1 + A * i) * ZS + k];
         fft::fft_dif<B2, -1>(z);
 #pragma unroll
-        for (int q = 0; q < B2; ++q) ss[(t1 * M1 + k) * B2 + q] = z[fft::bitrev(q, fft::ilog2(B2))];
+        for (int q = 0; q < B2; ++q)
+            ss[(t1 * B2 + q) * M1 + k] = z[fft::bitrev(q, fft::ilog2(B2))];
     }
     __syncthreads();
 
-    // 3b. X_c[j][k] = W_N0^{f c} sum_t1 W_RC^{f t1} S[t1][k][f mod B2], f = freq of kept row j
+    // 3b. X_c[j][k] = W_N0^{f c} sum_t1 W_RC^{f t1} S[t1][f mod B2][k], f = freq of kept row j
     float2 *dst = part + ((size_t)c * nimg + img) * NK;
-    constexpr int kRcStep = Cf::N0 / RC;         // W_RC^e = tw0[e * N0/RC]
+    constexpr int kRcStep = N0 / RC;             // W_RC^e = W_N0^{e N0/RC}
     for (int o = tid; o < NK; o += kNT) {
         const int j = o / M1, k = o % M1;
         const int f = kept_freq<Cf>(j);
         float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int t1 = 0; t1 < A; ++t1)
-            cmac(acc, ss[(t1 * M1 + k) * B2 + (f % B2)],
-                 tw0[((f % RC) * t1 * kRcStep) & (Cf::N0 - 1)]);
-        __stcg(dst + o, cmul(acc, tw0[(f * c) & (Cf::N0 - 1)]));
+            cmac(acc, ss[(t1 * B2 + (f % B2)) * M1 + k],
+                 tw.t0[((f % RC) * t1 * kRcStep) & (N0 - 1)]);
+        __stcg(dst + o, cmul(acc, tw.t0[(f * c) & (N0 - 1)]));
     }
-    (void)K0;
 }
 
 // ---------------------------------------------------------------------------
-// Phase B: Y[b][o][mode] = sum_i X[b][i][mode] W[blk][i][o][local], X = sum of partials
+// Phase B: Y[b][o][mode] = sum_i X[b][i][mode] W[blk][i][o][local], X = sum of partials.
+// One item: kG consecutive bins of one kept row, outputs [o0, o0+nob), batch rows
+// [b0, b0+nbb).  The weight slab is requested before the wait on phase A.
 // ---------------------------------------------------------------------------
-template <class Cf, int G, typename T>
-__device__ void phase_b(const float2 *__restrict__ part, const T *__restrict__ w,
-                        float2 *__restrict__ Y, int batch, int cin, int cout, int nimg_in,
-                        int group, int oblk, int ob, float *smem) {
-    constexpr int M0 = Cf::M0, M1 = Cf::M1, NK = Cf::NK, C = Cf::C;
-    const int mode0 = group * G;                 // G consecutive bins of one kept row
+struct BItem {
+    int group, o0, nob, b0, nbb;
+};
+
+template <class Cf, typename T>
+__device__ void phase_b_weights(const T *__restrict__ w, int cin, int cout, const BItem &it,
+                                int ob, char *smem) {
+    using W2 = typename Io<T>::W2;
+    constexpr int M0 = Cf::M0, M1 = Cf::M1;
+    const int mode0 = it.group * kG;
     const int j = mode0 / M1, k0 = mode0 % M1;
     const int blk = j >= M0 ? 1 : 0, l0 = j - blk * M0;
-    const int o0 = oblk * ob;
-    const int nob = min(ob, cout - o0);
-    float2 *ws = reinterpret_cast<float2 *>(smem);            // [cin][ob][G]
-    float2 *xs = ws + (size_t)cin * ob * G;                   // [batch][cin][G]
-    const int tid = threadIdx.x;
+    W2 *ws = reinterpret_cast<W2 *>(smem);                   // [cin][ob]
     const size_t mblk = (size_t)M0 * M1;
-    for (int e = tid; e < cin * nob * G; e += kNT) {
-        const int g = e % G, r = e / G, o = r % nob, i = r / nob;
-        const T *p = w + ((((size_t)blk * cin + i) * cout + o0 + o) * mblk + l0 * M1 + k0 + g) * 2;
-        ws[(i * ob + o) * G + g] = Io<T>::w2(p);
+    for (int e = threadIdx.x; e < cin * it.nob; e += kNT) {
+        const int o = e % it.nob, i = e / it.nob;
+        const T *p = w + ((((size_t)blk * cin + i) * cout + it.o0 + o) * mblk + l0 * M1 + k0) * 2;
+        if constexpr (sizeof(W2) == 16)
+            cp_async16(ws + i * ob + o, p);
+        else
+            cp_async8(ws + i * ob + o, p);
     }
-    for (int e = tid; e < batch * cin * G; e += kNT) {
-        const int g = e % G, r = e / G;            // r = b * cin + i
-        float2 acc = __ldcg(part + (size_t)r * NK + mode0 + g);
+    cp_async_commit();
+}
+
+template <class Cf, typename T>
+__device__ void phase_b(const float2 *__restrict__ part, float2 *__restrict__ Y, int cin,
+                        int cout, int nimg_in, const BItem &it, int ob, char *smem) {
+    using W2 = typename Io<T>::W2;
+    constexpr int NK = Cf::NK, C = Cf::C;
+    const int mode0 = it.group * kG;
+    const W2 *ws = reinterpret_cast<const W2 *>(smem);                       // [cin][ob]
+    float4 *xp = reinterpret_cast<float4 *>(smem + ((size_t)cin * ob * sizeof(W2) + 15) / 16 * 16);
+    const int tid = threadIdx.x;
+    const int nr = it.nbb * cin;                         // rows (b, i) of this item
+    // partial modes of the C chunks: xp[cc][r] = X_cc[b0*cin + r][mode0 .. mode0+1]
+    for (int e = tid; e < C * nr; e += kNT) {
+        const int r = e % nr, cc = e / nr;
+        cp_async16(xp + e, part + ((size_t)cc * nimg_in + (size_t)it.b0 * cin + r) * NK + mode0);
+    }
+    cp_async_commit();
+    cp_async_wait_all();                                 // also covers the weight slab
+    __syncthreads();
+    for (int r = tid; r < nr; r += kNT) {
+        float4 s = xp[r];
 #pragma unroll
-        for (int cc = 1; cc < C; ++cc)
-            acc = cadd(acc, __ldcg(part + ((size_t)cc * nimg_in + r) * NK + mode0 + g));
-        xs[e] = acc;
+        for (int cc = 1; cc < C; ++cc) {
+            const float4 q = xp[cc * nr + r];
+            s.x += q.x; s.y += q.y; s.z += q.z; s.w += q.w;
+        }
+        xp[r] = s;
     }
     __syncthreads();
-    constexpr int BB = 8;                          // batch rows per register block
-    for (int u = tid; u < nob * G; u += kNT) {
-        const int o = u / G, g = u % G;
-        for (int b0 = 0; b0 < batch; b0 += BB) {
-            float2 acc[BB];
+    constexpr int BB = 4;                                // batch rows per thread
+    const int nbq = (it.nbb + BB - 1) / BB;
+    for (int u = tid; u < it.nob * kG * nbq; u += kNT) {
+        const int g = u % kG, o = (u / kG) % it.nob, bq = u / (kG * it.nob);
+        float2 acc[BB];
 #pragma unroll
-            for (int bb = 0; bb < BB; ++bb) acc[bb] = make_float2(0.f, 0.f);
-            for (int i = 0; i < cin; ++i) {
-                const float2 wv = ws[(i * ob + o) * G + g];
+        for (int bb = 0; bb < BB; ++bb) acc[bb] = make_float2(0.f, 0.f);
+        for (int i = 0; i < cin; ++i) {
+            const float2 wv = Io<T>::wget(ws[i * ob + o], g);
 #pragma unroll
-                for (int bb = 0; bb < BB; ++bb)
-                    if (b0 + bb < batch) cmac(acc[bb], xs[((b0 + bb) * cin + i) * G + g], wv);
+            for (int bb = 0; bb < BB; ++bb) {
+                const int b = bq * BB + bb;
+                if (b < it.nbb) {
+                    const float4 xv = xp[b * cin + i];
+                    cmac(acc[bb], g == 0 ? make_float2(xv.x, xv.y) : make_float2(xv.z, xv.w), wv);
+                }
             }
+        }
 #pragma unroll
-            for (int bb = 0; bb < BB; ++bb)
-                if (b0 + bb < batch)
-                    __stcg(Y + ((size_t)(b0 + bb) * cout + o0 + o) * NK + mode0 + g, acc[bb]);
+        for (int bb = 0; bb < BB; ++bb) {
+            const int b = bq * BB + bb;
+            if (b < it.nbb)
+                __stcg(Y + ((size_t)(it.b0 + b) * cout + it.o0 + o) * NK + mode0 + g, acc[bb]);
         }
     }
 }
@@ -312,27 +376,30 @@ __device__ void phase_b(const float2 *__restrict__ part, const T *__restrict__ w
 // ---------------------------------------------------------------------------
 template <class Cf, typename T>
 __device__ void phase_c(const float2 *__restrict__ Y, T *__restrict__ y, int img, int c,
-                        float *smem, const float2 *tw0, const float2 *tw1) {
+                        char *smem, Tw tw) {
     constexpr int N0 = Cf::N0, N1 = Cf::N1, RC = Cf::RC, C = Cf::C, P = Cf::P, Q = Cf::Q;
-    constexpr int M1 = Cf::M1, A = Cf::A, B2 = Cf::B2, K0 = Cf::K0, NK = Cf::NK;
-    float2 *vs = reinterpret_cast<float2 *>(smem);            // [RC][M1] residue-ordered
-    float2 *ss = vs + RC * M1;                                // [A][M1][B2]
-    float2 *zo = ss + A * M1 * B2;                            // [RC][M1]
+    constexpr int M0 = Cf::M0, M1 = Cf::M1, A = Cf::A, B2 = Cf::B2, K0 = Cf::K0;
+    constexpr int NK = Cf::NK, ZS = Cf::ZS;
+    float2 *ys = reinterpret_cast<float2 *>(smem);           // [K0][M1]
+    float2 *vs = ys + NK;                                    // [RC][M1] residue-ordered
+    float2 *ss = vs + RC * M1;                               // [A][B2][M1]
+    float2 *zo = ss + A * B2 * M1;                           // [RC][ZS]
     const int tid = threadIdx.x;
     const float2 *src = Y + (size_t)img * NK;
 
-    // 1. V[q][k] = Y[j][k] conj(W_N0^{f c}), q = f mod RC (distinct for the kept rows)
+    // 1. the image's kept modes, all copies in flight at once
+    for (int e = tid; e < NK / 2; e += kNT) cp_async16(ys + 2 * e, src + 2 * e);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    // V[q][k] = Y[j][k] conj(W_N0^{f c}), q = f mod RC (distinct for the kept rows)
     for (int e = tid; e < RC * M1; e += kNT) {
         const int q = e / M1, k = e % M1;
-        // kept row j with f(j) == q (mod RC), if any
         int j = -1;
-        if (q < Cf::M0) j = q;
-        else if (q >= RC - Cf::M0) j = K0 - (RC - q);
+        if (q < M0) j = q;
+        else if (q >= RC - M0) j = K0 - (RC - q);
         float2 v = make_float2(0.f, 0.f);
-        if (j >= 0) {
-            const int f = kept_freq<Cf>(j);
-            v = cmulc(__ldcg(src + j * M1 + k), tw0[(f * c) & (N0 - 1)]);
-        }
+        if (j >= 0) v = cmulc(ys[j * M1 + k], tw.t0[(kept_freq<Cf>(j) * c) & (N0 - 1)]);
         vs[e] = v;
     }
     __syncthreads();
@@ -344,20 +411,21 @@ __device__ void phase_c(const float2 *__restrict__ Y, T *__restrict__ y, int img
         for (int i = 0; i < B2; ++i) z[i] = vs[(q1 + A * i) * M1 + k];
         fft::fft_dif<B2, 1>(z);
 #pragma unroll
-        for (int r = 0; r < B2; ++r) ss[(q1 * M1 + k) * B2 + r] = z[fft::bitrev(r, fft::ilog2(B2))];
+        for (int r = 0; r < B2; ++r)
+            ss[(q1 * B2 + r) * M1 + k] = z[fft::bitrev(r, fft::ilog2(B2))];
     }
     __syncthreads();
-    // 2b. Zo[t][k] = sum_q1 W_RC^{-q1 t} S[q1][k][t mod B2]
+    // 2b. Zo[t][k] = sum_q1 W_RC^{-q1 t} S[q1][t mod B2][k]
     constexpr int kRcStep = N0 / RC;
     for (int e = tid; e < RC * M1; e += kNT) {
         const int t = e / M1, k = e % M1;
         float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int q1 = 0; q1 < A; ++q1) {
-            const float2 wv = tw0[(q1 * t * kRcStep) & (N0 - 1)];
-            cmac(acc, ss[(q1 * M1 + k) * B2 + (t % B2)], make_float2(wv.x, -wv.y));
+            const float2 wv = tw.t0[(q1 * t * kRcStep) & (N0 - 1)];
+            cmac(acc, ss[(q1 * B2 + (t % B2)) * M1 + k], make_float2(wv.x, -wv.y));
         }
-        zo[e] = acc;
+        zo[t * ZS + k] = acc;
     }
     __syncthreads();
     // 3. rows: y[t][n1 + P n2] = s Re sum_k c_k W_N1^{-k n1} Zo[t][k] W_Q^{-k n2}
@@ -365,6 +433,7 @@ __device__ void phase_c(const float2 *__restrict__ Y, T *__restrict__ y, int img
     T *dst = y + (size_t)img * N0 * N1;
     for (int pr = tid; pr < Cf::PAIRS; pr += kNT) {
         const int t = pr / P, n1 = pr % P, t2 = t + RC / 2;
+        const float2 *twl = tw.t1 + n1 * Cf::TS;
         float2 ga[Q], gb[Q];
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
@@ -374,9 +443,9 @@ __device__ void phase_c(const float2 *__restrict__ Y, T *__restrict__ y, int img
 #pragma unroll
         for (int k = 0; k < M1; ++k) {
             const float ck = (k == 0 || 2 * k == N1) ? 1.f : 2.f;
-            const float2 w = tw1[(k * n1) & (N1 - 1)];
-            ga[k % Q] = cadd(ga[k % Q], cscale(cmulc(zo[t * M1 + k], w), ck));
-            gb[k % Q] = cadd(gb[k % Q], cscale(cmulc(zo[t2 * M1 + k], w), ck));
+            const float2 w = twl[k];
+            ga[k % Q] = cadd(ga[k % Q], cscale(cmulc(zo[t * ZS + k], w), ck));
+            gb[k % Q] = cadd(gb[k % Q], cscale(cmulc(zo[t2 * ZS + k], w), ck));
         }
         // Hermitian parts, packed: z[q] = Herm(ga)[q] + i Herm(gb)[q]
         float2 z[Q];
@@ -414,21 +483,25 @@ struct Args {
     int *err;
     int batch, cin, cout;
     int nA, nB, nC;
-    int ob;             // outputs per phase-B item
-    int nob;            // phase-B items per mode group
+    int ob, nob;        // phase B: outputs per item, output blocks
+    int bb, nbb;        // phase B: batch rows per item, batch blocks
 };
 
-template <class Cf, int G, typename T>
+template <class Cf, typename T>
 __global__ void __launch_bounds__(kNT)
 k_fused2d(Args a) {
-    extern __shared__ __align__(16) float smem[];
+    extern __shared__ __align__(16) char smem[];
     __shared__ int s_item;
     float2 *tw0 = reinterpret_cast<float2 *>(smem);
     float2 *tw1 = tw0 + Cf::N0;
-    float *work = reinterpret_cast<float *>(tw1 + Cf::N1);
+    char *work = smem + Cf::kSmemTw;
     const int tid = threadIdx.x;
     for (int e = tid; e < Cf::N0; e += kNT) tw0[e] = a.tw0[e];
-    for (int e = tid; e < Cf::N1; e += kNT) tw1[e] = a.tw1[e];
+    for (int e = tid; e < Cf::P * Cf::TS; e += kNT) {
+        const int n1 = e / Cf::TS, k = e % Cf::TS;
+        tw1[e] = a.tw1[(n1 * k) & (Cf::N1 - 1)];
+    }
+    const Tw tw{tw0, tw1};
     const int nimg_in = a.batch * a.cin;
     const int total = a.nA + a.nB + a.nC;
     for (;;) {
@@ -439,21 +512,31 @@ k_fused2d(Args a) {
         if (item >= total) break;
         if (item < a.nA) {
             phase_a<Cf, T>(static_cast<const T *>(a.x), a.part, nimg_in, item / Cf::C,
-                           item % Cf::C, work, tw0, tw1);
+                           item % Cf::C, work, tw);
             __syncthreads();
             if (tid == 0) {
                 __threadfence();
                 atomicAdd(&a.sync->done_a, 1);
             }
         } else if (item < a.nA + a.nB) {
-            const int it = item - a.nA;
+            int it = item - a.nA;
+            BItem bi;
+            const int bblk = it % a.nbb;
+            it /= a.nbb;
+            const int oblk = it % a.nob;
+            bi.group = it / a.nob;
+            bi.o0 = oblk * a.ob;
+            bi.nob = min(a.ob, a.cout - bi.o0);
+            bi.b0 = bblk * a.bb;
+            bi.nbb = min(a.bb, a.batch - bi.b0);
+            // the weights do not depend on phase A: request them first
+            phase_b_weights<Cf, T>(static_cast<const T *>(a.w), a.cin, a.cout, bi, a.ob, work);
             if (tid == 0) s_item = wait_count(&a.sync->done_a, a.nA, a.err) ? 1 : 0;
             __syncthreads();
             const bool ok = s_item != 0;
             __syncthreads();
-            if (ok)
-                phase_b<Cf, G, T>(a.part, static_cast<const T *>(a.w), a.Y, a.batch, a.cin,
-                                  a.cout, nimg_in, it / a.nob, it % a.nob, a.ob, work);
+            if (ok) phase_b<Cf, T>(a.part, a.Y, a.cin, a.cout, nimg_in, bi, a.ob, work);
+            else cp_async_wait_all();
             __syncthreads();
             if (tid == 0) {
                 __threadfence();
@@ -466,8 +549,7 @@ k_fused2d(Args a) {
             const bool ok = s_item != 0;
             __syncthreads();
             if (ok)
-                phase_c<Cf, T>(a.Y, static_cast<T *>(a.y), it / Cf::C, it % Cf::C, work, tw0,
-                               tw1);
+                phase_c<Cf, T>(a.Y, static_cast<T *>(a.y), it / Cf::C, it % Cf::C, work, tw);
         }
         __syncthreads();
     }
@@ -491,30 +573,33 @@ k_fused2d(Args a) {
 // 128 x 128 grid, 16 x 16 modes per block: chunks of 32 strided rows,
 // 16-point row FFTs (8 partial sums per bin), 8-point column FFTs.
 using Cfg128 = Cfg<128, 128, 16, 16, 32, 16, 8>;
-constexpr int kG128 = 4;   // modes per phase-B item
-
-template <class Cf, int G>
-struct Variant {
-    static size_t smem_bytes(int cin, int ob, int batch) {
-        const size_t tw = (size_t)(Cf::N0 + Cf::N1) * sizeof(float2);
-        const size_t a = (size_t)Cf::kSmemA * sizeof(float);
-        const size_t c = (size_t)Cf::kSmemC * sizeof(float);
-        const size_t b = ((size_t)cin * ob * G + (size_t)batch * cin * G) * sizeof(float2);
-        size_t m = a > c ? a : c;
-        m = m > b ? m : b;
-        return tw + m;
-    }
-};
 
 bool is_cfg128(const Geom &g) {
     return g.d == 2 && g.n[0] == 128 && g.n[1] == 128 && g.m[0] == 16 && g.m[1] == 16;
 }
 
-int pick_ob(int cin, int cout) {
-    // outputs per phase-B item: keep the W slab (cin x ob x G complex) <= 32 KiB
-    int ob = cout;
-    while (ob > 1 && (size_t)cin * ob * kG128 * sizeof(float2) > (32u << 10)) ob = (ob + 1) / 2;
-    return ob;
+struct BShape {
+    int ob, bb;
+};
+
+// Phase-B blocking: outputs per item so the weight slab fits kWsBudget, batch
+// rows per item so the C partials fit kXpBudget.
+BShape b_shape(fno_dtype_t dt, int64_t batch, int cin, int cout) {
+    const size_t w2 = dt == FNO_F32 ? 16 : 8;
+    BShape s;
+    s.ob = cout;
+    while (s.ob > 1 && (size_t)cin * s.ob * w2 > kWsBudget) s.ob = (s.ob + 1) / 2;
+    s.bb = (int)batch;
+    while (s.bb > 1 && (size_t)Cfg128::C * s.bb * cin * 16 > kXpBudget) s.bb = (s.bb + 1) / 2;
+    return s;
+}
+
+size_t smem_bytes(fno_dtype_t dt, int cin, const BShape &s) {
+    const size_t w2 = dt == FNO_F32 ? 16 : 8;
+    const size_t b = ((size_t)cin * s.ob * w2 + 15) / 16 * 16 + (size_t)Cfg128::C * s.bb * cin * 16;
+    size_t m = Cfg128::kSmemA > Cfg128::kSmemC ? Cfg128::kSmemA : Cfg128::kSmemC;
+    m = m > b ? m : b;
+    return Cfg128::kSmemTw + m;
 }
 
 struct Layout {
@@ -533,18 +618,16 @@ Layout layout(const Geom &g, int64_t batch, int cin, int cout) {
 
 template <typename T>
 void *kernel_ptr() {
-    return reinterpret_cast<void *>(&k_fused2d<Cfg128, kG128, T>);
+    return reinterpret_cast<void *>(&k_fused2d<Cfg128, T>);
 }
 
 }  // namespace
 
 bool fused_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout) {
-    if (!is_cfg128(g)) return false;
+    if (!is_cfg128(g) || (dtype != FNO_F32 && dtype != FNO_F16)) return false;
     if (batch * (int64_t)cin * Cfg128::C >= (1 << 30) || batch * (int64_t)cout * Cfg128::C >= (1 << 30))
         return false;
-    const int ob = pick_ob(cin, cout);
-    return Variant<Cfg128, kG128>::smem_bytes(cin, ob, (int)batch) <= 200 * 1024 &&
-           (dtype == FNO_F32 || dtype == FNO_F16);
+    return smem_bytes(dtype, cin, b_shape(dtype, batch, cin, cout)) <= 200 * 1024;
 }
 
 size_t fused_workspace_bytes(const Geom &g, fno_dtype_t, int64_t batch, int cin, int cout) {
@@ -554,8 +637,8 @@ size_t fused_workspace_bytes(const Geom &g, fno_dtype_t, int64_t batch, int cin,
 int fused_kernel_count(const Geom &, fno_dtype_t, int64_t, int, int) { return 1; }
 
 cudaError_t fused_plan_init(Plan &p) {
-    const int ob = pick_ob(p.cin, p.cout);
-    const size_t smem = Variant<Cfg128, kG128>::smem_bytes(p.cin, ob, (int)p.batch);
+    const BShape bs = b_shape(p.dtype, p.batch, p.cin, p.cout);
+    const size_t smem = smem_bytes(p.dtype, p.cin, bs);
     void *fn = p.dtype == FNO_F32 ? kernel_ptr<float>() : kernel_ptr<__half>();
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
@@ -566,7 +649,8 @@ cudaError_t fused_plan_init(Plan &p) {
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     p.fused_grid = p.num_sms * per_sm;
     p.fused_smem = smem;
-    p.fused_ob = ob;
+    p.fused_ob = bs.ob;
+    p.fused_bb = bs.bb;
     return cudaMemset(p.sync, 0, sizeof(SyncBlock));
 }
 
@@ -590,13 +674,16 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
     a.nA = (int)p.batch * p.cin * Cfg128::C;
     a.ob = p.fused_ob;
     a.nob = (p.cout + a.ob - 1) / a.ob;
-    a.nB = (int)(p.g.nkept / kG128) * a.nob;
+    a.bb = p.fused_bb;
+    a.nbb = (int)((p.batch + a.bb - 1) / a.bb);
+    a.nB = (int)(p.g.nkept / kG) * a.nob * a.nbb;
     a.nC = (int)p.batch * p.cout * Cfg128::C;
-    const int grid = p.fused_grid < a.nA + a.nB + a.nC ? p.fused_grid : a.nA + a.nB + a.nC;
+    const int total = a.nA + a.nB + a.nC;
+    const int grid = p.fused_grid < total ? p.fused_grid : total;
     if (p.dtype == FNO_F32)
-        k_fused2d<Cfg128, kG128, float><<<grid, kNT, p.fused_smem, s>>>(a);
+        k_fused2d<Cfg128, float><<<grid, kNT, p.fused_smem, s>>>(a);
     else
-        k_fused2d<Cfg128, kG128, __half><<<grid, kNT, p.fused_smem, s>>>(a);
+        k_fused2d<Cfg128, __half><<<grid, kNT, p.fused_smem, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -51,6 +51,7 @@ struct Plan {
     int fused_grid;
     size_t fused_smem;
     int fused_ob;
+    int fused_bb;
 };
 
 enum { kPathUnfused = 0, kPathFused2D = 1, kPathFused1D = 2 };
