@@ -175,7 +175,7 @@ fno_status_t fno_spectral_conv_plan(fno_plan_t *out, int ndim, const int64_t *n,
         total += ((size_t)g.n[a] * sizeof(float2) + 255) & ~size_t(255);
     }
     off[g.d] = total;
-    total += 512;                 // device error word, then the fused-path counters
+    total += 256 + ((fused_sync_bytes() + 255) & ~size_t(255));   // error word, counters
     std::vector<unsigned char> host(total, 0);
     for (int a = 0; a < g.d; ++a) {
         float2 *t = reinterpret_cast<float2 *>(host.data() + off[a]);

@@ -54,14 +54,21 @@ constexpr int kG = 2;                           // kept modes per phase-B item
 constexpr size_t kWsBudget = 16u << 10;         // phase-B weight slab (bytes)
 constexpr size_t kXpBudget = 24u << 10;         // phase-B partial modes (bytes)
 
-// Counters shared by the CTAs of one launch (plan-owned, zero between launches).
+// Counters shared by the CTAs of one launch (plan-owned, zero between
+// launches).  Each counter has its own 128-byte line; the end of a phase is
+// published as kFlagCopies flags on separate lines so that the CTAs waiting
+// for it spread their polling over many L2 lines instead of one.
+constexpr int kLine = 32;          // ints per 128-byte line
+constexpr int kFlagCopies = 32;
 struct SyncBlock {
-    int ticket;      // next work item
-    int exited;      // CTAs that have left the queue
-    int done_a;      // finished phase-A items
-    int done_b;      // finished phase-B items
-    int pad[60];
+    int ticket[kLine];             // [0]: next work item
+    int exited[kLine];             // [0]: CTAs that have left the queue
+    int done_a[kLine];             // [0]: finished phase-A items
+    int done_b[kLine];             // [0]: finished phase-B items
+    int flag_a[kFlagCopies][kLine];  // [i][0] = 1 once every phase-A item is done
+    int flag_b[kFlagCopies][kLine];  // [i][0] = 1 once every phase-B item is done
 };
+constexpr size_t kSyncBytes = sizeof(SyncBlock);
 
 template <int N0_, int N1_, int M0_, int M1_, int RC_, int Q_, int B2_>
 struct Cfg {
@@ -159,22 +166,32 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
-// Thread 0 waits until *ctr >= target; gives up (sets the error word) after
+// Thread 0 waits until *flag != 0; gives up (sets the error word) after
 // kWaitTimeoutNs or as soon as another CTA has reported an error.
-__device__ bool wait_count(const int *ctr, int target, int *err) {
-    if (ld_acquire(ctr) >= target) return true;
+__device__ bool wait_flag(const int *flag, int *err) {
+    if (ld_acquire(flag) != 0) return true;
     const long long t0 = globaltimer();
     for (unsigned spin = 0;; ++spin) {
-        if (ld_acquire(ctr) >= target) {
+        if (ld_acquire(flag) != 0) {
             __threadfence();
             return true;
         }
         if (*reinterpret_cast<volatile int *>(err) != 0) return false;
-        __nanosleep(32);
+        __nanosleep(64);
         if ((spin & 255u) == 255u && globaltimer() - t0 > kWaitTimeoutNs) {
             raise_dev_error(err, kDevTimeout);
             return false;
         }
+    }
+}
+
+// Thread 0 counts one finished item of a phase; the item that completes the
+// phase publishes every flag copy.
+__device__ void finish_item(int *counter, int total, int (*flags)[kLine]) {
+    __threadfence();
+    if (atomicAdd(counter, 1) == total - 1) {
+        __threadfence();
+        for (int i = 0; i < kFlagCopies; ++i) *reinterpret_cast<volatile int *>(&flags[i][0]) = 1;
     }
 }
 
@@ -505,7 +522,7 @@ k_fused2d(Args a) {
     const int nimg_in = a.batch * a.cin;
     const int total = a.nA + a.nB + a.nC;
     for (;;) {
-        if (tid == 0) s_item = atomicAdd(&a.sync->ticket, 1);
+        if (tid == 0) s_item = atomicAdd(&a.sync->ticket[0], 1);
         __syncthreads();
         const int item = s_item;
         __syncthreads();
@@ -514,10 +531,7 @@ k_fused2d(Args a) {
             phase_a<Cf, T>(static_cast<const T *>(a.x), a.part, nimg_in, item / Cf::C,
                            item % Cf::C, work, tw);
             __syncthreads();
-            if (tid == 0) {
-                __threadfence();
-                atomicAdd(&a.sync->done_a, 1);
-            }
+            if (tid == 0) finish_item(&a.sync->done_a[0], a.nA, a.sync->flag_a);
         } else if (item < a.nA + a.nB) {
             int it = item - a.nA;
             BItem bi;
@@ -531,20 +545,19 @@ k_fused2d(Args a) {
             bi.nbb = min(a.bb, a.batch - bi.b0);
             // the weights do not depend on phase A: request them first
             phase_b_weights<Cf, T>(static_cast<const T *>(a.w), a.cin, a.cout, bi, a.ob, work);
-            if (tid == 0) s_item = wait_count(&a.sync->done_a, a.nA, a.err) ? 1 : 0;
+            if (tid == 0)
+                s_item = wait_flag(&a.sync->flag_a[blockIdx.x % kFlagCopies][0], a.err) ? 1 : 0;
             __syncthreads();
             const bool ok = s_item != 0;
             __syncthreads();
             if (ok) phase_b<Cf, T>(a.part, a.Y, a.cin, a.cout, nimg_in, bi, a.ob, work);
             else cp_async_wait_all();
             __syncthreads();
-            if (tid == 0) {
-                __threadfence();
-                atomicAdd(&a.sync->done_b, 1);
-            }
+            if (tid == 0) finish_item(&a.sync->done_b[0], a.nB, a.sync->flag_b);
         } else {
             const int it = item - a.nA - a.nB;
-            if (tid == 0) s_item = wait_count(&a.sync->done_b, a.nB, a.err) ? 1 : 0;
+            if (tid == 0)
+                s_item = wait_flag(&a.sync->flag_b[blockIdx.x % kFlagCopies][0], a.err) ? 1 : 0;
             __syncthreads();
             const bool ok = s_item != 0;
             __syncthreads();
@@ -553,16 +566,20 @@ k_fused2d(Args a) {
         }
         __syncthreads();
     }
-    // the last CTA to leave resets the counters for the next launch
+    // the last CTA to leave resets the counters and flags for the next launch
     if (tid == 0) {
         __threadfence();
-        const int prev = atomicAdd(&a.sync->exited, 1);
+        const int prev = atomicAdd(&a.sync->exited[0], 1);
         if (prev == (int)gridDim.x - 1) {
-            a.sync->ticket = 0;
-            a.sync->done_a = 0;
-            a.sync->done_b = 0;
+            a.sync->ticket[0] = 0;
+            a.sync->done_a[0] = 0;
+            a.sync->done_b[0] = 0;
+            for (int i = 0; i < kFlagCopies; ++i) {
+                a.sync->flag_a[i][0] = 0;
+                a.sync->flag_b[i][0] = 0;
+            }
             __threadfence();
-            a.sync->exited = 0;
+            a.sync->exited[0] = 0;
         }
     }
 }
@@ -623,6 +640,8 @@ void *kernel_ptr() {
 
 }  // namespace
 
+size_t fused_sync_bytes() { return kSyncBytes; }
+
 bool fused_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout) {
     if (!is_cfg128(g) || (dtype != FNO_F32 && dtype != FNO_F16)) return false;
     if (batch * (int64_t)cin * Cfg128::C >= (1 << 30) || batch * (int64_t)cout * Cfg128::C >= (1 << 30))
@@ -651,7 +670,7 @@ cudaError_t fused_plan_init(Plan &p) {
     p.fused_smem = smem;
     p.fused_ob = bs.ob;
     p.fused_bb = bs.bb;
-    return cudaMemset(p.sync, 0, sizeof(SyncBlock));
+    return cudaMemset(p.sync, 0, kSyncBytes);
 }
 
 void fused_plan_release(Plan &) {}

@@ -5,6 +5,8 @@
 
 namespace fno {
 
+// Bytes of plan-owned device memory the fused kernels keep their counters in.
+size_t fused_sync_bytes();
 // True when the fused path handles this description.
 bool fused_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout);
 size_t fused_workspace_bytes(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin,
