@@ -59,14 +59,16 @@ constexpr size_t kXpBudget = 24u << 10;         // phase-B partial modes (bytes)
 // published as kFlagCopies flags on separate lines so that the CTAs waiting
 // for it spread their polling over many L2 lines instead of one.
 constexpr int kLine = 32;          // ints per 128-byte line
-constexpr int kFlagCopies = 32;
+constexpr int kFlagCopies = 16;
+constexpr int kMaxGroups = 16;     // batch groups of one launch
+constexpr int kTargetGroups = 4;
 struct SyncBlock {
-    int ticket[kLine];             // [0]: next work item
-    int exited[kLine];             // [0]: CTAs that have left the queue
-    int done_a[kLine];             // [0]: finished phase-A items
-    int done_b[kLine];             // [0]: finished phase-B items
-    int flag_a[kFlagCopies][kLine];  // [i][0] = 1 once every phase-A item is done
-    int flag_b[kFlagCopies][kLine];  // [i][0] = 1 once every phase-B item is done
+    int ticket[kLine];                         // [0]: next work item
+    int exited[kLine];                         // [0]: CTAs that have left the queue
+    int done_a[kMaxGroups][kLine];             // [g][0]: finished phase-A items of group g
+    int done_b[kMaxGroups][kLine];             // [g][0]: finished phase-B items of group g
+    int flag_a[kMaxGroups][kFlagCopies][kLine];  // [g][i][0] = 1: phase A of group g done
+    int flag_b[kMaxGroups][kFlagCopies][kLine];  // [g][i][0] = 1: phase B of group g done
 };
 constexpr size_t kSyncBytes = sizeof(SyncBlock);
 
@@ -188,6 +190,7 @@ __device__ bool wait_flag(const int *flag, int *err) {
 // Thread 0 counts one finished item of a phase; the item that completes the
 // phase publishes every flag copy.
 __device__ void finish_item(int *counter, int total, int (*flags)[kLine]) {
+    // flags points at the kFlagCopies lines of one group
     __threadfence();
     if (atomicAdd(counter, 1) == total - 1) {
         __threadfence();
@@ -305,19 +308,23 @@ __device__ void phase_a(const T *__restrict__ x, float2 *__restrict__ part, int 
 
 // ---------------------------------------------------------------------------
 // Phase B: Y[b][o][mode] = sum_i X[b][i][mode] W[blk][i][o][local], X = sum of partials.
-// One item: kG consecutive bins of one kept row, outputs [o0, o0+nob), batch rows
-// [b0, b0+nbb).  The weight slab is requested before the wait on phase A.
+// One item: kG consecutive bins of one kept row, outputs [o0, o0+nob), the batch
+// rows [b0, b0+nbb) of one batch group.  The weight slab is requested before the
+// item waits for phase A of its group.  Each thread accumulates a register tile
+// of BT batch rows x 2 outputs x 2 bins over every S-th input channel; the S
+// lanes that share a tile then combine their sums by a shuffle reduce-scatter.
 // ---------------------------------------------------------------------------
 struct BItem {
-    int group, o0, nob, b0, nbb;
+    int pair, o0, nob, b0, nbb;
 };
+constexpr int kBT = 4;      // batch rows per register tile
 
 template <class Cf, typename T>
 __device__ void phase_b_weights(const T *__restrict__ w, int cin, int cout, const BItem &it,
                                 int ob, char *smem) {
     using W2 = typename Io<T>::W2;
     constexpr int M0 = Cf::M0, M1 = Cf::M1;
-    const int mode0 = it.group * kG;
+    const int mode0 = it.pair * kG;
     const int j = mode0 / M1, k0 = mode0 % M1;
     const int blk = j >= M0 ? 1 : 0, l0 = j - blk * M0;
     W2 *ws = reinterpret_cast<W2 *>(smem);                   // [cin][ob]
@@ -333,12 +340,88 @@ __device__ void phase_b_weights(const T *__restrict__ w, int cin, int cout, cons
     cp_async_commit();
 }
 
+// lanes per tile (split of the input channels) for a given tile count
+__host__ __device__ inline int b_split(int tiles) {
+    int s = 1;
+    while (s < 16 && tiles * s * 2 <= kNT) s *= 2;
+    return s;
+}
+
+template <class Cf, typename T, int S>
+__device__ void phase_b_tiles(float2 *__restrict__ Y, int cin, int cout, const BItem &it,
+                              int ob, const typename Io<T>::W2 *ws, const float4 *xp,
+                              int tiles) {
+    using W2 = typename Io<T>::W2;
+    constexpr int NK = Cf::NK;
+    constexpr int V = kBT * 2 * kG;                      // values per tile
+    static_assert(V % S == 0, "tile values split evenly over the lanes");
+    const int mode0 = it.pair * kG;
+    const int no2 = (it.nob + 1) / 2;
+    // every lane of a warp runs the same number of passes (the shuffles below
+    // need the whole warp); lanes past the last tile add zeros and store nothing
+    const int total = tiles * S, bound = (total + 31) / 32 * 32;
+    for (int u = threadIdx.x; u < bound; u += kNT) {
+        const bool active = u < total;
+        const int s = u % S, tile = active ? u / S : 0;
+        const int o = 2 * (tile % no2), b = kBT * (tile / no2);
+        const bool o1 = o + 1 < it.nob;
+        float2 vv[V];                                    // [bb][oo][g]
+#pragma unroll
+        for (int q = 0; q < V; ++q) vv[q] = make_float2(0.f, 0.f);
+        for (int i = s; active && i < cin; i += S) {
+            const W2 w0 = ws[i * ob + o];
+            const W2 w1 = o1 ? ws[i * ob + o + 1] : w0;
+            float2 wv[2][kG];
+#pragma unroll
+            for (int g = 0; g < kG; ++g) {
+                wv[0][g] = Io<T>::wget(w0, g);
+                wv[1][g] = Io<T>::wget(w1, g);
+            }
+#pragma unroll
+            for (int bb = 0; bb < kBT; ++bb) {
+                const int bi = b + bb < it.nbb ? b + bb : it.nbb - 1;
+                const float4 xv = xp[bi * cin + i];
+                const float2 x0 = make_float2(xv.x, xv.y), x1 = make_float2(xv.z, xv.w);
+#pragma unroll
+                for (int oo = 0; oo < 2; ++oo) {
+                    cmac(vv[(bb * 2 + oo) * kG + 0], x0, wv[oo][0]);
+                    cmac(vv[(bb * 2 + oo) * kG + 1], x1, wv[oo][1]);
+                }
+            }
+        }
+        // reduce-scatter over the S adjacent lanes of the tile: lane s ends with
+        // the sums of values s*(V/S) .. s*(V/S) + V/S - 1 in vv[0 .. V/S)
+        fft::unroll<0, fft::ilog2(S)>([&](auto ri) {
+            constexpr int h = S >> (decltype(ri)::value + 1);
+            constexpr int len = V >> (decltype(ri)::value + 1);
+            const bool upper = (s & h) != 0;
+#pragma unroll
+            for (int q = 0; q < len; ++q) {
+                const float2 send = upper ? vv[q] : vv[q + len];
+                float2 keep = upper ? vv[q + len] : vv[q];
+                keep.x += __shfl_xor_sync(0xffffffffu, send.x, h);
+                keep.y += __shfl_xor_sync(0xffffffffu, send.y, h);
+                vv[q] = keep;
+            }
+        });
+        constexpr int per = V / S;
+#pragma unroll
+        for (int q = 0; q < per; ++q) {
+            const int v = s * per + q;
+            const int g = v % kG, oo = (v / kG) % 2, bb = v / (2 * kG);
+            if (active && b + bb < it.nbb && o + oo < it.nob)
+                __stcg(Y + ((size_t)(it.b0 + b + bb) * cout + it.o0 + o + oo) * NK + mode0 + g,
+                       vv[q]);
+        }
+    }
+}
+
 template <class Cf, typename T>
 __device__ void phase_b(const float2 *__restrict__ part, float2 *__restrict__ Y, int cin,
                         int cout, int nimg_in, const BItem &it, int ob, char *smem) {
     using W2 = typename Io<T>::W2;
     constexpr int NK = Cf::NK, C = Cf::C;
-    const int mode0 = it.group * kG;
+    const int mode0 = it.pair * kG;
     const W2 *ws = reinterpret_cast<const W2 *>(smem);                       // [cin][ob]
     float4 *xp = reinterpret_cast<float4 *>(smem + ((size_t)cin * ob * sizeof(W2) + 15) / 16 * 16);
     const int tid = threadIdx.x;
@@ -361,30 +444,14 @@ __device__ void phase_b(const float2 *__restrict__ part, float2 *__restrict__ Y,
         xp[r] = s;
     }
     __syncthreads();
-    constexpr int BB = 4;                                // batch rows per thread
-    const int nbq = (it.nbb + BB - 1) / BB;
-    for (int u = tid; u < it.nob * kG * nbq; u += kNT) {
-        const int g = u % kG, o = (u / kG) % it.nob, bq = u / (kG * it.nob);
-        float2 acc[BB];
-#pragma unroll
-        for (int bb = 0; bb < BB; ++bb) acc[bb] = make_float2(0.f, 0.f);
-        for (int i = 0; i < cin; ++i) {
-            const float2 wv = Io<T>::wget(ws[i * ob + o], g);
-#pragma unroll
-            for (int bb = 0; bb < BB; ++bb) {
-                const int b = bq * BB + bb;
-                if (b < it.nbb) {
-                    const float4 xv = xp[b * cin + i];
-                    cmac(acc[bb], g == 0 ? make_float2(xv.x, xv.y) : make_float2(xv.z, xv.w), wv);
-                }
-            }
-        }
-#pragma unroll
-        for (int bb = 0; bb < BB; ++bb) {
-            const int b = bq * BB + bb;
-            if (b < it.nbb)
-                __stcg(Y + ((size_t)(it.b0 + b) * cout + it.o0 + o) * NK + mode0 + g, acc[bb]);
-        }
+    const int nbt = (it.nbb + kBT - 1) / kBT, no2 = (it.nob + 1) / 2;
+    const int tiles = nbt * no2;
+    switch (b_split(tiles)) {
+        case 16: phase_b_tiles<Cf, T, 16>(Y, cin, cout, it, ob, ws, xp, tiles); break;
+        case 8: phase_b_tiles<Cf, T, 8>(Y, cin, cout, it, ob, ws, xp, tiles); break;
+        case 4: phase_b_tiles<Cf, T, 4>(Y, cin, cout, it, ob, ws, xp, tiles); break;
+        case 2: phase_b_tiles<Cf, T, 2>(Y, cin, cout, it, ob, ws, xp, tiles); break;
+        default: phase_b_tiles<Cf, T, 1>(Y, cin, cout, it, ob, ws, xp, tiles); break;
     }
 }
 
@@ -499,16 +566,48 @@ struct Args {
     const float2 *tw1;  // N1 twiddles
     int *err;
     int batch, cin, cout;
-    int nA, nB, nC;
+    int bg, ng;         // batch rows per group, groups
+    int npairs;         // phase B: kept-mode pairs
     int ob, nob;        // phase B: outputs per item, output blocks
-    int bb, nbb;        // phase B: batch rows per item, batch blocks
 };
+
+// Work items of group g, in ticket order: A(0), A(1), B(0), A(2), B(1), C(0),
+// ..., so that while a group mixes, the next one transforms and the previous
+// one runs its inverse.
+struct Item {
+    int phase;          // 0: A, 1: B, 2: C, -1: none left
+    int g, idx;
+};
+
+template <class Cf>
+__device__ Item decode_ticket(const Args &a, int t) {
+    for (int st = 0; st < a.ng + 2; ++st) {
+        if (st < a.ng) {
+            const int n = min(a.bg, a.batch - st * a.bg) * a.cin * Cf::C;
+            if (t < n) return Item{0, st, t};
+            t -= n;
+        }
+        if (st >= 1 && st - 1 < a.ng) {
+            const int n = a.npairs * a.nob;
+            if (t < n) return Item{1, st - 1, t};
+            t -= n;
+        }
+        if (st >= 2) {
+            const int g = st - 2;
+            const int n = min(a.bg, a.batch - g * a.bg) * a.cout * Cf::C;
+            if (t < n) return Item{2, g, t};
+            t -= n;
+        }
+    }
+    return Item{-1, 0, 0};
+}
 
 template <class Cf, typename T>
 __global__ void __launch_bounds__(kNT)
 k_fused2d(Args a) {
     extern __shared__ __align__(16) char smem[];
-    __shared__ int s_item;
+    __shared__ Item s_item;
+    __shared__ int s_ok;
     float2 *tw0 = reinterpret_cast<float2 *>(smem);
     float2 *tw1 = tw0 + Cf::N0;
     char *work = smem + Cf::kSmemTw;
@@ -520,49 +619,45 @@ k_fused2d(Args a) {
     }
     const Tw tw{tw0, tw1};
     const int nimg_in = a.batch * a.cin;
-    const int total = a.nA + a.nB + a.nC;
     for (;;) {
-        if (tid == 0) s_item = atomicAdd(&a.sync->ticket[0], 1);
+        if (tid == 0) s_item = decode_ticket<Cf>(a, atomicAdd(&a.sync->ticket[0], 1));
         __syncthreads();
-        const int item = s_item;
+        const Item it = s_item;
         __syncthreads();
-        if (item >= total) break;
-        if (item < a.nA) {
-            phase_a<Cf, T>(static_cast<const T *>(a.x), a.part, nimg_in, item / Cf::C,
-                           item % Cf::C, work, tw);
+        if (it.phase < 0) break;
+        const int nbg = min(a.bg, a.batch - it.g * a.bg);     // batch rows of the group
+        if (it.phase == 0) {
+            const int img = it.g * a.bg * a.cin + it.idx / Cf::C;
+            phase_a<Cf, T>(static_cast<const T *>(a.x), a.part, nimg_in, img, it.idx % Cf::C,
+                           work, tw);
             __syncthreads();
-            if (tid == 0) finish_item(&a.sync->done_a[0], a.nA, a.sync->flag_a);
-        } else if (item < a.nA + a.nB) {
-            int it = item - a.nA;
+            if (tid == 0)
+                finish_item(&a.sync->done_a[it.g][0], nbg * a.cin * Cf::C, a.sync->flag_a[it.g]);
+        } else if (it.phase == 1) {
             BItem bi;
-            const int bblk = it % a.nbb;
-            it /= a.nbb;
-            const int oblk = it % a.nob;
-            bi.group = it / a.nob;
-            bi.o0 = oblk * a.ob;
+            bi.pair = it.idx / a.nob;
+            bi.o0 = (it.idx % a.nob) * a.ob;
             bi.nob = min(a.ob, a.cout - bi.o0);
-            bi.b0 = bblk * a.bb;
-            bi.nbb = min(a.bb, a.batch - bi.b0);
+            bi.b0 = it.g * a.bg;
+            bi.nbb = nbg;
             // the weights do not depend on phase A: request them first
             phase_b_weights<Cf, T>(static_cast<const T *>(a.w), a.cin, a.cout, bi, a.ob, work);
             if (tid == 0)
-                s_item = wait_flag(&a.sync->flag_a[blockIdx.x % kFlagCopies][0], a.err) ? 1 : 0;
+                s_ok = wait_flag(&a.sync->flag_a[it.g][blockIdx.x % kFlagCopies][0], a.err);
             __syncthreads();
-            const bool ok = s_item != 0;
-            __syncthreads();
-            if (ok) phase_b<Cf, T>(a.part, a.Y, a.cin, a.cout, nimg_in, bi, a.ob, work);
+            if (s_ok) phase_b<Cf, T>(a.part, a.Y, a.cin, a.cout, nimg_in, bi, a.ob, work);
             else cp_async_wait_all();
             __syncthreads();
-            if (tid == 0) finish_item(&a.sync->done_b[0], a.nB, a.sync->flag_b);
-        } else {
-            const int it = item - a.nA - a.nB;
             if (tid == 0)
-                s_item = wait_flag(&a.sync->flag_b[blockIdx.x % kFlagCopies][0], a.err) ? 1 : 0;
+                finish_item(&a.sync->done_b[it.g][0], a.npairs * a.nob, a.sync->flag_b[it.g]);
+        } else {
+            if (tid == 0)
+                s_ok = wait_flag(&a.sync->flag_b[it.g][blockIdx.x % kFlagCopies][0], a.err);
             __syncthreads();
-            const bool ok = s_item != 0;
-            __syncthreads();
-            if (ok)
-                phase_c<Cf, T>(a.Y, static_cast<T *>(a.y), it / Cf::C, it % Cf::C, work, tw);
+            if (s_ok) {
+                const int img = it.g * a.bg * a.cout + it.idx / Cf::C;
+                phase_c<Cf, T>(a.Y, static_cast<T *>(a.y), img, it.idx % Cf::C, work, tw);
+            }
         }
         __syncthreads();
     }
@@ -572,11 +667,13 @@ k_fused2d(Args a) {
         const int prev = atomicAdd(&a.sync->exited[0], 1);
         if (prev == (int)gridDim.x - 1) {
             a.sync->ticket[0] = 0;
-            a.sync->done_a[0] = 0;
-            a.sync->done_b[0] = 0;
-            for (int i = 0; i < kFlagCopies; ++i) {
-                a.sync->flag_a[i][0] = 0;
-                a.sync->flag_b[i][0] = 0;
+            for (int g = 0; g < a.ng; ++g) {
+                a.sync->done_a[g][0] = 0;
+                a.sync->done_b[g][0] = 0;
+                for (int i = 0; i < kFlagCopies; ++i) {
+                    a.sync->flag_a[g][i][0] = 0;
+                    a.sync->flag_b[g][i][0] = 0;
+                }
             }
             __threadfence();
             a.sync->exited[0] = 0;
@@ -596,24 +693,26 @@ bool is_cfg128(const Geom &g) {
 }
 
 struct BShape {
-    int ob, bb;
+    int ob;     // outputs per phase-B item
+    int bg;     // batch rows per group
 };
 
-// Phase-B blocking: outputs per item so the weight slab fits kWsBudget, batch
-// rows per item so the C partials fit kXpBudget.
+// Batch groups of about batch/kTargetGroups rows; outputs per phase-B item so
+// that the weight slab fits kWsBudget and the group's partials fit kXpBudget.
 BShape b_shape(fno_dtype_t dt, int64_t batch, int cin, int cout) {
     const size_t w2 = dt == FNO_F32 ? 16 : 8;
     BShape s;
     s.ob = cout;
     while (s.ob > 1 && (size_t)cin * s.ob * w2 > kWsBudget) s.ob = (s.ob + 1) / 2;
-    s.bb = (int)batch;
-    while (s.bb > 1 && (size_t)Cfg128::C * s.bb * cin * 16 > kXpBudget) s.bb = (s.bb + 1) / 2;
+    s.bg = (int)((batch + kTargetGroups - 1) / kTargetGroups);
+    while (s.bg > 1 && (size_t)Cfg128::C * s.bg * cin * 16 > kXpBudget) s.bg = (s.bg + 1) / 2;
+    while ((batch + s.bg - 1) / s.bg > kMaxGroups) ++s.bg;
     return s;
 }
 
 size_t smem_bytes(fno_dtype_t dt, int cin, const BShape &s) {
     const size_t w2 = dt == FNO_F32 ? 16 : 8;
-    const size_t b = ((size_t)cin * s.ob * w2 + 15) / 16 * 16 + (size_t)Cfg128::C * s.bb * cin * 16;
+    const size_t b = ((size_t)cin * s.ob * w2 + 15) / 16 * 16 + (size_t)Cfg128::C * s.bg * cin * 16;
     size_t m = Cfg128::kSmemA > Cfg128::kSmemC ? Cfg128::kSmemA : Cfg128::kSmemC;
     m = m > b ? m : b;
     return Cfg128::kSmemTw + m;
@@ -669,7 +768,7 @@ cudaError_t fused_plan_init(Plan &p) {
     p.fused_grid = p.num_sms * per_sm;
     p.fused_smem = smem;
     p.fused_ob = bs.ob;
-    p.fused_bb = bs.bb;
+    p.fused_bb = bs.bg;
     return cudaMemset(p.sync, 0, kSyncBytes);
 }
 
@@ -690,14 +789,12 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
     a.batch = (int)p.batch;
     a.cin = p.cin;
     a.cout = p.cout;
-    a.nA = (int)p.batch * p.cin * Cfg128::C;
+    a.bg = p.fused_bb;
+    a.ng = (int)((p.batch + a.bg - 1) / a.bg);
+    a.npairs = (int)(p.g.nkept / kG);
     a.ob = p.fused_ob;
     a.nob = (p.cout + a.ob - 1) / a.ob;
-    a.bb = p.fused_bb;
-    a.nbb = (int)((p.batch + a.bb - 1) / a.bb);
-    a.nB = (int)(p.g.nkept / kG) * a.nob * a.nbb;
-    a.nC = (int)p.batch * p.cout * Cfg128::C;
-    const int total = a.nA + a.nB + a.nC;
+    const int total = (int)p.batch * (p.cin + p.cout) * Cfg128::C + a.ng * a.npairs * a.nob;
     const int grid = p.fused_grid < total ? p.fused_grid : total;
     if (p.dtype == FNO_F32)
         k_fused2d<Cfg128, float><<<grid, kNT, p.fused_smem, s>>>(a);
