@@ -35,6 +35,7 @@ EXPORTS = (
     "fno_spectral_conv_query", "fno_spectral_conv_plan",
     "fno_spectral_conv_workspace_size", "fno_spectral_conv_kernel_count",
     "fno_spectral_conv_forward", "fno_plan_get_device_error", "fno_plan_destroy",
+    "fno_spectral_conv_forward_static",
     "fno_model_plan", "fno_model_workspace_size", "fno_model_kernel_count",
     "fno_forward", "fno_model_get_device_error", "fno_model_destroy",
 )
@@ -91,6 +92,9 @@ def lib() -> ctypes.CDLL:
             L.fno_spectral_conv_workspace_size.argtypes = [_vp, psz]
             L.fno_spectral_conv_kernel_count.argtypes = [_vp, ctypes.POINTER(ctypes.c_int)]
             L.fno_spectral_conv_forward.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp]
+            L.fno_spectral_conv_forward_static.argtypes = [
+                ctypes.c_int, pi64, pi32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _st,
+                _vp, _vp, _vp, _vp]
             L.fno_plan_get_device_error.argtypes = [_vp, _vp]
             L.fno_plan_destroy.argtypes = [_vp]
             L.fno_model_plan.argtypes = [ctypes.POINTER(_vp), ctypes.POINTER(fno_model_desc_t)]
@@ -147,6 +151,13 @@ def fno_spectral_conv_kernel_count(plan):
 
 def fno_spectral_conv_forward(plan, x_ptr, w_ptr, y_ptr, ws_ptr, stream):
     return lib().fno_spectral_conv_forward(plan, x_ptr, w_ptr, y_ptr, ws_ptr, stream)
+
+
+def fno_spectral_conv_forward_static(ndim, n, modes, batch, cin, cout, dtype, x_ptr, w_ptr,
+                                     y_ptr, stream):
+    return lib().fno_spectral_conv_forward_static(
+        int(ndim), _arr(ctypes.c_int64, n), _arr(ctypes.c_int32, modes), int(batch), int(cin),
+        int(cout), int(dtype), x_ptr, w_ptr, y_ptr, stream)
 
 
 def fno_plan_get_device_error(plan, stream):

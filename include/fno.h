@@ -141,6 +141,34 @@ fno_status_t fno_spectral_conv_kernel_count(fno_plan_t plan, int *count);
 fno_status_t fno_spectral_conv_forward(fno_plan_t plan, const void *x, const void *w,
                                        void *y, void *workspace, fno_stream_t stream);
 
+/* y = SpectralConv(x; w) for callers that cannot allocate GPU memory.
+ * The pages on the FNO layer have no counterpart to this call; it exists for
+ * callers that may not call cudaMalloc (code running under another
+ * framework's allocator, or with a device memory budget fixed at start-up)
+ * and therefore can create neither a plan nor a workspace.
+ *   ndim, n, modes, batch, cin, cout, dtype   as in fno_spectral_conv_query
+ *   x, w, y   device pointers, layouts as in fno_spectral_conv_forward
+ * No plan, no workspace: the intermediates live in a fixed 16 MiB scratch
+ * array in device memory that the library reserves on every GPU that loads it,
+ * held until the process exits; the twiddle tables live in another such array.
+ * Shapes whose intermediates need more than 16 MiB (the workspace that
+ * fno_spectral_conv_query reports under FNO_PLAN_UNFUSED) are rejected with
+ * FNO_ERR_UNSUPPORTED before anything is enqueued.
+ * The call allocates nothing.  Its first call on a device looks up the device
+ * addresses of those arrays and fills the twiddle tables with a synchronous
+ * copy (with that device current), so that first call should come before any
+ * stream capture.  Every call shares the one scratch array, which keeps the
+ * last call's contents; none of it has to start at zero.  Calls that overlap
+ * on the GPU (different streams) race on the scratch and give wrong results;
+ * calls on one stream are safe.  Runs the separate-kernels path (the kernels of
+ * FNO_PLAN_UNFUSED).  Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, ALIASING,
+ * CUDA.                                                                     */
+fno_status_t fno_spectral_conv_forward_static(int ndim, const int64_t *n,
+                                              const int32_t *modes, int64_t batch,
+                                              int32_t cin, int32_t cout, fno_dtype_t dtype,
+                                              const void *x, const void *w, void *y,
+                                              fno_stream_t stream);
+
 /* Synchronise `stream`, then read and clear the plan's device error word.
  * Returns FNO_OK, FNO_ERR_DEVICE_TIMEOUT, FNO_ERR_DEVICE_BOUNDS or CUDA.   */
 fno_status_t fno_plan_get_device_error(fno_plan_t plan, fno_stream_t stream);
