@@ -4,7 +4,8 @@ Each ``csrc/*.cu`` translation unit is compiled by nvcc in parallel, then
 linked into ``fft_gemm_ifft_gb300/libfno.so`` (git-ignored).  The build is
 skipped when the library is newer than every source and header.  Set
 ``FNO_PTXAS_VERBOSE=1`` to print the register / shared-memory report of each
-kernel, and ``FNO_DEBUG_BOUNDS=1`` to compile the device index checks in.
+kernel, ``FNO_DEBUG_BOUNDS=1`` to compile the device index checks in, and
+``FNO_EXTRA_NVCC_FLAGS`` to pass tuning macros (e.g. ``-DFNO_TARGET_GROUPS=4``).
 """
 from __future__ import annotations
 
@@ -45,6 +46,9 @@ def _flags():
                 "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr"]
     if os.environ.get("FNO_PTXAS_VERBOSE"):
         f += ["-Xptxas", "-v"]
+    extra = os.environ.get("FNO_EXTRA_NVCC_FLAGS")
+    if extra:
+        f += extra.split()
     if os.environ.get("FNO_DEBUG_BOUNDS"):
         f += ["-DFNO_DEBUG_BOUNDS=1"]
     return f

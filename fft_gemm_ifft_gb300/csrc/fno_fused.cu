@@ -61,7 +61,10 @@ constexpr size_t kXpBudget = 24u << 10;         // phase-B partial modes (bytes)
 constexpr int kLine = 32;          // ints per 128-byte line
 constexpr int kFlagCopies = 16;
 constexpr int kMaxGroups = 16;     // batch groups of one launch
-constexpr int kTargetGroups = 4;
+#ifndef FNO_TARGET_GROUPS
+#define FNO_TARGET_GROUPS 1
+#endif
+constexpr int kTargetGroups = FNO_TARGET_GROUPS;   // batch groups the phases pipeline over
 struct SyncBlock {
     int ticket[kLine];                         // [0]: next work item
     int exited[kLine];                         // [0]: CTAs that have left the queue
