@@ -62,7 +62,7 @@ constexpr int kLine = 32;          // ints per 128-byte line
 constexpr int kFlagCopies = 16;
 constexpr int kMaxGroups = 16;     // batch groups of one launch
 #ifndef FNO_TARGET_GROUPS
-#define FNO_TARGET_GROUPS 1
+#define FNO_TARGET_GROUPS 2
 #endif
 constexpr int kTargetGroups = FNO_TARGET_GROUPS;   // batch groups the phases pipeline over
 struct SyncBlock {
