@@ -200,6 +200,7 @@ fno_status_t fno_spectral_conv_plan(fno_plan_t *out, int ndim, const int64_t *n,
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         cudaGetLastError();
+        if (p->path != kPathUnfused) fused_plan_release(*p);
         cudaFree(p->dev_tables);
         delete p;
         return FNO_ERR_CUDA;

@@ -34,10 +34,16 @@
 // distinct banks (padded row strides, bin index fastest); loads of the
 // mixing and inverse phases are issued as cp.async copies all at once, and
 // the weights of a mixing item are fetched before it waits for phase A.
+#include <cuda.h>
+
+#include <cmath>
+#include <cstring>
 #include <type_traits>
 
 #include "fno_fft.cuh"
 #include "fno_fused.cuh"
+
+#include <new>
 
 namespace fno {
 namespace {
@@ -322,7 +328,7 @@ struct BItem {
 };
 constexpr int kBT = 4;      // batch rows per register tile
 
-template <class Cf, typename T>
+template <class Cf, typename T, int NT>
 __device__ void phase_b_weights(const T *__restrict__ w, int cin, int cout, const BItem &it,
                                 int ob, char *smem) {
     using W2 = typename Io<T>::W2;
@@ -332,7 +338,7 @@ __device__ void phase_b_weights(const T *__restrict__ w, int cin, int cout, cons
     const int blk = j >= M0 ? 1 : 0, l0 = j - blk * M0;
     W2 *ws = reinterpret_cast<W2 *>(smem);                   // [cin][ob]
     const size_t mblk = (size_t)M0 * M1;
-    for (int e = threadIdx.x; e < cin * it.nob; e += kNT) {
+    for (int e = threadIdx.x; e < cin * it.nob; e += NT) {
         const int o = e % it.nob, i = e / it.nob;
         const T *p = w + ((((size_t)blk * cin + i) * cout + it.o0 + o) * mblk + l0 * M1 + k0) * 2;
         if constexpr (sizeof(W2) == 16)
@@ -344,13 +350,13 @@ __device__ void phase_b_weights(const T *__restrict__ w, int cin, int cout, cons
 }
 
 // lanes per tile (split of the input channels) for a given tile count
-__host__ __device__ inline int b_split(int tiles) {
+__host__ __device__ inline int b_split(int tiles, int nt) {
     int s = 1;
-    while (s < 16 && tiles * s * 2 <= kNT) s *= 2;
+    while (s < 16 && tiles * s * 2 <= nt) s *= 2;
     return s;
 }
 
-template <class Cf, typename T, int S>
+template <class Cf, typename T, int S, int NT>
 __device__ void phase_b_tiles(float2 *__restrict__ Y, int cin, int cout, const BItem &it,
                               int ob, const typename Io<T>::W2 *ws, const float4 *xp,
                               int tiles) {
@@ -363,7 +369,7 @@ __device__ void phase_b_tiles(float2 *__restrict__ Y, int cin, int cout, const B
     // every lane of a warp runs the same number of passes (the shuffles below
     // need the whole warp); lanes past the last tile add zeros and store nothing
     const int total = tiles * S, bound = (total + 31) / 32 * 32;
-    for (int u = threadIdx.x; u < bound; u += kNT) {
+    for (int u = threadIdx.x; u < bound; u += NT) {
         const bool active = u < total;
         const int s = u % S, tile = active ? u / S : 0;
         const int o = 2 * (tile % no2), b = kBT * (tile / no2);
@@ -419,7 +425,7 @@ __device__ void phase_b_tiles(float2 *__restrict__ Y, int cin, int cout, const B
     }
 }
 
-template <class Cf, typename T>
+template <class Cf, typename T, int NT>
 __device__ void phase_b(const float2 *__restrict__ part, float2 *__restrict__ Y, int cin,
                         int cout, int nimg_in, const BItem &it, int ob, char *smem) {
     using W2 = typename Io<T>::W2;
@@ -430,14 +436,14 @@ __device__ void phase_b(const float2 *__restrict__ part, float2 *__restrict__ Y,
     const int tid = threadIdx.x;
     const int nr = it.nbb * cin;                         // rows (b, i) of this item
     // partial modes of the C chunks: xp[cc][r] = X_cc[b0*cin + r][mode0 .. mode0+1]
-    for (int e = tid; e < C * nr; e += kNT) {
+    for (int e = tid; e < C * nr; e += NT) {
         const int r = e % nr, cc = e / nr;
         cp_async16(xp + e, part + ((size_t)cc * nimg_in + (size_t)it.b0 * cin + r) * NK + mode0);
     }
     cp_async_commit();
     cp_async_wait_all();                                 // also covers the weight slab
     __syncthreads();
-    for (int r = tid; r < nr; r += kNT) {
+    for (int r = tid; r < nr; r += NT) {
         float4 s = xp[r];
 #pragma unroll
         for (int cc = 1; cc < C; ++cc) {
@@ -449,12 +455,12 @@ __device__ void phase_b(const float2 *__restrict__ part, float2 *__restrict__ Y,
     __syncthreads();
     const int nbt = (it.nbb + kBT - 1) / kBT, no2 = (it.nob + 1) / 2;
     const int tiles = nbt * no2;
-    switch (b_split(tiles)) {
-        case 16: phase_b_tiles<Cf, T, 16>(Y, cin, cout, it, ob, ws, xp, tiles); break;
-        case 8: phase_b_tiles<Cf, T, 8>(Y, cin, cout, it, ob, ws, xp, tiles); break;
-        case 4: phase_b_tiles<Cf, T, 4>(Y, cin, cout, it, ob, ws, xp, tiles); break;
-        case 2: phase_b_tiles<Cf, T, 2>(Y, cin, cout, it, ob, ws, xp, tiles); break;
-        default: phase_b_tiles<Cf, T, 1>(Y, cin, cout, it, ob, ws, xp, tiles); break;
+    switch (b_split(tiles, NT)) {
+        case 16: phase_b_tiles<Cf, T, 16, NT>(Y, cin, cout, it, ob, ws, xp, tiles); break;
+        case 8: phase_b_tiles<Cf, T, 8, NT>(Y, cin, cout, it, ob, ws, xp, tiles); break;
+        case 4: phase_b_tiles<Cf, T, 4, NT>(Y, cin, cout, it, ob, ws, xp, tiles); break;
+        case 2: phase_b_tiles<Cf, T, 2, NT>(Y, cin, cout, it, ob, ws, xp, tiles); break;
+        default: phase_b_tiles<Cf, T, 1, NT>(Y, cin, cout, it, ob, ws, xp, tiles); break;
     }
 }
 
@@ -644,11 +650,11 @@ k_fused2d(Args a) {
             bi.b0 = it.g * a.bg;
             bi.nbb = nbg;
             // the weights do not depend on phase A: request them first
-            phase_b_weights<Cf, T>(static_cast<const T *>(a.w), a.cin, a.cout, bi, a.ob, work);
+            phase_b_weights<Cf, T, kNT>(static_cast<const T *>(a.w), a.cin, a.cout, bi, a.ob, work);
             if (tid == 0)
                 s_ok = wait_flag(&a.sync->flag_a[it.g][blockIdx.x % kFlagCopies][0], a.err);
             __syncthreads();
-            if (s_ok) phase_b<Cf, T>(a.part, a.Y, a.cin, a.cout, nimg_in, bi, a.ob, work);
+            if (s_ok) phase_b<Cf, T, kNT>(a.part, a.Y, a.cin, a.cout, nimg_in, bi, a.ob, work);
             else cp_async_wait_all();
             __syncthreads();
             if (tid == 0)
@@ -683,6 +689,479 @@ k_fused2d(Args a) {
         }
     }
 }
+
+// ---------------------------------------------------------------------------
+// Tensor-core variant for float32 storage (128 x 128, 16 x 16 modes)
+//
+// Phase A: TMA brings a whole input image (128 rows x 128 columns) into shared
+// memory with the 128-byte swizzle (the next image is prefetched into the
+// other buffer while this one is computed).  The row DFT Z = X T^T (T: cos /
+// -sin of bins 0..15, 32 x 128) runs on the tensor cores as tcgen05.mma
+// kind::tf32 with three passes (x_hi t_hi + x_hi t_lo + x_lo t_hi), where a
+// value's hi part is the value itself read at tf32 precision and its lo part
+// the exact remainder, so the product is accurate to about 2^-20 (the layer's
+// float32 bar is 1e-5).  The accumulator lives in tensor memory.  The column
+// DFT over the 128 rows is split 8 x 16 (16-point register FFTs + twiddled
+// sums) on the SIMT cores, and the 512 kept modes go to the workspace.
+// Phase C: the column inverse (16-point register FFTs) builds the operand
+// Zo = [Re | Im] (128 x 32) and the row inverse y = Zo Tinv^T (Tinv folds the
+// half-spectrum weights c(k) and the 1/(N0 N1) scale) is one more tcgen05
+// chain with N = 128; tensor memory is staged through swizzled shared memory
+// and written by TMA.  Phase B is the SIMT mixing shared with the other kernel.
+// ---------------------------------------------------------------------------
+namespace tc {
+
+constexpr int NT = 256;
+struct Cf {
+    static constexpr int N0 = 128, M0 = 16, M1 = 16, K0 = 32, NK = K0 * M1;
+    static constexpr int C = 1;            // one item covers a whole image
+};
+constexpr int kKChunks = 4;                // 32-column K chunks of the row DFT
+constexpr uint32_t kChunkBytes = 16384;    // 128 rows x 128 bytes
+constexpr uint32_t kImageBytes = kKChunks * kChunkBytes;
+// shared-memory map (offsets from a 1024-aligned base)
+constexpr uint32_t kR = 0;                 // 128 KiB: x tiles (A) / mixing (B) / inverse (C)
+constexpr uint32_t kXL = 131072;           // 32 KiB: lo parts of two K chunks (A)
+constexpr uint32_t kT = 163840;            // 32 KiB: forward twiddle operand, hi then lo
+constexpr uint32_t kTi = 196608;           // 32 KiB: inverse twiddle operand, hi then lo
+constexpr uint32_t kTw = 229376;           // 1 KiB: W_128^e
+constexpr uint32_t kSmemBytes = kTw + 1024 + 1024;   // + alignment slack
+constexpr uint32_t kTableBytes = 65536;    // forward + inverse operands (global image)
+constexpr int kTmemCols = 256;             // [0,32): forward D; [32,160): inverse D
+// inside R during a C item
+constexpr uint32_t kCY = 0, kCAhi = 8192, kCAlo = 24576, kCStage = 65536;
+// inside the current x buffer after its MMAs (A item)
+constexpr int kZS = 17;                    // row stride of the Z planes (floats)
+constexpr uint32_t kZr = 0, kZi = 128 * kZS * 4, kS = 2 * 128 * kZS * 4;
+
+// byte offset of (row, col) in a chunk of rows x 32 fp32 stored K-major with
+// the 128-byte swizzle (8-row atoms of 1024 bytes, 16-byte pieces permuted by
+// row % 8); the chunk must start on a 1024-byte boundary
+__host__ __device__ inline uint32_t sw_off(int row, int col) {
+    const uint32_t b = (uint32_t)col * 4, r = row & 7, j = b >> 4;
+    return (uint32_t)(row >> 3) * 1024 + r * 128 + ((j ^ r) << 4) + (b & 15);
+}
+__host__ __device__ inline float tf32_lo(float v) {
+    uint32_t u;
+    memcpy(&u, &v, 4);
+    u &= 0xFFFFE000u;
+    float h;
+    memcpy(&h, &u, 4);
+    return v - h;
+}
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// instruction descriptor: D f32, A/B tf32, K-major, M = 128
+__host__ __device__ constexpr uint32_t idesc_tf32(int n) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+__device__ __forceinline__ void mma_tf32(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t acc) {
+    asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}"
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+// Bounded wait for the phase `n` (0, 1, 2, ...) of an mbarrier; on time-out the
+// error word is set and the caller goes on (its results are then discarded).
+__device__ bool mbar_wait(uint64_t *bar, uint32_t n, int *err) {
+    const uint32_t a = smem_addr(bar), parity = n & 1;
+    uint32_t done = 0;
+    long long t0 = 0;
+    for (uint32_t spin = 0;; ++spin) {
+        asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                     "selp.u32 %0, 1, 0, p;\n}" : "=r"(done) : "r"(a), "r"(parity) : "memory");
+        if (done) return true;
+        if (spin == 0) t0 = globaltimer();
+        if ((spin & 1023u) == 1023u) {
+            if (*reinterpret_cast<volatile int *>(err) != 0) return false;
+            if (globaltimer() - t0 > kWaitTimeoutNs) {
+                raise_dev_error(err, kDevTimeout);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"
+                 "%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            uint64_t *bar) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int c0, int c1, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"(map), "r"(c0), "r"(c1), "r"(src) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+struct Barriers {
+    uint64_t x[2];      // TMA of the image in x buffer b
+    uint64_t slot[2];   // row-DFT MMAs that read lo slot s
+    uint64_t inv;       // inverse MMAs
+};
+struct Phases {         // completed-phase counters, identical in every thread
+    uint32_t x[2], slot[2], inv;
+};
+
+__device__ void issue_x(const CUtensorMap *map, char *base, int buf, int img, Barriers *bars) {
+    uint64_t *bar = &bars->x[buf];
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(smem_addr(bar)), "r"(kImageBytes) : "memory");
+    const uint32_t dst = smem_addr(base + kR + buf * kImageBytes);
+    for (int kc = 0; kc < kKChunks; ++kc)
+        tma_load_2d(dst + kc * kChunkBytes, map, 32 * kc, img * Cf::N0, bar);
+}
+
+// Phase A on the image already requested into x buffer `buf`.
+__device__ void phase_a(char *base, int buf, uint32_t tmem, Barriers *bars, Phases &ph,
+                        float2 *part, int img, int *err) {
+    const int tid = threadIdx.x;
+    char *xh = base + kR + buf * kImageBytes;
+    const float2 *tw = reinterpret_cast<const float2 *>(base + kTw);
+    bool ok = mbar_wait(&bars->x[buf], ph.x[buf], err);
+    ph.x[buf]++;
+    constexpr uint32_t idesc = idesc_tf32(32);
+    for (int kc = 0; kc < kKChunks; ++kc) {
+        const int slot = kc & 1;
+        if (kc >= 2) {                      // the MMAs of chunk kc-2 have read this slot
+            ok &= mbar_wait(&bars->slot[slot], ph.slot[slot], err);
+            ph.slot[slot]++;
+        }
+        // lo parts of chunk kc (elementwise, so the swizzled layout carries over)
+        const float4 *src = reinterpret_cast<const float4 *>(xh + kc * kChunkBytes);
+        float4 *dst = reinterpret_cast<float4 *>(base + kXL + slot * kChunkBytes);
+#pragma unroll
+        for (int r = 0; r < (int)(kChunkBytes / 16) / NT; ++r) {
+            const float4 v = src[tid + r * NT];
+            dst[tid + r * NT] = make_float4(tf32_lo(v.x), tf32_lo(v.y), tf32_lo(v.z), tf32_lo(v.w));
+        }
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc_after_sync();
+            const uint32_t ah = smem_addr(xh + kc * kChunkBytes);
+            const uint32_t al = smem_addr(base + kXL + slot * kChunkBytes);
+            const uint32_t bh = smem_addr(base + kT + kc * 4096);
+            const uint32_t bl = smem_addr(base + kT + 16384 + kc * 4096);
+#pragma unroll
+            for (int st = 0; st < 4; ++st) {
+                const uint32_t o = st * 32;
+                const uint32_t acc = (kc | st) ? 1u : 0u;
+                mma_tf32(tmem, desc_sw128(ah + o), desc_sw128(bh + o), idesc, acc);
+                mma_tf32(tmem, desc_sw128(ah + o), desc_sw128(bl + o), idesc, 1u);
+                mma_tf32(tmem, desc_sw128(al + o), desc_sw128(bh + o), idesc, 1u);
+            }
+            mma_commit(&bars->slot[slot]);
+        }
+    }
+    // every MMA of the image is done once the last chunk's commit has landed
+    ok &= mbar_wait(&bars->slot[0], ph.slot[0], err);
+    ph.slot[0]++;
+    ok &= mbar_wait(&bars->slot[1], ph.slot[1], err);
+    ph.slot[1]++;
+    tc_after_sync();
+    // Z (128 rows x 16 bins) from tensor memory into the now free x buffer
+    float *zr = reinterpret_cast<float *>(xh + kZr);
+    float *zi = reinterpret_cast<float *>(xh + kZi);
+    float2 *S = reinterpret_cast<float2 *>(xh + kS);
+    {
+        const int warp = tid >> 5, lane = tid & 31;
+        const int row = 32 * (warp & 3) + lane, half = warp >> 2;
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * half, v);
+        float *dz = (half ? zi : zr) + row * kZS;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) dz[k] = ok ? v[k] : 0.f;
+    }
+    tc_before_sync();
+    __syncthreads();
+    // column DFT over the 128 rows, r = r1 + 8 r2: 16-point FFTs over r2
+    if (tid < 128) {
+        const int r1 = tid >> 4, k = tid & 15;
+        float2 z[16];
+#pragma unroll
+        for (int r2 = 0; r2 < 16; ++r2) {
+            const int r = r1 + 8 * r2;
+            z[r2] = make_float2(zr[r * kZS + k], zi[r * kZS + k]);
+        }
+        fft::fft_dif<16, -1>(z);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) S[(r1 * 16 + q) * 16 + k] = z[fft::bitrev(q, 4)];
+    }
+    __syncthreads();
+    // X[j][k] = sum_r1 W_128^{f r1} S[r1][f mod 16][k]
+    float2 *dst = part + (size_t)img * Cf::NK;
+#pragma unroll
+    for (int rep = 0; rep < Cf::NK / NT; ++rep) {
+        const int o = tid + rep * NT;
+        const int j = o >> 4, k = o & 15;
+        const int f = kept_freq<Cf>(j);
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int r1 = 0; r1 < 8; ++r1) cmac(acc, S[(r1 * 16 + (f & 15)) * 16 + k], tw[(f * r1) & 127]);
+        __stcg(dst + o, acc);
+    }
+    fence_async_smem();      // these generic writes precede any later TMA into this buffer
+}
+
+// Phase C for one output image.
+__device__ void phase_c(char *base, uint32_t tmem, Barriers *bars, Phases &ph, const float2 *Y,
+                        const CUtensorMap *ymap, int img, int *err) {
+    const int tid = threadIdx.x;
+    float2 *ys = reinterpret_cast<float2 *>(base + kR + kCY);
+    char *ahi = base + kR + kCAhi, *alo = base + kR + kCAlo, *stage = base + kR + kCStage;
+    const float2 *tw = reinterpret_cast<const float2 *>(base + kTw);
+    const float2 *src = Y + (size_t)img * Cf::NK;
+    for (int e = tid; e < Cf::NK / 2; e += NT) cp_async16(ys + 2 * e, src + 2 * e);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    // Zo[r1 + 8 r2][k] = IFFT_16 over q of V[q], V[q] = Y[q] w^{-q r1} + Y[16+q] w^{-(112+q) r1}
+    if (tid < 128) {
+        const int r1 = tid >> 4, k = tid & 15;
+        float2 v[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            float2 a = cmulc(ys[q * 16 + k], tw[(q * r1) & 127]);
+            const float2 b = cmulc(ys[(16 + q) * 16 + k], tw[((112 + q) * r1) & 127]);
+            a.x += b.x;
+            a.y += b.y;
+            v[q] = a;
+        }
+        fft::fft_dif<16, 1>(v);
+#pragma unroll
+        for (int r2 = 0; r2 < 16; ++r2) {
+            const int row = r1 + 8 * r2;
+            const float2 z = v[fft::bitrev(r2, 4)];
+            *reinterpret_cast<float *>(ahi + sw_off(row, k)) = z.x;
+            *reinterpret_cast<float *>(ahi + sw_off(row, 16 + k)) = z.y;
+            *reinterpret_cast<float *>(alo + sw_off(row, k)) = tf32_lo(z.x);
+            *reinterpret_cast<float *>(alo + sw_off(row, 16 + k)) = tf32_lo(z.y);
+        }
+    }
+    fence_async_smem();
+    __syncthreads();
+    constexpr uint32_t idesc = idesc_tf32(128);
+    if (tid == 0) {
+        tc_after_sync();
+        const uint32_t ah = smem_addr(ahi), al = smem_addr(alo);
+        const uint32_t bh = smem_addr(base + kTi), bl = smem_addr(base + kTi + 16384);
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+            const uint32_t o = st * 32;
+            mma_tf32(tmem + 32, desc_sw128(ah + o), desc_sw128(bh + o), idesc, st ? 1u : 0u);
+            mma_tf32(tmem + 32, desc_sw128(ah + o), desc_sw128(bl + o), idesc, 1u);
+            mma_tf32(tmem + 32, desc_sw128(al + o), desc_sw128(bh + o), idesc, 1u);
+        }
+        mma_commit(&bars->inv);
+    }
+    const bool ok = mbar_wait(&bars->inv, ph.inv, err);
+    ph.inv++;
+    tc_after_sync();
+    // y rows from tensor memory into the swizzled staging tile
+    {
+        const int warp = tid >> 5, lane = tid & 31;
+        const int row = 32 * (warp & 3) + lane, half = warp >> 2;
+#pragma unroll
+        for (int part16 = 0; part16 < 4; ++part16) {
+            float v[16];
+            const int col0 = 64 * half + 16 * part16;
+            tmem_ld16(tmem + 32 + ((uint32_t)(32 * (warp & 3)) << 16) + col0, v);
+            const int cc = col0 >> 5;
+#pragma unroll
+            for (int p4 = 0; p4 < 4; ++p4) {
+                const int col = (col0 & 31) + 4 * p4;
+                *reinterpret_cast<float4 *>(stage + cc * kChunkBytes + sw_off(row, col)) =
+                    ok ? make_float4(v[4 * p4], v[4 * p4 + 1], v[4 * p4 + 2], v[4 * p4 + 3])
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+    }
+    tc_before_sync();
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        const uint32_t s0 = smem_addr(stage);
+        for (int cc = 0; cc < kKChunks; ++cc) tma_store_2d(ymap, 32 * cc, img * Cf::N0, s0 + cc * kChunkBytes);
+        bulk_commit();
+    }
+}
+
+__global__ void __launch_bounds__(NT, 1)
+k_fused2d_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
+             Args a, const float4 *tables) {
+    extern __shared__ __align__(1024) char smem_raw[];
+    char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+    __shared__ Barriers bars;
+    __shared__ uint32_t s_tmem;
+    __shared__ Item s_cur, s_next;
+    __shared__ int s_ok;
+    const int tid = threadIdx.x;
+    // twiddle operands (already in their swizzled shared-memory image) and W_128
+    for (int e = tid; e < (int)(kTableBytes / 16); e += NT)
+        reinterpret_cast<float4 *>(base + kT)[e] = tables[e];
+    for (int e = tid; e < 128; e += NT) reinterpret_cast<float2 *>(base + kTw)[e] = a.tw0[e];
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars.x[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars.slot[i])));
+        }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars.inv)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (tid < 32) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_addr(&s_tmem)), "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    fence_async_smem();
+    tc_before_sync();
+    __syncthreads();
+    tc_after_sync();
+    const uint32_t tmem = s_tmem;
+    Phases ph{{0, 0}, {0, 0}, 0};
+    const int nimg_in = a.batch * a.cin;
+    int buf = 0;
+    bool loaded = false;               // the current A item's image is already requested
+    if (tid == 0) s_cur = decode_ticket<Cf>(a, atomicAdd(&a.sync->ticket[0], 1));
+    __syncthreads();
+    Item cur = s_cur;
+    while (cur.phase >= 0) {
+        if (tid == 0) {
+            bulk_wait_read();          // staged output has been read before R is reused
+            const Item nxt = decode_ticket<Cf>(a, atomicAdd(&a.sync->ticket[0], 1));
+            s_next = nxt;
+            if (cur.phase == 0) {
+                if (!loaded) issue_x(&xmap, base, buf, cur.g * a.bg * a.cin + cur.idx, &bars);
+                if (nxt.phase == 0)
+                    issue_x(&xmap, base, buf ^ 1, nxt.g * a.bg * a.cin + nxt.idx, &bars);
+            }
+        }
+        __syncthreads();
+        const Item nxt = s_next;
+        const int nbg = min(a.bg, a.batch - cur.g * a.bg);
+        if (cur.phase == 0) {
+            phase_a(base, buf, tmem, &bars, ph, a.part, cur.g * a.bg * a.cin + cur.idx, a.err);
+            __syncthreads();
+            if (tid == 0)
+                finish_item(&a.sync->done_a[cur.g][0], nbg * a.cin, a.sync->flag_a[cur.g]);
+        } else if (cur.phase == 1) {
+            BItem bi;
+            bi.pair = cur.idx / a.nob;
+            bi.o0 = (cur.idx % a.nob) * a.ob;
+            bi.nob = min(a.ob, a.cout - bi.o0);
+            bi.b0 = cur.g * a.bg;
+            bi.nbb = nbg;
+            phase_b_weights<Cf, float, NT>(static_cast<const float *>(a.w), a.cin, a.cout, bi,
+                                           a.ob, base + kR);
+            if (tid == 0)
+                s_ok = wait_flag(&a.sync->flag_a[cur.g][blockIdx.x % kFlagCopies][0], a.err);
+            __syncthreads();
+            if (s_ok) phase_b<Cf, float, NT>(a.part, a.Y, a.cin, a.cout, nimg_in, bi, a.ob, base + kR);
+            else cp_async_wait_all();
+            __syncthreads();
+            if (tid == 0)
+                finish_item(&a.sync->done_b[cur.g][0], a.npairs * a.nob, a.sync->flag_b[cur.g]);
+        } else {
+            if (tid == 0)
+                s_ok = wait_flag(&a.sync->flag_b[cur.g][blockIdx.x % kFlagCopies][0], a.err);
+            __syncthreads();
+            if (s_ok)
+                phase_c(base, tmem, &bars, ph, a.Y, &ymap, cur.g * a.bg * a.cout + cur.idx, a.err);
+        }
+        const bool prefetched = cur.phase == 0 && nxt.phase == 0;
+        if (cur.phase == 0 && prefetched) buf ^= 1;
+        loaded = prefetched;
+        cur = nxt;
+        fence_async_smem();            // generic writes to R precede any later TMA into it
+        __syncthreads();
+    }
+    if (tid == 0) bulk_wait_all();
+    tc_before_sync();
+    __syncthreads();
+    tc_after_sync();
+    if (tid < 32)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    if (tid == 0) {
+        __threadfence();
+        const int prev = atomicAdd(&a.sync->exited[0], 1);
+        if (prev == (int)gridDim.x - 1) {
+            a.sync->ticket[0] = 0;
+            for (int g = 0; g < a.ng; ++g) {
+                a.sync->done_a[g][0] = 0;
+                a.sync->done_b[g][0] = 0;
+                for (int i = 0; i < kFlagCopies; ++i) {
+                    a.sync->flag_a[g][i][0] = 0;
+                    a.sync->flag_b[g][i][0] = 0;
+                }
+            }
+            __threadfence();
+            a.sync->exited[0] = 0;
+        }
+    }
+}
+
+// Host: the forward and inverse twiddle operands in their swizzled shared
+// memory image, hi and lo parts, computed in double.
+void make_tables(float *img) {
+    memset(img, 0, kTableBytes);
+    auto put = [&](uint32_t region, int row, int col, double v) {
+        // region: byte offset of the operand; chunks of 32 columns, 4096 B (32 rows)
+        // for the forward operand, one 16 KiB chunk (128 rows) for the inverse one
+        const float hi = (float)v;
+        const float lo = (float)(v - (double)(hi - tf32_lo(hi)));
+        img[(region + sw_off(row, col)) / 4] = hi;
+        img[(region + 16384 + sw_off(row, col)) / 4] = lo;
+    };
+    const double two_pi = 2.0 * M_PI;
+    for (int k = 0; k < 16; ++k)
+        for (int n = 0; n < 128; ++n) {
+            const double a = two_pi * k * n / 128.0;
+            const uint32_t chunk = (uint32_t)(n / 32) * 4096;
+            put(chunk, k, n % 32, std::cos(a));
+            put(chunk, 16 + k, n % 32, -std::sin(a));
+        }
+    const double scale = 1.0 / (128.0 * 128.0);
+    for (int n = 0; n < 128; ++n)
+        for (int k = 0; k < 16; ++k) {
+            const double a = two_pi * k * n / 128.0, c = k == 0 ? 1.0 : 2.0;
+            put(32768, n, k, c * scale * std::cos(a));
+            put(32768, n, 16 + k, -c * scale * std::sin(a));
+        }
+}
+
+}  // namespace tc
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -740,24 +1219,114 @@ void *kernel_ptr() {
     return reinterpret_cast<void *>(&k_fused2d<Cfg128, T>);
 }
 
+// ----- tensor-core variant: host side -----
+typedef CUresult (*EncodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+    static EncodeTiled fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(ptr);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// (rows x 128) float32 matrix, 32-column x 128-row boxes, 128-byte swizzle
+bool encode_rows(CUtensorMap *map, const void *ptr, int64_t rows) {
+    EncodeTiled fn = encoder();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {128 * sizeof(float)};
+    const cuuint32_t box[2] = {32, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr size_t kTcWsBudget = 64u << 10;
+constexpr size_t kTcXpBudget = 48u << 10;
+
+BShape b_shape_tc(int64_t batch, int cin, int cout) {
+    BShape s;
+    s.ob = cout;
+    while (s.ob > 1 && (size_t)cin * s.ob * 16 > kTcWsBudget) s.ob = (s.ob + 1) / 2;
+    s.bg = (int)((batch + kTargetGroups - 1) / kTargetGroups);
+    while (s.bg > 1 && (size_t)s.bg * cin * 16 > kTcXpBudget) s.bg = (s.bg + 1) / 2;
+    while ((batch + s.bg - 1) / s.bg > kMaxGroups) ++s.bg;
+    return s;
+}
+
+Layout layout_tc(const Geom &g, int64_t batch, int cin, int cout) {
+    Layout l;
+    l.part_off = 0;
+    l.y_off = ((size_t)batch * cin * g.nkept * sizeof(float2) + 255) & ~size_t(255);
+    l.total = l.y_off + (((size_t)batch * cout * g.nkept * sizeof(float2) + 255) & ~size_t(255));
+    return l;
+}
+
+bool use_tc(const Geom &g, fno_dtype_t dtype) { return is_cfg128(g) && dtype == FNO_F32; }
+
 }  // namespace
 
 size_t fused_sync_bytes() { return kSyncBytes; }
 
 bool fused_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout) {
     if (!is_cfg128(g) || (dtype != FNO_F32 && dtype != FNO_F16)) return false;
+    if (use_tc(g, dtype))
+        return batch * (int64_t)(cin > cout ? cin : cout) * 128 < (1ll << 31) &&
+               (size_t)cin * 16 <= kTcXpBudget;
     if (batch * (int64_t)cin * Cfg128::C >= (1 << 30) || batch * (int64_t)cout * Cfg128::C >= (1 << 30))
         return false;
     return smem_bytes(dtype, cin, b_shape(dtype, batch, cin, cout)) <= 200 * 1024;
 }
 
-size_t fused_workspace_bytes(const Geom &g, fno_dtype_t, int64_t batch, int cin, int cout) {
-    return layout(g, batch, cin, cout).total;
+size_t fused_workspace_bytes(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout) {
+    return use_tc(g, dtype) ? layout_tc(g, batch, cin, cout).total
+                            : layout(g, batch, cin, cout).total;
 }
 
 int fused_kernel_count(const Geom &, fno_dtype_t, int64_t, int, int) { return 1; }
 
 cudaError_t fused_plan_init(Plan &p) {
+    if (use_tc(p.g, p.dtype)) {
+        if (!encoder()) return cudaErrorNotSupported;
+        const BShape bs = b_shape_tc(p.batch, p.cin, p.cout);
+        cudaError_t e = cudaFuncSetAttribute(tc::k_fused2d_tc,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)tc::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc::k_fused2d_tc, tc::NT,
+                                                           tc::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        // one CTA per SM: each holds kTmemCols columns of tensor memory
+        p.fused_grid = p.num_sms;
+        p.fused_smem = tc::kSmemBytes;
+        p.fused_ob = bs.ob;
+        p.fused_bb = bs.bg;
+        float *host = new (std::nothrow) float[tc::kTableBytes / 4];
+        if (!host) return cudaErrorMemoryAllocation;
+        tc::make_tables(host);
+        e = cudaMalloc(&p.fused_tables, tc::kTableBytes);
+        if (e == cudaSuccess)
+            e = cudaMemcpy(p.fused_tables, host, tc::kTableBytes, cudaMemcpyHostToDevice);
+        delete[] host;
+        if (e != cudaSuccess) return e;
+        return cudaMemset(p.sync, 0, kSyncBytes);
+    }
     const BShape bs = b_shape(p.dtype, p.batch, p.cin, p.cout);
     const size_t smem = smem_bytes(p.dtype, p.cin, bs);
     void *fn = p.dtype == FNO_F32 ? kernel_ptr<float>() : kernel_ptr<__half>();
@@ -775,9 +1344,42 @@ cudaError_t fused_plan_init(Plan &p) {
     return cudaMemset(p.sync, 0, kSyncBytes);
 }
 
-void fused_plan_release(Plan &) {}
+void fused_plan_release(Plan &p) {
+    if (p.fused_tables) cudaFree(p.fused_tables);
+    p.fused_tables = nullptr;
+}
 
 cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
+    if (use_tc(p.g, p.dtype)) {
+        const Layout l = layout_tc(p.g, p.batch, p.cin, p.cout);
+        CUtensorMap xmap, ymap;
+        if (!encode_rows(&xmap, b.x, p.batch * p.cin * 128) ||
+            !encode_rows(&ymap, b.y, p.batch * p.cout * 128))
+            return cudaErrorInvalidValue;
+        Args a;
+        a.x = b.x;
+        a.w = b.w;
+        a.y = b.y;
+        a.part = reinterpret_cast<float2 *>(static_cast<char *>(b.ws) + l.part_off);
+        a.Y = reinterpret_cast<float2 *>(static_cast<char *>(b.ws) + l.y_off);
+        a.sync = reinterpret_cast<SyncBlock *>(p.sync);
+        a.tw0 = p.tw[0];
+        a.tw1 = p.tw[1];
+        a.err = p.dev_err;
+        a.batch = (int)p.batch;
+        a.cin = p.cin;
+        a.cout = p.cout;
+        a.bg = p.fused_bb;
+        a.ng = (int)((p.batch + a.bg - 1) / a.bg);
+        a.npairs = (int)(p.g.nkept / kG);
+        a.ob = p.fused_ob;
+        a.nob = (p.cout + a.ob - 1) / a.ob;
+        const int total = (int)p.batch * (p.cin + p.cout) + a.ng * a.npairs * a.nob;
+        const int grid = p.fused_grid < total ? p.fused_grid : total;
+        tc::k_fused2d_tc<<<grid, tc::NT, p.fused_smem, s>>>(
+            xmap, ymap, a, static_cast<const float4 *>(p.fused_tables));
+        return cudaGetLastError();
+    }
     const Layout l = layout(p.g, p.batch, p.cin, p.cout);
     Args a;
     a.x = b.x;

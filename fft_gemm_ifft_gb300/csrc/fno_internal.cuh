@@ -52,6 +52,7 @@ struct Plan {
     size_t fused_smem;
     int fused_ob;
     int fused_bb;
+    void *fused_tables;           // tensor-core path: twiddle operands (plan-owned)
 };
 
 enum { kPathUnfused = 0, kPathFused2D = 1, kPathFused1D = 2 };
