@@ -323,14 +323,26 @@ __device__ void phase_a(const T *__restrict__ x, float2 *__restrict__ part, int 
 // of BT batch rows x 2 outputs x 2 bins over every S-th input channel; the S
 // lanes that share a tile then combine their sums by a shuffle reduce-scatter.
 // ---------------------------------------------------------------------------
+// A group of threads that runs one item: the whole CTA, or one of the
+// independent streams of the tensor-core kernel (synchronised by a named barrier).
+struct CtaGroup {
+    int tid;
+    __device__ void sync() const { __syncthreads(); }
+};
+struct StreamGroup {
+    int tid;
+    int bar;      // named barrier id (1, 2, ...), 256 threads
+    __device__ void sync() const { asm volatile("bar.sync %0, 256;" ::"r"(bar) : "memory"); }
+};
+
 struct BItem {
     int pair, o0, nob, b0, nbb;
 };
 constexpr int kBT = 4;      // batch rows per register tile
 
-template <class Cf, typename T, int NT>
-__device__ void phase_b_weights(const T *__restrict__ w, int cin, int cout, const BItem &it,
-                                int ob, char *smem) {
+template <class Cf, typename T, int NT, class G>
+__device__ void phase_b_weights(const G &grp, const T *__restrict__ w, int cin, int cout,
+                                const BItem &it, int ob, char *smem) {
     using W2 = typename Io<T>::W2;
     constexpr int M0 = Cf::M0, M1 = Cf::M1;
     const int mode0 = it.pair * kG;
@@ -338,7 +350,7 @@ __device__ void phase_b_weights(const T *__restrict__ w, int cin, int cout, cons
     const int blk = j >= M0 ? 1 : 0, l0 = j - blk * M0;
     W2 *ws = reinterpret_cast<W2 *>(smem);                   // [cin][ob]
     const size_t mblk = (size_t)M0 * M1;
-    for (int e = threadIdx.x; e < cin * it.nob; e += NT) {
+    for (int e = grp.tid; e < cin * it.nob; e += NT) {
         const int o = e % it.nob, i = e / it.nob;
         const T *p = w + ((((size_t)blk * cin + i) * cout + it.o0 + o) * mblk + l0 * M1 + k0) * 2;
         if constexpr (sizeof(W2) == 16)
@@ -356,8 +368,8 @@ __host__ __device__ inline int b_split(int tiles, int nt) {
     return s;
 }
 
-template <class Cf, typename T, int S, int NT>
-__device__ void phase_b_tiles(float2 *__restrict__ Y, int cin, int cout, const BItem &it,
+template <class Cf, typename T, int S, int NT, class G>
+__device__ void phase_b_tiles(const G &grp, float2 *__restrict__ Y, int cin, int cout, const BItem &it,
                               int ob, const typename Io<T>::W2 *ws, const float4 *xp,
                               int tiles) {
     using W2 = typename Io<T>::W2;
@@ -369,7 +381,7 @@ __device__ void phase_b_tiles(float2 *__restrict__ Y, int cin, int cout, const B
     // every lane of a warp runs the same number of passes (the shuffles below
     // need the whole warp); lanes past the last tile add zeros and store nothing
     const int total = tiles * S, bound = (total + 31) / 32 * 32;
-    for (int u = threadIdx.x; u < bound; u += NT) {
+    for (int u = grp.tid; u < bound; u += NT) {
         const bool active = u < total;
         const int s = u % S, tile = active ? u / S : 0;
         const int o = 2 * (tile % no2), b = kBT * (tile / no2);
@@ -425,15 +437,15 @@ __device__ void phase_b_tiles(float2 *__restrict__ Y, int cin, int cout, const B
     }
 }
 
-template <class Cf, typename T, int NT>
-__device__ void phase_b(const float2 *__restrict__ part, float2 *__restrict__ Y, int cin,
+template <class Cf, typename T, int NT, class G>
+__device__ void phase_b(const G &grp, const float2 *__restrict__ part, float2 *__restrict__ Y, int cin,
                         int cout, int nimg_in, const BItem &it, int ob, char *smem) {
     using W2 = typename Io<T>::W2;
     constexpr int NK = Cf::NK, C = Cf::C;
     const int mode0 = it.pair * kG;
     const W2 *ws = reinterpret_cast<const W2 *>(smem);                       // [cin][ob]
     float4 *xp = reinterpret_cast<float4 *>(smem + ((size_t)cin * ob * sizeof(W2) + 15) / 16 * 16);
-    const int tid = threadIdx.x;
+    const int tid = grp.tid;
     const int nr = it.nbb * cin;                         // rows (b, i) of this item
     // partial modes of the C chunks: xp[cc][r] = X_cc[b0*cin + r][mode0 .. mode0+1]
     for (int e = tid; e < C * nr; e += NT) {
@@ -442,7 +454,7 @@ __device__ void phase_b(const float2 *__restrict__ part, float2 *__restrict__ Y,
     }
     cp_async_commit();
     cp_async_wait_all();                                 // also covers the weight slab
-    __syncthreads();
+    grp.sync();
     for (int r = tid; r < nr; r += NT) {
         float4 s = xp[r];
 #pragma unroll
@@ -452,15 +464,15 @@ __device__ void phase_b(const float2 *__restrict__ part, float2 *__restrict__ Y,
         }
         xp[r] = s;
     }
-    __syncthreads();
+    grp.sync();
     const int nbt = (it.nbb + kBT - 1) / kBT, no2 = (it.nob + 1) / 2;
     const int tiles = nbt * no2;
     switch (b_split(tiles, NT)) {
-        case 16: phase_b_tiles<Cf, T, 16, NT>(Y, cin, cout, it, ob, ws, xp, tiles); break;
-        case 8: phase_b_tiles<Cf, T, 8, NT>(Y, cin, cout, it, ob, ws, xp, tiles); break;
-        case 4: phase_b_tiles<Cf, T, 4, NT>(Y, cin, cout, it, ob, ws, xp, tiles); break;
-        case 2: phase_b_tiles<Cf, T, 2, NT>(Y, cin, cout, it, ob, ws, xp, tiles); break;
-        default: phase_b_tiles<Cf, T, 1, NT>(Y, cin, cout, it, ob, ws, xp, tiles); break;
+        case 16: phase_b_tiles<Cf, T, 16, NT>(grp, Y, cin, cout, it, ob, ws, xp, tiles); break;
+        case 8: phase_b_tiles<Cf, T, 8, NT>(grp, Y, cin, cout, it, ob, ws, xp, tiles); break;
+        case 4: phase_b_tiles<Cf, T, 4, NT>(grp, Y, cin, cout, it, ob, ws, xp, tiles); break;
+        case 2: phase_b_tiles<Cf, T, 2, NT>(grp, Y, cin, cout, it, ob, ws, xp, tiles); break;
+        default: phase_b_tiles<Cf, T, 1, NT>(grp, Y, cin, cout, it, ob, ws, xp, tiles); break;
     }
 }
 
@@ -650,11 +662,12 @@ k_fused2d(Args a) {
             bi.b0 = it.g * a.bg;
             bi.nbb = nbg;
             // the weights do not depend on phase A: request them first
-            phase_b_weights<Cf, T, kNT>(static_cast<const T *>(a.w), a.cin, a.cout, bi, a.ob, work);
+            phase_b_weights<Cf, T, kNT>(CtaGroup{tid}, static_cast<const T *>(a.w), a.cin, a.cout, bi,
+                                        a.ob, work);
             if (tid == 0)
                 s_ok = wait_flag(&a.sync->flag_a[it.g][blockIdx.x % kFlagCopies][0], a.err);
             __syncthreads();
-            if (s_ok) phase_b<Cf, T, kNT>(a.part, a.Y, a.cin, a.cout, nimg_in, bi, a.ob, work);
+            if (s_ok) phase_b<Cf, T, kNT>(CtaGroup{tid}, a.part, a.Y, a.cin, a.cout, nimg_in, bi, a.ob, work);
             else cp_async_wait_all();
             __syncthreads();
             if (tid == 0)
@@ -711,7 +724,8 @@ k_fused2d(Args a) {
 // ---------------------------------------------------------------------------
 namespace tc {
 
-constexpr int NT = 256;
+constexpr int kStreams = 2;                // independent item streams per CTA
+constexpr int NT = 256;                    // threads per stream
 struct Cf {
     static constexpr int N0 = 128, M0 = 16, M1 = 16, K0 = 32, NK = K0 * M1;
     static constexpr int C = 1;            // one item covers a whole image
@@ -720,17 +734,18 @@ constexpr int kKChunks = 4;                // 32-column K chunks of the row DFT
 constexpr uint32_t kChunkBytes = 16384;    // 128 rows x 128 bytes
 constexpr uint32_t kImageBytes = kKChunks * kChunkBytes;
 // shared-memory map (offsets from a 1024-aligned base)
-constexpr uint32_t kR = 0;                 // 128 KiB: x tiles (A) / mixing (B) / inverse (C)
-constexpr uint32_t kXL = 131072;           // 32 KiB: lo parts of two K chunks (A)
-constexpr uint32_t kT = 163840;            // 32 KiB: forward twiddle operand, hi then lo
-constexpr uint32_t kTi = 196608;           // 32 KiB: inverse twiddle operand, hi then lo
-constexpr uint32_t kTw = 229376;           // 1 KiB: W_128^e
+constexpr uint32_t kStreamBytes = 81920;   // per stream: x tile 64 KiB + lo slot 16 KiB
+constexpr uint32_t kXL = 65536;            // lo slot, inside a stream's region
+constexpr uint32_t kT = kStreams * kStreamBytes;   // 32 KiB: forward operand, hi then lo
+constexpr uint32_t kTi = kT + 32768;       // 32 KiB: inverse operand, hi then lo
+constexpr uint32_t kTw = kTi + 32768;      // 1 KiB: W_128^e
 constexpr uint32_t kSmemBytes = kTw + 1024 + 1024;   // + alignment slack
 constexpr uint32_t kTableBytes = 65536;    // forward + inverse operands (global image)
-constexpr int kTmemCols = 256;             // [0,32): forward D; [32,160): inverse D
-// inside R during a C item
-constexpr uint32_t kCY = 0, kCAhi = 8192, kCAlo = 24576, kCStage = 65536;
-// inside the current x buffer after its MMAs (A item)
+constexpr int kTmemCols = 512;             // stream s: [256 s, 256 s + 32) forward D,
+constexpr int kTmemInv = 32;               //           [256 s + 32, 256 s + 160) inverse D
+// inside a stream's region during a C item
+constexpr uint32_t kCY = 0, kCAhi = 8192, kCAlo = 24576, kCStage = 40960;
+// inside the x tile after its MMAs (A item)
 constexpr int kZS = 17;                    // row stride of the Z planes (floats)
 constexpr uint32_t kZr = 0, kZi = 128 * kZS * 4, kS = 2 * 128 * kZS * 4;
 
@@ -824,73 +839,69 @@ __device__ __forceinline__ void bulk_wait_read() {
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// one stream's barriers and completed-phase counters (counters identical in
+// every thread of the stream)
 struct Barriers {
-    uint64_t x[2];      // TMA of the image in x buffer b
-    uint64_t slot[2];   // row-DFT MMAs that read lo slot s
+    uint64_t x;         // TMA of the x tile
+    uint64_t mma;       // row-DFT MMAs of one K chunk (they read the lo slot)
     uint64_t inv;       // inverse MMAs
 };
-struct Phases {         // completed-phase counters, identical in every thread
-    uint32_t x[2], slot[2], inv;
+struct Phases {
+    uint32_t x, mma, inv;
+};
+struct Stream {
+    StreamGroup grp;
+    char *region;       // the stream's 80 KiB
+    uint32_t tmem;      // the stream's first tensor-memory column
+    Barriers *bars;
 };
 
-__device__ void issue_x(const CUtensorMap *map, char *base, int buf, int img, Barriers *bars) {
-    uint64_t *bar = &bars->x[buf];
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                 ::"r"(smem_addr(bar)), "r"(kImageBytes) : "memory");
-    const uint32_t dst = smem_addr(base + kR + buf * kImageBytes);
-    for (int kc = 0; kc < kKChunks; ++kc)
-        tma_load_2d(dst + kc * kChunkBytes, map, 32 * kc, img * Cf::N0, bar);
-}
-
-// Phase A on the image already requested into x buffer `buf`.
-__device__ void phase_a(char *base, int buf, uint32_t tmem, Barriers *bars, Phases &ph,
+// Phase A: the x tile of image `img` -> its 512 kept modes.
+__device__ void phase_a(const Stream &st, Phases &ph, const char *base, const CUtensorMap *xmap,
                         float2 *part, int img, int *err) {
-    const int tid = threadIdx.x;
-    char *xh = base + kR + buf * kImageBytes;
+    const int tid = st.grp.tid;
+    char *xh = st.region;
+    char *xl = st.region + kXL;
     const float2 *tw = reinterpret_cast<const float2 *>(base + kTw);
-    bool ok = mbar_wait(&bars->x[buf], ph.x[buf], err);
-    ph.x[buf]++;
+    if (tid == 0) {
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     ::"r"(smem_addr(&st.bars->x)), "r"(kImageBytes) : "memory");
+        const uint32_t dst = smem_addr(xh);
+        for (int kc = 0; kc < kKChunks; ++kc)
+            tma_load_2d(dst + kc * kChunkBytes, xmap, 32 * kc, img * Cf::N0, &st.bars->x);
+    }
+    bool ok = mbar_wait(&st.bars->x, ph.x++, err);
     constexpr uint32_t idesc = idesc_tf32(32);
     for (int kc = 0; kc < kKChunks; ++kc) {
-        const int slot = kc & 1;
-        if (kc >= 2) {                      // the MMAs of chunk kc-2 have read this slot
-            ok &= mbar_wait(&bars->slot[slot], ph.slot[slot], err);
-            ph.slot[slot]++;
-        }
+        if (kc > 0) ok &= mbar_wait(&st.bars->mma, ph.mma++, err);   // lo slot free again
         // lo parts of chunk kc (elementwise, so the swizzled layout carries over)
         const float4 *src = reinterpret_cast<const float4 *>(xh + kc * kChunkBytes);
-        float4 *dst = reinterpret_cast<float4 *>(base + kXL + slot * kChunkBytes);
+        float4 *dst = reinterpret_cast<float4 *>(xl);
 #pragma unroll
         for (int r = 0; r < (int)(kChunkBytes / 16) / NT; ++r) {
             const float4 v = src[tid + r * NT];
             dst[tid + r * NT] = make_float4(tf32_lo(v.x), tf32_lo(v.y), tf32_lo(v.z), tf32_lo(v.w));
         }
         fence_async_smem();
-        __syncthreads();
+        st.grp.sync();
         if (tid == 0) {
             tc_after_sync();
-            const uint32_t ah = smem_addr(xh + kc * kChunkBytes);
-            const uint32_t al = smem_addr(base + kXL + slot * kChunkBytes);
+            const uint32_t ah = smem_addr(xh + kc * kChunkBytes), al = smem_addr(xl);
             const uint32_t bh = smem_addr(base + kT + kc * 4096);
             const uint32_t bl = smem_addr(base + kT + 16384 + kc * 4096);
 #pragma unroll
-            for (int st = 0; st < 4; ++st) {
-                const uint32_t o = st * 32;
-                const uint32_t acc = (kc | st) ? 1u : 0u;
-                mma_tf32(tmem, desc_sw128(ah + o), desc_sw128(bh + o), idesc, acc);
-                mma_tf32(tmem, desc_sw128(ah + o), desc_sw128(bl + o), idesc, 1u);
-                mma_tf32(tmem, desc_sw128(al + o), desc_sw128(bh + o), idesc, 1u);
+            for (int s = 0; s < 4; ++s) {
+                const uint32_t o = s * 32;
+                mma_tf32(st.tmem, desc_sw128(ah + o), desc_sw128(bh + o), idesc, (kc | s) ? 1u : 0u);
+                mma_tf32(st.tmem, desc_sw128(ah + o), desc_sw128(bl + o), idesc, 1u);
+                mma_tf32(st.tmem, desc_sw128(al + o), desc_sw128(bh + o), idesc, 1u);
             }
-            mma_commit(&bars->slot[slot]);
+            mma_commit(&st.bars->mma);
         }
     }
-    // every MMA of the image is done once the last chunk's commit has landed
-    ok &= mbar_wait(&bars->slot[0], ph.slot[0], err);
-    ph.slot[0]++;
-    ok &= mbar_wait(&bars->slot[1], ph.slot[1], err);
-    ph.slot[1]++;
+    ok &= mbar_wait(&st.bars->mma, ph.mma++, err);   // the last chunk: every MMA is done
     tc_after_sync();
-    // Z (128 rows x 16 bins) from tensor memory into the now free x buffer
+    // Z (128 rows x 16 bins) from tensor memory into the now free x tile
     float *zr = reinterpret_cast<float *>(xh + kZr);
     float *zi = reinterpret_cast<float *>(xh + kZi);
     float2 *S = reinterpret_cast<float2 *>(xh + kS);
@@ -898,14 +909,15 @@ __device__ void phase_a(char *base, int buf, uint32_t tmem, Barriers *bars, Phas
         const int warp = tid >> 5, lane = tid & 31;
         const int row = 32 * (warp & 3) + lane, half = warp >> 2;
         float v[16];
-        tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * half, v);
+        tmem_ld16(st.tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * half, v);
         float *dz = (half ? zi : zr) + row * kZS;
 #pragma unroll
         for (int k = 0; k < 16; ++k) dz[k] = ok ? v[k] : 0.f;
     }
     tc_before_sync();
-    __syncthreads();
-    // column DFT over the 128 rows, r = r1 + 8 r2: 16-point FFTs over r2
+    st.grp.sync();
+    // column DFT over the 128 rows, r = r1 + 8 r2: 16-point FFTs over r2, one
+    // (r1, bin) per thread for half the stream, the twiddled sums for all of it
     if (tid < 128) {
         const int r1 = tid >> 4, k = tid & 15;
         float2 z[16];
@@ -918,7 +930,7 @@ __device__ void phase_a(char *base, int buf, uint32_t tmem, Barriers *bars, Phas
 #pragma unroll
         for (int q = 0; q < 16; ++q) S[(r1 * 16 + q) * 16 + k] = z[fft::bitrev(q, 4)];
     }
-    __syncthreads();
+    st.grp.sync();
     // X[j][k] = sum_r1 W_128^{f r1} S[r1][f mod 16][k]
     float2 *dst = part + (size_t)img * Cf::NK;
 #pragma unroll
@@ -931,21 +943,21 @@ __device__ void phase_a(char *base, int buf, uint32_t tmem, Barriers *bars, Phas
         for (int r1 = 0; r1 < 8; ++r1) cmac(acc, S[(r1 * 16 + (f & 15)) * 16 + k], tw[(f * r1) & 127]);
         __stcg(dst + o, acc);
     }
-    fence_async_smem();      // these generic writes precede any later TMA into this buffer
+    fence_async_smem();      // these generic writes precede the next TMA into this tile
 }
 
-// Phase C for one output image.
-__device__ void phase_c(char *base, uint32_t tmem, Barriers *bars, Phases &ph, const float2 *Y,
+// Phase C: the mixed modes of output image `img` -> its 128 rows.
+__device__ void phase_c(const Stream &st, Phases &ph, const char *base, const float2 *Y,
                         const CUtensorMap *ymap, int img, int *err) {
-    const int tid = threadIdx.x;
-    float2 *ys = reinterpret_cast<float2 *>(base + kR + kCY);
-    char *ahi = base + kR + kCAhi, *alo = base + kR + kCAlo, *stage = base + kR + kCStage;
+    const int tid = st.grp.tid;
+    float2 *ys = reinterpret_cast<float2 *>(st.region + kCY);
+    char *ahi = st.region + kCAhi, *alo = st.region + kCAlo, *stage = st.region + kCStage;
     const float2 *tw = reinterpret_cast<const float2 *>(base + kTw);
     const float2 *src = Y + (size_t)img * Cf::NK;
     for (int e = tid; e < Cf::NK / 2; e += NT) cp_async16(ys + 2 * e, src + 2 * e);
     cp_async_commit();
     cp_async_wait_all();
-    __syncthreads();
+    st.grp.sync();
     // Zo[r1 + 8 r2][k] = IFFT_16 over q of V[q], V[q] = Y[q] w^{-q r1} + Y[16+q] w^{-(112+q) r1}
     if (tid < 128) {
         const int r1 = tid >> 4, k = tid & 15;
@@ -970,77 +982,83 @@ __device__ void phase_c(char *base, uint32_t tmem, Barriers *bars, Phases &ph, c
         }
     }
     fence_async_smem();
-    __syncthreads();
+    st.grp.sync();
     constexpr uint32_t idesc = idesc_tf32(128);
+    const uint32_t dinv = st.tmem + kTmemInv;
     if (tid == 0) {
         tc_after_sync();
         const uint32_t ah = smem_addr(ahi), al = smem_addr(alo);
         const uint32_t bh = smem_addr(base + kTi), bl = smem_addr(base + kTi + 16384);
 #pragma unroll
-        for (int st = 0; st < 4; ++st) {
-            const uint32_t o = st * 32;
-            mma_tf32(tmem + 32, desc_sw128(ah + o), desc_sw128(bh + o), idesc, st ? 1u : 0u);
-            mma_tf32(tmem + 32, desc_sw128(ah + o), desc_sw128(bl + o), idesc, 1u);
-            mma_tf32(tmem + 32, desc_sw128(al + o), desc_sw128(bh + o), idesc, 1u);
+        for (int s = 0; s < 4; ++s) {
+            const uint32_t o = s * 32;
+            mma_tf32(dinv, desc_sw128(ah + o), desc_sw128(bh + o), idesc, s ? 1u : 0u);
+            mma_tf32(dinv, desc_sw128(ah + o), desc_sw128(bl + o), idesc, 1u);
+            mma_tf32(dinv, desc_sw128(al + o), desc_sw128(bh + o), idesc, 1u);
         }
-        mma_commit(&bars->inv);
+        mma_commit(&st.bars->inv);
     }
-    const bool ok = mbar_wait(&bars->inv, ph.inv, err);
-    ph.inv++;
+    const bool ok = mbar_wait(&st.bars->inv, ph.inv++, err);
     tc_after_sync();
-    // y rows from tensor memory into the swizzled staging tile
-    {
-        const int warp = tid >> 5, lane = tid & 31;
-        const int row = 32 * (warp & 3) + lane, half = warp >> 2;
+    // y rows: tensor memory -> swizzled staging (two 32-column boxes) -> TMA,
+    // in two halves of 64 columns
+    const int warp = tid >> 5, lane = tid & 31;
+    const int row = 32 * (warp & 3) + lane, sub = warp >> 2;
+    for (int half = 0; half < 2; ++half) {
+        if (half == 1) {
+            if (tid == 0) bulk_wait_read();      // the first half has left the staging tile
+            st.grp.sync();
+        }
 #pragma unroll
-        for (int part16 = 0; part16 < 4; ++part16) {
+        for (int p16 = 0; p16 < 2; ++p16) {
             float v[16];
-            const int col0 = 64 * half + 16 * part16;
-            tmem_ld16(tmem + 32 + ((uint32_t)(32 * (warp & 3)) << 16) + col0, v);
-            const int cc = col0 >> 5;
+            const int col0 = 64 * half + 32 * sub + 16 * p16;   // column of y
+            tmem_ld16(dinv + ((uint32_t)(32 * (warp & 3)) << 16) + col0, v);
+            char *box = stage + sub * kChunkBytes;
 #pragma unroll
             for (int p4 = 0; p4 < 4; ++p4) {
-                const int col = (col0 & 31) + 4 * p4;
-                *reinterpret_cast<float4 *>(stage + cc * kChunkBytes + sw_off(row, col)) =
+                const int col = 16 * p16 + 4 * p4;             // column inside the box
+                *reinterpret_cast<float4 *>(box + sw_off(row, col)) =
                     ok ? make_float4(v[4 * p4], v[4 * p4 + 1], v[4 * p4 + 2], v[4 * p4 + 3])
                        : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
+        fence_async_smem();
+        st.grp.sync();
+        if (tid == 0) {
+            const uint32_t s0 = smem_addr(stage);
+            tma_store_2d(ymap, 64 * half, img * Cf::N0, s0);
+            tma_store_2d(ymap, 64 * half + 32, img * Cf::N0, s0 + kChunkBytes);
+            bulk_commit();
+        }
     }
     tc_before_sync();
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-        const uint32_t s0 = smem_addr(stage);
-        for (int cc = 0; cc < kKChunks; ++cc) tma_store_2d(ymap, 32 * cc, img * Cf::N0, s0 + cc * kChunkBytes);
-        bulk_commit();
-    }
 }
 
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(kStreams * NT, 1)
 k_fused2d_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
              Args a, const float4 *tables) {
     extern __shared__ __align__(1024) char smem_raw[];
     char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
-    __shared__ Barriers bars;
+    __shared__ Barriers bars[kStreams];
     __shared__ uint32_t s_tmem;
-    __shared__ Item s_cur, s_next;
-    __shared__ int s_ok;
-    const int tid = threadIdx.x;
+    __shared__ Item s_cur[kStreams], s_next[kStreams];
+    __shared__ int s_ok[kStreams];
     // twiddle operands (already in their swizzled shared-memory image) and W_128
-    for (int e = tid; e < (int)(kTableBytes / 16); e += NT)
+    for (int e = threadIdx.x; e < (int)(kTableBytes / 16); e += kStreams * NT)
         reinterpret_cast<float4 *>(base + kT)[e] = tables[e];
-    for (int e = tid; e < 128; e += NT) reinterpret_cast<float2 *>(base + kTw)[e] = a.tw0[e];
-    if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars.x[i])));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars.slot[i])));
+    for (int e = threadIdx.x; e < 128; e += kStreams * NT)
+        reinterpret_cast<float2 *>(base + kTw)[e] = a.tw0[e];
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStreams; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[i].x)));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[i].mma)));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[i].inv)));
         }
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars.inv)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (tid < 32) {
+    if (threadIdx.x < 32) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(smem_addr(&s_tmem)), "r"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -1049,31 +1067,29 @@ k_fused2d_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     tc_before_sync();
     __syncthreads();
     tc_after_sync();
-    const uint32_t tmem = s_tmem;
-    Phases ph{{0, 0}, {0, 0}, 0};
+    const int sid = threadIdx.x / NT;
+    Stream st;
+    st.grp = StreamGroup{(int)threadIdx.x % NT, 1 + sid};
+    st.region = base + sid * kStreamBytes;
+    st.tmem = s_tmem + 256 * sid;
+    st.bars = &bars[sid];
+    const int tid = st.grp.tid;
+    Phases ph{0, 0, 0};
     const int nimg_in = a.batch * a.cin;
-    int buf = 0;
-    bool loaded = false;               // the current A item's image is already requested
-    if (tid == 0) s_cur = decode_ticket<Cf>(a, atomicAdd(&a.sync->ticket[0], 1));
-    __syncthreads();
-    Item cur = s_cur;
+    if (tid == 0) s_cur[sid] = decode_ticket<Cf>(a, atomicAdd(&a.sync->ticket[0], 1));
+    st.grp.sync();
+    Item cur = s_cur[sid];
     while (cur.phase >= 0) {
         if (tid == 0) {
-            bulk_wait_read();          // staged output has been read before R is reused
-            const Item nxt = decode_ticket<Cf>(a, atomicAdd(&a.sync->ticket[0], 1));
-            s_next = nxt;
-            if (cur.phase == 0) {
-                if (!loaded) issue_x(&xmap, base, buf, cur.g * a.bg * a.cin + cur.idx, &bars);
-                if (nxt.phase == 0)
-                    issue_x(&xmap, base, buf ^ 1, nxt.g * a.bg * a.cin + nxt.idx, &bars);
-            }
+            bulk_wait_read();          // staged output has been read before the region is reused
+            s_next[sid] = decode_ticket<Cf>(a, atomicAdd(&a.sync->ticket[0], 1));
         }
-        __syncthreads();
-        const Item nxt = s_next;
+        st.grp.sync();
+        const Item nxt = s_next[sid];
         const int nbg = min(a.bg, a.batch - cur.g * a.bg);
         if (cur.phase == 0) {
-            phase_a(base, buf, tmem, &bars, ph, a.part, cur.g * a.bg * a.cin + cur.idx, a.err);
-            __syncthreads();
+            phase_a(st, ph, base, &xmap, a.part, cur.g * a.bg * a.cin + cur.idx, a.err);
+            st.grp.sync();
             if (tid == 0)
                 finish_item(&a.sync->done_a[cur.g][0], nbg * a.cin, a.sync->flag_a[cur.g]);
         } else if (cur.phase == 1) {
@@ -1083,40 +1099,43 @@ k_fused2d_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             bi.nob = min(a.ob, a.cout - bi.o0);
             bi.b0 = cur.g * a.bg;
             bi.nbb = nbg;
-            phase_b_weights<Cf, float, NT>(static_cast<const float *>(a.w), a.cin, a.cout, bi,
-                                           a.ob, base + kR);
+            phase_b_weights<Cf, float, NT>(st.grp, static_cast<const float *>(a.w), a.cin, a.cout,
+                                           bi, a.ob, st.region);
             if (tid == 0)
-                s_ok = wait_flag(&a.sync->flag_a[cur.g][blockIdx.x % kFlagCopies][0], a.err);
-            __syncthreads();
-            if (s_ok) phase_b<Cf, float, NT>(a.part, a.Y, a.cin, a.cout, nimg_in, bi, a.ob, base + kR);
-            else cp_async_wait_all();
-            __syncthreads();
+                s_ok[sid] = wait_flag(&a.sync->flag_a[cur.g][(2 * blockIdx.x + sid) % kFlagCopies][0],
+                                      a.err);
+            st.grp.sync();
+            if (s_ok[sid])
+                phase_b<Cf, float, NT>(st.grp, a.part, a.Y, a.cin, a.cout, nimg_in, bi, a.ob,
+                                       st.region);
+            else
+                cp_async_wait_all();
+            st.grp.sync();
             if (tid == 0)
                 finish_item(&a.sync->done_b[cur.g][0], a.npairs * a.nob, a.sync->flag_b[cur.g]);
         } else {
             if (tid == 0)
-                s_ok = wait_flag(&a.sync->flag_b[cur.g][blockIdx.x % kFlagCopies][0], a.err);
-            __syncthreads();
-            if (s_ok)
-                phase_c(base, tmem, &bars, ph, a.Y, &ymap, cur.g * a.bg * a.cout + cur.idx, a.err);
+                s_ok[sid] = wait_flag(&a.sync->flag_b[cur.g][(2 * blockIdx.x + sid) % kFlagCopies][0],
+                                      a.err);
+            st.grp.sync();
+            if (s_ok[sid])
+                phase_c(st, ph, base, a.Y, &ymap, cur.g * a.bg * a.cout + cur.idx, a.err);
         }
-        const bool prefetched = cur.phase == 0 && nxt.phase == 0;
-        if (cur.phase == 0 && prefetched) buf ^= 1;
-        loaded = prefetched;
         cur = nxt;
-        fence_async_smem();            // generic writes to R precede any later TMA into it
-        __syncthreads();
+        fence_async_smem();            // generic writes precede any later TMA into the region
+        st.grp.sync();
     }
     if (tid == 0) bulk_wait_all();
     tc_before_sync();
     __syncthreads();
     tc_after_sync();
-    if (tid < 32)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    if (threadIdx.x < 32)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(s_tmem), "r"(kTmemCols));
+    // the last stream to leave resets the counters and flags for the next launch
     if (tid == 0) {
         __threadfence();
         const int prev = atomicAdd(&a.sync->exited[0], 1);
-        if (prev == (int)gridDim.x - 1) {
+        if (prev == kStreams * (int)gridDim.x - 1) {
             a.sync->ticket[0] = 0;
             for (int g = 0; g < a.ng; ++g) {
                 a.sync->done_a[g][0] = 0;
@@ -1255,8 +1274,8 @@ bool encode_rows(CUtensorMap *map, const void *ptr, int64_t rows) {
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr size_t kTcWsBudget = 64u << 10;
-constexpr size_t kTcXpBudget = 48u << 10;
+constexpr size_t kTcWsBudget = 32u << 10;
+constexpr size_t kTcXpBudget = 32u << 10;
 
 BShape b_shape_tc(int64_t batch, int cin, int cout) {
     BShape s;
@@ -1308,8 +1327,8 @@ cudaError_t fused_plan_init(Plan &p) {
                                              (int)tc::kSmemBytes);
         if (e != cudaSuccess) return e;
         int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc::k_fused2d_tc, tc::NT,
-                                                           tc::kSmemBytes);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc::k_fused2d_tc,
+                                                           tc::kStreams * tc::NT, tc::kSmemBytes);
         if (e != cudaSuccess) return e;
         if (per_sm < 1) return cudaErrorInvalidConfiguration;
         // one CTA per SM: each holds kTmemCols columns of tensor memory
@@ -1375,8 +1394,9 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
         a.ob = p.fused_ob;
         a.nob = (p.cout + a.ob - 1) / a.ob;
         const int total = (int)p.batch * (p.cin + p.cout) + a.ng * a.npairs * a.nob;
-        const int grid = p.fused_grid < total ? p.fused_grid : total;
-        tc::k_fused2d_tc<<<grid, tc::NT, p.fused_smem, s>>>(
+        const int grid = p.fused_grid;
+        (void)total;
+        tc::k_fused2d_tc<<<grid, tc::kStreams * tc::NT, p.fused_smem, s>>>(
             xmap, ymap, a, static_cast<const float4 *>(p.fused_tables));
         return cudaGetLastError();
     }
