@@ -28,6 +28,7 @@ FNO_F16 = 1
 
 FNO_PLAN_DEFAULT = 0
 FNO_PLAN_UNFUSED = 1
+FNO_PLAN_TRACE = 2
 
 # Every symbol include/fno.h declares.
 EXPORTS = (
@@ -35,7 +36,7 @@ EXPORTS = (
     "fno_spectral_conv_query", "fno_spectral_conv_plan",
     "fno_spectral_conv_workspace_size", "fno_spectral_conv_kernel_count",
     "fno_spectral_conv_forward", "fno_plan_get_device_error", "fno_plan_destroy",
-    "fno_spectral_conv_forward_static",
+    "fno_spectral_conv_forward_static", "fno_plan_get_trace",
     "fno_model_plan", "fno_model_workspace_size", "fno_model_kernel_count",
     "fno_forward", "fno_model_get_device_error", "fno_model_destroy",
 )
@@ -51,6 +52,12 @@ class fno_model_desc_t(ctypes.Structure):
                 ("h", ctypes.c_int64), ("w", ctypes.c_int64),
                 ("modes", ctypes.c_int32 * 2), ("dtype", ctypes.c_int),
                 ("flags", ctypes.c_uint32)]
+
+
+class fno_trace_record_t(ctypes.Structure):
+    _fields_ = [("item", ctypes.c_uint32), ("worker", ctypes.c_uint32),
+                ("t_start", ctypes.c_uint64), ("t_ready", ctypes.c_uint64),
+                ("t_compute", ctypes.c_uint64), ("t_end", ctypes.c_uint64)]
 
 
 class fno_model_params_t(ctypes.Structure):
@@ -95,6 +102,8 @@ def lib() -> ctypes.CDLL:
             L.fno_spectral_conv_forward_static.argtypes = [
                 ctypes.c_int, pi64, pi32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _st,
                 _vp, _vp, _vp, _vp]
+            L.fno_plan_get_trace.argtypes = [_vp, ctypes.POINTER(fno_trace_record_t),
+                                             ctypes.c_size_t, psz]
             L.fno_plan_get_device_error.argtypes = [_vp, _vp]
             L.fno_plan_destroy.argtypes = [_vp]
             L.fno_model_plan.argtypes = [ctypes.POINTER(_vp), ctypes.POINTER(fno_model_desc_t)]
@@ -158,6 +167,20 @@ def fno_spectral_conv_forward_static(ndim, n, modes, batch, cin, cout, dtype, x_
     return lib().fno_spectral_conv_forward_static(
         int(ndim), _arr(ctypes.c_int64, n), _arr(ctypes.c_int32, modes), int(batch), int(cin),
         int(cout), int(dtype), x_ptr, w_ptr, y_ptr, stream)
+
+
+def fno_plan_get_trace(plan, capacity=1 << 16):
+    """Returns (status, list of (phase, group, index, worker, t_start, t_ready,
+    t_compute, t_end))."""
+    buf = (fno_trace_record_t * max(1, capacity))()
+    n = ctypes.c_size_t(0)
+    st = lib().fno_plan_get_trace(plan, buf, capacity, ctypes.byref(n))
+    recs = []
+    if st == FNO_OK:
+        for r in buf[:min(n.value, capacity)]:
+            recs.append((r.item >> 24, (r.item >> 16) & 0xFF, r.item & 0xFFFF, r.worker,
+                         r.t_start, r.t_ready, r.t_compute, r.t_end))
+    return st, recs
 
 
 def fno_plan_get_device_error(plan, stream):

@@ -84,7 +84,7 @@ fno_status_t describe(int ndim, const int64_t *n, const int32_t *modes, int64_t 
     if (st != FNO_OK) return st;
     if (batch < 1 || cin < 1 || cout < 1) return FNO_ERR_INVALID_ARG;
     if (dtype != FNO_F32 && dtype != FNO_F16) return FNO_ERR_INVALID_ARG;
-    if (flags & ~FNO_PLAN_UNFUSED) return FNO_ERR_INVALID_ARG;
+    if (flags & ~(FNO_PLAN_UNFUSED | FNO_PLAN_TRACE)) return FNO_ERR_INVALID_ARG;
     // int64 element counts must not overflow and a tensor must stay addressable
     const double xe = (double)batch * cin * g->npix, ye = (double)batch * cout * g->npix;
     if (xe > 4.0e12 || ye > 4.0e12) return FNO_ERR_UNSUPPORTED;
@@ -245,6 +245,23 @@ fno_status_t fno_spectral_conv_forward(fno_plan_t plan, const void *x, const voi
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = p.path == kPathUnfused ? unfused_forward(p, b, s) : fused_forward(p, b, s);
     if (e != cudaSuccess) {
+        cudaGetLastError();
+        return FNO_ERR_CUDA;
+    }
+    return FNO_OK;
+}
+
+fno_status_t fno_plan_get_trace(fno_plan_t plan, fno_trace_record_t *records, size_t capacity,
+                                size_t *count) {
+    if (!plan || !count) return FNO_ERR_INVALID_ARG;
+    const Plan &p = *reinterpret_cast<Plan *>(plan);
+    if (!p.trace) return FNO_ERR_INVALID_ARG;
+    *count = p.trace_records;
+    const size_t n = capacity < p.trace_records ? capacity : p.trace_records;
+    if (n && !records) return FNO_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        (n && cudaMemcpy(records, p.trace, n * sizeof(fno_trace_record_t),
+                         cudaMemcpyDeviceToHost) != cudaSuccess)) {
         cudaGetLastError();
         return FNO_ERR_CUDA;
     }

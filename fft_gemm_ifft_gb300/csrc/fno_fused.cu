@@ -586,6 +586,7 @@ struct Args {
     const float2 *tw0;  // N0 twiddles
     const float2 *tw1;  // N1 twiddles
     int *err;
+    fno_trace_record_t *trace;   // nullptr unless FNO_PLAN_TRACE
     int batch, cin, cout;
     int bg, ng;         // batch rows per group, groups
     int npairs;         // phase B: kept-mode pairs
@@ -598,30 +599,56 @@ struct Args {
 struct Item {
     int phase;          // 0: A, 1: B, 2: C, -1: none left
     int g, idx;
+    int ticket;
 };
 
 template <class Cf>
 __device__ Item decode_ticket(const Args &a, int t) {
+    const int t0 = t;
     for (int st = 0; st < a.ng + 2; ++st) {
         if (st < a.ng) {
             const int n = min(a.bg, a.batch - st * a.bg) * a.cin * Cf::C;
-            if (t < n) return Item{0, st, t};
+            if (t < n) return Item{0, st, t, t0};
             t -= n;
         }
         if (st >= 1 && st - 1 < a.ng) {
             const int n = a.npairs * a.nob;
-            if (t < n) return Item{1, st - 1, t};
+            if (t < n) return Item{1, st - 1, t, t0};
             t -= n;
         }
         if (st >= 2) {
             const int g = st - 2;
             const int n = min(a.bg, a.batch - g * a.bg) * a.cout * Cf::C;
-            if (t < n) return Item{2, g, t};
+            if (t < n) return Item{2, g, t, t0};
             t -= n;
         }
     }
-    return Item{-1, 0, 0};
+    return Item{-1, 0, 0, t0};
 }
+
+__device__ __forceinline__ unsigned long long trace_now() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Trace stamps of one item, written by the thread that runs its serial part.
+struct TraceStamp {
+    unsigned long long t_start = 0, t_ready = 0, t_compute = 0;
+    __device__ void start(const Args &a) { if (a.trace) t_start = trace_now(); }
+    __device__ void ready(const Args &a) { if (a.trace) t_ready = trace_now(); }
+    __device__ void computed(const Args &a) { if (a.trace) t_compute = trace_now(); }
+    __device__ void end(const Args &a, const Item &it, unsigned worker) const {
+        if (!a.trace) return;
+        fno_trace_record_t r;
+        r.item = ((unsigned)it.phase << 24) | ((unsigned)it.g << 16) | (unsigned)it.idx;
+        r.worker = worker;
+        r.t_start = t_start;
+        r.t_ready = t_ready ? t_ready : t_start;
+        r.t_compute = t_compute ? t_compute : r.t_ready;
+        r.t_end = trace_now();
+        a.trace[it.ticket] = r;
+    }
+};
 
 template <class Cf, typename T>
 __global__ void __launch_bounds__(kNT)
@@ -647,6 +674,8 @@ k_fused2d(Args a) {
         __syncthreads();
         if (it.phase < 0) break;
         const int nbg = min(a.bg, a.batch - it.g * a.bg);     // batch rows of the group
+        TraceStamp ts;
+        if (tid == 0) ts.start(a);
         if (it.phase == 0) {
             const int img = it.g * a.bg * a.cin + it.idx / Cf::C;
             phase_a<Cf, T>(static_cast<const T *>(a.x), a.part, nimg_in, img, it.idx % Cf::C,
@@ -666,6 +695,7 @@ k_fused2d(Args a) {
                                         a.ob, work);
             if (tid == 0)
                 s_ok = wait_flag(&a.sync->flag_a[it.g][blockIdx.x % kFlagCopies][0], a.err);
+            if (tid == 0) ts.ready(a);
             __syncthreads();
             if (s_ok) phase_b<Cf, T, kNT>(CtaGroup{tid}, a.part, a.Y, a.cin, a.cout, nimg_in, bi, a.ob, work);
             else cp_async_wait_all();
@@ -675,6 +705,7 @@ k_fused2d(Args a) {
         } else {
             if (tid == 0)
                 s_ok = wait_flag(&a.sync->flag_b[it.g][blockIdx.x % kFlagCopies][0], a.err);
+            if (tid == 0) ts.ready(a);
             __syncthreads();
             if (s_ok) {
                 const int img = it.g * a.bg * a.cout + it.idx / Cf::C;
@@ -682,6 +713,7 @@ k_fused2d(Args a) {
             }
         }
         __syncthreads();
+        if (tid == 0) ts.end(a, it, blockIdx.x);
     }
     // the last CTA to leave resets the counters and flags for the next launch
     if (tid == 0) {
@@ -858,7 +890,7 @@ struct Stream {
 
 // Phase A: the x tile of image `img` -> its 512 kept modes.
 __device__ void phase_a(const Stream &st, Phases &ph, const char *base, const CUtensorMap *xmap,
-                        float2 *part, int img, int *err) {
+                        float2 *part, int img, int *err, const Args &a, TraceStamp &ts) {
     const int tid = st.grp.tid;
     char *xh = st.region;
     char *xl = st.region + kXL;
@@ -871,6 +903,7 @@ __device__ void phase_a(const Stream &st, Phases &ph, const char *base, const CU
             tma_load_2d(dst + kc * kChunkBytes, xmap, 32 * kc, img * Cf::N0, &st.bars->x);
     }
     bool ok = mbar_wait(&st.bars->x, ph.x++, err);
+    if (tid == 0) ts.ready(a);
     constexpr uint32_t idesc = idesc_tf32(32);
     for (int kc = 0; kc < kKChunks; ++kc) {
         if (kc > 0) ok &= mbar_wait(&st.bars->mma, ph.mma++, err);   // lo slot free again
@@ -900,6 +933,7 @@ __device__ void phase_a(const Stream &st, Phases &ph, const char *base, const CU
         }
     }
     ok &= mbar_wait(&st.bars->mma, ph.mma++, err);   // the last chunk: every MMA is done
+    if (tid == 0) ts.computed(a);
     tc_after_sync();
     // Z (128 rows x 16 bins) from tensor memory into the now free x tile
     float *zr = reinterpret_cast<float *>(xh + kZr);
@@ -948,7 +982,7 @@ __device__ void phase_a(const Stream &st, Phases &ph, const char *base, const CU
 
 // Phase C: the mixed modes of output image `img` -> its 128 rows.
 __device__ void phase_c(const Stream &st, Phases &ph, const char *base, const float2 *Y,
-                        const CUtensorMap *ymap, int img, int *err) {
+                        const CUtensorMap *ymap, int img, int *err, const Args &a, TraceStamp &ts) {
     const int tid = st.grp.tid;
     float2 *ys = reinterpret_cast<float2 *>(st.region + kCY);
     char *ahi = st.region + kCAhi, *alo = st.region + kCAlo, *stage = st.region + kCStage;
@@ -958,6 +992,7 @@ __device__ void phase_c(const Stream &st, Phases &ph, const char *base, const fl
     cp_async_commit();
     cp_async_wait_all();
     st.grp.sync();
+    if (tid == 0) ts.ready(a);
     // Zo[r1 + 8 r2][k] = IFFT_16 over q of V[q], V[q] = Y[q] w^{-q r1} + Y[16+q] w^{-(112+q) r1}
     if (tid < 128) {
         const int r1 = tid >> 4, k = tid & 15;
@@ -999,6 +1034,7 @@ __device__ void phase_c(const Stream &st, Phases &ph, const char *base, const fl
         mma_commit(&st.bars->inv);
     }
     const bool ok = mbar_wait(&st.bars->inv, ph.inv++, err);
+    if (tid == 0) ts.computed(a);
     tc_after_sync();
     // y rows: tensor memory -> swizzled staging (two 32-column boxes) -> TMA,
     // in two halves of 64 columns
@@ -1087,8 +1123,10 @@ k_fused2d_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         st.grp.sync();
         const Item nxt = s_next[sid];
         const int nbg = min(a.bg, a.batch - cur.g * a.bg);
+        TraceStamp ts;
+        if (tid == 0) ts.start(a);
         if (cur.phase == 0) {
-            phase_a(st, ph, base, &xmap, a.part, cur.g * a.bg * a.cin + cur.idx, a.err);
+            phase_a(st, ph, base, &xmap, a.part, cur.g * a.bg * a.cin + cur.idx, a.err, a, ts);
             st.grp.sync();
             if (tid == 0)
                 finish_item(&a.sync->done_a[cur.g][0], nbg * a.cin, a.sync->flag_a[cur.g]);
@@ -1104,6 +1142,7 @@ k_fused2d_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             if (tid == 0)
                 s_ok[sid] = wait_flag(&a.sync->flag_a[cur.g][(2 * blockIdx.x + sid) % kFlagCopies][0],
                                       a.err);
+            if (tid == 0) ts.ready(a);
             st.grp.sync();
             if (s_ok[sid])
                 phase_b<Cf, float, NT>(st.grp, a.part, a.Y, a.cin, a.cout, nimg_in, bi, a.ob,
@@ -1111,6 +1150,7 @@ k_fused2d_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             else
                 cp_async_wait_all();
             st.grp.sync();
+            if (tid == 0) ts.computed(a);
             if (tid == 0)
                 finish_item(&a.sync->done_b[cur.g][0], a.npairs * a.nob, a.sync->flag_b[cur.g]);
         } else {
@@ -1119,8 +1159,9 @@ k_fused2d_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                                       a.err);
             st.grp.sync();
             if (s_ok[sid])
-                phase_c(st, ph, base, a.Y, &ymap, cur.g * a.bg * a.cout + cur.idx, a.err);
+                phase_c(st, ph, base, a.Y, &ymap, cur.g * a.bg * a.cout + cur.idx, a.err, a, ts);
         }
+        if (tid == 0) ts.end(a, cur, 2 * blockIdx.x + sid);
         cur = nxt;
         fence_async_smem();            // generic writes precede any later TMA into the region
         st.grp.sync();
@@ -1344,6 +1385,13 @@ cudaError_t fused_plan_init(Plan &p) {
             e = cudaMemcpy(p.fused_tables, host, tc::kTableBytes, cudaMemcpyHostToDevice);
         delete[] host;
         if (e != cudaSuccess) return e;
+        if (p.flags & FNO_PLAN_TRACE) {
+            const int ng = (int)((p.batch + bs.bg - 1) / bs.bg);
+            p.trace_records = (size_t)p.batch * (p.cin + p.cout) +
+                              (size_t)ng * (p.g.nkept / kG) * ((p.cout + bs.ob - 1) / bs.ob);
+            e = cudaMalloc(&p.trace, p.trace_records * sizeof(fno_trace_record_t));
+            if (e != cudaSuccess) return e;
+        }
         return cudaMemset(p.sync, 0, kSyncBytes);
     }
     const BShape bs = b_shape(p.dtype, p.batch, p.cin, p.cout);
@@ -1360,12 +1408,21 @@ cudaError_t fused_plan_init(Plan &p) {
     p.fused_smem = smem;
     p.fused_ob = bs.ob;
     p.fused_bb = bs.bg;
+    if (p.flags & FNO_PLAN_TRACE) {
+        const int ng = (int)((p.batch + bs.bg - 1) / bs.bg);
+        p.trace_records = (size_t)p.batch * (p.cin + p.cout) * Cfg128::C +
+                          (size_t)ng * (p.g.nkept / kG) * ((p.cout + bs.ob - 1) / bs.ob);
+        e = cudaMalloc(&p.trace, p.trace_records * sizeof(fno_trace_record_t));
+        if (e != cudaSuccess) return e;
+    }
     return cudaMemset(p.sync, 0, kSyncBytes);
 }
 
 void fused_plan_release(Plan &p) {
     if (p.fused_tables) cudaFree(p.fused_tables);
+    if (p.trace) cudaFree(p.trace);
     p.fused_tables = nullptr;
+    p.trace = nullptr;
 }
 
 cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
@@ -1385,6 +1442,7 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
         a.tw0 = p.tw[0];
         a.tw1 = p.tw[1];
         a.err = p.dev_err;
+        a.trace = p.trace;
         a.batch = (int)p.batch;
         a.cin = p.cin;
         a.cout = p.cout;
@@ -1411,6 +1469,7 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
     a.tw0 = p.tw[0];
     a.tw1 = p.tw[1];
     a.err = p.dev_err;
+    a.trace = p.trace;
     a.batch = (int)p.batch;
     a.cin = p.cin;
     a.cout = p.cout;

@@ -53,6 +53,8 @@ struct Plan {
     int fused_ob;
     int fused_bb;
     void *fused_tables;           // tensor-core path: twiddle operands (plan-owned)
+    fno_trace_record_t *trace;    // FNO_PLAN_TRACE: one record per work item (plan-owned)
+    size_t trace_records;         // records one forward call produces
 };
 
 enum { kPathUnfused = 0, kPathFused2D = 1, kPathFused1D = 2 };

@@ -76,6 +76,21 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * ablation of the article's §5.2 note).  Results agree with the fused path
  * within rounding.                                                           */
 #define FNO_PLAN_UNFUSED 1u
+/* Record a timeline of the fused kernel's work items (read back with
+ * fno_plan_get_trace).  Costs a few timer reads and stores per item.        */
+#define FNO_PLAN_TRACE 2u
+
+/* One work item of the fused kernel, as recorded under FNO_PLAN_TRACE.
+ * Times are the GPU's global nanosecond timer.                              */
+typedef struct fno_trace_record_s {
+    uint32_t item;      /* phase << 24 | batch group << 16 | index in the phase-group
+                           (phase 0: forward transform, 1: mixing, 2: inverse)   */
+    uint32_t worker;    /* which CTA / stream ran it                              */
+    uint64_t t_start;   /* processing began                                       */
+    uint64_t t_ready;   /* its inputs were available (loads landed, waits over)   */
+    uint64_t t_compute; /* its arithmetic was done                                */
+    uint64_t t_end;     /* its outputs were issued and the item counted done      */
+} fno_trace_record_t;
 
 /* Human-readable name of a status code; never NULL. */
 const char *fno_status_string(fno_status_t status);
@@ -168,6 +183,14 @@ fno_status_t fno_spectral_conv_forward_static(int ndim, const int64_t *n,
                                               int32_t cin, int32_t cout, fno_dtype_t dtype,
                                               const void *x, const void *w, void *y,
                                               fno_stream_t stream);
+
+/* Copy the trace of the plan's last forward call (FNO_PLAN_TRACE) to host
+ * memory: up to `capacity` records, ordered by ticket; *count receives the
+ * number of records the call produced.  Synchronises the device.  Returns
+ * FNO_ERR_INVALID_ARG if the plan was made without FNO_PLAN_TRACE or does not
+ * run the fused kernel.                                                     */
+fno_status_t fno_plan_get_trace(fno_plan_t plan, fno_trace_record_t *records, size_t capacity,
+                                size_t *count);
 
 /* Synchronise `stream`, then read and clear the plan's device error word.
  * Returns FNO_OK, FNO_ERR_DEVICE_TIMEOUT, FNO_ERR_DEVICE_BOUNDS or CUDA.   */

@@ -179,3 +179,24 @@ def test_plan_create_destroy_many_times_no_leak():
     torch.cuda.synchronize()
     free1, _ = torch.cuda.mem_get_info()
     assert free0 - free1 < 8 << 20
+
+
+def test_trace_records_every_item():
+    case = workloads.CASES["2d_f32"]
+    conv = SpectralConv(case.n, case.modes, case.batch, case.cin, case.cout, case.dtype,
+                        capi.FNO_PLAN_TRACE)
+    x, w = workloads.make_x(case), workloads.make_w(case)
+    y = conv(to_dev(x), to_dev(w))
+    torch.cuda.synchronize()
+    st, recs = capi.fno_plan_get_trace(conv.handle)
+    assert st == capi.FNO_OK
+    phases = [r[0] for r in recs]
+    assert phases.count(0) == case.batch * case.cin and phases.count(2) == case.batch * case.cout
+    assert phases.count(1) > 0
+    for r in recs:
+        assert r[4] <= r[5] <= r[6] <= r[7], r
+    # tracing does not change the result
+    assert_close(y.cpu().numpy(), run_oracle(case, x, w), "f32", "traced forward")
+    st, _ = capi.fno_plan_get_trace(SpectralConv((16,), (4,), 1, 1, 1).handle)
+    assert st == capi.FNO_ERR_INVALID_ARG
+    conv.close()
