@@ -749,8 +749,8 @@ k_fused2d(Args a) {
 // DFT over the 128 rows is split 8 x 16 (16-point register FFTs + twiddled
 // sums) on the SIMT cores, and the 512 kept modes go to the workspace.
 // Phase C: the column inverse (16-point register FFTs) builds the operand
-// Zo = [Re | Im] (128 x 32) and the row inverse y = Zo Tinv^T (Tinv folds the
-// half-spectrum weights c(k) and the 1/(N0 N1) scale) is one more tcgen05
+// Zo = [Re | Im] (128 x 32, carrying the half-spectrum weights c(k) and the
+// 1/(N0 N1) scale) and the row inverse y = Zo Tinv^T is one more tcgen05
 // chain with N = 128; tensor memory is staged through swizzled shared memory
 // and written by TMA.  Phase B is the SIMT mixing shared with the other kernel.
 // ---------------------------------------------------------------------------
@@ -905,34 +905,49 @@ __device__ void phase_a(const Stream &st, Phases &ph, const char *base, const CU
     bool ok = mbar_wait(&st.bars->x, ph.x++, err);
     if (tid == 0) ts.ready(a);
     constexpr uint32_t idesc = idesc_tf32(32);
-    for (int kc = 0; kc < kKChunks; ++kc) {
-        if (kc > 0) ok &= mbar_wait(&st.bars->mma, ph.mma++, err);   // lo slot free again
-        // lo parts of chunk kc (elementwise, so the swizzled layout carries over)
-        const float4 *src = reinterpret_cast<const float4 *>(xh + kc * kChunkBytes);
-        float4 *dst = reinterpret_cast<float4 *>(xl);
+    const uint32_t ax = smem_addr(xh);
+    // 1. the two passes that read x at tf32 precision, for the whole image
+    if (tid == 0) {
+        tc_after_sync();
 #pragma unroll
-        for (int r = 0; r < (int)(kChunkBytes / 16) / NT; ++r) {
-            const float4 v = src[tid + r * NT];
-            dst[tid + r * NT] = make_float4(tf32_lo(v.x), tf32_lo(v.y), tf32_lo(v.z), tf32_lo(v.w));
-        }
-        fence_async_smem();
-        st.grp.sync();
-        if (tid == 0) {
-            tc_after_sync();
-            const uint32_t ah = smem_addr(xh + kc * kChunkBytes), al = smem_addr(xl);
+        for (int kc = 0; kc < kKChunks; ++kc) {
             const uint32_t bh = smem_addr(base + kT + kc * 4096);
             const uint32_t bl = smem_addr(base + kT + 16384 + kc * 4096);
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                const uint32_t o = s * 32;
-                mma_tf32(st.tmem, desc_sw128(ah + o), desc_sw128(bh + o), idesc, (kc | s) ? 1u : 0u);
-                mma_tf32(st.tmem, desc_sw128(ah + o), desc_sw128(bl + o), idesc, 1u);
-                mma_tf32(st.tmem, desc_sw128(al + o), desc_sw128(bh + o), idesc, 1u);
+                const uint32_t ao = ax + kc * kChunkBytes + s * 32, bo = s * 32;
+                mma_tf32(st.tmem, desc_sw128(ao), desc_sw128(bh + bo), idesc, (kc | s) ? 1u : 0u);
+                mma_tf32(st.tmem, desc_sw128(ao), desc_sw128(bl + bo), idesc, 1u);
             }
-            mma_commit(&st.bars->mma);
+        }
+        mma_commit(&st.bars->mma);
+    }
+    ok &= mbar_wait(&st.bars->mma, ph.mma++, err);
+    // 2. x's lo parts, in place (elementwise: the swizzled layout carries over)
+    {
+        float4 *xv = reinterpret_cast<float4 *>(xh);
+#pragma unroll
+        for (int r = 0; r < (int)(kImageBytes / 16) / NT; ++r) {
+            const float4 v = xv[tid + r * NT];
+            xv[tid + r * NT] = make_float4(tf32_lo(v.x), tf32_lo(v.y), tf32_lo(v.z), tf32_lo(v.w));
         }
     }
-    ok &= mbar_wait(&st.bars->mma, ph.mma++, err);   // the last chunk: every MMA is done
+    fence_async_smem();
+    st.grp.sync();
+    // 3. the pass with x's lo parts
+    if (tid == 0) {
+        tc_after_sync();
+#pragma unroll
+        for (int kc = 0; kc < kKChunks; ++kc) {
+            const uint32_t bh = smem_addr(base + kT + kc * 4096);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_tf32(st.tmem, desc_sw128(ax + kc * kChunkBytes + s * 32), desc_sw128(bh + s * 32),
+                         idesc, 1u);
+        }
+        mma_commit(&st.bars->mma);
+    }
+    ok &= mbar_wait(&st.bars->mma, ph.mma++, err);
     if (tid == 0) ts.computed(a);
     tc_after_sync();
     // Z (128 rows x 16 bins) from tensor memory into the now free x tile
@@ -950,22 +965,22 @@ __device__ void phase_a(const Stream &st, Phases &ph, const char *base, const CU
     }
     tc_before_sync();
     st.grp.sync();
-    // column DFT over the 128 rows, r = r1 + 8 r2: 16-point FFTs over r2, one
-    // (r1, bin) per thread for half the stream, the twiddled sums for all of it
-    if (tid < 128) {
+    // column DFT over the 128 rows, r = r1 + 16 r2: one 8-point FFT over r2
+    // per (r1, bin) and thread
+    {
         const int r1 = tid >> 4, k = tid & 15;
-        float2 z[16];
+        float2 z[8];
 #pragma unroll
-        for (int r2 = 0; r2 < 16; ++r2) {
-            const int r = r1 + 8 * r2;
+        for (int r2 = 0; r2 < 8; ++r2) {
+            const int r = r1 + 16 * r2;
             z[r2] = make_float2(zr[r * kZS + k], zi[r * kZS + k]);
         }
-        fft::fft_dif<16, -1>(z);
+        fft::fft_dif<8, -1>(z);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) S[(r1 * 16 + q) * 16 + k] = z[fft::bitrev(q, 4)];
+        for (int q = 0; q < 8; ++q) S[(r1 * 8 + q) * 16 + k] = z[fft::bitrev(q, 3)];
     }
     st.grp.sync();
-    // X[j][k] = sum_r1 W_128^{f r1} S[r1][f mod 16][k]
+    // X[j][k] = sum_r1 W_128^{f r1} S[r1][f mod 8][k]
     float2 *dst = part + (size_t)img * Cf::NK;
 #pragma unroll
     for (int rep = 0; rep < Cf::NK / NT; ++rep) {
@@ -974,7 +989,7 @@ __device__ void phase_a(const Stream &st, Phases &ph, const char *base, const CU
         const int f = kept_freq<Cf>(j);
         float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int r1 = 0; r1 < 8; ++r1) cmac(acc, S[(r1 * 16 + (f & 15)) * 16 + k], tw[(f * r1) & 127]);
+        for (int r1 = 0; r1 < 16; ++r1) cmac(acc, S[(r1 * 8 + (f & 7)) * 16 + k], tw[(f * r1) & 127]);
         __stcg(dst + o, acc);
     }
     fence_async_smem();      // these generic writes precede the next TMA into this tile
@@ -993,23 +1008,30 @@ __device__ void phase_c(const Stream &st, Phases &ph, const char *base, const fl
     cp_async_wait_all();
     st.grp.sync();
     if (tid == 0) ts.ready(a);
-    // Zo[r1 + 8 r2][k] = IFFT_16 over q of V[q], V[q] = Y[q] w^{-q r1} + Y[16+q] w^{-(112+q) r1}
-    if (tid < 128) {
+    // Zo[r1 + 16 r2][k] = IFFT_8 over q of V[q], V[q] = sum of Y[j] w^{-f(j) r1} over the
+    // four kept rows j with f(j) = q mod 8 (j = q, q+8, q+16, q+24); the operand
+    // row carries the half-spectrum weight c(k) and the 1/(N0 N1) scale
+    {
         const int r1 = tid >> 4, k = tid & 15;
-        float2 v[16];
+        const float ck = (k == 0 ? 1.f : 2.f) * (1.f / 16384.f);
+        float2 v[8];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-            float2 a = cmulc(ys[q * 16 + k], tw[(q * r1) & 127]);
-            const float2 b = cmulc(ys[(16 + q) * 16 + k], tw[((112 + q) * r1) & 127]);
-            a.x += b.x;
-            a.y += b.y;
-            v[q] = a;
+        for (int q = 0; q < 8; ++q) {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = q + 8 * u, f = kept_freq<Cf>(j);
+                const float2 t = cmulc(ys[j * 16 + k], tw[(f * r1) & 127]);
+                acc.x += t.x;
+                acc.y += t.y;
+            }
+            v[q] = make_float2(acc.x * ck, acc.y * ck);
         }
-        fft::fft_dif<16, 1>(v);
+        fft::fft_dif<8, 1>(v);
 #pragma unroll
-        for (int r2 = 0; r2 < 16; ++r2) {
-            const int row = r1 + 8 * r2;
-            const float2 z = v[fft::bitrev(r2, 4)];
+        for (int r2 = 0; r2 < 8; ++r2) {
+            const int row = r1 + 16 * r2;
+            const float2 z = v[fft::bitrev(r2, 3)];
             *reinterpret_cast<float *>(ahi + sw_off(row, k)) = z.x;
             *reinterpret_cast<float *>(ahi + sw_off(row, 16 + k)) = z.y;
             *reinterpret_cast<float *>(alo + sw_off(row, k)) = tf32_lo(z.x);
@@ -1081,9 +1103,9 @@ k_fused2d_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     __shared__ uint32_t s_tmem;
     __shared__ Item s_cur[kStreams], s_next[kStreams];
     __shared__ int s_ok[kStreams];
-    // twiddle operands (already in their swizzled shared-memory image) and W_128
-    for (int e = threadIdx.x; e < (int)(kTableBytes / 16); e += kStreams * NT)
-        reinterpret_cast<float4 *>(base + kT)[e] = tables[e];
+    __shared__ __align__(8) uint64_t bar_tab;
+    // W_128, then the twiddle operands (already in their swizzled shared-memory
+    // image) in one bulk copy
     for (int e = threadIdx.x; e < 128; e += kStreams * NT)
         reinterpret_cast<float2 *>(base + kTw)[e] = a.tw0[e];
     if (threadIdx.x == 0) {
@@ -1092,7 +1114,13 @@ k_fused2d_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[i].mma)));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[i].inv)));
         }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar_tab)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     ::"r"(smem_addr(&bar_tab)), "r"(kTableBytes) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(smem_addr(base + kT)), "l"(tables), "r"(kTableBytes), "r"(smem_addr(&bar_tab))
+                     : "memory");
     }
     if (threadIdx.x < 32) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -1103,6 +1131,7 @@ k_fused2d_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     tc_before_sync();
     __syncthreads();
     tc_after_sync();
+    mbar_wait(&bar_tab, 0, a.err);
     const int sid = threadIdx.x / NT;
     Stream st;
     st.grp = StreamGroup{(int)threadIdx.x % NT, 1 + sid};
@@ -1212,12 +1241,11 @@ void make_tables(float *img) {
             put(chunk, k, n % 32, std::cos(a));
             put(chunk, 16 + k, n % 32, -std::sin(a));
         }
-    const double scale = 1.0 / (128.0 * 128.0);
     for (int n = 0; n < 128; ++n)
         for (int k = 0; k < 16; ++k) {
-            const double a = two_pi * k * n / 128.0, c = k == 0 ? 1.0 : 2.0;
-            put(32768, n, k, c * scale * std::cos(a));
-            put(32768, n, 16 + k, -c * scale * std::sin(a));
+            const double a = two_pi * k * n / 128.0;
+            put(32768, n, k, std::cos(a));
+            put(32768, n, 16 + k, -std::sin(a));
         }
 }
 
