@@ -29,6 +29,7 @@ FNO_F16 = 1
 FNO_PLAN_DEFAULT = 0
 FNO_PLAN_UNFUSED = 1
 FNO_PLAN_TRACE = 2
+FNO_PLAN_TENSOR_CORES = 4
 
 # Every symbol include/fno.h declares.
 EXPORTS = (

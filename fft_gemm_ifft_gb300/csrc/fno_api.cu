@@ -68,7 +68,7 @@ size_t elem_bytes(fno_dtype_t t) { return t == FNO_F16 ? 2 : 4; }
 int choose_path(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout,
                 uint32_t flags) {
     if (flags & FNO_PLAN_UNFUSED) return kPathUnfused;
-    if (fused_supported(g, dtype, batch, cin, cout)) return kPathFused2D;
+    if (fused_supported(g, dtype, batch, cin, cout, flags)) return kPathFused2D;
     return kPathUnfused;
 }
 
@@ -84,7 +84,8 @@ fno_status_t describe(int ndim, const int64_t *n, const int32_t *modes, int64_t 
     if (st != FNO_OK) return st;
     if (batch < 1 || cin < 1 || cout < 1) return FNO_ERR_INVALID_ARG;
     if (dtype != FNO_F32 && dtype != FNO_F16) return FNO_ERR_INVALID_ARG;
-    if (flags & ~(FNO_PLAN_UNFUSED | FNO_PLAN_TRACE)) return FNO_ERR_INVALID_ARG;
+    if (flags & ~(FNO_PLAN_UNFUSED | FNO_PLAN_TRACE | FNO_PLAN_TENSOR_CORES))
+        return FNO_ERR_INVALID_ARG;
     // int64 element counts must not overflow and a tensor must stay addressable
     const double xe = (double)batch * cin * g->npix, ye = (double)batch * cout * g->npix;
     if (xe > 4.0e12 || ye > 4.0e12) return FNO_ERR_UNSUPPORTED;
@@ -93,7 +94,7 @@ fno_status_t describe(int ndim, const int64_t *n, const int32_t *modes, int64_t 
         sz->workspace = unfused_workspace_bytes(*g, batch, cin, cout);
         sz->kernels = unfused_kernel_count(*g);
     } else {
-        sz->workspace = fused_workspace_bytes(*g, dtype, batch, cin, cout);
+        sz->workspace = fused_workspace_bytes(*g, dtype, batch, cin, cout, flags);
         sz->kernels = fused_kernel_count(*g, dtype, batch, cin, cout);
     }
     sz->weight = (size_t)g->nblk * cin * cout * g->mblk * 2 * elem_bytes(dtype);

@@ -1364,15 +1364,18 @@ Layout layout_tc(const Geom &g, int64_t batch, int cin, int cout) {
     return l;
 }
 
-bool use_tc(const Geom &g, fno_dtype_t dtype) { return is_cfg128(g) && dtype == FNO_F32; }
+bool use_tc(const Geom &g, fno_dtype_t dtype, uint32_t flags) {
+    return is_cfg128(g) && dtype == FNO_F32 && (flags & FNO_PLAN_TENSOR_CORES);
+}
 
 }  // namespace
 
 size_t fused_sync_bytes() { return kSyncBytes; }
 
-bool fused_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout) {
+bool fused_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout,
+                     uint32_t flags) {
     if (!is_cfg128(g) || (dtype != FNO_F32 && dtype != FNO_F16)) return false;
-    if (use_tc(g, dtype))
+    if (use_tc(g, dtype, flags))
         return batch * (int64_t)(cin > cout ? cin : cout) * 128 < (1ll << 31) &&
                (size_t)cin * 16 <= kTcXpBudget;
     if (batch * (int64_t)cin * Cfg128::C >= (1 << 30) || batch * (int64_t)cout * Cfg128::C >= (1 << 30))
@@ -1380,15 +1383,16 @@ bool fused_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, i
     return smem_bytes(dtype, cin, b_shape(dtype, batch, cin, cout)) <= 200 * 1024;
 }
 
-size_t fused_workspace_bytes(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout) {
-    return use_tc(g, dtype) ? layout_tc(g, batch, cin, cout).total
+size_t fused_workspace_bytes(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout,
+                             uint32_t flags) {
+    return use_tc(g, dtype, flags) ? layout_tc(g, batch, cin, cout).total
                             : layout(g, batch, cin, cout).total;
 }
 
 int fused_kernel_count(const Geom &, fno_dtype_t, int64_t, int, int) { return 1; }
 
 cudaError_t fused_plan_init(Plan &p) {
-    if (use_tc(p.g, p.dtype)) {
+    if (use_tc(p.g, p.dtype, p.flags)) {
         if (!encoder()) return cudaErrorNotSupported;
         const BShape bs = b_shape_tc(p.batch, p.cin, p.cout);
         cudaError_t e = cudaFuncSetAttribute(tc::k_fused2d_tc,
@@ -1454,7 +1458,7 @@ void fused_plan_release(Plan &p) {
 }
 
 cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
-    if (use_tc(p.g, p.dtype)) {
+    if (use_tc(p.g, p.dtype, p.flags)) {
         const Layout l = layout_tc(p.g, p.batch, p.cin, p.cout);
         CUtensorMap xmap, ymap;
         if (!encode_rows(&xmap, b.x, p.batch * p.cin * 128) ||

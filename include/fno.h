@@ -79,6 +79,11 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
 /* Record a timeline of the fused kernel's work items (read back with
  * fno_plan_get_trace).  Costs a few timer reads and stores per item.        */
 #define FNO_PLAN_TRACE 2u
+/* Run the float32 128x128 layer on the tensor-core variant of the fused
+ * kernel (row DFTs as tcgen05 3xTF32 GEMMs fed by TMA) instead of the
+ * register-FFT variant.  Same results within rounding; on this workload the
+ * register-FFT variant is the faster one, so it is the default.            */
+#define FNO_PLAN_TENSOR_CORES 4u
 
 /* One work item of the fused kernel, as recorded under FNO_PLAN_TRACE.
  * Times are the GPU's global nanosecond timer.                              */

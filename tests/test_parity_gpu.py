@@ -46,7 +46,8 @@ def _lib(fno, oracle_mod):
     yield
 
 
-@pytest.mark.parametrize("flags", [0, FNO_PLAN_UNFUSED], ids=["default", "unfused"])
+@pytest.mark.parametrize("flags", [0, FNO_PLAN_UNFUSED, capi.FNO_PLAN_TENSOR_CORES],
+                         ids=["default", "unfused", "tensor_cores"])
 @pytest.mark.parametrize("spec", SMALL, ids=[case_id(c) for c in SMALL])
 def test_small_cases_match_oracle(spec, flags):
     n, modes, b, ci, co, dt = spec
@@ -114,8 +115,12 @@ def test_fused_and_unfused_agree_and_are_deterministic():
     a, _ = run_gpu(case, x, w)
     b, _ = run_gpu(case, x, w)
     c, _ = run_gpu(case, x, w, FNO_PLAN_UNFUSED)
+    d, _ = run_gpu(case, x, w, capi.FNO_PLAN_TENSOR_CORES)
+    e, _ = run_gpu(case, x, w, capi.FNO_PLAN_TENSOR_CORES)
     assert np.array_equal(a, b), "two runs of the same plan differ"
+    assert np.array_equal(d, e), "two runs of the tensor-core plan differ"
     assert_close(a, c.astype(np.float64), "f32", "fused vs unfused")
+    assert_close(d, c.astype(np.float64), "f32", "tensor cores vs unfused")
 
 
 def test_output_red_zones_untouched():
