@@ -183,10 +183,7 @@ __device__ bool wait_flag(const int *flag, int *err) {
     if (ld_acquire(flag) != 0) return true;
     const long long t0 = globaltimer();
     for (unsigned spin = 0;; ++spin) {
-        if (ld_acquire(flag) != 0) {
-            __threadfence();
-            return true;
-        }
+        if (ld_acquire(flag) != 0) return true;
         if (*reinterpret_cast<volatile int *>(err) != 0) return false;
         __nanosleep(64);
         if ((spin & 255u) == 255u && globaltimer() - t0 > kWaitTimeoutNs) {
@@ -196,15 +193,24 @@ __device__ bool wait_flag(const int *flag, int *err) {
     }
 }
 
-// Thread 0 counts one finished item of a phase; the item that completes the
-// phase publishes every flag copy.
+// Thread 0 counts one finished item of a phase (after a barrier of its
+// group, so the group's writes are ordered before it); the item that completes
+// the phase publishes every flag copy.  The count is an acquire-release atomic
+// rather than a full fence plus atomic: it releases this group's writes and,
+// for the last item, acquires every other item's.
 __device__ void finish_item(int *counter, int total, int (*flags)[kLine]) {
     // flags points at the kFlagCopies lines of one group
-    __threadfence();
-    if (atomicAdd(counter, 1) == total - 1) {
-        __threadfence();
-        for (int i = 0; i < kFlagCopies; ++i) *reinterpret_cast<volatile int *>(&flags[i][0]) = 1;
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+    if (old == total - 1) {
+        for (int i = 0; i < kFlagCopies; ++i)
+            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(&flags[i][0]), "r"(1) : "memory");
     }
+}
+
+// L2 prefetch of a byte range (16-byte aligned, multiple of 16 bytes)
+__device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 struct Tw {
@@ -587,6 +593,8 @@ struct Args {
     const float2 *tw1;  // N1 twiddles
     int *err;
     fno_trace_record_t *trace;   // nullptr unless FNO_PLAN_TRACE
+    size_t wbytes;               // weight tensor bytes
+    unsigned wslice;             // bytes of it each phase-A item prefetches into L2
     int batch, cin, cout;
     int bg, ng;         // batch rows per group, groups
     int npairs;         // phase B: kept-mode pairs
@@ -678,9 +686,17 @@ k_fused2d(Args a) {
         if (tid == 0) ts.start(a);
         if (it.phase == 0) {
             const int img = it.g * a.bg * a.cin + it.idx / Cf::C;
+            // the weights are read by the mixing items: bring them into L2 meanwhile
+            if (tid == 0 && a.wslice) {
+                const size_t off = (size_t)it.ticket * a.wslice;
+                if (off < a.wbytes)
+                    prefetch_l2(static_cast<const char *>(a.w) + off,
+                                (unsigned)min((size_t)a.wslice, a.wbytes - off));
+            }
             phase_a<Cf, T>(static_cast<const T *>(a.x), a.part, nimg_in, img, it.idx % Cf::C,
                            work, tw);
             __syncthreads();
+            if (tid == 0) ts.computed(a);
             if (tid == 0)
                 finish_item(&a.sync->done_a[it.g][0], nbg * a.cin * Cf::C, a.sync->flag_a[it.g]);
         } else if (it.phase == 1) {
@@ -700,6 +716,7 @@ k_fused2d(Args a) {
             if (s_ok) phase_b<Cf, T, kNT>(CtaGroup{tid}, a.part, a.Y, a.cin, a.cout, nimg_in, bi, a.ob, work);
             else cp_async_wait_all();
             __syncthreads();
+            if (tid == 0) ts.computed(a);
             if (tid == 0)
                 finish_item(&a.sync->done_b[it.g][0], a.npairs * a.nob, a.sync->flag_b[it.g]);
         } else {
@@ -1475,6 +1492,8 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
         a.tw1 = p.tw[1];
         a.err = p.dev_err;
         a.trace = p.trace;
+        a.wbytes = p.weight_bytes;
+        a.wslice = 0;
         a.batch = (int)p.batch;
         a.cin = p.cin;
         a.cout = p.cout;
@@ -1510,6 +1529,13 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
     a.npairs = (int)(p.g.nkept / kG);
     a.ob = p.fused_ob;
     a.nob = (p.cout + a.ob - 1) / a.ob;
+    {
+        // phase-A tickets are the first ones of each batch group's A segment;
+        // spread the weight bytes over the first nA tickets in 16-byte units
+        const size_t nA = (size_t)p.batch * p.cin * Cfg128::C;
+        a.wbytes = p.weight_bytes;
+        a.wslice = (unsigned)(((p.weight_bytes + nA - 1) / nA + 15) / 16 * 16);
+    }
     const int total = (int)p.batch * (p.cin + p.cout) * Cfg128::C + a.ng * a.npairs * a.nob;
     const int grid = p.fused_grid < total ? p.fused_grid : total;
     if (p.dtype == FNO_F32)
