@@ -71,6 +71,10 @@ constexpr int kMaxGroups = 16;     // batch groups of one launch
 #define FNO_TARGET_GROUPS 2
 #endif
 constexpr int kTargetGroups = FNO_TARGET_GROUPS;   // batch groups the phases pipeline over
+#ifndef FNO_WEIGHT_PREFETCH
+#define FNO_WEIGHT_PREFETCH 0
+#endif
+constexpr bool kWeightPrefetch = FNO_WEIGHT_PREFETCH;   // phase-A items prefetch W into L2
 struct SyncBlock {
     int ticket[kLine];                         // [0]: next work item
     int exited[kLine];                         // [0]: CTAs that have left the queue
@@ -1534,7 +1538,7 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
         // spread the weight bytes over the first nA tickets in 16-byte units
         const size_t nA = (size_t)p.batch * p.cin * Cfg128::C;
         a.wbytes = p.weight_bytes;
-        a.wslice = (unsigned)(((p.weight_bytes + nA - 1) / nA + 15) / 16 * 16);
+        a.wslice = kWeightPrefetch ? (unsigned)(((p.weight_bytes + nA - 1) / nA + 15) / 16 * 16) : 0u;
     }
     const int total = (int)p.batch * (p.cin + p.cout) * Cfg128::C + a.ng * a.npairs * a.nob;
     const int grid = p.fused_grid < total ? p.fused_grid : total;
