@@ -207,8 +207,10 @@ __device__ void finish_item(int *counter, int total, int (*flags)[kLine]) {
     int old;
     asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
     if (old == total - 1) {
-        for (int i = 0; i < kFlagCopies; ++i)
-            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(&flags[i][0]), "r"(1) : "memory");
+        // one fence orders everything this item acquired before all the flag
+        // stores (a release on each store would cost a fence apiece)
+        __threadfence();
+        for (int i = 0; i < kFlagCopies; ++i) *reinterpret_cast<volatile int *>(&flags[i][0]) = 1;
     }
 }
 
