@@ -143,6 +143,25 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of one float per rank (the slowest rank's time); a no-op
+    for a single process.  Works on any process-group backend: the tensor
+    lives on `device` (a CUDA device under NCCL, the CPU under gloo)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(batch_per_rank: int, world: int, steps: int, ms_max: float) -> float:
+    """Samples per second of the whole job: every rank runs `steps` forwards
+    of its own batch (weak scaling), timed by the slowest rank."""
+    return world * batch_per_rank * steps / (ms_max / 1e3)
+
+
 def bench_gpu(args, rank, world, local):
     import numpy as np
     import torch
@@ -210,11 +229,7 @@ def bench_gpu(args, rank, world, local):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    ms = start.elapsed_time(end)
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(start.elapsed_time(end), world, dev)
     stream.synchronize()
     assert conv.device_error(stream) == 0
 
@@ -239,13 +254,9 @@ def bench_gpu(args, rank, world, local):
             y_host.copy_(ys[i % nsets], non_blocking=True)
         e1.record(stream)
         stream.synchronize()
-    te = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_ms = float(te.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
 
-    samples_total = world * case.batch * steps
-    value = samples_total / (ms_max / 1e3)
+    value = whole_job_rate(case.batch, world, steps, ms_max)
     kernel_ms = ms_max / steps          # back-to-back graph replay: per-forward duration
     peak, peak_kind = measured_peaks()
     alg_bytes = case.algorithmic_bytes()
@@ -291,7 +302,7 @@ def bench_gpu(args, rank, world, local):
             "traffic": recorded_traffic(case.name),
         },
         "e2e": {
-            "value": round(case.batch * world * e2e_steps / (e2e_ms / 1e3), 1),
+            "value": round(whole_job_rate(case.batch, world, e2e_steps, e2e_ms), 1),
             "unit": "samples/s",
             "h2d_bytes_per_step": int(x_np.nbytes),
             "d2h_bytes_per_step": int(math.prod(case.y_shape) * case.elem_bytes),
