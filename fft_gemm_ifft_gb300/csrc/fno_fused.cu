@@ -681,8 +681,17 @@ k_fused2d(Args a) {
     }
     const Tw tw{tw0, tw1};
     const int nimg_in = a.batch * a.cin;
+    // thread 0 claims one ticket ahead: the atomic's round trip overlaps the
+    // current item.  A held ticket is always larger than its holder's current
+    // item and every dependency points to smaller tickets, so the smallest
+    // unfinished ticket can always run: no deadlock.
+    int next_ticket = 0;
+    if (tid == 0) next_ticket = atomicAdd(&a.sync->ticket[0], 1);
     for (;;) {
-        if (tid == 0) s_item = decode_ticket<Cf>(a, atomicAdd(&a.sync->ticket[0], 1));
+        if (tid == 0) {
+            s_item = decode_ticket<Cf>(a, next_ticket);
+            if (s_item.phase >= 0) next_ticket = atomicAdd(&a.sync->ticket[0], 1);
+        }
         __syncthreads();
         const Item it = s_item;
         __syncthreads();
