@@ -30,6 +30,7 @@ FNO_PLAN_DEFAULT = 0
 FNO_PLAN_UNFUSED = 1
 FNO_PLAN_TRACE = 2
 FNO_PLAN_TENSOR_CORES = 4
+FNO_PLAN_PERSISTENT = 8
 
 # Every symbol include/fno.h declares.
 EXPORTS = (

@@ -84,7 +84,7 @@ fno_status_t describe(int ndim, const int64_t *n, const int32_t *modes, int64_t 
     if (st != FNO_OK) return st;
     if (batch < 1 || cin < 1 || cout < 1) return FNO_ERR_INVALID_ARG;
     if (dtype != FNO_F32 && dtype != FNO_F16) return FNO_ERR_INVALID_ARG;
-    if (flags & ~(FNO_PLAN_UNFUSED | FNO_PLAN_TRACE | FNO_PLAN_TENSOR_CORES))
+    if (flags & ~(FNO_PLAN_UNFUSED | FNO_PLAN_TRACE | FNO_PLAN_TENSOR_CORES | FNO_PLAN_PERSISTENT))
         return FNO_ERR_INVALID_ARG;
     // int64 element counts must not overflow and a tensor must stay addressable
     const double xe = (double)batch * cin * g->npix, ye = (double)batch * cout * g->npix;
@@ -95,7 +95,7 @@ fno_status_t describe(int ndim, const int64_t *n, const int32_t *modes, int64_t 
         sz->kernels = unfused_kernel_count(*g);
     } else {
         sz->workspace = fused_workspace_bytes(*g, dtype, batch, cin, cout, flags);
-        sz->kernels = fused_kernel_count(*g, dtype, batch, cin, cout);
+        sz->kernels = fused_kernel_count(*g, dtype, batch, cin, cout, flags);
     }
     sz->weight = (size_t)g->nblk * cin * cout * g->mblk * 2 * elem_bytes(dtype);
     return FNO_OK;

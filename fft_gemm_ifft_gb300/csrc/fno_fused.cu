@@ -768,6 +768,76 @@ k_fused2d(Args a) {
 }
 
 // ---------------------------------------------------------------------------
+// Three-kernel variant: phase A, B and C as separate grids chained by
+// programmatic dependent launch.  Every CTA runs one item, so the hardware
+// block scheduler replaces the ticket queue and its atomics.  Kernel B (C) is
+// launched while kernel A (B) still runs; its CTAs become resident once every
+// CTA of the previous grid has started, fetch what does not depend on it (the
+// weight slab, the twiddles) and then wait in griddepcontrol.wait until the
+// previous grid has finished and its writes are visible.  The first kernel of
+// a forward is an ordinary launch, so it is ordered after whatever the stream
+// ran before (e.g. the producer of x).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <class Cf>
+__device__ __forceinline__ Tw load_twiddles(const Args &a, char *smem) {
+    float2 *tw0 = reinterpret_cast<float2 *>(smem);
+    float2 *tw1 = tw0 + Cf::N0;
+    for (int e = threadIdx.x; e < Cf::N0; e += kNT) tw0[e] = a.tw0[e];
+    for (int e = threadIdx.x; e < Cf::P * Cf::TS; e += kNT) {
+        const int n1 = e / Cf::TS, k = e % Cf::TS;
+        tw1[e] = a.tw1[(n1 * k) & (Cf::N1 - 1)];
+    }
+    return Tw{tw0, tw1};
+}
+
+template <class Cf, typename T>
+__global__ void __launch_bounds__(kNT) k_phase_a(Args a) {
+    extern __shared__ __align__(16) char smem[];
+    const Tw tw = load_twiddles<Cf>(a, smem);
+    __syncthreads();
+    pdl_trigger();
+    const int item = blockIdx.x;                 // image * C + chunk
+    phase_a<Cf, T>(static_cast<const T *>(a.x), a.part, a.batch * a.cin, item / Cf::C,
+                   item % Cf::C, smem + Cf::kSmemTw, tw);
+}
+
+// item = (pair * nob + output block) * batch blocks + batch block; a.bg = batch
+// rows per block, a.ng = batch blocks
+template <class Cf, typename T>
+__global__ void __launch_bounds__(kNT) k_phase_b(Args a) {
+    extern __shared__ __align__(16) char smem[];
+    int it = blockIdx.x;
+    const int bblk = it % a.ng;
+    it /= a.ng;
+    BItem bi;
+    bi.pair = it / a.nob;
+    bi.o0 = (it % a.nob) * a.ob;
+    bi.nob = min(a.ob, a.cout - bi.o0);
+    bi.b0 = bblk * a.bg;
+    bi.nbb = min(a.bg, a.batch - bi.b0);
+    const CtaGroup grp{(int)threadIdx.x};
+    phase_b_weights<Cf, T, kNT>(grp, static_cast<const T *>(a.w), a.cin, a.cout, bi, a.ob, smem);
+    pdl_trigger();
+    pdl_wait();                                  // kernel A's partial modes are complete
+    phase_b<Cf, T, kNT>(grp, a.part, a.Y, a.cin, a.cout, a.batch * a.cin, bi, a.ob, smem);
+}
+
+template <class Cf, typename T>
+__global__ void __launch_bounds__(kNT) k_phase_c(Args a) {
+    extern __shared__ __align__(16) char smem[];
+    const Tw tw = load_twiddles<Cf>(a, smem);
+    __syncthreads();
+    pdl_wait();                                  // kernel B's mixed modes are complete
+    const int item = blockIdx.x;
+    phase_c<Cf, T>(a.Y, static_cast<T *>(a.y), item / Cf::C, item % Cf::C, smem + Cf::kSmemTw, tw);
+}
+
+// ---------------------------------------------------------------------------
 // Tensor-core variant for float32 storage (128 x 128, 16 x 16 modes)
 //
 // Phase A: TMA brings a whole input image (128 rows x 128 columns) into shared
@@ -1421,7 +1491,68 @@ size_t fused_workspace_bytes(const Geom &g, fno_dtype_t dtype, int64_t batch, in
                             : layout(g, batch, cin, cout).total;
 }
 
-int fused_kernel_count(const Geom &, fno_dtype_t, int64_t, int, int) { return 1; }
+bool use_pdl(const Geom &g, fno_dtype_t dtype, uint32_t flags) {
+    return !use_tc(g, dtype, flags) && !(flags & FNO_PLAN_PERSISTENT);
+}
+
+int fused_kernel_count(const Geom &g, fno_dtype_t dtype, int64_t, int, int, uint32_t flags) {
+    return use_pdl(g, dtype, flags) ? 3 : 1;
+}
+
+// three-kernel variant: largest batch block whose C partials fit kXpBudget
+int pdl_batch_block(int64_t batch, int cin) {
+    int bb = (int)batch;
+    while (bb > 1 && (size_t)Cfg128::C * bb * cin * 16 > kXpBudget) bb = (bb + 1) / 2;
+    return bb;
+}
+
+template <typename T>
+cudaError_t pdl_init(Plan &p, const BShape &bs) {
+    const int bb = pdl_batch_block(p.batch, p.cin);
+    const size_t w2 = p.dtype == FNO_F32 ? 16 : 8;
+    const size_t sa = Cfg128::kSmemTw + Cfg128::kSmemA, sc = Cfg128::kSmemTw + Cfg128::kSmemC;
+    const size_t sb = ((size_t)p.cin * bs.ob * w2 + 15) / 16 * 16 + (size_t)Cfg128::C * bb * p.cin * 16;
+    cudaError_t e = cudaFuncSetAttribute(k_phase_a<Cfg128, T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_phase_b<Cfg128, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sb);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_phase_c<Cfg128, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sc);
+    p.fused_bb = bb;
+    p.fused_ob = bs.ob;
+    p.fused_smem = sb;                 // kernel B's; A and C use their fixed sizes
+    p.fused_grid = 0;
+    return e;
+}
+
+template <typename T>
+cudaError_t pdl_forward(const Plan &p, Args a, cudaStream_t s) {
+    a.bg = p.fused_bb;
+    a.ng = (int)((p.batch + a.bg - 1) / a.bg);
+    const int nA = (int)p.batch * p.cin * Cfg128::C;
+    const int nB = a.npairs * a.nob * a.ng;
+    const int nC = (int)p.batch * p.cout * Cfg128::C;
+    k_phase_a<Cfg128, T><<<nA, kNT, Cfg128::kSmemTw + Cfg128::kSmemA, s>>>(a);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kNT);
+    cfg.stream = s;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(nB);
+    cfg.dynamicSmemBytes = p.fused_smem;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_phase_b<Cfg128, T>, a);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(nC);
+    cfg.dynamicSmemBytes = Cfg128::kSmemTw + Cfg128::kSmemC;
+    e = cudaLaunchKernelEx(&cfg, k_phase_c<Cfg128, T>, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
 
 cudaError_t fused_plan_init(Plan &p) {
     if (use_tc(p.g, p.dtype, p.flags)) {
@@ -1459,6 +1590,8 @@ cudaError_t fused_plan_init(Plan &p) {
         return cudaMemset(p.sync, 0, kSyncBytes);
     }
     const BShape bs = b_shape(p.dtype, p.batch, p.cin, p.cout);
+    if (use_pdl(p.g, p.dtype, p.flags))
+        return p.dtype == FNO_F32 ? pdl_init<float>(p, bs) : pdl_init<__half>(p, bs);
     const size_t smem = smem_bytes(p.dtype, p.cin, bs);
     void *fn = p.dtype == FNO_F32 ? kernel_ptr<float>() : kernel_ptr<__half>();
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1525,7 +1658,7 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
         return cudaGetLastError();
     }
     const Layout l = layout(p.g, p.batch, p.cin, p.cout);
-    Args a;
+    Args a{};
     a.x = b.x;
     a.w = b.w;
     a.y = b.y;
@@ -1551,6 +1684,8 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
         a.wbytes = p.weight_bytes;
         a.wslice = kWeightPrefetch ? (unsigned)(((p.weight_bytes + nA - 1) / nA + 15) / 16 * 16) : 0u;
     }
+    if (use_pdl(p.g, p.dtype, p.flags))
+        return p.dtype == FNO_F32 ? pdl_forward<float>(p, a, s) : pdl_forward<__half>(p, a, s);
     const int total = (int)p.batch * (p.cin + p.cout) * Cfg128::C + a.ng * a.npairs * a.nob;
     const int grid = p.fused_grid < total ? p.fused_grid : total;
     if (p.dtype == FNO_F32)

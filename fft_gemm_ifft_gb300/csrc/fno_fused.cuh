@@ -12,7 +12,8 @@ bool fused_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, i
                      uint32_t flags);
 size_t fused_workspace_bytes(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin,
                              int cout, uint32_t flags);
-int fused_kernel_count(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout);
+int fused_kernel_count(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout,
+                       uint32_t flags);
 // Plan-time set-up (tables, attributes); called once from plan creation.
 cudaError_t fused_plan_init(Plan &p);
 void fused_plan_release(Plan &p);

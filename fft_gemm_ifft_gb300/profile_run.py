@@ -33,6 +33,8 @@ def main(argv=None) -> int:
         case = case.with_batch(args.batch)
     from . import capi
     flags = args.flags | (capi.FNO_PLAN_TRACE if args.trace else 0)
+    if args.trace and not flags & capi.FNO_PLAN_TENSOR_CORES:
+        flags |= capi.FNO_PLAN_PERSISTENT       # the trace covers the persistent kernels
     conv = SpectralConv(case.n, case.modes, case.batch, case.cin, case.cout, case.dtype, flags)
     x_np, w_np = workloads.make_x(case), workloads.make_w(case)
     set_bytes = x_np.nbytes + w_np.nbytes + math.prod(case.y_shape) * case.elem_bytes

@@ -84,6 +84,10 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * register-FFT variant.  Same results within rounding; on this workload the
  * register-FFT variant is the faster one, so it is the default.            */
 #define FNO_PLAN_TENSOR_CORES 4u
+/* Run the float32 / fp16 128x128 layer as ONE persistent kernel with a work
+ * queue instead of three kernels chained by programmatic dependent launch
+ * (the default).  FNO_PLAN_TRACE records only this variant.               */
+#define FNO_PLAN_PERSISTENT 8u
 
 /* One work item of the fused kernel, as recorded under FNO_PLAN_TRACE.
  * Times are the GPU's global nanosecond timer.                              */
@@ -156,7 +160,9 @@ fno_status_t fno_spectral_conv_kernel_count(fno_plan_t plan, int *count);
  * every call.  Calls on one stream, or stream-ordered, may share both.
  * Every pointer must be 16-byte aligned (FNO_ERR_MISALIGNED otherwise).
  * The call makes no allocation and no host synchronisation, so it may be
- * captured in a CUDA graph.  Launch failures return FNO_ERR_CUDA; faults
+ * captured in a CUDA graph.  Its first kernel is ordered after the work
+ * already on `stream` like any launch; its later kernels use programmatic
+ * dependent launch among themselves.  Launch failures return FNO_ERR_CUDA; faults
  * detected inside kernels are reported by fno_plan_get_device_error.        */
 fno_status_t fno_spectral_conv_forward(fno_plan_t plan, const void *x, const void *w,
                                        void *y, void *workspace, fno_stream_t stream);

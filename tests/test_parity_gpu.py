@@ -46,8 +46,9 @@ def _lib(fno, oracle_mod):
     yield
 
 
-@pytest.mark.parametrize("flags", [0, FNO_PLAN_UNFUSED, capi.FNO_PLAN_TENSOR_CORES],
-                         ids=["default", "unfused", "tensor_cores"])
+@pytest.mark.parametrize("flags", [0, FNO_PLAN_UNFUSED, capi.FNO_PLAN_TENSOR_CORES,
+                                   capi.FNO_PLAN_PERSISTENT],
+                         ids=["default", "unfused", "tensor_cores", "persistent"])
 @pytest.mark.parametrize("spec", SMALL, ids=[case_id(c) for c in SMALL])
 def test_small_cases_match_oracle(spec, flags):
     n, modes, b, ci, co, dt = spec
@@ -117,6 +118,8 @@ def test_fused_and_unfused_agree_and_are_deterministic():
     c, _ = run_gpu(case, x, w, FNO_PLAN_UNFUSED)
     d, _ = run_gpu(case, x, w, capi.FNO_PLAN_TENSOR_CORES)
     e, _ = run_gpu(case, x, w, capi.FNO_PLAN_TENSOR_CORES)
+    f, _ = run_gpu(case, x, w, capi.FNO_PLAN_PERSISTENT)
+    assert_close(f, c.astype(np.float64), "f32", "persistent vs unfused")
     assert np.array_equal(a, b), "two runs of the same plan differ"
     assert np.array_equal(d, e), "two runs of the tensor-core plan differ"
     assert_close(a, c.astype(np.float64), "f32", "fused vs unfused")
@@ -189,7 +192,7 @@ def test_plan_create_destroy_many_times_no_leak():
 def test_trace_records_every_item():
     case = workloads.CASES["2d_f32"]
     conv = SpectralConv(case.n, case.modes, case.batch, case.cin, case.cout, case.dtype,
-                        capi.FNO_PLAN_TRACE)
+                        capi.FNO_PLAN_TRACE | capi.FNO_PLAN_PERSISTENT)
     x, w = workloads.make_x(case), workloads.make_w(case)
     y = conv(to_dev(x), to_dev(w))
     torch.cuda.synchronize()
