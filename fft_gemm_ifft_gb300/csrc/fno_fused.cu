@@ -227,7 +227,7 @@ struct Tw {
 // ---------------------------------------------------------------------------
 // Phase A: one chunk of rows of one input image -> partial kept modes
 // ---------------------------------------------------------------------------
-template <class Cf, typename T>
+template <class Cf, typename T, bool kCluster = false>
 __device__ void phase_a(const T *__restrict__ x, float2 *__restrict__ part, int nimg, int img,
                         int c, char *smem, Tw tw) {
     constexpr int N0 = Cf::N0, N1 = Cf::N1, RC = Cf::RC, C = Cf::C, P = Cf::P, Q = Cf::Q;
@@ -313,7 +313,12 @@ __device__ void phase_a(const T *__restrict__ x, float2 *__restrict__ part, int 
     __syncthreads();
 
     // 3b. X_c[j][k] = W_N0^{f c} sum_t1 W_RC^{f t1} S[t1][f mod B2][k], f = freq of kept row j
-    float2 *dst = part + ((size_t)c * nimg + img) * NK;
+    //     Without a cluster the chunk's partial goes to the workspace (the mixing
+    //     sums the C partials); in a cluster of the image's C chunk-CTAs it stays
+    //     in shared memory (over the x rows, no longer needed) and each CTA sums
+    //     one C-th of the modes over the cluster's CTAs, writing X once.
+    float2 *xpart = reinterpret_cast<float2 *>(smem);
+    float2 *dst = part + ((size_t)(kCluster ? 0 : c) * nimg + img) * NK;
     constexpr int kRcStep = N0 / RC;             // W_RC^e = W_N0^{e N0/RC}
     for (int o = tid; o < NK; o += kNT) {
         const int j = o / M1, k = o % M1;
@@ -323,7 +328,36 @@ __device__ void phase_a(const T *__restrict__ x, float2 *__restrict__ part, int 
         for (int t1 = 0; t1 < A; ++t1)
             cmac(acc, ss[(t1 * B2 + (f % B2)) * M1 + k],
                  tw.t0[((f % RC) * t1 * kRcStep) & (N0 - 1)]);
-        __stcg(dst + o, cmul(acc, tw.t0[(f * c) & (N0 - 1)]));
+        acc = cmul(acc, tw.t0[(f * c) & (N0 - 1)]);
+        if constexpr (kCluster)
+            xpart[o] = acc;
+        else
+            __stcg(dst + o, acc);
+    }
+    if constexpr (kCluster) {
+        static_assert(NK % C == 0, "mode slices");
+        asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                     "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+        const uint32_t local = (uint32_t)__cvta_generic_to_shared(xpart);
+        constexpr int kSlice = NK / C;           // modes this CTA reduces
+        for (int o = c * kSlice + tid; o < (c + 1) * kSlice; o += kNT) {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                uint32_t remote;
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                             : "=r"(remote) : "r"(local + o * 8), "r"(r));
+                float2 v;
+                asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+                             : "=f"(v.x), "=f"(v.y) : "r"(remote) : "memory");
+                acc.x += v.x;
+                acc.y += v.y;
+            }
+            __stcg(dst + o, acc);
+        }
+        // no CTA may leave while another still reads its shared memory
+        asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                     "barrier.cluster.wait.acquire.aligned;" ::: "memory");
     }
 }
 
@@ -449,11 +483,11 @@ __device__ void phase_b_tiles(const G &grp, float2 *__restrict__ Y, int cin, int
     }
 }
 
-template <class Cf, typename T, int NT, class G>
+template <class Cf, typename T, int NT, class G, int kParts = Cf::C>
 __device__ void phase_b(const G &grp, const float2 *__restrict__ part, float2 *__restrict__ Y, int cin,
                         int cout, int nimg_in, const BItem &it, int ob, char *smem) {
     using W2 = typename Io<T>::W2;
-    constexpr int NK = Cf::NK, C = Cf::C;
+    constexpr int NK = Cf::NK, C = kParts;
     const int mode0 = it.pair * kG;
     const W2 *ws = reinterpret_cast<const W2 *>(smem);                       // [cin][ob]
     float4 *xp = reinterpret_cast<float4 *>(smem + ((size_t)cin * ob * sizeof(W2) + 15) / 16 * 16);
@@ -802,8 +836,8 @@ __global__ void __launch_bounds__(kNT) k_phase_a(Args a) {
     __syncthreads();
     pdl_trigger();
     const int item = blockIdx.x;                 // image * C + chunk
-    phase_a<Cf, T>(static_cast<const T *>(a.x), a.part, a.batch * a.cin, item / Cf::C,
-                   item % Cf::C, smem + Cf::kSmemTw, tw);
+    phase_a<Cf, T, true>(static_cast<const T *>(a.x), a.part, a.batch * a.cin, item / Cf::C,
+                         item % Cf::C, smem + Cf::kSmemTw, tw);
 }
 
 // item = (pair * nob + output block) * batch blocks + batch block; a.bg = batch
@@ -824,7 +858,8 @@ __global__ void __launch_bounds__(kNT) k_phase_b(Args a) {
     phase_b_weights<Cf, T, kNT>(grp, static_cast<const T *>(a.w), a.cin, a.cout, bi, a.ob, smem);
     pdl_trigger();
     pdl_wait();                                  // kernel A's partial modes are complete
-    phase_b<Cf, T, kNT>(grp, a.part, a.Y, a.cin, a.cout, a.batch * a.cin, bi, a.ob, smem);
+    phase_b<Cf, T, kNT, CtaGroup, 1>(grp, a.part, a.Y, a.cin, a.cout, a.batch * a.cin, bi, a.ob,
+                                     smem);
 }
 
 template <class Cf, typename T>
@@ -1499,10 +1534,10 @@ int fused_kernel_count(const Geom &g, fno_dtype_t dtype, int64_t, int, int, uint
     return use_pdl(g, dtype, flags) ? 3 : 1;
 }
 
-// three-kernel variant: largest batch block whose C partials fit kXpBudget
+// three-kernel variant: largest batch block whose (cluster-reduced) modes fit kXpBudget
 int pdl_batch_block(int64_t batch, int cin) {
     int bb = (int)batch;
-    while (bb > 1 && (size_t)Cfg128::C * bb * cin * 16 > kXpBudget) bb = (bb + 1) / 2;
+    while (bb > 1 && (size_t)bb * cin * 16 > kXpBudget) bb = (bb + 1) / 2;
     return bb;
 }
 
@@ -1511,7 +1546,7 @@ cudaError_t pdl_init(Plan &p, const BShape &bs) {
     const int bb = pdl_batch_block(p.batch, p.cin);
     const size_t w2 = p.dtype == FNO_F32 ? 16 : 8;
     const size_t sa = Cfg128::kSmemTw + Cfg128::kSmemA, sc = Cfg128::kSmemTw + Cfg128::kSmemC;
-    const size_t sb = ((size_t)p.cin * bs.ob * w2 + 15) / 16 * 16 + (size_t)Cfg128::C * bb * p.cin * 16;
+    const size_t sb = ((size_t)p.cin * bs.ob * w2 + 15) / 16 * 16 + (size_t)bb * p.cin * 16;
     cudaError_t e = cudaFuncSetAttribute(k_phase_a<Cfg128, T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa);
     if (e == cudaSuccess)
@@ -1534,7 +1569,23 @@ cudaError_t pdl_forward(const Plan &p, Args a, cudaStream_t s) {
     const int nA = (int)p.batch * p.cin * Cfg128::C;
     const int nB = a.npairs * a.nob * a.ng;
     const int nC = (int)p.batch * p.cout * Cfg128::C;
-    k_phase_a<Cfg128, T><<<nA, kNT, Cfg128::kSmemTw + Cfg128::kSmemA, s>>>(a);
+    {
+        // the C chunk-CTAs of one image form a cluster that reduces their partials
+        cudaLaunchAttribute cl;
+        cl.id = cudaLaunchAttributeClusterDimension;
+        cl.val.clusterDim.x = Cfg128::C;
+        cl.val.clusterDim.y = 1;
+        cl.val.clusterDim.z = 1;
+        cudaLaunchConfig_t ca = {};
+        ca.gridDim = dim3(nA);
+        ca.blockDim = dim3(kNT);
+        ca.dynamicSmemBytes = Cfg128::kSmemTw + Cfg128::kSmemA;
+        ca.stream = s;
+        ca.attrs = &cl;
+        ca.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&ca, k_phase_a<Cfg128, T>, a);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
