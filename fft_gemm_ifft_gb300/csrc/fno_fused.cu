@@ -585,27 +585,23 @@ __device__ void phase_c(const float2 *__restrict__ Y, T *__restrict__ y, int img
     for (int pr = tid; pr < Cf::PAIRS; pr += kNT) {
         const int t = pr / P, n1 = pr % P, t2 = t + RC / 2;
         const float2 *twl = tw.t1 + n1 * Cf::TS;
-        float2 ga[Q], gb[Q];
-#pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            ga[q] = make_float2(0.f, 0.f);
-            gb[q] = make_float2(0.f, 0.f);
-        }
-#pragma unroll
-        for (int k = 0; k < M1; ++k) {
-            const float ck = (k == 0 || 2 * k == N1) ? 1.f : 2.f;
-            const float2 w = twl[k];
-            ga[k % Q] = cadd(ga[k % Q], cscale(cmulc(zo[t * ZS + k], w), ck));
-            gb[k % Q] = cadd(gb[k % Q], cscale(cmulc(zo[t2 * ZS + k], w), ck));
-        }
-        // Hermitian parts, packed: z[q] = Herm(ga)[q] + i Herm(gb)[q]
+        // z[q] = Herm(ga)[q] + i Herm(gb)[q], accumulated directly: a bin k
+        // (q = k mod Q) with va = c_k W^{-k n1} Zo[t][k], vb likewise for row t2,
+        // adds (va + i vb)/2 at q and (conj va + i conj vb)/2 at Q - q
         float2 z[Q];
 #pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            const int qm = (Q - q) % Q;
-            const float2 ha = make_float2(0.5f * (ga[q].x + ga[qm].x), 0.5f * (ga[q].y - ga[qm].y));
-            const float2 hb = make_float2(0.5f * (gb[q].x + gb[qm].x), 0.5f * (gb[q].y - gb[qm].y));
-            z[q] = make_float2(ha.x - hb.y, ha.y + hb.x);
+        for (int q = 0; q < Q; ++q) z[q] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < M1; ++k) {
+            const float hk = (k == 0 || 2 * k == N1) ? 0.5f : 1.f;    // c_k / 2
+            const float2 w = twl[k];
+            const float2 va = cscale(cmulc(zo[t * ZS + k], w), hk);
+            const float2 vb = cscale(cmulc(zo[t2 * ZS + k], w), hk);
+            const int q = k % Q, qm = (Q - q) % Q;
+            z[q].x += va.x - vb.y;
+            z[q].y += va.y + vb.x;
+            z[qm].x += va.x + vb.y;
+            z[qm].y += vb.x - va.y;
         }
         fft::fft_dif<Q, 1>(z);
         T *ra = dst + (size_t)(c + C * t) * N1 + n1;
@@ -829,20 +825,20 @@ __device__ __forceinline__ Tw load_twiddles(const Args &a, char *smem) {
     return Tw{tw0, tw1};
 }
 
-template <class Cf, typename T>
+template <class Cf, typename T, bool kCluster>
 __global__ void __launch_bounds__(kNT) k_phase_a(Args a) {
     extern __shared__ __align__(16) char smem[];
     const Tw tw = load_twiddles<Cf>(a, smem);
     __syncthreads();
     pdl_trigger();
     const int item = blockIdx.x;                 // image * C + chunk
-    phase_a<Cf, T, true>(static_cast<const T *>(a.x), a.part, a.batch * a.cin, item / Cf::C,
-                         item % Cf::C, smem + Cf::kSmemTw, tw);
+    phase_a<Cf, T, kCluster>(static_cast<const T *>(a.x), a.part, a.batch * a.cin, item / Cf::C,
+                             item % Cf::C, smem + Cf::kSmemTw, tw);
 }
 
 // item = (pair * nob + output block) * batch blocks + batch block; a.bg = batch
 // rows per block, a.ng = batch blocks
-template <class Cf, typename T>
+template <class Cf, typename T, int kParts>
 __global__ void __launch_bounds__(kNT) k_phase_b(Args a) {
     extern __shared__ __align__(16) char smem[];
     int it = blockIdx.x;
@@ -858,8 +854,8 @@ __global__ void __launch_bounds__(kNT) k_phase_b(Args a) {
     phase_b_weights<Cf, T, kNT>(grp, static_cast<const T *>(a.w), a.cin, a.cout, bi, a.ob, smem);
     pdl_trigger();
     pdl_wait();                                  // kernel A's partial modes are complete
-    phase_b<Cf, T, kNT, CtaGroup, 1>(grp, a.part, a.Y, a.cin, a.cout, a.batch * a.cin, bi, a.ob,
-                                     smem);
+    phase_b<Cf, T, kNT, CtaGroup, kParts>(grp, a.part, a.Y, a.cin, a.cout, a.batch * a.cin, bi,
+                                          a.ob, smem);
 }
 
 template <class Cf, typename T>
@@ -1509,104 +1505,152 @@ bool use_tc(const Geom &g, fno_dtype_t dtype, uint32_t flags) {
 
 size_t fused_sync_bytes() { return kSyncBytes; }
 
-bool fused_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout,
-                     uint32_t flags) {
-    if (!is_cfg128(g) || (dtype != FNO_F32 && dtype != FNO_F16)) return false;
-    if (use_tc(g, dtype, flags))
-        return batch * (int64_t)(cin > cout ? cin : cout) * 128 < (1ll << 31) &&
-               (size_t)cin * 16 <= kTcXpBudget;
-    if (batch * (int64_t)cin * Cfg128::C >= (1 << 30) || batch * (int64_t)cout * Cfg128::C >= (1 << 30))
-        return false;
-    return smem_bytes(dtype, cin, b_shape(dtype, batch, cin, cout)) <= 200 * 1024;
+// 256 x 256 grid, 32 x 32 modes per block: chunks of 64 strided rows, 32-point
+// row FFTs (8 partial sums per bin), 8-point column FFTs; the four chunk-CTAs
+// of an image reduce their partial modes in a cluster.
+using Cfg256 = Cfg<256, 256, 32, 32, 64, 32, 8>;
+
+bool is_cfg256(const Geom &g) {
+    return g.d == 2 && g.n[0] == 256 && g.n[1] == 256 && g.m[0] == 32 && g.m[1] == 32;
 }
 
-size_t fused_workspace_bytes(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout,
-                             uint32_t flags) {
-    return use_tc(g, dtype, flags) ? layout_tc(g, batch, cin, cout).total
-                            : layout(g, batch, cin, cout).total;
-}
-
-bool use_pdl(const Geom &g, fno_dtype_t dtype, uint32_t flags) {
-    return !use_tc(g, dtype, flags) && !(flags & FNO_PLAN_PERSISTENT);
-}
-
-int fused_kernel_count(const Geom &g, fno_dtype_t dtype, int64_t, int, int, uint32_t flags) {
-    return use_pdl(g, dtype, flags) ? 3 : 1;
-}
-
-// three-kernel variant: largest batch block whose (cluster-reduced) modes fit kXpBudget
-int pdl_batch_block(int64_t batch, int cin) {
-    int bb = (int)batch;
-    while (bb > 1 && (size_t)bb * cin * 16 > kXpBudget) bb = (bb + 1) / 2;
-    return bb;
-}
-
-template <typename T>
-cudaError_t pdl_init(Plan &p, const BShape &bs) {
-    const int bb = pdl_batch_block(p.batch, p.cin);
-    const size_t w2 = p.dtype == FNO_F32 ? 16 : 8;
-    const size_t sa = Cfg128::kSmemTw + Cfg128::kSmemA, sc = Cfg128::kSmemTw + Cfg128::kSmemC;
-    const size_t sb = ((size_t)p.cin * bs.ob * w2 + 15) / 16 * 16 + (size_t)bb * p.cin * 16;
-    cudaError_t e = cudaFuncSetAttribute(k_phase_a<Cfg128, T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_phase_b<Cfg128, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)sb);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_phase_c<Cfg128, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)sc);
-    p.fused_bb = bb;
-    p.fused_ob = bs.ob;
-    p.fused_smem = sb;                 // kernel B's; A and C use their fixed sizes
-    p.fused_grid = 0;
-    return e;
-}
-
-template <typename T>
-cudaError_t pdl_forward(const Plan &p, Args a, cudaStream_t s) {
-    a.bg = p.fused_bb;
-    a.ng = (int)((p.batch + a.bg - 1) / a.bg);
-    const int nA = (int)p.batch * p.cin * Cfg128::C;
-    const int nB = a.npairs * a.nob * a.ng;
-    const int nC = (int)p.batch * p.cout * Cfg128::C;
-    {
-        // the C chunk-CTAs of one image form a cluster that reduces their partials
+// Three-kernel variant, per shape: whether phase A reduces its partials in a
+// cluster, and the kernels' shared memory.
+template <class Cf>
+struct Pdl {
+    static constexpr bool kCluster = Cf::N0 >= 256;
+    static constexpr int kParts = kCluster ? 1 : Cf::C;
+    static int batch_block(int64_t batch, int cin) {
+        int bb = (int)batch;
+        while (bb > 1 && (size_t)kParts * bb * cin * 16 > kXpBudget) bb = (bb + 1) / 2;
+        return bb;
+    }
+    static size_t smem_b(fno_dtype_t dt, int cin, int ob, int bb) {
+        const size_t w2 = dt == FNO_F32 ? 16 : 8;
+        return ((size_t)cin * ob * w2 + 15) / 16 * 16 + (size_t)kParts * bb * cin * 16;
+    }
+    static size_t part_bytes(const Geom &g, int64_t batch, int cin) {
+        return (size_t)kParts * batch * cin * g.nkept * sizeof(float2);
+    }
+    template <typename T>
+    static cudaError_t init(Plan &p) {
+        const size_t w2 = p.dtype == FNO_F32 ? 16 : 8;
+        int ob = p.cout;
+        while (ob > 1 && (size_t)p.cin * ob * w2 > kWsBudget) ob = (ob + 1) / 2;
+        const int bb = batch_block(p.batch, p.cin);
+        const size_t sa = Cf::kSmemTw + Cf::kSmemA, sc = Cf::kSmemTw + Cf::kSmemC;
+        const size_t sb = smem_b(p.dtype, p.cin, ob, bb);
+        cudaError_t e = cudaFuncSetAttribute(k_phase_a<Cf, T, kCluster>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_phase_b<Cf, T, kParts>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sb);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_phase_c<Cf, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)sc);
+        p.fused_bb = bb;
+        p.fused_ob = ob;
+        p.fused_smem = sb;             // kernel B's; A and C use their fixed sizes
+        p.fused_grid = 0;
+        return e;
+    }
+    template <typename T>
+    static cudaError_t forward(const Plan &p, Args a, cudaStream_t s) {
+        a.bg = p.fused_bb;
+        a.ng = (int)((p.batch + a.bg - 1) / a.bg);
+        a.ob = p.fused_ob;
+        a.nob = (p.cout + a.ob - 1) / a.ob;
+        a.npairs = (int)(p.g.nkept / kG);
+        const int nA = (int)p.batch * p.cin * Cf::C;
+        const int nB = a.npairs * a.nob * a.ng;
+        const int nC = (int)p.batch * p.cout * Cf::C;
         cudaLaunchAttribute cl;
         cl.id = cudaLaunchAttributeClusterDimension;
-        cl.val.clusterDim.x = Cfg128::C;
+        cl.val.clusterDim.x = Cf::C;
         cl.val.clusterDim.y = 1;
         cl.val.clusterDim.z = 1;
         cudaLaunchConfig_t ca = {};
         ca.gridDim = dim3(nA);
         ca.blockDim = dim3(kNT);
-        ca.dynamicSmemBytes = Cfg128::kSmemTw + Cfg128::kSmemA;
+        ca.dynamicSmemBytes = Cf::kSmemTw + Cf::kSmemA;
         ca.stream = s;
-        ca.attrs = &cl;
-        ca.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&ca, k_phase_a<Cfg128, T>, a);
+        ca.attrs = kCluster ? &cl : nullptr;
+        ca.numAttrs = kCluster ? 1 : 0;
+        cudaError_t e = cudaLaunchKernelEx(&ca, k_phase_a<Cf, T, kCluster>, a);
         if (e != cudaSuccess) return e;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.blockDim = dim3(kNT);
+        cfg.stream = s;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(nB);
+        cfg.dynamicSmemBytes = p.fused_smem;
+        e = cudaLaunchKernelEx(&cfg, k_phase_b<Cf, T, kParts>, a);
+        if (e != cudaSuccess) return e;
+        cfg.gridDim = dim3(nC);
+        cfg.dynamicSmemBytes = Cf::kSmemTw + Cf::kSmemC;
+        e = cudaLaunchKernelEx(&cfg, k_phase_c<Cf, T>, a);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
     }
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kNT);
-    cfg.stream = s;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    cfg.gridDim = dim3(nB);
-    cfg.dynamicSmemBytes = p.fused_smem;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_phase_b<Cfg128, T>, a);
-    if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(nC);
-    cfg.dynamicSmemBytes = Cfg128::kSmemTw + Cfg128::kSmemC;
-    e = cudaLaunchKernelEx(&cfg, k_phase_c<Cfg128, T>, a);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+};
+
+enum Variant { kVarNone, kVarPdl128, kVarPdl256, kVarPersistent128, kVarTc128 };
+
+// Which fused kernel(s) a description runs on.
+Variant variant(const Geom &g, fno_dtype_t dtype, uint32_t flags) {
+    if (dtype != FNO_F32 && dtype != FNO_F16) return kVarNone;
+    if (is_cfg256(g)) return kVarPdl256;
+    if (!is_cfg128(g)) return kVarNone;
+    if (use_tc(g, dtype, flags)) return kVarTc128;
+    if (flags & FNO_PLAN_PERSISTENT) return kVarPersistent128;
+    return kVarPdl128;
+}
+
+bool fused_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout,
+                     uint32_t flags) {
+    const Variant v = variant(g, dtype, flags);
+    if (v == kVarNone) return false;
+    const int C = v == kVarPdl256 ? Cfg256::C : Cfg128::C;
+    if (batch * (int64_t)cin * C >= (1 << 30) || batch * (int64_t)cout * C >= (1 << 30))
+        return false;
+    if (v == kVarTc128)
+        return batch * (int64_t)(cin > cout ? cin : cout) * 128 < (1ll << 31) &&
+               (size_t)cin * 16 <= kTcXpBudget;
+    if (v == kVarPersistent128)
+        return smem_bytes(dtype, cin, b_shape(dtype, batch, cin, cout)) <= 200 * 1024;
+    // three-kernel variants: a weight slab of one output and one batch row must fit
+    const size_t w2 = dtype == FNO_F32 ? 16 : 8;
+    return (size_t)cin * w2 <= kWsBudget && (size_t)cin * 16 * Cfg128::C <= kXpBudget;
+}
+
+size_t fused_workspace_bytes(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout,
+                             uint32_t flags) {
+    const Variant v = variant(g, dtype, flags);
+    if (v == kVarTc128) return layout_tc(g, batch, cin, cout).total;
+    if (v == kVarPersistent128) return layout(g, batch, cin, cout).total;
+    const size_t part = v == kVarPdl256 ? Pdl<Cfg256>::part_bytes(g, batch, cin)
+                                        : Pdl<Cfg128>::part_bytes(g, batch, cin);
+    const size_t y = (size_t)batch * cout * g.nkept * sizeof(float2);
+    return ((part + 255) & ~size_t(255)) + ((y + 255) & ~size_t(255));
+}
+
+int fused_kernel_count(const Geom &g, fno_dtype_t dtype, int64_t, int, int, uint32_t flags) {
+    const Variant v = variant(g, dtype, flags);
+    return (v == kVarPdl128 || v == kVarPdl256) ? 3 : 1;
 }
 
 cudaError_t fused_plan_init(Plan &p) {
-    if (use_tc(p.g, p.dtype, p.flags)) {
+    const Variant v = variant(p.g, p.dtype, p.flags);
+    if (v == kVarPdl128)
+        return p.dtype == FNO_F32 ? Pdl<Cfg128>::init<float>(p) : Pdl<Cfg128>::init<__half>(p);
+    if (v == kVarPdl256)
+        return p.dtype == FNO_F32 ? Pdl<Cfg256>::init<float>(p) : Pdl<Cfg256>::init<__half>(p);
+    if (v == kVarTc128)
+    {
         if (!encoder()) return cudaErrorNotSupported;
         const BShape bs = b_shape_tc(p.batch, p.cin, p.cout);
         cudaError_t e = cudaFuncSetAttribute(tc::k_fused2d_tc,
@@ -1641,8 +1685,6 @@ cudaError_t fused_plan_init(Plan &p) {
         return cudaMemset(p.sync, 0, kSyncBytes);
     }
     const BShape bs = b_shape(p.dtype, p.batch, p.cin, p.cout);
-    if (use_pdl(p.g, p.dtype, p.flags))
-        return p.dtype == FNO_F32 ? pdl_init<float>(p, bs) : pdl_init<__half>(p, bs);
     const size_t smem = smem_bytes(p.dtype, p.cin, bs);
     void *fn = p.dtype == FNO_F32 ? kernel_ptr<float>() : kernel_ptr<__half>();
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1674,7 +1716,9 @@ void fused_plan_release(Plan &p) {
 }
 
 cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
-    if (use_tc(p.g, p.dtype, p.flags)) {
+    const Variant v = variant(p.g, p.dtype, p.flags);
+    if (v == kVarTc128)
+    {
         const Layout l = layout_tc(p.g, p.batch, p.cin, p.cout);
         CUtensorMap xmap, ymap;
         if (!encode_rows(&xmap, b.x, p.batch * p.cin * 128) ||
@@ -1708,6 +1752,27 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
             xmap, ymap, a, static_cast<const float4 *>(p.fused_tables));
         return cudaGetLastError();
     }
+    if (v == kVarPdl128 || v == kVarPdl256) {
+        const size_t part = v == kVarPdl256 ? Pdl<Cfg256>::part_bytes(p.g, p.batch, p.cin)
+                                            : Pdl<Cfg128>::part_bytes(p.g, p.batch, p.cin);
+        Args a{};
+        a.x = b.x;
+        a.w = b.w;
+        a.y = b.y;
+        a.part = static_cast<float2 *>(b.ws);
+        a.Y = reinterpret_cast<float2 *>(static_cast<char *>(b.ws) + ((part + 255) & ~size_t(255)));
+        a.tw0 = p.tw[0];
+        a.tw1 = p.tw[1];
+        a.err = p.dev_err;
+        a.batch = (int)p.batch;
+        a.cin = p.cin;
+        a.cout = p.cout;
+        if (v == kVarPdl256)
+            return p.dtype == FNO_F32 ? Pdl<Cfg256>::forward<float>(p, a, s)
+                                      : Pdl<Cfg256>::forward<__half>(p, a, s);
+        return p.dtype == FNO_F32 ? Pdl<Cfg128>::forward<float>(p, a, s)
+                                  : Pdl<Cfg128>::forward<__half>(p, a, s);
+    }
     const Layout l = layout(p.g, p.batch, p.cin, p.cout);
     Args a{};
     a.x = b.x;
@@ -1735,8 +1800,6 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
         a.wbytes = p.weight_bytes;
         a.wslice = kWeightPrefetch ? (unsigned)(((p.weight_bytes + nA - 1) / nA + 15) / 16 * 16) : 0u;
     }
-    if (use_pdl(p.g, p.dtype, p.flags))
-        return p.dtype == FNO_F32 ? pdl_forward<float>(p, a, s) : pdl_forward<__half>(p, a, s);
     const int total = (int)p.batch * (p.cin + p.cout) * Cfg128::C + a.ng * a.npairs * a.nob;
     const int grid = p.fused_grid < total ? p.fused_grid : total;
     if (p.dtype == FNO_F32)

@@ -28,6 +28,7 @@ SMALL = [
     ((64, 64), (16, 16), 2, 8, 8, "f32"),
     ((256, 256), (32, 32), 1, 8, 8, "f16"),
     ((256, 256), (32, 32), 2, 3, 5, "f16"),
+    ((256, 256), (32, 32), 3, 4, 2, "f32"),
     ((64, 64), (8, 8), 2, 4, 6, "f16"),
     ((64, 64, 64), (16, 16, 16), 1, 4, 4, "f32"),
     ((8, 8, 8), (2, 3, 4), 2, 3, 2, "f32"),
