@@ -1,0 +1,394 @@
+// fno_fused3d.cu -- the 3-D spectral-convolution layer (a volume N0 x N1 x N2,
+// 2*M0 x 2*M1 x M2 kept modes in four corner blocks) as three kernels chained
+// by programmatic dependent launch, the steps of the TurboFNO article
+// (gsyq.cn/news/457482) §2.1-§2.3 with the volume's intermediates kept in
+// registers, shared memory and L2.
+//
+//   kernel A  (volume, chunk c), the C0 chunk-CTAs of a volume form a cluster.
+//     A CTA takes the planes i0 = c + C0 t (t < R0 = N0 / C0) of one input
+//     volume one after another through a cp.async ring of shared-memory
+//     stages.  Each plane gets the truncated 2-D transform of the 2-D kernels
+//     (row DFT over the last axis keeping M2 bins, column DFT over axis 1
+//     keeping 2*M1 rows, with the whole plane as one chunk), and its kept
+//     modes are folded into an R0-point DFT over t held in registers:
+//         P_c[r] = sum_t S(c + C0 t) W_R0^{r t}.
+//     Since W_N0^{f (c + C0 t)} = W_N0^{f c} W_R0^{f t}, the axis-0 transform
+//     of the volume is X[f] = sum_c W_N0^{f c} P_c[f mod R0] (one decimation-
+//     in-time step); the cluster's CTAs evaluate it through distributed shared
+//     memory, each for one C0-th of the plane modes, and write X once.
+//   kernel B  the per-mode channel mixing shared with the 2-D kernels: every
+//     item reads its weight slab once for all batch rows.
+//   kernel C  (volume, chunk c).  Z_c[r] = sum_{f = r mod R0} Y[f] conj(W_N0^{f c});
+//     an R0-point inverse DFT over r gives the 2-D spectra of the planes
+//     c + C0 t, and each plane's inverse (column transform back to N1 rows,
+//     then the half-spectrum row transform with c(0) = 1, c(k) = 2 and the
+//     1/(N0 N1 N2) scale) is stored.
+#include "fno_fused_dev.cuh"
+
+namespace fno {
+namespace {
+
+template <int N0_, int N1_, int N2_, int M0_, int M1_, int M2_, int C0_, int Q_, int B2_>
+struct Cfg3 {
+    static constexpr int N0 = N0_, N1 = N1_, N2 = N2_, M0 = M0_, M1 = M1_, M2 = M2_;
+    static constexpr int C0 = C0_;                 // chunk-CTAs per volume (one cluster)
+    static constexpr int R0 = N0 / C0;             // planes per chunk: i0 = c + C0 t
+    static constexpr int K0 = 2 * M0;              // kept rows on axis 0
+    using Pl = Cfg<N1, N2, M1, M2, N1, Q_, B2_>;   // one plane as a single chunk
+    static constexpr int NKP = Pl::NK;             // kept modes per plane, [2 M1][M2]
+    static constexpr int NK = K0 * NKP;            // kept modes per volume, [2 M0][2 M1][M2]
+    static constexpr int QT = NKP / kNT;           // plane modes per thread
+    static constexpr int KR = K0 / R0;             // kept rows per residue mod R0
+    static constexpr int kCols = NKP / C0;         // plane modes each CTA reduces
+    static constexpr int kStages = 3;              // plane ring depth
+    static_assert(N0 % C0 == 0 && M0 % R0 == 0, "kept rows j0 = r + R0 m share residue r");
+    static_assert(NKP % kNT == 0 && NKP % C0 == 0 && (R0 * kCols) % kNT == 0, "tiling");
+    static_assert(C0 >= 2 && C0 <= 8, "portable cluster");
+    static_assert(M2 % kG == 0, "mode pairs stay in one kept row");
+    static_assert(Pl::C == 1, "the plane transform covers the whole plane");
+
+    // weights: block b = h0 + 2 h1 (h_a = 1 for the high kept rows on axis a),
+    // each M0 x M1 x M2 modes
+    static constexpr size_t MBLK = (size_t)M0 * M1 * M2;
+    __device__ static void wmap(int o, int &blk, int &local) {
+        const int j0 = o / NKP, rest = o % NKP;
+        const int j1 = rest / M2, k = rest % M2;
+        const int h0 = j0 >= M0 ? 1 : 0, h1 = j1 >= M1 ? 1 : 0;
+        blk = h0 | (h1 << 1);
+        local = ((j0 - h0 * M0) * M1 + (j1 - h1 * M1)) * M2 + k;
+    }
+
+    // shared memory: twiddles W_N1 [N1], W_N2^{n1 k} [P][TS], W_N0 [N0]
+    static constexpr size_t kSmemTw = ((N1 + Pl::P * Pl::TS + N0) * 8 + 15) / 16 * 16;
+    template <typename T>
+    static constexpr size_t stage_bytes() { return (size_t)N1 * Pl::XS * sizeof(T); }
+    template <typename T>
+    static constexpr size_t ring_bytes() {
+        // the ring also holds the chunk's residues [R0][NKP] at the end
+        return kStages * stage_bytes<T>() > (size_t)R0 * NKP * 8 ? kStages * stage_bytes<T>()
+                                                                : (size_t)R0 * NKP * 8;
+    }
+    template <typename T>
+    static constexpr size_t smem_a() { return kSmemTw + ring_bytes<T>() + (size_t)N1 * Pl::ZS * 8; }
+    static constexpr size_t kSmemC = kSmemTw + (size_t)R0 * NKP * 8 + (size_t)N1 * M2 * 8 +
+                                     (size_t)Pl::A * Pl::B2 * M2 * 8 + (size_t)N1 * Pl::ZS * 8;
+    static_assert(stage_bytes<float>() % 16 == 0 && stage_bytes<__half>() % 16 == 0, "align");
+    static_assert((size_t)Pl::A * Pl::B2 * M2 * 8 <= stage_bytes<__half>(),
+                  "the column pass works in the stage of its plane");
+};
+
+using Cfg3d64 = Cfg3<64, 64, 64, 16, 16, 16, 8, 16, 8>;
+
+// Twiddles of the 3-D layer into shared memory: the plane transform's tables
+// (W_N1 for axis 1, W_N2^{n1 k} per row lane) and W_N0 for axis 0.
+template <class C3>
+__device__ __forceinline__ Tw load_tw3(const Args &a, char *smem, const float2 **twa) {
+    using Pl = typename C3::Pl;
+    float2 *t0 = reinterpret_cast<float2 *>(smem);
+    float2 *t1 = t0 + C3::N1;
+    float2 *ta = t1 + Pl::P * Pl::TS;
+    for (int e = threadIdx.x; e < C3::N1; e += kNT) t0[e] = a.tw1[e];
+    for (int e = threadIdx.x; e < Pl::P * Pl::TS; e += kNT) {
+        const int n1 = e / Pl::TS, k = e % Pl::TS;
+        t1[e] = a.tw2[(n1 * k) & (C3::N2 - 1)];
+    }
+    for (int e = threadIdx.x; e < C3::N0; e += kNT) ta[e] = a.tw0[e];
+    *twa = ta;
+    return Tw{t0, t1};
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float2 ld_dsmem(uint32_t local, int rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+                 : "=f"(v.x), "=f"(v.y) : "r"(remote) : "memory");
+    return v;
+}
+
+// Frequency of kept row j on axis 0.
+template <class C3>
+__device__ __forceinline__ int freq0(int j) {
+    return j < C3::M0 ? j : C3::N0 - C3::K0 + j;
+}
+
+// grid: volumes x C0 CTAs, clusters of C0 along x (cluster rank = blockIdx.x % C0)
+template <class C3, typename T>
+__global__ void __launch_bounds__(kNT) k_phase_a3(Args a) {
+    using Pl = typename C3::Pl;
+    constexpr int N0 = C3::N0, N1 = C3::N1, N2 = C3::N2, C0 = C3::C0, R0 = C3::R0;
+    constexpr int NKP = C3::NKP, QT = C3::QT, S = C3::kStages;
+    constexpr size_t kStage = C3::template stage_bytes<T>();
+    extern __shared__ __align__(16) char smem[];
+    const float2 *twa;
+    const Tw tw = load_tw3<C3>(a, smem, &twa);
+    char *ring = smem + C3::kSmemTw;
+    float2 *zs = reinterpret_cast<float2 *>(ring + C3::template ring_bytes<T>());   // [N1][ZS]
+    const int vol = blockIdx.x / C0, c = blockIdx.x % C0;
+    const T *src = static_cast<const T *>(a.x) + (size_t)vol * N0 * N1 * N2;
+    pdl_trigger();                               // kernel B may start fetching weights
+
+    // plane c + C0 t into stage t % S, rows padded to Pl::XS samples
+    auto issue = [&](int t) {
+        T *dst = reinterpret_cast<T *>(ring + (t % S) * kStage);
+        const T *p = src + (size_t)(c + C0 * t) * N1 * N2;
+        constexpr int kPer = 16 / (int)sizeof(T);
+        constexpr int kRow = N2 / kPer;
+        for (int e = threadIdx.x; e < N1 * kRow; e += kNT) {
+            const int row = e / kRow, s = e % kRow;
+            cp_async16(dst + row * Pl::XS + s * kPer, p + (size_t)row * N2 + s * kPer);
+        }
+    };
+#pragma unroll
+    for (int t = 0; t < S - 1; ++t) {
+        if (t < R0) issue(t);
+        cp_async_commit();
+    }
+    float2 acc[R0][QT];
+#pragma unroll
+    for (int r = 0; r < R0; ++r)
+#pragma unroll
+        for (int q = 0; q < QT; ++q) acc[r][q] = make_float2(0.f, 0.f);
+
+    for (int t = 0; t < R0; ++t) {
+        // the stage refilled here held plane t - 1, released by the barrier that
+        // ended the previous iteration
+        if (t + S - 1 < R0) issue(t + S - 1);
+        cp_async_commit();
+        asm volatile("cp.async.wait_group %0;" ::"n"(S - 1) : "memory");
+        __syncthreads();                         // plane t is in its stage
+        const T *xs = reinterpret_cast<const T *>(ring + (t % S) * kStage);
+        a_row_dft<Pl, T>(xs, zs, tw);
+        __syncthreads();
+        float2 *ss = reinterpret_cast<float2 *>(ring + (t % S) * kStage);   // plane t consumed
+        a_col_fft<Pl>(zs, ss);
+        __syncthreads();
+        float2 wr[R0];                           // W_R0^{r t} = W_N0^{C0 r t}
+#pragma unroll
+        for (int r = 0; r < R0; ++r) wr[r] = twa[(C0 * r * t) & (N0 - 1)];
+#pragma unroll
+        for (int q = 0; q < QT; ++q) {
+            const float2 v = a_kept_mode<Pl>(ss, threadIdx.x + q * kNT, 0, tw);
+#pragma unroll
+            for (int r = 0; r < R0; ++r) cmac(acc[r][q], v, wr[r]);
+        }
+        __syncthreads();
+    }
+
+    // residues to shared memory (over the ring), then the cluster's combine
+    float2 *pm = reinterpret_cast<float2 *>(ring);   // [R0][NKP]
+#pragma unroll
+    for (int r = 0; r < R0; ++r)
+#pragma unroll
+        for (int q = 0; q < QT; ++q) pm[r * NKP + threadIdx.x + q * kNT] = acc[r][q];
+    cluster_sync();
+    const uint32_t local = smem_addr(pm);
+    float2 *X = a.part + (size_t)vol * C3::NK;
+    for (int u = threadIdx.x; u < R0 * C3::kCols; u += kNT) {
+        const int r = u / C3::kCols, col = c * C3::kCols + u % C3::kCols;
+        float2 v[C0];
+#pragma unroll
+        for (int cc = 0; cc < C0; ++cc) v[cc] = ld_dsmem(local + (uint32_t)(r * NKP + col) * 8, cc);
+#pragma unroll
+        for (int m = 0; m < C3::KR; ++m) {
+            const int j0 = r + R0 * m, f0 = freq0<C3>(j0);
+            float2 s = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int cc = 0; cc < C0; ++cc) cmac(s, v[cc], twa[(f0 * cc) & (N0 - 1)]);
+            __stcg(X + (size_t)j0 * NKP + col, s);
+        }
+    }
+    cluster_sync();                              // peers may still read this CTA's residues
+}
+
+// grid: volumes x C0 CTAs
+template <class C3, typename T>
+__global__ void __launch_bounds__(kNT) k_phase_c3(Args a) {
+    using Pl = typename C3::Pl;
+    constexpr int N0 = C3::N0, N1 = C3::N1, N2 = C3::N2, C0 = C3::C0, R0 = C3::R0;
+    constexpr int NKP = C3::NKP, QT = C3::QT, M2 = C3::M2;
+    extern __shared__ __align__(16) char smem[];
+    const float2 *twa;
+    const Tw tw = load_tw3<C3>(a, smem, &twa);
+    float2 *spec = reinterpret_cast<float2 *>(smem + C3::kSmemTw);   // [R0][NKP]
+    float2 *vs = spec + R0 * NKP;                                    // [N1][M2]
+    float2 *ss = vs + N1 * M2;                                       // [A][B2][M2]
+    float2 *zo = ss + Pl::A * Pl::B2 * M2;                           // [N1][ZS]
+    __syncthreads();
+    pdl_wait();                                  // kernel B's mixed modes are complete
+    const int vol = blockIdx.x / C0, c = blockIdx.x % C0;
+    const float2 *Yv = a.Y + (size_t)vol * C3::NK;
+
+    // 1. Z[r] = sum_m Y[r + R0 m] conj(W_N0^{f c}) for this thread's plane modes,
+    //    then the R0-point inverse DFT over r: spectra of planes c + C0 t
+    float2 z[QT][R0];
+#pragma unroll
+    for (int r = 0; r < R0; ++r) {
+#pragma unroll
+        for (int q = 0; q < QT; ++q) z[q][r] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m < C3::KR; ++m) {
+            const int j0 = r + R0 * m;
+            const float2 w = twa[(freq0<C3>(j0) * c) & (N0 - 1)];
+            const float2 wc = make_float2(w.x, -w.y);
+#pragma unroll
+            for (int q = 0; q < QT; ++q)
+                cmac(z[q][r], __ldcg(Yv + (size_t)j0 * NKP + threadIdx.x + q * kNT), wc);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < QT; ++q) {
+        fft::fft_dif<R0, 1>(z[q]);
+#pragma unroll
+        for (int t = 0; t < R0; ++t)
+            spec[t * NKP + threadIdx.x + q * kNT] = z[q][fft::bitrev(t, fft::ilog2(R0))];
+    }
+    __syncthreads();
+
+    // 2. every plane of the chunk: column inverse, row inverse, store
+    const float scale = 1.0f / ((float)N0 * (float)N1 * (float)N2);
+    T *dst = static_cast<T *>(a.y) + (size_t)vol * N0 * N1 * N2;
+    for (int t = 0; t < R0; ++t) {
+        c_residues<Pl>(spec + t * NKP, vs, 0, tw);
+        __syncthreads();
+        c_col_ifft<Pl>(vs, ss);
+        __syncthreads();
+        c_col_combine<Pl>(ss, zo, tw);
+        __syncthreads();
+        // zo is rewritten two barriers after this pass, vs and ss earlier ones
+        c_row_store<Pl, T>(zo, dst + (size_t)(c + C0 * t) * N1 * N2, 0, tw, scale);
+    }
+}
+
+template <class C3>
+struct Pdl3 {
+    static int batch_block(int64_t batch, int cin) {
+        int bb = (int)batch;
+        while (bb > 1 && (size_t)bb * cin * 16 > kXpBudget) bb = (bb + 1) / 2;
+        return bb;
+    }
+    static int out_block(fno_dtype_t dt, int cin, int cout) {
+        const size_t w2 = dt == FNO_F32 ? 16 : 8;
+        int ob = cout;
+        while (ob > 1 && (size_t)cin * ob * w2 > kWsBudget) ob = (ob + 1) / 2;
+        return ob;
+    }
+    static size_t smem_b(fno_dtype_t dt, int cin, int ob, int bb) {
+        const size_t w2 = dt == FNO_F32 ? 16 : 8;
+        return ((size_t)cin * ob * w2 + 15) / 16 * 16 + (size_t)bb * cin * 16;
+    }
+    template <typename T>
+    static cudaError_t init(Plan &p) {
+        const int ob = out_block(p.dtype, p.cin, p.cout), bb = batch_block(p.batch, p.cin);
+        cudaError_t e = cudaFuncSetAttribute(k_phase_a3<C3, T>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)C3::template smem_a<T>());
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_phase_b<C3, T, 1>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem_b(p.dtype, p.cin, ob, bb));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_phase_c3<C3, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)C3::kSmemC);
+        p.fused_bb = bb;
+        p.fused_ob = ob;
+        p.fused_smem = smem_b(p.dtype, p.cin, ob, bb);
+        p.fused_grid = 0;
+        return e;
+    }
+    template <typename T>
+    static cudaError_t forward(const Plan &p, Args a, cudaStream_t s) {
+        a.bg = p.fused_bb;
+        a.ng = (int)((p.batch + a.bg - 1) / a.bg);
+        a.ob = p.fused_ob;
+        a.nob = (p.cout + a.ob - 1) / a.ob;
+        a.npairs = C3::NK / kG;
+        cudaLaunchAttribute cl;
+        cl.id = cudaLaunchAttributeClusterDimension;
+        cl.val.clusterDim.x = C3::C0;
+        cl.val.clusterDim.y = 1;
+        cl.val.clusterDim.z = 1;
+        cudaLaunchConfig_t ca = {};
+        ca.gridDim = dim3((unsigned)(p.batch * p.cin * C3::C0));
+        ca.blockDim = dim3(kNT);
+        ca.dynamicSmemBytes = C3::template smem_a<T>();
+        ca.stream = s;
+        ca.attrs = &cl;
+        ca.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&ca, k_phase_a3<C3, T>, a);
+        if (e != cudaSuccess) return e;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.blockDim = dim3(kNT);
+        cfg.stream = s;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3((unsigned)(a.npairs * a.nob * a.ng));
+        cfg.dynamicSmemBytes = p.fused_smem;
+        e = cudaLaunchKernelEx(&cfg, k_phase_b<C3, T, 1>, a);
+        if (e != cudaSuccess) return e;
+        cfg.gridDim = dim3((unsigned)(p.batch * p.cout * C3::C0));
+        cfg.dynamicSmemBytes = C3::kSmemC;
+        e = cudaLaunchKernelEx(&cfg, k_phase_c3<C3, T>, a);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
+};
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+}  // namespace
+
+bool fused3d_match(const Geom &g, fno_dtype_t dtype) {
+    using C3 = Cfg3d64;
+    return g.d == 3 && (dtype == FNO_F32 || dtype == FNO_F16) && g.n[0] == C3::N0 &&
+           g.n[1] == C3::N1 && g.n[2] == C3::N2 && g.m[0] == C3::M0 && g.m[1] == C3::M1 &&
+           g.m[2] == C3::M2;
+}
+
+bool fused3d_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout) {
+    using C3 = Cfg3d64;
+    if (!fused3d_match(g, dtype)) return false;
+    const size_t w2 = dtype == FNO_F32 ? 16 : 8;
+    // grids fit in x; one output's weight slab and one batch row of modes fit
+    // the mixing item's shared memory
+    return batch * (int64_t)(cin > cout ? cin : cout) * C3::C0 < (1ll << 31) &&
+           (int64_t)(C3::NK / kG) * cout * batch < (1ll << 31) &&
+           (size_t)cin * w2 <= kWsBudget && (size_t)cin * 16 <= kXpBudget;
+}
+
+size_t fused3d_workspace_bytes(const Geom &g, int64_t batch, int cin, int cout) {
+    return align256((size_t)batch * cin * g.nkept * sizeof(float2)) +
+           align256((size_t)batch * cout * g.nkept * sizeof(float2));
+}
+
+cudaError_t fused3d_plan_init(Plan &p) {
+    return p.dtype == FNO_F32 ? Pdl3<Cfg3d64>::init<float>(p) : Pdl3<Cfg3d64>::init<__half>(p);
+}
+
+cudaError_t fused3d_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
+    Args a{};
+    a.x = b.x;
+    a.w = b.w;
+    a.y = b.y;
+    a.part = static_cast<float2 *>(b.ws);
+    a.Y = reinterpret_cast<float2 *>(static_cast<char *>(b.ws) +
+                                     align256((size_t)p.batch * p.cin * p.g.nkept * sizeof(float2)));
+    a.tw0 = p.tw[0];
+    a.tw1 = p.tw[1];
+    a.tw2 = p.tw[2];
+    a.err = p.dev_err;
+    a.batch = (int)p.batch;
+    a.cin = p.cin;
+    a.cout = p.cout;
+    return p.dtype == FNO_F32 ? Pdl3<Cfg3d64>::forward<float>(p, a, s)
+                              : Pdl3<Cfg3d64>::forward<__half>(p, a, s);
+}
+
+}  // namespace fno

@@ -111,5 +111,13 @@ struct Buffers {
 size_t unfused_workspace_bytes(const Geom &g, int64_t batch, int cin, int cout);
 int unfused_kernel_count(const Geom &g);
 cudaError_t unfused_forward(const Plan &p, const Buffers &b, cudaStream_t s);
+// Single steps of the unfused path, for composite sequences: a DFT along one
+// full axis over the kept rows (forward) or back to every row (inverse), with
+// the (outer, N, inner) view of the tensor; and the per-mode mixing.
+cudaError_t launch_axis_forward(const float2 *in, float2 *out, int64_t outer, int n, int64_t inner,
+                                int m, const float2 *tw, int num_sms, cudaStream_t s);
+cudaError_t launch_axis_inverse(const float2 *in, float2 *out, int64_t outer, int n, int64_t inner,
+                                int m, const float2 *tw, int num_sms, cudaStream_t s);
+cudaError_t launch_mix(const Plan &p, const float2 *X, const void *w, float2 *Y, cudaStream_t s);
 
 }  // namespace fno

@@ -253,6 +253,40 @@ static cudaError_t unfused_forward_t(const Plan &p, const Buffers &bf, cudaStrea
     return cudaGetLastError();
 }
 
+cudaError_t launch_axis_forward(const float2 *in, float2 *out, int64_t outer, int n, int64_t inner,
+                                int m, const float2 *tw, int num_sms, cudaStream_t s) {
+    k_fwd_full<<<grid_for(outer * 2 * m * inner, num_sms), kThreads, 0, s>>>(in, out, outer, n,
+                                                                           inner, m, tw);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_axis_inverse(const float2 *in, float2 *out, int64_t outer, int n, int64_t inner,
+                                int m, const float2 *tw, int num_sms, cudaStream_t s) {
+    k_inv_full<<<grid_for(outer * n * inner, num_sms), kThreads, 0, s>>>(in, out, outer, n, inner,
+                                                                       m, tw);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mix(const Plan &p, const float2 *X, const void *w, float2 *Y, cudaStream_t s) {
+    const Geom &g = p.g;
+    KeptGeom kg;
+    kg.d = g.d;
+    for (int a = 0; a < FNO_MAX_NDIM; ++a) {
+        kg.kdim[a] = a < g.d ? g.kdim[a] : 1;
+        kg.m[a] = a < g.d ? g.m[a] : 1;
+    }
+    kg.nkept = g.nkept;
+    kg.mblk = g.mblk;
+    const int grid = grid_for(p.batch * p.cout * g.nkept, p.num_sms);
+    if (p.dtype == FNO_F32)
+        k_mix<float><<<grid, kThreads, 0, s>>>(X, static_cast<const float *>(w), Y, p.batch,
+                                              p.cin, p.cout, kg);
+    else
+        k_mix<__half><<<grid, kThreads, 0, s>>>(X, static_cast<const __half *>(w), Y, p.batch,
+                                               p.cin, p.cout, kg);
+    return cudaGetLastError();
+}
+
 cudaError_t unfused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
     return p.dtype == FNO_F32 ? unfused_forward_t<float>(p, b, s)
                               : unfused_forward_t<__half>(p, b, s);

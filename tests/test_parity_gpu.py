@@ -31,6 +31,8 @@ SMALL = [
     ((256, 256), (32, 32), 3, 4, 2, "f32"),
     ((64, 64), (8, 8), 2, 4, 6, "f16"),
     ((64, 64, 64), (16, 16, 16), 1, 4, 4, "f32"),
+    ((64, 64, 64), (16, 16, 16), 2, 5, 3, "f32"),
+    ((64, 64, 64), (16, 16, 16), 3, 3, 5, "f16"),
     ((8, 8, 8), (2, 3, 4), 2, 3, 2, "f32"),
     ((4, 8, 16), (2, 4, 9), 2, 2, 2, "f32"),
     ((32, 32, 32), (8, 8, 8), 2, 3, 4, "f16"),
@@ -125,6 +127,17 @@ def test_fused_and_unfused_agree_and_are_deterministic():
     assert np.array_equal(d, e), "two runs of the tensor-core plan differ"
     assert_close(a, c.astype(np.float64), "f32", "fused vs unfused")
     assert_close(d, c.astype(np.float64), "f32", "tensor cores vs unfused")
+
+
+def test_fused_3d_and_unfused_agree():
+    case = workloads.CASES["3d_f32"]
+    x, w = workloads.make_x(case), workloads.make_w(case)
+    a, ka = run_gpu(case, x, w)
+    b, _ = run_gpu(case, x, w)
+    c, kc = run_gpu(case, x, w, FNO_PLAN_UNFUSED)
+    assert ka == 3 and kc == 7
+    assert np.array_equal(a, b), "two runs of the same plan differ"
+    assert_close(a, c.astype(np.float64), "f32", "3-D fused vs unfused")
 
 
 def test_output_red_zones_untouched():
