@@ -68,7 +68,7 @@ size_t elem_bytes(fno_dtype_t t) { return t == FNO_F16 ? 2 : 4; }
 int choose_path(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout,
                 uint32_t flags) {
     if (flags & FNO_PLAN_UNFUSED) return kPathUnfused;
-    if (fused_supported(g, dtype, batch, cin, cout, flags)) return kPathFused2D;
+    if (fused_supported(g, dtype, batch, cin, cout, flags)) return kPathFused;
     return kPathUnfused;
 }
 

@@ -78,11 +78,6 @@ __device__ Item decode_ticket(const Args &a, int t) {
     return Item{-1, 0, 0, t0};
 }
 
-__device__ __forceinline__ unsigned long long trace_now() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
 // Trace stamps of one item, written by the thread that runs its serial part.
 struct TraceStamp {
     unsigned long long t_start = 0, t_ready = 0, t_compute = 0;
@@ -232,22 +227,27 @@ __device__ __forceinline__ Tw load_twiddles(const Args &a, char *smem) {
 template <class Cf, typename T, bool kCluster>
 __global__ void __launch_bounds__(kNT) k_phase_a(Args a) {
     extern __shared__ __align__(16) char smem[];
+    const unsigned long long t0 = a.trace ? trace_now() : 0;
     const Tw tw = load_twiddles<Cf>(a, smem);
     __syncthreads();
     pdl_trigger();
     const int item = blockIdx.x;                 // image * C + chunk
     phase_a<Cf, T, kCluster>(static_cast<const T *>(a.x), a.part, a.batch * a.cin, item / Cf::C,
                              item % Cf::C, smem + Cf::kSmemTw, tw);
+    cta_record(a, 0, 0, t0, t0);
 }
 
 template <class Cf, typename T>
 __global__ void __launch_bounds__(kNT) k_phase_c(Args a) {
     extern __shared__ __align__(16) char smem[];
+    const unsigned long long t0 = a.trace ? trace_now() : 0;
     const Tw tw = load_twiddles<Cf>(a, smem);
     __syncthreads();
     pdl_wait();                                  // kernel B's mixed modes are complete
+    const unsigned long long t1 = a.trace ? trace_now() : 0;
     const int item = blockIdx.x;
     phase_c<Cf, T>(a.Y, static_cast<T *>(a.y), item / Cf::C, item % Cf::C, smem + Cf::kSmemTw, tw);
+    cta_record(a, 2, a.trace_c, t0, t1);
 }
 
 // ---------------------------------------------------------------------------
@@ -938,6 +938,12 @@ struct Pdl {
         p.fused_ob = ob;
         p.fused_smem = sb;             // kernel B's; A and C use their fixed sizes
         p.fused_grid = 0;
+        if (e == cudaSuccess && (p.flags & FNO_PLAN_TRACE)) {
+            const size_t nB = (size_t)(p.g.nkept / kG) * ((p.cout + ob - 1) / ob) *
+                              ((p.batch + bb - 1) / bb);
+            p.trace_records = (size_t)p.batch * (p.cin + p.cout) * Cf::C + nB;
+            e = cudaMalloc(&p.trace, p.trace_records * sizeof(fno_trace_record_t));
+        }
         return e;
     }
     template <typename T>
@@ -950,6 +956,9 @@ struct Pdl {
         const int nA = (int)p.batch * p.cin * Cf::C;
         const int nB = a.npairs * a.nob * a.ng;
         const int nC = (int)p.batch * p.cout * Cf::C;
+        a.trace = p.trace;
+        a.trace_b = nA;
+        a.trace_c = nA + nB;
         cudaLaunchAttribute cl;
         cl.id = cudaLaunchAttributeClusterDimension;
         cl.val.clusterDim.x = Cf::C;
@@ -973,10 +982,12 @@ struct Pdl {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         cfg.gridDim = dim3(nB);
+        cfg.blockDim = dim3(kNTB);
         cfg.dynamicSmemBytes = p.fused_smem;
         e = cudaLaunchKernelEx(&cfg, k_phase_b<Cf, T, kParts>, a);
         if (e != cudaSuccess) return e;
         cfg.gridDim = dim3(nC);
+        cfg.blockDim = dim3(kNT);
         cfg.dynamicSmemBytes = Cf::kSmemTw + Cf::kSmemC;
         e = cudaLaunchKernelEx(&cfg, k_phase_c<Cf, T>, a);
         if (e != cudaSuccess) return e;
@@ -984,11 +995,12 @@ struct Pdl {
     }
 };
 
-enum Variant { kVarNone, kVarPdl128, kVarPdl256, kVarPersistent128, kVarTc128, kVarPdl3d };
+enum Variant { kVarNone, kVarPdl128, kVarPdl256, kVarPersistent128, kVarTc128, kVarPdl3d, kVarOne1d };
 
 // Which fused kernel(s) a description runs on.
 Variant variant(const Geom &g, fno_dtype_t dtype, uint32_t flags) {
     if (dtype != FNO_F32 && dtype != FNO_F16) return kVarNone;
+    if (g.d == 1) return kVarOne1d;
     if (fused3d_match(g, dtype)) return kVarPdl3d;
     if (is_cfg256(g)) return kVarPdl256;
     if (!is_cfg128(g)) return kVarNone;
@@ -1002,6 +1014,7 @@ bool fused_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, i
     const Variant v = variant(g, dtype, flags);
     if (v == kVarNone) return false;
     if (v == kVarPdl3d) return fused3d_supported(g, dtype, batch, cin, cout);
+    if (v == kVarOne1d) return fused1d_supported(g, dtype, batch, cin, cout);
     const int C = v == kVarPdl256 ? Cfg256::C : Cfg128::C;
     if (batch * (int64_t)cin * C >= (1 << 30) || batch * (int64_t)cout * C >= (1 << 30))
         return false;
@@ -1019,6 +1032,7 @@ size_t fused_workspace_bytes(const Geom &g, fno_dtype_t dtype, int64_t batch, in
                              uint32_t flags) {
     const Variant v = variant(g, dtype, flags);
     if (v == kVarPdl3d) return fused3d_workspace_bytes(g, batch, cin, cout);
+    if (v == kVarOne1d) return 0;
     if (v == kVarTc128) return layout_tc(g, batch, cin, cout).total;
     if (v == kVarPersistent128) return layout(g, batch, cin, cout).total;
     const size_t part = v == kVarPdl256 ? Pdl<Cfg256>::part_bytes(g, batch, cin)
@@ -1035,6 +1049,7 @@ int fused_kernel_count(const Geom &g, fno_dtype_t dtype, int64_t, int, int, uint
 cudaError_t fused_plan_init(Plan &p) {
     const Variant v = variant(p.g, p.dtype, p.flags);
     if (v == kVarPdl3d) return fused3d_plan_init(p);
+    if (v == kVarOne1d) return cudaSuccess;
     if (v == kVarPdl128)
         return p.dtype == FNO_F32 ? Pdl<Cfg128>::init<float>(p) : Pdl<Cfg128>::init<__half>(p);
     if (v == kVarPdl256)
@@ -1108,6 +1123,7 @@ void fused_plan_release(Plan &p) {
 cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
     const Variant v = variant(p.g, p.dtype, p.flags);
     if (v == kVarPdl3d) return fused3d_forward(p, b, s);
+    if (v == kVarOne1d) return fused1d_forward(p, b, s);
     if (v == kVarTc128)
     {
         const Layout l = layout_tc(p.g, p.batch, p.cin, p.cout);

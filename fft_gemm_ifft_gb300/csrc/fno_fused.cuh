@@ -19,6 +19,10 @@ cudaError_t fused_plan_init(Plan &p);
 void fused_plan_release(Plan &p);
 cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s);
 
+// The 1-D layer's kernel (one cluster per sample).
+bool fused1d_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout);
+cudaError_t fused1d_forward(const Plan &p, const Buffers &b, cudaStream_t s);
+
 // The 3-D layer's kernels (64 x 64 x 64, 16 x 16 x 16 modes per corner block).
 bool fused3d_match(const Geom &g, fno_dtype_t dtype);
 bool fused3d_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout);

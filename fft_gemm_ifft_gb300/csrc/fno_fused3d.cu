@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(kNT) k_phase_a3(Args a) {
     constexpr int NKP = C3::NKP, QT = C3::QT, S = C3::kStages;
     constexpr size_t kStage = C3::template stage_bytes<T>();
     extern __shared__ __align__(16) char smem[];
+    const unsigned long long t0 = a.trace ? trace_now() : 0;
     const float2 *twa;
     const Tw tw = load_tw3<C3>(a, smem, &twa);
     char *ring = smem + C3::kSmemTw;
@@ -203,6 +204,7 @@ __global__ void __launch_bounds__(kNT) k_phase_a3(Args a) {
         }
     }
     cluster_sync();                              // peers may still read this CTA's residues
+    cta_record(a, 0, 0, t0, t0);
 }
 
 // grid: volumes x C0 CTAs
@@ -212,6 +214,7 @@ __global__ void __launch_bounds__(kNT) k_phase_c3(Args a) {
     constexpr int N0 = C3::N0, N1 = C3::N1, N2 = C3::N2, C0 = C3::C0, R0 = C3::R0;
     constexpr int NKP = C3::NKP, QT = C3::QT, M2 = C3::M2;
     extern __shared__ __align__(16) char smem[];
+    const unsigned long long t0 = a.trace ? trace_now() : 0;
     const float2 *twa;
     const Tw tw = load_tw3<C3>(a, smem, &twa);
     float2 *spec = reinterpret_cast<float2 *>(smem + C3::kSmemTw);   // [R0][NKP]
@@ -220,6 +223,7 @@ __global__ void __launch_bounds__(kNT) k_phase_c3(Args a) {
     float2 *zo = ss + Pl::A * Pl::B2 * M2;                           // [N1][ZS]
     __syncthreads();
     pdl_wait();                                  // kernel B's mixed modes are complete
+    const unsigned long long t1 = a.trace ? trace_now() : 0;
     const int vol = blockIdx.x / C0, c = blockIdx.x % C0;
     const float2 *Yv = a.Y + (size_t)vol * C3::NK;
 
@@ -262,6 +266,7 @@ __global__ void __launch_bounds__(kNT) k_phase_c3(Args a) {
         // zo is rewritten two barriers after this pass, vs and ss earlier ones
         c_row_store<Pl, T>(zo, dst + (size_t)(c + C0 * t) * N1 * N2, 0, tw, scale);
     }
+    cta_record(a, 2, a.trace_c, t0, t1);
 }
 
 template <class C3>
@@ -298,6 +303,12 @@ struct Pdl3 {
         p.fused_ob = ob;
         p.fused_smem = smem_b(p.dtype, p.cin, ob, bb);
         p.fused_grid = 0;
+        if (e == cudaSuccess && (p.flags & FNO_PLAN_TRACE)) {
+            const size_t nB = (size_t)(C3::NK / kG) * ((p.cout + ob - 1) / ob) *
+                              ((p.batch + bb - 1) / bb);
+            p.trace_records = (size_t)p.batch * (p.cin + p.cout) * C3::C0 + nB;
+            e = cudaMalloc(&p.trace, p.trace_records * sizeof(fno_trace_record_t));
+        }
         return e;
     }
     template <typename T>
@@ -307,6 +318,9 @@ struct Pdl3 {
         a.ob = p.fused_ob;
         a.nob = (p.cout + a.ob - 1) / a.ob;
         a.npairs = C3::NK / kG;
+        a.trace = p.trace;
+        a.trace_b = (int)(p.batch * p.cin * C3::C0);
+        a.trace_c = a.trace_b + a.npairs * a.nob * a.ng;
         cudaLaunchAttribute cl;
         cl.id = cudaLaunchAttributeClusterDimension;
         cl.val.clusterDim.x = C3::C0;
@@ -330,10 +344,12 @@ struct Pdl3 {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         cfg.gridDim = dim3((unsigned)(a.npairs * a.nob * a.ng));
+        cfg.blockDim = dim3(kNTB);
         cfg.dynamicSmemBytes = p.fused_smem;
         e = cudaLaunchKernelEx(&cfg, k_phase_b<C3, T, 1>, a);
         if (e != cudaSuccess) return e;
         cfg.gridDim = dim3((unsigned)(p.batch * p.cout * C3::C0));
+        cfg.blockDim = dim3(kNT);
         cfg.dynamicSmemBytes = C3::kSmemC;
         e = cudaLaunchKernelEx(&cfg, k_phase_c3<C3, T>, a);
         if (e != cudaSuccess) return e;

@@ -26,7 +26,14 @@ using fft::cscale;
 constexpr int kNT = 128;                        // threads per CTA
 constexpr long long kWaitTimeoutNs = 500000000;  // bounded device waits: 0.5 s
 constexpr int kG = 2;                           // kept modes per phase-B item
-constexpr size_t kWsBudget = 16u << 10;         // phase-B weight slab (bytes)
+#ifndef FNO_WS_BUDGET
+#define FNO_WS_BUDGET 16384
+#endif
+#ifndef FNO_B_THREADS
+#define FNO_B_THREADS 128
+#endif
+constexpr size_t kWsBudget = FNO_WS_BUDGET;      // phase-B weight slab (bytes)
+constexpr int kNTB = FNO_B_THREADS;              // threads of a three-kernel phase-B CTA
 constexpr size_t kXpBudget = 24u << 10;         // phase-B partial modes (bytes)
 
 // Counters shared by the CTAs of one launch (plan-owned, zero between
@@ -667,12 +674,39 @@ struct Args {
     int bg, ng;         // batch rows per group, groups
     int npairs;         // phase B: kept-mode pairs
     int ob, nob;        // phase B: outputs per item, output blocks
+    int trace_b, trace_c;   // three-kernel variants: first trace record of kernel B, C
 };
+
+__device__ __forceinline__ unsigned long long trace_now() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Three-kernel variants: one trace record per CTA, written once every thread of
+// the CTA is done (t_start: entry, t_ready: the wait for the previous kernel
+// returned).  A no-op unless the plan traces.
+__device__ __forceinline__ void cta_record(const Args &a, int phase, int first,
+                                           unsigned long long t_start,
+                                           unsigned long long t_ready) {
+    if (!a.trace) return;
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    fno_trace_record_t r;
+    r.item = ((unsigned)phase << 24) | (blockIdx.x & 0xFFFFFFu);
+    r.worker = smid;
+    r.t_start = t_start;
+    r.t_ready = t_ready;
+    r.t_compute = r.t_end = trace_now();
+    a.trace[first + blockIdx.x] = r;
+}
 
 // item = (pair * nob + output block) * batch blocks + batch block; a.bg = batch
 // rows per block, a.ng = batch blocks
 template <class Cf, typename T, int kParts>
-__global__ void __launch_bounds__(kNT) k_phase_b(Args a) {
+__global__ void __launch_bounds__(kNTB) k_phase_b(Args a) {
     extern __shared__ __align__(16) char smem[];
     int it = blockIdx.x;
     const int bblk = it % a.ng;
@@ -684,11 +718,14 @@ __global__ void __launch_bounds__(kNT) k_phase_b(Args a) {
     bi.b0 = bblk * a.bg;
     bi.nbb = min(a.bg, a.batch - bi.b0);
     const CtaGroup grp{(int)threadIdx.x};
-    phase_b_weights<Cf, T, kNT>(grp, static_cast<const T *>(a.w), a.cin, a.cout, bi, a.ob, smem);
+    const unsigned long long t0 = a.trace ? trace_now() : 0;
+    phase_b_weights<Cf, T, kNTB>(grp, static_cast<const T *>(a.w), a.cin, a.cout, bi, a.ob, smem);
     pdl_trigger();
     pdl_wait();                                  // kernel A's partial modes are complete
-    phase_b<Cf, T, kNT, CtaGroup, kParts>(grp, a.part, a.Y, a.cin, a.cout, a.batch * a.cin, bi,
+    const unsigned long long t1 = a.trace ? trace_now() : 0;
+    phase_b<Cf, T, kNTB, CtaGroup, kParts>(grp, a.part, a.Y, a.cin, a.cout, a.batch * a.cin, bi,
                                           a.ob, smem);
+    cta_record(a, 1, a.trace_b, t0, t1);
 }
 
 }  // namespace

@@ -57,7 +57,7 @@ struct Plan {
     size_t trace_records;         // records one forward call produces
 };
 
-enum { kPathUnfused = 0, kPathFused2D = 1, kPathFused1D = 2 };
+enum { kPathUnfused = 0, kPathFused = 1 };
 
 // --------------------------------------------------------------------------
 // Small device helpers

@@ -14,7 +14,6 @@ using namespace fno;
 
 namespace {
 
-constexpr int kThreads = 256;
 constexpr int kMaxCout = 8;
 
 struct Model {
@@ -31,59 +30,194 @@ __device__ __forceinline__ float gelu(float v) {
     return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
 }
 
-int grid_for(int64_t total) {
-    const int64_t blocks = (total + kThreads - 1) / kThreads;
-    return (int)(blocks < 65535 * 16 ? blocks : 65535 * 16);
+// ---------------------------------------------------------------------------
+// Register-tiled 1x1 linears.  A CTA of kTT threads owns kTP pixels of one
+// image and kTO output channels; the input channels are staged kTK at a time
+// in shared memory (cp.async, zero-filled past the edges), together with the
+// matching weight columns stored transposed.  Thread (og, pg) accumulates 4
+// outputs x 8 pixels (pixels pg*4.. and 64+pg*4..), so every k step is one
+// float4 weight load (a broadcast: a warp touches two og) and two float4
+// activation loads (conflict-free) for 32 FMAs.  The pixel count must be a
+// multiple of 4 (the 16-byte copies); channel counts are arbitrary.
+// ---------------------------------------------------------------------------
+constexpr int kTT = 256;   // threads per CTA
+constexpr int kTP = 128;   // pixels per tile
+constexpr int kTO = 64;    // output channels per tile
+constexpr int kTK = 64;    // input channels per shared-memory chunk
+
+struct TileSmem {
+    float a[kTK][kTP];     // activations [k][pixel]
+    float w[kTK][kTO];     // weights, transposed [k][output]
+    float red[kTT / 16][kTP];   // projection: partial sums of the 16 output groups
+};
+
+__device__ __forceinline__ void cp_async16(void *s, const void *g) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 ::"r"((unsigned)__cvta_generic_to_shared(s)), "l"(g) : "memory");
 }
 
-// a[b][c][p] = sum_j W[c][j] x[b][j][p] + bias[c]   (1x1 linear, channels-first)
-// optionally + add[b][c][p], optionally followed by GELU.
-__global__ void __launch_bounds__(kThreads)
-k_linear1x1(const float *__restrict__ x, const float *__restrict__ W,
-            const float *__restrict__ bias, const float *__restrict__ add,
-            float *__restrict__ out, int64_t batch, int cin, int cout, int64_t npix,
-            int apply_gelu) {
-    const int64_t total = batch * cout * npix;
-    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t p = idx % npix;
-        const int64_t t = idx / npix;
-        const int c = (int)(t % cout);
-        const int64_t b = t / cout;
-        const float *src = x + b * cin * npix + p;
-        const float *wr = W + (int64_t)c * cin;
-        float acc = bias[c];
-        for (int j = 0; j < cin; ++j) acc = fmaf(wr[j], src[(int64_t)j * npix], acc);
-        if (add) acc += add[idx];
-        out[idx] = apply_gelu ? gelu(acc) : acc;
+// Input channels [k0, k0 + kc) of pixels [p0, p0 + kTP) of one image (a_img),
+// and the weights W[o0 + o][k0 + k] (row length cin) of outputs o < no.
+__device__ void load_chunk(TileSmem &s, const float *__restrict__ a_img, int cin, int64_t npix,
+                           int64_t p0, int k0, int kc, const float *__restrict__ W, int o0,
+                           int no) {
+    const int tid = threadIdx.x;
+    for (int e = tid; e < kTK * (kTP / 4); e += kTT) {
+        const int k = e / (kTP / 4), g = e % (kTP / 4);
+        const int64_t px = p0 + 4 * g;
+        float *dst = &s.a[k][4 * g];
+        if (k < kc && px < npix)
+            cp_async16(dst, a_img + (int64_t)(k0 + k) * npix + px);
+        else
+            *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    for (int e = tid; e < kTK * kTO; e += kTT) {
+        const int k = e / kTO, o = e % kTO;
+        s.w[k][o] = (k < kc && o < no) ? W[(int64_t)(o0 + o) * cin + k0 + k] : 0.f;
+    }
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
 }
 
-// out[b][o][p] = sum_k P2[o][k] gelu(sum_c P1[k][c] a[b][c][p] + c1[k]) + c2[o]
-__global__ void __launch_bounds__(kThreads)
-k_projection(const float *__restrict__ a, const float *__restrict__ P1,
-             const float *__restrict__ c1, const float *__restrict__ P2,
-             const float *__restrict__ c2, float *__restrict__ out, int64_t batch, int width,
-             int hidden, int cout, int64_t npix) {
-    const int64_t total = batch * npix;
-    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t p = idx % npix;
-        const int64_t b = idx / npix;
-        const float *src = a + b * width * npix + p;
-        float acc[kMaxCout];
-        for (int o = 0; o < kMaxCout; ++o) acc[o] = o < cout ? c2[o] : 0.f;
-        for (int k = 0; k < hidden; ++k) {
-            float h = c1[k];
-            const float *wr = P1 + (int64_t)k * width;
-            for (int c = 0; c < width; ++c) h = fmaf(wr[c], src[(int64_t)c * npix], h);
-            h = gelu(h);
+// acc[i][j] += sum_k w[k][og*4 + i] a[k][pix(j)], pix(j) = pg*4 + j (j < 4), 64 + pg*4 + j - 4
+__device__ __forceinline__ void fma_chunk(const TileSmem &s, int kc, int og, int pg,
+                                          float (&acc)[4][8]) {
+#pragma unroll 4
+    for (int k = 0; k < kc; ++k) {
+        const float4 w4 = *reinterpret_cast<const float4 *>(&s.w[k][og * 4]);
+        const float4 a0 = *reinterpret_cast<const float4 *>(&s.a[k][pg * 4]);
+        const float4 a1 = *reinterpret_cast<const float4 *>(&s.a[k][64 + pg * 4]);
+        const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-            for (int o = 0; o < kMaxCout; ++o)
-                if (o < cout) acc[o] = fmaf(P2[o * hidden + k], h, acc[o]);
-        }
-        for (int o = 0; o < cout; ++o) out[(b * cout + o) * npix + p] = acc[o];
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(wv[i], av[j], acc[i][j]);
     }
+}
+
+// out[b][o][p] = act(sum_j W[o][j] x[b][j][p] + bias[o] (+ add[b][o][p]))
+// grid: (pixel tiles, output tiles, batch)
+__global__ void __launch_bounds__(kTT)
+k_linear_tiled(const float *__restrict__ x, const float *__restrict__ W,
+               const float *__restrict__ bias, const float *__restrict__ add,
+               float *__restrict__ out, int cin, int cout, int64_t npix, int apply_gelu) {
+    extern __shared__ __align__(16) char smem_raw[];
+    TileSmem &s = *reinterpret_cast<TileSmem *>(smem_raw);
+    const int64_t p0 = (int64_t)blockIdx.x * kTP;
+    const int o0 = blockIdx.y * kTO, no = min(kTO, cout - o0);
+    const int64_t b = blockIdx.z;
+    const int og = threadIdx.x / 16, pg = threadIdx.x % 16;
+    float acc[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    const float *a_img = x + b * cin * npix;
+    for (int k0 = 0; k0 < cin; k0 += kTK) {
+        const int kc = min(kTK, cin - k0);
+        load_chunk(s, a_img, cin, npix, p0, k0, kc, W, o0, no);
+        fma_chunk(s, kc, og, pg, acc);
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int o = og * 4 + i;
+        if (o >= no) continue;
+        const float bo = bias[o0 + o];
+        const int64_t row = (b * cout + o0 + o) * npix;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t px = p0 + h * 64 + pg * 4;
+            if (px >= npix) continue;
+            float4 v = make_float4(acc[i][4 * h] + bo, acc[i][4 * h + 1] + bo,
+                                   acc[i][4 * h + 2] + bo, acc[i][4 * h + 3] + bo);
+            if (add) {
+                const float4 q = __ldcs(reinterpret_cast<const float4 *>(add + row + px));
+                v.x += q.x; v.y += q.y; v.z += q.z; v.w += q.w;
+            }
+            if (apply_gelu) {
+                v.x = gelu(v.x); v.y = gelu(v.y); v.z = gelu(v.z); v.w = gelu(v.w);
+            }
+            *reinterpret_cast<float4 *>(out + row + px) = v;
+        }
+    }
+}
+
+// out[b][o][p] = sum_k P2[o][k] gelu(sum_c P1[k][c] a[b][c][p] + c1[k]) + c2[o], o < cout
+// grid: (pixel tiles, batch); the hidden units run in tiles of kTO; kCo >= cout
+// partial outputs are held per thread
+template <int kCo>
+__global__ void __launch_bounds__(kTT)
+k_projection_tiled(const float *__restrict__ a, const float *__restrict__ P1,
+                   const float *__restrict__ c1, const float *__restrict__ P2,
+                   const float *__restrict__ c2, float *__restrict__ out, int width, int hidden,
+                   int cout, int64_t npix) {
+    extern __shared__ __align__(16) char smem_raw[];
+    TileSmem &s = *reinterpret_cast<TileSmem *>(smem_raw);
+    const int64_t p0 = (int64_t)blockIdx.x * kTP;
+    const int64_t b = blockIdx.y;
+    const int og = threadIdx.x / 16, pg = threadIdx.x % 16;
+    const float *a_img = a + b * width * npix;
+    float part[kCo][8];
+#pragma unroll
+    for (int o = 0; o < kCo; ++o)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) part[o][j] = 0.f;
+    for (int h0 = 0; h0 < hidden; h0 += kTO) {
+        const int nh = min(kTO, hidden - h0);
+        float acc[4][8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+        for (int k0 = 0; k0 < width; k0 += kTK) {
+            const int kc = min(kTK, width - k0);
+            load_chunk(s, a_img, width, npix, p0, k0, kc, P1, h0, nh);
+            fma_chunk(s, kc, og, pg, acc);
+            __syncthreads();
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int h = og * 4 + i;
+            if (h >= nh) continue;
+            const float ch = c1[h0 + h];
+#pragma unroll
+            for (int o = 0; o < kCo; ++o) {
+                if (o >= cout) break;
+                const float p2 = P2[(int64_t)o * hidden + h0 + h];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) part[o][j] = fmaf(p2, gelu(acc[i][j] + ch), part[o][j]);
+            }
+        }
+    }
+    // sum the 16 output groups' partials of every pixel
+    for (int o = 0; o < cout; ++o) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float v = 0.f;
+#pragma unroll
+            for (int q = 0; q < kCo; ++q)
+                if (q == o) v = part[q][j];
+            s.red[og][(j < 4 ? 0 : 64) + pg * 4 + (j & 3)] = v;
+        }
+        __syncthreads();
+        if (threadIdx.x < kTP && p0 + threadIdx.x < npix) {
+            float v = c2[o];
+            for (int g = 0; g < kTT / 16; ++g) v += s.red[g][threadIdx.x];
+            out[(b * cout + o) * npix + p0 + threadIdx.x] = v;
+        }
+        __syncthreads();
+    }
+}
+
+using ProjFn = void (*)(const float *, const float *, const float *, const float *,
+                       const float *, float *, int, int, int, int64_t);
+ProjFn projection_kernel(int cout) {
+    if (cout <= 1) return k_projection_tiled<1>;
+    if (cout <= 2) return k_projection_tiled<2>;
+    if (cout <= 4) return k_projection_tiled<4>;
+    return k_projection_tiled<kMaxCout>;
 }
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -101,7 +235,7 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
     if (d->batch < 1 || d->cin_lift < 1 || d->width < 1 || d->nlayers < 1 || d->hidden < 1 ||
         d->cout < 1)
         return FNO_ERR_INVALID_ARG;
-    if (d->cout > kMaxCout) return FNO_ERR_UNSUPPORTED;
+    if (d->cout > kMaxCout || d->batch > 65535) return FNO_ERR_UNSUPPORTED;
     if (d->dtype != FNO_F32) return FNO_ERR_UNSUPPORTED;
     const int64_t n[2] = {d->h, d->w};
     size_t spec_ws = 0;
@@ -116,6 +250,16 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
     if (st != FNO_OK) {
         delete m;
         return st;
+    }
+    const int smem = (int)sizeof(TileSmem);
+    if (cudaFuncSetAttribute(k_linear_tiled, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess ||
+        cudaFuncSetAttribute(projection_kernel(d->cout),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+        cudaGetLastError();
+        fno_plan_destroy(m->spec);
+        delete m;
+        return FNO_ERR_CUDA;
     }
     int spec_kernels = 0;
     fno_spectral_conv_kernel_count(m->spec, &spec_kernels);
@@ -157,12 +301,14 @@ fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_param
     float *S = reinterpret_cast<float *>(ws + m.act_bytes);
     float *T = reinterpret_cast<float *>(ws + 2 * m.act_bytes);
     void *spec_ws = ws + 3 * m.act_bytes;
-    const int64_t act = d.batch * d.width * m.npix;
     const size_t spec_stride = (size_t)2 * d.width * d.width * d.modes[0] * d.modes[1] * 2;
 
-    k_linear1x1<<<grid_for(act), kThreads, 0, s>>>(
-        static_cast<const float *>(x), p->lift_w, p->lift_b, nullptr, A, d.batch, d.cin_lift,
-        d.width, m.npix, 0);
+    const unsigned ptiles = (unsigned)((m.npix + kTP - 1) / kTP);
+    const dim3 lin_grid(ptiles, (unsigned)((d.width + kTO - 1) / kTO), (unsigned)d.batch);
+    const size_t smem = sizeof(TileSmem);
+    k_linear_tiled<<<lin_grid, kTT, smem, s>>>(static_cast<const float *>(x), p->lift_w,
+                                               p->lift_b, nullptr, A, d.cin_lift, d.width,
+                                               m.npix, 0);
     if (cudaGetLastError() != cudaSuccess) return FNO_ERR_CUDA;
     for (int l = 0; l < d.nlayers; ++l) {
         fno_status_t st = fno_spectral_conv_forward(m.spec, A, p->spec_w + l * spec_stride, S,
@@ -170,17 +316,17 @@ fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_param
                                                     stream);
         if (st != FNO_OK) return st;
         const int last = (l == d.nlayers - 1);
-        k_linear1x1<<<grid_for(act), kThreads, 0, s>>>(
+        k_linear_tiled<<<lin_grid, kTT, smem, s>>>(
             A, p->pw_w + (size_t)l * d.width * d.width, p->pw_b + (size_t)l * d.width, S, T,
-            d.batch, d.width, d.width, m.npix, last ? 0 : 1);
+            d.width, d.width, m.npix, last ? 0 : 1);
         if (cudaGetLastError() != cudaSuccess) return FNO_ERR_CUDA;
         float *tmp = A;
         A = T;
         T = tmp;
     }
-    k_projection<<<grid_for(d.batch * m.npix), kThreads, 0, s>>>(
-        A, p->proj1_w, p->proj1_b, p->proj2_w, p->proj2_b, static_cast<float *>(out), d.batch,
-        d.width, d.hidden, d.cout, m.npix);
+    projection_kernel(d.cout)<<<dim3(ptiles, (unsigned)d.batch), kTT, smem, s>>>(
+        A, p->proj1_w, p->proj1_b, p->proj2_w, p->proj2_b, static_cast<float *>(out), d.width,
+        d.hidden, d.cout, m.npix);
     if (cudaGetLastError() != cudaSuccess) return FNO_ERR_CUDA;
     return FNO_OK;
 }

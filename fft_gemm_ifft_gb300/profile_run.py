@@ -1,11 +1,15 @@
 """Run a workload's forward a fixed number of times, for profiler captures.
 
     python -m fft_gemm_ifft_gb300.profile_run --workload 2d_f32 --iters 20 [--flags 0]
+    python -m fft_gemm_ifft_gb300.profile_run --workload fno2d_f32 --iters 20 --time
 
 Inputs are seeded (``workloads``) and rotate through enough (x, w, y) sets to
 exceed twice the L2 size, as in the benchmark; every forward is an eager call
-through the C ABI on one stream.  Exits non-zero if the device error word is
-set.  The profiler picks kernels with -k/-s/-c.
+through the C ABI on one stream.  ``--workload fno2d_f32`` runs the FNO stack
+(``fno_forward``) instead of one layer.  With ``--time`` the forwards are timed
+with CUDA events on the launching stream (after the same number of warm-up
+forwards) and the median and 10th/90th percentiles are printed.  Exits non-zero
+if the device error word is set.  The profiler picks kernels with -k/-s/-c.
 """
 from __future__ import annotations
 
@@ -22,19 +26,20 @@ def main(argv=None) -> int:
     ap.add_argument("--batch", type=int, default=0, help="override the batch size")
     ap.add_argument("--trace", default="", help="write the last call's work-item trace "
                     "(CSV) here and print a per-phase summary")
+    ap.add_argument("--time", action="store_true", help="time each forward with CUDA events")
     args = ap.parse_args(argv)
 
     import torch
 
     from . import SpectralConv, build, workloads
     build.build()
+    if args.workload == workloads.FNO_CASE.name:
+        return run_fno(args)
     case = workloads.CASES[args.workload]
     if args.batch:
         case = case.with_batch(args.batch)
     from . import capi
     flags = args.flags | (capi.FNO_PLAN_TRACE if args.trace else 0)
-    if args.trace and not flags & capi.FNO_PLAN_TENSOR_CORES:
-        flags |= capi.FNO_PLAN_PERSISTENT       # the trace covers the persistent kernels
     conv = SpectralConv(case.n, case.modes, case.batch, case.cin, case.cout, case.dtype, flags)
     x_np, w_np = workloads.make_x(case), workloads.make_w(case)
     set_bytes = x_np.nbytes + w_np.nbytes + math.prod(case.y_shape) * case.elem_bytes
@@ -43,8 +48,12 @@ def main(argv=None) -> int:
     xs = [torch.from_numpy(x_np).cuda() for _ in range(nsets)]
     ws = [torch.from_numpy(w_np).cuda() for _ in range(nsets)]
     ys = [torch.empty(case.y_shape, dtype=conv.torch_dtype, device="cuda") for _ in range(nsets)]
-    for i in range(args.iters):
-        conv(xs[i % nsets], ws[i % nsets], ys[i % nsets])
+    step = lambda i: conv(xs[i % nsets], ws[i % nsets], ys[i % nsets])
+    if args.time:
+        report_times(case.name, case.batch, time_steps(step, args.iters))
+    else:
+        for i in range(args.iters):
+            step(i)
     torch.cuda.synchronize()
     if args.trace:
         tst, recs = capi.fno_plan_get_trace(conv.handle)
@@ -55,6 +64,53 @@ def main(argv=None) -> int:
     st = conv.device_error()
     conv.close()
     print(f"{args.iters} forwards of {case.name}, kernels/forward {conv.kernel_count}, "
+          f"device status {st}")
+    return 0 if st == 0 else 1
+
+
+def time_steps(step, iters):
+    """Per-call device times (microseconds) of `iters` calls after as many warm-up
+    calls, CUDA events on the current stream."""
+    import torch
+    for i in range(iters):
+        step(i)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(iters + 1)]
+    torch.cuda.synchronize()
+    ev[0].record()
+    for i in range(iters):
+        step(i)
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    return sorted(ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(iters))
+
+
+def report_times(name, batch, ts):
+    med = ts[len(ts) // 2]
+    print(f"{name}: median {med:.2f} us (p10 {ts[len(ts) // 10]:.2f}, p90 "
+          f"{ts[(9 * len(ts)) // 10]:.2f}) over {len(ts)} calls, {batch / med * 1e6:.1f} samples/s")
+
+
+def run_fno(args) -> int:
+    import torch
+
+    from . import FnoModel, workloads
+    case = workloads.FNO_CASE
+    batch = args.batch or case.batch
+    m = FnoModel(batch, case.h, case.w, case.modes, case.cin_lift, case.width, case.nlayers,
+                 case.hidden, case.cout, flags=args.flags)
+    x = torch.from_numpy(workloads.make_fno_inputs(case, batch)).cuda()
+    p = {k: torch.from_numpy(v).cuda() for k, v in workloads.make_fno_params(case).items()}
+    y = torch.empty(m.y_shape, device="cuda")
+    step = lambda i: m(x, p, y)
+    if args.time:
+        report_times(case.name, batch, time_steps(step, args.iters))
+    else:
+        for i in range(args.iters):
+            step(i)
+    torch.cuda.synchronize()
+    st = m.device_error()
+    m.close()
+    print(f"{args.iters} forwards of {case.name}, kernels/forward {m.kernel_count}, "
           f"device status {st}")
     return 0 if st == 0 else 1
 

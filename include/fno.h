@@ -76,8 +76,10 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * ablation of the article's §5.2 note).  Results agree with the fused path
  * within rounding.                                                           */
 #define FNO_PLAN_UNFUSED 1u
-/* Record a timeline of the fused kernel's work items (read back with
- * fno_plan_get_trace).  Costs a few timer reads and stores per item.        */
+/* Record a timeline of the fused kernels' work items (read back with
+ * fno_plan_get_trace): the persistent kernel's queue items, or one record per
+ * CTA of each kernel of the three-kernel variants (2-D and 3-D layers).
+ * Costs a few timer reads, a barrier and a store per item.                  */
 #define FNO_PLAN_TRACE 2u
 /* Run the float32 128x128 layer on the tensor-core variant of the fused
  * kernel (row DFTs as tcgen05 3xTF32 GEMMs fed by TMA) instead of the
@@ -93,8 +95,9 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * Times are the GPU's global nanosecond timer.                              */
 typedef struct fno_trace_record_s {
     uint32_t item;      /* phase << 24 | batch group << 16 | index in the phase-group
-                           (phase 0: forward transform, 1: mixing, 2: inverse)   */
-    uint32_t worker;    /* which CTA / stream ran it                              */
+                           (phase 0: forward transform, 1: mixing, 2: inverse); in
+                           the three-kernel variants phase << 24 | CTA index     */
+    uint32_t worker;    /* which CTA / stream ran it (three-kernel variants: the SM) */
     uint64_t t_start;   /* processing began                                       */
     uint64_t t_ready;   /* its inputs were available (loads landed, waits over)   */
     uint64_t t_compute; /* its arithmetic was done                                */
@@ -196,10 +199,11 @@ fno_status_t fno_spectral_conv_forward_static(int ndim, const int64_t *n,
                                               fno_stream_t stream);
 
 /* Copy the trace of the plan's last forward call (FNO_PLAN_TRACE) to host
- * memory: up to `capacity` records, ordered by ticket; *count receives the
- * number of records the call produced.  Synchronises the device.  Returns
- * FNO_ERR_INVALID_ARG if the plan was made without FNO_PLAN_TRACE or does not
- * run the fused kernel.                                                     */
+ * memory: up to `capacity` records, ordered by ticket (three-kernel variants:
+ * kernel A's CTAs, then B's, then C's); *count receives the number of records
+ * the call produced.  Synchronises the device.  Returns FNO_ERR_INVALID_ARG if
+ * the plan was made without FNO_PLAN_TRACE or runs a path that records none
+ * (separate kernels, the 1-D kernel).                                       */
 fno_status_t fno_plan_get_trace(fno_plan_t plan, fno_trace_record_t *records, size_t capacity,
                                 size_t *count);
 

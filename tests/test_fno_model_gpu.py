@@ -37,6 +37,25 @@ def test_small_stack_matches_oracle():
     assert_close(got, ref, "f32", "small FNO stack")
 
 
+@pytest.mark.parametrize("shape", [
+    # batch, width, nlayers, h, w, modes, hidden, cout: channel counts that are
+    # not multiples of the 64-wide tiles and span two input-channel chunks,
+    # several output groups, and pixel counts below one 128-pixel tile
+    (3, 70, 1, 16, 16, (4, 4), 70, 3),
+    (2, 5, 2, 2, 2, (1, 1), 9, 1),
+    (1, 12, 2, 8, 16, (2, 3), 130, 8),
+], ids=["ragged_channels", "tiny_grid", "wide_hidden"])
+def test_stack_ragged_tiles(shape):
+    b, width, nl, h, w, modes, hidden, cout = shape
+    case = workloads.FnoCase("ragged", batch=b, width=width, nlayers=nl, h=h, w=w,
+                             modes=modes, hidden=hidden, cout=cout)
+    x = workloads.make_fno_inputs(case)
+    p = workloads.make_fno_params(case)
+    got, _ = run_model(case, x, p, case.batch)
+    ref = oracle.fno_forward(x, workloads.fno_params_for_oracle(p), case.modes)
+    assert_close(got, ref, "f32", f"FNO stack {shape}")
+
+
 def test_full_stack_sampled():
     case = workloads.FNO_CASE
     x = workloads.make_fno_inputs(case)

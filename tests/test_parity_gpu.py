@@ -14,6 +14,10 @@ pytestmark = pytest.mark.gpu
 SMALL = [
     # (n, modes, batch, cin, cout, dtype)
     ((256,), (16,), 4, 16, 16, "f32"),
+    ((256,), (16,), 3, 5, 11, "f16"),
+    ((1024,), (64,), 3, 12, 20, "f32"),
+    ((512,), (257,), 2, 4, 3, "f16"),
+    ((256,), (129,), 1, 64, 2, "f32"),
     ((16,), (9,), 2, 3, 5, "f32"),
     ((8,), (5,), 1, 1, 1, "f32"),
     ((128, 128), (16, 16), 3, 32, 32, "f32"),
@@ -129,6 +133,19 @@ def test_fused_and_unfused_agree_and_are_deterministic():
     assert_close(d, c.astype(np.float64), "f32", "tensor cores vs unfused")
 
 
+@pytest.mark.parametrize("name,kernels", [("1d_f32", 1), ("2d_f32", 3), ("2d_f16", 3),
+                                          ("3d_f32", 3)])
+def test_every_workload_runs_fused(name, kernels):
+    case = workloads.CASES[name]
+    conv = SpectralConv(case.n, case.modes, case.batch, case.cin, case.cout, case.dtype)
+    assert conv.kernel_count == kernels
+    conv.close()
+    conv = SpectralConv(case.n, case.modes, case.batch, case.cin, case.cout, case.dtype,
+                        FNO_PLAN_UNFUSED)
+    assert conv.kernel_count == 2 * len(case.n) + 1
+    conv.close()
+
+
 def test_fused_3d_and_unfused_agree():
     case = workloads.CASES["3d_f32"]
     x, w = workloads.make_x(case), workloads.make_w(case)
@@ -138,6 +155,38 @@ def test_fused_3d_and_unfused_agree():
     assert ka == 3 and kc == 7
     assert np.array_equal(a, b), "two runs of the same plan differ"
     assert_close(a, c.astype(np.float64), "f32", "3-D fused vs unfused")
+
+
+@pytest.mark.parametrize("name,chunks", [("2d_f32", 4), ("3d_f32", 8)])
+def test_trace_three_kernel_variant(name, chunks):
+    # one record per CTA of each kernel; kernel B's CTAs start before A's last
+    # one ends at the earliest (programmatic dependent launch), never wait past it
+    case = workloads.CASES[name]
+    conv = SpectralConv(case.n, case.modes, case.batch, case.cin, case.cout, case.dtype,
+                        capi.FNO_PLAN_TRACE)
+    x, w = workloads.make_x(case), workloads.make_w(case)
+    y = conv(to_dev(x), to_dev(w))
+    torch.cuda.synchronize()
+    st, recs = capi.fno_plan_get_trace(conv.handle)
+    assert st == capi.FNO_OK
+    phases = [r[0] for r in recs]
+    assert phases.count(0) == case.batch * case.cin * chunks
+    assert phases.count(2) == case.batch * case.cout * chunks
+    assert phases.count(1) > 0 and len(recs) == len(phases)
+    for r in recs:
+        assert 0 < r[4] <= r[5] <= r[7], r
+    end_a = max(r[7] for r in recs if r[0] == 0)
+    end_b = max(r[7] for r in recs if r[0] == 1)
+    assert min(r[5] for r in recs if r[0] == 1) >= end_a - 1000   # globaltimer granularity
+    assert min(r[5] for r in recs if r[0] == 2) >= end_b - 1000
+    if name == "2d_f32":
+        ref = run_oracle(case, x, w)
+    else:
+        ref = None
+    got = y.cpu().numpy()
+    if ref is not None:
+        assert_close(got, ref, "f32", "traced three-kernel forward")
+    conv.close()
 
 
 def test_output_red_zones_untouched():
