@@ -179,8 +179,8 @@ def bench_gpu(args, rank, world, local):
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0)) or (126 << 20)
     nsets = max(2, math.ceil(2 * l2 / set_bytes))
-    xs = [torch.from_numpy(x_np).to(dev) for _ in range(nsets)]
-    ws = [torch.from_numpy(w_np).to(dev) for _ in range(nsets)]
+    xs = [workloads.to_torch_storage(x_np, case.dtype).to(dev) for _ in range(nsets)]
+    ws = [workloads.to_torch_storage(w_np, case.dtype).to(dev) for _ in range(nsets)]
     ys = [torch.empty(case.y_shape, dtype=conv.torch_dtype, device=dev) for _ in range(nsets)]
 
     stream = torch.cuda.Stream(device=dev)
@@ -235,7 +235,7 @@ def bench_gpu(args, rank, world, local):
 
     # end to end through the public API: pinned host input -> device -> layer
     # -> pinned host output, every step
-    x_host = torch.from_numpy(x_np).pin_memory()
+    x_host = workloads.to_torch_storage(x_np, case.dtype).pin_memory()
     y_host = torch.empty(case.y_shape, dtype=conv.torch_dtype).pin_memory()
     e2e_steps = max(3, args.e2e_steps)
     with torch.cuda.stream(stream):
@@ -272,7 +272,7 @@ def bench_gpu(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32" if case.dtype == "f32" else "f16-storage/f32-accumulate",
+        "dtype": "f32" if case.dtype == "f32" else f"{case.dtype}-storage/f32-accumulate",
         "data": "synthetic (seeded N(0,1) fields, U[0,1)/(Cin*Cout) complex weights)",
         "config": {
             "workload": f"{case.name}: {case.ndim}-D spectral conv, B={case.batch}, "

@@ -9,8 +9,8 @@ stream to the library.  PyTorch is used for device memory and streams only.
 from __future__ import annotations
 
 from . import capi
-from .capi import (FNO_F16, FNO_F32, FNO_PLAN_DEFAULT, FNO_PLAN_UNFUSED,  # noqa: F401
-                   fno_status_string)
+from .capi import (FNO_BF16, FNO_F16, FNO_F32, FNO_PLAN_DEFAULT,  # noqa: F401
+                   FNO_PLAN_UNFUSED, fno_status_string)
 
 __all__ = ["capi", "FnoError", "SpectralConv", "FnoModel", "check"]
 
@@ -57,8 +57,9 @@ class SpectralConv:
         self.n, self.modes = tuple(int(v) for v in n), tuple(int(v) for v in modes)
         self.batch, self.cin, self.cout = int(batch), int(cin), int(cout)
         self.dtype = dtype
-        self.torch_dtype = torch.float32 if dtype == "f32" else torch.float16
-        code = FNO_F32 if dtype == "f32" else FNO_F16
+        self.torch_dtype = {"f32": torch.float32, "f16": torch.float16,
+                            "bf16": torch.bfloat16}[dtype]
+        code = capi.DTYPE_CODES[dtype]
         st, self.handle = capi.fno_spectral_conv_plan(len(self.n), self.n, self.modes, batch,
                                                       cin, cout, code, flags)
         check(st, "fno_spectral_conv_plan")

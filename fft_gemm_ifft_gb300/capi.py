@@ -25,6 +25,8 @@ FNO_ERR_ALIASING = 8
 
 FNO_F32 = 0
 FNO_F16 = 1
+FNO_BF16 = 2
+DTYPE_CODES = {"f32": FNO_F32, "f16": FNO_F16, "bf16": FNO_BF16}
 
 FNO_PLAN_DEFAULT = 0
 FNO_PLAN_UNFUSED = 1

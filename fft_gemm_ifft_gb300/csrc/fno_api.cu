@@ -62,7 +62,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 fno_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? FNO_OK : FNO_ERR_CUDA; }
 
-size_t elem_bytes(fno_dtype_t t) { return t == FNO_F16 ? 2 : 4; }
+size_t elem_bytes(fno_dtype_t t) { return (t == FNO_F16 || t == FNO_BF16) ? 2 : 4; }
 
 // Which kernel sequence a valid description runs on.
 int choose_path(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout,
@@ -83,7 +83,7 @@ fno_status_t describe(int ndim, const int64_t *n, const int32_t *modes, int64_t 
     fno_status_t st = make_geom(g, ndim, n, modes);
     if (st != FNO_OK) return st;
     if (batch < 1 || cin < 1 || cout < 1) return FNO_ERR_INVALID_ARG;
-    if (dtype != FNO_F32 && dtype != FNO_F16) return FNO_ERR_INVALID_ARG;
+    if (dtype != FNO_F32 && dtype != FNO_F16 && dtype != FNO_BF16) return FNO_ERR_INVALID_ARG;
     if (flags & ~(FNO_PLAN_UNFUSED | FNO_PLAN_TRACE | FNO_PLAN_TENSOR_CORES | FNO_PLAN_PERSISTENT))
         return FNO_ERR_INVALID_ARG;
     // int64 element counts must not overflow and a tensor must stay addressable

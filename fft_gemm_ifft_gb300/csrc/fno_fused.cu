@@ -999,13 +999,13 @@ enum Variant { kVarNone, kVarPdl128, kVarPdl256, kVarPersistent128, kVarTc128, k
 
 // Which fused kernel(s) a description runs on.
 Variant variant(const Geom &g, fno_dtype_t dtype, uint32_t flags) {
-    if (dtype != FNO_F32 && dtype != FNO_F16) return kVarNone;
+    if (dtype != FNO_F32 && dtype != FNO_F16 && dtype != FNO_BF16) return kVarNone;
     if (g.d == 1) return kVarOne1d;
     if (fused3d_match(g, dtype)) return kVarPdl3d;
     if (is_cfg256(g)) return kVarPdl256;
     if (!is_cfg128(g)) return kVarNone;
     if (use_tc(g, dtype, flags)) return kVarTc128;
-    if (flags & FNO_PLAN_PERSISTENT) return kVarPersistent128;
+    if ((flags & FNO_PLAN_PERSISTENT) && dtype != FNO_BF16) return kVarPersistent128;
     return kVarPdl128;
 }
 
@@ -1051,9 +1051,9 @@ cudaError_t fused_plan_init(Plan &p) {
     if (v == kVarPdl3d) return fused3d_plan_init(p);
     if (v == kVarOne1d) return cudaSuccess;
     if (v == kVarPdl128)
-        return p.dtype == FNO_F32 ? Pdl<Cfg128>::init<float>(p) : Pdl<Cfg128>::init<__half>(p);
+        return with_storage(p.dtype, [&](auto t) { return Pdl<Cfg128>::init<decltype(t)>(p); });
     if (v == kVarPdl256)
-        return p.dtype == FNO_F32 ? Pdl<Cfg256>::init<float>(p) : Pdl<Cfg256>::init<__half>(p);
+        return with_storage(p.dtype, [&](auto t) { return Pdl<Cfg256>::init<decltype(t)>(p); });
     if (v == kVarTc128)
     {
         if (!encoder()) return cudaErrorNotSupported;
@@ -1174,11 +1174,11 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
         a.batch = (int)p.batch;
         a.cin = p.cin;
         a.cout = p.cout;
-        if (v == kVarPdl256)
-            return p.dtype == FNO_F32 ? Pdl<Cfg256>::forward<float>(p, a, s)
-                                      : Pdl<Cfg256>::forward<__half>(p, a, s);
-        return p.dtype == FNO_F32 ? Pdl<Cfg128>::forward<float>(p, a, s)
-                                  : Pdl<Cfg128>::forward<__half>(p, a, s);
+        return with_storage(p.dtype, [&](auto t) {
+            using T = decltype(t);
+            return v == kVarPdl256 ? Pdl<Cfg256>::forward<T>(p, a, s)
+                                   : Pdl<Cfg128>::forward<T>(p, a, s);
+        });
     }
     const Layout l = layout(p.g, p.batch, p.cin, p.cout);
     Args a{};

@@ -112,7 +112,8 @@ k_fused1d(const T *__restrict__ x, const T *__restrict__ w, T *__restrict__ y, i
 }  // namespace
 
 bool fused1d_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout) {
-    return g.d == 1 && (dtype == FNO_F32 || dtype == FNO_F16) && g.n[0] <= 1024 &&
+    return g.d == 1 && (dtype == FNO_F32 || dtype == FNO_F16 || dtype == FNO_BF16) &&
+           g.n[0] <= 1024 &&
            batch * kG1 < (1ll << 31) &&
            smem1_bytes((int)g.n[0], g.m[0], cin, cout) <= kSmem1Max;
 }
@@ -131,15 +132,12 @@ cudaError_t fused1d_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
     cfg.stream = s;
     cfg.attrs = &cl;
     cfg.numAttrs = 1;
-    cudaError_t e;
-    if (p.dtype == FNO_F32)
-        e = cudaLaunchKernelEx(&cfg, k_fused1d<float>, static_cast<const float *>(b.x),
-                               static_cast<const float *>(b.w), static_cast<float *>(b.y), p.cin,
-                               p.cout, N, M, static_cast<const float2 *>(p.tw[0]));
-    else
-        e = cudaLaunchKernelEx(&cfg, k_fused1d<__half>, static_cast<const __half *>(b.x),
-                               static_cast<const __half *>(b.w), static_cast<__half *>(b.y),
-                               p.cin, p.cout, N, M, static_cast<const float2 *>(p.tw[0]));
+    const cudaError_t e = with_storage(p.dtype, [&](auto t) {
+        using T = decltype(t);
+        return cudaLaunchKernelEx(&cfg, k_fused1d<T>, static_cast<const T *>(b.x),
+                                  static_cast<const T *>(b.w), static_cast<T *>(b.y), p.cin,
+                                  p.cout, N, M, static_cast<const float2 *>(p.tw[0]));
+    });
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

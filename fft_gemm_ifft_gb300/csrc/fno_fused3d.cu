@@ -363,7 +363,8 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 bool fused3d_match(const Geom &g, fno_dtype_t dtype) {
     using C3 = Cfg3d64;
-    return g.d == 3 && (dtype == FNO_F32 || dtype == FNO_F16) && g.n[0] == C3::N0 &&
+    return g.d == 3 && (dtype == FNO_F32 || dtype == FNO_F16 || dtype == FNO_BF16) &&
+           g.n[0] == C3::N0 &&
            g.n[1] == C3::N1 && g.n[2] == C3::N2 && g.m[0] == C3::M0 && g.m[1] == C3::M1 &&
            g.m[2] == C3::M2;
 }
@@ -385,7 +386,7 @@ size_t fused3d_workspace_bytes(const Geom &g, int64_t batch, int cin, int cout) 
 }
 
 cudaError_t fused3d_plan_init(Plan &p) {
-    return p.dtype == FNO_F32 ? Pdl3<Cfg3d64>::init<float>(p) : Pdl3<Cfg3d64>::init<__half>(p);
+    return with_storage(p.dtype, [&](auto t) { return Pdl3<Cfg3d64>::init<decltype(t)>(p); });
 }
 
 cudaError_t fused3d_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
@@ -403,8 +404,8 @@ cudaError_t fused3d_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
     a.batch = (int)p.batch;
     a.cin = p.cin;
     a.cout = p.cout;
-    return p.dtype == FNO_F32 ? Pdl3<Cfg3d64>::forward<float>(p, a, s)
-                              : Pdl3<Cfg3d64>::forward<__half>(p, a, s);
+    return with_storage(p.dtype,
+                        [&](auto t) { return Pdl3<Cfg3d64>::forward<decltype(t)>(p, a, s); });
 }
 
 }  // namespace fno

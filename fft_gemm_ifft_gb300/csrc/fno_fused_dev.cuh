@@ -135,6 +135,23 @@ template <> struct Io<__half> {
     }
 };
 
+template <> struct Io<__nv_bfloat16> {
+    using W2 = uint2;                                // two complex weights (4 bfloat16)
+    static __device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
+        const uint2 a = __ldcs(reinterpret_cast<const uint2 *>(p));
+        const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&a.x));
+        const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&a.y));
+        return make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16 *p, float v) {
+        *p = __float2bfloat16_rn(v);
+    }
+    static __device__ __forceinline__ float2 wget(const uint2 &w, int g) {
+        const unsigned u = g == 0 ? w.x : w.y;
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u));
+    }
+};
+
 __device__ __forceinline__ int ld_acquire(const int *p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -237,6 +254,7 @@ __device__ __forceinline__ void a_load_rows(const T *__restrict__ src, int c, fl
 //    x[t][n1 + P n2] over n2.  Lanes P*g .. P*g+P-1 share rows (t, t + RC/2).
 __device__ __forceinline__ float smp(const float *p) { return *p; }
 __device__ __forceinline__ float smp(const __half *p) { return __half2float(*p); }
+__device__ __forceinline__ float smp(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 
 template <class Cf, typename S = float>
 __device__ __forceinline__ void a_row_dft(const S *xs, float2 *zs, Tw tw) {

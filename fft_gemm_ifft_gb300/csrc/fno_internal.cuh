@@ -6,6 +6,7 @@
 // Y[b,o,k] = sum_i X[b,i,k] W[blk(k), i, o, local(k)]; y = inverse(Y).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -91,6 +92,27 @@ template <> struct Storage<__half> {
         return __half22float2(*reinterpret_cast<const __half2 *>(p));
     }
 };
+
+template <> struct Storage<__nv_bfloat16> {
+    static __device__ __forceinline__ float load(const __nv_bfloat16 *p) {
+        return __bfloat162float(*p);
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16 *p, float v) {
+        *p = __float2bfloat16_rn(v);
+    }
+    static __device__ __forceinline__ float2 load2(const __nv_bfloat16 *p) {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+    }
+};
+
+// Calls f with a value of the storage type of `dt` (float, __half or
+// __nv_bfloat16), so that a generic lambda can pick the kernel instance.
+template <class F>
+decltype(auto) with_storage(fno_dtype_t dt, F &&f) {
+    if (dt == FNO_F16) return f(__half());
+    if (dt == FNO_BF16) return f(__nv_bfloat16());
+    return f(0.0f);
+}
 
 // Sets the device error word once (first error wins).
 __device__ __forceinline__ void raise_dev_error(int *err, int code) {

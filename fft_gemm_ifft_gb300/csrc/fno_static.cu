@@ -117,7 +117,7 @@ extern "C" fno_status_t fno_spectral_conv_forward_static(
     // the layer's intermediates must fit the static scratch array
     if (unfused_workspace_bytes(g, batch, cin, cout) > kStaticScratchBytes)
         return FNO_ERR_UNSUPPORTED;
-    const size_t eb = dtype == FNO_F16 ? 2 : 4;
+    const size_t eb = dtype == FNO_F32 ? 4 : 2;
     const size_t xb = (size_t)batch * cin * g.npix * eb, yb = (size_t)batch * cout * g.npix * eb;
     if (overlaps(y, yb, x, xb) || overlaps(y, yb, w, weight_bytes)) return FNO_ERR_ALIASING;
 

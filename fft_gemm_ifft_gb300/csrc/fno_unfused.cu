@@ -278,18 +278,17 @@ cudaError_t launch_mix(const Plan &p, const float2 *X, const void *w, float2 *Y,
     kg.nkept = g.nkept;
     kg.mblk = g.mblk;
     const int grid = grid_for(p.batch * p.cout * g.nkept, p.num_sms);
-    if (p.dtype == FNO_F32)
-        k_mix<float><<<grid, kThreads, 0, s>>>(X, static_cast<const float *>(w), Y, p.batch,
-                                              p.cin, p.cout, kg);
-    else
-        k_mix<__half><<<grid, kThreads, 0, s>>>(X, static_cast<const __half *>(w), Y, p.batch,
-                                               p.cin, p.cout, kg);
+    with_storage(p.dtype, [&](auto t) {
+        using T = decltype(t);
+        k_mix<T><<<grid, kThreads, 0, s>>>(X, static_cast<const T *>(w), Y, p.batch, p.cin,
+                                          p.cout, kg);
+        return 0;
+    });
     return cudaGetLastError();
 }
 
 cudaError_t unfused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
-    return p.dtype == FNO_F32 ? unfused_forward_t<float>(p, b, s)
-                              : unfused_forward_t<__half>(p, b, s);
+    return with_storage(p.dtype, [&](auto t) { return unfused_forward_t<decltype(t)>(p, b, s); });
 }
 
 }  // namespace fno

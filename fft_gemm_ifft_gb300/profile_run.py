@@ -45,8 +45,8 @@ def main(argv=None) -> int:
     set_bytes = x_np.nbytes + w_np.nbytes + math.prod(case.y_shape) * case.elem_bytes
     l2 = int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 0)) or (126 << 20)
     nsets = max(2, math.ceil(2 * l2 / set_bytes))
-    xs = [torch.from_numpy(x_np).cuda() for _ in range(nsets)]
-    ws = [torch.from_numpy(w_np).cuda() for _ in range(nsets)]
+    xs = [workloads.to_torch_storage(x_np, case.dtype).cuda() for _ in range(nsets)]
+    ws = [workloads.to_torch_storage(w_np, case.dtype).cuda() for _ in range(nsets)]
     ys = [torch.empty(case.y_shape, dtype=conv.torch_dtype, device="cuda") for _ in range(nsets)]
     step = lambda i: conv(xs[i % nsets], ws[i % nsets], ys[i % nsets])
     if args.time:

@@ -18,6 +18,7 @@ name       dim   shape                                                  dtype
 1d_f32     1     B=4, C=16, N=256, modes 16                             f32
 2d_f32     2     B=8, C=32, 128x128, modes 16x16 (2 blocks)             f32
 2d_f16     2     B=32, C=64, 256x256, modes 32x32 (2 blocks)            f16
+2d_bf16    2     the 2d_f16 problem with bfloat16 storage               bf16
 3d_f32     3     B=4, C=32, 64^3, modes 16^3 (4 blocks)                 f32
 fno2d_f32  2     B=16, 3 -> 64 -> 4 layers -> 128 -> 1, 128x128, 16x16  f32
 =========  ====  =====================================================  =====
@@ -47,7 +48,7 @@ class SpectralConvCase:
     batch: int
     cin: int
     cout: int
-    dtype: str                  # "f32" or "f16" (storage; accumulation is fp32)
+    dtype: str                  # "f32", "f16" or "bf16" (storage; accumulation is fp32)
     index: int = 0              # workload index used for the seeds
 
     @property
@@ -72,7 +73,8 @@ class SpectralConvCase:
 
     @property
     def np_dtype(self):
-        return np.float32 if self.dtype == "f32" else np.float16
+        """Host array dtype: bfloat16 values are held exactly in float32."""
+        return np.float16 if self.dtype == "f16" else np.float32
 
     @property
     def elem_bytes(self) -> int:
@@ -114,6 +116,7 @@ CASES: Dict[str, SpectralConvCase] = {
     "1d_f32": SpectralConvCase("1d_f32", (256,), (16,), 4, 16, 16, "f32", 0),
     "2d_f32": SpectralConvCase("2d_f32", (128, 128), (16, 16), 8, 32, 32, "f32", 1),
     "2d_f16": SpectralConvCase("2d_f16", (256, 256), (32, 32), 32, 64, 64, "f16", 2),
+    "2d_bf16": SpectralConvCase("2d_bf16", (256, 256), (32, 32), 32, 64, 64, "bf16", 2),
     "3d_f32": SpectralConvCase("3d_f32", (64, 64, 64), (16, 16, 16), 4, 32, 32, "f32", 3),
 }
 FNO_CASE = FnoCase("fno2d_f32")
@@ -125,11 +128,29 @@ def _gen(seed: int) -> torch.Generator:
     return g
 
 
+TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def to_storage(a, dtype: str) -> np.ndarray:
+    """Round values once to the storage dtype (a cast, no arithmetic).  The
+    host array is float32 for f32 and bf16 (bfloat16 values are exact in
+    float32) and float16 for f16."""
+    if dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64)).to(torch.bfloat16)
+        return t.to(torch.float32).numpy()
+    return np.asarray(a).astype(np.float16 if dtype == "f16" else np.float32)
+
+
+def to_torch_storage(a: np.ndarray, dtype: str) -> torch.Tensor:
+    """Host storage array -> CPU tensor of the storage dtype."""
+    return torch.from_numpy(np.ascontiguousarray(a)).to(TORCH_DTYPES[dtype])
+
+
 def make_x(case: SpectralConvCase, seed: int | None = None) -> np.ndarray:
     """N(0,1) input in the storage dtype, shape (B, Cin, N...)."""
     g = _gen(1000 + case.index if seed is None else seed)
     x = torch.randn(case.x_shape, generator=g, dtype=torch.float64)
-    return x.numpy().astype(case.np_dtype)
+    return to_storage(x.numpy(), case.dtype)
 
 
 def make_w(case: SpectralConvCase, seed: int | None = None) -> np.ndarray:
@@ -138,7 +159,7 @@ def make_w(case: SpectralConvCase, seed: int | None = None) -> np.ndarray:
     g = _gen(2000 + case.index if seed is None else seed)
     w = torch.rand(case.weight_shape + (2,), generator=g, dtype=torch.float64)
     w = w / float(case.cin * case.cout)
-    return w.numpy().astype(case.np_dtype)
+    return to_storage(w.numpy(), case.dtype)
 
 
 def as_complex(w: np.ndarray) -> np.ndarray:

@@ -62,7 +62,8 @@ typedef enum fno_status_e {
 
 typedef enum fno_dtype_e {
     FNO_F32 = 0,   /* float32 storage, float32 arithmetic                                 */
-    FNO_F16 = 1    /* IEEE half storage (x, w, y), float32 accumulation                   */
+    FNO_F16 = 1,   /* IEEE half storage (x, w, y), float32 accumulation                   */
+    FNO_BF16 = 2   /* bfloat16 storage (x, w, y), float32 accumulation                    */
 } fno_dtype_t;
 
 typedef void *fno_stream_t;                 /* a cudaStream_t                            */

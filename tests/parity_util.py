@@ -12,8 +12,8 @@ from fft_gemm_ifft_gb300 import SpectralConv, workloads
 # few wrong elements that a norm over a large tensor would average away:
 # float32 allows 1e-4 of the largest output magnitude; half storage allows
 # 1e-2 of it (the output rounding alone is 2^-11 of each element).
-REL_L2 = {"f32": 1e-5, "f16": 1e-2}
-ELEMWISE = {"f32": 1e-4, "f16": 1e-2}
+REL_L2 = {"f32": 1e-5, "f16": 1e-2, "bf16": 1e-2}
+ELEMWISE = {"f32": 1e-4, "f16": 1e-2, "bf16": 1e-2}
 
 
 def rel_l2(got, ref):
@@ -35,14 +35,18 @@ def assert_close(got, ref, dtype, what=""):
     return r
 
 
-def to_dev(a: np.ndarray) -> torch.Tensor:
+def to_dev(a: np.ndarray, dtype: str = "") -> torch.Tensor:
+    """Host array -> device tensor; dtype "bf16" casts the (exactly
+    representable) float32 values to bfloat16 storage."""
+    if dtype == "bf16":
+        return workloads.to_torch_storage(a, dtype).cuda()
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
 def run_gpu(case, x_np, w_np, flags=0):
     conv = SpectralConv(case.n, case.modes, x_np.shape[0], case.cin, case.cout, case.dtype,
                         flags)
-    y = conv(to_dev(x_np), to_dev(w_np))
+    y = conv(to_dev(x_np, case.dtype), to_dev(w_np, case.dtype))
     torch.cuda.synchronize()
     assert conv.device_error() == 0
     out = y.float().cpu().numpy()

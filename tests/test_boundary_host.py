@@ -53,6 +53,7 @@ Q = capi.fno_spectral_conv_query
     ((1, [256], [16], 4, 16, 16, F32), 1 * 16 * 16 * 16 * 8),
     ((2, [128, 128], [16, 16], 8, 32, 32, F32), 2 * 32 * 32 * 256 * 8),
     ((2, [256, 256], [32, 32], 32, 64, 64, F16), 2 * 64 * 64 * 1024 * 4),
+    ((2, [256, 256], [32, 32], 32, 64, 64, capi.FNO_BF16), 2 * 64 * 64 * 1024 * 4),
     ((3, [64, 64, 64], [16, 16, 16], 4, 32, 32, F32), 4 * 32 * 32 * 4096 * 8),
     ((2, [8, 8], [4, 5], 1, 1, 1, F32), 2 * 1 * 1 * 20 * 8),     # all modes, Nyquist kept
 ])
@@ -75,6 +76,7 @@ def test_query_valid(L, args, wbytes):
     ((1, [16], [4], 1, 0, 1, F32), capi.FNO_ERR_INVALID_ARG),          # cin 0
     ((1, [16], [4], 1, 1, -2, F32), capi.FNO_ERR_INVALID_ARG),         # cout < 0
     ((1, [16], [4], 1, 1, 1, 7), capi.FNO_ERR_INVALID_ARG),            # dtype
+    ((1, [16], [4], 1, 1, 1, 3), capi.FNO_ERR_INVALID_ARG),            # dtype
     ((1, [2048], [4], 1, 1, 1, F32), capi.FNO_ERR_UNSUPPORTED),        # N too large
 ])
 def test_query_rejects(L, args, code):

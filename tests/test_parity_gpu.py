@@ -15,6 +15,7 @@ SMALL = [
     # (n, modes, batch, cin, cout, dtype)
     ((256,), (16,), 4, 16, 16, "f32"),
     ((256,), (16,), 3, 5, 11, "f16"),
+    ((256,), (16,), 2, 5, 7, "bf16"),
     ((1024,), (64,), 3, 12, 20, "f32"),
     ((512,), (257,), 2, 4, 3, "f16"),
     ((256,), (129,), 1, 64, 2, "f32"),
@@ -24,6 +25,8 @@ SMALL = [
     ((128, 128), (16, 16), 1, 5, 7, "f32"),
     ((128, 128), (1, 1), 2, 4, 4, "f32"),
     ((128, 128), (16, 16), 2, 6, 5, "f16"),
+    ((128, 128), (16, 16), 2, 6, 5, "bf16"),
+    ((32, 32), (4, 4), 2, 3, 3, "bf16"),
     ((128, 128), (16, 16), 2, 64, 64, "f32"),
     ((128, 128), (16, 16), 1, 64, 37, "f32"),
     ((128, 128), (16, 16), 9, 3, 2, "f32"),
@@ -32,11 +35,13 @@ SMALL = [
     ((64, 64), (16, 16), 2, 8, 8, "f32"),
     ((256, 256), (32, 32), 1, 8, 8, "f16"),
     ((256, 256), (32, 32), 2, 3, 5, "f16"),
+    ((256, 256), (32, 32), 1, 4, 4, "bf16"),
     ((256, 256), (32, 32), 3, 4, 2, "f32"),
     ((64, 64), (8, 8), 2, 4, 6, "f16"),
     ((64, 64, 64), (16, 16, 16), 1, 4, 4, "f32"),
     ((64, 64, 64), (16, 16, 16), 2, 5, 3, "f32"),
     ((64, 64, 64), (16, 16, 16), 3, 3, 5, "f16"),
+    ((64, 64, 64), (16, 16, 16), 1, 3, 2, "bf16"),
     ((8, 8, 8), (2, 3, 4), 2, 3, 2, "f32"),
     ((4, 8, 16), (2, 4, 9), 2, 2, 2, "f32"),
     ((32, 32, 32), (8, 8, 8), 2, 3, 4, "f16"),
@@ -63,8 +68,8 @@ def test_small_cases_match_oracle(spec, flags):
     x = workloads.make_x(case, seed=100 + sum(n))
     w = workloads.make_w(case, seed=200 + sum(modes))
     # a random weight with negative parts too, so sign errors cannot cancel
-    w = (w * case.cin * case.cout * 2 - 1).astype(case.np_dtype) / np.float32(case.cin)
-    w = w.astype(case.np_dtype)
+    w = workloads.to_storage((w.astype(np.float64) * case.cin * case.cout * 2 - 1) / case.cin,
+                             case.dtype)
     got, _ = run_gpu(case, x, w, flags)
     ref = run_oracle(case, x, w)
     assert_close(got, ref, dt, case_id(spec))
@@ -105,7 +110,8 @@ def test_full_size_workload_full_compare(name):
     assert_close(got, ref, case.dtype, name)
 
 
-@pytest.mark.parametrize("name,samples", [("2d_f16", (0, 31)), ("3d_f32", (0, 3))])
+@pytest.mark.parametrize("name,samples", [("2d_f16", (0, 31)), ("2d_bf16", (0, 31)),
+                                          ("3d_f32", (0, 3))])
 def test_full_size_workload_sampled(name, samples):
     # the GPU runs the whole batch; the oracle checks whole samples of it
     # (each sample's output depends only on that sample's input)
@@ -134,7 +140,7 @@ def test_fused_and_unfused_agree_and_are_deterministic():
 
 
 @pytest.mark.parametrize("name,kernels", [("1d_f32", 1), ("2d_f32", 3), ("2d_f16", 3),
-                                          ("3d_f32", 3)])
+                                          ("2d_bf16", 3), ("3d_f32", 3)])
 def test_every_workload_runs_fused(name, kernels):
     case = workloads.CASES[name]
     conv = SpectralConv(case.n, case.modes, case.batch, case.cin, case.cout, case.dtype)
