@@ -16,6 +16,9 @@ TurboFNO article (gsyq.cn/news/457482):
 * ``mix``            -- §2.2, per-mode complex contraction over input channels;
 * ``inverse_modes``  -- §2.3 / §3.3, zero-padded inverse real FFT;
 * ``spectral_conv``  -- the three in order;
+* ``spectral_conv_backward`` -- dL/dx and dL/dw of the layer for a real loss,
+  the derivatives of the three steps above (the pages print no backward pass);
+* ``adjoint_modes``  -- the adjoint of ``forward_modes`` (used by the above);
 * ``fno_forward``    -- the lift / 4 x (spectral conv + 1x1 linear, GELU) /
   projection stack of the 2-D FNO workload.
 
@@ -71,7 +74,11 @@ def _load():
             lib.fno_oracle_spectral_conv.argtypes = sig + [ctypes.c_int64] * 3 + [_f64p] * 3
             lib.fno_oracle_fno_forward.argtypes = (
                 [ctypes.c_int64] * 3 + [_i32p] + [ctypes.c_int64] * 5 + [_f64p] * 11)
-            for f in ("forward_modes", "inverse_modes", "mix", "spectral_conv", "fno_forward"):
+            lib.fno_oracle_adjoint_modes.argtypes = sig + [ctypes.c_int64, _f64p, _f64p]
+            lib.fno_oracle_spectral_conv_backward.argtypes = (
+                sig + [ctypes.c_int64] * 3 + [_f64p] * 5)
+            for f in ("forward_modes", "inverse_modes", "mix", "spectral_conv", "fno_forward",
+                      "adjoint_modes", "spectral_conv_backward"):
                 getattr(lib, "fno_oracle_" + f).restype = ctypes.c_int
             lib.fno_oracle_set_threads.argtypes = [ctypes.c_int]
             lib.fno_oracle_get_threads.restype = ctypes.c_int
@@ -187,6 +194,42 @@ def spectral_conv(x: np.ndarray, w: np.ndarray, modes) -> np.ndarray:
                                             m.ctypes.data_as(_i32p), B, cin, cout,
                                             _d(x), _d(ws), _d(y)), "spectral_conv")
     return y
+
+
+def adjoint_modes(dX: np.ndarray, n, modes) -> np.ndarray:
+    """Kept-mode gradients (..., K...) complex -> dx (..., N...) real, the
+    adjoint of ``forward_modes``: dx_n = sum over kept k of Re(dX_k e^{+2 pi i k.n/N})."""
+    n, m = _geom(n, modes)
+    d = m.size
+    lead = dX.shape[:-d]
+    nimg = int(np.prod(lead, dtype=np.int64))
+    Gs = _split(dX)
+    out = np.empty(lead + tuple(int(v) for v in n), dtype=np.float64)
+    _check(_load().fno_oracle_adjoint_modes(d, n.ctypes.data_as(_i64p),
+                                            m.ctypes.data_as(_i32p), nimg, _d(Gs), _d(out)),
+           "adjoint_modes")
+    return out
+
+
+def spectral_conv_backward(x: np.ndarray, w: np.ndarray, dy: np.ndarray, modes):
+    """Gradients of a real loss through the layer, given dy = dL/dy:
+    returns (dx, dw) with dx (B, Cin, N...) real and dw (nblk, Cin, Cout, m...)
+    complex = dL/dRe(w) + i dL/dIm(w)."""
+    d = len(modes)
+    x = _f64(x)
+    dy = _f64(dy)
+    n, m = _geom(x.shape[-d:], modes)
+    B, cin = x.shape[:2]
+    cout = w.shape[2]
+    if w.shape[1] != cin or dy.shape != (B, cout) + tuple(int(v) for v in n):
+        raise ValueError("x, w and dy shapes do not agree")
+    ws = _split(w)
+    dx = np.empty(x.shape, dtype=np.float64)
+    dw = np.empty(w.shape + (2,), dtype=np.float64)
+    _check(_load().fno_oracle_spectral_conv_backward(
+        d, n.ctypes.data_as(_i64p), m.ctypes.data_as(_i32p), B, cin, cout,
+        _d(x), _d(ws), _d(dy), _d(dx), _d(dw)), "spectral_conv_backward")
+    return dx, dw[..., 0] + 1j * dw[..., 1]
 
 
 def fno_forward(x: np.ndarray, params: dict, modes) -> np.ndarray:

@@ -309,6 +309,138 @@ int fno_oracle_spectral_conv(int d, const int64_t *n, const int32_t *m,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Gradients of the layer for a real loss L, given dy = dL/dy.  The pages print
+ * no backward pass; these are the derivatives of the forward definition above,
+ * with the usual convention for a complex quantity z: dz = dL/dRe(z) + i dL/dIm(z).
+ *   y = (1/prod N) sum_k c(k_last) Re(Y_k e^{+i theta})      (step a3)
+ *       => dY_k = (c(k_last)/prod N) sum_n dy_n e^{-i theta}  (the forward DFT of dy)
+ *   Y[b,o,k] = sum_i X[b,i,k] W[i,o,k]                        (step a2)
+ *       => dX[b,i,k] = sum_o dY[b,o,k] conj(W[i,o,k])
+ *          dW[i,o,k] = sum_b dY[b,o,k] conj(X[b,i,k])
+ *   X_k = sum_n x_n e^{-i theta}                              (step a1)
+ *       => dx_n = sum_{k kept} Re(dX_k e^{+i theta})
+ * dx is the real part of the unnormalised inverse complex FFT of the full
+ * spectrum that holds dX at the kept positions and zero elsewhere (each kept
+ * mode once, no half-spectrum weight).                                      */
+
+/* dx of nimg images from their kept-mode gradients dX.                      */
+int fno_oracle_adjoint_modes(int d, const int64_t *n, const int32_t *m,
+                             int64_t nimg, const double *dX, double *dx)
+{
+    geom_t g;
+    if (make_geom(&g, d, n, m)) return -1;
+    int64_t maxn = 1;
+    for (int a = 0; a < d; ++a) if (n[a] > maxn) maxn = n[a];
+    int err = 0;
+#pragma omp parallel
+    {
+        double *re = malloc(sizeof(double) * g.npix);
+        double *im = malloc(sizeof(double) * g.npix);
+        double *lre = malloc(sizeof(double) * maxn);
+        double *lim = malloc(sizeof(double) * maxn);
+        if (!re || !im || !lre || !lim) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+#pragma omp for schedule(dynamic)
+            for (int64_t img = 0; img < nimg; ++img) {
+                memset(re, 0, sizeof(double) * g.npix);
+                memset(im, 0, sizeof(double) * g.npix);
+                const double *Gi = dX + img * g.nkept * 2;
+                for (int64_t kk = 0; kk < g.nkept; ++kk) {
+                    int64_t f, b, l, kb;
+                    kept_mode(&g, kk, &f, &b, &l, &kb);
+                    re[f] = Gi[2 * kk];
+                    im[f] = Gi[2 * kk + 1];
+                }
+                for (int a = 0; a < d; ++a) fft_axis(re, im, d, g.n, a, +1, lre, lim);
+                double *o = dx + img * g.npix;
+                for (int64_t p = 0; p < g.npix; ++p) o[p] = re[p];
+            }
+        }
+        free(re); free(im); free(lre); free(lim);
+    }
+    return err ? -4 : 0;
+}
+
+/* The layer's gradients: dx (B, cin, N...) and dw (nblk, cin, cout, m...)
+ * complex from x, w and dy (B, cout, N...).  Either output may be NULL.    */
+int fno_oracle_spectral_conv_backward(int d, const int64_t *n, const int32_t *m,
+                                      int64_t batch, int64_t cin, int64_t cout,
+                                      const double *x, const double *w, const double *dy,
+                                      double *dx, double *dw)
+{
+    geom_t g;
+    if (make_geom(&g, d, n, m)) return -1;
+    const int64_t nlast = n[d - 1];
+    double *dY = malloc(sizeof(double) * 2 * batch * cout * g.nkept);
+    double *X = malloc(sizeof(double) * 2 * batch * cin * g.nkept);
+    int rc = (dY && X) ? 0 : -4;
+    /* dY = c(k_last) / prod N * (forward DFT of dy at the kept modes) */
+    if (!rc) rc = fno_oracle_forward_modes(d, n, m, batch * cout, dy, dY);
+    if (!rc) {
+        for (int64_t r = 0; r < batch * cout; ++r)
+            for (int64_t kk = 0; kk < g.nkept; ++kk) {
+                int64_t f, b, l, kb;
+                kept_mode(&g, kk, &f, &b, &l, &kb);
+                double c = (kb == 0 || 2 * kb == nlast) ? 1.0 : 2.0;
+                dY[(r * g.nkept + kk) * 2] *= c / (double)g.npix;
+                dY[(r * g.nkept + kk) * 2 + 1] *= c / (double)g.npix;
+            }
+    }
+    if (!rc && dx) {
+        /* dX[b,i,k] = sum_o dY[b,o,k] conj(W[blk,i,o,l]); dx = adjoint of the DFT */
+#pragma omp parallel for collapse(2) schedule(static)
+        for (int64_t b = 0; b < batch; ++b) {
+            for (int64_t i = 0; i < cin; ++i) {
+                for (int64_t kk = 0; kk < g.nkept; ++kk) {
+                    int64_t f, blk, l, kb;
+                    kept_mode(&g, kk, &f, &blk, &l, &kb);
+                    double ar = 0.0, ai = 0.0;
+                    for (int64_t o = 0; o < cout; ++o) {
+                        const double *gv = dY + ((b * cout + o) * g.nkept + kk) * 2;
+                        const double *wv = w + (((blk * cin + i) * cout + o) * g.mblk + l) * 2;
+                        ar += gv[0] * wv[0] + gv[1] * wv[1];
+                        ai += gv[1] * wv[0] - gv[0] * wv[1];
+                    }
+                    X[((b * cin + i) * g.nkept + kk) * 2] = ar;
+                    X[((b * cin + i) * g.nkept + kk) * 2 + 1] = ai;
+                }
+            }
+        }
+        rc = fno_oracle_adjoint_modes(d, n, m, batch * cin, X, dx);
+    }
+    if (!rc && dw) {
+        /* dW[blk,i,o,l] = sum_b dY[b,o,k] conj(X[b,i,k]), X the forward modes of x */
+        rc = fno_oracle_forward_modes(d, n, m, batch * cin, x, X);
+        if (!rc) {
+#pragma omp parallel for collapse(2) schedule(static)
+            for (int64_t i = 0; i < cin; ++i) {
+                for (int64_t o = 0; o < cout; ++o) {
+                    for (int64_t kk = 0; kk < g.nkept; ++kk) {
+                        int64_t f, blk, l, kb;
+                        kept_mode(&g, kk, &f, &blk, &l, &kb);
+                        double ar = 0.0, ai = 0.0;
+                        for (int64_t b = 0; b < batch; ++b) {
+                            const double *gv = dY + ((b * cout + o) * g.nkept + kk) * 2;
+                            const double *xv = X + ((b * cin + i) * g.nkept + kk) * 2;
+                            ar += gv[0] * xv[0] + gv[1] * xv[1];
+                            ai += gv[1] * xv[0] - gv[0] * xv[1];
+                        }
+                        double *wv = dw + (((blk * cin + i) * cout + o) * g.mblk + l) * 2;
+                        wv[0] = ar;
+                        wv[1] = ai;
+                    }
+                }
+            }
+        }
+    }
+    free(dY);
+    free(X);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
 /* FNO forward stack (2-D grid), channels-first:
  *   a_0 = L x + l_b                              (1x1 lift, cin_lift -> width)
  *   t_l = SpecConv_l(a_l) + P_l a_l + p_l         (l = 0 .. nlayers-1)

@@ -408,6 +408,90 @@ def test_fno_single_spectral_layer_against_numpy_fft(oracle_mod):
 
 
 # ---------------------------------------------------------------------------
+# Backward pass: pinned to the (pinned) forward by the identities a gradient
+# of a real loss must satisfy.  The layer is linear in x and in w, so with
+# L = <dy, y> the gradients are the adjoints: <dx, u> = <dy, S_w(u)> for every
+# real u, and sum Re(conj(dw) V) = <dy, S_V(x)> for every complex V.  A dropped
+# half-spectrum weight, a wrong scale, a missing conjugate or a transposed
+# weight (Cin != Cout) breaks them.  Finite differences (exact here because L
+# is linear) pin single entries, including the Nyquist bin.
+# ---------------------------------------------------------------------------
+
+BACKWARD_SHAPES = [
+    ((16,), (9,), 2, 3, 4),            # 1-D with the Nyquist bin kept
+    ((8, 16), (3, 5), 2, 3, 2),        # 2-D, two blocks
+    ((8, 8), (4, 5), 1, 2, 3),         # 2-D, touching blocks, Nyquist kept
+    ((4, 8, 8), (2, 3, 4), 2, 2, 3),   # 3-D, four blocks
+]
+
+
+def _rand_case(r, n, modes, b, ci, co):
+    nblk = 2 ** (len(n) - 1)
+    x = r.standard_normal((b, ci) + n)
+    w = r.standard_normal((nblk, ci, co) + modes) + 1j * r.standard_normal((nblk, ci, co) + modes)
+    dy = r.standard_normal((b, co) + n)
+    return x, w, dy
+
+
+@pytest.mark.parametrize("shape", BACKWARD_SHAPES)
+def test_backward_dx_is_the_adjoint(oracle_mod, shape):
+    n, modes, b, ci, co = shape
+    r = np.random.default_rng(41)
+    x, w, dy = _rand_case(r, n, modes, b, ci, co)
+    dx, _ = oracle_mod.spectral_conv_backward(x, w, dy, modes)
+    for _ in range(3):
+        u = r.standard_normal(x.shape)
+        lhs = float(np.sum(dx * u))
+        rhs = float(np.sum(dy * oracle_mod.spectral_conv(u, w, modes)))
+        assert abs(lhs - rhs) <= 1e-11 * max(1.0, abs(rhs))
+
+
+@pytest.mark.parametrize("shape", BACKWARD_SHAPES)
+def test_backward_dw_is_the_adjoint(oracle_mod, shape):
+    n, modes, b, ci, co = shape
+    r = np.random.default_rng(43)
+    x, w, dy = _rand_case(r, n, modes, b, ci, co)
+    _, dw = oracle_mod.spectral_conv_backward(x, w, dy, modes)
+    assert dw.shape == w.shape
+    for _ in range(3):
+        v = r.standard_normal(w.shape) + 1j * r.standard_normal(w.shape)
+        lhs = float(np.sum((np.conj(dw) * v).real))
+        rhs = float(np.sum(dy * oracle_mod.spectral_conv(x, v, modes)))
+        assert abs(lhs - rhs) <= 1e-11 * max(1.0, abs(rhs))
+
+
+def test_backward_finite_differences(oracle_mod):
+    # L(x, w) = <dy, S_w(x)> is linear in x and in (Re w, Im w): a unit step
+    # gives the derivative exactly
+    n, modes = (8,), (5,)                      # bin 4 = N/2 is kept
+    r = np.random.default_rng(47)
+    x, w, dy = _rand_case(r, n, modes, 2, 2, 3)
+    dx, dw = oracle_mod.spectral_conv_backward(x, w, dy, modes)
+    L = lambda xx, ww: float(np.sum(dy * oracle_mod.spectral_conv(xx, ww, modes)))
+    base = L(x, w)
+    for idx in [(0, 0, 0), (1, 1, 5), (0, 1, 7)]:
+        e = np.zeros_like(x)
+        e[idx] = 1.0
+        assert abs((L(x + e, w) - base) - dx[idx]) < 1e-11
+    for idx in [(0, 0, 0, 0), (0, 1, 2, 4), (0, 0, 1, 2)]:
+        e = np.zeros(w.shape, dtype=complex)
+        e[idx] = 1.0
+        assert abs((L(x, w + e) - base) - dw[idx].real) < 1e-11
+        assert abs((L(x, w + 1j * e) - base) - dw[idx].imag) < 1e-11
+
+
+def test_adjoint_modes_of_unit_mode(oracle_mod):
+    # one kept mode with gradient 1 at frequency (f0, k) gives cos(2 pi (f0 n0/N0 + k n1/N1))
+    n, modes = (8, 8), (2, 3)
+    dX = np.zeros((1, 4, 3), dtype=complex)
+    dX[0, 3, 2] = 1.0                          # high row 3 -> f0 = 8 - 4 + 3 = 7, k = 2
+    got = oracle_mod.adjoint_modes(dX, n, modes)
+    n0, n1 = np.meshgrid(np.arange(8), np.arange(8), indexing="ij")
+    want = np.cos(2 * np.pi * (7 * n0 / 8 + 2 * n1 / 8))
+    assert np.max(np.abs(got[0] - want)) < 1e-13
+
+
+# ---------------------------------------------------------------------------
 # Workload generators: shapes and determinism only (no arithmetic to pin)
 # ---------------------------------------------------------------------------
 
