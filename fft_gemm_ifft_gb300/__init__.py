@@ -89,6 +89,30 @@ class SpectralConv:
 
     __call__ = forward
 
+    def backward(self, x, w, dy, need_dx=True, need_dw=True, dx=None, dw=None, stream=None):
+        """Gradients (dx, dw) of a real loss given dy = dL/dy; the plan must have
+        been made with FNO_PLAN_BACKWARD.  dw is dL/dRe(w) + i dL/dIm(w) in w's
+        interleaved layout.  Either may be skipped (returned as None)."""
+        import torch
+        _require(dy, self.torch_dtype, self.y_shape, "dy")
+        if need_dx:
+            _require(w, self.torch_dtype, self.w_shape, "w")
+            if dx is None:
+                dx = torch.empty(self.x_shape, dtype=self.torch_dtype, device=dy.device)
+            _require(dx, self.torch_dtype, self.x_shape, "dx")
+        if need_dw:
+            _require(x, self.torch_dtype, self.x_shape, "x")
+            if dw is None:
+                dw = torch.empty(self.w_shape, dtype=self.torch_dtype, device=dy.device)
+            _require(dw, self.torch_dtype, self.w_shape, "dw")
+        ptr = lambda t: t.data_ptr() if t is not None else None
+        ws = self.workspace.data_ptr() if self.workspace is not None else None
+        check(capi.fno_spectral_conv_backward(
+            self.handle, ptr(x) if need_dw else None, ptr(w) if need_dx else None, dy.data_ptr(),
+            ptr(dx) if need_dx else None, ptr(dw) if need_dw else None, ws,
+            _stream_handle(stream)), "fno_spectral_conv_backward")
+        return (dx if need_dx else None), (dw if need_dw else None)
+
     def device_error(self, stream=None) -> int:
         return capi.fno_plan_get_device_error(self.handle, _stream_handle(stream))
 

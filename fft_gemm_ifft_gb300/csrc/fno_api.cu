@@ -73,7 +73,7 @@ int choose_path(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int co
 }
 
 struct Sizes {
-    size_t workspace, weight;
+    size_t workspace, weight, adjoint_workspace;
     int path, kernels;
 };
 
@@ -84,7 +84,8 @@ fno_status_t describe(int ndim, const int64_t *n, const int32_t *modes, int64_t 
     if (st != FNO_OK) return st;
     if (batch < 1 || cin < 1 || cout < 1) return FNO_ERR_INVALID_ARG;
     if (dtype != FNO_F32 && dtype != FNO_F16 && dtype != FNO_BF16) return FNO_ERR_INVALID_ARG;
-    if (flags & ~(FNO_PLAN_UNFUSED | FNO_PLAN_TRACE | FNO_PLAN_TENSOR_CORES | FNO_PLAN_PERSISTENT))
+    if (flags & ~(FNO_PLAN_UNFUSED | FNO_PLAN_TRACE | FNO_PLAN_TENSOR_CORES |
+                  FNO_PLAN_PERSISTENT | FNO_PLAN_BACKWARD))
         return FNO_ERR_INVALID_ARG;
     // int64 element counts must not overflow and a tensor must stay addressable
     const double xe = (double)batch * cin * g->npix, ye = (double)batch * cout * g->npix;
@@ -98,6 +99,19 @@ fno_status_t describe(int ndim, const int64_t *n, const int32_t *modes, int64_t 
         sz->kernels = fused_kernel_count(*g, dtype, batch, cin, cout, flags);
     }
     sz->weight = (size_t)g->nblk * cin * cout * g->mblk * 2 * elem_bytes(dtype);
+    sz->adjoint_workspace = 0;
+    if (flags & FNO_PLAN_BACKWARD) {
+        // the adjoint layer (Cout -> Cin) runs dx; its plan never traces
+        Geom ga;
+        Sizes sa;
+        st = describe(ndim, n, modes, batch, cout, cin, dtype,
+                      flags & ~(FNO_PLAN_BACKWARD | FNO_PLAN_TRACE), &ga, &sa);
+        if (st != FNO_OK) return st;
+        sz->adjoint_workspace = sa.workspace;
+        const BackwardLayout bl =
+            backward_layout(*g, batch, cin, cout, sz->weight, sa.workspace);
+        if (bl.total > sz->workspace) sz->workspace = bl.total;
+    }
     return FNO_OK;
 }
 
@@ -206,6 +220,22 @@ fno_status_t fno_spectral_conv_plan(fno_plan_t *out, int ndim, const int64_t *n,
         delete p;
         return FNO_ERR_CUDA;
     }
+    if (flags & FNO_PLAN_BACKWARD) {
+        st = fno_spectral_conv_plan(&p->adjoint, ndim, n, modes, batch, cout, cin, dtype,
+                                    flags & ~(FNO_PLAN_BACKWARD | FNO_PLAN_TRACE));
+        if (st != FNO_OK) {
+            fno_plan_destroy(reinterpret_cast<fno_plan_t>(p));
+            return st;
+        }
+        const BackwardLayout bl = backward_layout(g, batch, cin, cout, sz.weight,
+                                                  sz.adjoint_workspace);
+        p->bw_wt = bl.wt;
+        p->bw_adj = bl.adj;
+        p->bw_x = bl.x;
+        p->bw_g = bl.g;
+        p->bw_sa = bl.sa;
+        p->bw_sb = bl.sb;
+    }
     *out = reinterpret_cast<fno_plan_t>(p);
     return FNO_OK;
 }
@@ -252,6 +282,56 @@ fno_status_t fno_spectral_conv_forward(fno_plan_t plan, const void *x, const voi
     return FNO_OK;
 }
 
+fno_status_t fno_spectral_conv_backward(fno_plan_t plan, const void *x, const void *w,
+                                        const void *dy, void *dx, void *dw, void *workspace,
+                                        fno_stream_t stream) {
+    if (!plan || !dy || (!dx && !dw)) return FNO_ERR_INVALID_ARG;
+    const Plan &p = *reinterpret_cast<Plan *>(plan);
+    if (!(p.flags & FNO_PLAN_BACKWARD) || !p.adjoint) return FNO_ERR_INVALID_ARG;
+    if ((dx && !w) || (dw && !x) || (p.workspace_bytes && !workspace))
+        return FNO_ERR_INVALID_ARG;
+    const void *ptrs[] = {x, w, dy, dx, dw, workspace};
+    for (const void *q : ptrs)
+        if (q && !aligned16(q)) return FNO_ERR_MISALIGNED;
+    const size_t eb = elem_bytes(p.dtype);
+    const size_t xb = (size_t)p.batch * p.cin * p.g.npix * eb;
+    const size_t yb = (size_t)p.batch * p.cout * p.g.npix * eb;
+    const size_t wb = p.weight_bytes, wsb = p.workspace_bytes;
+    if (dx && (overlaps(dx, xb, x, xb) || overlaps(dx, xb, w, wb) || overlaps(dx, xb, dy, yb) ||
+               overlaps(dx, xb, dw, wb) || overlaps(dx, xb, workspace, wsb)))
+        return FNO_ERR_ALIASING;
+    if (dw && (overlaps(dw, wb, x, xb) || overlaps(dw, wb, w, wb) || overlaps(dw, wb, dy, yb) ||
+               overlaps(dw, wb, workspace, wsb)))
+        return FNO_ERR_ALIASING;
+    if (inject("launch")) return FNO_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    if (dx) {
+        // dx = the layer applied to dy with W' = conj(W) transposed (Cout -> Cin)
+        if (launch_adjoint_weights(p, w, ws + p.bw_wt, s) != cudaSuccess) {
+            cudaGetLastError();
+            return FNO_ERR_CUDA;
+        }
+        fno_status_t st = fno_spectral_conv_forward(p.adjoint, dy, ws + p.bw_wt, dx,
+                                                    ws + p.bw_adj, stream);
+        if (st != FNO_OK) return st;
+    }
+    if (dw) {
+        float2 *X = reinterpret_cast<float2 *>(ws + p.bw_x);
+        float2 *G = reinterpret_cast<float2 *>(ws + p.bw_g);
+        float2 *sa = reinterpret_cast<float2 *>(ws + p.bw_sa);
+        float2 *sb = reinterpret_cast<float2 *>(ws + p.bw_sb);
+        cudaError_t e = unfused_forward_modes(p, x, p.batch * p.cin, sa, sb, X, s);
+        if (e == cudaSuccess) e = unfused_forward_modes(p, dy, p.batch * p.cout, sa, sb, G, s);
+        if (e == cudaSuccess) e = launch_grad_w(p, X, G, dw, s);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return FNO_ERR_CUDA;
+        }
+    }
+    return FNO_OK;
+}
+
 fno_status_t fno_plan_get_trace(fno_plan_t plan, fno_trace_record_t *records, size_t capacity,
                                 size_t *count) {
     if (!plan || !count) return FNO_ERR_INVALID_ARG;
@@ -290,10 +370,11 @@ fno_status_t fno_plan_destroy(fno_plan_t plan) {
     if (!plan) return FNO_OK;
     Plan *p = reinterpret_cast<Plan *>(plan);
     cudaError_t e = cudaSuccess;
+    fno_status_t st = fno_plan_destroy(p->adjoint);
     if (p->path != kPathUnfused) fused_plan_release(*p);
     if (p->dev_tables) e = cudaFree(p->dev_tables);
     delete p;
-    return from_cuda(e);
+    return st != FNO_OK ? st : from_cuda(e);
 }
 
 }  // extern "C"

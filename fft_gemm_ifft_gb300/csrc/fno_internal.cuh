@@ -56,7 +56,17 @@ struct Plan {
     void *fused_tables;           // tensor-core path: twiddle operands (plan-owned)
     fno_trace_record_t *trace;    // FNO_PLAN_TRACE: one record per work item (plan-owned)
     size_t trace_records;         // records one forward call produces
+    // FNO_PLAN_BACKWARD: the adjoint layer's plan and the backward workspace map
+    fno_plan_t adjoint;
+    size_t bw_wt, bw_adj, bw_x, bw_g, bw_sa, bw_sb;   // byte offsets in the workspace
 };
+
+// Backward workspace map of a description (offsets and total size).
+struct BackwardLayout {
+    size_t wt, adj, x, g, sa, sb, total;
+};
+BackwardLayout backward_layout(const Geom &g, int64_t batch, int cin, int cout,
+                               size_t weight_bytes, size_t adjoint_workspace);
 
 enum { kPathUnfused = 0, kPathFused = 1 };
 
@@ -141,5 +151,15 @@ cudaError_t launch_axis_forward(const float2 *in, float2 *out, int64_t outer, in
 cudaError_t launch_axis_inverse(const float2 *in, float2 *out, int64_t outer, int n, int64_t inner,
                                 int m, const float2 *tw, int num_sms, cudaStream_t s);
 cudaError_t launch_mix(const Plan &p, const float2 *X, const void *w, float2 *Y, cudaStream_t s);
+// Truncated forward DFT of nch real images x (storage dtype of p) to their
+// kept modes out[nch][|K|], through the per-axis kernels; sa, sb hold
+// unfused_modes_scratch_elems(g, nch) complex values each.
+int64_t unfused_modes_scratch_elems(const Geom &g, int64_t nch);
+cudaError_t unfused_forward_modes(const Plan &p, const void *x, int64_t nch, float2 *sa,
+                                  float2 *sb, float2 *out, cudaStream_t s);
+// Backward kernels (fno_backward.cu).
+cudaError_t launch_adjoint_weights(const Plan &p, const void *w, void *wt, cudaStream_t s);
+cudaError_t launch_grad_w(const Plan &p, const float2 *X, const float2 *G, void *dw,
+                          cudaStream_t s);
 
 }  // namespace fno

@@ -253,6 +253,55 @@ static cudaError_t unfused_forward_t(const Plan &p, const Buffers &bf, cudaStrea
     return cudaGetLastError();
 }
 
+int64_t unfused_modes_scratch_elems(const Geom &g, int64_t nch) {
+    const int d = g.d;
+    const int64_t ml = g.m[d - 1];
+    int64_t best = 0;
+    if (d > 1) {
+        int64_t s0 = nch * ml;
+        for (int j = 0; j < d - 1; ++j) s0 *= g.n[j];
+        best = s0;
+    }
+    // outputs of the full-axis passes a = d-2 .. 1 (the pass a = 0 writes out)
+    for (int a = d - 2; a >= 1; --a) {
+        int64_t s = nch * ml;
+        for (int j = 0; j < d - 1; ++j) s *= (j < a) ? g.n[j] : g.kdim[j];
+        best = std::max(best, s);
+    }
+    return best;
+}
+
+template <typename T>
+static cudaError_t forward_modes_t(const Plan &p, const T *x, int64_t nch, float2 *sa,
+                                   float2 *sb, float2 *out, cudaStream_t s) {
+    const Geom &g = p.g;
+    const int d = g.d;
+    const int64_t ml = g.m[d - 1];
+    int64_t lines = nch;
+    for (int j = 0; j < d - 1; ++j) lines *= g.n[j];
+    float2 *cur = d == 1 ? out : sa;
+    k_fwd_last<T><<<grid_for(lines * ml, p.num_sms), kThreads, 0, s>>>(
+        x, cur, lines, (int)g.n[d - 1], (int)ml, p.tw[d - 1]);
+    for (int a = d - 2; a >= 0; --a) {
+        float2 *dst = a == 0 ? out : (cur == sa ? sb : sa);
+        int64_t outer = nch, inner = ml;
+        for (int j = 0; j < a; ++j) outer *= g.n[j];
+        for (int j = a + 1; j < d - 1; ++j) inner *= g.kdim[j];
+        k_fwd_full<<<grid_for(outer * g.kdim[a] * inner, p.num_sms), kThreads, 0, s>>>(
+            cur, dst, outer, (int)g.n[a], inner, g.m[a], p.tw[a]);
+        cur = dst;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t unfused_forward_modes(const Plan &p, const void *x, int64_t nch, float2 *sa,
+                                  float2 *sb, float2 *out, cudaStream_t s) {
+    return with_storage(p.dtype, [&](auto t) {
+        using T = decltype(t);
+        return forward_modes_t<T>(p, static_cast<const T *>(x), nch, sa, sb, out, s);
+    });
+}
+
 cudaError_t launch_axis_forward(const float2 *in, float2 *out, int64_t outer, int n, int64_t inner,
                                 int m, const float2 *tw, int num_sms, cudaStream_t s) {
     k_fwd_full<<<grid_for(outer * 2 * m * inner, num_sms), kThreads, 0, s>>>(in, out, outer, n,

@@ -91,6 +91,10 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * queue instead of three kernels chained by programmatic dependent launch
  * (the default).  FNO_PLAN_TRACE records only this variant.               */
 #define FNO_PLAN_PERSISTENT 8u
+/* Also prepare the plan for fno_spectral_conv_backward: the plan then holds
+ * an internal plan of the adjoint layer (Cin and Cout swapped) and reports a
+ * workspace size that covers the backward call as well.                    */
+#define FNO_PLAN_BACKWARD 16u
 
 /* One work item of the fused kernel, as recorded under FNO_PLAN_TRACE.
  * Times are the GPU's global nanosecond timer.                              */
@@ -198,6 +202,26 @@ fno_status_t fno_spectral_conv_forward_static(int ndim, const int64_t *n,
                                               int32_t cin, int32_t cout, fno_dtype_t dtype,
                                               const void *x, const void *w, void *y,
                                               fno_stream_t stream);
+
+/* Gradients of the layer for a real loss L, given dy = dL/dy (B, Cout, N...)
+ * in the storage dtype.  The pages define only the forward pass; this is its
+ * derivative, with dz = dL/dRe(z) + i dL/dIm(z) for a complex z:
+ *   dY = c(k_last) / prod(N) * (truncated forward DFT of dy),
+ *   dx = the layer applied to dy with the weights W'[blk][o][i] =
+ *        conj(W[blk][i][o]) (Cout -> Cin): the fused forward path of the
+ *        adjoint plan, after one kernel writes W' into the workspace;
+ *   dw[blk][i][o][l] = sum_b dY[b][o][k] conj(X[b][i][k]), X the truncated
+ *        forward DFT of x (dense per-axis DFT kernels plus one reduction
+ *        kernel over the batch), same layout and dtype as w.
+ * dx (B, Cin, N...) or dw may be NULL to skip it (not both); x is needed only
+ * for dw, w only for dx.  The plan must have been made with
+ * FNO_PLAN_BACKWARD; the workspace is the plan's (fno_spectral_conv_workspace_size).
+ * Asynchronous on `stream`; no allocation.  Errors: INVALID_ARG (NULL
+ * handle, missing flag, missing operand), MISALIGNED, ALIASING (an output
+ * overlaps an input, the other output or the workspace), CUDA.              */
+fno_status_t fno_spectral_conv_backward(fno_plan_t plan, const void *x, const void *w,
+                                        const void *dy, void *dx, void *dw, void *workspace,
+                                        fno_stream_t stream);
 
 /* Copy the trace of the plan's last forward call (FNO_PLAN_TRACE) to host
  * memory: up to `capacity` records, ordered by ticket (three-kernel variants:

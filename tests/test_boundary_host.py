@@ -137,3 +137,14 @@ def test_model_desc_validation(L):
     d.cout = 1
     d.dtype = F16
     assert capi.fno_model_plan(d)[0] == capi.FNO_ERR_UNSUPPORTED
+
+
+def test_backward_flag_adds_workspace(L):
+    st, ws0, wb = Q(2, [128, 128], [16, 16], 8, 32, 16, F32)
+    assert st == capi.FNO_OK
+    st, ws1, wb1 = Q(2, [128, 128], [16, 16], 8, 32, 16, F32, flags=capi.FNO_PLAN_BACKWARD)
+    assert st == capi.FNO_OK and wb1 == wb
+    # the adjoint weights, the kept modes of x (8*32*512) and dy (8*16*512)
+    assert ws1 >= wb + 8 * 32 * 512 * 8 + 8 * 16 * 512 * 8
+    st, _, _ = Q(1, [16], [4], 1, 1, 1, F32, flags=capi.FNO_PLAN_BACKWARD | 0x40)
+    assert st == capi.FNO_ERR_INVALID_ARG
