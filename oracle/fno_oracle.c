@@ -25,6 +25,8 @@
  * Method, in the order the pages give it:
  *   1. complex radix-2 FFT (bit reversal + butterflies, twiddles from libm
  *      cos/sin in double) along every axis of each (batch, channel) image;
+ *      an axis whose length is not a power of two takes the plain O(N^2)
+ *      DFT sum instead;
  *   2. explicit loops pick the kept modes block by block;
  *   3. explicit triple loop for the per-mode mixing;
  *   4. scatter the mixed modes into a zero full spectrum with the c(k)
@@ -49,8 +51,34 @@
 /* ------------------------------------------------------------------------ */
 /* 1-D complex radix-2 FFT, in place.  sign = -1: forward kernel
  * e^{-2 pi i k n/N}; sign = +1: inverse kernel, no normalisation.           */
+static void direct_dft(double *re, double *im, int64_t n, int sign)
+{
+    double *tr = malloc(sizeof(double) * n), *ti = malloc(sizeof(double) * n);
+    if (!tr || !ti) { free(tr); free(ti); return; }
+    for (int64_t k = 0; k < n; ++k) {
+        double sr = 0.0, si = 0.0;
+        for (int64_t j = 0; j < n; ++j) {
+            /* angle of (j k mod n) / n: the product is reduced exactly first */
+            double ang = (double)sign * 2.0 * ORACLE_PI * (double)((j * k) % n) / (double)n;
+            double c = cos(ang), s = sin(ang);
+            sr += re[j] * c - im[j] * s;
+            si += re[j] * s + im[j] * c;
+        }
+        tr[k] = sr;
+        ti[k] = si;
+    }
+    memcpy(re, tr, sizeof(double) * n);
+    memcpy(im, ti, sizeof(double) * n);
+    free(tr);
+    free(ti);
+}
+
 void fno_oracle_fft(double *re, double *im, int64_t n, int sign)
 {
+    if (n & (n - 1)) {          /* not a power of two */
+        direct_dft(re, im, n, sign);
+        return;
+    }
     /* bit-reversal permutation */
     int64_t j = 0;
     for (int64_t i = 1; i < n; ++i) {
@@ -129,7 +157,7 @@ static int make_geom(geom_t *g, int d, const int64_t *n, const int32_t *m)
     for (int a = 0; a < d; ++a) {
         g->n[a] = n[a];
         g->m[a] = m[a];
-        if (n[a] < 1 || (n[a] & (n[a] - 1))) return -2;     /* radix-2 only */
+        if (n[a] < 1) return -2;
         if (a < d - 1) {
             if (m[a] < 1 || 2 * (int64_t)m[a] > n[a]) return -3;
             g->kdim[a] = 2 * (int64_t)m[a];

@@ -59,7 +59,7 @@ def rng(seed):
 # 1-D radix-2 FFT
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("n", [1, 2, 4, 8, 16, 32, 64, 256])
+@pytest.mark.parametrize("n", [1, 2, 4, 8, 16, 32, 64, 256, 3, 6, 12, 15, 100])
 @pytest.mark.parametrize("inverse", [False, True])
 def test_fft_matches_brute_force(oracle_mod, n, inverse):
     r = rng(n)
@@ -116,6 +116,7 @@ def test_fft_parseval_linearity_shift(oracle_mod):
 @pytest.mark.parametrize("n,modes", [
     ((16,), (5,)), ((16,), (9,)), ((8, 8), (2, 3)), ((8, 16), (4, 9)),
     ((4, 4, 8), (1, 2, 3)), ((4, 8, 8), (2, 1, 5)),
+    ((12,), (7,)), ((6, 10), (2, 4)), ((5, 6, 7), (2, 3, 4)),      # any extent
 ])
 def test_forward_modes_brute_force(oracle_mod, n, modes):
     r = rng(sum(n) + sum(modes))
@@ -170,7 +171,8 @@ def inverse_brute(Y, n, modes):
     return y / np.prod(n)
 
 
-@pytest.mark.parametrize("n,modes", [((16,), (9,)), ((8, 8), (2, 5)), ((4, 4, 8), (2, 1, 3))])
+@pytest.mark.parametrize("n,modes", [((16,), (9,)), ((8, 8), (2, 5)), ((4, 4, 8), (2, 1, 3)),
+                                     ((12,), (7,)), ((6, 9), (3, 5)), ((5, 6, 7), (2, 2, 4))])
 def test_inverse_modes_brute_force_and_numpy(oracle_mod, n, modes):
     r = rng(3 + len(n))
     kshape = oracle_mod.kept_shape(n, modes)
@@ -419,6 +421,7 @@ def test_fno_single_spectral_layer_against_numpy_fft(oracle_mod):
 
 BACKWARD_SHAPES = [
     ((16,), (9,), 2, 3, 4),            # 1-D with the Nyquist bin kept
+    ((6, 9), (2, 5), 2, 2, 3),         # extents that are not powers of two
     ((8, 16), (3, 5), 2, 3, 2),        # 2-D, two blocks
     ((8, 8), (4, 5), 1, 2, 3),         # 2-D, touching blocks, Nyquist kept
     ((4, 8, 8), (2, 3, 4), 2, 2, 3),   # 3-D, four blocks
