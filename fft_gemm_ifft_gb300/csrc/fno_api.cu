@@ -19,7 +19,7 @@ using namespace fno;
 namespace {
 
 constexpr int kVersion = 10000;   // 1.0.0
-constexpr int64_t kMaxN = 1024;
+constexpr int64_t kMaxN = 4096;
 
 // Host-side fault injection for the failure-path tests: FNO_FAULT_INJECT names
 // one site ("plan_alloc" or "launch") at which the library behaves as if the
@@ -29,7 +29,6 @@ bool inject(const char *site) {
     return v && std::strcmp(v, site) == 0;
 }
 
-bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
 
 fno_status_t make_geom(Geom *g, int ndim, const int64_t *n, const int32_t *modes) {
     if (ndim < 1 || ndim > FNO_MAX_NDIM || !n || !modes) return FNO_ERR_INVALID_ARG;
@@ -37,7 +36,7 @@ fno_status_t make_geom(Geom *g, int ndim, const int64_t *n, const int32_t *modes
     g->d = ndim;
     g->nkept = g->npix = g->nblk = g->mblk = 1;
     for (int a = 0; a < ndim; ++a) {
-        if (!is_pow2(n[a]) || n[a] < 2) return FNO_ERR_INVALID_ARG;
+        if (n[a] < 2) return FNO_ERR_INVALID_ARG;
         if (n[a] > kMaxN) return FNO_ERR_UNSUPPORTED;
         const int64_t m = modes[a];
         if (m < 1) return FNO_ERR_INVALID_ARG;

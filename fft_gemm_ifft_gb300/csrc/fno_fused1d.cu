@@ -113,7 +113,7 @@ k_fused1d(const T *__restrict__ x, const T *__restrict__ w, T *__restrict__ y, i
 
 bool fused1d_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout) {
     return g.d == 1 && (dtype == FNO_F32 || dtype == FNO_F16 || dtype == FNO_BF16) &&
-           g.n[0] <= 1024 &&
+           g.n[0] <= 1024 && (g.n[0] & (g.n[0] - 1)) == 0 &&
            batch * kG1 < (1ll << 31) &&
            smem1_bytes((int)g.n[0], g.m[0], cin, cout) <= kSmem1Max;
 }

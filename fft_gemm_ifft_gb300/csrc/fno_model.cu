@@ -236,6 +236,8 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
         d->cout < 1)
         return FNO_ERR_INVALID_ARG;
     if (d->cout > kMaxCout || d->batch > 65535) return FNO_ERR_UNSUPPORTED;
+    // the tiled 1x1 linears move pixel rows in 16-byte copies
+    if ((d->h * d->w) % 4 != 0) return FNO_ERR_UNSUPPORTED;
     if (d->dtype != FNO_F32) return FNO_ERR_UNSUPPORTED;
     const int64_t n[2] = {d->h, d->w};
     size_t spec_ws = 0;

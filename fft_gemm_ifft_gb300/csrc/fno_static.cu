@@ -99,6 +99,9 @@ extern "C" fno_status_t fno_spectral_conv_forward_static(
                                               FNO_PLAN_UNFUSED, nullptr, &weight_bytes);
     if (st != FNO_OK) return st;
     if (!x || !w || !y) return FNO_ERR_INVALID_ARG;
+    // the static twiddle tables cover power-of-two extents up to kMaxStaticN
+    for (int a = 0; a < ndim; ++a)
+        if (n[a] > kMaxStaticN || (n[a] & (n[a] - 1)) != 0) return FNO_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return FNO_ERR_MISALIGNED;
 
     Plan p{};

@@ -6,7 +6,7 @@
 // step of §2.1-§2.3 is its own launch and the intermediates round-trip
 // through device memory.  Every axis pass is a direct (dense) DFT over the
 // kept frequencies only, so it is exact up to float rounding for any
-// power-of-two extent; it serves as the ablation baseline and covers shapes
+// extent; it serves as the ablation baseline and covers shapes
 // the fused kernels are not specialised for.
 #include <algorithm>
 
@@ -23,6 +23,12 @@ struct KeptGeom {            // by-value kernel argument
     int32_t m[FNO_MAX_NDIM];
     int64_t nkept, mblk;
 };
+
+// (k n) mod N for a twiddle-table index: a mask for power-of-two N, else a
+// remainder (the product stays below 2^31 for N <= 4096)
+__device__ __forceinline__ int tw_idx(int prod, int N) {
+    return (N & (N - 1)) == 0 ? (prod & (N - 1)) : (prod % N);
+}
 
 // Frequency of kept row r on a full axis: low rows 0..m-1, then high rows
 // N-m..N-1 (TurboFNO §2.2 keeps the low-frequency modes; the high rows are
@@ -45,7 +51,7 @@ k_fwd_last(const T *__restrict__ x, float2 *__restrict__ out, int64_t nlines, in
         float2 acc = make_float2(0.f, 0.f);
         for (int n = 0; n < N; ++n) {
             const float v = Storage<T>::load(src + n);
-            const float2 w = tw[(k * n) & (N - 1)];
+            const float2 w = tw[tw_idx(k * n, N)];
             acc.x = fmaf(v, w.x, acc.x);
             acc.y = fmaf(v, w.y, acc.y);
         }
@@ -68,7 +74,7 @@ k_fwd_full(const float2 *__restrict__ in, float2 *__restrict__ out, int64_t oute
         const int f = kept_freq(r, m, N);
         const float2 *src = in + o * N * inner + q;
         float2 acc = make_float2(0.f, 0.f);
-        for (int n = 0; n < N; ++n) cfma(acc, src[n * inner], tw[(f * n) & (N - 1)]);
+        for (int n = 0; n < N; ++n) cfma(acc, src[n * inner], tw[tw_idx(f * n, N)]);
         out[idx] = acc;
     }
 }
@@ -123,7 +129,7 @@ k_inv_full(const float2 *__restrict__ in, float2 *__restrict__ out, int64_t oute
         const float2 *src = in + o * K * inner + q;
         float2 acc = make_float2(0.f, 0.f);
         for (int r = 0; r < K; ++r) {
-            const float2 w = tw[(kept_freq(r, m, N) * n) & (N - 1)];
+            const float2 w = tw[tw_idx(kept_freq(r, m, N) * n, N)];
             cfma(acc, src[r * inner], make_float2(w.x, -w.y));   // conjugate twiddle
         }
         out[idx] = acc;
@@ -146,7 +152,7 @@ k_inv_last(const float2 *__restrict__ in, T *__restrict__ y, int64_t nlines, int
         for (int k = 0; k < M; ++k) {
             const float c = (k == 0 || 2 * k == N) ? 1.f : 2.f;
             const float2 v = src[k];
-            const float2 w = tw[(k * n) & (N - 1)];
+            const float2 w = tw[tw_idx(k * n, N)];
             // Re(v * conj(w)) with w = e^{-i theta}
             acc = fmaf(c, fmaf(v.x, w.x, v.y * w.y), acc);
         }

@@ -27,6 +27,8 @@ def main(argv=None) -> int:
     ap.add_argument("--trace", default="", help="write the last call's work-item trace "
                     "(CSV) here and print a per-phase summary")
     ap.add_argument("--time", action="store_true", help="time each forward with CUDA events")
+    ap.add_argument("--backward", action="store_true",
+                    help="run (and time) fno_spectral_conv_backward (dx and dw) instead")
     args = ap.parse_args(argv)
 
     import torch
@@ -40,6 +42,8 @@ def main(argv=None) -> int:
         case = case.with_batch(args.batch)
     from . import capi
     flags = args.flags | (capi.FNO_PLAN_TRACE if args.trace else 0)
+    if args.backward:
+        flags |= capi.FNO_PLAN_BACKWARD
     conv = SpectralConv(case.n, case.modes, case.batch, case.cin, case.cout, case.dtype, flags)
     x_np, w_np = workloads.make_x(case), workloads.make_w(case)
     set_bytes = x_np.nbytes + w_np.nbytes + math.prod(case.y_shape) * case.elem_bytes
@@ -49,6 +53,13 @@ def main(argv=None) -> int:
     ws = [workloads.to_torch_storage(w_np, case.dtype).cuda() for _ in range(nsets)]
     ys = [torch.empty(case.y_shape, dtype=conv.torch_dtype, device="cuda") for _ in range(nsets)]
     step = lambda i: conv(xs[i % nsets], ws[i % nsets], ys[i % nsets])
+    if args.backward:
+        dxs = [torch.empty_like(x) for x in xs]
+        dws = [torch.empty_like(w) for w in ws]
+        step = lambda i: conv.backward(xs[i % nsets], ws[i % nsets], ys[(i + 1) % nsets],
+                                       dx=dxs[i % nsets], dw=dws[i % nsets])
+        for y in ys:
+            y.copy_(torch.randn(y.shape, dtype=torch.float32).to(y.dtype))
     if args.time:
         report_times(case.name, case.batch, time_steps(step, args.iters))
     else:

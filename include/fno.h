@@ -122,11 +122,13 @@ int fno_version(void);
 /* Validate a layer description and report its memory needs without touching
  * the GPU (no CUDA call is made).
  *   ndim          1, 2 or 3
- *   n[ndim]       spatial extents; each a power of two, 2 <= N <= 1024
+ *   n[ndim]       spatial extents, 2 <= N <= 4096 (any length: extents
+ *                 that are not powers of two, and shapes without a fused
+ *                 kernel, run on the separate per-axis kernels)
  *   modes[ndim]   per-block modes; 1 <= m_a and 2 m_a <= N_a on full axes,
  *                 1 <= m_{d-1} <= N_{d-1}/2 + 1 on the last axis
  *   batch, cin, cout  >= 1
- *   dtype         FNO_F32 or FNO_F16
+ *   dtype         FNO_F32, FNO_F16 or FNO_BF16
  *   flags         FNO_PLAN_* bits
  * Outputs (each may be NULL):
  *   workspace_bytes  device scratch the forward call needs (caller-owned)
@@ -275,7 +277,9 @@ typedef struct fno_model_params_s {
 } fno_model_params_t;
 
 /* Validate the description and create the stack's plan (one spectral plan
- * shared by the layers).  Errors as for fno_spectral_conv_plan.            */
+ * shared by the layers).  Errors as for fno_spectral_conv_plan; also
+ * UNSUPPORTED for dtype other than FNO_F32, cout > 8, batch > 65535, or
+ * h*w not a multiple of 4.                                                  */
 fno_status_t fno_model_plan(fno_model_t *model, const fno_model_desc_t *desc);
 
 /* Device workspace bytes fno_forward needs (activations + layer scratch).  */

@@ -23,6 +23,8 @@ CASES = [
     ((16, 32), (3, 7), 2, 3, 5, "f32"),
     ((8, 8, 16), (2, 3, 9), 2, 2, 3, "bf16"),
     ((32, 32), (4, 4), 3, 4, 2, "bf16"),
+    ((6, 9), (2, 5), 2, 2, 3, "f32"),
+    ((1000,), (40,), 2, 3, 2, "f32"),
 ]
 
 

@@ -66,7 +66,8 @@ def test_query_valid(L, args, wbytes):
 @pytest.mark.parametrize("args,code", [
     ((0, [8], [2], 1, 1, 1, F32), capi.FNO_ERR_INVALID_ARG),           # rank 0
     ((4, [8] * 4, [2] * 4, 1, 1, 1, F32), capi.FNO_ERR_INVALID_ARG),   # rank 4
-    ((1, [12], [2], 1, 1, 1, F32), capi.FNO_ERR_INVALID_ARG),          # not a power of two
+    ((1, [12], [2], 1, 1, 1, F32), capi.FNO_OK),                       # any extent
+    ((1, [12], [8], 1, 1, 1, F32), capi.FNO_ERR_INVALID_ARG),          # m > N/2 + 1
     ((1, [1], [1], 1, 1, 1, F32), capi.FNO_ERR_INVALID_ARG),           # N < 2
     ((1, [16], [0], 1, 1, 1, F32), capi.FNO_ERR_INVALID_ARG),          # m = 0
     ((1, [16], [10], 1, 1, 1, F32), capi.FNO_ERR_INVALID_ARG),         # m > N/2 + 1
@@ -77,7 +78,8 @@ def test_query_valid(L, args, wbytes):
     ((1, [16], [4], 1, 1, -2, F32), capi.FNO_ERR_INVALID_ARG),         # cout < 0
     ((1, [16], [4], 1, 1, 1, 7), capi.FNO_ERR_INVALID_ARG),            # dtype
     ((1, [16], [4], 1, 1, 1, 3), capi.FNO_ERR_INVALID_ARG),            # dtype
-    ((1, [2048], [4], 1, 1, 1, F32), capi.FNO_ERR_UNSUPPORTED),        # N too large
+    ((1, [4096], [4], 1, 1, 1, F32), capi.FNO_OK),
+    ((1, [4097], [4], 1, 1, 1, F32), capi.FNO_ERR_UNSUPPORTED),        # N too large
 ])
 def test_query_rejects(L, args, code):
     st, _, _ = Q(*args)
@@ -136,6 +138,10 @@ def test_model_desc_validation(L):
     assert capi.fno_model_plan(d)[0] == capi.FNO_ERR_UNSUPPORTED
     d.cout = 1
     d.dtype = F16
+    assert capi.fno_model_plan(d)[0] == capi.FNO_ERR_UNSUPPORTED
+    d.dtype = F32
+    d.h, d.w = 5, 6                        # h*w not a multiple of 4
+    d.modes[0], d.modes[1] = 2, 3
     assert capi.fno_model_plan(d)[0] == capi.FNO_ERR_UNSUPPORTED
 
 

@@ -44,7 +44,8 @@ def test_small_stack_matches_oracle():
     (3, 70, 1, 16, 16, (4, 4), 70, 3),
     (2, 5, 2, 2, 2, (1, 1), 9, 1),
     (1, 12, 2, 8, 16, (2, 3), 130, 8),
-], ids=["ragged_channels", "tiny_grid", "wide_hidden"])
+    (2, 6, 1, 12, 20, (3, 4), 10, 1),
+], ids=["ragged_channels", "tiny_grid", "wide_hidden", "grid_not_power_of_two"])
 def test_stack_ragged_tiles(shape):
     b, width, nl, h, w, modes, hidden, cout = shape
     case = workloads.FnoCase("ragged", batch=b, width=width, nlayers=nl, h=h, w=w,

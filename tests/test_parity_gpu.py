@@ -39,6 +39,14 @@ SMALL = [
     ((256, 256), (32, 32), 3, 4, 2, "f32"),
     ((64, 64), (8, 8), 2, 4, 6, "f16"),
     ((64, 64, 64), (16, 16, 16), 1, 4, 4, "f32"),
+    # extents that are not powers of two, and large extents (separate kernels)
+    ((12,), (7,), 2, 3, 4, "f32"),
+    ((2048,), (64,), 2, 4, 4, "f32"),
+    ((3000,), (100,), 1, 2, 3, "f32"),
+    ((4096,), (17,), 1, 2, 2, "bf16"),
+    ((6, 10), (2, 4), 2, 3, 2, "f32"),
+    ((24, 40), (5, 9), 2, 4, 3, "f16"),
+    ((6, 10, 14), (2, 3, 4), 1, 2, 3, "f32"),
     ((64, 64, 64), (16, 16, 16), 2, 5, 3, "f32"),
     ((64, 64, 64), (16, 16, 16), 3, 3, 5, "f16"),
     ((64, 64, 64), (16, 16, 16), 1, 3, 2, "bf16"),
