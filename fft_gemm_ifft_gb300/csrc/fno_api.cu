@@ -73,7 +73,7 @@ int choose_path(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int co
 
 struct Sizes {
     size_t workspace, weight, adjoint_workspace;
-    int path, kernels;
+    int path, kernels, bw_parts;
 };
 
 fno_status_t describe(int ndim, const int64_t *n, const int32_t *modes, int64_t batch,
@@ -99,6 +99,7 @@ fno_status_t describe(int ndim, const int64_t *n, const int32_t *modes, int64_t 
     }
     sz->weight = (size_t)g->nblk * cin * cout * g->mblk * 2 * elem_bytes(dtype);
     sz->adjoint_workspace = 0;
+    sz->bw_parts = 0;
     if (flags & FNO_PLAN_BACKWARD) {
         // the adjoint layer (Cout -> Cin) runs dx; its plan never traces
         Geom ga;
@@ -107,8 +108,9 @@ fno_status_t describe(int ndim, const int64_t *n, const int32_t *modes, int64_t 
                       flags & ~(FNO_PLAN_BACKWARD | FNO_PLAN_TRACE), &ga, &sa);
         if (st != FNO_OK) return st;
         sz->adjoint_workspace = sa.workspace;
+        sz->bw_parts = sz->path == kPathFused ? fused_modes_parts(*g, dtype, flags) : 0;
         const BackwardLayout bl =
-            backward_layout(*g, batch, cin, cout, sz->weight, sa.workspace);
+            backward_layout(*g, batch, cin, cout, sz->weight, sa.workspace, sz->bw_parts);
         if (bl.total > sz->workspace) sz->workspace = bl.total;
     }
     return FNO_OK;
@@ -227,7 +229,8 @@ fno_status_t fno_spectral_conv_plan(fno_plan_t *out, int ndim, const int64_t *n,
             return st;
         }
         const BackwardLayout bl = backward_layout(g, batch, cin, cout, sz.weight,
-                                                  sz.adjoint_workspace);
+                                                  sz.adjoint_workspace, sz.bw_parts);
+        p->bw_parts = sz.bw_parts;
         p->bw_wt = bl.wt;
         p->bw_adj = bl.adj;
         p->bw_x = bl.x;
@@ -320,9 +323,15 @@ fno_status_t fno_spectral_conv_backward(fno_plan_t plan, const void *x, const vo
         float2 *G = reinterpret_cast<float2 *>(ws + p.bw_g);
         float2 *sa = reinterpret_cast<float2 *>(ws + p.bw_sa);
         float2 *sb = reinterpret_cast<float2 *>(ws + p.bw_sb);
-        cudaError_t e = unfused_forward_modes(p, x, p.batch * p.cin, sa, sb, X, s);
-        if (e == cudaSuccess) e = unfused_forward_modes(p, dy, p.batch * p.cout, sa, sb, G, s);
-        if (e == cudaSuccess) e = launch_grad_w(p, X, G, dw, s);
+        cudaError_t e;
+        if (p.bw_parts > 0) {
+            e = fused_forward_modes(p, x, p.batch * p.cin, X, s);
+            if (e == cudaSuccess) e = fused_forward_modes(p, dy, p.batch * p.cout, G, s);
+        } else {
+            e = unfused_forward_modes(p, x, p.batch * p.cin, sa, sb, X, s);
+            if (e == cudaSuccess) e = unfused_forward_modes(p, dy, p.batch * p.cout, sa, sb, G, s);
+        }
+        if (e == cudaSuccess) e = launch_grad_w(p, X, G, p.bw_parts > 0 ? p.bw_parts : 1, dw, s);
         if (e != cudaSuccess) {
             cudaGetLastError();
             return FNO_ERR_CUDA;

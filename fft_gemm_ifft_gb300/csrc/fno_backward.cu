@@ -14,8 +14,9 @@
 // conj(W[blk][i][o][l]) (Cout inputs -> Cin outputs): the inverse step of the
 // forward supplies the c(k)/prod(N) factor.  So dx reuses the fused forward
 // kernels through the adjoint plan, after k_adjoint_weights writes W' into the
-// workspace.  dW needs the kept modes of x and dy (the per-axis DFT kernels)
-// and one reduction over the batch per weight (k_grad_w).
+// workspace.  dW needs the kept modes of x and dy (the forward-transform kernel
+// of the three-kernel path where the shape has one, else the per-axis DFT
+// kernels) and one reduction over the batch per weight (k_grad_w).
 #include <algorithm>
 
 #include "fno_internal.cuh"
@@ -60,10 +61,12 @@ k_adjoint_weights(const T *__restrict__ w, T *__restrict__ wt, int64_t nblk, int
 
 // dW[blk][i][o][l] = c / prod(N) sum_b G[b][o][k] conj(X[b][i][k]), k the kept
 // mode of (blk, l), G = F(dy), X = F(x)
+// X and G may each be the sum of `parts` partial copies ([parts][images][|K|])
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
-k_grad_w(const float2 *__restrict__ X, const float2 *__restrict__ G, T *__restrict__ dw,
-         int64_t batch, int cin, int cout, int64_t nblk, ModeGeom mg, float inv_npix) {
+k_grad_w(const float2 *__restrict__ X, const float2 *__restrict__ G, int parts,
+         T *__restrict__ dw, int64_t batch, int cin, int cout, int64_t nblk, ModeGeom mg,
+         float inv_npix) {
     const int64_t total = nblk * cin * cout * mg.mblk;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -85,9 +88,15 @@ k_grad_w(const float2 *__restrict__ X, const float2 *__restrict__ G, T *__restri
         }
         const float c = (rlast == 0 || 2 * rlast == mg.nlast) ? inv_npix : 2.f * inv_npix;
         float2 acc = make_float2(0.f, 0.f);
+        const int64_t gstride = batch * cout * mg.nkept, xstride = batch * cin * mg.nkept;
         for (int64_t b = 0; b < batch; ++b) {
-            const float2 g = G[(b * cout + o) * mg.nkept + kk];
-            const float2 x = X[(b * cin + i) * mg.nkept + kk];
+            float2 g = make_float2(0.f, 0.f), x = make_float2(0.f, 0.f);
+            for (int q = 0; q < parts; ++q) {
+                const float2 gq = G[q * gstride + (b * cout + o) * mg.nkept + kk];
+                const float2 xq = X[q * xstride + (b * cin + i) * mg.nkept + kk];
+                g.x += gq.x; g.y += gq.y;
+                x.x += xq.x; x.y += xq.y;
+            }
             acc.x = fmaf(g.x, x.x, fmaf(g.y, x.y, acc.x));     // g conj(x)
             acc.y = fmaf(g.y, x.x, fmaf(-g.x, x.y, acc.y));
         }
@@ -101,14 +110,16 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 }  // namespace
 
 BackwardLayout backward_layout(const Geom &g, int64_t batch, int cin, int cout,
-                               size_t weight_bytes, size_t adjoint_workspace) {
+                               size_t weight_bytes, size_t adjoint_workspace, int parts) {
     BackwardLayout l;
-    const int64_t scratch = unfused_modes_scratch_elems(g, batch * std::max(cin, cout));
+    const int64_t scratch =
+        parts > 0 ? 0 : unfused_modes_scratch_elems(g, batch * std::max(cin, cout));
+    const size_t copies = parts > 0 ? (size_t)parts : 1;
     l.wt = 0;
     l.adj = l.wt + align256(weight_bytes);
     l.x = l.adj + align256(adjoint_workspace);
-    l.g = l.x + align256((size_t)batch * cin * g.nkept * sizeof(float2));
-    l.sa = l.g + align256((size_t)batch * cout * g.nkept * sizeof(float2));
+    l.g = l.x + align256(copies * batch * cin * g.nkept * sizeof(float2));
+    l.sa = l.g + align256(copies * batch * cout * g.nkept * sizeof(float2));
     l.sb = l.sa + align256((size_t)scratch * sizeof(float2));
     l.total = l.sb + align256((size_t)scratch * sizeof(float2));
     return l;
@@ -125,7 +136,7 @@ cudaError_t launch_adjoint_weights(const Plan &p, const void *w, void *wt, cudaS
     return cudaGetLastError();
 }
 
-cudaError_t launch_grad_w(const Plan &p, const float2 *X, const float2 *G, void *dw,
+cudaError_t launch_grad_w(const Plan &p, const float2 *X, const float2 *G, int parts, void *dw,
                           cudaStream_t s) {
     ModeGeom mg;
     mg.d = p.g.d;
@@ -141,7 +152,7 @@ cudaError_t launch_grad_w(const Plan &p, const float2 *X, const float2 *G, void 
     with_storage(p.dtype, [&](auto t) {
         using T = decltype(t);
         k_grad_w<T><<<grid_for(total, p.num_sms), kThreads, 0, s>>>(
-            X, G, static_cast<T *>(dw), p.batch, p.cin, p.cout, p.g.nblk, mg, inv_npix);
+            X, G, parts, static_cast<T *>(dw), p.batch, p.cin, p.cout, p.g.nblk, mg, inv_npix);
         return 0;
     });
     return cudaGetLastError();

@@ -946,6 +946,24 @@ struct Pdl {
         }
         return e;
     }
+    // kernel A alone over nimg images (an ordinary launch)
+    template <typename T>
+    static cudaError_t forward_a(const Args &a, int64_t nimg, cudaStream_t s) {
+        cudaLaunchAttribute cl;
+        cl.id = cudaLaunchAttributeClusterDimension;
+        cl.val.clusterDim.x = Cf::C;
+        cl.val.clusterDim.y = 1;
+        cl.val.clusterDim.z = 1;
+        cudaLaunchConfig_t ca = {};
+        ca.gridDim = dim3((unsigned)(nimg * Cf::C));
+        ca.blockDim = dim3(kNT);
+        ca.dynamicSmemBytes = Cf::kSmemTw + Cf::kSmemA;
+        ca.stream = s;
+        ca.attrs = kCluster ? &cl : nullptr;
+        ca.numAttrs = kCluster ? 1 : 0;
+        cudaError_t e = cudaLaunchKernelEx(&ca, k_phase_a<Cf, T, kCluster>, a);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     template <typename T>
     static cudaError_t forward(const Plan &p, Args a, cudaStream_t s) {
         a.bg = p.fused_bb;
@@ -1044,6 +1062,35 @@ size_t fused_workspace_bytes(const Geom &g, fno_dtype_t dtype, int64_t batch, in
 int fused_kernel_count(const Geom &g, fno_dtype_t dtype, int64_t, int, int, uint32_t flags) {
     const Variant v = variant(g, dtype, flags);
     return (v == kVarPdl128 || v == kVarPdl256 || v == kVarPdl3d) ? 3 : 1;
+}
+
+int fused_modes_parts(const Geom &g, fno_dtype_t dtype, uint32_t flags) {
+    switch (variant(g, dtype, flags)) {
+        case kVarPdl128: return Pdl<Cfg128>::kParts;
+        case kVarPdl256: return Pdl<Cfg256>::kParts;
+        case kVarPdl3d: return 1;
+        default: return 0;
+    }
+}
+
+cudaError_t fused_forward_modes(const Plan &p, const void *x, int64_t nimg, float2 *parts,
+                                cudaStream_t s) {
+    const Variant v = variant(p.g, p.dtype, p.flags);
+    if (v == kVarPdl3d) return fused3d_forward_modes(p, x, nimg, parts, s);
+    if (v != kVarPdl128 && v != kVarPdl256) return cudaErrorInvalidValue;
+    Args a{};
+    a.x = x;
+    a.part = parts;
+    a.tw0 = p.tw[0];
+    a.tw1 = p.tw[1];
+    a.err = p.dev_err;
+    a.batch = (int)nimg;      // images = batch * cin
+    a.cin = 1;
+    return with_storage(p.dtype, [&](auto t) {
+        using T = decltype(t);
+        return v == kVarPdl256 ? Pdl<Cfg256>::forward_a<T>(a, nimg, s)
+                               : Pdl<Cfg128>::forward_a<T>(a, nimg, s);
+    });
 }
 
 cudaError_t fused_plan_init(Plan &p) {

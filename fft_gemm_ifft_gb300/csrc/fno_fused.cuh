@@ -19,6 +19,17 @@ cudaError_t fused_plan_init(Plan &p);
 void fused_plan_release(Plan &p);
 cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s);
 
+// Kept modes of nimg images by the forward-transform kernel of the
+// three-kernel path alone (used by the backward pass).  fused_modes_parts
+// returns how many partial copies that kernel writes ([parts][nimg][|K|]
+// complex float, summed by the reader), or 0 when the plan's variant has no
+// such kernel.
+int fused_modes_parts(const Geom &g, fno_dtype_t dtype, uint32_t flags);
+cudaError_t fused_forward_modes(const Plan &p, const void *x, int64_t nimg, float2 *parts,
+                                cudaStream_t s);
+cudaError_t fused3d_forward_modes(const Plan &p, const void *x, int64_t nimg, float2 *out,
+                                  cudaStream_t s);
+
 // The 1-D layer's kernel (one cluster per sample).
 bool fused1d_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout);
 cudaError_t fused1d_forward(const Plan &p, const Buffers &b, cudaStream_t s);

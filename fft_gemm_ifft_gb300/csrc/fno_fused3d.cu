@@ -389,6 +389,35 @@ cudaError_t fused3d_plan_init(Plan &p) {
     return with_storage(p.dtype, [&](auto t) { return Pdl3<Cfg3d64>::init<decltype(t)>(p); });
 }
 
+cudaError_t fused3d_forward_modes(const Plan &p, const void *x, int64_t nimg, float2 *out,
+                                  cudaStream_t s) {
+    using C3 = Cfg3d64;
+    Args a{};
+    a.x = x;
+    a.part = out;
+    a.tw0 = p.tw[0];
+    a.tw1 = p.tw[1];
+    a.tw2 = p.tw[2];
+    a.err = p.dev_err;
+    return with_storage(p.dtype, [&](auto t) {
+        using T = decltype(t);
+        cudaLaunchAttribute cl;
+        cl.id = cudaLaunchAttributeClusterDimension;
+        cl.val.clusterDim.x = C3::C0;
+        cl.val.clusterDim.y = 1;
+        cl.val.clusterDim.z = 1;
+        cudaLaunchConfig_t ca = {};
+        ca.gridDim = dim3((unsigned)(nimg * C3::C0));
+        ca.blockDim = dim3(kNT);
+        ca.dynamicSmemBytes = C3::template smem_a<T>();
+        ca.stream = s;
+        ca.attrs = &cl;
+        ca.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&ca, k_phase_a3<C3, T>, a);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    });
+}
+
 cudaError_t fused3d_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
     Args a{};
     a.x = b.x;

@@ -59,14 +59,17 @@ struct Plan {
     // FNO_PLAN_BACKWARD: the adjoint layer's plan and the backward workspace map
     fno_plan_t adjoint;
     size_t bw_wt, bw_adj, bw_x, bw_g, bw_sa, bw_sb;   // byte offsets in the workspace
+    int bw_parts;                 // partial copies of the kept modes (0: per-axis kernels)
 };
 
 // Backward workspace map of a description (offsets and total size).
 struct BackwardLayout {
     size_t wt, adj, x, g, sa, sb, total;
 };
+// parts = partial copies the forward-transform kernel writes, 0 when the
+// per-axis kernels (and their scratch) compute the kept modes
 BackwardLayout backward_layout(const Geom &g, int64_t batch, int cin, int cout,
-                               size_t weight_bytes, size_t adjoint_workspace);
+                               size_t weight_bytes, size_t adjoint_workspace, int parts);
 
 enum { kPathUnfused = 0, kPathFused = 1 };
 
@@ -159,7 +162,7 @@ cudaError_t unfused_forward_modes(const Plan &p, const void *x, int64_t nch, flo
                                   float2 *sb, float2 *out, cudaStream_t s);
 // Backward kernels (fno_backward.cu).
 cudaError_t launch_adjoint_weights(const Plan &p, const void *w, void *wt, cudaStream_t s);
-cudaError_t launch_grad_w(const Plan &p, const float2 *X, const float2 *G, void *dw,
+cudaError_t launch_grad_w(const Plan &p, const float2 *X, const float2 *G, int parts, void *dw,
                           cudaStream_t s);
 
 }  // namespace fno
