@@ -60,20 +60,26 @@ k_adjoint_weights(const T *__restrict__ w, T *__restrict__ wt, int64_t nblk, int
 }
 
 // dW[blk][i][o][l] = c / prod(N) sum_b G[b][o][k] conj(X[b][i][k]), k the kept
-// mode of (blk, l), G = F(dy), X = F(x)
-// X and G may each be the sum of `parts` partial copies ([parts][images][|K|])
+// mode of (blk, l), G = F(dy), X = F(x).  X and G may each be the sum of
+// `parts` partial copies ([parts][images][|K|]).  A thread owns kOB
+// consecutive outputs o of one (blk, i, l), so each X value it loads serves
+// kOB products; consecutive threads take consecutive l (coalesced).
+constexpr int kOB = 8;
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 k_grad_w(const float2 *__restrict__ X, const float2 *__restrict__ G, int parts,
          T *__restrict__ dw, int64_t batch, int cin, int cout, int64_t nblk, ModeGeom mg,
          float inv_npix) {
-    const int64_t total = nblk * cin * cout * mg.mblk;
+    const int nog = (cout + kOB - 1) / kOB;
+    const int64_t total = nblk * cin * nog * mg.mblk;
+    const int64_t gstride = batch * cout * mg.nkept, xstride = batch * cin * mg.nkept;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
         const int64_t l = idx % mg.mblk;
         int64_t t = idx / mg.mblk;
-        const int o = (int)(t % cout);
-        t /= cout;
+        const int o0 = (int)(t % nog) * kOB;
+        t /= nog;
         const int i = (int)(t % cin);
         const int blk = (int)(t / cin);
         // kept index: local index per axis, plus m_a on the high rows of a full axis
@@ -87,21 +93,37 @@ k_grad_w(const float2 *__restrict__ X, const float2 *__restrict__ G, int parts,
             stride *= mg.kdim[a];
         }
         const float c = (rlast == 0 || 2 * rlast == mg.nlast) ? inv_npix : 2.f * inv_npix;
-        float2 acc = make_float2(0.f, 0.f);
-        const int64_t gstride = batch * cout * mg.nkept, xstride = batch * cin * mg.nkept;
+        const int no = min(kOB, cout - o0);
+        float2 acc[kOB];
+#pragma unroll
+        for (int q = 0; q < kOB; ++q) acc[q] = make_float2(0.f, 0.f);
         for (int64_t b = 0; b < batch; ++b) {
-            float2 g = make_float2(0.f, 0.f), x = make_float2(0.f, 0.f);
-            for (int q = 0; q < parts; ++q) {
-                const float2 gq = G[q * gstride + (b * cout + o) * mg.nkept + kk];
-                const float2 xq = X[q * xstride + (b * cin + i) * mg.nkept + kk];
-                g.x += gq.x; g.y += gq.y;
-                x.x += xq.x; x.y += xq.y;
+            float2 x = make_float2(0.f, 0.f);
+            for (int p = 0; p < parts; ++p) {
+                const float2 xp = X[p * xstride + (b * cin + i) * mg.nkept + kk];
+                x.x += xp.x;
+                x.y += xp.y;
             }
-            acc.x = fmaf(g.x, x.x, fmaf(g.y, x.y, acc.x));     // g conj(x)
-            acc.y = fmaf(g.y, x.x, fmaf(-g.x, x.y, acc.y));
+#pragma unroll
+            for (int q = 0; q < kOB; ++q) {
+                if (q >= no) break;
+                float2 g = make_float2(0.f, 0.f);
+                for (int p = 0; p < parts; ++p) {
+                    const float2 gp = G[p * gstride + (b * cout + o0 + q) * mg.nkept + kk];
+                    g.x += gp.x;
+                    g.y += gp.y;
+                }
+                acc[q].x = fmaf(g.x, x.x, fmaf(g.y, x.y, acc[q].x));     // g conj(x)
+                acc[q].y = fmaf(g.y, x.x, fmaf(-g.x, x.y, acc[q].y));
+            }
         }
-        Storage<T>::store(dw + idx * 2, acc.x * c);
-        Storage<T>::store(dw + idx * 2 + 1, acc.y * c);
+#pragma unroll
+        for (int q = 0; q < kOB; ++q) {
+            if (q >= no) break;
+            T *d = dw + ((((int64_t)blk * cin + i) * cout + o0 + q) * mg.mblk + l) * 2;
+            Storage<T>::store(d, acc[q].x * c);
+            Storage<T>::store(d + 1, acc[q].y * c);
+        }
     }
 }
 
@@ -147,7 +169,7 @@ cudaError_t launch_grad_w(const Plan &p, const float2 *X, const float2 *G, int p
     mg.nkept = p.g.nkept;
     mg.mblk = p.g.mblk;
     mg.nlast = p.g.n[p.g.d - 1];
-    const int64_t total = p.g.nblk * p.cin * p.cout * p.g.mblk;
+    const int64_t total = p.g.nblk * p.cin * ((p.cout + kOB - 1) / kOB) * p.g.mblk;
     const float inv_npix = (float)(1.0 / (double)p.g.npix);
     with_storage(p.dtype, [&](auto t) {
         using T = decltype(t);

@@ -17,6 +17,7 @@ CASES = [
     ((256,), (16,), 3, 5, 7, "f32"),
     ((16,), (9,), 2, 3, 4, "f32"),
     ((128, 128), (16, 16), 2, 6, 4, "f32"),
+    ((128, 128), (16, 16), 2, 6, 20, "f32"),
     ((128, 128), (16, 16), 2, 3, 5, "f16"),
     ((256, 256), (32, 32), 1, 4, 3, "f16"),
     ((64, 64, 64), (16, 16, 16), 1, 3, 2, "f32"),
