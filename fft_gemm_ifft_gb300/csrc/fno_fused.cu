@@ -896,13 +896,30 @@ size_t fused_sync_bytes() { return kSyncBytes; }
 // of an image reduce their partial modes in a cluster.
 using Cfg256 = Cfg<256, 256, 32, 32, 64, 32, 8>;
 
+// Chunking of the three-kernel 128 x 128 path, forward (A) and inverse (C)
+// kernels chosen independently (the mixed modes do not depend on it):
+// 0: 32-row chunks, 16-point row FFTs over 8 lanes; 1: 64-row chunks,
+// 32-point row FFTs over 4 lanes; 2: as 1 with 16-point column FFTs;
+// 3: 64-row chunks, 16-point row FFTs.
+#ifndef FNO_CFG128_A
+#define FNO_CFG128_A 0
+#endif
+#ifndef FNO_CFG128_C
+#define FNO_CFG128_C 0
+#endif
+template <int V>
+using Cfg128V = std::conditional_t<
+    V == 1, Cfg<128, 128, 16, 16, 64, 32, 8>,
+    std::conditional_t<V == 2, Cfg<128, 128, 16, 16, 64, 32, 16>,
+                       std::conditional_t<V == 3, Cfg<128, 128, 16, 16, 64, 16, 8>, Cfg128>>>;
+
 bool is_cfg256(const Geom &g) {
     return g.d == 2 && g.n[0] == 256 && g.n[1] == 256 && g.m[0] == 32 && g.m[1] == 32;
 }
 
 // Three-kernel variant, per shape: whether phase A reduces its partials in a
 // cluster, and the kernels' shared memory.
-template <class Cf>
+template <class Cf, class CfC = Cf>
 struct Pdl {
     static constexpr bool kCluster = Cf::N0 >= 256;
     static constexpr int kParts = kCluster ? 1 : Cf::C;
@@ -924,16 +941,16 @@ struct Pdl {
         int ob = p.cout;
         while (ob > 1 && (size_t)p.cin * ob * w2 > kWsBudget) ob = (ob + 1) / 2;
         const int bb = batch_block(p.batch, p.cin);
-        const size_t sa = Cf::kSmemTw + Cf::kSmemA, sc = Cf::kSmemTw + Cf::kSmemC;
-        const size_t sb = smem_b(p.dtype, p.cin, ob, bb);
+        const size_t sa = Cf::kSmemTw + Cf::kSmemA, sc = CfC::kSmemTw + CfC::kSmemC;
+        const size_t sb = smem_b(p.dtype, p.cin, ob + 1, bb);   // padded slab rows
         cudaError_t e = cudaFuncSetAttribute(k_phase_a<Cf, T, kCluster>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k_phase_b<Cf, T, kParts>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sb);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_phase_c<Cf, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)sc);
+            e = cudaFuncSetAttribute(k_phase_c<CfC, T>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
         p.fused_bb = bb;
         p.fused_ob = ob;
         p.fused_smem = sb;             // kernel B's; A and C use their fixed sizes
@@ -941,7 +958,7 @@ struct Pdl {
         if (e == cudaSuccess && (p.flags & FNO_PLAN_TRACE)) {
             const size_t nB = (size_t)(p.g.nkept / kG) * ((p.cout + ob - 1) / ob) *
                               ((p.batch + bb - 1) / bb);
-            p.trace_records = (size_t)p.batch * (p.cin + p.cout) * Cf::C + nB;
+            p.trace_records = (size_t)p.batch * (p.cin * Cf::C + p.cout * CfC::C) + nB;
             e = cudaMalloc(&p.trace, p.trace_records * sizeof(fno_trace_record_t));
         }
         return e;
@@ -973,7 +990,7 @@ struct Pdl {
         a.npairs = (int)(p.g.nkept / kG);
         const int nA = (int)p.batch * p.cin * Cf::C;
         const int nB = a.npairs * a.nob * a.ng;
-        const int nC = (int)p.batch * p.cout * Cf::C;
+        const int nC = (int)p.batch * p.cout * CfC::C;
         a.trace = p.trace;
         a.trace_b = nA;
         a.trace_c = nA + nB;
@@ -1006,12 +1023,14 @@ struct Pdl {
         if (e != cudaSuccess) return e;
         cfg.gridDim = dim3(nC);
         cfg.blockDim = dim3(kNT);
-        cfg.dynamicSmemBytes = Cf::kSmemTw + Cf::kSmemC;
-        e = cudaLaunchKernelEx(&cfg, k_phase_c<Cf, T>, a);
+        cfg.dynamicSmemBytes = CfC::kSmemTw + CfC::kSmemC;
+        e = cudaLaunchKernelEx(&cfg, k_phase_c<CfC, T>, a);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
 };
+
+using Pdl128 = Pdl<Cfg128V<FNO_CFG128_A>, Cfg128V<FNO_CFG128_C>>;
 
 enum Variant { kVarNone, kVarPdl128, kVarPdl256, kVarPersistent128, kVarTc128, kVarPdl3d, kVarOne1d };
 
@@ -1043,7 +1062,7 @@ bool fused_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, i
         return smem_bytes(dtype, cin, b_shape(dtype, batch, cin, cout)) <= 200 * 1024;
     // three-kernel variants: a weight slab of one output and one batch row must fit
     const size_t w2 = dtype == FNO_F32 ? 16 : 8;
-    return (size_t)cin * w2 <= kWsBudget && (size_t)cin * 16 * Cfg128::C <= kXpBudget;
+    return (size_t)cin * w2 <= kWsBudget && (size_t)cin * 16 * Pdl128::kParts <= kXpBudget;
 }
 
 size_t fused_workspace_bytes(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout,
@@ -1054,7 +1073,7 @@ size_t fused_workspace_bytes(const Geom &g, fno_dtype_t dtype, int64_t batch, in
     if (v == kVarTc128) return layout_tc(g, batch, cin, cout).total;
     if (v == kVarPersistent128) return layout(g, batch, cin, cout).total;
     const size_t part = v == kVarPdl256 ? Pdl<Cfg256>::part_bytes(g, batch, cin)
-                                        : Pdl<Cfg128>::part_bytes(g, batch, cin);
+                                        : Pdl128::part_bytes(g, batch, cin);
     const size_t y = (size_t)batch * cout * g.nkept * sizeof(float2);
     return ((part + 255) & ~size_t(255)) + ((y + 255) & ~size_t(255));
 }
@@ -1066,7 +1085,7 @@ int fused_kernel_count(const Geom &g, fno_dtype_t dtype, int64_t, int, int, uint
 
 int fused_modes_parts(const Geom &g, fno_dtype_t dtype, uint32_t flags) {
     switch (variant(g, dtype, flags)) {
-        case kVarPdl128: return Pdl<Cfg128>::kParts;
+        case kVarPdl128: return Pdl128::kParts;
         case kVarPdl256: return Pdl<Cfg256>::kParts;
         case kVarPdl3d: return 1;
         default: return 0;
@@ -1089,7 +1108,7 @@ cudaError_t fused_forward_modes(const Plan &p, const void *x, int64_t nimg, floa
     return with_storage(p.dtype, [&](auto t) {
         using T = decltype(t);
         return v == kVarPdl256 ? Pdl<Cfg256>::forward_a<T>(a, nimg, s)
-                               : Pdl<Cfg128>::forward_a<T>(a, nimg, s);
+                               : Pdl128::forward_a<T>(a, nimg, s);
     });
 }
 
@@ -1098,7 +1117,7 @@ cudaError_t fused_plan_init(Plan &p) {
     if (v == kVarPdl3d) return fused3d_plan_init(p);
     if (v == kVarOne1d) return cudaSuccess;
     if (v == kVarPdl128)
-        return with_storage(p.dtype, [&](auto t) { return Pdl<Cfg128>::init<decltype(t)>(p); });
+        return with_storage(p.dtype, [&](auto t) { return Pdl128::init<decltype(t)>(p); });
     if (v == kVarPdl256)
         return with_storage(p.dtype, [&](auto t) { return Pdl<Cfg256>::init<decltype(t)>(p); });
     if (v == kVarTc128)
@@ -1208,7 +1227,7 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
     }
     if (v == kVarPdl128 || v == kVarPdl256) {
         const size_t part = v == kVarPdl256 ? Pdl<Cfg256>::part_bytes(p.g, p.batch, p.cin)
-                                            : Pdl<Cfg128>::part_bytes(p.g, p.batch, p.cin);
+                                            : Pdl128::part_bytes(p.g, p.batch, p.cin);
         Args a{};
         a.x = b.x;
         a.w = b.w;
@@ -1224,7 +1243,7 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
         return with_storage(p.dtype, [&](auto t) {
             using T = decltype(t);
             return v == kVarPdl256 ? Pdl<Cfg256>::forward<T>(p, a, s)
-                                   : Pdl<Cfg128>::forward<T>(p, a, s);
+                                   : Pdl128::forward<T>(p, a, s);
         });
     }
     const Layout l = layout(p.g, p.batch, p.cin, p.cout);

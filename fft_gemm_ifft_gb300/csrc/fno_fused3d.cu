@@ -295,13 +295,13 @@ struct Pdl3 {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k_phase_b<C3, T, 1>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem_b(p.dtype, p.cin, ob, bb));
+                                     (int)smem_b(p.dtype, p.cin, ob + 1, bb));
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k_phase_c3<C3, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)C3::kSmemC);
         p.fused_bb = bb;
         p.fused_ob = ob;
-        p.fused_smem = smem_b(p.dtype, p.cin, ob, bb);
+        p.fused_smem = smem_b(p.dtype, p.cin, ob + 1, bb);   // padded slab rows
         p.fused_grid = 0;
         if (e == cudaSuccess && (p.flags & FNO_PLAN_TRACE)) {
             const size_t nB = (size_t)(C3::NK / kG) * ((p.cout + ob - 1) / ob) *

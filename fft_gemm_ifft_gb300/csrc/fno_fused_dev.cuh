@@ -511,7 +511,8 @@ __device__ void phase_b_tiles(const G &grp, float2 *__restrict__ Y, int cin, int
 
 template <class Cf, typename T, int NT, class G, int kParts = Cf::C>
 __device__ void phase_b(const G &grp, const float2 *__restrict__ part, float2 *__restrict__ Y, int cin,
-                        int cout, int nimg_in, const BItem &it, int ob, char *smem) {
+                        int cout, int nimg_in, const BItem &it, int ob, char *smem,
+                        unsigned long long *t_loaded = nullptr) {
     using W2 = typename Io<T>::W2;
     constexpr int NK = Cf::NK, C = kParts;
     const int mode0 = it.pair * kG;
@@ -527,6 +528,7 @@ __device__ void phase_b(const G &grp, const float2 *__restrict__ part, float2 *_
     cp_async_commit();
     cp_async_wait_all();                                 // also covers the weight slab
     grp.sync();
+    if (t_loaded && tid == 0) *t_loaded = (unsigned long long)globaltimer();
     for (int r = tid; r < nr; r += NT) {
         float4 s = xp[r];
 #pragma unroll
@@ -706,7 +708,8 @@ __device__ __forceinline__ unsigned long long trace_now() {
 // returned).  A no-op unless the plan traces.
 __device__ __forceinline__ void cta_record(const Args &a, int phase, int first,
                                            unsigned long long t_start,
-                                           unsigned long long t_ready) {
+                                           unsigned long long t_ready,
+                                           unsigned long long t_compute = 0) {
     if (!a.trace) return;
     __syncthreads();
     if (threadIdx.x != 0) return;
@@ -717,7 +720,8 @@ __device__ __forceinline__ void cta_record(const Args &a, int phase, int first,
     r.worker = smid;
     r.t_start = t_start;
     r.t_ready = t_ready;
-    r.t_compute = r.t_end = trace_now();
+    r.t_end = trace_now();
+    r.t_compute = t_compute ? t_compute : r.t_end;
     a.trace[first + blockIdx.x] = r;
 }
 
@@ -737,13 +741,19 @@ __global__ void __launch_bounds__(kNTB) k_phase_b(Args a) {
     bi.nbb = min(a.bg, a.batch - bi.b0);
     const CtaGroup grp{(int)threadIdx.x};
     const unsigned long long t0 = a.trace ? trace_now() : 0;
-    phase_b_weights<Cf, T, kNTB>(grp, static_cast<const T *>(a.w), a.cin, a.cout, bi, a.ob, smem);
+    // weight slab rows padded by one entry: the lanes of a warp read S input
+    // channels of one output pair, which an unpadded row stride would put on
+    // the same banks
+    const int wstride = a.ob + 1;
+    phase_b_weights<Cf, T, kNTB>(grp, static_cast<const T *>(a.w), a.cin, a.cout, bi, wstride,
+                                 smem);
     pdl_trigger();
     pdl_wait();                                  // kernel A's partial modes are complete
     const unsigned long long t1 = a.trace ? trace_now() : 0;
+    unsigned long long tl = 0;
     phase_b<Cf, T, kNTB, CtaGroup, kParts>(grp, a.part, a.Y, a.cin, a.cout, a.batch * a.cin, bi,
-                                          a.ob, smem);
-    cta_record(a, 1, a.trace_b, t0, t1);
+                                          wstride, smem, a.trace ? &tl : nullptr);
+    cta_record(a, 1, a.trace_b, t0, t1, tl);
 }
 
 }  // namespace
