@@ -166,5 +166,16 @@ __host__ __device__ __forceinline__ void split_real_pair(const float2 (&z)[N], f
     B = c2(0.5f * (p.y + m.y), 0.5f * (m.x - p.x));
 }
 
+// The same split without the factor 1/2 (2A and 2B), for callers that fold
+// the 1/2 into a twiddle they multiply by anyway.
+template <int N, int Q>
+__host__ __device__ __forceinline__ void split_real_pair2(const float2 (&z)[N], float2 &A2,
+                                                          float2 &B2) {
+    const float2 p = bin<N, Q>(z);
+    const float2 m = bin<N, (N - Q) % N>(z);
+    A2 = c2(p.x + m.x, p.y - m.y);
+    B2 = c2(p.y + m.y, m.x - p.x);
+}
+
 }  // namespace fft
 }  // namespace fno

@@ -105,14 +105,12 @@ k_fused2d(Args a) {
     __shared__ int s_ok;
     float2 *tw0 = reinterpret_cast<float2 *>(smem);
     float2 *tw1 = tw0 + Cf::N0;
+    float2 *tw1i = tw1 + Cf::P * Cf::TS;
     char *work = smem + Cf::kSmemTw;
     const int tid = threadIdx.x;
     for (int e = tid; e < Cf::N0; e += kNT) tw0[e] = a.tw0[e];
-    for (int e = tid; e < Cf::P * Cf::TS; e += kNT) {
-        const int n1 = e / Cf::TS, k = e % Cf::TS;
-        tw1[e] = a.tw1[(n1 * k) & (Cf::N1 - 1)];
-    }
-    const Tw tw{tw0, tw1};
+    fill_row_tables<Cf>(a.tw1, tw1, tw1i, 1.0f / ((float)Cf::N0 * (float)Cf::N1));
+    const Tw tw{tw0, tw1, tw1i};
     const int nimg_in = a.batch * a.cin;
     // thread 0 claims one ticket ahead: the atomic's round trip overlaps the
     // current item.  A held ticket is always larger than its holder's current
@@ -216,12 +214,10 @@ template <class Cf>
 __device__ __forceinline__ Tw load_twiddles(const Args &a, char *smem) {
     float2 *tw0 = reinterpret_cast<float2 *>(smem);
     float2 *tw1 = tw0 + Cf::N0;
+    float2 *tw1i = tw1 + Cf::P * Cf::TS;
     for (int e = threadIdx.x; e < Cf::N0; e += kNT) tw0[e] = a.tw0[e];
-    for (int e = threadIdx.x; e < Cf::P * Cf::TS; e += kNT) {
-        const int n1 = e / Cf::TS, k = e % Cf::TS;
-        tw1[e] = a.tw1[(n1 * k) & (Cf::N1 - 1)];
-    }
-    return Tw{tw0, tw1};
+    fill_row_tables<Cf>(a.tw1, tw1, tw1i, 1.0f / ((float)Cf::N0 * (float)Cf::N1));
+    return Tw{tw0, tw1, tw1i};
 }
 
 template <class Cf, typename T, bool kCluster>
@@ -923,6 +919,10 @@ template <class Cf, class CfC = Cf>
 struct Pdl {
     static constexpr bool kCluster = Cf::N0 >= 256;
     static constexpr int kParts = kCluster ? 1 : Cf::C;
+    // threads of a kernel-B CTA: the 128 x 128 items are small enough that
+    // splitting each over 8 warps shortens the path after kernel A (measured:
+    // 23.4 -> 22.3 us on the 8 x 32-channel workload); 4 warps elsewhere
+    static constexpr int kBThreads = Cf::N0 == 128 ? 256 : 128;
     static int batch_block(int64_t batch, int cin) {
         int bb = (int)batch;
         while (bb > 1 && (size_t)kParts * bb * cin * 16 > kXpBudget) bb = (bb + 1) / 2;
@@ -946,7 +946,7 @@ struct Pdl {
         cudaError_t e = cudaFuncSetAttribute(k_phase_a<Cf, T, kCluster>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_phase_b<Cf, T, kParts>,
+            e = cudaFuncSetAttribute(k_phase_b<Cf, T, kParts, kBThreads>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sb);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k_phase_c<CfC, T>,
@@ -1017,9 +1017,9 @@ struct Pdl {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         cfg.gridDim = dim3(nB);
-        cfg.blockDim = dim3(kNTB);
+        cfg.blockDim = dim3(kBThreads);
         cfg.dynamicSmemBytes = p.fused_smem;
-        e = cudaLaunchKernelEx(&cfg, k_phase_b<Cf, T, kParts>, a);
+        e = cudaLaunchKernelEx(&cfg, k_phase_b<Cf, T, kParts, kBThreads>, a);
         if (e != cudaSuccess) return e;
         cfg.gridDim = dim3(nC);
         cfg.blockDim = dim3(kNT);

@@ -58,8 +58,8 @@ struct Cfg3 {
         local = ((j0 - h0 * M0) * M1 + (j1 - h1 * M1)) * M2 + k;
     }
 
-    // shared memory: twiddles W_N1 [N1], W_N2^{n1 k} [P][TS], W_N0 [N0]
-    static constexpr size_t kSmemTw = ((N1 + Pl::P * Pl::TS + N0) * 8 + 15) / 16 * 16;
+    // shared memory: twiddles W_N1 [N1], the row tables [2][P][TS], W_N0 [N0]
+    static constexpr size_t kSmemTw = ((N1 + 2 * Pl::P * Pl::TS + N0) * 8 + 15) / 16 * 16;
     template <typename T>
     static constexpr size_t stage_bytes() { return (size_t)N1 * Pl::XS * sizeof(T); }
     template <typename T>
@@ -86,15 +86,14 @@ __device__ __forceinline__ Tw load_tw3(const Args &a, char *smem, const float2 *
     using Pl = typename C3::Pl;
     float2 *t0 = reinterpret_cast<float2 *>(smem);
     float2 *t1 = t0 + C3::N1;
-    float2 *ta = t1 + Pl::P * Pl::TS;
+    float2 *t1i = t1 + Pl::P * Pl::TS;
+    float2 *ta = t1i + Pl::P * Pl::TS;
     for (int e = threadIdx.x; e < C3::N1; e += kNT) t0[e] = a.tw1[e];
-    for (int e = threadIdx.x; e < Pl::P * Pl::TS; e += kNT) {
-        const int n1 = e / Pl::TS, k = e % Pl::TS;
-        t1[e] = a.tw2[(n1 * k) & (C3::N2 - 1)];
-    }
+    fill_row_tables<Pl>(a.tw2, t1, t1i,
+                        1.0f / ((float)C3::N0 * (float)C3::N1 * (float)C3::N2));
     for (int e = threadIdx.x; e < C3::N0; e += kNT) ta[e] = a.tw0[e];
     *twa = ta;
-    return Tw{t0, t1};
+    return Tw{t0, t1, t1i};
 }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -254,7 +253,6 @@ __global__ void __launch_bounds__(kNT) k_phase_c3(Args a) {
     __syncthreads();
 
     // 2. every plane of the chunk: column inverse, row inverse, store
-    const float scale = 1.0f / ((float)N0 * (float)N1 * (float)N2);
     T *dst = static_cast<T *>(a.y) + (size_t)vol * N0 * N1 * N2;
     for (int t = 0; t < R0; ++t) {
         c_residues<Pl>(spec + t * NKP, vs, 0, tw);
@@ -264,7 +262,7 @@ __global__ void __launch_bounds__(kNT) k_phase_c3(Args a) {
         c_col_combine<Pl>(ss, zo, tw);
         __syncthreads();
         // zo is rewritten two barriers after this pass, vs and ss earlier ones
-        c_row_store<Pl, T>(zo, dst + (size_t)(c + C0 * t) * N1 * N2, 0, tw, scale);
+        c_row_store<Pl, T>(zo, dst + (size_t)(c + C0 * t) * N1 * N2, 0, tw);
     }
     cta_record(a, 2, a.trace_c, t0, t1);
 }
@@ -293,7 +291,7 @@ struct Pdl3 {
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)C3::template smem_a<T>());
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_phase_b<C3, T, 1>,
+            e = cudaFuncSetAttribute(k_phase_b<C3, T, 1, kNT>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)smem_b(p.dtype, p.cin, ob + 1, bb));
         if (e == cudaSuccess)
@@ -344,9 +342,9 @@ struct Pdl3 {
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         cfg.gridDim = dim3((unsigned)(a.npairs * a.nob * a.ng));
-        cfg.blockDim = dim3(kNTB);
+        cfg.blockDim = dim3(kNT);
         cfg.dynamicSmemBytes = p.fused_smem;
-        e = cudaLaunchKernelEx(&cfg, k_phase_b<C3, T, 1>, a);
+        e = cudaLaunchKernelEx(&cfg, k_phase_b<C3, T, 1, kNT>, a);
         if (e != cudaSuccess) return e;
         cfg.gridDim = dim3((unsigned)(p.batch * p.cout * C3::C0));
         cfg.blockDim = dim3(kNT);

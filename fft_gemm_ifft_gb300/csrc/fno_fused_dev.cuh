@@ -29,11 +29,7 @@ constexpr int kG = 2;                           // kept modes per phase-B item
 #ifndef FNO_WS_BUDGET
 #define FNO_WS_BUDGET 16384
 #endif
-#ifndef FNO_B_THREADS
-#define FNO_B_THREADS 128
-#endif
 constexpr size_t kWsBudget = FNO_WS_BUDGET;      // phase-B weight slab (bytes)
-constexpr int kNTB = FNO_B_THREADS;              // threads of a three-kernel phase-B CTA
 constexpr size_t kXpBudget = 24u << 10;         // phase-B partial modes (bytes)
 
 // Counters shared by the CTAs of one launch (plan-owned, zero between
@@ -90,7 +86,7 @@ struct Cfg {
         RC * XS * 4 + RC * ZS * 8 + (size_t)A * B2 * M1 * 8;
     static constexpr size_t kSmemC =
         NK * 8 + RC * M1 * 8 + (size_t)A * B2 * M1 * 8 + RC * ZS * 8;
-    static constexpr size_t kSmemTw = ((N0 + P * TS) * 8 + 15) / 16 * 16;
+    static constexpr size_t kSmemTw = ((N0 + 2 * P * TS) * 8 + 15) / 16 * 16;
     // weights: block 0 holds the low kept rows, block 1 the high ones, each
     // M0 x M1 modes
     static constexpr size_t MBLK = (size_t)M0 * M1;
@@ -222,8 +218,24 @@ __device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes) {
 
 struct Tw {
     const float2 *t0;   // [N0]      W_N0^e
-    const float2 *t1;   // [P][TS]   W_N1^{n1 k}
+    const float2 *t1;   // [P][TS]   W_N1^{n1 k} / 2         (forward row pass)
+    const float2 *t1i;  // [P][TS]   W_N1^{n1 k} c(k)/2 s    (inverse row pass, used conjugated)
 };
+
+// Row-pass tables of a configuration from the plan's W_N1 table: the forward
+// carries the 1/2 of the real-pair split, the inverse the half-spectrum weight
+// c(k)/2 and the output scale s (powers of two: every entry is exact).
+template <class Cf>
+__device__ __forceinline__ void fill_row_tables(const float2 *__restrict__ src, float2 *t1,
+                                                float2 *t1i, float s) {
+    for (int e = threadIdx.x; e < Cf::P * Cf::TS; e += kNT) {
+        const int n1 = e / Cf::TS, k = e % Cf::TS;
+        const float2 w = src[(n1 * k) & (Cf::N1 - 1)];
+        t1[e] = make_float2(0.5f * w.x, 0.5f * w.y);
+        const float h = ((k == 0 || 2 * k == Cf::N1) ? 0.5f : 1.f) * s;
+        t1i[e] = make_float2(h * w.x, h * w.y);
+    }
+}
 
 // ---------------------------------------------------------------------------
 // Phase A: one chunk of rows of one input image -> partial kept modes
@@ -275,8 +287,8 @@ __device__ __forceinline__ void a_row_dft(const S *xs, float2 *zs, Tw tw) {
             fft::unroll<0, KB>([&](auto qi) {
                 constexpr int q = decltype(qi)::value;
                 constexpr int k = kb * KB + q;
-                float2 a, b;
-                fft::split_real_pair<Q, k % Q>(z, a, b);
+                float2 a, b;                      // twice the two rows' bins;
+                fft::split_real_pair2<Q, k % Q>(z, a, b);   // the table holds W / 2
                 const float2 w = twl[k];
                 vv[q] = cmul(a, w);
                 vv[KB + q] = cmul(b, w);
@@ -606,25 +618,24 @@ __device__ __forceinline__ void c_col_combine(const float2 *ss, float2 *zo, Tw t
 // 3. rows: y[t][n1 + P n2] = s Re sum_k c_k W_N1^{-k n1} Zo[t][k] W_Q^{-k n2}, stored to
 //    rows c + C t of the image at dst
 template <class Cf, typename T>
-__device__ __forceinline__ void c_row_store(const float2 *zo, T *__restrict__ dst, int c, Tw tw,
-                                            float scale) {
+__device__ __forceinline__ void c_row_store(const float2 *zo, T *__restrict__ dst, int c, Tw tw) {
     constexpr int N1 = Cf::N1, RC = Cf::RC, C = Cf::C, P = Cf::P, Q = Cf::Q;
     constexpr int M1 = Cf::M1, ZS = Cf::ZS;
     for (int pr = threadIdx.x; pr < Cf::PAIRS; pr += kNT) {
         const int t = pr / P, n1 = pr % P, t2 = t + RC / 2;
-        const float2 *twl = tw.t1 + n1 * Cf::TS;
+        const float2 *twl = tw.t1i + n1 * Cf::TS;
         // z[q] = Herm(ga)[q] + i Herm(gb)[q], accumulated directly: a bin k
         // (q = k mod Q) with va = c_k W^{-k n1} Zo[t][k], vb likewise for row t2,
-        // adds (va + i vb)/2 at q and (conj va + i conj vb)/2 at Q - q
+        // adds (va + i vb)/2 at q and (conj va + i conj vb)/2 at Q - q; the
+        // table entry carries c_k/2 and the output scale
         float2 z[Q];
 #pragma unroll
         for (int q = 0; q < Q; ++q) z[q] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < M1; ++k) {
-            const float hk = (k == 0 || 2 * k == N1) ? 0.5f : 1.f;    // c_k / 2
             const float2 w = twl[k];
-            const float2 va = cscale(cmulc(zo[t * ZS + k], w), hk);
-            const float2 vb = cscale(cmulc(zo[t2 * ZS + k], w), hk);
+            const float2 va = cmulc(zo[t * ZS + k], w);
+            const float2 vb = cmulc(zo[t2 * ZS + k], w);
             const int q = k % Q, qm = (Q - q) % Q;
             z[q].x += va.x - vb.y;
             z[q].y += va.y + vb.x;
@@ -637,8 +648,8 @@ __device__ __forceinline__ void c_row_store(const float2 *zo, T *__restrict__ ds
 #pragma unroll
         for (int n2 = 0; n2 < Q; ++n2) {
             const float2 v = z[fft::bitrev(n2, fft::ilog2(Q))];
-            Io<T>::store(ra + P * n2, v.x * scale);
-            Io<T>::store(rb + P * n2, v.y * scale);
+            Io<T>::store(ra + P * n2, v.x);
+            Io<T>::store(rb + P * n2, v.y);
         }
     }
 }
@@ -666,7 +677,7 @@ __device__ void phase_c(const float2 *__restrict__ Y, T *__restrict__ y, int img
     __syncthreads();
     c_col_combine<Cf>(ss, zo, tw);
     __syncthreads();
-    c_row_store<Cf, T>(zo, y + (size_t)img * N0 * N1, c, tw, 1.0f / ((float)N0 * (float)N1));
+    c_row_store<Cf, T>(zo, y + (size_t)img * N0 * N1, c, tw);
 }
 
 __device__ __forceinline__ void pdl_trigger() {
@@ -727,7 +738,7 @@ __device__ __forceinline__ void cta_record(const Args &a, int phase, int first,
 
 // item = (pair * nob + output block) * batch blocks + batch block; a.bg = batch
 // rows per block, a.ng = batch blocks
-template <class Cf, typename T, int kParts>
+template <class Cf, typename T, int kParts, int kNTB>
 __global__ void __launch_bounds__(kNTB) k_phase_b(Args a) {
     extern __shared__ __align__(16) char smem[];
     int it = blockIdx.x;

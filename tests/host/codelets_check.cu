@@ -63,6 +63,10 @@ static void check_split() {
         br += b[n] * cos(t); bi += b[n] * sin(t);
     }
     double err = fmax(fmax(fabs(A.x - ar), fabs(A.y - ai)), fmax(fabs(B.x - br), fabs(B.y - bi)));
+    // the unscaled split returns exactly twice the scaled one
+    float2 A2, B2;
+    split_real_pair2<N, Q>(v, A2, B2);
+    if (A2.x != 2.f * A.x || A2.y != 2.f * A.y || B2.x != 2.f * B.x || B2.y != 2.f * B.y) err = 1.0;
     printf("split<%d,%d> %.3e %.3e\n", N, Q, err, hypot(ar, ai) + hypot(br, bi));
 }
 
