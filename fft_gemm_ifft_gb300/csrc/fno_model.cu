@@ -5,10 +5,12 @@
 // bias, summed, GELU (none after the last layer)], and a two-layer 1x1
 // projection with a GELU between.  Each spectral convolution runs through the
 // layer plan (fused path); the 1x1 linears, bias, sum and GELU run here.
+#include <algorithm>
 #include <cstring>
 #include <new>
 
 #include "fno_internal.cuh"
+#include "fno_tc.cuh"
 
 using namespace fno;
 
@@ -24,6 +26,9 @@ struct Model {
     size_t spec_ws_bytes;
     size_t ws_bytes;
     int kernels;
+    // tensor-core linears (0 grid: the register-tiled SIMT kernels run instead)
+    int layer_tc_grid, head_tc_grid;
+    size_t layer_tc_smem, head_tc_smem;
 };
 
 __device__ __forceinline__ float gelu(float v) {
@@ -211,6 +216,227 @@ k_projection_tiled(const float *__restrict__ a, const float *__restrict__ P1,
     }
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core 1x1 linears (tcgen05, 3xTF32).  A 1x1 linear over a channels-
+// first activation is the dense GEMM D[p][o] = sum_i act[i][p] W[o][i] with
+// M = 128 pixels per tile, N = the output channels, K = the input channels.
+// Both operands are staged K-major with the 128-byte swizzle: the weights once
+// per CTA (hi = the value read at tf32 precision, lo = the exact remainder),
+// the activation tile transposed on its way into shared memory (each thread
+// owns one pixel row and writes 16-byte pieces, conflict-free under the
+// swizzle).  Three chains (hi*hi + hi*lo + lo*hi) accumulate in tensor
+// memory; the epilogue reads one pixel's N sums per thread (32x32b loads, a
+// warp per 32 lanes) and applies bias, the spectral sum and GELU (layer) or
+// GELU and the second projection (head).  A CTA walks tiles grid-stride.
+// ---------------------------------------------------------------------------
+namespace lintc {
+
+constexpr int kThreads = 512;            // four threads per pixel row of a tile
+constexpr int kParts4 = kThreads / 128;  // threads sharing a pixel (column quarters)
+constexpr int kRows = 128;               // M
+constexpr uint32_t kChunk = 16384;       // 128 rows x 128 bytes (32 fp32 of K)
+constexpr int kMaxK = 64;                // input channels (two 32-wide K chunks)
+constexpr int kMaxN = 128;               // output channels per tile
+
+struct Smem {                            // offsets from a 1024-aligned base
+    uint32_t ahi, alo, whi, wlo, total;
+};
+__host__ __device__ inline Smem smem_map(int k, int n) {
+    const uint32_t kc = (uint32_t)(k / 32);
+    const uint32_t wchunk = (uint32_t)n * 128;   // n rows x 128 bytes
+    Smem s;
+    s.ahi = 0;
+    s.alo = kc * kChunk;
+    s.whi = 2 * kc * kChunk;
+    s.wlo = s.whi + kc * ((wchunk + 1023) / 1024 * 1024);
+    s.total = s.wlo + kc * ((wchunk + 1023) / 1024 * 1024) + 1024;   // + alignment slack
+    return s;
+}
+
+// kHead = false: out[b][o][p] = act(sum_i W[o][i] a[b][i][p] + bias[o] + add[b][o][p])
+// kHead = true:  out[b][q][p] = sum_h P2[q][h] gelu(sum_i W[h][i] a[b][i][p] + bias[h]) + c2[q]
+// KC = input channels / 32, NG = output channels / 16 (fully unrolled, so that
+// every load of a tile is in flight before its first use)
+template <bool kHead, int KC, int NG>
+__global__ void __launch_bounds__(kThreads, 2)
+k_linear_tc(const float *__restrict__ a, const float *__restrict__ W,
+            const float *__restrict__ bias, const float *__restrict__ add,
+            const float *__restrict__ P2, const float *__restrict__ c2, float *__restrict__ out,
+            int cout2, int64_t npix, int64_t ntiles, int apply_gelu, int *err) {
+    using namespace tcu;
+    constexpr int cin = 32 * KC, n = 16 * NG;
+    static_assert(NG % kParts4 == 0 || NG < kParts4, "column groups split over the threads of a pixel");
+    constexpr int kCinT = cin / kParts4;                 // input channels loaded per thread
+    constexpr int kGroupsT = NG >= kParts4 ? NG / kParts4 : 1;   // column groups per thread
+    extern __shared__ __align__(1024) char smem_raw[];
+    char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t s_tmem;
+    __shared__ float s_head[kHead ? kParts4 * kMaxCout * 128 : 1];
+    const Smem sm = smem_map(cin, n);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    // thread -> (pixel row, quarter): warps w, w+4, w+8, w+12 share tensor-memory lanes
+    const int row = 32 * (warp & 3) + (tid & 31), quarter = warp >> 2;
+    constexpr uint32_t wchunk = ((uint32_t)n * 128 + 1023) / 1024 * 1024;
+    // weights, hi and lo, as the B operand (N rows = outputs, K = inputs)
+    for (int e = tid; e < n * cin; e += kThreads) {
+        const int o = e / cin, i = e % cin;
+        const float w = W[(int64_t)o * cin + i];
+        const uint32_t off = (uint32_t)(i / 32) * wchunk + sw_off(o, i % 32);
+        *reinterpret_cast<float *>(base + sm.whi + off) = w;
+        *reinterpret_cast<float *>(base + sm.wlo + off) = tf32_lo(w);
+    }
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    constexpr uint32_t ncols = n <= 32 ? 32 : (n <= 64 ? 64 : 128);
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(tc_smem_addr(&s_tmem)), "r"(ncols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    fence_async_smem();
+    tc_before_sync();
+    __syncthreads();
+    tc_after_sync();
+    const uint32_t tmem = s_tmem;
+    constexpr uint32_t idesc = idesc_tf32(n);
+    const int64_t ptiles = (npix + kRows - 1) / kRows;
+    uint32_t phase = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int64_t b = tile / ptiles, p0 = (tile % ptiles) * kRows;
+        const int64_t p = p0 + row;
+        const bool pin = p < npix;
+        // activation tile, transposed: row = pixel, K = input channel; this
+        // thread's quarter of the channels, every load in flight before a store
+        const int i0 = quarter * kCinT;
+        const float *ab = a + (b * cin + i0) * npix + p;
+        float av[kCinT];
+#pragma unroll
+        for (int i = 0; i < kCinT; ++i) av[i] = pin ? __ldcs(ab + (int64_t)i * npix) : 0.f;
+#pragma unroll
+        for (int i4 = 0; i4 < kCinT / 4; ++i4) {
+            const int i = i0 + 4 * i4;
+            const float4 v = make_float4(av[4 * i4], av[4 * i4 + 1], av[4 * i4 + 2], av[4 * i4 + 3]);
+            const uint32_t off = (uint32_t)(i / 32) * kChunk + sw_off(row, i % 32);
+            *reinterpret_cast<float4 *>(base + sm.ahi + off) = v;
+            *reinterpret_cast<float4 *>(base + sm.alo + off) =
+                make_float4(tf32_lo(v.x), tf32_lo(v.y), tf32_lo(v.z), tf32_lo(v.w));
+        }
+        fence_async_smem();
+        tc_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc_after_sync();
+            const uint32_t ah = tc_smem_addr(base + sm.ahi), al = tc_smem_addr(base + sm.alo);
+            const uint32_t wh = tc_smem_addr(base + sm.whi), wl = tc_smem_addr(base + sm.wlo);
+#pragma unroll
+            for (int c = 0; c < KC; ++c) {
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint32_t ao = c * kChunk + s * 32, bo = c * wchunk + s * 32;
+                    mma_tf32(tmem, desc_sw128(ah + ao), desc_sw128(wh + bo), idesc,
+                             (c | s) ? 1u : 0u);
+                    mma_tf32(tmem, desc_sw128(ah + ao), desc_sw128(wl + bo), idesc, 1u);
+                    mma_tf32(tmem, desc_sw128(al + ao), desc_sw128(wh + bo), idesc, 1u);
+                }
+            }
+            mma_commit(&bar);
+        }
+        // this thread's column groups (quarter q takes groups q, q + 4, ...)
+        const bool has_cols = quarter < NG;
+        // the spectral sums of these outputs are fetched while the MMAs run
+        float sv[kHead ? 1 : 16 * kGroupsT];
+        if constexpr (!kHead) {
+#pragma unroll
+            for (int gg = 0; gg < kGroupsT; ++gg)
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const int o = 16 * (quarter + kParts4 * gg) + q;
+                    sv[16 * gg + q] = (add && pin && has_cols)
+                                          ? __ldcs(add + (b * n + o) * npix + p) : 0.f;
+                }
+        }
+        const bool ok = mbar_wait(&bar, phase++, err);
+        tc_after_sync();
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        float hacc[kHead ? kMaxCout : 1];
+#pragma unroll
+        for (int q = 0; q < (kHead ? kMaxCout : 1); ++q) hacc[q] = 0.f;
+#pragma unroll
+        for (int gg = 0; gg < kGroupsT; ++gg) {
+            const int g = quarter + kParts4 * gg;
+            if (g < NG) {
+                float v[16];
+                tmem_ld16(lane_addr + 16 * g, v);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const int o = 16 * g + q;
+                    const float t = (ok ? v[q] : 0.f) + bias[o];
+                    if constexpr (kHead) {
+                        const float h = gelu(t);
+#pragma unroll
+                        for (int c = 0; c < kMaxCout; ++c)
+                            if (c < cout2) hacc[c] = fmaf(P2[(int64_t)c * n + o], h, hacc[c]);
+                    } else {
+                        float r = t + sv[16 * gg + q];
+                        if (apply_gelu) r = gelu(r);
+                        if (pin) out[(b * n + o) * npix + p] = r;
+                    }
+                }
+            }
+        }
+        if constexpr (kHead) {
+            // the four quarters of a pixel add their partial sums
+#pragma unroll
+            for (int c = 0; c < kMaxCout; ++c)
+                if (c < cout2) s_head[(quarter * kMaxCout + c) * 128 + row] = hacc[c];
+            __syncthreads();
+            if (quarter == 0 && pin) {
+                for (int c = 0; c < cout2; ++c) {
+                    float v = c2[c];
+#pragma unroll
+                    for (int qq = 0; qq < kParts4; ++qq) v += s_head[(qq * kMaxCout + c) * 128 + row];
+                    out[(b * cout2 + c) * npix + p] = v;
+                }
+            }
+        }
+        tc_before_sync();
+        __syncthreads();            // tensor memory and the A tile are reused by the next tile
+    }
+    if (warp == 0) {
+        tc_after_sync();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(ncols));
+    }
+}
+
+// Whether a linear with these channel counts runs on the tensor cores.
+inline bool eligible(int cin, int n) {
+    return (cin == 32 || cin == 64) && (n == 32 || n == 48 || n == 64 || n == 128);
+}
+
+using TcFn = void (*)(const float *, const float *, const float *, const float *,
+                      const float *, const float *, float *, int, int64_t, int64_t, int, int *);
+
+template <bool kHead, int KC>
+TcFn pick_n(int n) {
+    switch (n) {
+        case 32: return k_linear_tc<kHead, KC, 2>;
+        case 48: return k_linear_tc<kHead, KC, 3>;
+        case 64: return k_linear_tc<kHead, KC, 4>;
+        default: return k_linear_tc<kHead, KC, 8>;
+    }
+}
+template <bool kHead>
+TcFn kernel(int cin, int n) {
+    return cin == 32 ? pick_n<kHead, 1>(n) : pick_n<kHead, 2>(n);
+}
+
+}  // namespace lintc
+
 using ProjFn = void (*)(const float *, const float *, const float *, const float *,
                        const float *, float *, int, int, int, int64_t);
 ProjFn projection_kernel(int cout) {
@@ -263,6 +489,40 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
         delete m;
         return FNO_ERR_CUDA;
     }
+    // tensor-core linears where the channel counts fit one K x N tile
+    m->layer_tc_grid = m->head_tc_grid = 0;
+    const int64_t ntiles = d->batch * ((d->h * d->w + lintc::kRows - 1) / lintc::kRows);
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    auto setup_tc = [&](lintc::TcFn fn, int cin, int n, int *grid, size_t *smem_bytes) {
+        if (!lintc::eligible(cin, n)) return true;
+        const size_t sb = lintc::smem_map(cin, n).total;
+        int per_sm = 0;
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sb) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
+                cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, lintc::kThreads, sb) !=
+                cudaSuccess)
+            return false;
+        if (per_sm < 1) return true;
+        const int64_t g = std::min<int64_t>(ntiles, (int64_t)sms * per_sm);
+        *grid = (int)g;
+        *smem_bytes = sb;
+        return true;
+    };
+    const bool tc_ok = lintc::eligible(d->width, d->width), th_ok =
+        lintc::eligible(d->width, d->hidden);
+    if ((tc_ok && !setup_tc(lintc::kernel<false>(d->width, d->width), d->width, d->width,
+                            &m->layer_tc_grid, &m->layer_tc_smem)) ||
+        (th_ok && !setup_tc(lintc::kernel<true>(d->width, d->hidden), d->width, d->hidden,
+                            &m->head_tc_grid, &m->head_tc_smem))) {
+        cudaGetLastError();
+        fno_plan_destroy(m->spec);
+        delete m;
+        return FNO_ERR_CUDA;
+    }
     int spec_kernels = 0;
     fno_spectral_conv_kernel_count(m->spec, &spec_kernels);
     m->npix = d->h * d->w;
@@ -306,6 +566,8 @@ fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_param
     const size_t spec_stride = (size_t)2 * d.width * d.width * d.modes[0] * d.modes[1] * 2;
 
     const unsigned ptiles = (unsigned)((m.npix + kTP - 1) / kTP);
+    const int64_t ntiles = d.batch * ((m.npix + lintc::kRows - 1) / lintc::kRows);
+    int *err = reinterpret_cast<Plan *>(m.spec)->dev_err;
     const dim3 lin_grid(ptiles, (unsigned)((d.width + kTO - 1) / kTO), (unsigned)d.batch);
     const size_t smem = sizeof(TileSmem);
     k_linear_tiled<<<lin_grid, kTT, smem, s>>>(static_cast<const float *>(x), p->lift_w,
@@ -318,17 +580,29 @@ fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_param
                                                     stream);
         if (st != FNO_OK) return st;
         const int last = (l == d.nlayers - 1);
-        k_linear_tiled<<<lin_grid, kTT, smem, s>>>(
-            A, p->pw_w + (size_t)l * d.width * d.width, p->pw_b + (size_t)l * d.width, S, T,
-            d.width, d.width, m.npix, last ? 0 : 1);
+        if (m.layer_tc_grid)
+            lintc::kernel<false>(d.width, d.width)<<<m.layer_tc_grid, lintc::kThreads,
+                                                     m.layer_tc_smem, s>>>(
+                A, p->pw_w + (size_t)l * d.width * d.width, p->pw_b + (size_t)l * d.width, S,
+                nullptr, nullptr, T, 0, m.npix, ntiles, last ? 0 : 1, err);
+        else
+            k_linear_tiled<<<lin_grid, kTT, smem, s>>>(
+                A, p->pw_w + (size_t)l * d.width * d.width, p->pw_b + (size_t)l * d.width, S, T,
+                d.width, d.width, m.npix, last ? 0 : 1);
         if (cudaGetLastError() != cudaSuccess) return FNO_ERR_CUDA;
         float *tmp = A;
         A = T;
         T = tmp;
     }
-    projection_kernel(d.cout)<<<dim3(ptiles, (unsigned)d.batch), kTT, smem, s>>>(
-        A, p->proj1_w, p->proj1_b, p->proj2_w, p->proj2_b, static_cast<float *>(out), d.width,
-        d.hidden, d.cout, m.npix);
+    if (m.head_tc_grid)
+        lintc::kernel<true>(d.width, d.hidden)<<<m.head_tc_grid, lintc::kThreads,
+                                                 m.head_tc_smem, s>>>(
+            A, p->proj1_w, p->proj1_b, nullptr, p->proj2_w, p->proj2_b,
+            static_cast<float *>(out), d.cout, m.npix, ntiles, 1, err);
+    else
+        projection_kernel(d.cout)<<<dim3(ptiles, (unsigned)d.batch), kTT, smem, s>>>(
+            A, p->proj1_w, p->proj1_b, p->proj2_w, p->proj2_b, static_cast<float *>(out),
+            d.width, d.hidden, d.cout, m.npix);
     if (cudaGetLastError() != cudaSuccess) return FNO_ERR_CUDA;
     return FNO_OK;
 }

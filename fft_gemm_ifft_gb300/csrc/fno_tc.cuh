@@ -1,0 +1,100 @@
+// fno_tc.cuh -- tcgen05 building blocks shared by the tensor-core kernels:
+// the 128-byte-swizzled K-major operand layout for 32-bit elements, its
+// shared-memory descriptor, the tf32 instruction descriptor, the 3xTF32 split,
+// MMA issue / commit, tensor-memory loads and a bounded mbarrier wait.
+#pragma once
+
+#include <cstring>
+
+#include "fno_internal.cuh"
+
+namespace fno {
+namespace tcu {
+
+__device__ __forceinline__ uint32_t tc_smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ long long tc_globaltimer() {
+    long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+constexpr long long kTcWaitTimeoutNs = 500000000;   // bounded device waits: 0.5 s
+
+// byte offset of (row, col) in a chunk of rows x 32 fp32 stored K-major with
+// the 128-byte swizzle (8-row atoms of 1024 bytes, 16-byte pieces permuted by
+// row % 8); the chunk must start on a 1024-byte boundary
+__host__ __device__ inline uint32_t sw_off(int row, int col) {
+    const uint32_t b = (uint32_t)col * 4, r = row & 7, j = b >> 4;
+    return (uint32_t)(row >> 3) * 1024 + r * 128 + ((j ^ r) << 4) + (b & 15);
+}
+__host__ __device__ inline float tf32_lo(float v) {
+    uint32_t u;
+    memcpy(&u, &v, 4);
+    u &= 0xFFFFE000u;
+    float h;
+    memcpy(&h, &u, 4);
+    return v - h;
+}
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// instruction descriptor: D f32, A/B tf32, K-major, M = 128
+__host__ __device__ constexpr uint32_t idesc_tf32(int n) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+__device__ __forceinline__ void mma_tf32(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t acc) {
+    asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}"
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(tc_smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+// Bounded wait for the phase `n` (0, 1, 2, ...) of an mbarrier; on time-out the
+// error word is set and the caller goes on (its results are then discarded).
+__device__ inline bool mbar_wait(uint64_t *bar, uint32_t n, int *err) {
+    const uint32_t a = tc_smem_addr(bar), parity = n & 1;
+    uint32_t done = 0;
+    long long t0 = 0;
+    for (uint32_t spin = 0;; ++spin) {
+        asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                     "selp.u32 %0, 1, 0, p;\n}" : "=r"(done) : "r"(a), "r"(parity) : "memory");
+        if (done) return true;
+        if (spin == 0) t0 = tc_globaltimer();
+        if ((spin & 1023u) == 1023u) {
+            if (*reinterpret_cast<volatile int *>(err) != 0) return false;
+            if (tc_globaltimer() - t0 > kTcWaitTimeoutNs) {
+                raise_dev_error(err, kDevTimeout);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"
+                 "%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace tcu
+}  // namespace fno

@@ -45,7 +45,13 @@ def test_small_stack_matches_oracle():
     (2, 5, 2, 2, 2, (1, 1), 9, 1),
     (1, 12, 2, 8, 16, (2, 3), 130, 8),
     (2, 6, 1, 12, 20, (3, 4), 10, 1),
-], ids=["ragged_channels", "tiny_grid", "wide_hidden", "grid_not_power_of_two"])
+    # tensor-core linears (32 / 64 input channels, multiples of 16 outputs),
+    # including a last tile with fewer than 128 pixels
+    (2, 32, 2, 8, 16, (2, 3), 48, 3),
+    (1, 64, 1, 8, 8, (2, 2), 16, 2),
+    (3, 64, 2, 16, 32, (4, 4), 128, 1),
+], ids=["ragged_channels", "tiny_grid", "wide_hidden", "grid_not_power_of_two",
+        "tc_32_channels", "tc_partial_tile", "tc_64_channels"])
 def test_stack_ragged_tiles(shape):
     b, width, nl, h, w, modes, hidden, cout = shape
     case = workloads.FnoCase("ragged", batch=b, width=width, nlayers=nl, h=h, w=w,
