@@ -884,9 +884,15 @@ struct Pdl {
         p.fused_ob = ob;
         p.fused_smem = sb;             // kernel B's; A and C use their fixed sizes
         p.fused_grid = 0;
+        // tensor-core mixing where the kept modes arrive reduced (one copy)
+        p.fused_mixtc = kParts == 1 && !(p.flags & FNO_PLAN_SIMT_MIX) &&
+                        mixtc_supported(p.g.d, p.dtype, p.batch, p.cin, p.cout, Cf::M1,
+                                        p.g.nkept);
+        if (e == cudaSuccess && p.fused_mixtc) e = mixtc_init(p.dtype);
         if (e == cudaSuccess && (p.flags & FNO_PLAN_TRACE)) {
-            const size_t nB = (size_t)(p.g.nkept / kG) * ((p.cout + ob - 1) / ob) *
-                              ((p.batch + bb - 1) / bb);
+            const size_t nB = p.fused_mixtc ? (size_t)mixtc_items(p.g.nkept)
+                                            : (size_t)(p.g.nkept / kG) * ((p.cout + ob - 1) / ob) *
+                                                  ((p.batch + bb - 1) / bb);
             p.trace_records = (size_t)p.batch * (p.cin * Cf::C + p.cout * CfC::C) + nB;
             e = cudaMalloc(&p.trace, p.trace_records * sizeof(fno_trace_record_t));
         }
@@ -918,7 +924,7 @@ struct Pdl {
         a.nob = (p.cout + a.ob - 1) / a.ob;
         a.npairs = (int)(p.g.nkept / kG);
         const int nA = (int)p.batch * p.cin * Cf::C;
-        const int nB = a.npairs * a.nob * a.ng;
+        const int nB = p.fused_mixtc ? mixtc_items(p.g.nkept) : a.npairs * a.nob * a.ng;
         const int nC = (int)p.batch * p.cout * CfC::C;
         a.trace = p.trace;
         a.trace_b = nA;
@@ -945,10 +951,28 @@ struct Pdl {
         cfg.stream = s;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        cfg.gridDim = dim3(nB);
-        cfg.blockDim = dim3(kBThreads);
-        cfg.dynamicSmemBytes = p.fused_smem;
-        e = cudaLaunchKernelEx(&cfg, k_phase_b<Cf, T, kParts, kBThreads>, a);
+        if (p.fused_mixtc) {
+            MixTcArgs m;
+            m.X = a.part;
+            m.w = a.w;
+            m.Y = a.Y;
+            m.err = a.err;
+            m.trace = a.trace;
+            m.trace_first = nA;
+            m.batch = (int)p.batch;
+            m.cin = p.cin;
+            m.cout = p.cout;
+            m.m0 = Cf::M0;
+            m.m1 = Cf::M1;
+            m.mblk = (int)Cf::MBLK;
+            m.nk = Cf::NK;
+            e = mixtc_launch(p.dtype, m, s);
+        } else {
+            cfg.gridDim = dim3(nB);
+            cfg.blockDim = dim3(kBThreads);
+            cfg.dynamicSmemBytes = p.fused_smem;
+            e = cudaLaunchKernelEx(&cfg, k_phase_b<Cf, T, kParts, kBThreads>, a);
+        }
         if (e != cudaSuccess) return e;
         cfg.gridDim = dim3(nC);
         cfg.blockDim = dim3(kNT);

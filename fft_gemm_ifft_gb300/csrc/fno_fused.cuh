@@ -30,6 +30,23 @@ cudaError_t fused_forward_modes(const Plan &p, const void *x, int64_t nimg, floa
 cudaError_t fused3d_forward_modes(const Plan &p, const void *x, int64_t nimg, float2 *out,
                                   cudaStream_t s);
 
+// Tensor-core mixing (kernel B of the three-kernel 2-D path) for 16-bit
+// storage: four adjacent modes per CTA, real-block complex GEMMs on tcgen05.
+struct MixTcArgs {
+    const float2 *X;              // kept modes [batch * cin][nk]
+    const void *w;                // weights (2, cin, cout, m0, m1) interleaved complex
+    float2 *Y;                    // mixed modes [batch * cout][nk]
+    int *err;
+    fno_trace_record_t *trace;    // nullptr unless tracing
+    int trace_first;
+    int batch, cin, cout, m0, m1, mblk, nk;
+};
+bool mixtc_supported(int d, fno_dtype_t dtype, int64_t batch, int cin, int cout, int m1,
+                     int64_t nkept);
+int mixtc_items(int64_t nkept);
+cudaError_t mixtc_init(fno_dtype_t dtype);
+cudaError_t mixtc_launch(fno_dtype_t dtype, const MixTcArgs &args, cudaStream_t s);
+
 // The 1-D layer's kernel (one cluster per sample).
 bool fused1d_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout);
 cudaError_t fused1d_forward(const Plan &p, const Buffers &b, cudaStream_t s);

@@ -1,0 +1,287 @@
+// fno_mix_tc.cu -- the per-mode channel mixing on the tensor cores, for 16-bit
+// storage (fp16 / bfloat16 operands, float32 accumulation).
+//
+// The mixing of the TurboFNO article (gsyq.cn/news/457482) §2.2, Y[b,o,k] =
+// sum_i X[b,i,k] W[i,o,k], is per mode k a complex (B x Cin) . (Cin x Cout)
+// product.  Written in real-block form with the output channels on the M side,
+//
+//     [Yr]   [ Wr^T  -Wi^T ] [Xr]
+//     [Yi] = [ Wi^T   Wr^T ] [Xi]      (M = 2 Cout rows, K = 2 Cin, N = batch)
+//
+// it is one tcgen05.mma chain (kind::f16, M = 128, K = 128 in 8 steps of 16)
+// per mode, accumulating in tensor memory.  A CTA takes a run of four
+// adjacent modes of one kept row (adjacent in the weight tensor too): it
+// builds the four 128 x 128 real-block weight operands in shared memory (128-
+// byte swizzle, K-major) from 16-byte loads of the weights -- before waiting
+// for the forward-transform kernel, since they do not depend on it -- then
+// the four operands [Xr; Xi]^T (N rows = batch) from the kept modes, issues
+// the four chains into four column ranges of tensor memory, and writes Y for
+// the four modes of every (b, o) as one 32-byte piece through a shared-memory
+// staging tile.  Channel counts up to 64 are zero-padded to the tile.
+#include "fno_fused_dev.cuh"
+#include "fno_tc.cuh"
+
+namespace fno {
+namespace {
+
+using namespace tcu;
+
+constexpr int kMT = 256;                  // threads
+constexpr int kRun = 4;                   // modes per CTA
+constexpr int kCh = 64;                   // channel tile (Cin, Cout <= 64)
+constexpr uint32_t kAChunk = 128 * 128;   // 128 rows x 128 bytes (64 elements of K)
+constexpr uint32_t kAMode = 2 * kAChunk;  // one mode's weight operand (K = 128)
+constexpr int kMaxB = 64;                 // batch rows (N) per CTA
+constexpr uint32_t kBChunk = kMaxB * 128;
+constexpr uint32_t kBMode = 2 * kBChunk;
+constexpr uint32_t kOffB = kRun * kAMode;                 // 128 KiB of weight operands
+constexpr uint32_t kSmem = kOffB + kRun * kBMode + 1024;  // + 64 KiB of X operands + align
+constexpr uint32_t kTmemCols = 256;                        // kRun x N (N <= 64)
+
+template <typename T> struct Bits;
+template <> struct Bits<__half> {
+    static constexpr bool kBf16 = false;
+    static __device__ __forceinline__ unsigned short from(float v) {
+        return __half_as_ushort(__float2half_rn(v));
+    }
+};
+template <> struct Bits<__nv_bfloat16> {
+    static constexpr bool kBf16 = true;
+    static __device__ __forceinline__ unsigned short from(float v) {
+        return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kMT, 1) k_mix_tc(MixTcArgs a) {
+    extern __shared__ __align__(1024) char smem_raw[];
+    char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t s_tmem;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const unsigned long long t0 = a.trace ? trace_now() : 0;
+    const int mode0 = blockIdx.x * kRun;
+    const int nbp = (a.batch + 15) / 16 * 16;                // N: batch padded to 16
+    // kept row j and bin k of mode0; weight block and local index
+    const int j = mode0 / a.m1, k = mode0 % a.m1;
+    const int blk = j >= a.m0 ? 1 : 0;
+    const int local0 = (j - blk * a.m0) * a.m1 + k;
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(tc_smem_addr(&s_tmem)), "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    // 1. zero the operands where the channel counts leave padding
+    if (a.cin < kCh || a.cout < kCh) {
+        for (int e = tid; e < (int)(kRun * kAMode / 16); e += kMT)
+            reinterpret_cast<uint4 *>(base)[e] = make_uint4(0, 0, 0, 0);
+        __syncthreads();
+    }
+    // 2. weight operands of the four modes (independent of kernel A)
+    using U = unsigned short;
+    const T *w = static_cast<const T *>(a.w);
+    // a unit = one output o and eight consecutive input channels: eight 16-byte
+    // loads (four modes each), then per mode and quadrant one 16-byte store of
+    // eight consecutive K elements (conflict-free under the swizzle)
+    for (int un = tid; un < kCh * (kCh / 8); un += kMT) {
+        const int o = un % kCh, i0 = 8 * (un / kCh);
+        if (o >= a.cout || i0 >= a.cin) continue;
+        uint4 q[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            q[t] = make_uint4(0, 0, 0, 0);
+            if (i0 + t < a.cin)
+                q[t] = __ldg(reinterpret_cast<const uint4 *>(
+                    w + ((((size_t)blk * a.cin + i0 + t) * a.cout + o) * a.mblk + local0) * 2));
+        }
+#pragma unroll
+        for (int r = 0; r < kRun; ++r) {
+            // element t of mode r: re = half 2r, im = half 2r + 1 of q[t]
+            U re[8], im[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const uint32_t word = r == 0 ? q[t].x : (r == 1 ? q[t].y : (r == 2 ? q[t].z : q[t].w));
+                re[t] = (U)(word & 0xFFFF);
+                im[t] = (U)(word >> 16);
+            }
+            auto pack = [](const U (&v)[8], bool negate) {
+                uint4 p;
+                const uint32_t m = negate ? 0x80008000u : 0u;
+                p.x = ((uint32_t)v[0] | ((uint32_t)v[1] << 16)) ^ m;
+                p.y = ((uint32_t)v[2] | ((uint32_t)v[3] << 16)) ^ m;
+                p.z = ((uint32_t)v[4] | ((uint32_t)v[5] << 16)) ^ m;
+                p.w = ((uint32_t)v[6] | ((uint32_t)v[7] << 16)) ^ m;
+                return p;
+            };
+            char *A = base + r * kAMode;
+            // row o: [Wr | -Wi], row 64 + o: [Wi | Wr]; K columns i0.. and 64 + i0..
+            *reinterpret_cast<uint4 *>(A + sw_off16(o, i0)) = pack(re, false);
+            *reinterpret_cast<uint4 *>(A + kAChunk + sw_off16(o, i0)) = pack(im, true);
+            *reinterpret_cast<uint4 *>(A + sw_off16(kCh + o, i0)) = pack(im, false);
+            *reinterpret_cast<uint4 *>(A + kAChunk + sw_off16(kCh + o, i0)) = pack(re, false);
+        }
+    }
+    pdl_trigger();
+    pdl_wait();                                  // kernel A's kept modes are complete
+    const unsigned long long t1 = a.trace ? trace_now() : 0;
+    // 3. X operands: row n = batch index, K columns [Xr(i) | Xi(i)].  A unit is
+    //    one batch row and eight input channels: sixteen 16-byte loads, then per
+    //    mode two 16-byte stores
+    for (int un = tid; un < nbp * (kCh / 8); un += kMT) {
+        const int bb = un / (kCh / 8), i0 = 8 * (un % (kCh / 8));
+        float4 v[16];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            v[2 * t] = v[2 * t + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (bb < a.batch && i0 + t < a.cin) {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    a.X + ((size_t)bb * a.cin + i0 + t) * a.nk + mode0);
+                v[2 * t] = __ldcg(src);
+                v[2 * t + 1] = __ldcg(src + 1);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kRun; ++r) {
+            uint32_t pr[4], pi[4];
+#pragma unroll
+            for (int t2 = 0; t2 < 4; ++t2) {
+                float xr[2], xi[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float4 &u4 = v[2 * (2 * t2 + h) + r / 2];
+                    xr[h] = (r & 1) ? u4.z : u4.x;
+                    xi[h] = (r & 1) ? u4.w : u4.y;
+                }
+                pr[t2] = (uint32_t)Bits<T>::from(xr[0]) | ((uint32_t)Bits<T>::from(xr[1]) << 16);
+                pi[t2] = (uint32_t)Bits<T>::from(xi[0]) | ((uint32_t)Bits<T>::from(xi[1]) << 16);
+            }
+            char *B = base + kOffB + r * kBMode;
+            *reinterpret_cast<uint4 *>(B + sw_off16(bb, i0)) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+            *reinterpret_cast<uint4 *>(B + kBChunk + sw_off16(bb, i0)) =
+                make_uint4(pi[0], pi[1], pi[2], pi[3]);
+        }
+    }
+    fence_async_smem();
+    tc_before_sync();
+    __syncthreads();
+    tc_after_sync();
+    const uint32_t tmem = s_tmem;
+    if (tid == 0) {
+        const uint32_t idesc = idesc_f16(nbp, Bits<T>::kBf16);
+#pragma unroll
+        for (int r = 0; r < kRun; ++r) {
+            const uint32_t am = tc_smem_addr(base + r * kAMode);
+            const uint32_t bm = tc_smem_addr(base + kOffB + r * kBMode);
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_f16(tmem + r * nbp, desc_sw128(am + c * kAChunk + s * 32),
+                            desc_sw128(bm + c * kBChunk + s * 32), idesc, (c | s) ? 1u : 0u);
+        }
+        mma_commit(&bar);
+    }
+    const bool ok = mbar_wait(&bar, 0, a.err);
+    tc_after_sync();
+    // 4. tensor memory -> staging [b][o][4 modes] complex (over the weight operands,
+    //    which the finished MMAs no longer read)
+    float *stage = reinterpret_cast<float *>(base);
+    {
+        const int m = 32 * (warp & 3) + (tid & 31);          // D row: o (re) or 64 + o (im)
+        const int o = m % kCh, part = m / kCh;
+        for (int r = 2 * (warp >> 2); r < 2 * (warp >> 2) + 2; ++r) {
+            for (int g = 0; g < nbp / 16; ++g) {
+                float v[16];
+                tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + r * nbp + 16 * g, v);
+                if (o < a.cout) {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int b = 16 * g + q;
+                        if (b < a.batch)
+                            stage[(((size_t)b * kCh + o) * kRun + r) * 2 + part] = ok ? v[q] : 0.f;
+                    }
+                }
+            }
+        }
+    }
+    tc_before_sync();
+    __syncthreads();
+    // 5. Y for the four modes of every (b, o): 32 contiguous bytes
+    for (int e = tid; e < a.batch * a.cout; e += kMT) {
+        const int b = e / a.cout, o = e % a.cout;
+        const float4 *s4 = reinterpret_cast<const float4 *>(stage + ((size_t)b * kCh + o) * kRun * 2);
+        float4 *dst = reinterpret_cast<float4 *>(a.Y + ((size_t)b * a.cout + o) * a.nk + mode0);
+        __stcg(dst, s4[0]);
+        __stcg(dst + 1, s4[1]);
+    }
+    if (warp == 0) {
+        tc_after_sync();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols));
+    }
+    if (a.trace) {
+        __syncthreads();
+        if (tid == 0) {
+            unsigned smid;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+            fno_trace_record_t rec;
+            rec.item = (1u << 24) | (blockIdx.x & 0xFFFFFFu);
+            rec.worker = smid;
+            rec.t_start = t0;
+            rec.t_ready = t1;
+            rec.t_compute = rec.t_end = trace_now();
+            a.trace[a.trace_first + blockIdx.x] = rec;
+        }
+    }
+}
+
+}  // namespace
+
+bool mixtc_supported(int d, fno_dtype_t dtype, int64_t batch, int cin, int cout, int m1,
+                     int64_t nkept) {
+    return d == 2 && (dtype == FNO_F16 || dtype == FNO_BF16) && cin <= kCh && cout <= kCh &&
+           batch >= 1 && batch <= kMaxB && m1 % kRun == 0 && nkept % kRun == 0;
+}
+
+int mixtc_items(int64_t nkept) { return (int)(nkept / kRun); }
+
+cudaError_t mixtc_init(fno_dtype_t dtype) {
+    return with_storage(dtype, [&](auto t) {
+        using T = decltype(t);
+        if constexpr (std::is_same<T, float>::value) {
+            return cudaErrorInvalidValue;
+        } else {
+            return cudaFuncSetAttribute(k_mix_tc<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kSmem);
+        }
+    });
+}
+
+cudaError_t mixtc_launch(fno_dtype_t dtype, const MixTcArgs &args, cudaStream_t s) {
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(args.nk / kRun));
+    cfg.blockDim = dim3(kMT);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = s;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return with_storage(dtype, [&](auto t) {
+        using T = decltype(t);
+        if constexpr (std::is_same<T, float>::value) {
+            return cudaErrorInvalidValue;
+        } else {
+            cudaError_t e = cudaLaunchKernelEx(&cfg, k_mix_tc<T>, args);
+            return e != cudaSuccess ? e : cudaGetLastError();
+        }
+    });
+}
+
+}  // namespace fno

@@ -235,8 +235,6 @@ constexpr int kThreads = 512;            // four threads per pixel row of a tile
 constexpr int kParts4 = kThreads / 128;  // threads sharing a pixel (column quarters)
 constexpr int kRows = 128;               // M
 constexpr uint32_t kChunk = 16384;       // 128 rows x 128 bytes (32 fp32 of K)
-constexpr int kMaxK = 64;                // input channels (two 32-wide K chunks)
-constexpr int kMaxN = 128;               // output channels per tile
 
 struct Smem {                            // offsets from a 1024-aligned base
     uint32_t ahi, alo, whi, wlo, total;

@@ -96,5 +96,24 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// byte offset of (row, col) in a chunk of rows x 64 16-bit elements stored
+// K-major with the 128-byte swizzle (same atoms as above, 8 elements per
+// 16-byte piece)
+__host__ __device__ inline uint32_t sw_off16(int row, int col) {
+    const uint32_t b = (uint32_t)col * 2, r = row & 7, j = b >> 4;
+    return (uint32_t)(row >> 3) * 1024 + r * 128 + ((j ^ r) << 4) + (b & 15);
+}
+// instruction descriptor: D f32, A/B f16 (bf16 = false) or bf16, K-major, M = 128
+__host__ __device__ constexpr uint32_t idesc_f16(int n, bool bf16) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t acc) {
+    asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
 }  // namespace tcu
 }  // namespace fno

@@ -95,6 +95,10 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * an internal plan of the adjoint layer (Cin and Cout swapped) and reports a
  * workspace size that covers the backward call as well.                    */
 #define FNO_PLAN_BACKWARD 16u
+/* Mix with the SIMT kernel where the tensor-core mixing kernel would run
+ * (2-D fp16 / bf16 layers with at most 64 channels and 64 samples; the
+ * tensor-core kernel is the default there).  An ablation switch.            */
+#define FNO_PLAN_SIMT_MIX 32u
 
 /* One work item of the fused kernel, as recorded under FNO_PLAN_TRACE.
  * Times are the GPU's global nanosecond timer.                              */

@@ -67,8 +67,8 @@ def _lib(fno, oracle_mod):
 
 
 @pytest.mark.parametrize("flags", [0, FNO_PLAN_UNFUSED, capi.FNO_PLAN_TENSOR_CORES,
-                                   capi.FNO_PLAN_PERSISTENT],
-                         ids=["default", "unfused", "tensor_cores", "persistent"])
+                                   capi.FNO_PLAN_PERSISTENT, capi.FNO_PLAN_SIMT_MIX],
+                         ids=["default", "unfused", "tensor_cores", "persistent", "simt_mix"])
 @pytest.mark.parametrize("spec", SMALL, ids=[case_id(c) for c in SMALL])
 def test_small_cases_match_oracle(spec, flags):
     n, modes, b, ci, co, dt = spec
@@ -158,6 +158,21 @@ def test_every_workload_runs_fused(name, kernels):
                         FNO_PLAN_UNFUSED)
     assert conv.kernel_count == 2 * len(case.n) + 1
     conv.close()
+
+
+@pytest.mark.parametrize("name", ["2d_f16", "2d_bf16"])
+def test_tensor_core_and_simt_mixing_agree(name):
+    # both within the half-storage bar of the oracle (sampled) and of each other
+    case = workloads.CASES[name]
+    x, w = workloads.make_x(case), workloads.make_w(case)
+    a, _ = run_gpu(case, x, w)
+    b, _ = run_gpu(case, x, w, capi.FNO_PLAN_SIMT_MIX)
+    c, _ = run_gpu(case, x, w)
+    assert np.array_equal(a, c), "two runs of the tensor-core mixing differ"
+    assert_close(a, b.astype(np.float64), case.dtype, "tensor-core vs SIMT mixing")
+    for s in (0, case.batch - 1):
+        ref = run_oracle(case, x[s:s + 1], w)
+        assert_close(a[s:s + 1], ref, case.dtype, f"{name}[b={s}] tensor-core mixing")
 
 
 def test_fused_3d_and_unfused_agree():
