@@ -35,6 +35,7 @@ FNO_PLAN_TENSOR_CORES = 4
 FNO_PLAN_PERSISTENT = 8
 FNO_PLAN_BACKWARD = 16
 FNO_PLAN_SIMT_MIX = 32
+FNO_PLAN_SIMT_TRANSFORM = 64
 
 # Every symbol include/fno.h declares.
 EXPORTS = (

@@ -84,7 +84,8 @@ fno_status_t describe(int ndim, const int64_t *n, const int32_t *modes, int64_t 
     if (batch < 1 || cin < 1 || cout < 1) return FNO_ERR_INVALID_ARG;
     if (dtype != FNO_F32 && dtype != FNO_F16 && dtype != FNO_BF16) return FNO_ERR_INVALID_ARG;
     if (flags & ~(FNO_PLAN_UNFUSED | FNO_PLAN_TRACE | FNO_PLAN_TENSOR_CORES |
-                  FNO_PLAN_PERSISTENT | FNO_PLAN_BACKWARD | FNO_PLAN_SIMT_MIX))
+                  FNO_PLAN_PERSISTENT | FNO_PLAN_BACKWARD | FNO_PLAN_SIMT_MIX |
+                  FNO_PLAN_SIMT_TRANSFORM))
         return FNO_ERR_INVALID_ARG;
     // int64 element counts must not overflow and a tensor must stay addressable
     const double xe = (double)batch * cin * g->npix, ye = (double)batch * cout * g->npix;

@@ -35,6 +35,7 @@
 // mixing and inverse phases are issued as cp.async copies all at once, and
 // the weights of a mixing item are fetched before it waits for phase A.
 #include <new>
+#include <vector>
 
 #include "fno_fused_dev.cuh"
 #include "fno_tc.cuh"
@@ -696,6 +697,250 @@ void make_tables(float *img) {
 }  // namespace tc
 
 // ---------------------------------------------------------------------------
+// Kernel A of the three-kernel path on the tensor cores: one CTA transforms a
+// whole input image, so the kept modes leave it complete (no partial copies).
+//
+// TMA brings the image into shared memory as M tiles of 128 rows, K-major with
+// the 128-byte swizzle.  The row DFT of bins 0..M1-1 is the GEMM
+// Z = X . T^T, T[j][n] = cos(2 pi j n / N1) (j < M1) and -sin(...) (j >= M1),
+// on tcgen05 with the accumulator in tensor memory: fp32 images run three
+// kind::tf32 passes (x_hi t_hi + x_hi t_lo + x_lo t_hi, x_lo the exact
+// remainder written over the tile in place), 16-bit images one kind::f16 pass
+// (their tolerance class is 1e-2).  The column DFT over the N0 rows, kept rows
+// only, runs on the SIMT cores from the tensor-memory rows: r = r1 + R1 r2,
+// B2-point register FFTs over r2, then X[j][k] = sum_r1 W_N0^{f r1} S[r1][f mod B2][k].
+// ---------------------------------------------------------------------------
+namespace tca {
+
+constexpr int NT = 256;
+template <typename T> struct Shape;
+template <> struct Shape<float> {          // 128 x 128, 16 x 16 modes
+    static constexpr int N0 = 128, N1 = 128, M0 = 16, M1 = 16, kE = 32, B2 = 8;
+    static constexpr bool kSplit = true;
+    static constexpr int kMinBlocks = 2;
+};
+template <> struct Shape<__half> {         // 256 x 256, 32 x 32 modes
+    static constexpr int N0 = 256, N1 = 256, M0 = 32, M1 = 32, kE = 64, B2 = 16;
+    static constexpr bool kSplit = false;
+    static constexpr int kMinBlocks = 1;
+};
+template <> struct Shape<__nv_bfloat16> : Shape<__half> {};
+
+template <typename T>
+struct Geo {
+    using S = Shape<T>;
+    static constexpr int N0 = S::N0, N1 = S::N1, M0 = S::M0, M1 = S::M1, kE = S::kE;
+    static constexpr int KC = N1 / kE;                  // K chunks of 128 bytes
+    static constexpr int MT = N0 / 128;                 // M tiles
+    static constexpr int N = 2 * M1;                    // MMA N: bins, re then im
+    static constexpr int K0 = 2 * M0, NK = K0 * M1;
+    static constexpr int B2 = S::B2, R1 = N0 / B2;
+    static constexpr uint32_t kTile = 16384;            // 128 rows x 128 bytes
+    static constexpr uint32_t kXBytes = (uint32_t)MT * KC * kTile;
+    static constexpr uint32_t kTChunk = (uint32_t)N * 128;
+    static constexpr uint32_t kTBytes = (S::kSplit ? 2u : 1u) * KC * kTChunk;
+    static constexpr int ZS = M1 + 1;                   // Z plane row stride (floats)
+    static constexpr uint32_t kZBytes = (uint32_t)N0 * ZS * 4 * 2;
+    static constexpr uint32_t kSBytes = (uint32_t)R1 * B2 * M1 * 8;
+    static constexpr uint32_t kRegion = kXBytes > kZBytes + kSBytes ? kXBytes : kZBytes + kSBytes;
+    static constexpr uint32_t kT = kRegion;              // offsets from a 1024-aligned base
+    static constexpr uint32_t kTw = kT + kTBytes;
+    static constexpr uint32_t kSmem = kTw + N0 * 8 + 1024;
+    static constexpr uint32_t kTmemCols = MT * N <= 32 ? 32 : (MT * N <= 64 ? 64 : 128);
+    static_assert(R1 * M1 % NT == 0 || R1 * M1 < NT, "column units");
+    static_assert(NK % NT == 0, "kept modes per thread");
+};
+
+template <typename T>
+__global__ void __launch_bounds__(NT, Shape<T>::kMinBlocks)
+k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *tables) {
+    using Gm = Geo<T>;
+    using namespace tcu;
+    extern __shared__ __align__(1024) char smem_raw[];
+    char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+    __shared__ __align__(8) uint64_t bar_x, bar_t, bar_mma;
+    __shared__ uint32_t s_tmem;
+    const unsigned long long t0 = a.trace ? trace_now() : 0;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int img = blockIdx.x;
+    float2 *tw = reinterpret_cast<float2 *>(base + Gm::kTw);
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_x)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_t)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_mma)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        // the twiddle operand (already in its swizzled image) in one bulk copy
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     ::"r"(tc_smem_addr(&bar_t)), "r"(Gm::kTBytes) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(tc_smem_addr(base + Gm::kT)), "l"(tables), "r"(Gm::kTBytes),
+                     "r"(tc_smem_addr(&bar_t)) : "memory");
+        // the image: MT x KC boxes of 128 rows x 128 bytes
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     ::"r"(tc_smem_addr(&bar_x)), "r"(Gm::kXBytes) : "memory");
+        for (int t = 0; t < Gm::MT; ++t)
+            for (int kc = 0; kc < Gm::KC; ++kc)
+                tc::tma_load_2d(tc_smem_addr(base + (t * Gm::KC + kc) * Gm::kTile), &xmap,
+                                kc * Gm::kE, img * Gm::N0 + 128 * t, &bar_x);
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(tc_smem_addr(&s_tmem)), "r"(Gm::kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    for (int e = tid; e < Gm::N0; e += NT) tw[e] = a.tw0[e];
+    tc_before_sync();
+    __syncthreads();
+    tc_after_sync();
+    pdl_trigger();
+    const uint32_t tmem = s_tmem;
+    bool ok = mbar_wait(&bar_t, 0, a.err);
+    ok &= mbar_wait(&bar_x, 0, a.err);
+    const uint32_t xs = tc_smem_addr(base), ts = tc_smem_addr(base + Gm::kT);
+    if (tid == 0) {
+        tc_after_sync();
+        for (int t = 0; t < Gm::MT; ++t) {
+            const uint32_t d = tmem + t * Gm::N;
+            for (int kc = 0; kc < Gm::KC; ++kc) {
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint32_t ao = xs + (t * Gm::KC + kc) * Gm::kTile + s * 32;
+                    const uint32_t bo = ts + kc * Gm::kTChunk + s * 32;
+                    const uint32_t acc = (kc | s) ? 1u : 0u;
+                    if constexpr (Shape<T>::kSplit) {
+                        constexpr uint32_t id = idesc_tf32(Gm::N);
+                        mma_tf32(d, desc_sw128(ao), desc_sw128(bo), id, acc);
+                        mma_tf32(d, desc_sw128(ao), desc_sw128(bo + Gm::KC * Gm::kTChunk), id, 1u);
+                    } else {
+                        constexpr uint32_t id =
+                            idesc_f16(Gm::N, std::is_same<T, __nv_bfloat16>::value);
+                        mma_f16(d, desc_sw128(ao), desc_sw128(bo), id, acc);
+                    }
+                }
+            }
+        }
+        mma_commit(&bar_mma);
+    }
+    ok &= mbar_wait(&bar_mma, 0, a.err);
+    if constexpr (Shape<T>::kSplit) {
+        // x's lo parts over the tile (elementwise: the swizzled layout carries over),
+        // then the pass x_lo t_hi
+        float4 *xv = reinterpret_cast<float4 *>(base);
+        for (int e = tid; e < (int)(Gm::kXBytes / 16); e += NT) {
+            const float4 v = xv[e];
+            xv[e] = make_float4(tf32_lo(v.x), tf32_lo(v.y), tf32_lo(v.z), tf32_lo(v.w));
+        }
+        fence_async_smem();
+        tc_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc_after_sync();
+            constexpr uint32_t id = idesc_tf32(Gm::N);
+            for (int t = 0; t < Gm::MT; ++t)
+                for (int kc = 0; kc < Gm::KC; ++kc)
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        mma_tf32(tmem + t * Gm::N,
+                                 desc_sw128(xs + (t * Gm::KC + kc) * Gm::kTile + s * 32),
+                                 desc_sw128(ts + kc * Gm::kTChunk + s * 32), id, 1u);
+            mma_commit(&bar_mma);
+        }
+        ok &= mbar_wait(&bar_mma, 1, a.err);
+    }
+    tc_after_sync();
+    // Z planes (re, im) from tensor memory into the region the tile occupied:
+    // warps w and w + 4 read the same lanes, the first the re, the second the im half
+    float *zr = reinterpret_cast<float *>(base);
+    float *zi = zr + Gm::N0 * Gm::ZS;
+    float2 *S = reinterpret_cast<float2 *>(base + Gm::kZBytes);
+    {
+        const int half = warp >> 2;
+        float *dz = half ? zi : zr;
+        for (int t = 0; t < Gm::MT; ++t) {
+            const int row = 128 * t + 32 * (warp & 3) + (tid & 31);
+#pragma unroll
+            for (int g = 0; g < Gm::M1 / 16; ++g) {
+                float v[16];
+                tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + t * Gm::N + half * Gm::M1 +
+                              16 * g, v);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) dz[row * Gm::ZS + 16 * g + q] = ok ? v[q] : 0.f;
+            }
+        }
+    }
+    tc_before_sync();
+    __syncthreads();
+    // column DFT: S[r1][q][k] = B2-point DFT over r2 of Z[r1 + R1 r2][k]
+    for (int u = tid; u < Gm::R1 * Gm::M1; u += NT) {
+        const int r1 = u / Gm::M1, k = u % Gm::M1;
+        float2 z[Gm::B2];
+#pragma unroll
+        for (int r2 = 0; r2 < Gm::B2; ++r2) {
+            const int r = r1 + Gm::R1 * r2;
+            z[r2] = make_float2(zr[r * Gm::ZS + k], zi[r * Gm::ZS + k]);
+        }
+        fft::fft_dif<Gm::B2, -1>(z);
+#pragma unroll
+        for (int q = 0; q < Gm::B2; ++q)
+            S[(r1 * Gm::B2 + q) * Gm::M1 + k] = z[fft::bitrev(q, fft::ilog2(Gm::B2))];
+    }
+    __syncthreads();
+    // kept modes: X[j][k] = sum_r1 W_N0^{f r1} S[r1][f mod B2][k]
+    float2 *dst = a.part + (size_t)img * Gm::NK;
+    for (int o = tid; o < Gm::NK; o += NT) {
+        const int j = o / Gm::M1, k = o % Gm::M1;
+        const int f = j < Gm::M0 ? j : Gm::N0 - Gm::K0 + j;
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int r1 = 0; r1 < Gm::R1; ++r1)
+            cmac(acc, S[(r1 * Gm::B2 + (f % Gm::B2)) * Gm::M1 + k], tw[(f * r1) & (Gm::N0 - 1)]);
+        __stcg(dst + o, acc);
+    }
+    tc_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc_after_sync();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(Gm::kTmemCols));
+    }
+    cta_record(a, 0, 0, t0, t0);
+}
+
+// Host: the twiddle operand in its swizzled shared-memory image (hi then lo for
+// fp32, one 16-bit copy otherwise), computed in double.
+template <typename T>
+void make_table(std::vector<unsigned char> &img) {
+    using Gm = Geo<T>;
+    using tcu::sw_off;
+    using tcu::sw_off16;
+    using tcu::tf32_lo;
+    img.assign(Gm::kTBytes, 0);
+    const double two_pi = 2.0 * M_PI;
+    for (int j = 0; j < Gm::N; ++j)
+        for (int n = 0; n < Gm::N1; ++n) {
+            const int k = j % Gm::M1;
+            const double ang = two_pi * (double)k * (double)n / (double)Gm::N1;
+            const double v = j < Gm::M1 ? std::cos(ang) : -std::sin(ang);
+            const uint32_t chunk = (uint32_t)(n / Gm::kE) * Gm::kTChunk;
+            if constexpr (Shape<T>::kSplit) {
+                const float hi = (float)v;
+                const float lo = (float)(v - (double)(hi - tf32_lo(hi)));
+                const uint32_t off = chunk + sw_off(j, n % Gm::kE);
+                memcpy(&img[off], &hi, 4);
+                memcpy(&img[Gm::KC * Gm::kTChunk + off], &lo, 4);
+            } else {
+                const uint32_t off = chunk + sw_off16(j, n % Gm::kE);
+                const T h = std::is_same<T, __half>::value ? T(__float2half_rn((float)v))
+                                                           : T(__float2bfloat16_rn((float)v));
+                memcpy(&img[off], &h, 2);
+            }
+        }
+}
+
+}  // namespace tca
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 // 128 x 128 grid, 16 x 16 modes per block: chunks of 32 strided rows,
@@ -752,27 +997,8 @@ void *kernel_ptr() {
 }
 
 // ----- tensor-core variant: host side -----
-typedef CUresult (*EncodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled encoder() {
-    static EncodeTiled fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiled>(ptr);
-        else
-            cudaGetLastError();
-    }
-    return fn;
-}
+using tcu::encoder;
+using tcu::EncodeTiled;
 
 // (rows x 128) float32 matrix, 32-column x 128-row boxes, 128-byte swizzle
 bool encode_rows(CUtensorMap *map, const void *ptr, int64_t rows) {
@@ -844,6 +1070,15 @@ bool is_cfg256(const Geom &g) {
 
 // Three-kernel variant, per shape: whether phase A reduces its partials in a
 // cluster, and the kernels' shared memory.
+// Whether kernel A runs on the tensor cores for this shape and storage type:
+// fp32 128 x 128 (16 x 16 modes) and 16-bit 256 x 256 (32 x 32 modes).
+template <class Cf>
+bool tca_shape(fno_dtype_t dt) {
+    if (dt == FNO_F32)
+        return Cf::N0 == 128 && Cf::N1 == 128 && Cf::M0 == 16 && Cf::M1 == 16;
+    return Cf::N0 == 256 && Cf::N1 == 256 && Cf::M0 == 32 && Cf::M1 == 32;
+}
+
 template <class Cf, class CfC = Cf>
 struct Pdl {
     static constexpr bool kCluster = Cf::N0 >= 256;
@@ -852,40 +1087,71 @@ struct Pdl {
     // splitting each over 8 warps shortens the path after kernel A (measured:
     // 23.4 -> 22.3 us on the 8 x 32-channel workload); 4 warps elsewhere
     static constexpr int kBThreads = Cf::N0 == 128 ? 256 : 128;
-    static int batch_block(int64_t batch, int cin) {
+    // (no CUDA call: sizes are reported before any device work; a plan whose
+    // driver lacks the tensor-map encoder fails at creation)
+    static bool use_tca(fno_dtype_t dt, uint32_t flags) {
+        return tca_shape<Cf>(dt) && !(flags & FNO_PLAN_SIMT_TRANSFORM);
+    }
+    // partial copies of the kept modes kernel A leaves (one from the tensor-core kernel)
+    static int parts(fno_dtype_t dt, uint32_t flags) { return use_tca(dt, flags) ? 1 : kParts; }
+    static int batch_block(int64_t batch, int cin, int np) {
         int bb = (int)batch;
-        while (bb > 1 && (size_t)kParts * bb * cin * 16 > kXpBudget) bb = (bb + 1) / 2;
+        while (bb > 1 && (size_t)np * bb * cin * 16 > kXpBudget) bb = (bb + 1) / 2;
         return bb;
     }
-    static size_t smem_b(fno_dtype_t dt, int cin, int ob, int bb) {
+    static size_t smem_b(fno_dtype_t dt, int cin, int ob, int bb, int np) {
         const size_t w2 = dt == FNO_F32 ? 16 : 8;
-        return ((size_t)cin * ob * w2 + 15) / 16 * 16 + (size_t)kParts * bb * cin * 16;
+        return ((size_t)cin * ob * w2 + 15) / 16 * 16 + (size_t)np * bb * cin * 16;
     }
-    static size_t part_bytes(const Geom &g, int64_t batch, int cin) {
-        return (size_t)kParts * batch * cin * g.nkept * sizeof(float2);
+    static size_t part_bytes(const Geom &g, int64_t batch, int cin, fno_dtype_t dt,
+                             uint32_t flags) {
+        return (size_t)parts(dt, flags) * batch * cin * g.nkept * sizeof(float2);
+    }
+    template <typename T, int NP>
+    static void *kernel_b() {
+        return reinterpret_cast<void *>(&k_phase_b<Cf, T, NP, kBThreads>);
     }
     template <typename T>
     static cudaError_t init(Plan &p) {
         const size_t w2 = p.dtype == FNO_F32 ? 16 : 8;
+        p.fused_tca = use_tca(p.dtype, p.flags);
+        const int np = parts(p.dtype, p.flags);
         int ob = p.cout;
         while (ob > 1 && (size_t)p.cin * ob * w2 > kWsBudget) ob = (ob + 1) / 2;
-        const int bb = batch_block(p.batch, p.cin);
+        const int bb = batch_block(p.batch, p.cin, np);
         const size_t sa = Cf::kSmemTw + Cf::kSmemA, sc = CfC::kSmemTw + CfC::kSmemC;
-        const size_t sb = smem_b(p.dtype, p.cin, ob + 1, bb);   // padded slab rows
+        const size_t sb = smem_b(p.dtype, p.cin, ob + 1, bb, np);   // padded slab rows
         cudaError_t e = cudaFuncSetAttribute(k_phase_a<Cf, T, kCluster>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_phase_b<Cf, T, kParts, kBThreads>,
+            e = cudaFuncSetAttribute(np == 1 ? kernel_b<T, 1>() : kernel_b<T, kParts>(),
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sb);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k_phase_c<CfC, T>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
+        if constexpr (!std::is_same<T, float>::value || Cf::N0 == 128) {
+            if (e == cudaSuccess && p.fused_tca && !tcu::encoder()) e = cudaErrorNotSupported;
+            if (e == cudaSuccess && p.fused_tca) {
+                using Gm = tca::Geo<T>;
+                e = cudaFuncSetAttribute(tca::k_phase_a_tc<T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Gm::kSmem);
+                std::vector<unsigned char> img;
+                if (e == cudaSuccess) {
+                    tca::make_table<T>(img);
+                    e = cudaMalloc(&p.fused_tables, img.size());
+                }
+                if (e == cudaSuccess)
+                    e = cudaMemcpy(p.fused_tables, img.data(), img.size(),
+                                   cudaMemcpyHostToDevice);
+            }
+        }
         p.fused_bb = bb;
         p.fused_ob = ob;
         p.fused_smem = sb;             // kernel B's; A and C use their fixed sizes
         p.fused_grid = 0;
         // tensor-core mixing where the kept modes arrive reduced (one copy)
-        p.fused_mixtc = kParts == 1 && !(p.flags & FNO_PLAN_SIMT_MIX) &&
+        p.fused_mixtc = np == 1 && !(p.flags & FNO_PLAN_SIMT_MIX) &&
                         mixtc_supported(p.g.d, p.dtype, p.batch, p.cin, p.cout, Cf::M1,
                                         p.g.nkept);
         if (e == cudaSuccess && p.fused_mixtc) e = mixtc_init(p.dtype);
@@ -893,12 +1159,14 @@ struct Pdl {
             const size_t nB = p.fused_mixtc ? (size_t)mixtc_items(p.g.nkept)
                                             : (size_t)(p.g.nkept / kG) * ((p.cout + ob - 1) / ob) *
                                                   ((p.batch + bb - 1) / bb);
-            p.trace_records = (size_t)p.batch * (p.cin * Cf::C + p.cout * CfC::C) + nB;
+            const size_t nA = (size_t)p.batch * p.cin * (p.fused_tca ? 1 : Cf::C);
+            p.trace_records = nA + (size_t)p.batch * p.cout * CfC::C + nB;
             e = cudaMalloc(&p.trace, p.trace_records * sizeof(fno_trace_record_t));
         }
         return e;
     }
-    // kernel A alone over nimg images (an ordinary launch)
+    // kernel A alone over nimg images (an ordinary launch; the register-FFT
+    // kernel, whose partial-copy count the backward pass's workspace assumes)
     template <typename T>
     static cudaError_t forward_a(const Args &a, int64_t nimg, cudaStream_t s) {
         cudaLaunchAttribute cl;
@@ -923,25 +1191,41 @@ struct Pdl {
         a.ob = p.fused_ob;
         a.nob = (p.cout + a.ob - 1) / a.ob;
         a.npairs = (int)(p.g.nkept / kG);
-        const int nA = (int)p.batch * p.cin * Cf::C;
+        const int nA = (int)p.batch * p.cin * (p.fused_tca ? 1 : Cf::C);
         const int nB = p.fused_mixtc ? mixtc_items(p.g.nkept) : a.npairs * a.nob * a.ng;
         const int nC = (int)p.batch * p.cout * CfC::C;
         a.trace = p.trace;
         a.trace_b = nA;
         a.trace_c = nA + nB;
-        cudaLaunchAttribute cl;
-        cl.id = cudaLaunchAttributeClusterDimension;
-        cl.val.clusterDim.x = Cf::C;
-        cl.val.clusterDim.y = 1;
-        cl.val.clusterDim.z = 1;
-        cudaLaunchConfig_t ca = {};
-        ca.gridDim = dim3(nA);
-        ca.blockDim = dim3(kNT);
-        ca.dynamicSmemBytes = Cf::kSmemTw + Cf::kSmemA;
-        ca.stream = s;
-        ca.attrs = kCluster ? &cl : nullptr;
-        ca.numAttrs = kCluster ? 1 : 0;
-        cudaError_t e = cudaLaunchKernelEx(&ca, k_phase_a<Cf, T, kCluster>, a);
+        cudaError_t e = cudaSuccess;
+        bool done_a = false;
+        if constexpr (!std::is_same<T, float>::value || Cf::N0 == 128) {
+            if (p.fused_tca) {
+                using Gm = tca::Geo<T>;
+                CUtensorMap xmap;
+                if (!tcu::encode_rows_tiled(&xmap, a.x, (int64_t)p.batch * p.cin * Gm::N0,
+                                            Gm::N1, sizeof(T), Gm::kE, tcu::tma_type<T>()))
+                    return cudaErrorInvalidValue;
+                tca::k_phase_a_tc<T><<<nA, tca::NT, Gm::kSmem, s>>>(xmap, a, p.fused_tables);
+                e = cudaGetLastError();
+                done_a = true;
+            }
+        }
+        if (!done_a) {
+            cudaLaunchAttribute cl;
+            cl.id = cudaLaunchAttributeClusterDimension;
+            cl.val.clusterDim.x = Cf::C;
+            cl.val.clusterDim.y = 1;
+            cl.val.clusterDim.z = 1;
+            cudaLaunchConfig_t ca = {};
+            ca.gridDim = dim3(nA);
+            ca.blockDim = dim3(kNT);
+            ca.dynamicSmemBytes = Cf::kSmemTw + Cf::kSmemA;
+            ca.stream = s;
+            ca.attrs = kCluster ? &cl : nullptr;
+            ca.numAttrs = kCluster ? 1 : 0;
+            e = cudaLaunchKernelEx(&ca, k_phase_a<Cf, T, kCluster>, a);
+        }
         if (e != cudaSuccess) return e;
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -971,7 +1255,10 @@ struct Pdl {
             cfg.gridDim = dim3(nB);
             cfg.blockDim = dim3(kBThreads);
             cfg.dynamicSmemBytes = p.fused_smem;
-            e = cudaLaunchKernelEx(&cfg, k_phase_b<Cf, T, kParts, kBThreads>, a);
+            if (p.fused_tca)
+                e = cudaLaunchKernelEx(&cfg, k_phase_b<Cf, T, 1, kBThreads>, a);
+            else
+                e = cudaLaunchKernelEx(&cfg, k_phase_b<Cf, T, kParts, kBThreads>, a);
         }
         if (e != cudaSuccess) return e;
         cfg.gridDim = dim3(nC);
@@ -1025,8 +1312,8 @@ size_t fused_workspace_bytes(const Geom &g, fno_dtype_t dtype, int64_t batch, in
     if (v == kVarOne1d) return 0;
     if (v == kVarTc128) return layout_tc(g, batch, cin, cout).total;
     if (v == kVarPersistent128) return layout(g, batch, cin, cout).total;
-    const size_t part = v == kVarPdl256 ? Pdl<Cfg256>::part_bytes(g, batch, cin)
-                                        : Pdl128::part_bytes(g, batch, cin);
+    const size_t part = v == kVarPdl256 ? Pdl<Cfg256>::part_bytes(g, batch, cin, dtype, flags)
+                                        : Pdl128::part_bytes(g, batch, cin, dtype, flags);
     const size_t y = (size_t)batch * cout * g.nkept * sizeof(float2);
     return ((part + 255) & ~size_t(255)) + ((y + 255) & ~size_t(255));
 }
@@ -1179,8 +1466,9 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
         return cudaGetLastError();
     }
     if (v == kVarPdl128 || v == kVarPdl256) {
-        const size_t part = v == kVarPdl256 ? Pdl<Cfg256>::part_bytes(p.g, p.batch, p.cin)
-                                            : Pdl128::part_bytes(p.g, p.batch, p.cin);
+        const size_t part = v == kVarPdl256
+                                ? Pdl<Cfg256>::part_bytes(p.g, p.batch, p.cin, p.dtype, p.flags)
+                                : Pdl128::part_bytes(p.g, p.batch, p.cin, p.dtype, p.flags);
         Args a{};
         a.x = b.x;
         a.w = b.w;

@@ -55,6 +55,7 @@ struct Plan {
     int fused_bb;
     void *fused_tables;           // tensor-core path: twiddle operands (plan-owned)
     bool fused_mixtc;             // three-kernel path mixes on the tensor cores
+    bool fused_tca;               // three-kernel path transforms (kernel A) on the tensor cores
     fno_trace_record_t *trace;    // FNO_PLAN_TRACE: one record per work item (plan-owned)
     size_t trace_records;         // records one forward call produces
     // FNO_PLAN_BACKWARD: the adjoint layer's plan and the backward workspace map

@@ -4,6 +4,8 @@
 // MMA issue / commit, tensor-memory loads and a bounded mbarrier wait.
 #pragma once
 
+#include <cuda.h>
+
 #include <cstring>
 
 #include "fno_internal.cuh"
@@ -113,6 +115,53 @@ __device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint
     asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
                  ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+// ----- host: TMA tensor maps -----
+typedef CUresult (*EncodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's cuTensorMapEncodeTiled through the runtime's entry-point query
+// (no link against the driver library); nullptr if unavailable.
+inline EncodeTiled encoder() {
+    static EncodeTiled fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(ptr);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+template <typename T> inline CUtensorMapDataType tma_type();
+template <> inline CUtensorMapDataType tma_type<float>() { return CU_TENSOR_MAP_DATA_TYPE_FLOAT32; }
+template <> inline CUtensorMapDataType tma_type<__half>() { return CU_TENSOR_MAP_DATA_TYPE_FLOAT16; }
+template <> inline CUtensorMapDataType tma_type<__nv_bfloat16>() {
+    return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
+
+// A (rows x cols) row-major matrix read in boxes of box_cols (128 bytes) x 128
+// rows with the 128-byte swizzle.
+inline bool encode_rows_tiled(CUtensorMap *map, const void *ptr, int64_t rows, int cols,
+                              size_t elem, int box_cols, CUtensorMapDataType type) {
+    EncodeTiled fn = encoder();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * elem};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, type, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace tcu

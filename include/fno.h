@@ -99,6 +99,11 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * (2-D fp16 / bf16 layers with at most 64 channels and 64 samples; the
  * tensor-core kernel is the default there).  An ablation switch.            */
 #define FNO_PLAN_SIMT_MIX 32u
+/* Run the forward transform of the three-kernel 2-D path with the register-
+ * FFT kernel where the tensor-core kernel would run (fp32 128x128 with 16x16
+ * modes and 16-bit 256x256 with 32x32 modes, where the row DFT is a tcgen05
+ * GEMM; the tensor-core kernel is the default there).  An ablation switch.  */
+#define FNO_PLAN_SIMT_TRANSFORM 64u
 
 /* One work item of the fused kernel, as recorded under FNO_PLAN_TRACE.
  * Times are the GPU's global nanosecond timer.                              */

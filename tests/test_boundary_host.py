@@ -152,5 +152,5 @@ def test_backward_flag_adds_workspace(L):
     assert st == capi.FNO_OK and wb1 == wb
     # the adjoint weights, the kept modes of x (8*32*512) and dy (8*16*512)
     assert ws1 >= wb + 8 * 32 * 512 * 8 + 8 * 16 * 512 * 8
-    st, _, _ = Q(1, [16], [4], 1, 1, 1, F32, flags=capi.FNO_PLAN_BACKWARD | 0x40)
+    st, _, _ = Q(1, [16], [4], 1, 1, 1, F32, flags=capi.FNO_PLAN_BACKWARD | 0x100)
     assert st == capi.FNO_ERR_INVALID_ARG

@@ -67,8 +67,10 @@ def _lib(fno, oracle_mod):
 
 
 @pytest.mark.parametrize("flags", [0, FNO_PLAN_UNFUSED, capi.FNO_PLAN_TENSOR_CORES,
-                                   capi.FNO_PLAN_PERSISTENT, capi.FNO_PLAN_SIMT_MIX],
-                         ids=["default", "unfused", "tensor_cores", "persistent", "simt_mix"])
+                                   capi.FNO_PLAN_PERSISTENT, capi.FNO_PLAN_SIMT_MIX,
+                                   capi.FNO_PLAN_SIMT_TRANSFORM],
+                         ids=["default", "unfused", "tensor_cores", "persistent", "simt_mix",
+                              "simt_transform"])
 @pytest.mark.parametrize("spec", SMALL, ids=[case_id(c) for c in SMALL])
 def test_small_cases_match_oracle(spec, flags):
     n, modes, b, ci, co, dt = spec
@@ -186,8 +188,8 @@ def test_fused_3d_and_unfused_agree():
     assert_close(a, c.astype(np.float64), "f32", "3-D fused vs unfused")
 
 
-@pytest.mark.parametrize("name,chunks", [("2d_f32", 4), ("3d_f32", 8)])
-def test_trace_three_kernel_variant(name, chunks):
+@pytest.mark.parametrize("name,chunks_a,chunks_c", [("2d_f32", 1, 4), ("3d_f32", 8, 8)])
+def test_trace_three_kernel_variant(name, chunks_a, chunks_c):
     # one record per CTA of each kernel; kernel B's CTAs start before A's last
     # one ends at the earliest (programmatic dependent launch), never wait past it
     case = workloads.CASES[name]
@@ -199,8 +201,8 @@ def test_trace_three_kernel_variant(name, chunks):
     st, recs = capi.fno_plan_get_trace(conv.handle)
     assert st == capi.FNO_OK
     phases = [r[0] for r in recs]
-    assert phases.count(0) == case.batch * case.cin * chunks
-    assert phases.count(2) == case.batch * case.cout * chunks
+    assert phases.count(0) == case.batch * case.cin * chunks_a
+    assert phases.count(2) == case.batch * case.cout * chunks_c
     assert phases.count(1) > 0 and len(recs) == len(phases)
     for r in recs:
         assert 0 < r[4] <= r[5] <= r[7], r
