@@ -248,453 +248,6 @@ __global__ void __launch_bounds__(kNT) k_phase_c(Args a) {
     cta_record(a, 2, a.trace_c, t0, t1);
 }
 
-// ---------------------------------------------------------------------------
-// Tensor-core variant for float32 storage (128 x 128, 16 x 16 modes)
-//
-// Phase A: TMA brings a whole input image (128 rows x 128 columns) into shared
-// memory with the 128-byte swizzle (the next image is prefetched into the
-// other buffer while this one is computed).  The row DFT Z = X T^T (T: cos /
-// -sin of bins 0..15, 32 x 128) runs on the tensor cores as tcgen05.mma
-// kind::tf32 with three passes (x_hi t_hi + x_hi t_lo + x_lo t_hi), where a
-// value's hi part is the value itself read at tf32 precision and its lo part
-// the exact remainder, so the product is accurate to about 2^-20 (the layer's
-// float32 bar is 1e-5).  The accumulator lives in tensor memory.  The column
-// DFT over the 128 rows is split 8 x 16 (16-point register FFTs + twiddled
-// sums) on the SIMT cores, and the 512 kept modes go to the workspace.
-// Phase C: the column inverse (16-point register FFTs) builds the operand
-// Zo = [Re | Im] (128 x 32, carrying the half-spectrum weights c(k) and the
-// 1/(N0 N1) scale) and the row inverse y = Zo Tinv^T is one more tcgen05
-// chain with N = 128; tensor memory is staged through swizzled shared memory
-// and written by TMA.  Phase B is the SIMT mixing shared with the other kernel.
-// ---------------------------------------------------------------------------
-namespace tc {
-
-constexpr int kStreams = 2;                // independent item streams per CTA
-constexpr int NT = 256;                    // threads per stream
-struct Cf {
-    static constexpr int N0 = 128, M0 = 16, M1 = 16, K0 = 32, NK = K0 * M1;
-    static constexpr int C = 1;            // one item covers a whole image
-    static constexpr size_t MBLK = (size_t)M0 * M1;
-    __device__ static void wmap(int o, int &blk, int &local) {
-        const int j = o / M1, k = o % M1;
-        blk = j >= M0 ? 1 : 0;
-        local = (j - blk * M0) * M1 + k;
-    }
-};
-constexpr int kKChunks = 4;                // 32-column K chunks of the row DFT
-constexpr uint32_t kChunkBytes = 16384;    // 128 rows x 128 bytes
-constexpr uint32_t kImageBytes = kKChunks * kChunkBytes;
-// shared-memory map (offsets from a 1024-aligned base)
-constexpr uint32_t kStreamBytes = 81920;   // per stream: x tile 64 KiB + lo slot 16 KiB
-constexpr uint32_t kT = kStreams * kStreamBytes;   // 32 KiB: forward operand, hi then lo
-constexpr uint32_t kTi = kT + 32768;       // 32 KiB: inverse operand, hi then lo
-constexpr uint32_t kTw = kTi + 32768;      // 1 KiB: W_128^e
-constexpr uint32_t kSmemBytes = kTw + 1024 + 1024;   // + alignment slack
-constexpr uint32_t kTableBytes = 65536;    // forward + inverse operands (global image)
-constexpr int kTmemCols = 512;             // stream s: [256 s, 256 s + 32) forward D,
-constexpr int kTmemInv = 32;               //           [256 s + 32, 256 s + 160) inverse D
-// inside a stream's region during a C item
-constexpr uint32_t kCY = 0, kCAhi = 8192, kCAlo = 24576, kCStage = 40960;
-// inside the x tile after its MMAs (A item)
-constexpr int kZS = 17;                    // row stride of the Z planes (floats)
-constexpr uint32_t kZr = 0, kZi = 128 * kZS * 4, kS = 2 * 128 * kZS * 4;
-
-using namespace tcu;
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                            uint64_t *bar) {
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                 " [%0], [%1, {%2, %3}], [%4];"
-                 ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int c0, int c1, uint32_t src) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
-                 ::"l"(map), "r"(c0), "r"(c1), "r"(src) : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// one stream's barriers and completed-phase counters (counters identical in
-// every thread of the stream)
-struct Barriers {
-    uint64_t x;         // TMA of the x tile
-    uint64_t mma;       // row-DFT MMAs of one K chunk (they read the lo slot)
-    uint64_t inv;       // inverse MMAs
-};
-struct Phases {
-    uint32_t x, mma, inv;
-};
-struct Stream {
-    StreamGroup grp;
-    char *region;       // the stream's 80 KiB
-    uint32_t tmem;      // the stream's first tensor-memory column
-    Barriers *bars;
-};
-
-// Phase A: the x tile of image `img` -> its 512 kept modes.
-__device__ void phase_a(const Stream &st, Phases &ph, const char *base, const CUtensorMap *xmap,
-                        float2 *part, int img, int *err, const Args &a, TraceStamp &ts) {
-    const int tid = st.grp.tid;
-    char *xh = st.region;
-    const float2 *tw = reinterpret_cast<const float2 *>(base + kTw);
-    if (tid == 0) {
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                     ::"r"(smem_addr(&st.bars->x)), "r"(kImageBytes) : "memory");
-        const uint32_t dst = smem_addr(xh);
-        for (int kc = 0; kc < kKChunks; ++kc)
-            tma_load_2d(dst + kc * kChunkBytes, xmap, 32 * kc, img * Cf::N0, &st.bars->x);
-    }
-    bool ok = mbar_wait(&st.bars->x, ph.x++, err);
-    if (tid == 0) ts.ready(a);
-    constexpr uint32_t idesc = idesc_tf32(32);
-    const uint32_t ax = smem_addr(xh);
-    // 1. the two passes that read x at tf32 precision, for the whole image
-    if (tid == 0) {
-        tc_after_sync();
-#pragma unroll
-        for (int kc = 0; kc < kKChunks; ++kc) {
-            const uint32_t bh = smem_addr(base + kT + kc * 4096);
-            const uint32_t bl = smem_addr(base + kT + 16384 + kc * 4096);
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint32_t ao = ax + kc * kChunkBytes + s * 32, bo = s * 32;
-                mma_tf32(st.tmem, desc_sw128(ao), desc_sw128(bh + bo), idesc, (kc | s) ? 1u : 0u);
-                mma_tf32(st.tmem, desc_sw128(ao), desc_sw128(bl + bo), idesc, 1u);
-            }
-        }
-        mma_commit(&st.bars->mma);
-    }
-    ok &= mbar_wait(&st.bars->mma, ph.mma++, err);
-    // 2. x's lo parts, in place (elementwise: the swizzled layout carries over)
-    {
-        float4 *xv = reinterpret_cast<float4 *>(xh);
-#pragma unroll
-        for (int r = 0; r < (int)(kImageBytes / 16) / NT; ++r) {
-            const float4 v = xv[tid + r * NT];
-            xv[tid + r * NT] = make_float4(tf32_lo(v.x), tf32_lo(v.y), tf32_lo(v.z), tf32_lo(v.w));
-        }
-    }
-    fence_async_smem();
-    st.grp.sync();
-    // 3. the pass with x's lo parts
-    if (tid == 0) {
-        tc_after_sync();
-#pragma unroll
-        for (int kc = 0; kc < kKChunks; ++kc) {
-            const uint32_t bh = smem_addr(base + kT + kc * 4096);
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_tf32(st.tmem, desc_sw128(ax + kc * kChunkBytes + s * 32), desc_sw128(bh + s * 32),
-                         idesc, 1u);
-        }
-        mma_commit(&st.bars->mma);
-    }
-    ok &= mbar_wait(&st.bars->mma, ph.mma++, err);
-    if (tid == 0) ts.computed(a);
-    tc_after_sync();
-    // Z (128 rows x 16 bins) from tensor memory into the now free x tile
-    float *zr = reinterpret_cast<float *>(xh + kZr);
-    float *zi = reinterpret_cast<float *>(xh + kZi);
-    float2 *S = reinterpret_cast<float2 *>(xh + kS);
-    {
-        const int warp = tid >> 5, lane = tid & 31;
-        const int row = 32 * (warp & 3) + lane, half = warp >> 2;
-        float v[16];
-        tmem_ld16(st.tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * half, v);
-        float *dz = (half ? zi : zr) + row * kZS;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) dz[k] = ok ? v[k] : 0.f;
-    }
-    tc_before_sync();
-    st.grp.sync();
-    // column DFT over the 128 rows, r = r1 + 16 r2: one 8-point FFT over r2
-    // per (r1, bin) and thread
-    {
-        const int r1 = tid >> 4, k = tid & 15;
-        float2 z[8];
-#pragma unroll
-        for (int r2 = 0; r2 < 8; ++r2) {
-            const int r = r1 + 16 * r2;
-            z[r2] = make_float2(zr[r * kZS + k], zi[r * kZS + k]);
-        }
-        fft::fft_dif<8, -1>(z);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) S[(r1 * 8 + q) * 16 + k] = z[fft::bitrev(q, 3)];
-    }
-    st.grp.sync();
-    // X[j][k] = sum_r1 W_128^{f r1} S[r1][f mod 8][k]
-    float2 *dst = part + (size_t)img * Cf::NK;
-#pragma unroll
-    for (int rep = 0; rep < Cf::NK / NT; ++rep) {
-        const int o = tid + rep * NT;
-        const int j = o >> 4, k = o & 15;
-        const int f = kept_freq<Cf>(j);
-        float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int r1 = 0; r1 < 16; ++r1) cmac(acc, S[(r1 * 8 + (f & 7)) * 16 + k], tw[(f * r1) & 127]);
-        __stcg(dst + o, acc);
-    }
-    fence_async_smem();      // these generic writes precede the next TMA into this tile
-}
-
-// Phase C: the mixed modes of output image `img` -> its 128 rows.
-__device__ void phase_c(const Stream &st, Phases &ph, const char *base, const float2 *Y,
-                        const CUtensorMap *ymap, int img, int *err, const Args &a, TraceStamp &ts) {
-    const int tid = st.grp.tid;
-    float2 *ys = reinterpret_cast<float2 *>(st.region + kCY);
-    char *ahi = st.region + kCAhi, *alo = st.region + kCAlo, *stage = st.region + kCStage;
-    const float2 *tw = reinterpret_cast<const float2 *>(base + kTw);
-    const float2 *src = Y + (size_t)img * Cf::NK;
-    for (int e = tid; e < Cf::NK / 2; e += NT) cp_async16(ys + 2 * e, src + 2 * e);
-    cp_async_commit();
-    cp_async_wait_all();
-    st.grp.sync();
-    if (tid == 0) ts.ready(a);
-    // Zo[r1 + 16 r2][k] = IFFT_8 over q of V[q], V[q] = sum of Y[j] w^{-f(j) r1} over the
-    // four kept rows j with f(j) = q mod 8 (j = q, q+8, q+16, q+24); the operand
-    // row carries the half-spectrum weight c(k) and the 1/(N0 N1) scale
-    {
-        const int r1 = tid >> 4, k = tid & 15;
-        const float ck = (k == 0 ? 1.f : 2.f) * (1.f / 16384.f);
-        float2 v[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int j = q + 8 * u, f = kept_freq<Cf>(j);
-                const float2 t = cmulc(ys[j * 16 + k], tw[(f * r1) & 127]);
-                acc.x += t.x;
-                acc.y += t.y;
-            }
-            v[q] = make_float2(acc.x * ck, acc.y * ck);
-        }
-        fft::fft_dif<8, 1>(v);
-#pragma unroll
-        for (int r2 = 0; r2 < 8; ++r2) {
-            const int row = r1 + 16 * r2;
-            const float2 z = v[fft::bitrev(r2, 3)];
-            *reinterpret_cast<float *>(ahi + sw_off(row, k)) = z.x;
-            *reinterpret_cast<float *>(ahi + sw_off(row, 16 + k)) = z.y;
-            *reinterpret_cast<float *>(alo + sw_off(row, k)) = tf32_lo(z.x);
-            *reinterpret_cast<float *>(alo + sw_off(row, 16 + k)) = tf32_lo(z.y);
-        }
-    }
-    fence_async_smem();
-    st.grp.sync();
-    constexpr uint32_t idesc = idesc_tf32(128);
-    const uint32_t dinv = st.tmem + kTmemInv;
-    if (tid == 0) {
-        tc_after_sync();
-        const uint32_t ah = smem_addr(ahi), al = smem_addr(alo);
-        const uint32_t bh = smem_addr(base + kTi), bl = smem_addr(base + kTi + 16384);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            const uint32_t o = s * 32;
-            mma_tf32(dinv, desc_sw128(ah + o), desc_sw128(bh + o), idesc, s ? 1u : 0u);
-            mma_tf32(dinv, desc_sw128(ah + o), desc_sw128(bl + o), idesc, 1u);
-            mma_tf32(dinv, desc_sw128(al + o), desc_sw128(bh + o), idesc, 1u);
-        }
-        mma_commit(&st.bars->inv);
-    }
-    const bool ok = mbar_wait(&st.bars->inv, ph.inv++, err);
-    if (tid == 0) ts.computed(a);
-    tc_after_sync();
-    // y rows: tensor memory -> swizzled staging (two 32-column boxes) -> TMA,
-    // in two halves of 64 columns
-    const int warp = tid >> 5, lane = tid & 31;
-    const int row = 32 * (warp & 3) + lane, sub = warp >> 2;
-    for (int half = 0; half < 2; ++half) {
-        if (half == 1) {
-            if (tid == 0) bulk_wait_read();      // the first half has left the staging tile
-            st.grp.sync();
-        }
-#pragma unroll
-        for (int p16 = 0; p16 < 2; ++p16) {
-            float v[16];
-            const int col0 = 64 * half + 32 * sub + 16 * p16;   // column of y
-            tmem_ld16(dinv + ((uint32_t)(32 * (warp & 3)) << 16) + col0, v);
-            char *box = stage + sub * kChunkBytes;
-#pragma unroll
-            for (int p4 = 0; p4 < 4; ++p4) {
-                const int col = 16 * p16 + 4 * p4;             // column inside the box
-                *reinterpret_cast<float4 *>(box + sw_off(row, col)) =
-                    ok ? make_float4(v[4 * p4], v[4 * p4 + 1], v[4 * p4 + 2], v[4 * p4 + 3])
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        fence_async_smem();
-        st.grp.sync();
-        if (tid == 0) {
-            const uint32_t s0 = smem_addr(stage);
-            tma_store_2d(ymap, 64 * half, img * Cf::N0, s0);
-            tma_store_2d(ymap, 64 * half + 32, img * Cf::N0, s0 + kChunkBytes);
-            bulk_commit();
-        }
-    }
-    tc_before_sync();
-}
-
-__global__ void __launch_bounds__(kStreams * NT, 1)
-k_fused2d_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
-             Args a, const float4 *tables) {
-    extern __shared__ __align__(1024) char smem_raw[];
-    char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                          ~static_cast<uintptr_t>(1023));
-    __shared__ Barriers bars[kStreams];
-    __shared__ uint32_t s_tmem;
-    __shared__ Item s_cur[kStreams], s_next[kStreams];
-    __shared__ int s_ok[kStreams];
-    __shared__ __align__(8) uint64_t bar_tab;
-    // W_128, then the twiddle operands (already in their swizzled shared-memory
-    // image) in one bulk copy
-    for (int e = threadIdx.x; e < 128; e += kStreams * NT)
-        reinterpret_cast<float2 *>(base + kTw)[e] = a.tw0[e];
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kStreams; ++i) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[i].x)));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[i].mma)));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[i].inv)));
-        }
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar_tab)));
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                     ::"r"(smem_addr(&bar_tab)), "r"(kTableBytes) : "memory");
-        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                     ::"r"(smem_addr(base + kT)), "l"(tables), "r"(kTableBytes), "r"(smem_addr(&bar_tab))
-                     : "memory");
-    }
-    if (threadIdx.x < 32) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_addr(&s_tmem)), "r"(kTmemCols));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-    }
-    fence_async_smem();
-    tc_before_sync();
-    __syncthreads();
-    tc_after_sync();
-    mbar_wait(&bar_tab, 0, a.err);
-    const int sid = threadIdx.x / NT;
-    Stream st;
-    st.grp = StreamGroup{(int)threadIdx.x % NT, 1 + sid};
-    st.region = base + sid * kStreamBytes;
-    st.tmem = s_tmem + 256 * sid;
-    st.bars = &bars[sid];
-    const int tid = st.grp.tid;
-    Phases ph{0, 0, 0};
-    const int nimg_in = a.batch * a.cin;
-    if (tid == 0) s_cur[sid] = decode_ticket<Cf>(a, atomicAdd(&a.sync->ticket[0], 1));
-    st.grp.sync();
-    Item cur = s_cur[sid];
-    while (cur.phase >= 0) {
-        if (tid == 0) {
-            bulk_wait_read();          // staged output has been read before the region is reused
-            s_next[sid] = decode_ticket<Cf>(a, atomicAdd(&a.sync->ticket[0], 1));
-        }
-        st.grp.sync();
-        const Item nxt = s_next[sid];
-        const int nbg = min(a.bg, a.batch - cur.g * a.bg);
-        TraceStamp ts;
-        if (tid == 0) ts.start(a);
-        if (cur.phase == 0) {
-            phase_a(st, ph, base, &xmap, a.part, cur.g * a.bg * a.cin + cur.idx, a.err, a, ts);
-            st.grp.sync();
-            if (tid == 0)
-                finish_item(&a.sync->done_a[cur.g][0], nbg * a.cin, a.sync->flag_a[cur.g]);
-        } else if (cur.phase == 1) {
-            BItem bi;
-            bi.pair = cur.idx / a.nob;
-            bi.o0 = (cur.idx % a.nob) * a.ob;
-            bi.nob = min(a.ob, a.cout - bi.o0);
-            bi.b0 = cur.g * a.bg;
-            bi.nbb = nbg;
-            phase_b_weights<Cf, float, NT>(st.grp, static_cast<const float *>(a.w), a.cin, a.cout,
-                                           bi, a.ob, st.region);
-            if (tid == 0)
-                s_ok[sid] = wait_flag(&a.sync->flag_a[cur.g][(2 * blockIdx.x + sid) % kFlagCopies][0],
-                                      a.err);
-            if (tid == 0) ts.ready(a);
-            st.grp.sync();
-            if (s_ok[sid])
-                phase_b<Cf, float, NT>(st.grp, a.part, a.Y, a.cin, a.cout, nimg_in, bi, a.ob,
-                                       st.region);
-            else
-                cp_async_wait_all();
-            st.grp.sync();
-            if (tid == 0) ts.computed(a);
-            if (tid == 0)
-                finish_item(&a.sync->done_b[cur.g][0], a.npairs * a.nob, a.sync->flag_b[cur.g]);
-        } else {
-            if (tid == 0)
-                s_ok[sid] = wait_flag(&a.sync->flag_b[cur.g][(2 * blockIdx.x + sid) % kFlagCopies][0],
-                                      a.err);
-            st.grp.sync();
-            if (s_ok[sid])
-                phase_c(st, ph, base, a.Y, &ymap, cur.g * a.bg * a.cout + cur.idx, a.err, a, ts);
-        }
-        if (tid == 0) ts.end(a, cur, 2 * blockIdx.x + sid);
-        cur = nxt;
-        fence_async_smem();            // generic writes precede any later TMA into the region
-        st.grp.sync();
-    }
-    if (tid == 0) bulk_wait_all();
-    tc_before_sync();
-    __syncthreads();
-    tc_after_sync();
-    if (threadIdx.x < 32)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(s_tmem), "r"(kTmemCols));
-    // the last stream to leave resets the counters and flags for the next launch
-    if (tid == 0) {
-        __threadfence();
-        const int prev = atomicAdd(&a.sync->exited[0], 1);
-        if (prev == kStreams * (int)gridDim.x - 1) {
-            a.sync->ticket[0] = 0;
-            for (int g = 0; g < a.ng; ++g) {
-                a.sync->done_a[g][0] = 0;
-                a.sync->done_b[g][0] = 0;
-                for (int i = 0; i < kFlagCopies; ++i) {
-                    a.sync->flag_a[g][i][0] = 0;
-                    a.sync->flag_b[g][i][0] = 0;
-                }
-            }
-            __threadfence();
-            a.sync->exited[0] = 0;
-        }
-    }
-}
-
-// Host: the forward and inverse twiddle operands in their swizzled shared
-// memory image, hi and lo parts, computed in double.
-void make_tables(float *img) {
-    memset(img, 0, kTableBytes);
-    auto put = [&](uint32_t region, int row, int col, double v) {
-        // region: byte offset of the operand; chunks of 32 columns, 4096 B (32 rows)
-        // for the forward operand, one 16 KiB chunk (128 rows) for the inverse one
-        const float hi = (float)v;
-        const float lo = (float)(v - (double)(hi - tf32_lo(hi)));
-        img[(region + sw_off(row, col)) / 4] = hi;
-        img[(region + 16384 + sw_off(row, col)) / 4] = lo;
-    };
-    const double two_pi = 2.0 * M_PI;
-    for (int k = 0; k < 16; ++k)
-        for (int n = 0; n < 128; ++n) {
-            const double a = two_pi * k * n / 128.0;
-            const uint32_t chunk = (uint32_t)(n / 32) * 4096;
-            put(chunk, k, n % 32, std::cos(a));
-            put(chunk, 16 + k, n % 32, -std::sin(a));
-        }
-    for (int n = 0; n < 128; ++n)
-        for (int k = 0; k < 16; ++k) {
-            const double a = two_pi * k * n / 128.0;
-            put(32768, n, k, std::cos(a));
-            put(32768, n, 16 + k, -std::sin(a));
-        }
-}
-
-}  // namespace tc
 
 // ---------------------------------------------------------------------------
 // Kernel A of the three-kernel path on the tensor cores: one CTA transforms a
@@ -781,7 +334,7 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
                      ::"r"(tc_smem_addr(&bar_x)), "r"(Gm::kXBytes) : "memory");
         for (int t = 0; t < Gm::MT; ++t)
             for (int kc = 0; kc < Gm::KC; ++kc)
-                tc::tma_load_2d(tc_smem_addr(base + (t * Gm::KC + kc) * Gm::kTile), &xmap,
+                tma_load_2d(tc_smem_addr(base + (t * Gm::KC + kc) * Gm::kTile), &xmap,
                                 kc * Gm::kE, img * Gm::N0 + 128 * t, &bar_x);
     }
     if (warp == 0) {
@@ -1000,43 +553,6 @@ void *kernel_ptr() {
 using tcu::encoder;
 using tcu::EncodeTiled;
 
-// (rows x 128) float32 matrix, 32-column x 128-row boxes, 128-byte swizzle
-bool encode_rows(CUtensorMap *map, const void *ptr, int64_t rows) {
-    EncodeTiled fn = encoder();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {128 * sizeof(float)};
-    const cuuint32_t box[2] = {32, 128};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(ptr), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-constexpr size_t kTcWsBudget = 32u << 10;
-constexpr size_t kTcXpBudget = 32u << 10;
-
-BShape b_shape_tc(int64_t batch, int cin, int cout) {
-    BShape s;
-    s.ob = cout;
-    while (s.ob > 1 && (size_t)cin * s.ob * 16 > kTcWsBudget) s.ob = (s.ob + 1) / 2;
-    s.bg = (int)((batch + kTargetGroups - 1) / kTargetGroups);
-    while (s.bg > 1 && (size_t)s.bg * cin * 16 > kTcXpBudget) s.bg = (s.bg + 1) / 2;
-    while ((batch + s.bg - 1) / s.bg > kMaxGroups) ++s.bg;
-    return s;
-}
-
-Layout layout_tc(const Geom &g, int64_t batch, int cin, int cout) {
-    Layout l;
-    l.part_off = 0;
-    l.y_off = ((size_t)batch * cin * g.nkept * sizeof(float2) + 255) & ~size_t(255);
-    l.total = l.y_off + (((size_t)batch * cout * g.nkept * sizeof(float2) + 255) & ~size_t(255));
-    return l;
-}
-
-bool use_tc(const Geom &g, fno_dtype_t dtype, uint32_t flags) {
-    return is_cfg128(g) && dtype == FNO_F32 && (flags & FNO_PLAN_TENSOR_CORES);
-}
 
 }  // namespace
 
@@ -1089,8 +605,12 @@ struct Pdl {
     static constexpr int kBThreads = Cf::N0 == 128 ? 256 : 128;
     // (no CUDA call: sizes are reported before any device work; a plan whose
     // driver lacks the tensor-map encoder fails at creation)
+    // fp32 on request (FNO_PLAN_TENSOR_CORES: at 128 x 128 the register-FFT kernel
+    // is measured faster), 16-bit by default (FNO_PLAN_SIMT_TRANSFORM opts out)
     static bool use_tca(fno_dtype_t dt, uint32_t flags) {
-        return tca_shape<Cf>(dt) && !(flags & FNO_PLAN_SIMT_TRANSFORM);
+        if (!tca_shape<Cf>(dt)) return false;
+        return dt == FNO_F32 ? (flags & FNO_PLAN_TENSOR_CORES) != 0
+                             : (flags & FNO_PLAN_SIMT_TRANSFORM) == 0;
     }
     // partial copies of the kept modes kernel A leaves (one from the tensor-core kernel)
     static int parts(fno_dtype_t dt, uint32_t flags) { return use_tca(dt, flags) ? 1 : kParts; }
@@ -1272,7 +792,7 @@ struct Pdl {
 
 using Pdl128 = Pdl<Cfg128V<FNO_CFG128_A>, Cfg128V<FNO_CFG128_C>>;
 
-enum Variant { kVarNone, kVarPdl128, kVarPdl256, kVarPersistent128, kVarTc128, kVarPdl3d, kVarOne1d };
+enum Variant { kVarNone, kVarPdl128, kVarPdl256, kVarPersistent128, kVarPdl3d, kVarOne1d };
 
 // Which fused kernel(s) a description runs on.
 Variant variant(const Geom &g, fno_dtype_t dtype, uint32_t flags) {
@@ -1281,7 +801,6 @@ Variant variant(const Geom &g, fno_dtype_t dtype, uint32_t flags) {
     if (fused3d_match(g, dtype)) return kVarPdl3d;
     if (is_cfg256(g)) return kVarPdl256;
     if (!is_cfg128(g)) return kVarNone;
-    if (use_tc(g, dtype, flags)) return kVarTc128;
     if ((flags & FNO_PLAN_PERSISTENT) && dtype != FNO_BF16) return kVarPersistent128;
     return kVarPdl128;
 }
@@ -1295,9 +814,6 @@ bool fused_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, i
     const int C = v == kVarPdl256 ? Cfg256::C : Cfg128::C;
     if (batch * (int64_t)cin * C >= (1 << 30) || batch * (int64_t)cout * C >= (1 << 30))
         return false;
-    if (v == kVarTc128)
-        return batch * (int64_t)(cin > cout ? cin : cout) * 128 < (1ll << 31) &&
-               (size_t)cin * 16 <= kTcXpBudget;
     if (v == kVarPersistent128)
         return smem_bytes(dtype, cin, b_shape(dtype, batch, cin, cout)) <= 200 * 1024;
     // three-kernel variants: a weight slab of one output and one batch row must fit
@@ -1310,7 +826,6 @@ size_t fused_workspace_bytes(const Geom &g, fno_dtype_t dtype, int64_t batch, in
     const Variant v = variant(g, dtype, flags);
     if (v == kVarPdl3d) return fused3d_workspace_bytes(g, batch, cin, cout);
     if (v == kVarOne1d) return 0;
-    if (v == kVarTc128) return layout_tc(g, batch, cin, cout).total;
     if (v == kVarPersistent128) return layout(g, batch, cin, cout).total;
     const size_t part = v == kVarPdl256 ? Pdl<Cfg256>::part_bytes(g, batch, cin, dtype, flags)
                                         : Pdl128::part_bytes(g, batch, cin, dtype, flags);
@@ -1360,41 +875,7 @@ cudaError_t fused_plan_init(Plan &p) {
         return with_storage(p.dtype, [&](auto t) { return Pdl128::init<decltype(t)>(p); });
     if (v == kVarPdl256)
         return with_storage(p.dtype, [&](auto t) { return Pdl<Cfg256>::init<decltype(t)>(p); });
-    if (v == kVarTc128)
-    {
-        if (!encoder()) return cudaErrorNotSupported;
-        const BShape bs = b_shape_tc(p.batch, p.cin, p.cout);
-        cudaError_t e = cudaFuncSetAttribute(tc::k_fused2d_tc,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)tc::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc::k_fused2d_tc,
-                                                           tc::kStreams * tc::NT, tc::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        if (per_sm < 1) return cudaErrorInvalidConfiguration;
-        // one CTA per SM: each holds kTmemCols columns of tensor memory
-        p.fused_grid = p.num_sms;
-        p.fused_smem = tc::kSmemBytes;
-        p.fused_ob = bs.ob;
-        p.fused_bb = bs.bg;
-        float *host = new (std::nothrow) float[tc::kTableBytes / 4];
-        if (!host) return cudaErrorMemoryAllocation;
-        tc::make_tables(host);
-        e = cudaMalloc(&p.fused_tables, tc::kTableBytes);
-        if (e == cudaSuccess)
-            e = cudaMemcpy(p.fused_tables, host, tc::kTableBytes, cudaMemcpyHostToDevice);
-        delete[] host;
-        if (e != cudaSuccess) return e;
-        if (p.flags & FNO_PLAN_TRACE) {
-            const int ng = (int)((p.batch + bs.bg - 1) / bs.bg);
-            p.trace_records = (size_t)p.batch * (p.cin + p.cout) +
-                              (size_t)ng * (p.g.nkept / kG) * ((p.cout + bs.ob - 1) / bs.ob);
-            e = cudaMalloc(&p.trace, p.trace_records * sizeof(fno_trace_record_t));
-            if (e != cudaSuccess) return e;
-        }
-        return cudaMemset(p.sync, 0, kSyncBytes);
-    }
+
     const BShape bs = b_shape(p.dtype, p.batch, p.cin, p.cout);
     const size_t smem = smem_bytes(p.dtype, p.cin, bs);
     void *fn = p.dtype == FNO_F32 ? kernel_ptr<float>() : kernel_ptr<__half>();
@@ -1430,41 +911,7 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
     const Variant v = variant(p.g, p.dtype, p.flags);
     if (v == kVarPdl3d) return fused3d_forward(p, b, s);
     if (v == kVarOne1d) return fused1d_forward(p, b, s);
-    if (v == kVarTc128)
-    {
-        const Layout l = layout_tc(p.g, p.batch, p.cin, p.cout);
-        CUtensorMap xmap, ymap;
-        if (!encode_rows(&xmap, b.x, p.batch * p.cin * 128) ||
-            !encode_rows(&ymap, b.y, p.batch * p.cout * 128))
-            return cudaErrorInvalidValue;
-        Args a;
-        a.x = b.x;
-        a.w = b.w;
-        a.y = b.y;
-        a.part = reinterpret_cast<float2 *>(static_cast<char *>(b.ws) + l.part_off);
-        a.Y = reinterpret_cast<float2 *>(static_cast<char *>(b.ws) + l.y_off);
-        a.sync = reinterpret_cast<SyncBlock *>(p.sync);
-        a.tw0 = p.tw[0];
-        a.tw1 = p.tw[1];
-        a.err = p.dev_err;
-        a.trace = p.trace;
-        a.wbytes = p.weight_bytes;
-        a.wslice = 0;
-        a.batch = (int)p.batch;
-        a.cin = p.cin;
-        a.cout = p.cout;
-        a.bg = p.fused_bb;
-        a.ng = (int)((p.batch + a.bg - 1) / a.bg);
-        a.npairs = (int)(p.g.nkept / kG);
-        a.ob = p.fused_ob;
-        a.nob = (p.cout + a.ob - 1) / a.ob;
-        const int total = (int)p.batch * (p.cin + p.cout) + a.ng * a.npairs * a.nob;
-        const int grid = p.fused_grid;
-        (void)total;
-        tc::k_fused2d_tc<<<grid, tc::kStreams * tc::NT, p.fused_smem, s>>>(
-            xmap, ymap, a, static_cast<const float4 *>(p.fused_tables));
-        return cudaGetLastError();
-    }
+
     if (v == kVarPdl128 || v == kVarPdl256) {
         const size_t part = v == kVarPdl256
                                 ? Pdl<Cfg256>::part_bytes(p.g, p.batch, p.cin, p.dtype, p.flags)

@@ -82,10 +82,12 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * CTA of each kernel of the three-kernel variants (2-D and 3-D layers).
  * Costs a few timer reads, a barrier and a store per item.                  */
 #define FNO_PLAN_TRACE 2u
-/* Run the float32 128x128 layer on the tensor-core variant of the fused
- * kernel (row DFTs as tcgen05 3xTF32 GEMMs fed by TMA) instead of the
- * register-FFT variant.  Same results within rounding; on this workload the
- * register-FFT variant is the faster one, so it is the default.            */
+/* Run the forward transform of the float32 128x128 layer (16x16 modes) on
+ * the tensor cores: each image's row DFT as a tcgen05 3xTF32 GEMM (TMA-staged
+ * operands, accumulator in tensor memory) inside the three-kernel path.  Same
+ * results within rounding; at this size the register-FFT kernel is measured
+ * faster (22.3 vs 22.8 us on the 8 x 32-channel workload), so it is the
+ * default.  (16-bit 256x256 layers use the tensor-core transform by default.) */
 #define FNO_PLAN_TENSOR_CORES 4u
 /* Run the float32 / fp16 128x128 layer as ONE persistent kernel with a work
  * queue instead of three kernels chained by programmatic dependent launch
@@ -99,10 +101,9 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * (2-D fp16 / bf16 layers with at most 64 channels and 64 samples; the
  * tensor-core kernel is the default there).  An ablation switch.            */
 #define FNO_PLAN_SIMT_MIX 32u
-/* Run the forward transform of the three-kernel 2-D path with the register-
- * FFT kernel where the tensor-core kernel would run (fp32 128x128 with 16x16
- * modes and 16-bit 256x256 with 32x32 modes, where the row DFT is a tcgen05
- * GEMM; the tensor-core kernel is the default there).  An ablation switch.  */
+/* Run the forward transform of the 16-bit 256x256 layer (32x32 modes) with
+ * the register-FFT kernel instead of the tensor-core kernel (a kind::f16
+ * tcgen05 GEMM per image, the default there).  An ablation switch.          */
 #define FNO_PLAN_SIMT_TRANSFORM 64u
 
 /* One work item of the fused kernel, as recorded under FNO_PLAN_TRACE.
