@@ -460,6 +460,217 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
     cta_record(a, 0, 0, t0, t0);
 }
 
+// ---------------------------------------------------------------------------
+// Kernel C on the tensor cores, for 16-bit 256 x 256 layers: one CTA inverts a
+// whole output image.  The column inverse over the kept rows runs on the SIMT
+// cores (32-point inverse register FFTs over the residues q = q1 + 8 q2, then
+// the twiddled sums over q1), giving Zo[t][k] for every row t; the row inverse
+// is then the GEMM y = s Zo' . Tinv^T with Zo' = [Re Zo | Im Zo] (K = 64) and
+// Tinv[n] = [c(k) cos(2 pi k n / N1) | -c(k) sin(...)], one kind::tf32 chain per
+// 128-row tile with N = 256 output samples in tensor memory (tf32 keeps the
+// float32 range of Zo; its 2^-11 precision is within the 16-bit tolerance
+// class).  The epilogue scales by s = 1/(N0 N1), converts to the storage type
+// and stores 64-column boxes by TMA through two swizzled staging tiles.
+// ---------------------------------------------------------------------------
+template <typename T>
+struct GeoC {
+    static constexpr int N0 = 256, N1 = 256, M0 = 32, M1 = 32, K0 = 64, NK = K0 * M1;
+    static constexpr int B2 = 32, A = N0 / B2;          // column inverse split
+    static constexpr int MT = 2;                        // 128-row tiles
+    static constexpr uint32_t kTile = 16384;            // 128 rows x 128 bytes
+    static constexpr uint32_t kA = 0;                   // [MT][2 chunks] Zo operand, 64 KiB
+    static constexpr uint32_t kB = kA + MT * 2 * kTile; // [2 chunks][256 rows] table, 64 KiB
+    static constexpr uint32_t kTBytes = 2 * 256 * 128;
+    static constexpr uint32_t kY = kB + kTBytes;        // kept modes, 16 KiB
+    static constexpr uint32_t kS = kY + NK * 8;         // [A][B2][M1] residue sums, 64 KiB
+    static constexpr uint32_t kTw = kS + A * B2 * M1 * 8;
+    static constexpr uint32_t kSmem = kTw + N0 * 8 + 1024;
+    static constexpr uint32_t kStage = kS;              // 2 x 16 KiB output boxes over S
+    static constexpr uint32_t kTmemCols = 512;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(NT, 1)
+k_phase_c_tc(const __grid_constant__ CUtensorMap ymap, Args a, const void *table) {
+    using Gm = GeoC<T>;
+    using namespace tcu;
+    extern __shared__ __align__(1024) char smem_raw[];
+    char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+    __shared__ __align__(8) uint64_t bar_t, bar_mma;
+    __shared__ uint32_t s_tmem;
+    const unsigned long long t0 = a.trace ? trace_now() : 0;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int img = blockIdx.x;
+    float2 *ys = reinterpret_cast<float2 *>(base + Gm::kY);
+    float2 *S = reinterpret_cast<float2 *>(base + Gm::kS);
+    float2 *tw = reinterpret_cast<float2 *>(base + Gm::kTw);
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_t)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_mma)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     ::"r"(tc_smem_addr(&bar_t)), "r"(Gm::kTBytes) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(tc_smem_addr(base + Gm::kB)), "l"(table), "r"(Gm::kTBytes),
+                     "r"(tc_smem_addr(&bar_t)) : "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(tc_smem_addr(&s_tmem)), "r"(Gm::kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    for (int e = tid; e < Gm::N0; e += NT) tw[e] = a.tw0[e];
+    tc_before_sync();
+    __syncthreads();
+    tc_after_sync();
+    const uint32_t tmem = s_tmem;
+    pdl_wait();                                  // kernel B's mixed modes are complete
+    const unsigned long long t1 = a.trace ? trace_now() : 0;
+    const float2 *src = a.Y + (size_t)img * Gm::NK;
+    for (int e = tid; e < Gm::NK / 2; e += NT) cp_async16(ys + 2 * e, src + 2 * e);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    // 1. S[q1][r][k] = inverse B2-point DFT over q2 of V[q1 + A q2][k], V the kept
+    //    modes placed at their frequency rows (zero elsewhere)
+    for (int u = tid; u < Gm::A * Gm::M1; u += NT) {
+        const int q1 = u / Gm::M1, k = u % Gm::M1;
+        float2 z[Gm::B2];
+#pragma unroll
+        for (int q2 = 0; q2 < Gm::B2; ++q2) {
+            const int q = q1 + Gm::A * q2;
+            int j = -1;
+            if (q < Gm::M0) j = q;
+            else if (q >= Gm::N0 - Gm::M0) j = q - (Gm::N0 - Gm::K0);
+            z[q2] = j >= 0 ? ys[j * Gm::M1 + k] : make_float2(0.f, 0.f);
+        }
+        fft::fft_dif<Gm::B2, 1>(z);
+#pragma unroll
+        for (int r = 0; r < Gm::B2; ++r)
+            S[(q1 * Gm::B2 + r) * Gm::M1 + k] = z[fft::bitrev(r, fft::ilog2(Gm::B2))];
+    }
+    __syncthreads();
+    // 2. Zo[t][k] = sum_q1 conj(W_N0^{q1 t}) S[q1][t mod B2][k], four bins per unit,
+    //    into the K-major operand: chunk 0 the real parts, chunk 1 the imaginary
+    for (int u = tid; u < Gm::N0 * (Gm::M1 / 4); u += NT) {
+        const int t = u / (Gm::M1 / 4), k0 = 4 * (u % (Gm::M1 / 4));
+        float2 acc[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q1 = 0; q1 < Gm::A; ++q1) {
+            const float2 wv = tw[(q1 * t) & (Gm::N0 - 1)];
+            const float2 wc = make_float2(wv.x, -wv.y);
+            const float4 *s4 = reinterpret_cast<const float4 *>(
+                S + (q1 * Gm::B2 + (t % Gm::B2)) * Gm::M1 + k0);
+            const float4 p0 = s4[0], p1 = s4[1];
+            cmac(acc[0], make_float2(p0.x, p0.y), wc);
+            cmac(acc[1], make_float2(p0.z, p0.w), wc);
+            cmac(acc[2], make_float2(p1.x, p1.y), wc);
+            cmac(acc[3], make_float2(p1.z, p1.w), wc);
+        }
+        char *At = base + Gm::kA + (t / 128) * 2 * Gm::kTile;
+        const uint32_t off = sw_off(t % 128, k0);
+        *reinterpret_cast<float4 *>(At + off) =
+            make_float4(acc[0].x, acc[1].x, acc[2].x, acc[3].x);
+        *reinterpret_cast<float4 *>(At + Gm::kTile + off) =
+            make_float4(acc[0].y, acc[1].y, acc[2].y, acc[3].y);
+    }
+    fence_async_smem();
+    tc_before_sync();
+    __syncthreads();
+    bool ok = mbar_wait(&bar_t, 0, a.err);
+    if (tid == 0) {
+        tc_after_sync();
+        constexpr uint32_t id = idesc_tf32(256);
+        const uint32_t as = tc_smem_addr(base + Gm::kA), bs = tc_smem_addr(base + Gm::kB);
+        for (int t = 0; t < Gm::MT; ++t)
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_tf32(tmem + 256 * t, desc_sw128(as + (t * 2 + c) * Gm::kTile + s * 32),
+                             desc_sw128(bs + c * 256 * 128 + s * 32), id, (c | s) ? 1u : 0u);
+        mma_commit(&bar_mma);
+    }
+    ok &= mbar_wait(&bar_mma, 0, a.err);
+    tc_after_sync();
+    // 3. rows out: warp w reads lanes 32 (w % 4).. of tensor memory; the two warp
+    //    halves take column blocks 2h and 2h + 1 (64 outputs each) per tile
+    const float scale = 1.0f / ((float)Gm::N0 * (float)Gm::N1);
+    const int half = warp >> 2, lrow = 32 * (warp & 3) + (tid & 31);
+    char *stage = base + Gm::kStage + half * Gm::kTile;
+    for (int t = 0; t < Gm::MT; ++t) {
+        for (int step = 0; step < 2; ++step) {
+            const int cb = 2 * half + step;               // 64-column block of y
+            if (t | step) {
+                if (tid == 0) bulk_wait_read();           // the staging tiles were stored
+                __syncthreads();
+            }
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                float v[16];
+                tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256 * t + 64 * cb + 16 * g, v);
+                uint32_t pk[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float lo = ok ? v[2 * q] * scale : 0.f, hi = ok ? v[2 * q + 1] * scale : 0.f;
+                    T tl, th;
+                    if constexpr (std::is_same<T, __half>::value) {
+                        tl = __float2half_rn(lo);
+                        th = __float2half_rn(hi);
+                    } else {
+                        tl = __float2bfloat16_rn(lo);
+                        th = __float2bfloat16_rn(hi);
+                    }
+                    uint16_t ul, uh;
+                    memcpy(&ul, &tl, 2);
+                    memcpy(&uh, &th, 2);
+                    pk[q] = (uint32_t)ul | ((uint32_t)uh << 16);
+                }
+                *reinterpret_cast<uint4 *>(stage + sw_off16(lrow, 16 * g)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4 *>(stage + sw_off16(lrow, 16 * g + 8)) =
+                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+            fence_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                for (int h = 0; h < 2; ++h)
+                    tma_store_2d(&ymap, 64 * (2 * h + step), img * Gm::N0 + 128 * t,
+                                 tc_smem_addr(base + Gm::kStage + h * Gm::kTile));
+                bulk_commit();
+            }
+        }
+    }
+    if (tid == 0) bulk_wait_all();
+    tc_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc_after_sync();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(Gm::kTmemCols));
+    }
+    cta_record(a, 2, a.trace_c, t0, t1);
+}
+
+// Host: the inverse row-DFT operand: [chunk: re, im][n][k] with c(k) folded in.
+template <typename T>
+void make_table_c(std::vector<unsigned char> &img) {
+    using Gm = GeoC<T>;
+    using tcu::sw_off;
+    img.assign(Gm::kTBytes, 0);
+    const double two_pi = 2.0 * M_PI;
+    for (int n = 0; n < Gm::N1; ++n)
+        for (int k = 0; k < Gm::M1; ++k) {
+            const double ck = (k == 0 || 2 * k == Gm::N1) ? 1.0 : 2.0;
+            const double ang = two_pi * (double)k * (double)n / (double)Gm::N1;
+            const float c = (float)(ck * std::cos(ang)), sn = (float)(-ck * std::sin(ang));
+            memcpy(&img[sw_off(n, k)], &c, 4);
+            memcpy(&img[256 * 128 + sw_off(n, k)], &sn, 4);
+        }
+}
+
 // Host: the twiddle operand in its swizzled shared-memory image (hi then lo for
 // fp32, one 16-bit copy otherwise), computed in double.
 template <typename T>
@@ -656,14 +867,26 @@ struct Pdl {
                 e = cudaFuncSetAttribute(tca::k_phase_a_tc<T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Gm::kSmem);
-                std::vector<unsigned char> img;
-                if (e == cudaSuccess) {
-                    tca::make_table<T>(img);
-                    e = cudaMalloc(&p.fused_tables, img.size());
+                // the inverse on the tensor cores too, for 16-bit storage
+                std::vector<unsigned char> img, imgc;
+                if (e == cudaSuccess) tca::make_table<T>(img);
+                if constexpr (!std::is_same<T, float>::value) {
+                    p.fused_tcc = true;
+                    if (e == cudaSuccess)
+                        e = cudaFuncSetAttribute(tca::k_phase_c_tc<T>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)tca::GeoC<T>::kSmem);
+                    tca::make_table_c<T>(imgc);
                 }
+                const size_t off_c = (img.size() + 255) & ~size_t(255);
+                if (e == cudaSuccess) e = cudaMalloc(&p.fused_tables, off_c + imgc.size());
                 if (e == cudaSuccess)
                     e = cudaMemcpy(p.fused_tables, img.data(), img.size(),
                                    cudaMemcpyHostToDevice);
+                if (e == cudaSuccess && !imgc.empty())
+                    e = cudaMemcpy(static_cast<char *>(p.fused_tables) + off_c, imgc.data(),
+                                   imgc.size(), cudaMemcpyHostToDevice);
+                p.fused_table_c = off_c;
             }
         }
         p.fused_bb = bb;
@@ -680,7 +903,8 @@ struct Pdl {
                                             : (size_t)(p.g.nkept / kG) * ((p.cout + ob - 1) / ob) *
                                                   ((p.batch + bb - 1) / bb);
             const size_t nA = (size_t)p.batch * p.cin * (p.fused_tca ? 1 : Cf::C);
-            p.trace_records = nA + (size_t)p.batch * p.cout * CfC::C + nB;
+            const size_t nC = (size_t)p.batch * p.cout * (p.fused_tcc ? 1 : CfC::C);
+            p.trace_records = nA + nC + nB;
             e = cudaMalloc(&p.trace, p.trace_records * sizeof(fno_trace_record_t));
         }
         return e;
@@ -713,7 +937,7 @@ struct Pdl {
         a.npairs = (int)(p.g.nkept / kG);
         const int nA = (int)p.batch * p.cin * (p.fused_tca ? 1 : Cf::C);
         const int nB = p.fused_mixtc ? mixtc_items(p.g.nkept) : a.npairs * a.nob * a.ng;
-        const int nC = (int)p.batch * p.cout * CfC::C;
+        const int nC = (int)p.batch * p.cout * (p.fused_tcc ? 1 : CfC::C);
         a.trace = p.trace;
         a.trace_b = nA;
         a.trace_c = nA + nB;
@@ -783,6 +1007,21 @@ struct Pdl {
         if (e != cudaSuccess) return e;
         cfg.gridDim = dim3(nC);
         cfg.blockDim = dim3(kNT);
+        if constexpr (!std::is_same<T, float>::value) {
+            if (p.fused_tcc) {
+                using Gc = tca::GeoC<T>;
+                CUtensorMap ymap;
+                if (!tcu::encode_rows_tiled(&ymap, a.y, (int64_t)p.batch * p.cout * Gc::N0,
+                                            Gc::N1, sizeof(T), 64, tcu::tma_type<T>()))
+                    return cudaErrorInvalidValue;
+                cfg.blockDim = dim3(tca::NT);
+                cfg.dynamicSmemBytes = Gc::kSmem;
+                const void *tab = static_cast<const char *>(p.fused_tables) + p.fused_table_c;
+                e = cudaLaunchKernelEx(&cfg, tca::k_phase_c_tc<T>, ymap, a, tab);
+                if (e != cudaSuccess) return e;
+                return cudaGetLastError();
+            }
+        }
         cfg.dynamicSmemBytes = CfC::kSmemTw + CfC::kSmemC;
         e = cudaLaunchKernelEx(&cfg, k_phase_c<CfC, T>, a);
         if (e != cudaSuccess) return e;

@@ -56,6 +56,8 @@ struct Plan {
     void *fused_tables;           // tensor-core path: twiddle operands (plan-owned)
     bool fused_mixtc;             // three-kernel path mixes on the tensor cores
     bool fused_tca;               // three-kernel path transforms (kernel A) on the tensor cores
+    bool fused_tcc;               // ... and inverts (kernel C) on the tensor cores
+    size_t fused_table_c;         // byte offset of kernel C's operand in fused_tables
     fno_trace_record_t *trace;    // FNO_PLAN_TRACE: one record per work item (plan-owned)
     size_t trace_records;         // records one forward call produces
     // FNO_PLAN_BACKWARD: the adjoint layer's plan and the backward workspace map

@@ -163,15 +163,17 @@ def test_every_workload_runs_fused(name, kernels):
 
 
 @pytest.mark.parametrize("name", ["2d_f16", "2d_bf16"])
-def test_tensor_core_and_simt_mixing_agree(name):
+def test_tensor_core_and_simt_kernels_agree(name):
     # both within the half-storage bar of the oracle (sampled) and of each other
     case = workloads.CASES[name]
     x, w = workloads.make_x(case), workloads.make_w(case)
     a, _ = run_gpu(case, x, w)
     b, _ = run_gpu(case, x, w, capi.FNO_PLAN_SIMT_MIX)
     c, _ = run_gpu(case, x, w)
-    assert np.array_equal(a, c), "two runs of the tensor-core mixing differ"
+    d, _ = run_gpu(case, x, w, capi.FNO_PLAN_SIMT_MIX | capi.FNO_PLAN_SIMT_TRANSFORM)
+    assert np.array_equal(a, c), "two runs of the tensor-core kernels differ"
     assert_close(a, b.astype(np.float64), case.dtype, "tensor-core vs SIMT mixing")
+    assert_close(a, d.astype(np.float64), case.dtype, "tensor-core vs SIMT kernels")
     for s in (0, case.batch - 1):
         ref = run_oracle(case, x[s:s + 1], w)
         assert_close(a[s:s + 1], ref, case.dtype, f"{name}[b={s}] tensor-core mixing")
