@@ -89,6 +89,19 @@ class SpectralConv:
 
     __call__ = forward
 
+    def pack_weights(self, w, out=None, stream=None):
+        """The packed copy of w for a plan made with FNO_PLAN_PACKED_WEIGHTS
+        (pass it to forward in place of w)."""
+        import torch
+        _require(w, self.torch_dtype, self.w_shape, "w")
+        if out is None:
+            out = torch.empty_like(w)
+        _require(out, self.torch_dtype, self.w_shape, "out")
+        check(capi.fno_spectral_conv_pack_weights(self.handle, w.data_ptr(), out.data_ptr(),
+                                                  _stream_handle(stream)),
+              "fno_spectral_conv_pack_weights")
+        return out
+
     def backward(self, x, w, dy, need_dx=True, need_dw=True, dx=None, dw=None, stream=None):
         """Gradients (dx, dw) of a real loss given dy = dL/dy; the plan must have
         been made with FNO_PLAN_BACKWARD.  dw is dL/dRe(w) + i dL/dIm(w) in w's

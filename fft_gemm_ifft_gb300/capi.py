@@ -36,6 +36,7 @@ FNO_PLAN_PERSISTENT = 8
 FNO_PLAN_BACKWARD = 16
 FNO_PLAN_SIMT_MIX = 32
 FNO_PLAN_SIMT_TRANSFORM = 64
+FNO_PLAN_PACKED_WEIGHTS = 128
 
 # Every symbol include/fno.h declares.
 EXPORTS = (
@@ -44,6 +45,7 @@ EXPORTS = (
     "fno_spectral_conv_workspace_size", "fno_spectral_conv_kernel_count",
     "fno_spectral_conv_forward", "fno_plan_get_device_error", "fno_plan_destroy",
     "fno_spectral_conv_forward_static", "fno_plan_get_trace", "fno_spectral_conv_backward",
+    "fno_spectral_conv_pack_weights",
     "fno_model_plan", "fno_model_workspace_size", "fno_model_kernel_count",
     "fno_forward", "fno_model_get_device_error", "fno_model_destroy",
 )
@@ -110,6 +112,7 @@ def lib() -> ctypes.CDLL:
                 ctypes.c_int, pi64, pi32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _st,
                 _vp, _vp, _vp, _vp]
             L.fno_spectral_conv_backward.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+            L.fno_spectral_conv_pack_weights.argtypes = [_vp, _vp, _vp, _vp]
             L.fno_plan_get_trace.argtypes = [_vp, ctypes.POINTER(fno_trace_record_t),
                                              ctypes.c_size_t, psz]
             L.fno_plan_get_device_error.argtypes = [_vp, _vp]
@@ -173,6 +176,10 @@ def fno_spectral_conv_forward(plan, x_ptr, w_ptr, y_ptr, ws_ptr, stream):
 def fno_spectral_conv_backward(plan, x_ptr, w_ptr, dy_ptr, dx_ptr, dw_ptr, ws_ptr, stream):
     return lib().fno_spectral_conv_backward(plan, x_ptr, w_ptr, dy_ptr, dx_ptr, dw_ptr, ws_ptr,
                                             stream)
+
+
+def fno_spectral_conv_pack_weights(plan, w_ptr, wp_ptr, stream):
+    return lib().fno_spectral_conv_pack_weights(plan, w_ptr, wp_ptr, stream)
 
 
 def fno_spectral_conv_forward_static(ndim, n, modes, batch, cin, cout, dtype, x_ptr, w_ptr,

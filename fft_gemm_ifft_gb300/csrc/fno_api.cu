@@ -85,7 +85,11 @@ fno_status_t describe(int ndim, const int64_t *n, const int32_t *modes, int64_t 
     if (dtype != FNO_F32 && dtype != FNO_F16 && dtype != FNO_BF16) return FNO_ERR_INVALID_ARG;
     if (flags & ~(FNO_PLAN_UNFUSED | FNO_PLAN_TRACE | FNO_PLAN_TENSOR_CORES |
                   FNO_PLAN_PERSISTENT | FNO_PLAN_BACKWARD | FNO_PLAN_SIMT_MIX |
-                  FNO_PLAN_SIMT_TRANSFORM))
+                  FNO_PLAN_SIMT_TRANSFORM | FNO_PLAN_PACKED_WEIGHTS))
+        return FNO_ERR_INVALID_ARG;
+    // packed weights: groups of four kept modes; the backward reads the standard layout
+    if ((flags & FNO_PLAN_PACKED_WEIGHTS) &&
+        (g->nkept % 4 != 0 || (flags & FNO_PLAN_BACKWARD)))
         return FNO_ERR_INVALID_ARG;
     // int64 element counts must not overflow and a tensor must stay addressable
     const double xe = (double)batch * cin * g->npix, ye = (double)batch * cout * g->npix;
@@ -279,6 +283,22 @@ fno_status_t fno_spectral_conv_forward(fno_plan_t plan, const void *x, const voi
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = p.path == kPathUnfused ? unfused_forward(p, b, s) : fused_forward(p, b, s);
     if (e != cudaSuccess) {
+        cudaGetLastError();
+        return FNO_ERR_CUDA;
+    }
+    return FNO_OK;
+}
+
+fno_status_t fno_spectral_conv_pack_weights(fno_plan_t plan, const void *w, void *w_packed,
+                                            fno_stream_t stream) {
+    if (!plan || !w || !w_packed) return FNO_ERR_INVALID_ARG;
+    const Plan &p = *reinterpret_cast<Plan *>(plan);
+    if (!(p.flags & FNO_PLAN_PACKED_WEIGHTS)) return FNO_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(w_packed)) return FNO_ERR_MISALIGNED;
+    if (overlaps(w, p.weight_bytes, w_packed, p.weight_bytes)) return FNO_ERR_ALIASING;
+    if (inject("launch")) return FNO_ERR_CUDA;
+    if (launch_pack_weights(p, w, w_packed, reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess) {
         cudaGetLastError();
         return FNO_ERR_CUDA;
     }

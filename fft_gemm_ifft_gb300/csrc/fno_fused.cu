@@ -156,7 +156,7 @@ k_fused2d(Args a) {
             bi.nbb = nbg;
             // the weights do not depend on phase A: request them first
             phase_b_weights<Cf, T, kNT>(CtaGroup{tid}, static_cast<const T *>(a.w), a.cin, a.cout, bi,
-                                        a.ob, work);
+                                        a.ob, work, a.wpacked != 0);
             if (tid == 0)
                 s_ok = wait_flag(&a.sync->flag_a[it.g][blockIdx.x % kFlagCopies][0], a.err);
             if (tid == 0) ts.ready(a);
@@ -994,6 +994,7 @@ struct Pdl {
             m.m1 = Cf::M1;
             m.mblk = (int)Cf::MBLK;
             m.nk = Cf::NK;
+            m.packed = a.wpacked;
             e = mixtc_launch(p.dtype, m, s);
         } else {
             cfg.gridDim = dim3(nB);
@@ -1159,6 +1160,7 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
         a.x = b.x;
         a.w = b.w;
         a.y = b.y;
+        a.wpacked = (p.flags & FNO_PLAN_PACKED_WEIGHTS) ? 1 : 0;
         a.part = static_cast<float2 *>(b.ws);
         a.Y = reinterpret_cast<float2 *>(static_cast<char *>(b.ws) + ((part + 255) & ~size_t(255)));
         a.tw0 = p.tw[0];
@@ -1178,6 +1180,7 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
     a.x = b.x;
     a.w = b.w;
     a.y = b.y;
+    a.wpacked = (p.flags & FNO_PLAN_PACKED_WEIGHTS) ? 1 : 0;
     a.part = reinterpret_cast<float2 *>(static_cast<char *>(b.ws) + l.part_off);
     a.Y = reinterpret_cast<float2 *>(static_cast<char *>(b.ws) + l.y_off);
     a.sync = reinterpret_cast<SyncBlock *>(p.sync);

@@ -40,6 +40,7 @@ struct MixTcArgs {
     fno_trace_record_t *trace;    // nullptr unless tracing
     int trace_first;
     int batch, cin, cout, m0, m1, mblk, nk;
+    int packed;                   // w is in the packed mode-major layout
 };
 bool mixtc_supported(int d, fno_dtype_t dtype, int64_t batch, int cin, int cout, int m1,
                      int64_t nkept);

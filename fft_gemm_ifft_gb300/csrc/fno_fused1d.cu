@@ -29,7 +29,7 @@ size_t smem1_bytes(int n, int m, int cin, int cout) {
 template <typename T>
 __global__ void __launch_bounds__(kT1)
 k_fused1d(const T *__restrict__ x, const T *__restrict__ w, T *__restrict__ y, int cin,
-          int cout, int N, int M, const float2 *__restrict__ tw_g) {
+          int cout, int N, int M, const float2 *__restrict__ tw_g, int packed) {
     extern __shared__ __align__(16) float2 sm1[];
     float2 *tw = sm1;                      // [N]      e^{-2 pi i j / N}
     float2 *X = tw + N;                    // [cin][M] bins of every input channel
@@ -88,7 +88,8 @@ k_fused1d(const T *__restrict__ x, const T *__restrict__ w, T *__restrict__ y, i
         float2 acc = make_float2(0.f, 0.f);
         for (int i = 0; i < cin; ++i)
             cfma(acc, X[(size_t)i * M + k],
-                 Storage<T>::load2(w + (((int64_t)i * cout + o) * M + k) * 2));
+                 Storage<T>::load2(w + (packed ? packed_index(k, i, o, cin, cout)
+                                               : ((size_t)i * cout + o) * M + k) * 2));
         Y[e] = acc;
     }
     __syncthreads();
@@ -136,7 +137,8 @@ cudaError_t fused1d_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
         using T = decltype(t);
         return cudaLaunchKernelEx(&cfg, k_fused1d<T>, static_cast<const T *>(b.x),
                                   static_cast<const T *>(b.w), static_cast<T *>(b.y), p.cin,
-                                  p.cout, N, M, static_cast<const float2 *>(p.tw[0]));
+                                  p.cout, N, M, static_cast<const float2 *>(p.tw[0]),
+                                  (p.flags & FNO_PLAN_PACKED_WEIGHTS) ? 1 : 0);
     });
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -431,6 +431,7 @@ cudaError_t fused3d_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
     a.batch = (int)p.batch;
     a.cin = p.cin;
     a.cout = p.cout;
+    a.wpacked = (p.flags & FNO_PLAN_PACKED_WEIGHTS) ? 1 : 0;
     return with_storage(p.dtype,
                         [&](auto t) { return Pdl3<Cfg3d64>::forward<decltype(t)>(p, a, s); });
 }

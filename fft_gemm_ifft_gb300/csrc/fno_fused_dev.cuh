@@ -429,14 +429,18 @@ constexpr int kBT = 4;      // batch rows per register tile
 
 template <class Cf, typename T, int NT, class G>
 __device__ void phase_b_weights(const G &grp, const T *__restrict__ w, int cin, int cout,
-                                const BItem &it, int ob, char *smem) {
+                                const BItem &it, int ob, char *smem, bool packed = false) {
     using W2 = typename Io<T>::W2;
     int blk, local;
     Cf::wmap(it.pair * kG, blk, local);          // the pair is adjacent in its block
     W2 *ws = reinterpret_cast<W2 *>(smem);                   // [cin][ob]
     for (int e = grp.tid; e < cin * it.nob; e += NT) {
         const int o = e % it.nob, i = e / it.nob;
-        const T *p = w + ((((size_t)blk * cin + i) * cout + it.o0 + o) * Cf::MBLK + local) * 2;
+        // the pair's two modes are adjacent in both layouts (the pair starts at an
+        // even kept index: within one group of four when packed)
+        const T *p = packed
+                         ? w + packed_index(it.pair * kG, i, it.o0 + o, cin, cout) * 2
+                         : w + ((((size_t)blk * cin + i) * cout + it.o0 + o) * Cf::MBLK + local) * 2;
         if constexpr (sizeof(W2) == 16)
             cp_async16(ws + i * ob + o, p);
         else
@@ -706,6 +710,7 @@ struct Args {
     int npairs;         // phase B: kept-mode pairs
     int ob, nob;        // phase B: outputs per item, output blocks
     int trace_b, trace_c;   // three-kernel variants: first trace record of kernel B, C
+    int wpacked;            // w is in the packed mode-major layout
 };
 
 __device__ __forceinline__ unsigned long long trace_now() {
@@ -757,7 +762,7 @@ __global__ void __launch_bounds__(kNTB) k_phase_b(Args a) {
     // the same banks
     const int wstride = a.ob + 1;
     phase_b_weights<Cf, T, kNTB>(grp, static_cast<const T *>(a.w), a.cin, a.cout, bi, wstride,
-                                 smem);
+                                 smem, a.wpacked != 0);
     pdl_trigger();
     pdl_wait();                                  // kernel A's partial modes are complete
     const unsigned long long t1 = a.trace ? trace_now() : 0;

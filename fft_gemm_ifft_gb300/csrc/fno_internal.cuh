@@ -131,6 +131,13 @@ decltype(auto) with_storage(fno_dtype_t dt, F &&f) {
     return f(0.0f);
 }
 
+// Complex-element index of weight (kept mode kk, input i, output o) in the
+// packed mode-major layout: groups of four kept modes, [group][i][o][4].
+__host__ __device__ __forceinline__ size_t packed_index(int64_t kk, int i, int o, int cin,
+                                                         int cout) {
+    return ((((size_t)(kk >> 2) * cin + i) * cout + o) << 2) + (size_t)(kk & 3);
+}
+
 // Sets the device error word once (first error wins).
 __device__ __forceinline__ void raise_dev_error(int *err, int code) {
     if (err) atomicCAS(err, 0, code);
@@ -158,6 +165,8 @@ cudaError_t launch_axis_forward(const float2 *in, float2 *out, int64_t outer, in
 cudaError_t launch_axis_inverse(const float2 *in, float2 *out, int64_t outer, int n, int64_t inner,
                                 int m, const float2 *tw, int num_sms, cudaStream_t s);
 cudaError_t launch_mix(const Plan &p, const float2 *X, const void *w, float2 *Y, cudaStream_t s);
+// Standard (nblk, Cin, Cout, m...) weights -> the packed layout.
+cudaError_t launch_pack_weights(const Plan &p, const void *w, void *wp, cudaStream_t s);
 // Truncated forward DFT of nch real images x (storage dtype of p) to their
 // kept modes out[nch][|K|], through the per-axis kernels; sa, sb hold
 // unfused_modes_scratch_elems(g, nch) complex values each.

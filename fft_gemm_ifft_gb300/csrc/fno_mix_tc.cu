@@ -97,7 +97,9 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_tc(MixTcArgs a) {
             q[t] = make_uint4(0, 0, 0, 0);
             if (i0 + t < a.cin)
                 q[t] = __ldg(reinterpret_cast<const uint4 *>(
-                    w + ((((size_t)blk * a.cin + i0 + t) * a.cout + o) * a.mblk + local0) * 2));
+                    a.packed ? w + packed_index(mode0, i0 + t, o, a.cin, a.cout) * 2
+                             : w + ((((size_t)blk * a.cin + i0 + t) * a.cout + o) * a.mblk +
+                                    local0) * 2));
         }
 #pragma unroll
         for (int r = 0; r < kRun; ++r) {

@@ -83,7 +83,7 @@ k_fwd_full(const float2 *__restrict__ in, float2 *__restrict__ out, int64_t oute
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 k_mix(const float2 *__restrict__ X, const T *__restrict__ w, float2 *__restrict__ Y,
-      int64_t batch, int cin, int cout, KeptGeom g) {
+      int64_t batch, int cin, int cout, KeptGeom g, int packed) {
     const int64_t total = batch * cout * g.nkept;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -105,8 +105,9 @@ k_mix(const float2 *__restrict__ X, const T *__restrict__ w, float2 *__restrict_
             stride *= g.m[a];
         }
         const float2 *xs = X + b * cin * g.nkept + kk;
-        const T *ws = w + ((((int64_t)blk * cin) * cout + o) * g.mblk + local) * 2;
-        const int64_t wstride = (int64_t)cout * g.mblk * 2;
+        const T *ws = packed ? w + packed_index(kk, 0, o, cin, cout) * 2
+                             : w + ((((int64_t)blk * cin) * cout + o) * g.mblk + local) * 2;
+        const int64_t wstride = packed ? (int64_t)cout * 4 * 2 : (int64_t)cout * g.mblk * 2;
         float2 acc = make_float2(0.f, 0.f);
         for (int i = 0; i < cin; ++i)
             cfma(acc, xs[(int64_t)i * g.nkept], Storage<T>::load2(ws + i * wstride));
@@ -239,7 +240,8 @@ static cudaError_t unfused_forward_t(const Plan &p, const Buffers &bf, cudaStrea
     kg.nkept = g.nkept;
     kg.mblk = g.mblk;
     k_mix<T><<<grid_for(p.batch * p.cout * g.nkept, sms), kThreads, 0, s>>>(
-        cur, reinterpret_cast<const T *>(bf.w), nxt, p.batch, p.cin, p.cout, kg);
+        cur, reinterpret_cast<const T *>(bf.w), nxt, p.batch, p.cin, p.cout, kg,
+        (p.flags & FNO_PLAN_PACKED_WEIGHTS) ? 1 : 0);
     std::swap(cur, nxt);
     // a3, full axes 0..d-2
     for (int a = 0; a < d - 1; ++a) {
@@ -308,6 +310,59 @@ cudaError_t unfused_forward_modes(const Plan &p, const void *x, int64_t nch, flo
     });
 }
 
+// Packed weights, one destination element per thread (coalesced writes):
+// wp[(q cin + i) cout + o][r] = w[blk(k)][i][o][local(k)], k = 4 q + r
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+k_pack_weights(const T *__restrict__ w, T *__restrict__ wp, int cin, int cout, KeptGeom g) {
+    const int64_t total = g.nkept * cin * cout;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int r = (int)(idx & 3);
+        int64_t t = idx >> 2;
+        const int o = (int)(t % cout);
+        t /= cout;
+        const int i = (int)(t % cin);
+        const int64_t kk = (t / cin) * 4 + r;
+        int64_t rem = kk, local = 0, stride = 1;
+        int blk = 0;
+        for (int a = g.d - 1; a >= 0; --a) {
+            const int64_t rr = rem % g.kdim[a];
+            rem /= g.kdim[a];
+            int64_t l = rr;
+            if (a < g.d - 1 && rr >= g.m[a]) {
+                l = rr - g.m[a];
+                blk |= 1 << a;
+            }
+            local += l * stride;
+            stride *= g.m[a];
+        }
+        const T *src = w + ((((int64_t)blk * cin + i) * cout + o) * g.mblk + local) * 2;
+        wp[idx * 2] = src[0];
+        wp[idx * 2 + 1] = src[1];
+    }
+}
+
+cudaError_t launch_pack_weights(const Plan &p, const void *w, void *wp, cudaStream_t s) {
+    const Geom &g = p.g;
+    KeptGeom kg;
+    kg.d = g.d;
+    for (int a = 0; a < FNO_MAX_NDIM; ++a) {
+        kg.kdim[a] = a < g.d ? g.kdim[a] : 1;
+        kg.m[a] = a < g.d ? g.m[a] : 1;
+    }
+    kg.nkept = g.nkept;
+    kg.mblk = g.mblk;
+    const int grid = grid_for(g.nkept * p.cin * p.cout, p.num_sms);
+    with_storage(p.dtype, [&](auto t) {
+        using T = decltype(t);
+        k_pack_weights<T><<<grid, kThreads, 0, s>>>(static_cast<const T *>(w), static_cast<T *>(wp),
+                                                    p.cin, p.cout, kg);
+        return 0;
+    });
+    return cudaGetLastError();
+}
+
 cudaError_t launch_axis_forward(const float2 *in, float2 *out, int64_t outer, int n, int64_t inner,
                                 int m, const float2 *tw, int num_sms, cudaStream_t s) {
     k_fwd_full<<<grid_for(outer * 2 * m * inner, num_sms), kThreads, 0, s>>>(in, out, outer, n,
@@ -336,7 +391,7 @@ cudaError_t launch_mix(const Plan &p, const float2 *X, const void *w, float2 *Y,
     with_storage(p.dtype, [&](auto t) {
         using T = decltype(t);
         k_mix<T><<<grid, kThreads, 0, s>>>(X, static_cast<const T *>(w), Y, p.batch, p.cin,
-                                          p.cout, kg);
+                                          p.cout, kg, (p.flags & FNO_PLAN_PACKED_WEIGHTS) ? 1 : 0);
         return 0;
     });
     return cudaGetLastError();

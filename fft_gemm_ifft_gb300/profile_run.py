@@ -51,6 +51,8 @@ def main(argv=None) -> int:
     nsets = max(2, math.ceil(2 * l2 / set_bytes))
     xs = [workloads.to_torch_storage(x_np, case.dtype).cuda() for _ in range(nsets)]
     ws = [workloads.to_torch_storage(w_np, case.dtype).cuda() for _ in range(nsets)]
+    if flags & capi.FNO_PLAN_PACKED_WEIGHTS:
+        ws = [conv.pack_weights(w) for w in ws]
     ys = [torch.empty(case.y_shape, dtype=conv.torch_dtype, device="cuda") for _ in range(nsets)]
     step = lambda i: conv(xs[i % nsets], ws[i % nsets], ys[i % nsets])
     if args.backward:

@@ -105,6 +105,13 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * the register-FFT kernel instead of the tensor-core kernel (a kind::f16
  * tcgen05 GEMM per image, the default there).  An ablation switch.          */
 #define FNO_PLAN_SIMT_TRANSFORM 64u
+/* The weights passed to fno_spectral_conv_forward are in the packed
+ * mode-major layout written by fno_spectral_conv_pack_weights (weights are
+ * parameters: pack once per update, use many times).  Packed, every mixing
+ * kernel reads a mode group's Cin x Cout weights as one contiguous run instead
+ * of 16-byte pieces strided by the mode count.  Requires |K| % 4 == 0; not
+ * combinable with FNO_PLAN_BACKWARD.                                        */
+#define FNO_PLAN_PACKED_WEIGHTS 128u
 
 /* One work item of the fused kernel, as recorded under FNO_PLAN_TRACE.
  * Times are the GPU's global nanosecond timer.                              */
@@ -214,6 +221,16 @@ fno_status_t fno_spectral_conv_forward_static(int ndim, const int64_t *n,
                                               int32_t cin, int32_t cout, fno_dtype_t dtype,
                                               const void *x, const void *w, void *y,
                                               fno_stream_t stream);
+
+/* Write w (nblk, Cin, Cout, m...) in the packed layout of the plan's storage
+ * type: w_packed[(q * Cin + i) * Cout + o][r] = W of kept mode k = 4 q + r
+ * (kept modes in the order of the layer's kept-mode index: axis by axis, low
+ * rows then high rows on full axes), interleaved complex; same size as w.
+ * For plans made with FNO_PLAN_PACKED_WEIGHTS.  Asynchronous on `stream`.
+ * Errors: INVALID_ARG (NULL, plan without the flag), MISALIGNED, ALIASING
+ * (w and w_packed overlap), CUDA.                                           */
+fno_status_t fno_spectral_conv_pack_weights(fno_plan_t plan, const void *w, void *w_packed,
+                                            fno_stream_t stream);
 
 /* Gradients of the layer for a real loss L, given dy = dL/dy (B, Cout, N...)
  * in the storage dtype.  The pages define only the forward pass; this is its

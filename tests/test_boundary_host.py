@@ -87,7 +87,7 @@ def test_query_rejects(L, args, code):
 
 
 def test_query_rejects_unknown_flags_and_nulls(L):
-    st, _, _ = Q(1, [16], [4], 1, 1, 1, F32, flags=0x80)
+    st, _, _ = Q(1, [16], [4], 1, 1, 1, F32, flags=0x1000)
     assert st == capi.FNO_ERR_INVALID_ARG
     import ctypes
     assert L.fno_spectral_conv_query(1, None, None, 1, 1, 1, 0, 0, None, None) == \
@@ -154,3 +154,15 @@ def test_backward_flag_adds_workspace(L):
     assert ws1 >= wb + 8 * 32 * 512 * 8 + 8 * 16 * 512 * 8
     st, _, _ = Q(1, [16], [4], 1, 1, 1, F32, flags=capi.FNO_PLAN_BACKWARD | 0x100)
     assert st == capi.FNO_ERR_INVALID_ARG
+
+
+def test_packed_weights_flag_validation(L):
+    P = capi.FNO_PLAN_PACKED_WEIGHTS
+    assert Q(2, [128, 128], [16, 16], 8, 32, 32, F32, flags=P)[0] == capi.FNO_OK
+    assert Q(1, [16], [5], 1, 2, 2, F32, flags=P)[0] == capi.FNO_ERR_INVALID_ARG   # |K| = 5
+    assert Q(1, [16], [8], 1, 2, 2, F32, flags=P | capi.FNO_PLAN_BACKWARD)[0] == \
+        capi.FNO_ERR_INVALID_ARG
+    # same weight bytes in both layouts
+    assert Q(2, [32, 32], [4, 4], 1, 3, 5, F32, flags=P)[2] == \
+        Q(2, [32, 32], [4, 4], 1, 3, 5, F32)[2]
+    assert capi.fno_spectral_conv_pack_weights(None, None, None, None) == capi.FNO_ERR_INVALID_ARG

@@ -222,6 +222,38 @@ def test_trace_three_kernel_variant(name, chunks_a, chunks_c):
     conv.close()
 
 
+PACKED_CASES = [
+    ((256,), (16,), 3, 5, 7, "f32"),               # 1-D cluster kernel
+    ((128, 128), (16, 16), 2, 6, 5, "f32"),        # three-kernel 128^2
+    ((128, 128), (16, 16), 2, 6, 5, "f32", capi.FNO_PLAN_PERSISTENT),
+    ((256, 256), (32, 32), 2, 3, 5, "f16"),        # tensor-core mixing
+    ((256, 256), (32, 32), 1, 4, 4, "bf16", capi.FNO_PLAN_SIMT_MIX),
+    ((64, 64, 64), (16, 16, 16), 1, 3, 2, "f32"),  # 3-D
+    ((16, 32), (3, 8), 2, 3, 5, "f32"),            # separate kernels
+]
+
+
+@pytest.mark.parametrize("spec", PACKED_CASES, ids=[case_id(c[:6]) + ("_f" if len(c) > 6 else "")
+                                                   for c in PACKED_CASES])
+def test_packed_weights_match_oracle(spec):
+    n, modes, b, ci, co, dt = spec[:6]
+    flags = capi.FNO_PLAN_PACKED_WEIGHTS | (spec[6] if len(spec) > 6 else 0)
+    case = workloads.small_case(n, modes, b, ci, co, dt)
+    x = workloads.make_x(case, seed=61)
+    w = workloads.to_storage((workloads.make_w(case, seed=62).astype(np.float64) * ci * co * 2 - 1)
+                             / ci, dt)
+    conv = SpectralConv(n, modes, b, ci, co, dt, flags)
+    W = to_dev(w, dt)
+    wp = conv.pack_weights(W)
+    torch.cuda.synchronize()
+    assert not torch.equal(wp, W) or w.size <= 8
+    y = conv(to_dev(x, dt), wp)
+    torch.cuda.synchronize()
+    assert conv.device_error() == 0
+    assert_close(y.float().cpu().numpy(), run_oracle(case, x, w), dt, "packed weights")
+    conv.close()
+
+
 def test_output_red_zones_untouched():
     case = workloads.small_case((64, 64), (8, 8), 2, 3, 4, "f32")
     x, w = workloads.make_x(case, seed=3), workloads.make_w(case, seed=4)
