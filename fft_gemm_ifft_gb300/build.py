@@ -4,8 +4,7 @@ Each ``csrc/*.cu`` translation unit is compiled by nvcc in parallel, then
 linked into ``fft_gemm_ifft_gb300/libfno.so`` (git-ignored).  The build is
 skipped when the library is newer than every source and header.  Set
 ``FNO_PTXAS_VERBOSE=1`` to print the register / shared-memory report of each
-kernel, ``FNO_DEBUG_BOUNDS=1`` to compile the device index checks in, and
-``FNO_EXTRA_NVCC_FLAGS`` to pass tuning macros (e.g. ``-DFNO_TARGET_GROUPS=4``).
+kernel, and ``FNO_EXTRA_NVCC_FLAGS`` to pass tuning macros (e.g. ``-DFNO_TARGET_GROUPS=4``).
 """
 from __future__ import annotations
 
@@ -49,8 +48,6 @@ def _flags():
     extra = os.environ.get("FNO_EXTRA_NVCC_FLAGS")
     if extra:
         f += extra.split()
-    if os.environ.get("FNO_DEBUG_BOUNDS"):
-        f += ["-DFNO_DEBUG_BOUNDS=1"]
     return f
 
 

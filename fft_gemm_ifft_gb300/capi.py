@@ -45,7 +45,7 @@ EXPORTS = (
     "fno_spectral_conv_workspace_size", "fno_spectral_conv_kernel_count",
     "fno_spectral_conv_forward", "fno_plan_get_device_error", "fno_plan_destroy",
     "fno_spectral_conv_forward_static", "fno_plan_get_trace", "fno_spectral_conv_backward",
-    "fno_spectral_conv_pack_weights",
+    "fno_spectral_conv_pack_weights", "fno_plan_check_bounded_wait",
     "fno_model_plan", "fno_model_workspace_size", "fno_model_kernel_count",
     "fno_forward", "fno_model_get_device_error", "fno_model_destroy",
 )
@@ -116,6 +116,7 @@ def lib() -> ctypes.CDLL:
             L.fno_plan_get_trace.argtypes = [_vp, ctypes.POINTER(fno_trace_record_t),
                                              ctypes.c_size_t, psz]
             L.fno_plan_get_device_error.argtypes = [_vp, _vp]
+            L.fno_plan_check_bounded_wait.argtypes = [_vp, ctypes.c_int, _vp]
             L.fno_plan_destroy.argtypes = [_vp]
             L.fno_model_plan.argtypes = [ctypes.POINTER(_vp), ctypes.POINTER(fno_model_desc_t)]
             L.fno_model_workspace_size.argtypes = [_vp, psz]
@@ -205,6 +206,10 @@ def fno_plan_get_trace(plan, capacity=1 << 16):
 
 def fno_plan_get_device_error(plan, stream):
     return lib().fno_plan_get_device_error(plan, stream)
+
+
+def fno_plan_check_bounded_wait(plan, which, stream):
+    return lib().fno_plan_check_bounded_wait(plan, int(which), stream)
 
 
 def fno_plan_destroy(plan):

@@ -8,13 +8,34 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "fno_internal.cuh"
 #include "fno_fused.cuh"
 
 using namespace fno;
+
+namespace fno {
+
+cudaError_t raise_smem_limit_fn(const void *fn, size_t bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, size_t> limit;   // (device, kernel)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    size_t &cur = limit[{dev, fn}];
+    if (bytes <= cur) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) cur = bytes;
+    return e;
+}
+
+}  // namespace fno
 
 namespace {
 
@@ -393,6 +414,12 @@ fno_status_t fno_plan_get_device_error(fno_plan_t plan, fno_stream_t stream) {
     if (v == kDevTimeout) return FNO_ERR_DEVICE_TIMEOUT;
     if (v == kDevBounds) return FNO_ERR_DEVICE_BOUNDS;
     return FNO_OK;
+}
+
+fno_status_t fno_plan_check_bounded_wait(fno_plan_t plan, int which, fno_stream_t stream) {
+    if (!plan || (which != 0 && which != 1)) return FNO_ERR_INVALID_ARG;
+    const Plan &p = *reinterpret_cast<Plan *>(plan);
+    return from_cuda(launch_wait_check(p, which, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 fno_status_t fno_plan_destroy(fno_plan_t plan) {

@@ -765,7 +765,34 @@ using tcu::encoder;
 using tcu::EncodeTiled;
 
 
+// Self-test of the two bounded waits the fused kernels use.  which 0: thread 0
+// waits on a flag word that nothing sets (the form CTAs use to wait for a
+// phase of another CTA); which 1: thread 0 waits on phase 0 of an mbarrier
+// that nothing arrives on (the form the tensor-core kernels use for TMA and
+// MMA completion).  Each wait must give up within its limit, set the error
+// word to the time-out code and return, leaving the context usable.
+__global__ void k_wait_check(const int *never_set, int *err, int which) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    if (which == 0) {
+        wait_flag(never_set, err);
+    } else {
+        const uint32_t a = tcu::tc_smem_addr(&bar);
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(a) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tcu::mbar_wait(&bar, 0, err);
+        asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(a) : "memory");
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_check(const Plan &p, int which, cudaStream_t s) {
+    // the flag is a word of the error line that no kernel writes
+    const int *never_set = p.dev_err + kLine / 2;
+    k_wait_check<<<1, 32, 0, s>>>(never_set, p.dev_err, which);
+    return cudaGetLastError();
+}
 
 size_t fused_sync_bytes() { return kSyncBytes; }
 
@@ -852,30 +879,23 @@ struct Pdl {
         const int bb = batch_block(p.batch, p.cin, np);
         const size_t sa = Cf::kSmemTw + Cf::kSmemA, sc = CfC::kSmemTw + CfC::kSmemC;
         const size_t sb = smem_b(p.dtype, p.cin, ob + 1, bb, np);   // padded slab rows
-        cudaError_t e = cudaFuncSetAttribute(k_phase_a<Cf, T, kCluster>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa);
+        cudaError_t e = raise_smem_limit(k_phase_a<Cf, T, kCluster>, (int)sa);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(np == 1 ? kernel_b<T, 1>() : kernel_b<T, kParts>(),
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sb);
+            e = raise_smem_limit(np == 1 ? kernel_b<T, 1>() : kernel_b<T, kParts>(), (int)sb);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_phase_c<CfC, T>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
+            e = raise_smem_limit(k_phase_c<CfC, T>, (int)sc);
         if constexpr (!std::is_same<T, float>::value || Cf::N0 == 128) {
             if (e == cudaSuccess && p.fused_tca && !tcu::encoder()) e = cudaErrorNotSupported;
             if (e == cudaSuccess && p.fused_tca) {
                 using Gm = tca::Geo<T>;
-                e = cudaFuncSetAttribute(tca::k_phase_a_tc<T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Gm::kSmem);
+                e = raise_smem_limit(tca::k_phase_a_tc<T>, (int)Gm::kSmem);
                 // the inverse on the tensor cores too, for 16-bit storage
                 std::vector<unsigned char> img, imgc;
                 if (e == cudaSuccess) tca::make_table<T>(img);
                 if constexpr (!std::is_same<T, float>::value) {
                     p.fused_tcc = true;
                     if (e == cudaSuccess)
-                        e = cudaFuncSetAttribute(tca::k_phase_c_tc<T>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)tca::GeoC<T>::kSmem);
+                        e = raise_smem_limit(tca::k_phase_c_tc<T>, (int)tca::GeoC<T>::kSmem);
                     tca::make_table_c<T>(imgc);
                 }
                 const size_t off_c = (img.size() + 255) & ~size_t(255);
@@ -1119,8 +1139,7 @@ cudaError_t fused_plan_init(Plan &p) {
     const BShape bs = b_shape(p.dtype, p.batch, p.cin, p.cout);
     const size_t smem = smem_bytes(p.dtype, p.cin, bs);
     void *fn = p.dtype == FNO_F32 ? kernel_ptr<float>() : kernel_ptr<__half>();
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = raise_smem_limit(fn, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kNT, smem);

@@ -287,16 +287,11 @@ struct Pdl3 {
     template <typename T>
     static cudaError_t init(Plan &p) {
         const int ob = out_block(p.dtype, p.cin, p.cout), bb = batch_block(p.batch, p.cin);
-        cudaError_t e = cudaFuncSetAttribute(k_phase_a3<C3, T>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)C3::template smem_a<T>());
+        cudaError_t e = raise_smem_limit(k_phase_a3<C3, T>, (int)C3::template smem_a<T>());
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_phase_b<C3, T, 1, kNT>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem_b(p.dtype, p.cin, ob + 1, bb));
+            e = raise_smem_limit(k_phase_b<C3, T, 1, kNT>, smem_b(p.dtype, p.cin, ob + 1, bb));
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_phase_c3<C3, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)C3::kSmemC);
+            e = raise_smem_limit(k_phase_c3<C3, T>, (int)C3::kSmemC);
         p.fused_bb = bb;
         p.fused_ob = ob;
         p.fused_smem = smem_b(p.dtype, p.cin, ob + 1, bb);   // padded slab rows

@@ -167,6 +167,17 @@ cudaError_t launch_axis_inverse(const float2 *in, float2 *out, int64_t outer, in
 cudaError_t launch_mix(const Plan &p, const float2 *X, const void *w, float2 *Y, cudaStream_t s);
 // Standard (nblk, Cin, Cout, m...) weights -> the packed layout.
 cudaError_t launch_pack_weights(const Plan &p, const void *w, void *wp, cudaStream_t s);
+// A kernel's dynamic shared-memory limit is an attribute of the process (per
+// device), not of a plan: plans only ever raise it, so that a plan made later
+// with a smaller need cannot break the launches of an earlier, larger one.
+cudaError_t raise_smem_limit_fn(const void *fn, size_t bytes);
+template <typename F>
+cudaError_t raise_smem_limit(F fn, size_t bytes) {
+    return raise_smem_limit_fn((const void *)fn, bytes);
+}
+
+// one CTA runs a bounded wait that nothing satisfies (which 0: flag, 1: mbarrier)
+cudaError_t launch_wait_check(const Plan &p, int which, cudaStream_t s);
 // Truncated forward DFT of nch real images x (storage dtype of p) to their
 // kept modes out[nch][|K|], through the per-axis kernels; sa, sb hold
 // unfused_modes_scratch_elems(g, nch) complex values each.

@@ -258,8 +258,7 @@ cudaError_t mixtc_init(fno_dtype_t dtype) {
         if constexpr (std::is_same<T, float>::value) {
             return cudaErrorInvalidValue;
         } else {
-            return cudaFuncSetAttribute(k_mix_tc<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kSmem);
+            return raise_smem_limit(k_mix_tc<T>, (int)kSmem);
         }
     });
 }

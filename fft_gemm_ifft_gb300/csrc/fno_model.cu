@@ -478,10 +478,8 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
         return st;
     }
     const int smem = (int)sizeof(TileSmem);
-    if (cudaFuncSetAttribute(k_linear_tiled, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess ||
-        cudaFuncSetAttribute(projection_kernel(d->cout),
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+    if (raise_smem_limit(k_linear_tiled, smem) != cudaSuccess ||
+        raise_smem_limit(projection_kernel(d->cout), smem) != cudaSuccess) {
         cudaGetLastError();
         fno_plan_destroy(m->spec);
         delete m;
@@ -497,7 +495,7 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
         if (!lintc::eligible(cin, n)) return true;
         const size_t sb = lintc::smem_map(cin, n).total;
         int per_sm = 0;
-        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sb) !=
+        if (raise_smem_limit(fn, (int)sb) !=
                 cudaSuccess ||
             cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
                 cudaSuccess ||

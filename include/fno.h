@@ -56,7 +56,7 @@ typedef enum fno_status_e {
     FNO_ERR_OUT_OF_MEMORY = 4,   /* plan-owned device or host memory could not be had    */
     FNO_ERR_CUDA = 5,            /* a CUDA runtime call or kernel launch failed          */
     FNO_ERR_DEVICE_TIMEOUT = 6,  /* a bounded device-side wait gave up                   */
-    FNO_ERR_DEVICE_BOUNDS = 7,   /* a device-side index check failed (debug builds)      */
+    FNO_ERR_DEVICE_BOUNDS = 7,   /* reserved: a device index check (none in this version) */
     FNO_ERR_ALIASING = 8         /* the output overlaps an input or the workspace        */
 } fno_status_t;
 
@@ -264,6 +264,17 @@ fno_status_t fno_plan_get_trace(fno_plan_t plan, fno_trace_record_t *records, si
 /* Synchronise `stream`, then read and clear the plan's device error word.
  * Returns FNO_OK, FNO_ERR_DEVICE_TIMEOUT, FNO_ERR_DEVICE_BOUNDS or CUDA.   */
 fno_status_t fno_plan_get_device_error(fno_plan_t plan, fno_stream_t stream);
+
+/* Self-test of the bounded device waits.  Launches one CTA on `stream` that
+ * waits for something no one will do -- which = 0: a flag word in the plan's
+ * memory that no kernel writes (the wait CTAs of one launch use for each
+ * other's phases); which = 1: phase 0 of an mbarrier nothing arrives on (the
+ * wait of the tensor-core kernels for TMA and MMA completion).  The wait gives
+ * up after its limit (0.5 s), sets the plan's device error word and returns,
+ * so the next fno_plan_get_device_error returns FNO_ERR_DEVICE_TIMEOUT and the
+ * context stays usable.  Asynchronous; no allocation.  Errors: INVALID_ARG
+ * (NULL plan, `which` not 0 or 1), CUDA (launch failed).                    */
+fno_status_t fno_plan_check_bounded_wait(fno_plan_t plan, int which, fno_stream_t stream);
 
 /* Release the plan and its device memory.  NULL is accepted (no-op).  The
  * caller must make sure no work that uses the plan is still running.       */
