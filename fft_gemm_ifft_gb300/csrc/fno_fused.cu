@@ -350,6 +350,7 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
     const uint32_t tmem = s_tmem;
     bool ok = mbar_wait(&bar_t, 0, a.err);
     ok &= mbar_wait(&bar_x, 0, a.err);
+    const unsigned long long t_x = a.trace ? trace_now() : 0;     // the image has landed
     const uint32_t xs = tc_smem_addr(base), ts = tc_smem_addr(base + Gm::kT);
     if (tid == 0) {
         tc_after_sync();
@@ -402,6 +403,7 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
         ok &= mbar_wait(&bar_mma, 1, a.err);
     }
     tc_after_sync();
+    const unsigned long long t_z = a.trace ? trace_now() : 0;     // the row DFT is done
     // Z planes (re, im) from tensor memory into the region the tile occupied:
     // warps w and w + 4 read the same lanes, the first the re, the second the im half
     float *zr = reinterpret_cast<float *>(base);
@@ -457,7 +459,7 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(Gm::kTmemCols));
     }
-    cta_record(a, 0, 0, t0, t0);
+    cta_record(a, 0, 0, t0, t_x, t_z);
 }
 
 // ---------------------------------------------------------------------------
@@ -702,6 +704,205 @@ void make_table(std::vector<unsigned char> &img) {
         }
 }
 
+// ---------------------------------------------------------------------------
+// Kernel C on the tensor cores for fp32 128 x 128 layers (16 x 16 modes per
+// block): one CTA inverts a whole output image, two CTAs per SM.
+//   1. column inverse on the SIMT cores.  The kept rows are the signed
+//      frequencies g = -16 .. 15; with g = g1 + 8 g2 (g1 = 0..7, g2 = -2..1) and
+//      t = t1 + 16 t2, Zo[t][k] = sum_g V[g][k] e^{+2 pi i g t / 128} becomes
+//      U[g1][t1][k] = sum_g2 V[g1 + 8 g2][k] e^{+2 pi i (g1 + 8 g2) t1 / 128}
+//      (four terms) followed by 8-point inverse register FFTs over g1 for
+//      every (t1, k);
+//   2. row inverse as the GEMM y = Zo' . T^T with Zo' = [Re Zo | Im Zo] (K = 32)
+//      and T[n] = s [c(k) cos(2 pi k n / 128) | -c(k) sin(...)], s = 1/128^2, in
+//      three kind::tf32 passes (Zo_hi T_hi + Zo_hi T_lo + Zo_lo T_hi, hi/lo the
+//      tf32 head of a float and the exact remainder), N = 128 outputs in tensor
+//      memory;
+//   3. the 128 x 128 tile leaves through four swizzled 32-column staging boxes
+//      (over the operands, free once the MMAs completed) by TMA stores.
+// ---------------------------------------------------------------------------
+struct GeoC32 {
+    static constexpr int N0 = 128, N1 = 128, M0 = 16, M1 = 16, K0 = 32, NK = K0 * M1;
+    static constexpr int G1 = 8, T1 = N0 / G1;          // g = g1 + 8 g2, t = t1 + 16 t2
+    static constexpr uint32_t kTile = 16384;            // 128 rows x 128 bytes
+    static constexpr uint32_t kT = 0;                   // T hi, T lo (B operands)
+    static constexpr uint32_t kTBytes = 2 * kTile;
+    static constexpr uint32_t kA = kT + kTBytes;        // Zo' hi, Zo' lo (A operands)
+    static constexpr uint32_t kS = kA + 2 * kTile;      // U[G1][T1][M1]
+    static constexpr uint32_t kY = kS + G1 * T1 * M1 * 8;
+    static constexpr uint32_t kTw = kY + NK * 8;
+    static constexpr uint32_t kSmem = kTw + N0 * 8 + 1024;
+    static constexpr uint32_t kStage = 0;               // 4 output boxes over T and A
+    static constexpr uint32_t kTmemCols = 128;
+    static_assert(kS >= 4 * kTile, "staging boxes fit over the operands");
+};
+
+__global__ void __launch_bounds__(NT, 2)
+k_phase_c_tc32(const __grid_constant__ CUtensorMap ymap, Args a, const void *table) {
+    using Gm = GeoC32;
+    using namespace tcu;
+    extern __shared__ __align__(1024) char smem_raw[];
+    char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+    __shared__ __align__(8) uint64_t bar_t, bar_mma;
+    __shared__ uint32_t s_tmem;
+    const unsigned long long t0 = a.trace ? trace_now() : 0;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int img = blockIdx.x;
+    float2 *ys = reinterpret_cast<float2 *>(base + Gm::kY);
+    float2 *S = reinterpret_cast<float2 *>(base + Gm::kS);
+    float2 *tw = reinterpret_cast<float2 *>(base + Gm::kTw);
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_t)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_mma)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     ::"r"(tc_smem_addr(&bar_t)), "r"(Gm::kTBytes) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(tc_smem_addr(base + Gm::kT)), "l"(table), "r"(Gm::kTBytes),
+                     "r"(tc_smem_addr(&bar_t)) : "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(tc_smem_addr(&s_tmem)), "r"(Gm::kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    for (int e = tid; e < Gm::N0; e += NT) tw[e] = a.tw0[e];
+    tc_before_sync();
+    __syncthreads();
+    tc_after_sync();
+    const uint32_t tmem = s_tmem;
+    pdl_wait();                                  // kernel B's mixed modes are complete
+    const unsigned long long t1 = a.trace ? trace_now() : 0;
+    const float2 *src = a.Y + (size_t)img * Gm::NK;
+    for (int e = tid; e < Gm::NK / 2; e += NT) cp_async16(ys + 2 * e, src + 2 * e);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    // 1. U[g1][t1][k0..k0+3]: kept row j holds g = j (j < 16) or j - 32
+    for (int u = tid; u < Gm::G1 * Gm::T1 * (Gm::M1 / 4); u += NT) {
+        const int k0 = 4 * (u % (Gm::M1 / 4)), t1 = (u / (Gm::M1 / 4)) % Gm::T1;
+        const int g1 = u / (Gm::M1 / 4 * Gm::T1);
+        float2 acc[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int g2 = -2; g2 < 2; ++g2) {
+            const int g = g1 + 8 * g2, j = g < 0 ? g + Gm::K0 : g;
+            const float2 wv = tw[(g * t1) & (Gm::N0 - 1)];        // e^{-2 pi i g t1 / 128}
+            const float2 wc = make_float2(wv.x, -wv.y);
+            const float4 *y4 = reinterpret_cast<const float4 *>(ys + j * Gm::M1 + k0);
+            const float4 p0 = y4[0], p1 = y4[1];
+            cmac(acc[0], make_float2(p0.x, p0.y), wc);
+            cmac(acc[1], make_float2(p0.z, p0.w), wc);
+            cmac(acc[2], make_float2(p1.x, p1.y), wc);
+            cmac(acc[3], make_float2(p1.z, p1.w), wc);
+        }
+        float4 *d = reinterpret_cast<float4 *>(S + (g1 * Gm::T1 + t1) * Gm::M1 + k0);
+        d[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+        d[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+    }
+    __syncthreads();
+    // 2. Zo[t1 + 16 t2][k] = sum_g1 e^{+2 pi i g1 t2 / 8} U[g1][t1][k], split into the
+    //    tf32 head and remainder and written as the K-major operands: columns
+    //    0..15 the real parts, 16..31 the imaginary
+    char *Ahi = base + Gm::kA, *Alo = Ahi + Gm::kTile;
+    for (int u = tid; u < Gm::T1 * Gm::M1; u += NT) {
+        const int k = u % Gm::M1, t1 = u / Gm::M1;
+        float2 z[Gm::G1];
+#pragma unroll
+        for (int g1 = 0; g1 < Gm::G1; ++g1) z[g1] = S[(g1 * Gm::T1 + t1) * Gm::M1 + k];
+        fft::fft_dif<Gm::G1, 1>(z);
+#pragma unroll
+        for (int t2 = 0; t2 < Gm::G1; ++t2) {
+            const float2 v = z[fft::bitrev(t2, fft::ilog2(Gm::G1))];
+            const int t = t1 + Gm::T1 * t2;
+            const uint32_t ore = sw_off(t, k), oim = sw_off(t, Gm::M1 + k);
+            *reinterpret_cast<float *>(Ahi + ore) = v.x;
+            *reinterpret_cast<float *>(Ahi + oim) = v.y;
+            *reinterpret_cast<float *>(Alo + ore) = tf32_lo(v.x);
+            *reinterpret_cast<float *>(Alo + oim) = tf32_lo(v.y);
+        }
+    }
+    fence_async_smem();
+    tc_before_sync();
+    __syncthreads();
+    bool ok = mbar_wait(&bar_t, 0, a.err);
+    if (tid == 0) {
+        tc_after_sync();
+        constexpr uint32_t id = idesc_tf32(Gm::N1);
+        const uint32_t ah = tc_smem_addr(Ahi), al = tc_smem_addr(Alo);
+        const uint32_t th = tc_smem_addr(base + Gm::kT), tl = th + Gm::kTile;
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            mma_tf32(tmem, desc_sw128(ah + s * 32), desc_sw128(th + s * 32), id, s ? 1u : 0u);
+            mma_tf32(tmem, desc_sw128(ah + s * 32), desc_sw128(tl + s * 32), id, 1u);
+            mma_tf32(tmem, desc_sw128(al + s * 32), desc_sw128(th + s * 32), id, 1u);
+        }
+        mma_commit(&bar_mma);
+    }
+    ok &= mbar_wait(&bar_mma, 0, a.err);
+    tc_after_sync();
+    const unsigned long long t_m = a.trace ? trace_now() : 0;
+    // 3. warp w reads lanes 32 (w % 4).. of tensor memory (the image rows), the two
+    //    warp halves columns 0..63 and 64..127, into boxes 2h and 2h + 1
+    {
+        const int half = warp >> 2, lrow = 32 * (warp & 3) + (tid & 31);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            float v[16];
+            tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 64 * half + 16 * g, v);
+            char *box = base + Gm::kStage + (2 * half + (g >> 1)) * Gm::kTile;
+            const int col0 = 16 * (g & 1);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<float4 *>(box + sw_off(lrow, col0 + 4 * q)) =
+                    ok ? make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3])
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    fence_async_smem();
+    tc_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+        for (int b = 0; b < 4; ++b)
+            tma_store_2d(&ymap, 32 * b, img * Gm::N0,
+                         tc_smem_addr(base + Gm::kStage + b * Gm::kTile));
+        bulk_commit();
+        bulk_wait_read();                        // the staging boxes may be released
+    }
+    __syncthreads();
+    if (warp == 0) {
+        tc_after_sync();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(Gm::kTmemCols));
+    }
+    cta_record(a, 2, a.trace_c, t0, t1, t_m);   // compute: the row-inverse MMAs are done
+}
+
+// Host: the fp32 inverse row-DFT operand, [hi, lo][n][k] (k < 16: cos, else
+// -sin), with c(k) and the output scale 1/128^2 folded in, computed in double.
+void make_table_c32(std::vector<unsigned char> &img) {
+    using Gm = GeoC32;
+    using tcu::sw_off;
+    using tcu::tf32_lo;
+    img.assign(Gm::kTBytes, 0);
+    const double two_pi = 2.0 * M_PI, s = 1.0 / ((double)Gm::N0 * (double)Gm::N1);
+    for (int n = 0; n < Gm::N1; ++n)
+        for (int k = 0; k < Gm::M1; ++k) {
+            const double ck = (k == 0 || 2 * k == Gm::N1) ? 1.0 : 2.0;
+            const double ang = two_pi * (double)k * (double)n / (double)Gm::N1;
+            const double v[2] = {s * ck * std::cos(ang), -s * ck * std::sin(ang)};
+            for (int h = 0; h < 2; ++h) {
+                const float hi = (float)v[h];
+                const float lo = (float)(v[h] - (double)(hi - tf32_lo(hi)));
+                const uint32_t off = sw_off(n, h * Gm::M1 + k);
+                memcpy(&img[off], &hi, 4);
+                memcpy(&img[Gm::kTile + off], &lo, 4);
+            }
+        }
+}
+
 }  // namespace tca
 
 // ---------------------------------------------------------------------------
@@ -850,6 +1051,12 @@ struct Pdl {
         return dt == FNO_F32 ? (flags & FNO_PLAN_TENSOR_CORES) != 0
                              : (flags & FNO_PLAN_SIMT_TRANSFORM) == 0;
     }
+    // Whether kernel C runs on the tensor cores: 16-bit 256 x 256 together with
+    // kernel A; fp32 128 x 128 by default (FNO_PLAN_SIMT_TRANSFORM opts out)
+    static bool use_tcc(fno_dtype_t dt, uint32_t flags) {
+        if (!tca_shape<CfC>(dt) || (flags & FNO_PLAN_SIMT_TRANSFORM)) return false;
+        return dt == FNO_F32 ? true : use_tca(dt, flags);
+    }
     // partial copies of the kept modes kernel A leaves (one from the tensor-core kernel)
     static int parts(fno_dtype_t dt, uint32_t flags) { return use_tca(dt, flags) ? 1 : kParts; }
     static int batch_block(int64_t batch, int cin, int np) {
@@ -885,22 +1092,27 @@ struct Pdl {
         if (e == cudaSuccess)
             e = raise_smem_limit(k_phase_c<CfC, T>, (int)sc);
         if constexpr (!std::is_same<T, float>::value || Cf::N0 == 128) {
-            if (e == cudaSuccess && p.fused_tca && !tcu::encoder()) e = cudaErrorNotSupported;
+            p.fused_tcc = use_tcc(p.dtype, p.flags);
+            if (e == cudaSuccess && (p.fused_tca || p.fused_tcc) && !tcu::encoder())
+                e = cudaErrorNotSupported;
+            std::vector<unsigned char> img, imgc;
             if (e == cudaSuccess && p.fused_tca) {
-                using Gm = tca::Geo<T>;
-                e = raise_smem_limit(tca::k_phase_a_tc<T>, (int)Gm::kSmem);
-                // the inverse on the tensor cores too, for 16-bit storage
-                std::vector<unsigned char> img, imgc;
-                if (e == cudaSuccess) tca::make_table<T>(img);
-                if constexpr (!std::is_same<T, float>::value) {
-                    p.fused_tcc = true;
-                    if (e == cudaSuccess)
-                        e = raise_smem_limit(tca::k_phase_c_tc<T>, (int)tca::GeoC<T>::kSmem);
+                e = raise_smem_limit(tca::k_phase_a_tc<T>, (int)tca::Geo<T>::kSmem);
+                tca::make_table<T>(img);
+            }
+            if (e == cudaSuccess && p.fused_tcc) {
+                if constexpr (std::is_same<T, float>::value) {
+                    e = raise_smem_limit(tca::k_phase_c_tc32, (int)tca::GeoC32::kSmem);
+                    tca::make_table_c32(imgc);
+                } else {
+                    e = raise_smem_limit(tca::k_phase_c_tc<T>, (int)tca::GeoC<T>::kSmem);
                     tca::make_table_c<T>(imgc);
                 }
+            }
+            if (e == cudaSuccess && (p.fused_tca || p.fused_tcc)) {
                 const size_t off_c = (img.size() + 255) & ~size_t(255);
-                if (e == cudaSuccess) e = cudaMalloc(&p.fused_tables, off_c + imgc.size());
-                if (e == cudaSuccess)
+                e = cudaMalloc(&p.fused_tables, off_c + imgc.size());
+                if (e == cudaSuccess && !img.empty())
                     e = cudaMemcpy(p.fused_tables, img.data(), img.size(),
                                    cudaMemcpyHostToDevice);
                 if (e == cudaSuccess && !imgc.empty())
@@ -1028,6 +1240,21 @@ struct Pdl {
         if (e != cudaSuccess) return e;
         cfg.gridDim = dim3(nC);
         cfg.blockDim = dim3(kNT);
+        if constexpr (std::is_same<T, float>::value && CfC::N0 == 128) {
+            if (p.fused_tcc) {
+                using Gc = tca::GeoC32;
+                CUtensorMap ymap;
+                if (!tcu::encode_rows_tiled(&ymap, a.y, (int64_t)p.batch * p.cout * Gc::N0,
+                                            Gc::N1, sizeof(float), 32, tcu::tma_type<float>()))
+                    return cudaErrorInvalidValue;
+                cfg.blockDim = dim3(tca::NT);
+                cfg.dynamicSmemBytes = Gc::kSmem;
+                const void *tab = static_cast<const char *>(p.fused_tables) + p.fused_table_c;
+                e = cudaLaunchKernelEx(&cfg, tca::k_phase_c_tc32, ymap, a, tab);
+                if (e != cudaSuccess) return e;
+                return cudaGetLastError();
+            }
+        }
         if constexpr (!std::is_same<T, float>::value) {
             if (p.fused_tcc) {
                 using Gc = tca::GeoC<T>;

@@ -27,6 +27,9 @@ def main(argv=None) -> int:
     ap.add_argument("--trace", default="", help="write the last call's work-item trace "
                     "(CSV) here and print a per-phase summary")
     ap.add_argument("--time", action="store_true", help="time each forward with CUDA events")
+    ap.add_argument("--sets", type=int, default=0,
+                    help="input sets rotated over (default: enough to cover twice the L2; "
+                         "1 keeps the inputs L2-resident)")
     ap.add_argument("--backward", action="store_true",
                     help="run (and time) fno_spectral_conv_backward (dx and dw) instead")
     args = ap.parse_args(argv)
@@ -48,7 +51,7 @@ def main(argv=None) -> int:
     x_np, w_np = workloads.make_x(case), workloads.make_w(case)
     set_bytes = x_np.nbytes + w_np.nbytes + math.prod(case.y_shape) * case.elem_bytes
     l2 = int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 0)) or (126 << 20)
-    nsets = max(2, math.ceil(2 * l2 / set_bytes))
+    nsets = args.sets or max(2, math.ceil(2 * l2 / set_bytes))
     xs = [workloads.to_torch_storage(x_np, case.dtype).cuda() for _ in range(nsets)]
     ws = [workloads.to_torch_storage(w_np, case.dtype).cuda() for _ in range(nsets)]
     if flags & capi.FNO_PLAN_PACKED_WEIGHTS:

@@ -101,9 +101,12 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * (2-D fp16 / bf16 layers with at most 64 channels and 64 samples; the
  * tensor-core kernel is the default there).  An ablation switch.            */
 #define FNO_PLAN_SIMT_MIX 32u
-/* Run the forward transform of the 16-bit 256x256 layer (32x32 modes) with
- * the register-FFT kernel instead of the tensor-core kernel (a kind::f16
- * tcgen05 GEMM per image, the default there).  An ablation switch.          */
+/* Run the transforms on the register-FFT kernels instead of the tensor-core
+ * kernels that are the default for these shapes: for the 16-bit 256x256
+ * layer (32x32 modes) both the forward transform (a kind::f16 tcgen05 GEMM
+ * per image) and the inverse (a kind::tf32 GEMM per image); for the float32
+ * 128x128 layer (16x16 modes) the inverse (a 3xTF32 GEMM per image, TMA
+ * stores).  An ablation switch.                                             */
 #define FNO_PLAN_SIMT_TRANSFORM 64u
 /* The weights passed to fno_spectral_conv_forward are in the packed
  * mode-major layout written by fno_spectral_conv_pack_weights (weights are
