@@ -1034,6 +1034,11 @@ bool tca_shape(fno_dtype_t dt) {
     return Cf::N0 == 256 && Cf::N1 == 256 && Cf::M0 == 32 && Cf::M1 == 32;
 }
 
+#ifndef FNO_PDL_XP_BUDGET
+#define FNO_PDL_XP_BUDGET (64u << 10)
+#endif
+constexpr size_t kPdlXpBudget = FNO_PDL_XP_BUDGET;   // kernel B's partial modes (bytes)
+
 template <class Cf, class CfC = Cf>
 struct Pdl {
     static constexpr bool kCluster = Cf::N0 >= 256;
@@ -1061,7 +1066,7 @@ struct Pdl {
     static int parts(fno_dtype_t dt, uint32_t flags) { return use_tca(dt, flags) ? 1 : kParts; }
     static int batch_block(int64_t batch, int cin, int np) {
         int bb = (int)batch;
-        while (bb > 1 && (size_t)np * bb * cin * 16 > kXpBudget) bb = (bb + 1) / 2;
+        while (bb > 1 && (size_t)np * bb * cin * 16 > kPdlXpBudget) bb = (bb + 1) / 2;
         return bb;
     }
     static size_t smem_b(fno_dtype_t dt, int cin, int ob, int bb, int np) {

@@ -302,18 +302,24 @@ k_linear_tc(const float *__restrict__ a, const float *__restrict__ W,
     const uint32_t tmem = s_tmem;
     constexpr uint32_t idesc = idesc_tf32(n);
     const int64_t ptiles = (npix + kRows - 1) / kRows;
+    const int i0 = quarter * kCinT;
+    // activation tile, transposed: row = pixel, K = input channel; this thread's
+    // quarter of the channels.  The next tile's loads are issued before the
+    // current tile's MMAs are waited for, so they land under its epilogue.
+    float av[kCinT];
+    auto load_tile = [&](int64_t t) {
+        const int64_t tb = t / ptiles, tp = (t % ptiles) * kRows + row;
+        const bool tin = t < ntiles && tp < npix;
+        const float *ab = a + (tb * cin + i0) * npix + tp;
+#pragma unroll
+        for (int i = 0; i < kCinT; ++i) av[i] = tin ? __ldcs(ab + (int64_t)i * npix) : 0.f;
+    };
+    load_tile(blockIdx.x);
     uint32_t phase = 0;
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int64_t b = tile / ptiles, p0 = (tile % ptiles) * kRows;
         const int64_t p = p0 + row;
         const bool pin = p < npix;
-        // activation tile, transposed: row = pixel, K = input channel; this
-        // thread's quarter of the channels, every load in flight before a store
-        const int i0 = quarter * kCinT;
-        const float *ab = a + (b * cin + i0) * npix + p;
-        float av[kCinT];
-#pragma unroll
-        for (int i = 0; i < kCinT; ++i) av[i] = pin ? __ldcs(ab + (int64_t)i * npix) : 0.f;
 #pragma unroll
         for (int i4 = 0; i4 < kCinT / 4; ++i4) {
             const int i = i0 + 4 * i4;
@@ -343,6 +349,7 @@ k_linear_tc(const float *__restrict__ a, const float *__restrict__ W,
             }
             mma_commit(&bar);
         }
+        load_tile(tile + gridDim.x);    // av is in shared memory: prefetch the next tile
         // this thread's column groups (quarter q takes groups q, q + 4, ...)
         const bool has_cols = quarter < NG;
         // the spectral sums of these outputs are fetched while the MMAs run
@@ -503,6 +510,19 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
                 cudaSuccess)
             return false;
         if (per_sm < 1) return true;
+        // the occupancy query can under-count here; two CTAs fit when their
+        // shared memory (dynamic, static, reserved) and registers do
+        cudaFuncAttributes fa;
+        int smem_sm = 0, reserved = 0;
+        if (cudaFuncGetAttributes(&fa, fn) == cudaSuccess &&
+            cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) ==
+                cudaSuccess &&
+            cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) ==
+                cudaSuccess &&
+            2 * (sb + fa.sharedSizeBytes + (size_t)reserved) <= (size_t)smem_sm &&
+            2 * fa.numRegs * lintc::kThreads <= 65536)
+            per_sm = std::max(per_sm, 2);
+        cudaGetLastError();
         const int64_t g = std::min<int64_t>(ntiles, (int64_t)sms * per_sm);
         *grid = (int)g;
         *smem_bytes = sb;
