@@ -1135,6 +1135,7 @@ struct Pdl {
                         mixtc_supported(p.g.d, p.dtype, p.batch, p.cin, p.cout, Cf::M1,
                                         p.g.nkept);
         if (e == cudaSuccess && p.fused_mixtc) e = mixtc_init(p.dtype);
+
         if (e == cudaSuccess && (p.flags & FNO_PLAN_TRACE)) {
             const size_t nB = p.fused_mixtc ? (size_t)mixtc_items(p.g.nkept)
                                             : (size_t)(p.g.nkept / kG) * ((p.cout + ob - 1) / ob) *

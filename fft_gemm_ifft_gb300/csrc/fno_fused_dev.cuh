@@ -178,6 +178,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
+
 // Thread 0 waits until *flag != 0; gives up (sets the error word) after
 // kWaitTimeoutNs or as soon as another CTA has reported an error.
 __device__ bool wait_flag(const int *flag, int *err) {
@@ -434,17 +435,27 @@ __device__ void phase_b_weights(const G &grp, const T *__restrict__ w, int cin, 
     int blk, local;
     Cf::wmap(it.pair * kG, blk, local);          // the pair is adjacent in its block
     W2 *ws = reinterpret_cast<W2 *>(smem);                   // [cin][ob]
-    for (int e = grp.tid; e < cin * it.nob; e += NT) {
-        const int o = e % it.nob, i = e / it.nob;
-        // the pair's two modes are adjacent in both layouts (the pair starts at an
-        // even kept index: within one group of four when packed)
-        const T *p = packed
-                         ? w + packed_index(it.pair * kG, i, it.o0 + o, cin, cout) * 2
-                         : w + ((((size_t)blk * cin + i) * cout + it.o0 + o) * Cf::MBLK + local) * 2;
+    // element e = i * nob + o of the slab; a thread steps by NT elements, with
+    // the divisions done once
+    const int nob = it.nob;
+    int i = grp.tid / nob, o = grp.tid - i * nob;
+    const int di = NT / nob, dO = NT - di * nob;
+    // the pair's two modes are adjacent in both layouts (the pair starts at an even
+    // kept index: within one group of four when packed)
+    const T *base = w + (((size_t)blk * cin * cout + it.o0) * Cf::MBLK + local) * 2;
+    while (i < cin) {
+        const T *p = packed ? w + packed_index(it.pair * kG, i, it.o0 + o, cin, cout) * 2
+                            : base + (size_t)(i * cout + o) * (Cf::MBLK * 2);
         if constexpr (sizeof(W2) == 16)
             cp_async16(ws + i * ob + o, p);
         else
             cp_async8(ws + i * ob + o, p);
+        i += di;
+        o += dO;
+        if (o >= nob) {
+            o -= nob;
+            ++i;
+        }
     }
     cp_async_commit();
 }
@@ -525,36 +536,52 @@ __device__ void phase_b_tiles(const G &grp, float2 *__restrict__ Y, int cin, int
     }
 }
 
-template <class Cf, typename T, int NT, class G, int kParts = Cf::C>
-__device__ void phase_b(const G &grp, const float2 *__restrict__ part, float2 *__restrict__ Y, int cin,
-                        int cout, int nimg_in, const BItem &it, int ob, char *smem,
-                        unsigned long long *t_loaded = nullptr) {
-    using W2 = typename Io<T>::W2;
-    constexpr int NK = Cf::NK, C = kParts;
+// The partial modes of the item's rows into xp: xp[cc][r] = X_cc[b0*cin + r][mode0 ..
+// mode0+1] for the kParts partial copies (issued, not committed)
+template <class Cf, int NT, class G, int kParts = Cf::C>
+__device__ __forceinline__ void phase_b_issue_parts(const G &grp, const float2 *__restrict__ part,
+                                                    int cin, int nimg_in, const BItem &it,
+                                                    float4 *xp) {
+    constexpr int NK = Cf::NK;
     const int mode0 = it.pair * kG;
-    const W2 *ws = reinterpret_cast<const W2 *>(smem);                       // [cin][ob]
-    float4 *xp = reinterpret_cast<float4 *>(smem + ((size_t)cin * ob * sizeof(W2) + 15) / 16 * 16);
-    const int tid = grp.tid;
     const int nr = it.nbb * cin;                         // rows (b, i) of this item
-    // partial modes of the C chunks: xp[cc][r] = X_cc[b0*cin + r][mode0 .. mode0+1]
-    for (int e = tid; e < C * nr; e += NT) {
-        const int r = e % nr, cc = e / nr;
-        cp_async16(xp + e, part + ((size_t)cc * nimg_in + (size_t)it.b0 * cin + r) * NK + mode0);
-    }
-    cp_async_commit();
-    cp_async_wait_all();                                 // also covers the weight slab
-    grp.sync();
-    if (t_loaded && tid == 0) *t_loaded = (unsigned long long)globaltimer();
-    for (int r = tid; r < nr; r += NT) {
-        float4 s = xp[r];
 #pragma unroll
-        for (int cc = 1; cc < C; ++cc) {
-            const float4 q = xp[cc * nr + r];
-            s.x += q.x; s.y += q.y; s.z += q.z; s.w += q.w;
-        }
-        xp[r] = s;
+    for (int cc = 0; cc < kParts; ++cc) {
+        const float2 *src = part + ((size_t)cc * nimg_in + (size_t)it.b0 * cin) * NK + mode0;
+        for (int r = grp.tid; r < nr; r += NT) cp_async16(xp + cc * nr + r, src + (size_t)r * NK);
     }
-    grp.sync();
+}
+
+// byte offset of the partial modes behind the weight slab [cin][ob] in an item's
+// shared memory
+template <typename T>
+__host__ __device__ inline size_t b_xp_offset(int cin, int ob) {
+    return ((size_t)cin * ob * sizeof(typename Io<T>::W2) + 15) / 16 * 16;
+}
+
+// Given the item's weight slab and partials in shared memory (visible to the
+// group): sum the partials, then the register tiles and the stores of Y.
+template <class Cf, typename T, int NT, class G, int kParts = Cf::C>
+__device__ void phase_b_compute(const G &grp, float2 *__restrict__ Y, int cin, int cout,
+                                const BItem &it, int ob, char *smem) {
+    using W2 = typename Io<T>::W2;
+    constexpr int C = kParts;
+    const W2 *ws = reinterpret_cast<const W2 *>(smem);                       // [cin][ob]
+    float4 *xp = reinterpret_cast<float4 *>(smem + b_xp_offset<T>(cin, ob));
+    const int tid = grp.tid;
+    const int nr = it.nbb * cin;
+    if constexpr (C > 1) {
+        for (int r = tid; r < nr; r += NT) {
+            float4 s = xp[r];
+#pragma unroll
+            for (int cc = 1; cc < C; ++cc) {
+                const float4 q = xp[cc * nr + r];
+                s.x += q.x; s.y += q.y; s.z += q.z; s.w += q.w;
+            }
+            xp[r] = s;
+        }
+        grp.sync();
+    }
     const int nbt = (it.nbb + kBT - 1) / kBT, no2 = (it.nob + 1) / 2;
     const int tiles = nbt * no2;
     switch (b_split(tiles, NT)) {
@@ -564,6 +591,19 @@ __device__ void phase_b(const G &grp, const float2 *__restrict__ part, float2 *_
         case 2: phase_b_tiles<Cf, T, 2, NT>(grp, Y, cin, cout, it, ob, ws, xp, tiles); break;
         default: phase_b_tiles<Cf, T, 1, NT>(grp, Y, cin, cout, it, ob, ws, xp, tiles); break;
     }
+}
+
+template <class Cf, typename T, int NT, class G, int kParts = Cf::C>
+__device__ void phase_b(const G &grp, const float2 *__restrict__ part, float2 *__restrict__ Y, int cin,
+                        int cout, int nimg_in, const BItem &it, int ob, char *smem,
+                        unsigned long long *t_loaded = nullptr) {
+    float4 *xp = reinterpret_cast<float4 *>(smem + b_xp_offset<T>(cin, ob));
+    phase_b_issue_parts<Cf, NT, G, kParts>(grp, part, cin, nimg_in, it, xp);
+    cp_async_commit();
+    cp_async_wait_all();                                 // also covers the weight slab
+    grp.sync();
+    if (t_loaded && grp.tid == 0) *t_loaded = (unsigned long long)globaltimer();
+    phase_b_compute<Cf, T, NT, G, kParts>(grp, Y, cin, cout, it, ob, smem);
 }
 
 // ---------------------------------------------------------------------------
@@ -743,10 +783,7 @@ __device__ __forceinline__ void cta_record(const Args &a, int phase, int first,
 
 // item = (pair * nob + output block) * batch blocks + batch block; a.bg = batch
 // rows per block, a.ng = batch blocks
-template <class Cf, typename T, int kParts, int kNTB>
-__global__ void __launch_bounds__(kNTB) k_phase_b(Args a) {
-    extern __shared__ __align__(16) char smem[];
-    int it = blockIdx.x;
+__device__ __forceinline__ BItem b_item(const Args &a, int it) {
     const int bblk = it % a.ng;
     it /= a.ng;
     BItem bi;
@@ -755,6 +792,13 @@ __global__ void __launch_bounds__(kNTB) k_phase_b(Args a) {
     bi.nob = min(a.ob, a.cout - bi.o0);
     bi.b0 = bblk * a.bg;
     bi.nbb = min(a.bg, a.batch - bi.b0);
+    return bi;
+}
+
+template <class Cf, typename T, int kParts, int kNTB>
+__global__ void __launch_bounds__(kNTB) k_phase_b(Args a) {
+    extern __shared__ __align__(16) char smem[];
+    const BItem bi = b_item(a, blockIdx.x);
     const CtaGroup grp{(int)threadIdx.x};
     const unsigned long long t0 = a.trace ? trace_now() : 0;
     // weight slab rows padded by one entry: the lanes of a warp read S input
