@@ -338,7 +338,8 @@ def bench_gpu(args, rank, world, local):
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "algorithmic_bytes_per_launch": alg_bytes,
-            "traffic": recorded_traffic(case.name),
+            # the committed capture covers the default kernels only
+            "traffic": recorded_traffic(case.name) if args.flags == 0 else None,
         },
         "e2e": {
             "value": round(whole_job_rate(case.batch, world, e2e_steps, e2e_ms), 1),
