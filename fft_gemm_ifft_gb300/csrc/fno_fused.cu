@@ -256,10 +256,9 @@ __global__ void __launch_bounds__(kNT) k_phase_c(Args a) {
 // TMA brings the image into shared memory as M tiles of 128 rows, K-major with
 // the 128-byte swizzle.  The row DFT of bins 0..M1-1 is the GEMM
 // Z = X . T^T, T[j][n] = cos(2 pi j n / N1) (j < M1) and -sin(...) (j >= M1),
-// on tcgen05 with the accumulator in tensor memory: fp32 images run three
-// kind::tf32 passes (x_hi t_hi + x_hi t_lo + x_lo t_hi, x_lo the exact
-// remainder written over the tile in place), 16-bit images one kind::f16 pass
-// (their tolerance class is 1e-2).  The column DFT over the N0 rows, kept rows
+// on tcgen05 with the accumulator in tensor memory, one kind::f16 pass for the
+// 16-bit images of this kernel (their tolerance class is 1e-2; fp32 images
+// have their own pipelined kernel below).  The column DFT over the N0 rows, kept rows
 // only, runs on the SIMT cores from the tensor-memory rows: r = r1 + R1 r2,
 // B2-point register FFTs over r2, then X[j][k] = sum_r1 W_N0^{f r1} S[r1][f mod B2][k].
 // ---------------------------------------------------------------------------
@@ -267,14 +266,8 @@ namespace tca {
 
 constexpr int NT = 256;
 template <typename T> struct Shape;
-template <> struct Shape<float> {          // 128 x 128, 16 x 16 modes
-    static constexpr int N0 = 128, N1 = 128, M0 = 16, M1 = 16, kE = 32, B2 = 8;
-    static constexpr bool kSplit = true;
-    static constexpr int kMinBlocks = 2;
-};
 template <> struct Shape<__half> {         // 256 x 256, 32 x 32 modes
     static constexpr int N0 = 256, N1 = 256, M0 = 32, M1 = 32, kE = 64, B2 = 16;
-    static constexpr bool kSplit = false;
     static constexpr int kMinBlocks = 1;
 };
 template <> struct Shape<__nv_bfloat16> : Shape<__half> {};
@@ -291,7 +284,7 @@ struct Geo {
     static constexpr uint32_t kTile = 16384;            // 128 rows x 128 bytes
     static constexpr uint32_t kXBytes = (uint32_t)MT * KC * kTile;
     static constexpr uint32_t kTChunk = (uint32_t)N * 128;
-    static constexpr uint32_t kTBytes = (S::kSplit ? 2u : 1u) * KC * kTChunk;
+    static constexpr uint32_t kTBytes = KC * kTChunk;
     static constexpr int ZS = M1 + 1;                   // Z plane row stride (floats)
     static constexpr uint32_t kZBytes = (uint32_t)N0 * ZS * 4 * 2;
     static constexpr uint32_t kSBytes = (uint32_t)R1 * B2 * M1 * 8;
@@ -362,46 +355,14 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
                     const uint32_t ao = xs + (t * Gm::KC + kc) * Gm::kTile + s * 32;
                     const uint32_t bo = ts + kc * Gm::kTChunk + s * 32;
                     const uint32_t acc = (kc | s) ? 1u : 0u;
-                    if constexpr (Shape<T>::kSplit) {
-                        constexpr uint32_t id = idesc_tf32(Gm::N);
-                        mma_tf32(d, desc_sw128(ao), desc_sw128(bo), id, acc);
-                        mma_tf32(d, desc_sw128(ao), desc_sw128(bo + Gm::KC * Gm::kTChunk), id, 1u);
-                    } else {
-                        constexpr uint32_t id =
-                            idesc_f16(Gm::N, std::is_same<T, __nv_bfloat16>::value);
-                        mma_f16(d, desc_sw128(ao), desc_sw128(bo), id, acc);
-                    }
+                    constexpr uint32_t id = idesc_f16(Gm::N, std::is_same<T, __nv_bfloat16>::value);
+                    mma_f16(d, desc_sw128(ao), desc_sw128(bo), id, acc);
                 }
             }
         }
         mma_commit(&bar_mma);
     }
     ok &= mbar_wait(&bar_mma, 0, a.err);
-    if constexpr (Shape<T>::kSplit) {
-        // x's lo parts over the tile (elementwise: the swizzled layout carries over),
-        // then the pass x_lo t_hi
-        float4 *xv = reinterpret_cast<float4 *>(base);
-        for (int e = tid; e < (int)(Gm::kXBytes / 16); e += NT) {
-            const float4 v = xv[e];
-            xv[e] = make_float4(tf32_lo(v.x), tf32_lo(v.y), tf32_lo(v.z), tf32_lo(v.w));
-        }
-        fence_async_smem();
-        tc_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            tc_after_sync();
-            constexpr uint32_t id = idesc_tf32(Gm::N);
-            for (int t = 0; t < Gm::MT; ++t)
-                for (int kc = 0; kc < Gm::KC; ++kc)
-#pragma unroll
-                    for (int s = 0; s < 4; ++s)
-                        mma_tf32(tmem + t * Gm::N,
-                                 desc_sw128(xs + (t * Gm::KC + kc) * Gm::kTile + s * 32),
-                                 desc_sw128(ts + kc * Gm::kTChunk + s * 32), id, 1u);
-            mma_commit(&bar_mma);
-        }
-        ok &= mbar_wait(&bar_mma, 1, a.err);
-    }
     tc_after_sync();
     const unsigned long long t_z = a.trace ? trace_now() : 0;     // the row DFT is done
     // Z planes (re, im) from tensor memory into the region the tile occupied:
@@ -460,6 +421,195 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
                      "r"(Gm::kTmemCols));
     }
     cta_record(a, 0, 0, t0, t_x, t_z);
+}
+
+// ---------------------------------------------------------------------------
+// Kernel A on the tensor cores for fp32 128 x 128 layers (16 x 16 modes), a
+// pipeline over the image's four 32-column K chunks.  Each chunk has its own
+// TMA barrier; pass 1 multiplies the chunk by [T_hi; T_lo] (N = 64: columns
+// 0..31 of the accumulator take x T_hi, 32..63 x T_lo) as soon as it lands,
+// then, while the next chunk's pass 1 runs, the threads overwrite the chunk
+// with its tf32 remainder x_lo and pass 2 adds x_lo T_hi into columns 0..31.
+// Z = the two column halves summed; the column DFT and the kept modes follow
+// on the SIMT cores as in the 16-bit kernel.  Two CTAs per SM.
+// ---------------------------------------------------------------------------
+struct Geo32 {
+    static constexpr int N0 = 128, N1 = 128, M0 = 16, M1 = 16, K0 = 32, NK = K0 * M1;
+    static constexpr int KC = 4;                        // K chunks of 32 fp32 (128 bytes)
+    static constexpr int B2 = 8, R1 = N0 / B2;          // column DFT: r = r1 + 16 r2
+    static constexpr uint32_t kTile = 16384;            // one K chunk of the image
+    static constexpr uint32_t kXBytes = KC * kTile;
+    static constexpr uint32_t kTChunk = 64 * 128;       // [T_hi rows 0..31 | T_lo rows 0..31]
+    static constexpr uint32_t kTBytes = KC * kTChunk;
+    static constexpr int ZS = M1 + 1;                   // Z plane row stride (floats)
+    static constexpr uint32_t kZBytes = (uint32_t)N0 * ZS * 4 * 2;
+    static constexpr uint32_t kSBytes = (uint32_t)R1 * B2 * M1 * 8;
+    static_assert(kZBytes + kSBytes <= kXBytes, "Z planes and sums fit over the image");
+    static constexpr uint32_t kT = kXBytes;
+    static constexpr uint32_t kTw = kT + kTBytes;
+    static constexpr uint32_t kSmem = kTw + N0 * 8 + 1024;
+    static constexpr uint32_t kTmemCols = 64;
+};
+
+__global__ void __launch_bounds__(NT, 2)
+k_phase_a_tc32(const __grid_constant__ CUtensorMap xmap, Args a, const void *tables) {
+    using Gm = Geo32;
+    using namespace tcu;
+    extern __shared__ __align__(1024) char smem_raw[];
+    char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+    __shared__ __align__(8) uint64_t bar_t, bar_fin, bar_x[Gm::KC], bar_p1[Gm::KC];
+    __shared__ uint32_t s_tmem;
+    const unsigned long long t0 = a.trace ? trace_now() : 0;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int img = blockIdx.x;
+    float2 *tw = reinterpret_cast<float2 *>(base + Gm::kTw);
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_t)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_fin)));
+        for (int kc = 0; kc < Gm::KC; ++kc) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_x[kc])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_p1[kc])));
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     ::"r"(tc_smem_addr(&bar_t)), "r"(Gm::kTBytes) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(tc_smem_addr(base + Gm::kT)), "l"(tables), "r"(Gm::kTBytes),
+                     "r"(tc_smem_addr(&bar_t)) : "memory");
+        for (int kc = 0; kc < Gm::KC; ++kc) {
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                         ::"r"(tc_smem_addr(&bar_x[kc])), "r"(Gm::kTile) : "memory");
+            tma_load_2d(tc_smem_addr(base + kc * Gm::kTile), &xmap, kc * 32, img * Gm::N0,
+                        &bar_x[kc]);
+        }
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(tc_smem_addr(&s_tmem)), "r"(Gm::kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    for (int e = tid; e < Gm::N0; e += NT) tw[e] = a.tw0[e];
+    tc_before_sync();
+    __syncthreads();
+    tc_after_sync();
+    pdl_trigger();
+    const uint32_t tmem = s_tmem;
+    const uint32_t xs = tc_smem_addr(base), ts = tc_smem_addr(base + Gm::kT);
+    bool ok = true;
+    // pass 1 of chunk kc (one thread): x [T_hi; T_lo]^T into columns 0..63
+    auto pass1 = [&](int kc) {
+        ok &= mbar_wait(&bar_x[kc], 0, a.err);
+        tc_after_sync();
+        constexpr uint32_t id = idesc_tf32(64);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+            mma_tf32(tmem, desc_sw128(xs + kc * Gm::kTile + s * 32),
+                     desc_sw128(ts + kc * Gm::kTChunk + s * 32), id, (kc | s) ? 1u : 0u);
+        mma_commit(&bar_p1[kc]);
+    };
+    if (tid == 0) {
+        ok &= mbar_wait(&bar_t, 0, a.err);
+        pass1(0);
+    }
+    for (int kc = 0; kc < Gm::KC; ++kc) {
+        if (tid == 0 && kc + 1 < Gm::KC) pass1(kc + 1);
+        ok &= mbar_wait(&bar_p1[kc], 0, a.err);          // pass 1 has read chunk kc
+        // x_lo over chunk kc (elementwise: the swizzled layout carries over)
+        float4 *xv = reinterpret_cast<float4 *>(base + kc * Gm::kTile);
+        for (int e = tid; e < (int)(Gm::kTile / 16); e += NT) {
+            const float4 v = xv[e];
+            xv[e] = make_float4(tf32_lo(v.x), tf32_lo(v.y), tf32_lo(v.z), tf32_lo(v.w));
+        }
+        fence_async_smem();
+        tc_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc_after_sync();
+            constexpr uint32_t id = idesc_tf32(32);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_tf32(tmem, desc_sw128(xs + kc * Gm::kTile + s * 32),
+                         desc_sw128(ts + kc * Gm::kTChunk + s * 32), id, 1u);
+        }
+    }
+    if (tid == 0) mma_commit(&bar_fin);
+    ok &= mbar_wait(&bar_fin, 0, a.err);
+    tc_after_sync();
+    const unsigned long long t_z = a.trace ? trace_now() : 0;     // the row DFT is done
+    // Z planes from tensor memory into the region the image occupied: warps w
+    // and w + 4 read the same lanes, the first the re, the second the im bins,
+    // each summing the T_hi and T_lo column halves
+    float *zr = reinterpret_cast<float *>(base);
+    float *zi = zr + Gm::N0 * Gm::ZS;
+    float2 *S = reinterpret_cast<float2 *>(base + Gm::kZBytes);
+    {
+        const int half = warp >> 2, row = 32 * (warp & 3) + (tid & 31);
+        const uint32_t lanes = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        float v[16], u[16];
+        tmem_ld16(lanes + half * Gm::M1, v);
+        tmem_ld16(lanes + 32 + half * Gm::M1, u);
+        float *dz = half ? zi : zr;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) dz[row * Gm::ZS + q] = ok ? v[q] + u[q] : 0.f;
+    }
+    tc_before_sync();
+    __syncthreads();
+    // column DFT: S[r1][q][k] = B2-point DFT over r2 of Z[r1 + R1 r2][k]
+    for (int u = tid; u < Gm::R1 * Gm::M1; u += NT) {
+        const int r1 = u / Gm::M1, k = u % Gm::M1;
+        float2 z[Gm::B2];
+#pragma unroll
+        for (int r2 = 0; r2 < Gm::B2; ++r2) {
+            const int r = r1 + Gm::R1 * r2;
+            z[r2] = make_float2(zr[r * Gm::ZS + k], zi[r * Gm::ZS + k]);
+        }
+        fft::fft_dif<Gm::B2, -1>(z);
+#pragma unroll
+        for (int q = 0; q < Gm::B2; ++q)
+            S[(r1 * Gm::B2 + q) * Gm::M1 + k] = z[fft::bitrev(q, fft::ilog2(Gm::B2))];
+    }
+    __syncthreads();
+    // kept modes: X[j][k] = sum_r1 W_N0^{f r1} S[r1][f mod B2][k]
+    float2 *dst = a.part + (size_t)img * Gm::NK;
+    for (int o = tid; o < Gm::NK; o += NT) {
+        const int j = o / Gm::M1, k = o % Gm::M1;
+        const int f = j < Gm::M0 ? j : Gm::N0 - Gm::K0 + j;
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int r1 = 0; r1 < Gm::R1; ++r1)
+            cmac(acc, S[(r1 * Gm::B2 + (f % Gm::B2)) * Gm::M1 + k], tw[(f * r1) & (Gm::N0 - 1)]);
+        __stcg(dst + o, acc);
+    }
+    tc_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc_after_sync();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(Gm::kTmemCols));
+    }
+    cta_record(a, 0, 0, t0, t0, t_z);
+}
+
+// Host: kernel A's fp32 operand image, per K chunk [T_hi | T_lo] with T[j][n] =
+// cos(2 pi k n / 128) (j = k < 16) or -sin (j = 16 + k), split in double.
+void make_table32(std::vector<unsigned char> &img) {
+    using Gm = Geo32;
+    using tcu::sw_off;
+    using tcu::tf32_lo;
+    img.assign(Gm::kTBytes, 0);
+    const double two_pi = 2.0 * M_PI;
+    for (int j = 0; j < 2 * Gm::M1; ++j)
+        for (int n = 0; n < Gm::N1; ++n) {
+            const int k = j % Gm::M1;
+            const double ang = two_pi * (double)k * (double)n / (double)Gm::N1;
+            const double v = j < Gm::M1 ? std::cos(ang) : -std::sin(ang);
+            const float hi = (float)v;
+            const float lo = (float)(v - (double)(hi - tf32_lo(hi)));
+            const uint32_t chunk = (uint32_t)(n / 32) * Gm::kTChunk;
+            memcpy(&img[chunk + sw_off(j, n % 32)], &hi, 4);
+            memcpy(&img[chunk + sw_off(2 * Gm::M1 + j, n % 32)], &lo, 4);
+        }
 }
 
 // ---------------------------------------------------------------------------
@@ -673,14 +823,12 @@ void make_table_c(std::vector<unsigned char> &img) {
         }
 }
 
-// Host: the twiddle operand in its swizzled shared-memory image (hi then lo for
-// fp32, one 16-bit copy otherwise), computed in double.
+// Host: the 16-bit twiddle operand in its swizzled shared-memory image,
+// computed in double and rounded once.
 template <typename T>
 void make_table(std::vector<unsigned char> &img) {
     using Gm = Geo<T>;
-    using tcu::sw_off;
     using tcu::sw_off16;
-    using tcu::tf32_lo;
     img.assign(Gm::kTBytes, 0);
     const double two_pi = 2.0 * M_PI;
     for (int j = 0; j < Gm::N; ++j)
@@ -689,18 +837,10 @@ void make_table(std::vector<unsigned char> &img) {
             const double ang = two_pi * (double)k * (double)n / (double)Gm::N1;
             const double v = j < Gm::M1 ? std::cos(ang) : -std::sin(ang);
             const uint32_t chunk = (uint32_t)(n / Gm::kE) * Gm::kTChunk;
-            if constexpr (Shape<T>::kSplit) {
-                const float hi = (float)v;
-                const float lo = (float)(v - (double)(hi - tf32_lo(hi)));
-                const uint32_t off = chunk + sw_off(j, n % Gm::kE);
-                memcpy(&img[off], &hi, 4);
-                memcpy(&img[Gm::KC * Gm::kTChunk + off], &lo, 4);
-            } else {
-                const uint32_t off = chunk + sw_off16(j, n % Gm::kE);
-                const T h = std::is_same<T, __half>::value ? T(__float2half_rn((float)v))
-                                                           : T(__float2bfloat16_rn((float)v));
-                memcpy(&img[off], &h, 2);
-            }
+            const uint32_t off = chunk + sw_off16(j, n % Gm::kE);
+            const T h = std::is_same<T, __half>::value ? T(__float2half_rn((float)v))
+                                                       : T(__float2bfloat16_rn((float)v));
+            memcpy(&img[off], &h, 2);
         }
 }
 
@@ -1049,12 +1189,11 @@ struct Pdl {
     static constexpr int kBThreads = Cf::N0 == 128 ? 256 : 128;
     // (no CUDA call: sizes are reported before any device work; a plan whose
     // driver lacks the tensor-map encoder fails at creation)
-    // fp32 on request (FNO_PLAN_TENSOR_CORES: at 128 x 128 the register-FFT kernel
-    // is measured faster), 16-bit by default (FNO_PLAN_SIMT_TRANSFORM opts out)
+    // Whether kernel A runs on the tensor cores: by default for the shapes that
+    // have a tensor-core kernel (FNO_PLAN_SIMT_TRANSFORM opts out)
     static bool use_tca(fno_dtype_t dt, uint32_t flags) {
         if (!tca_shape<Cf>(dt)) return false;
-        return dt == FNO_F32 ? (flags & FNO_PLAN_TENSOR_CORES) != 0
-                             : (flags & FNO_PLAN_SIMT_TRANSFORM) == 0;
+        return (flags & FNO_PLAN_SIMT_TRANSFORM) == 0;
     }
     // Whether kernel C runs on the tensor cores: 16-bit 256 x 256 together with
     // kernel A; fp32 128 x 128 by default (FNO_PLAN_SIMT_TRANSFORM opts out)
@@ -1102,8 +1241,13 @@ struct Pdl {
                 e = cudaErrorNotSupported;
             std::vector<unsigned char> img, imgc;
             if (e == cudaSuccess && p.fused_tca) {
-                e = raise_smem_limit(tca::k_phase_a_tc<T>, (int)tca::Geo<T>::kSmem);
-                tca::make_table<T>(img);
+                if constexpr (std::is_same<T, float>::value) {
+                    e = raise_smem_limit(tca::k_phase_a_tc32, (int)tca::Geo32::kSmem);
+                    tca::make_table32(img);
+                } else {
+                    e = raise_smem_limit(tca::k_phase_a_tc<T>, (int)tca::Geo<T>::kSmem);
+                    tca::make_table<T>(img);
+                }
             }
             if (e == cudaSuccess && p.fused_tcc) {
                 if constexpr (std::is_same<T, float>::value) {
@@ -1183,12 +1327,20 @@ struct Pdl {
         bool done_a = false;
         if constexpr (!std::is_same<T, float>::value || Cf::N0 == 128) {
             if (p.fused_tca) {
-                using Gm = tca::Geo<T>;
                 CUtensorMap xmap;
-                if (!tcu::encode_rows_tiled(&xmap, a.x, (int64_t)p.batch * p.cin * Gm::N0,
-                                            Gm::N1, sizeof(T), Gm::kE, tcu::tma_type<T>()))
-                    return cudaErrorInvalidValue;
-                tca::k_phase_a_tc<T><<<nA, tca::NT, Gm::kSmem, s>>>(xmap, a, p.fused_tables);
+                if constexpr (std::is_same<T, float>::value) {
+                    using Gm = tca::Geo32;
+                    if (!tcu::encode_rows_tiled(&xmap, a.x, (int64_t)p.batch * p.cin * Gm::N0,
+                                                Gm::N1, sizeof(T), 32, tcu::tma_type<T>()))
+                        return cudaErrorInvalidValue;
+                    tca::k_phase_a_tc32<<<nA, tca::NT, Gm::kSmem, s>>>(xmap, a, p.fused_tables);
+                } else {
+                    using Gm = tca::Geo<T>;
+                    if (!tcu::encode_rows_tiled(&xmap, a.x, (int64_t)p.batch * p.cin * Gm::N0,
+                                                Gm::N1, sizeof(T), Gm::kE, tcu::tma_type<T>()))
+                        return cudaErrorInvalidValue;
+                    tca::k_phase_a_tc<T><<<nA, tca::NT, Gm::kSmem, s>>>(xmap, a, p.fused_tables);
+                }
                 e = cudaGetLastError();
                 done_a = true;
             }

@@ -82,12 +82,10 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * CTA of each kernel of the three-kernel variants (2-D and 3-D layers).
  * Costs a few timer reads, a barrier and a store per item.                  */
 #define FNO_PLAN_TRACE 2u
-/* Run the forward transform of the float32 128x128 layer (16x16 modes) on
- * the tensor cores: each image's row DFT as a tcgen05 3xTF32 GEMM (TMA-staged
- * operands, accumulator in tensor memory) inside the three-kernel path.  Same
- * results within rounding; at this size the register-FFT kernel is measured
- * faster (22.3 vs 22.8 us on the 8 x 32-channel workload), so it is the
- * default.  (16-bit 256x256 layers use the tensor-core transform by default.) */
+/* Accepted for compatibility and without effect: the forward transform of
+ * the float32 128x128 layer (16x16 modes) runs on the tensor cores by default
+ * (each image's row DFT as a pipelined tcgen05 3xTF32 GEMM over TMA-staged
+ * K chunks); FNO_PLAN_SIMT_TRANSFORM selects the register-FFT kernels.       */
 #define FNO_PLAN_TENSOR_CORES 4u
 /* Run the float32 / fp16 128x128 layer as ONE persistent kernel with a work
  * queue instead of three kernels chained by programmatic dependent launch
@@ -103,10 +101,10 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
 #define FNO_PLAN_SIMT_MIX 32u
 /* Run the transforms on the register-FFT kernels instead of the tensor-core
  * kernels that are the default for these shapes: for the 16-bit 256x256
- * layer (32x32 modes) both the forward transform (a kind::f16 tcgen05 GEMM
- * per image) and the inverse (a kind::tf32 GEMM per image); for the float32
- * 128x128 layer (16x16 modes) the inverse (a 3xTF32 GEMM per image, TMA
- * stores).  An ablation switch.                                             */
+ * layer (32x32 modes) the forward transform (a kind::f16 tcgen05 GEMM per
+ * image) and the inverse (a kind::tf32 GEMM per image); for the float32
+ * 128x128 layer (16x16 modes) the forward transform and the inverse (3xTF32
+ * GEMMs per image, TMA loads and stores).  An ablation switch.              */
 #define FNO_PLAN_SIMT_TRANSFORM 64u
 /* The weights passed to fno_spectral_conv_forward are in the packed
  * mode-major layout written by fno_spectral_conv_pack_weights (weights are

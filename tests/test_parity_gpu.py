@@ -139,14 +139,14 @@ def test_fused_and_unfused_agree_and_are_deterministic():
     a, _ = run_gpu(case, x, w)
     b, _ = run_gpu(case, x, w)
     c, _ = run_gpu(case, x, w, FNO_PLAN_UNFUSED)
-    d, _ = run_gpu(case, x, w, capi.FNO_PLAN_TENSOR_CORES)
-    e, _ = run_gpu(case, x, w, capi.FNO_PLAN_TENSOR_CORES)
+    d, _ = run_gpu(case, x, w, capi.FNO_PLAN_SIMT_TRANSFORM)
+    e, _ = run_gpu(case, x, w, capi.FNO_PLAN_SIMT_TRANSFORM)
     f, _ = run_gpu(case, x, w, capi.FNO_PLAN_PERSISTENT)
     assert_close(f, c.astype(np.float64), "f32", "persistent vs unfused")
     assert np.array_equal(a, b), "two runs of the same plan differ"
-    assert np.array_equal(d, e), "two runs of the tensor-core plan differ"
+    assert np.array_equal(d, e), "two runs of the register-FFT plan differ"
     assert_close(a, c.astype(np.float64), "f32", "fused vs unfused")
-    assert_close(d, c.astype(np.float64), "f32", "tensor cores vs unfused")
+    assert_close(d, c.astype(np.float64), "f32", "register-FFT kernels vs unfused")
 
 
 @pytest.mark.parametrize("name,kernels", [("1d_f32", 1), ("2d_f32", 3), ("2d_f16", 3),
@@ -190,7 +190,7 @@ def test_fused_3d_and_unfused_agree():
     assert_close(a, c.astype(np.float64), "f32", "3-D fused vs unfused")
 
 
-@pytest.mark.parametrize("name,chunks_a,chunks_c", [("2d_f32", 4, 1), ("3d_f32", 8, 8)])
+@pytest.mark.parametrize("name,chunks_a,chunks_c", [("2d_f32", 1, 1), ("3d_f32", 8, 8)])
 def test_trace_three_kernel_variant(name, chunks_a, chunks_c):
     # one record per CTA of each kernel; kernel B's CTAs start before A's last
     # one ends at the earliest (programmatic dependent launch), never wait past it
