@@ -148,13 +148,17 @@ class FnoModel:
                    "proj2_w", "proj2_b")
 
     def __init__(self, batch, h, w, modes=(16, 16), cin_lift=3, width=64, nlayers=4,
-                 hidden=128, cout=1, flags=0):
+                 hidden=128, cout=1, flags=0, dtype="f32"):
         import torch
         d = capi.fno_model_desc_t()
         d.batch, d.cin_lift, d.width, d.nlayers = batch, cin_lift, width, nlayers
         d.hidden, d.cout, d.h, d.w = hidden, cout, h, w
         d.modes[0], d.modes[1] = modes
-        d.dtype, d.flags = FNO_F32, flags
+        d.dtype, d.flags = capi.DTYPE_CODES[dtype], flags
+        self.dtype = dtype
+        # x, the activations, spec_w and out in the storage type; 1x1 weights float32
+        self.torch_dtype = {"f32": torch.float32, "f16": torch.float16,
+                            "bf16": torch.bfloat16}[dtype]
         self.desc = d
         st, self.handle = capi.fno_model_plan(d)
         check(st, "fno_model_plan")
@@ -175,14 +179,15 @@ class FnoModel:
 
     def forward(self, x, params: dict, out=None, stream=None):
         import torch
-        _require(x, torch.float32, self.x_shape, "x")
+        _require(x, self.torch_dtype, self.x_shape, "x")
         p = capi.fno_model_params_t()
         for k in self.PARAM_NAMES:
-            _require(params[k], torch.float32, self.shapes[k], k)
+            want = self.torch_dtype if k == "spec_w" else torch.float32
+            _require(params[k], want, self.shapes[k], k)
             setattr(p, k, params[k].data_ptr())
         if out is None:
-            out = torch.empty(self.y_shape, dtype=torch.float32, device=x.device)
-        _require(out, torch.float32, self.y_shape, "out")
+            out = torch.empty(self.y_shape, dtype=self.torch_dtype, device=x.device)
+        _require(out, self.torch_dtype, self.y_shape, "out")
         check(capi.fno_forward(self.handle, x.data_ptr(), p, out.data_ptr(),
                                self.workspace.data_ptr(), _stream_handle(stream)), "fno_forward")
         return out

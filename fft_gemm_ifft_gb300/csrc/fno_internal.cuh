@@ -101,12 +101,27 @@ template <> struct Storage<float> {
     static __device__ __forceinline__ float2 load2(const float *p) {
         return *reinterpret_cast<const float2 *>(p);
     }
+    // four consecutive elements (16-byte aligned for float, 8-byte otherwise)
+    static __device__ __forceinline__ float4 load4(const float *p) {
+        return *reinterpret_cast<const float4 *>(p);
+    }
+    static __device__ __forceinline__ void store4(float *p, float4 v) {
+        *reinterpret_cast<float4 *>(p) = v;
+    }
 };
 template <> struct Storage<__half> {
     static __device__ __forceinline__ float load(const __half *p) { return __half2float(*p); }
     static __device__ __forceinline__ void store(__half *p, float v) { *p = __float2half_rn(v); }
     static __device__ __forceinline__ float2 load2(const __half *p) {
         return __half22float2(*reinterpret_cast<const __half2 *>(p));
+    }
+    static __device__ __forceinline__ float4 load4(const __half *p) {
+        const float2 a = load2(p), b = load2(p + 2);
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+    static __device__ __forceinline__ void store4(__half *p, float4 v) {
+        reinterpret_cast<__half2 *>(p)[0] = __floats2half2_rn(v.x, v.y);
+        reinterpret_cast<__half2 *>(p)[1] = __floats2half2_rn(v.z, v.w);
     }
 };
 
@@ -119,6 +134,14 @@ template <> struct Storage<__nv_bfloat16> {
     }
     static __device__ __forceinline__ float2 load2(const __nv_bfloat16 *p) {
         return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+    }
+    static __device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
+        const float2 a = load2(p), b = load2(p + 2);
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+    static __device__ __forceinline__ void store4(__nv_bfloat16 *p, float4 v) {
+        reinterpret_cast<__nv_bfloat162 *>(p)[0] = __floats2bfloat162_rn(v.x, v.y);
+        reinterpret_cast<__nv_bfloat162 *>(p)[1] = __floats2bfloat162_rn(v.z, v.w);
     }
 };
 

@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <cstring>
 #include <new>
+#include <type_traits>
 
 #include "fno_internal.cuh"
 #include "fno_tc.cuh"
@@ -22,7 +23,7 @@ struct Model {
     fno_model_desc_t desc;
     fno_plan_t spec;
     int64_t npix;
-    size_t act_bytes;      // one activation buffer (B, width, H, W) float32
+    size_t act_bytes;      // one activation buffer (B, width, H, W) in the storage type
     size_t spec_ws_bytes;
     size_t ws_bytes;
     int kernels;
@@ -61,9 +62,11 @@ __device__ __forceinline__ void cp_async16(void *s, const void *g) {
                  ::"r"((unsigned)__cvta_generic_to_shared(s)), "l"(g) : "memory");
 }
 
-// Input channels [k0, k0 + kc) of pixels [p0, p0 + kTP) of one image (a_img),
-// and the weights W[o0 + o][k0 + k] (row length cin) of outputs o < no.
-__device__ void load_chunk(TileSmem &s, const float *__restrict__ a_img, int cin, int64_t npix,
+// Input channels [k0, k0 + kc) of pixels [p0, p0 + kTP) of one image (a_img,
+// in the activation storage type; float32 in shared memory), and the weights
+// W[o0 + o][k0 + k] (row length cin) of outputs o < no.
+template <typename T>
+__device__ void load_chunk(TileSmem &s, const T *__restrict__ a_img, int cin, int64_t npix,
                            int64_t p0, int k0, int kc, const float *__restrict__ W, int o0,
                            int no) {
     const int tid = threadIdx.x;
@@ -71,10 +74,17 @@ __device__ void load_chunk(TileSmem &s, const float *__restrict__ a_img, int cin
         const int k = e / (kTP / 4), g = e % (kTP / 4);
         const int64_t px = p0 + 4 * g;
         float *dst = &s.a[k][4 * g];
-        if (k < kc && px < npix)
-            cp_async16(dst, a_img + (int64_t)(k0 + k) * npix + px);
-        else
-            *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+        const bool in = k < kc && px < npix;
+        if constexpr (std::is_same<T, float>::value) {
+            if (in)
+                cp_async16(dst, a_img + (int64_t)(k0 + k) * npix + px);
+            else
+                *reinterpret_cast<float4 *>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            *reinterpret_cast<float4 *>(dst) =
+                in ? Storage<T>::load4(a_img + (int64_t)(k0 + k) * npix + px)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
     for (int e = tid; e < kTK * kTO; e += kTT) {
         const int k = e / kTO, o = e % kTO;
@@ -101,12 +111,14 @@ __device__ __forceinline__ void fma_chunk(const TileSmem &s, int kc, int og, int
     }
 }
 
-// out[b][o][p] = act(sum_j W[o][j] x[b][j][p] + bias[o] (+ add[b][o][p]))
+// out[b][o][p] = act(sum_j W[o][j] x[b][j][p] + bias[o] (+ add[b][o][p])); x, add
+// and out in the activation storage type T, arithmetic in float32
 // grid: (pixel tiles, output tiles, batch)
+template <typename T>
 __global__ void __launch_bounds__(kTT)
-k_linear_tiled(const float *__restrict__ x, const float *__restrict__ W,
-               const float *__restrict__ bias, const float *__restrict__ add,
-               float *__restrict__ out, int cin, int cout, int64_t npix, int apply_gelu) {
+k_linear_tiled(const T *__restrict__ x, const float *__restrict__ W,
+               const float *__restrict__ bias, const T *__restrict__ add,
+               T *__restrict__ out, int cin, int cout, int64_t npix, int apply_gelu) {
     extern __shared__ __align__(16) char smem_raw[];
     TileSmem &s = *reinterpret_cast<TileSmem *>(smem_raw);
     const int64_t p0 = (int64_t)blockIdx.x * kTP;
@@ -118,10 +130,10 @@ k_linear_tiled(const float *__restrict__ x, const float *__restrict__ W,
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-    const float *a_img = x + b * cin * npix;
+    const T *a_img = x + b * cin * npix;
     for (int k0 = 0; k0 < cin; k0 += kTK) {
         const int kc = min(kTK, cin - k0);
-        load_chunk(s, a_img, cin, npix, p0, k0, kc, W, o0, no);
+        load_chunk<T>(s, a_img, cin, npix, p0, k0, kc, W, o0, no);
         fma_chunk(s, kc, og, pg, acc);
         __syncthreads();
     }
@@ -138,13 +150,17 @@ k_linear_tiled(const float *__restrict__ x, const float *__restrict__ W,
             float4 v = make_float4(acc[i][4 * h] + bo, acc[i][4 * h + 1] + bo,
                                    acc[i][4 * h + 2] + bo, acc[i][4 * h + 3] + bo);
             if (add) {
-                const float4 q = __ldcs(reinterpret_cast<const float4 *>(add + row + px));
+                float4 q;
+                if constexpr (std::is_same<T, float>::value)
+                    q = __ldcs(reinterpret_cast<const float4 *>(add + row + px));
+                else
+                    q = Storage<T>::load4(add + row + px);
                 v.x += q.x; v.y += q.y; v.z += q.z; v.w += q.w;
             }
             if (apply_gelu) {
                 v.x = gelu(v.x); v.y = gelu(v.y); v.z = gelu(v.z); v.w = gelu(v.w);
             }
-            *reinterpret_cast<float4 *>(out + row + px) = v;
+            Storage<T>::store4(out + row + px, v);
         }
     }
 }
@@ -152,18 +168,18 @@ k_linear_tiled(const float *__restrict__ x, const float *__restrict__ W,
 // out[b][o][p] = sum_k P2[o][k] gelu(sum_c P1[k][c] a[b][c][p] + c1[k]) + c2[o], o < cout
 // grid: (pixel tiles, batch); the hidden units run in tiles of kTO; kCo >= cout
 // partial outputs are held per thread
-template <int kCo>
+template <int kCo, typename T>
 __global__ void __launch_bounds__(kTT)
-k_projection_tiled(const float *__restrict__ a, const float *__restrict__ P1,
+k_projection_tiled(const T *__restrict__ a, const float *__restrict__ P1,
                    const float *__restrict__ c1, const float *__restrict__ P2,
-                   const float *__restrict__ c2, float *__restrict__ out, int width, int hidden,
+                   const float *__restrict__ c2, T *__restrict__ out, int width, int hidden,
                    int cout, int64_t npix) {
     extern __shared__ __align__(16) char smem_raw[];
     TileSmem &s = *reinterpret_cast<TileSmem *>(smem_raw);
     const int64_t p0 = (int64_t)blockIdx.x * kTP;
     const int64_t b = blockIdx.y;
     const int og = threadIdx.x / 16, pg = threadIdx.x % 16;
-    const float *a_img = a + b * width * npix;
+    const T *a_img = a + b * width * npix;
     float part[kCo][8];
 #pragma unroll
     for (int o = 0; o < kCo; ++o)
@@ -178,7 +194,7 @@ k_projection_tiled(const float *__restrict__ a, const float *__restrict__ P1,
             for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
         for (int k0 = 0; k0 < width; k0 += kTK) {
             const int kc = min(kTK, width - k0);
-            load_chunk(s, a_img, width, npix, p0, k0, kc, P1, h0, nh);
+            load_chunk<T>(s, a_img, width, npix, p0, k0, kc, P1, h0, nh);
             fma_chunk(s, kc, og, pg, acc);
             __syncthreads();
         }
@@ -210,7 +226,7 @@ k_projection_tiled(const float *__restrict__ a, const float *__restrict__ P1,
         if (threadIdx.x < kTP && p0 + threadIdx.x < npix) {
             float v = c2[o];
             for (int g = 0; g < kTT / 16; ++g) v += s.red[g][threadIdx.x];
-            out[(b * cout + o) * npix + p0 + threadIdx.x] = v;
+            Storage<T>::store(out + (b * cout + o) * npix + p0 + threadIdx.x, v);
         }
         __syncthreads();
     }
@@ -442,13 +458,15 @@ TcFn kernel(int cin, int n) {
 
 }  // namespace lintc
 
-using ProjFn = void (*)(const float *, const float *, const float *, const float *,
-                       const float *, float *, int, int, int, int64_t);
-ProjFn projection_kernel(int cout) {
-    if (cout <= 1) return k_projection_tiled<1>;
-    if (cout <= 2) return k_projection_tiled<2>;
-    if (cout <= 4) return k_projection_tiled<4>;
-    return k_projection_tiled<kMaxCout>;
+template <typename T>
+using ProjFn = void (*)(const T *, const float *, const float *, const float *,
+                        const float *, T *, int, int, int, int64_t);
+template <typename T>
+ProjFn<T> projection_kernel(int cout) {
+    if (cout <= 1) return k_projection_tiled<1, T>;
+    if (cout <= 2) return k_projection_tiled<2, T>;
+    if (cout <= 4) return k_projection_tiled<4, T>;
+    return k_projection_tiled<kMaxCout, T>;
 }
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -469,24 +487,29 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
     if (d->cout > kMaxCout || d->batch > 65535) return FNO_ERR_UNSUPPORTED;
     // the tiled 1x1 linears move pixel rows in 16-byte copies
     if ((d->h * d->w) % 4 != 0) return FNO_ERR_UNSUPPORTED;
-    if (d->dtype != FNO_F32) return FNO_ERR_UNSUPPORTED;
+    if (d->dtype != FNO_F32 && d->dtype != FNO_F16 && d->dtype != FNO_BF16)
+        return FNO_ERR_INVALID_ARG;
     const int64_t n[2] = {d->h, d->w};
     size_t spec_ws = 0;
     fno_status_t st = fno_spectral_conv_query(2, n, d->modes, d->batch, d->width, d->width,
-                                              FNO_F32, d->flags, &spec_ws, nullptr);
+                                              d->dtype, d->flags, &spec_ws, nullptr);
     if (st != FNO_OK) return st;
     Model *m = new (std::nothrow) Model();
     if (!m) return FNO_ERR_OUT_OF_MEMORY;
     m->desc = *d;
     st = fno_spectral_conv_plan(&m->spec, 2, n, d->modes, d->batch, d->width, d->width,
-                                FNO_F32, d->flags);
+                                d->dtype, d->flags);
     if (st != FNO_OK) {
         delete m;
         return st;
     }
     const int smem = (int)sizeof(TileSmem);
-    if (raise_smem_limit(k_linear_tiled, smem) != cudaSuccess ||
-        raise_smem_limit(projection_kernel(d->cout), smem) != cudaSuccess) {
+    const cudaError_t se = with_storage(d->dtype, [&](auto t) {
+        using T = decltype(t);
+        cudaError_t e = raise_smem_limit(k_linear_tiled<T>, smem);
+        return e == cudaSuccess ? raise_smem_limit(projection_kernel<T>(d->cout), smem) : e;
+    });
+    if (se != cudaSuccess) {
         cudaGetLastError();
         fno_plan_destroy(m->spec);
         delete m;
@@ -528,8 +551,10 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
         *smem_bytes = sb;
         return true;
     };
-    const bool tc_ok = lintc::eligible(d->width, d->width), th_ok =
-        lintc::eligible(d->width, d->hidden);
+    // (float32 activations only: the 16-bit stack runs the register-tiled linears)
+    const bool f32 = d->dtype == FNO_F32;
+    const bool tc_ok = f32 && lintc::eligible(d->width, d->width),
+               th_ok = f32 && lintc::eligible(d->width, d->hidden);
     if ((tc_ok && !setup_tc(lintc::kernel<false>(d->width, d->width), d->width, d->width,
                             &m->layer_tc_grid, &m->layer_tc_smem)) ||
         (th_ok && !setup_tc(lintc::kernel<true>(d->width, d->hidden), d->width, d->hidden,
@@ -542,7 +567,7 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
     int spec_kernels = 0;
     fno_spectral_conv_kernel_count(m->spec, &spec_kernels);
     m->npix = d->h * d->w;
-    m->act_bytes = align256((size_t)d->batch * d->width * m->npix * sizeof(float));
+    m->act_bytes = align256((size_t)d->batch * d->width * m->npix * (f32 ? 4 : 2));
     m->spec_ws_bytes = spec_ws;
     m->ws_bytes = 3 * m->act_bytes + align256(spec_ws);
     m->kernels = 1 + d->nlayers * (spec_kernels + 1) + 1;
@@ -574,53 +599,69 @@ fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_param
         if (!aligned16(q)) return FNO_ERR_MISALIGNED;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    char *ws = static_cast<char *>(workspace);
-    float *A = reinterpret_cast<float *>(ws);
-    float *S = reinterpret_cast<float *>(ws + m.act_bytes);
-    float *T = reinterpret_cast<float *>(ws + 2 * m.act_bytes);
-    void *spec_ws = ws + 3 * m.act_bytes;
-    const size_t spec_stride = (size_t)2 * d.width * d.width * d.modes[0] * d.modes[1] * 2;
+    return with_storage(d.dtype, [&](auto t) -> fno_status_t {
+        using T = decltype(t);
+        char *ws = static_cast<char *>(workspace);
+        T *A = reinterpret_cast<T *>(ws);
+        T *S = reinterpret_cast<T *>(ws + m.act_bytes);
+        T *Tn = reinterpret_cast<T *>(ws + 2 * m.act_bytes);
+        void *spec_ws = ws + 3 * m.act_bytes;
+        // one layer's spectral weights, in elements of the storage type
+        const size_t spec_stride = (size_t)2 * d.width * d.width * d.modes[0] * d.modes[1] * 2;
+        const T *spec_w = static_cast<const T *>(p->spec_w);
 
-    const unsigned ptiles = (unsigned)((m.npix + kTP - 1) / kTP);
-    const int64_t ntiles = d.batch * ((m.npix + lintc::kRows - 1) / lintc::kRows);
-    int *err = reinterpret_cast<Plan *>(m.spec)->dev_err;
-    const dim3 lin_grid(ptiles, (unsigned)((d.width + kTO - 1) / kTO), (unsigned)d.batch);
-    const size_t smem = sizeof(TileSmem);
-    k_linear_tiled<<<lin_grid, kTT, smem, s>>>(static_cast<const float *>(x), p->lift_w,
-                                               p->lift_b, nullptr, A, d.cin_lift, d.width,
-                                               m.npix, 0);
-    if (cudaGetLastError() != cudaSuccess) return FNO_ERR_CUDA;
-    for (int l = 0; l < d.nlayers; ++l) {
-        fno_status_t st = fno_spectral_conv_forward(m.spec, A, p->spec_w + l * spec_stride, S,
-                                                    m.spec_ws_bytes ? spec_ws : nullptr,
-                                                    stream);
-        if (st != FNO_OK) return st;
-        const int last = (l == d.nlayers - 1);
-        if (m.layer_tc_grid)
-            lintc::kernel<false>(d.width, d.width)<<<m.layer_tc_grid, lintc::kThreads,
-                                                     m.layer_tc_smem, s>>>(
-                A, p->pw_w + (size_t)l * d.width * d.width, p->pw_b + (size_t)l * d.width, S,
-                nullptr, nullptr, T, 0, m.npix, ntiles, last ? 0 : 1, err);
-        else
-            k_linear_tiled<<<lin_grid, kTT, smem, s>>>(
-                A, p->pw_w + (size_t)l * d.width * d.width, p->pw_b + (size_t)l * d.width, S, T,
-                d.width, d.width, m.npix, last ? 0 : 1);
+        const unsigned ptiles = (unsigned)((m.npix + kTP - 1) / kTP);
+        const int64_t ntiles = d.batch * ((m.npix + lintc::kRows - 1) / lintc::kRows);
+        int *err = reinterpret_cast<Plan *>(m.spec)->dev_err;
+        const dim3 lin_grid(ptiles, (unsigned)((d.width + kTO - 1) / kTO), (unsigned)d.batch);
+        const size_t smem = sizeof(TileSmem);
+        k_linear_tiled<T><<<lin_grid, kTT, smem, s>>>(static_cast<const T *>(x), p->lift_w,
+                                                      p->lift_b, nullptr, A, d.cin_lift, d.width,
+                                                      m.npix, 0);
         if (cudaGetLastError() != cudaSuccess) return FNO_ERR_CUDA;
-        float *tmp = A;
-        A = T;
-        T = tmp;
-    }
-    if (m.head_tc_grid)
-        lintc::kernel<true>(d.width, d.hidden)<<<m.head_tc_grid, lintc::kThreads,
-                                                 m.head_tc_smem, s>>>(
-            A, p->proj1_w, p->proj1_b, nullptr, p->proj2_w, p->proj2_b,
-            static_cast<float *>(out), d.cout, m.npix, ntiles, 1, err);
-    else
-        projection_kernel(d.cout)<<<dim3(ptiles, (unsigned)d.batch), kTT, smem, s>>>(
-            A, p->proj1_w, p->proj1_b, p->proj2_w, p->proj2_b, static_cast<float *>(out),
-            d.width, d.hidden, d.cout, m.npix);
-    if (cudaGetLastError() != cudaSuccess) return FNO_ERR_CUDA;
-    return FNO_OK;
+        for (int l = 0; l < d.nlayers; ++l) {
+            fno_status_t st = fno_spectral_conv_forward(m.spec, A, spec_w + l * spec_stride, S,
+                                                        m.spec_ws_bytes ? spec_ws : nullptr,
+                                                        stream);
+            if (st != FNO_OK) return st;
+            const int last = (l == d.nlayers - 1);
+            bool done = false;
+            if constexpr (std::is_same<T, float>::value) {
+                if (m.layer_tc_grid) {
+                    lintc::kernel<false>(d.width, d.width)<<<m.layer_tc_grid, lintc::kThreads,
+                                                             m.layer_tc_smem, s>>>(
+                        A, p->pw_w + (size_t)l * d.width * d.width,
+                        p->pw_b + (size_t)l * d.width, S, nullptr, nullptr, Tn, 0, m.npix,
+                        ntiles, last ? 0 : 1, err);
+                    done = true;
+                }
+            }
+            if (!done)
+                k_linear_tiled<T><<<lin_grid, kTT, smem, s>>>(
+                    A, p->pw_w + (size_t)l * d.width * d.width, p->pw_b + (size_t)l * d.width,
+                    S, Tn, d.width, d.width, m.npix, last ? 0 : 1);
+            if (cudaGetLastError() != cudaSuccess) return FNO_ERR_CUDA;
+            T *tmp = A;
+            A = Tn;
+            Tn = tmp;
+        }
+        bool done = false;
+        if constexpr (std::is_same<T, float>::value) {
+            if (m.head_tc_grid) {
+                lintc::kernel<true>(d.width, d.hidden)<<<m.head_tc_grid, lintc::kThreads,
+                                                         m.head_tc_smem, s>>>(
+                    A, p->proj1_w, p->proj1_b, nullptr, p->proj2_w, p->proj2_b,
+                    static_cast<float *>(out), d.cout, m.npix, ntiles, 1, err);
+                done = true;
+            }
+        }
+        if (!done)
+            projection_kernel<T>(d.cout)<<<dim3(ptiles, (unsigned)d.batch), kTT, smem, s>>>(
+                A, p->proj1_w, p->proj1_b, p->proj2_w, p->proj2_b, static_cast<T *>(out),
+                d.width, d.hidden, d.cout, m.npix);
+        if (cudaGetLastError() != cudaSuccess) return FNO_ERR_CUDA;
+        return FNO_OK;
+    });
 }
 
 fno_status_t fno_model_get_device_error(fno_model_t model, fno_stream_t stream) {

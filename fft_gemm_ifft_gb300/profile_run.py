@@ -27,6 +27,8 @@ def main(argv=None) -> int:
     ap.add_argument("--trace", default="", help="write the last call's work-item trace "
                     "(CSV) here and print a per-phase summary")
     ap.add_argument("--time", action="store_true", help="time each forward with CUDA events")
+    ap.add_argument("--dtype", default="f32", choices=["f32", "f16", "bf16"],
+                    help="storage type of the FNO stack (fno2d_f32 workload shape)")
     ap.add_argument("--sets", type=int, default=0,
                     help="input sets rotated over (default: enough to cover twice the L2; "
                          "1 keeps the inputs L2-resident)")
@@ -112,11 +114,15 @@ def run_fno(args) -> int:
     from . import FnoModel, workloads
     case = workloads.FNO_CASE
     batch = args.batch or case.batch
+    dt = args.dtype
     m = FnoModel(batch, case.h, case.w, case.modes, case.cin_lift, case.width, case.nlayers,
-                 case.hidden, case.cout, flags=args.flags)
-    x = torch.from_numpy(workloads.make_fno_inputs(case, batch)).cuda()
-    p = {k: torch.from_numpy(v).cuda() for k, v in workloads.make_fno_params(case).items()}
-    y = torch.empty(m.y_shape, device="cuda")
+                 case.hidden, case.cout, flags=args.flags, dtype=dt)
+    x = workloads.to_torch_storage(
+        workloads.to_storage(workloads.make_fno_inputs(case, batch), dt), dt).cuda()
+    p = {k: (workloads.to_torch_storage(workloads.to_storage(v, dt), dt) if k == "spec_w"
+             else torch.from_numpy(v)).cuda()
+         for k, v in workloads.make_fno_params(case).items()}
+    y = torch.empty(m.y_shape, dtype=m.torch_dtype, device="cuda")
     step = lambda i: m(x, p, y)
     if args.time:
         report_times(case.name, batch, time_steps(step, args.iters))

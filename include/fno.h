@@ -299,14 +299,17 @@ typedef struct fno_model_desc_s {
     int32_t cout;        /* output channels                                     */
     int64_t h, w;        /* grid                                                */
     int32_t modes[2];    /* per-block modes (rows, half-axis bins)              */
-    fno_dtype_t dtype;   /* FNO_F32 only in this version                        */
+    fno_dtype_t dtype;   /* storage of x, activations, spec_w and out: FNO_F32,
+                            FNO_F16 or FNO_BF16 (arithmetic float32 throughout;
+                            the 1x1 weights and biases stay float32)           */
     uint32_t flags;      /* FNO_PLAN_* bits, applied to every spectral layer    */
 } fno_model_desc_t;
 
 typedef struct fno_model_params_s {
     const float *lift_w;   /* (width, cin_lift)                                  */
     const float *lift_b;   /* (width)                                            */
-    const float *spec_w;   /* nlayers x (2, width, width, m0, m1) complex        */
+    const void *spec_w;    /* nlayers x (2, width, width, m0, m1) complex, in the
+                              storage dtype (interleaved re, im)                */
     const float *pw_w;     /* nlayers x (width, width)                           */
     const float *pw_b;     /* nlayers x (width)                                  */
     const float *proj1_w;  /* (hidden, width)                                    */
@@ -317,8 +320,10 @@ typedef struct fno_model_params_s {
 
 /* Validate the description and create the stack's plan (one spectral plan
  * shared by the layers).  Errors as for fno_spectral_conv_plan; also
- * UNSUPPORTED for dtype other than FNO_F32, cout > 8, batch > 65535, or
- * h*w not a multiple of 4.                                                  */
+ * INVALID_ARG for an unknown dtype, UNSUPPORTED for cout > 8,
+ * batch > 65535, or h*w not a multiple of 4.  The 1x1 linears run on the
+ * tensor cores (3xTF32) for float32 storage where the channel counts fit one
+ * tile, else as register-tiled float32 GEMMs.                               */
 fno_status_t fno_model_plan(fno_model_t *model, const fno_model_desc_t *desc);
 
 /* Device workspace bytes fno_forward needs (activations + layer scratch).  */
@@ -328,9 +333,10 @@ fno_status_t fno_model_workspace_size(fno_model_t model, size_t *bytes);
 fno_status_t fno_model_kernel_count(fno_model_t model, int *count);
 
 /* out = FNO(x), enqueued on `stream`.
- *   x    device, (batch, cin_lift, h, w) float32
+ *   x    device, (batch, cin_lift, h, w) in the storage dtype
  *   p    host struct of device pointers (all 16-byte aligned)
- *   out  device, (batch, cout, h, w) float32; must not overlap the inputs
+ *   out  device, (batch, cout, h, w) in the storage dtype; must not overlap
+ *        the inputs
  *   workspace  device, fno_model_workspace_size bytes
  * No allocation, no host synchronisation (graph-capturable).               */
 fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_params_t *p,

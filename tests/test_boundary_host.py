@@ -137,8 +137,8 @@ def test_model_desc_validation(L):
     d.cout = 9                             # more outputs than the projection kernel holds
     assert capi.fno_model_plan(d)[0] == capi.FNO_ERR_UNSUPPORTED
     d.cout = 1
-    d.dtype = F16
-    assert capi.fno_model_plan(d)[0] == capi.FNO_ERR_UNSUPPORTED
+    d.dtype = 7                            # not a storage type
+    assert capi.fno_model_plan(d)[0] == capi.FNO_ERR_INVALID_ARG
     d.dtype = F32
     d.h, d.w = 5, 6                        # h*w not a multiple of 4
     d.modes[0], d.modes[1] = 2, 3

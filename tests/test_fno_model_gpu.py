@@ -72,3 +72,32 @@ def test_full_stack_sampled():
     for b in (0, case.batch - 1):
         ref = oracle.fno_forward(x[b:b + 1], q, case.modes)
         assert_close(got[b:b + 1], ref, "f32", f"FNO b={b}")
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("shape", [
+    # batch, width, nlayers, h, w, modes, hidden, cout
+    (2, 8, 2, 32, 32, (4, 4), 16, 2),
+    (3, 70, 1, 16, 16, (4, 4), 70, 3),           # ragged channel tiles
+    (2, 64, 2, 128, 128, (16, 16), 128, 1),      # the three-kernel 128^2 layer, 16-bit
+], ids=["small", "ragged_channels", "layer_128"])
+def test_stack_16bit_storage(dt, shape):
+    # x, the activations, spec_w and out stored in fp16 / bf16, arithmetic in
+    # float32; the oracle runs in float64 on the same rounded x and spec_w, so
+    # the difference is the rounding of the stored activations (the 16-bit
+    # tolerance class)
+    b, width, nl, h, w, modes, hidden, cout = shape
+    case = workloads.FnoCase("half", batch=b, width=width, nlayers=nl, h=h, w=w, modes=modes,
+                             hidden=hidden, cout=cout)
+    x = workloads.to_storage(workloads.make_fno_inputs(case), dt)
+    p = workloads.make_fno_params(case)
+    p["spec_w"] = workloads.to_storage(p["spec_w"], dt)
+    m = FnoModel(b, h, w, modes, case.cin_lift, width, nl, hidden, cout, dtype=dt)
+    dev = {k: to_dev(v, dt) if k == "spec_w" else to_dev(v) for k, v in p.items()}
+    y = m(to_dev(x, dt), dev)
+    torch.cuda.synchronize()
+    assert y.dtype == m.torch_dtype
+    assert m.device_error() == 0
+    m.close()
+    ref = oracle.fno_forward(x.astype(np.float64), workloads.fno_params_for_oracle(p), modes)
+    assert_close(y.float().cpu().numpy(), ref, dt, f"16-bit FNO stack {shape}")
