@@ -285,6 +285,26 @@ def bench_gpu(args, rank, world, local):
     stream.synchronize()
     assert conv.device_error(stream) == 0
 
+    # L2-resident ("hot") figure for workloads whose set fits in L2: the same
+    # number of forwards on one (x, w, y) set, reported beside the rotated value
+    hot_ms = None
+    if set_bytes < l2:
+        with torch.cuda.stream(stream):
+            g_hot = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_hot, stream=stream):
+                for _ in range(per_graph):
+                    conv(xs[0], ws[0], ys[0], stream=stream)
+            for _ in range(3):
+                g_hot.replay()
+            h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            h0.record(stream)
+            for _ in range(reps):
+                g_hot.replay()
+            h1.record(stream)
+        torch.cuda.synchronize(dev)
+        hot_ms = max_over_ranks(h0.elapsed_time(h1), world, dev) / (reps * per_graph)
+        assert conv.device_error(stream) == 0
+
     # end to end through the public API: every step copies its input from pinned
     # host memory, runs the layer and copies its output back to pinned host
     # memory.  The steps are pipelined over three device buffer slots and three
@@ -325,6 +345,7 @@ def bench_gpu(args, rank, world, local):
             "plan_flags": args.flags,
             "weights": ("packed mode-major once per set, outside the timed region"
                         if args.flags & 128 else "as given (nblk, Cin, Cout, modes)"),
+            "hot_l2_ms_per_step": hot_ms,
         },
         "roofline": {
             "bound": "hbm",
@@ -374,10 +395,24 @@ def cpu_baseline(case, x_np, w_np, seconds: float):
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return {"value": round(done / el, 3), "unit": "samples/s", "cores": oracle.get_threads(),
+    cores = oracle.get_threads()
+    # the same oracle on one thread, over a third of the time
+    oracle.set_threads(1)
+    done1, t1 = 0, time.perf_counter()
+    while True:
+        b = done1 % case.batch
+        oracle.spectral_conv(x_np[b:b + 1].astype(np.float64), wc, case.modes)
+        done1 += 1
+        el1 = time.perf_counter() - t1
+        if el1 >= seconds / 3:
+            break
+    oracle.set_threads(nthreads)
+    return {"value": round(done / el, 3), "unit": "samples/s", "cores": cores,
             "kind": "oracle",
+            "value_1_thread": round(done1 / el1, 3),
             "sample": f"{done} single samples of {case.name} (one batch element each, "
-                      f"{el:.1f} s, float64 radix-2 FFT + explicit loops, OpenMP)"}
+                      f"{el:.1f} s, float64 radix-2 FFT + explicit loops, OpenMP); "
+                      f"one thread: {done1} samples in {el1:.1f} s"}
 
 
 def bench_reference(args, rank, world):
