@@ -1142,23 +1142,6 @@ size_t fused_sync_bytes() { return kSyncBytes; }
 // of an image reduce their partial modes in a cluster.
 using Cfg256 = Cfg<256, 256, 32, 32, 64, 32, 8>;
 
-// Chunking of the three-kernel 128 x 128 path, forward (A) and inverse (C)
-// kernels chosen independently (the mixed modes do not depend on it):
-// 0: 32-row chunks, 16-point row FFTs over 8 lanes; 1: 64-row chunks,
-// 32-point row FFTs over 4 lanes; 2: as 1 with 16-point column FFTs;
-// 3: 64-row chunks, 16-point row FFTs.
-#ifndef FNO_CFG128_A
-#define FNO_CFG128_A 0
-#endif
-#ifndef FNO_CFG128_C
-#define FNO_CFG128_C 0
-#endif
-template <int V>
-using Cfg128V = std::conditional_t<
-    V == 1, Cfg<128, 128, 16, 16, 64, 32, 8>,
-    std::conditional_t<V == 2, Cfg<128, 128, 16, 16, 64, 32, 16>,
-                       std::conditional_t<V == 3, Cfg<128, 128, 16, 16, 64, 16, 8>, Cfg128>>>;
-
 bool is_cfg256(const Geom &g) {
     return g.d == 2 && g.n[0] == 256 && g.n[1] == 256 && g.m[0] == 32 && g.m[1] == 32;
 }
@@ -1435,7 +1418,7 @@ struct Pdl {
     }
 };
 
-using Pdl128 = Pdl<Cfg128V<FNO_CFG128_A>, Cfg128V<FNO_CFG128_C>>;
+using Pdl128 = Pdl<Cfg128>;
 
 enum Variant { kVarNone, kVarPdl128, kVarPdl256, kVarPersistent128, kVarPdl3d, kVarOne1d };
 
