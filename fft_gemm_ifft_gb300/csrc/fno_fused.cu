@@ -637,7 +637,8 @@ struct GeoC {
     static constexpr uint32_t kS = kY + NK * 8;         // [A][B2][M1] residue sums, 64 KiB
     static constexpr uint32_t kTw = kS + A * B2 * M1 * 8;
     static constexpr uint32_t kSmem = kTw + N0 * 8 + 1024;
-    static constexpr uint32_t kStage = kS;              // 2 x 16 KiB output boxes over S
+    static_assert(A * B2 * M1 * 8 >= 4 * kTile && MT * 2 * kTile >= 4 * kTile,
+                  "two rounds of output boxes fit over the sums and over the operand");
     static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -748,17 +749,19 @@ k_phase_c_tc(const __grid_constant__ CUtensorMap ymap, Args a, const void *table
     ok &= mbar_wait(&bar_mma, 0, a.err);
     tc_after_sync();
     // 3. rows out: warp w reads lanes 32 (w % 4).. of tensor memory; the two warp
-    //    halves take column blocks 2h and 2h + 1 (64 outputs each) per tile
+    //    halves take column blocks 2h and 2h + 1 (64 outputs each) per tile.
+    //    Round r = 2 t + step stages its two 64-column boxes in a region of its
+    //    own (rounds 0, 1 over the residue sums, 2, 3 over the Zo operand, both
+    //    free once the MMAs completed), so no round waits for an earlier store.
     const float scale = 1.0f / ((float)Gm::N0 * (float)Gm::N1);
     const int half = warp >> 2, lrow = 32 * (warp & 3) + (tid & 31);
-    char *stage = base + Gm::kStage + half * Gm::kTile;
     for (int t = 0; t < Gm::MT; ++t) {
         for (int step = 0; step < 2; ++step) {
             const int cb = 2 * half + step;               // 64-column block of y
-            if (t | step) {
-                if (tid == 0) bulk_wait_read();           // the staging tiles were stored
-                __syncthreads();
-            }
+            const int round = 2 * t + step;
+            char *region = base + (round < 2 ? Gm::kS + round * 2 * Gm::kTile
+                                             : Gm::kA + (round - 2) * 2 * Gm::kTile);
+            char *stage = region + half * Gm::kTile;
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 float v[16];
@@ -790,12 +793,12 @@ k_phase_c_tc(const __grid_constant__ CUtensorMap ymap, Args a, const void *table
             if (tid == 0) {
                 for (int h = 0; h < 2; ++h)
                     tma_store_2d(&ymap, 64 * (2 * h + step), img * Gm::N0 + 128 * t,
-                                 tc_smem_addr(base + Gm::kStage + h * Gm::kTile));
+                                 tc_smem_addr(region + h * Gm::kTile));
                 bulk_commit();
             }
         }
     }
-    if (tid == 0) bulk_wait_all();
+    if (tid == 0) bulk_wait_read();              // the staging regions may be released
     tc_before_sync();
     __syncthreads();
     if (warp == 0) {
