@@ -18,6 +18,8 @@
 // the four chains into four column ranges of tensor memory, and writes Y for
 // the four modes of every (b, o) as one 32-byte piece through a shared-memory
 // staging tile.  Channel counts up to 64 are zero-padded to the tile.
+#include <type_traits>
+
 #include "fno_fused_dev.cuh"
 #include "fno_tc.cuh"
 
@@ -27,16 +29,20 @@ namespace {
 using namespace tcu;
 
 constexpr int kMT = 256;                  // threads
-constexpr int kRun = 4;                   // modes per CTA
+#ifndef FNO_MIX_RUN
+#define FNO_MIX_RUN 4
+#endif
+constexpr int kRun = FNO_MIX_RUN;         // modes per CTA (2 or 4)
+static_assert(kRun == 2 || kRun == 4, "modes per CTA");
 constexpr int kCh = 64;                   // channel tile (Cin, Cout <= 64)
 constexpr uint32_t kAChunk = 128 * 128;   // 128 rows x 128 bytes (64 elements of K)
 constexpr uint32_t kAMode = 2 * kAChunk;  // one mode's weight operand (K = 128)
 constexpr int kMaxB = 64;                 // batch rows (N) per CTA
 constexpr uint32_t kBChunk = kMaxB * 128;
 constexpr uint32_t kBMode = 2 * kBChunk;
-constexpr uint32_t kOffB = kRun * kAMode;                 // 128 KiB of weight operands
-constexpr uint32_t kSmem = kOffB + kRun * kBMode + 1024;  // + 64 KiB of X operands + align
-constexpr uint32_t kTmemCols = 256;                        // kRun x N (N <= 64)
+constexpr uint32_t kOffB = kRun * kAMode;                 // weight operands, 32 KiB a mode
+constexpr uint32_t kSmem = kOffB + kRun * kBMode + 1024;  // + X operands, 16 KiB a mode + align
+constexpr uint32_t kTmemCols = kRun * 64;                  // kRun x N (N <= 64)
 
 template <typename T> struct Bits;
 template <> struct Bits<__half> {
@@ -53,7 +59,7 @@ template <> struct Bits<__nv_bfloat16> {
 };
 
 template <typename T>
-__global__ void __launch_bounds__(kMT, 1) k_mix_tc(MixTcArgs a) {
+__global__ void __launch_bounds__(kMT, kRun == 2 ? 2 : 1) k_mix_tc(MixTcArgs a) {
     extern __shared__ __align__(1024) char smem_raw[];
     char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
@@ -91,12 +97,14 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_tc(MixTcArgs a) {
     for (int un = tid; un < kCh * (kCh / 8); un += kMT) {
         const int o = un % kCh, i0 = 8 * (un / kCh);
         if (o >= a.cout || i0 >= a.cin) continue;
-        uint4 q[8];
+        // the run's kRun modes of one (i, o): kRun x 4 bytes, contiguous in both layouts
+        using WV = std::conditional_t<kRun == 4, uint4, uint2>;
+        WV q[8];
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-            q[t] = make_uint4(0, 0, 0, 0);
+            q[t] = WV{};
             if (i0 + t < a.cin)
-                q[t] = __ldg(reinterpret_cast<const uint4 *>(
+                q[t] = __ldg(reinterpret_cast<const WV *>(
                     a.packed ? w + packed_index(mode0, i0 + t, o, a.cin, a.cout) * 2
                              : w + ((((size_t)blk * a.cin + i0 + t) * a.cout + o) * a.mblk +
                                     local0) * 2));
@@ -107,7 +115,7 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_tc(MixTcArgs a) {
             U re[8], im[8];
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-                const uint32_t word = r == 0 ? q[t].x : (r == 1 ? q[t].y : (r == 2 ? q[t].z : q[t].w));
+                const uint32_t word = reinterpret_cast<const uint32_t *>(&q[t])[r];
                 re[t] = (U)(word & 0xFFFF);
                 im[t] = (U)(word >> 16);
             }
@@ -136,15 +144,17 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_tc(MixTcArgs a) {
     //    mode two 16-byte stores
     for (int un = tid; un < nbp * (kCh / 8); un += kMT) {
         const int bb = un / (kCh / 8), i0 = 8 * (un % (kCh / 8));
-        float4 v[16];
+        constexpr int kV = kRun / 2;                     // float4 per (b, i): two modes each
+        float4 v[8 * kV];
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-            v[2 * t] = v[2 * t + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int h = 0; h < kV; ++h) v[kV * t + h] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (bb < a.batch && i0 + t < a.cin) {
                 const float4 *src = reinterpret_cast<const float4 *>(
                     a.X + ((size_t)bb * a.cin + i0 + t) * a.nk + mode0);
-                v[2 * t] = __ldcg(src);
-                v[2 * t + 1] = __ldcg(src + 1);
+#pragma unroll
+                for (int h = 0; h < kV; ++h) v[kV * t + h] = __ldcg(src + h);
             }
         }
 #pragma unroll
@@ -155,7 +165,7 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_tc(MixTcArgs a) {
                 float xr[2], xi[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const float4 &u4 = v[2 * (2 * t2 + h) + r / 2];
+                    const float4 &u4 = v[kV * (2 * t2 + h) + r / 2];
                     xr[h] = (r & 1) ? u4.z : u4.x;
                     xi[h] = (r & 1) ? u4.w : u4.y;
                 }
@@ -196,7 +206,8 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_tc(MixTcArgs a) {
     {
         const int m = 32 * (warp & 3) + (tid & 31);          // D row: o (re) or 64 + o (im)
         const int o = m % kCh, part = m / kCh;
-        for (int r = 2 * (warp >> 2); r < 2 * (warp >> 2) + 2; ++r) {
+        // warps 0-3 the first half of the run's modes, warps 4-7 the second
+        for (int r = (kRun / 2) * (warp >> 2); r < (kRun / 2) * (warp >> 2) + kRun / 2; ++r) {
             for (int g = 0; g < nbp / 16; ++g) {
                 float v[16];
                 tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + r * nbp + 16 * g, v);
@@ -213,13 +224,13 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_tc(MixTcArgs a) {
     }
     tc_before_sync();
     __syncthreads();
-    // 5. Y for the four modes of every (b, o): 32 contiguous bytes
+    // 5. Y for the run's modes of every (b, o): kRun x 8 contiguous bytes
     for (int e = tid; e < a.batch * a.cout; e += kMT) {
         const int b = e / a.cout, o = e % a.cout;
         const float4 *s4 = reinterpret_cast<const float4 *>(stage + ((size_t)b * kCh + o) * kRun * 2);
         float4 *dst = reinterpret_cast<float4 *>(a.Y + ((size_t)b * a.cout + o) * a.nk + mode0);
-        __stcg(dst, s4[0]);
-        __stcg(dst + 1, s4[1]);
+#pragma unroll
+        for (int h = 0; h < kRun / 2; ++h) __stcg(dst + h, s4[h]);
     }
     if (warp == 0) {
         tc_after_sync();
