@@ -61,7 +61,9 @@ struct Cfg3 {
     // shared memory: twiddles W_N1 [N1], the row tables [2][P][TS], W_N0 [N0]
     static constexpr size_t kSmemTw = ((N1 + 2 * Pl::P * Pl::TS + N0) * 8 + 15) / 16 * 16;
     template <typename T>
-    static constexpr size_t stage_bytes() { return (size_t)N1 * Pl::XS * sizeof(T); }
+    static constexpr size_t stage_bytes() {
+        return (size_t)N1 * Pl::template xs_of<T>() * sizeof(T);
+    }
     template <typename T>
     static constexpr size_t ring_bytes() {
         // the ring also holds the chunk's residues [R0][NKP] at the end
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(kNT) k_phase_a3(Args a) {
     const T *src = static_cast<const T *>(a.x) + (size_t)vol * N0 * N1 * N2;
     pdl_trigger();                               // kernel B may start fetching weights
 
-    // plane c + C0 t into stage t % S, rows padded to Pl::XS samples
+    // plane c + C0 t into stage t % S, rows padded to xs_of<T>() samples
     auto issue = [&](int t) {
         T *dst = reinterpret_cast<T *>(ring + (t % S) * kStage);
         const T *p = src + (size_t)(c + C0 * t) * N1 * N2;
@@ -140,7 +142,8 @@ __global__ void __launch_bounds__(kNT) k_phase_a3(Args a) {
         constexpr int kRow = N2 / kPer;
         for (int e = threadIdx.x; e < N1 * kRow; e += kNT) {
             const int row = e / kRow, s = e % kRow;
-            cp_async16(dst + row * Pl::XS + s * kPer, p + (size_t)row * N2 + s * kPer);
+            cp_async16(dst + row * Pl::template xs_of<T>() + s * kPer,
+                       p + (size_t)row * N2 + s * kPer);
         }
     };
 #pragma unroll
@@ -162,7 +165,7 @@ __global__ void __launch_bounds__(kNT) k_phase_a3(Args a) {
         asm volatile("cp.async.wait_group %0;" ::"n"(S - 1) : "memory");
         __syncthreads();                         // plane t is in its stage
         const T *xs = reinterpret_cast<const T *>(ring + (t % S) * kStage);
-        a_row_dft<Pl, T>(xs, zs, tw);
+        a_row_dft<Pl, T, Pl::template xs_of<T>()>(xs, zs, tw);
         __syncthreads();
         float2 *ss = reinterpret_cast<float2 *>(ring + (t % S) * kStage);   // plane t consumed
         a_col_fft<Pl>(zs, ss);

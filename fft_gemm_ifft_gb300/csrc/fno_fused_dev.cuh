@@ -68,7 +68,16 @@ struct Cfg {
     static constexpr int P = N1 / Q;             // row partial sums per bin
     static constexpr int B2 = B2_;               // column FFT length
     static constexpr int A = RC / B2;            // column partial sums
-    static constexpr int XS = N1 + 8;            // x row stride in smem (floats)
+    // x row stride in shared memory (floats): the P lanes of a row read
+    // consecutive samples and a warp's 32 / P rows start P banks apart, so the
+    // row DFT's loads are conflict-free
+    static constexpr int XS = N1 + P;
+    // row stride of raw storage-type rows (the 3-D plane ring): XS where its rows
+    // stay 16-byte aligned, else N1 + 8
+    template <typename S>
+    static constexpr int xs_of() {
+        return ((size_t)XS * sizeof(S)) % 16 == 0 ? XS : N1 + 8;
+    }
     static constexpr int ZS = M1 + 4;            // Z row stride in smem (float2)
     static constexpr int TS = M1 + 1;            // per-lane twiddle row stride (float2)
     static constexpr int PAIRS = RC * P / 2;     // row-FFT work units (2 rows each)
@@ -269,9 +278,9 @@ __device__ __forceinline__ float smp(const float *p) { return *p; }
 __device__ __forceinline__ float smp(const __half *p) { return __half2float(*p); }
 __device__ __forceinline__ float smp(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 
-template <class Cf, typename S = float>
+template <class Cf, typename S = float, int XS = Cf::XS>
 __device__ __forceinline__ void a_row_dft(const S *xs, float2 *zs, Tw tw) {
-    constexpr int RC = Cf::RC, P = Cf::P, Q = Cf::Q, M1 = Cf::M1, XS = Cf::XS, ZS = Cf::ZS;
+    constexpr int RC = Cf::RC, P = Cf::P, Q = Cf::Q, M1 = Cf::M1, ZS = Cf::ZS;
     constexpr int KB = Cf::KB;
     for (int pr = threadIdx.x; pr < Cf::PAIRS; pr += kNT) {
         const int t = pr / P, n1 = pr % P, t2 = t + RC / 2;
