@@ -1206,6 +1206,7 @@ struct Pdl {
     static void *kernel_b() {
         return reinterpret_cast<void *>(&k_phase_b<Cf, T, NP, kBThreads>);
     }
+
     template <typename T>
     static cudaError_t init(Plan &p) {
         const size_t w2 = p.dtype == FNO_F32 ? 16 : 8;
@@ -1265,6 +1266,7 @@ struct Pdl {
                         mixtc_supported(p.g.d, p.dtype, p.batch, p.cin, p.cout, Cf::M1,
                                         p.g.nkept);
         if (e == cudaSuccess && p.fused_mixtc) e = mixtc_init(p.dtype);
+        p.fused_bstream = 0;
 
         if (e == cudaSuccess && (p.flags & FNO_PLAN_TRACE)) {
             const size_t nB = p.fused_mixtc ? (size_t)mixtc_items(p.g.nkept)

@@ -16,8 +16,10 @@
 //     of the volume is X[f] = sum_c W_N0^{f c} P_c[f mod R0] (one decimation-
 //     in-time step); the cluster's CTAs evaluate it through distributed shared
 //     memory, each for one C0-th of the plane modes, and write X once.
-//   kernel B  the per-mode channel mixing shared with the 2-D kernels: every
-//     item reads its weight slab once for all batch rows.
+//   kernel B  the per-mode channel mixing.  For batches up to 16 (few rows per
+//     weight) the weight-streaming kernel: one CTA per run of 8 modes of a
+//     last-axis line, thread (o, r) reading W straight from global memory for
+//     every batch row; otherwise the slab kernel shared with the 2-D layers.
 //   kernel C  (volume, chunk c).  Z_c[r] = sum_{f = r mod R0} Y[f] conj(W_N0^{f c});
 //     an R0-point inverse DFT over r gives the 2-D spectra of the planes
 //     c + C0 t, and each plane's inverse (column transform back to N1 rows,
@@ -50,6 +52,7 @@ struct Cfg3 {
     // weights: block b = h0 + 2 h1 (h_a = 1 for the high kept rows on axis a),
     // each M0 x M1 x M2 modes
     static constexpr size_t MBLK = (size_t)M0 * M1 * M2;
+    static constexpr int MR = M2;                  // kept modes along one line of the last axis
     __device__ static void wmap(int o, int &blk, int &local) {
         const int j0 = o / NKP, rest = o % NKP;
         const int j1 = rest / M2, k = rest % M2;
@@ -270,6 +273,9 @@ __global__ void __launch_bounds__(kNT) k_phase_c3(Args a) {
     cta_record(a, 2, a.trace_c, t0, t1);
 }
 
+#ifndef FNO_MIX_STREAM
+#define FNO_MIX_STREAM 1
+#endif
 template <class C3>
 struct Pdl3 {
     static int batch_block(int64_t batch, int cin) {
@@ -287,6 +293,13 @@ struct Pdl3 {
         const size_t w2 = dt == FNO_F32 ? 16 : 8;
         return ((size_t)cin * ob * w2 + 15) / 16 * 16 + (size_t)bb * cin * 16;
     }
+    static constexpr int kStreamR = 8;           // modes per CTA of the streaming mixing
+    template <typename T>
+    static void *stream_kernel(int64_t batch) {
+        if (batch <= 4) return reinterpret_cast<void *>(&k_mix_stream<C3, T, 1, kStreamR, 4>);
+        if (batch <= 8) return reinterpret_cast<void *>(&k_mix_stream<C3, T, 1, kStreamR, 8>);
+        return reinterpret_cast<void *>(&k_mix_stream<C3, T, 1, kStreamR, 16>);
+    }
     template <typename T>
     static cudaError_t init(Plan &p) {
         const int ob = out_block(p.dtype, p.cin, p.cout), bb = batch_block(p.batch, p.cin);
@@ -299,9 +312,18 @@ struct Pdl3 {
         p.fused_ob = ob;
         p.fused_smem = smem_b(p.dtype, p.cin, ob + 1, bb);   // padded slab rows
         p.fused_grid = 0;
+        // small batches: the weight-streaming mixing (each weight serves few rows)
+        p.fused_bstream = 0;
+        const size_t xs = (size_t)p.batch * p.cin * kStreamR * 8;   // the run's kept modes
+        if (FNO_MIX_STREAM && p.batch <= 16 && p.cout * kStreamR <= 4 * kMixThreads &&
+            xs <= (64u << 10)) {
+            p.fused_bstream = kStreamR;
+            if (e == cudaSuccess) e = raise_smem_limit(stream_kernel<T>(p.batch), xs);
+        }
         if (e == cudaSuccess && (p.flags & FNO_PLAN_TRACE)) {
-            const size_t nB = (size_t)(C3::NK / kG) * ((p.cout + ob - 1) / ob) *
-                              ((p.batch + bb - 1) / bb);
+            const size_t nB = p.fused_bstream ? (size_t)(C3::NK / p.fused_bstream)
+                                              : (size_t)(C3::NK / kG) * ((p.cout + ob - 1) / ob) *
+                                                    ((p.batch + bb - 1) / bb);
             p.trace_records = (size_t)p.batch * (p.cin + p.cout) * C3::C0 + nB;
             e = cudaMalloc(&p.trace, p.trace_records * sizeof(fno_trace_record_t));
         }
@@ -316,7 +338,8 @@ struct Pdl3 {
         a.npairs = C3::NK / kG;
         a.trace = p.trace;
         a.trace_b = (int)(p.batch * p.cin * C3::C0);
-        a.trace_c = a.trace_b + a.npairs * a.nob * a.ng;
+        a.trace_c = a.trace_b + (p.fused_bstream ? C3::NK / p.fused_bstream
+                                                 : a.npairs * a.nob * a.ng);
         cudaLaunchAttribute cl;
         cl.id = cudaLaunchAttributeClusterDimension;
         cl.val.clusterDim.x = C3::C0;
@@ -339,10 +362,22 @@ struct Pdl3 {
         cfg.stream = s;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        cfg.gridDim = dim3((unsigned)(a.npairs * a.nob * a.ng));
-        cfg.blockDim = dim3(kNT);
-        cfg.dynamicSmemBytes = p.fused_smem;
-        e = cudaLaunchKernelEx(&cfg, k_phase_b<C3, T, 1, kNT>, a);
+        if (p.fused_bstream) {
+            cfg.gridDim = dim3((unsigned)(C3::NK / p.fused_bstream));
+            cfg.blockDim = dim3(kMixThreads);
+            cfg.dynamicSmemBytes = (size_t)p.batch * p.cin * p.fused_bstream * 8;
+            if (p.batch <= 4)
+                e = cudaLaunchKernelEx(&cfg, k_mix_stream<C3, T, 1, kStreamR, 4>, a);
+            else if (p.batch <= 8)
+                e = cudaLaunchKernelEx(&cfg, k_mix_stream<C3, T, 1, kStreamR, 8>, a);
+            else
+                e = cudaLaunchKernelEx(&cfg, k_mix_stream<C3, T, 1, kStreamR, 16>, a);
+        } else {
+            cfg.gridDim = dim3((unsigned)(a.npairs * a.nob * a.ng));
+            cfg.blockDim = dim3(kNT);
+            cfg.dynamicSmemBytes = p.fused_smem;
+            e = cudaLaunchKernelEx(&cfg, k_phase_b<C3, T, 1, kNT>, a);
+        }
         if (e != cudaSuccess) return e;
         cfg.gridDim = dim3((unsigned)(p.batch * p.cout * C3::C0));
         cfg.blockDim = dim3(kNT);

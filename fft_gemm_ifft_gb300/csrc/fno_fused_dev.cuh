@@ -99,6 +99,7 @@ struct Cfg {
     // weights: block 0 holds the low kept rows, block 1 the high ones, each
     // M0 x M1 modes
     static constexpr size_t MBLK = (size_t)M0 * M1;
+    static constexpr int MR = M1;                // kept modes along one line of the last axis
     __device__ static void wmap(int o, int &blk, int &local) {
         const int j = o / M1, k = o % M1;
         blk = j >= M0 ? 1 : 0;
@@ -802,6 +803,82 @@ __device__ __forceinline__ BItem b_item(const Args &a, int it) {
     bi.b0 = bblk * a.bg;
     bi.nbb = min(a.bg, a.batch - bi.b0);
     return bi;
+}
+
+// Mixing that streams the weights: one CTA per run of R adjacent kept modes
+// (one line of the last axis), every output channel and batch row.  The run's
+// kept modes X[b][i][r] (summed over the partial copies) go to shared memory;
+// thread (o, r) then walks the input channels, reading W[blk][i][o][local + r]
+// straight from global memory (a warp reads 32 / R runs of R x 8 contiguous
+// bytes) and accumulating Y[b][o][r] for the kMaxB batch rows in registers.
+// Each weight is read once and used for every batch row with no shared-memory
+// staging; for small batches this is the weight stream's own bound.
+constexpr int kMixThreads = 256;
+#ifndef FNO_MIX_STREAM_DEPTH
+#define FNO_MIX_STREAM_DEPTH 8
+#endif
+template <class Cf, typename T, int kParts, int R, int kMaxB>
+__global__ void __launch_bounds__(kMixThreads) k_mix_stream(Args a) {
+    extern __shared__ __align__(16) char smem[];
+    float2 *xs = reinterpret_cast<float2 *>(smem);          // [batch][cin][R]
+    static_assert(Cf::MR % R == 0, "a run stays on one line of the last axis");
+    const int tid = threadIdx.x;
+    const int mode0 = blockIdx.x * R;
+    int blk, local;
+    Cf::wmap(mode0, blk, local);
+    const unsigned long long t0 = a.trace ? trace_now() : 0;
+    pdl_trigger();
+    pdl_wait();                                  // kernel A's kept modes are complete
+    const unsigned long long t1 = a.trace ? trace_now() : 0;
+    constexpr int NK = Cf::NK;
+    const int nimg = a.batch * a.cin;
+    for (int e = tid; e < nimg * R; e += kMixThreads) {
+        const int r = e % R, row = e / R;
+        float2 acc = __ldcg(a.part + (size_t)row * NK + mode0 + r);
+#pragma unroll
+        for (int p = 1; p < kParts; ++p) {
+            const float2 v = __ldcg(a.part + ((size_t)p * nimg + row) * NK + mode0 + r);
+            acc.x += v.x;
+            acc.y += v.y;
+        }
+        xs[e] = acc;
+    }
+    __syncthreads();
+    const T *w = static_cast<const T *>(a.w);
+    const size_t istride = (size_t)a.cout * Cf::MBLK * 2;    // next input channel (elements)
+    for (int e = tid; e < a.cout * R; e += kMixThreads) {
+        const int r = e % R, o = e / R;
+        float2 acc[kMaxB];
+#pragma unroll
+        for (int b = 0; b < kMaxB; ++b) acc[b] = make_float2(0.f, 0.f);
+        const T *wp = w + ((((size_t)blk * a.cin) * a.cout + o) * Cf::MBLK + local + r) * 2;
+        // kWv weights in flight before the first product
+        constexpr int kWv = FNO_MIX_STREAM_DEPTH;
+        for (int i0 = 0; i0 < a.cin; i0 += kWv) {
+            float2 wv[kWv];
+#pragma unroll
+            for (int q = 0; q < kWv; ++q) {
+                const int i = i0 + q;
+                wv[q] = i < a.cin ? Storage<T>::load2(
+                                        a.wpacked ? w + packed_index(mode0 + r, i, o, a.cin,
+                                                                     a.cout) * 2
+                                                  : wp + (size_t)i * istride)
+                                  : make_float2(0.f, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < kWv; ++q) {
+                const int i = i0 + q;
+                if (i >= a.cin) break;
+#pragma unroll
+                for (int b = 0; b < kMaxB; ++b)
+                    if (b < a.batch) cmac(acc[b], xs[(b * a.cin + i) * R + r], wv[q]);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kMaxB; ++b)
+            if (b < a.batch) __stcg(a.Y + ((size_t)b * a.cout + o) * NK + mode0 + r, acc[b]);
+    }
+    cta_record(a, 1, a.trace_b, t0, t1);
 }
 
 template <class Cf, typename T, int kParts, int kNTB>

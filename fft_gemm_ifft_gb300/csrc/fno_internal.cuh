@@ -53,6 +53,7 @@ struct Plan {
     size_t fused_smem;
     int fused_ob;
     int fused_bb;
+    int fused_bstream;            // > 0: kernel B streams the weights, this many modes a CTA
     void *fused_tables;           // tensor-core path: twiddle operands (plan-owned)
     bool fused_mixtc;             // three-kernel path mixes on the tensor cores
     bool fused_tca;               // three-kernel path transforms (kernel A) on the tensor cores
