@@ -75,8 +75,12 @@ struct Cfg3 {
     }
     template <typename T>
     static constexpr size_t smem_a() { return kSmemTw + ring_bytes<T>() + (size_t)N1 * Pl::ZS * 8; }
-    static constexpr size_t kSmemC = kSmemTw + (size_t)R0 * NKP * 8 + (size_t)N1 * M2 * 8 +
-                                     (size_t)Pl::A * Pl::B2 * M2 * 8 + (size_t)N1 * Pl::ZS * 8;
+    // kernel C: twiddles, the chunk's plane spectra [R0][NKP], the residue sums
+    // [A][B2][M2], and one region that holds a plane's residues [N1][M2] until
+    // the column pass has read them and its spectral rows [N1][ZS] after
+    static constexpr size_t kSmemC = kSmemTw + (size_t)R0 * NKP * 8 +
+                                     (size_t)Pl::A * Pl::B2 * M2 * 8 +
+                                     (size_t)N1 * (Pl::ZS > M2 ? Pl::ZS : M2) * 8;
     static_assert(stage_bytes<float>() % 16 == 0 && stage_bytes<__half>() % 16 == 0, "align");
     static_assert((size_t)Pl::A * Pl::B2 * M2 * 8 <= stage_bytes<__half>(),
                   "the column pass works in the stage of its plane");
@@ -223,9 +227,9 @@ __global__ void __launch_bounds__(kNT) k_phase_c3(Args a) {
     const float2 *twa;
     const Tw tw = load_tw3<C3>(a, smem, &twa);
     float2 *spec = reinterpret_cast<float2 *>(smem + C3::kSmemTw);   // [R0][NKP]
-    float2 *vs = spec + R0 * NKP;                                    // [N1][M2]
-    float2 *ss = vs + N1 * M2;                                       // [A][B2][M2]
-    float2 *zo = ss + Pl::A * Pl::B2 * M2;                           // [N1][ZS]
+    float2 *ss = spec + R0 * NKP;                                    // [A][B2][M2]
+    float2 *vs = ss + Pl::A * Pl::B2 * M2;                           // [N1][M2], then
+    float2 *zo = vs;                                                 // [N1][ZS]
     __syncthreads();
     pdl_wait();                                  // kernel B's mixed modes are complete
     const unsigned long long t1 = a.trace ? trace_now() : 0;
@@ -267,8 +271,8 @@ __global__ void __launch_bounds__(kNT) k_phase_c3(Args a) {
         __syncthreads();
         c_col_combine<Pl>(ss, zo, tw);
         __syncthreads();
-        // zo is rewritten two barriers after this pass, vs and ss earlier ones
         c_row_store<Pl, T>(zo, dst + (size_t)(c + C0 * t) * N1 * N2, 0, tw);
+        __syncthreads();                         // zo is the next plane's residue region
     }
     cta_record(a, 2, a.trace_c, t0, t1);
 }
