@@ -289,6 +289,9 @@ __global__ void __launch_bounds__(kNT) k_phase_c3(Args a) {
 #ifndef FNO_MIX_STREAM
 #define FNO_MIX_STREAM 1
 #endif
+#ifndef FNO_STREAM_R
+#define FNO_STREAM_R 16
+#endif
 template <class C3>
 struct Pdl3 {
     static int batch_block(int64_t batch, int cin) {
@@ -306,7 +309,7 @@ struct Pdl3 {
         const size_t w2 = dt == FNO_F32 ? 16 : 8;
         return ((size_t)cin * ob * w2 + 15) / 16 * 16 + (size_t)bb * cin * 16;
     }
-    static constexpr int kStreamR = 8;           // modes per CTA of the streaming mixing
+    static constexpr int kStreamR = FNO_STREAM_R;   // modes per CTA of the streaming mixing
     template <typename T>
     static void *stream_kernel(int64_t batch) {
         if (batch <= 4) return reinterpret_cast<void *>(&k_mix_stream<C3, T, 1, kStreamR, 4>);

@@ -808,9 +808,10 @@ __device__ __forceinline__ BItem b_item(const Args &a, int it) {
 // Mixing that streams the weights: one CTA per run of R adjacent kept modes
 // (one line of the last axis), every output channel and batch row.  The run's
 // kept modes X[b][i][r] (summed over the partial copies) go to shared memory;
-// thread (o, r) then walks the input channels, reading W[blk][i][o][local + r]
-// straight from global memory (a warp reads 32 / R runs of R x 8 contiguous
-// bytes) and accumulating Y[b][o][r] for the kMaxB batch rows in registers.
+// thread (o, r-pair) then walks the input channels, reading two modes of
+// W[blk][i][o][local + r] per load straight from global memory (a warp reads
+// 64 / R runs of R x 8 contiguous bytes) and accumulating Y[b][o][r..r+1]
+// for the kMaxB batch rows in registers.
 // Each weight is read once and used for every batch row with no shared-memory
 // staging; for small batches this is the weight stream's own bound.
 constexpr int kMixThreads = 256;
@@ -846,37 +847,49 @@ __global__ void __launch_bounds__(kMixThreads) k_mix_stream(Args a) {
     __syncthreads();
     const T *w = static_cast<const T *>(a.w);
     const size_t istride = (size_t)a.cout * Cf::MBLK * 2;    // next input channel (elements)
-    for (int e = tid; e < a.cout * R; e += kMixThreads) {
-        const int r = e % R, o = e / R;
-        float2 acc[kMaxB];
+    // thread (o, rp): modes r = 2 rp and 2 rp + 1 of the run, one 2-mode load a weight
+    static_assert(R % 2 == 0, "mode pairs");
+    constexpr int RP = R / 2;
+    for (int e = tid; e < a.cout * RP; e += kMixThreads) {
+        const int r = 2 * (e % RP), o = e / RP;
+        float2 acc0[kMaxB], acc1[kMaxB];
 #pragma unroll
-        for (int b = 0; b < kMaxB; ++b) acc[b] = make_float2(0.f, 0.f);
+        for (int b = 0; b < kMaxB; ++b) acc0[b] = acc1[b] = make_float2(0.f, 0.f);
         const T *wp = w + ((((size_t)blk * a.cin) * a.cout + o) * Cf::MBLK + local + r) * 2;
-        // kWv weights in flight before the first product
+        // kWv weight pairs in flight before the first product
         constexpr int kWv = FNO_MIX_STREAM_DEPTH;
         for (int i0 = 0; i0 < a.cin; i0 += kWv) {
-            float2 wv[kWv];
+            float4 wv[kWv];
 #pragma unroll
             for (int q = 0; q < kWv; ++q) {
                 const int i = i0 + q;
-                wv[q] = i < a.cin ? Storage<T>::load2(
+                wv[q] = i < a.cin ? Storage<T>::load4(
                                         a.wpacked ? w + packed_index(mode0 + r, i, o, a.cin,
                                                                      a.cout) * 2
                                                   : wp + (size_t)i * istride)
-                                  : make_float2(0.f, 0.f);
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int q = 0; q < kWv; ++q) {
                 const int i = i0 + q;
                 if (i >= a.cin) break;
+                const float2 w0 = make_float2(wv[q].x, wv[q].y), w1 = make_float2(wv[q].z, wv[q].w);
 #pragma unroll
-                for (int b = 0; b < kMaxB; ++b)
-                    if (b < a.batch) cmac(acc[b], xs[(b * a.cin + i) * R + r], wv[q]);
+                for (int b = 0; b < kMaxB; ++b) {
+                    if (b < a.batch) {
+                        const float4 x2 = *reinterpret_cast<const float4 *>(
+                            &xs[(b * a.cin + i) * R + r]);
+                        cmac(acc0[b], make_float2(x2.x, x2.y), w0);
+                        cmac(acc1[b], make_float2(x2.z, x2.w), w1);
+                    }
+                }
             }
         }
 #pragma unroll
         for (int b = 0; b < kMaxB; ++b)
-            if (b < a.batch) __stcg(a.Y + ((size_t)b * a.cout + o) * NK + mode0 + r, acc[b]);
+            if (b < a.batch)
+                __stcg(reinterpret_cast<float4 *>(a.Y + ((size_t)b * a.cout + o) * NK + mode0 + r),
+                       make_float4(acc0[b].x, acc0[b].y, acc1[b].x, acc1[b].y));
     }
     cta_record(a, 1, a.trace_b, t0, t1);
 }
