@@ -242,8 +242,9 @@ k_projection_tiled(const T *__restrict__ a, const float *__restrict__ P1,
 // owns one pixel row and writes 16-byte pieces, conflict-free under the
 // swizzle).  Three chains (hi*hi + hi*lo + lo*hi) accumulate in tensor
 // memory; the epilogue reads one pixel's N sums per thread (32x32b loads, a
-// warp per 32 lanes) and applies bias, the spectral sum and GELU (layer) or
-// GELU and the second projection (head).  A CTA walks tiles grid-stride.
+// warp per 32 lanes) and applies bias, the spectral sum and GELU (layer,
+// k_linear_tc) or GELU and the second projection (head, k_head_tc, which
+// double-buffers the tile and the accumulator).  A CTA walks tiles grid-stride.
 // ---------------------------------------------------------------------------
 namespace lintc {
 
@@ -267,17 +268,19 @@ __host__ __device__ inline Smem smem_map(int k, int n) {
     return s;
 }
 
-// kHead = false: out[b][o][p] = act(sum_i W[o][i] a[b][i][p] + bias[o] + add[b][o][p])
-// kHead = true:  out[b][q][p] = sum_h P2[q][h] gelu(sum_i W[h][i] a[b][i][p] + bias[h]) + c2[q]
+// out[b][o][p] = act(sum_i W[o][i] a[b][i][p] + bias[o] + add[b][o][p])
 // KC = input channels / 32, NG = output channels / 16 (fully unrolled, so that
 // every load of a tile is in flight before its first use)
-template <bool kHead, int KC, int NG>
+template <int KC, int NG>
 __global__ void __launch_bounds__(kThreads, 2)
 k_linear_tc(const float *__restrict__ a, const float *__restrict__ W,
             const float *__restrict__ bias, const float *__restrict__ add,
             const float *__restrict__ P2, const float *__restrict__ c2, float *__restrict__ out,
             int cout2, int64_t npix, int64_t ntiles, int apply_gelu, int *err) {
     using namespace tcu;
+    (void)P2;
+    (void)c2;
+    (void)cout2;
     constexpr int cin = 32 * KC, n = 16 * NG;
     static_assert(NG % kParts4 == 0 || NG < kParts4, "column groups split over the threads of a pixel");
     constexpr int kCinT = cin / kParts4;                 // input channels loaded per thread
@@ -287,7 +290,6 @@ k_linear_tc(const float *__restrict__ a, const float *__restrict__ W,
                                           ~static_cast<uintptr_t>(1023));
     __shared__ __align__(8) uint64_t bar;
     __shared__ uint32_t s_tmem;
-    __shared__ float s_head[kHead ? kParts4 * kMaxCout * 128 : 1];
     const Smem sm = smem_map(cin, n);
     const int tid = threadIdx.x, warp = tid >> 5;
     // thread -> (pixel row, quarter): warps w, w+4, w+8, w+12 share tensor-memory lanes
@@ -369,23 +371,18 @@ k_linear_tc(const float *__restrict__ a, const float *__restrict__ W,
         // this thread's column groups (quarter q takes groups q, q + 4, ...)
         const bool has_cols = quarter < NG;
         // the spectral sums of these outputs are fetched while the MMAs run
-        float sv[kHead ? 1 : 16 * kGroupsT];
-        if constexpr (!kHead) {
+        float sv[16 * kGroupsT];
 #pragma unroll
-            for (int gg = 0; gg < kGroupsT; ++gg)
+        for (int gg = 0; gg < kGroupsT; ++gg)
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const int o = 16 * (quarter + kParts4 * gg) + q;
-                    sv[16 * gg + q] = (add && pin && has_cols)
-                                          ? __ldcs(add + (b * n + o) * npix + p) : 0.f;
-                }
-        }
+            for (int q = 0; q < 16; ++q) {
+                const int o = 16 * (quarter + kParts4 * gg) + q;
+                sv[16 * gg + q] = (add && pin && has_cols)
+                                      ? __ldcs(add + (b * n + o) * npix + p) : 0.f;
+            }
         const bool ok = mbar_wait(&bar, phase++, err);
         tc_after_sync();
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        float hacc[kHead ? kMaxCout : 1];
-#pragma unroll
-        for (int q = 0; q < (kHead ? kMaxCout : 1); ++q) hacc[q] = 0.f;
 #pragma unroll
         for (int gg = 0; gg < kGroupsT; ++gg) {
             const int g = quarter + kParts4 * gg;
@@ -395,32 +392,9 @@ k_linear_tc(const float *__restrict__ a, const float *__restrict__ W,
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
                     const int o = 16 * g + q;
-                    const float t = (ok ? v[q] : 0.f) + bias[o];
-                    if constexpr (kHead) {
-                        const float h = gelu(t);
-#pragma unroll
-                        for (int c = 0; c < kMaxCout; ++c)
-                            if (c < cout2) hacc[c] = fmaf(P2[(int64_t)c * n + o], h, hacc[c]);
-                    } else {
-                        float r = t + sv[16 * gg + q];
-                        if (apply_gelu) r = gelu(r);
-                        if (pin) out[(b * n + o) * npix + p] = r;
-                    }
-                }
-            }
-        }
-        if constexpr (kHead) {
-            // the four quarters of a pixel add their partial sums
-#pragma unroll
-            for (int c = 0; c < kMaxCout; ++c)
-                if (c < cout2) s_head[(quarter * kMaxCout + c) * 128 + row] = hacc[c];
-            __syncthreads();
-            if (quarter == 0 && pin) {
-                for (int c = 0; c < cout2; ++c) {
-                    float v = c2[c];
-#pragma unroll
-                    for (int qq = 0; qq < kParts4; ++qq) v += s_head[(qq * kMaxCout + c) * 128 + row];
-                    out[(b * cout2 + c) * npix + p] = v;
+                    float r = (ok ? v[q] : 0.f) + bias[o] + sv[16 * gg + q];
+                    if (apply_gelu) r = gelu(r);
+                    if (pin) out[(b * n + o) * npix + p] = r;
                 }
             }
         }
@@ -442,18 +416,189 @@ inline bool eligible(int cin, int n) {
 using TcFn = void (*)(const float *, const float *, const float *, const float *,
                       const float *, const float *, float *, int, int64_t, int64_t, int, int *);
 
-template <bool kHead, int KC>
+template <int KC>
 TcFn pick_n(int n) {
     switch (n) {
-        case 32: return k_linear_tc<kHead, KC, 2>;
-        case 48: return k_linear_tc<kHead, KC, 3>;
-        case 64: return k_linear_tc<kHead, KC, 4>;
-        default: return k_linear_tc<kHead, KC, 8>;
+        case 32: return k_linear_tc<KC, 2>;
+        case 48: return k_linear_tc<KC, 3>;
+        case 64: return k_linear_tc<KC, 4>;
+        default: return k_linear_tc<KC, 8>;
     }
 }
-template <bool kHead>
-TcFn kernel(int cin, int n) {
-    return cin == 32 ? pick_n<kHead, 1>(n) : pick_n<kHead, 2>(n);
+inline TcFn kernel(int cin, int n) { return cin == 32 ? pick_n<1>(n) : pick_n<2>(n); }
+
+// The projection head, pipelined over its tiles: two activation-tile buffers
+// and two tensor-memory accumulators, so that while the threads run tile k's
+// epilogue (a GELU per hidden unit and the second projection) the tensor
+// cores already multiply tile k + 1, whose loads and tf32 split ran before
+// tile k's product was waited for.  One CTA per SM (the double buffer needs
+// most of the shared memory).
+__host__ __device__ inline uint32_t head_smem(int k, int n) {
+    const uint32_t kc = (uint32_t)(k / 32);
+    const uint32_t wchunk = ((uint32_t)n * 128 + 1023) / 1024 * 1024;
+    return 2 * (2 * kc * kChunk) + 2 * kc * wchunk + 1024;
+}
+template <int KC, int NG>
+__global__ void __launch_bounds__(kThreads, 1)
+k_head_tc(const float *__restrict__ a, const float *__restrict__ W,
+          const float *__restrict__ bias, const float *__restrict__ add,
+          const float *__restrict__ P2, const float *__restrict__ c2, float *__restrict__ out,
+          int cout2, int64_t npix, int64_t ntiles, int apply_gelu, int *err) {
+    using namespace tcu;
+    (void)add;
+    (void)apply_gelu;
+    constexpr int cin = 32 * KC, n = 16 * NG;
+    static_assert(NG % kParts4 == 0 || NG < kParts4, "column groups split over the threads of a pixel");
+    constexpr int kCinT = cin / kParts4;
+    constexpr int kGroupsT = NG >= kParts4 ? NG / kParts4 : 1;
+    constexpr uint32_t kBuf = 2 * KC * kChunk;                  // one tile: hi then lo
+    constexpr uint32_t wchunk = ((uint32_t)n * 128 + 1023) / 1024 * 1024;
+    constexpr uint32_t kW = 2 * kBuf, kWlo = kW + KC * wchunk;
+    extern __shared__ __align__(1024) char smem_raw[];
+    char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+    __shared__ __align__(8) uint64_t bar[2];
+    __shared__ uint32_t s_tmem;
+    __shared__ float s_head[kParts4 * kMaxCout * 128];
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int row = 32 * (warp & 3) + (tid & 31), quarter = warp >> 2;
+    for (int e = tid; e < n * cin; e += kThreads) {
+        const int o = e / cin, i = e % cin;
+        const float w = W[(int64_t)o * cin + i];
+        const uint32_t off = (uint32_t)(i / 32) * wchunk + sw_off(o, i % 32);
+        *reinterpret_cast<float *>(base + kW + off) = w;
+        *reinterpret_cast<float *>(base + kWlo + off) = tf32_lo(w);
+    }
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar[0])));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar[1])));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    constexpr uint32_t ncols = 2 * n <= 64 ? 64 : (2 * n <= 128 ? 128 : 256);
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(tc_smem_addr(&s_tmem)), "r"(ncols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    fence_async_smem();
+    tc_before_sync();
+    __syncthreads();
+    tc_after_sync();
+    const uint32_t tmem = s_tmem;
+    constexpr uint32_t idesc = idesc_tf32(n);
+    const int64_t ptiles = (npix + kRows - 1) / kRows;
+    const int i0 = quarter * kCinT;
+    // tile t's activations, transposed into buffer `buf` as the K-major A operand
+    auto load_split = [&](int64_t t, int buf) {
+        const int64_t tb = t / ptiles, tp = (t % ptiles) * kRows + row;
+        const bool tin = tp < npix;
+        const float *ab = a + (tb * cin + i0) * npix + tp;
+        float av[kCinT];
+#pragma unroll
+        for (int i = 0; i < kCinT; ++i) av[i] = tin ? __ldcs(ab + (int64_t)i * npix) : 0.f;
+        char *hi = base + buf * kBuf, *lo = hi + KC * kChunk;
+#pragma unroll
+        for (int i4 = 0; i4 < kCinT / 4; ++i4) {
+            const int i = i0 + 4 * i4;
+            const float4 v = make_float4(av[4 * i4], av[4 * i4 + 1], av[4 * i4 + 2], av[4 * i4 + 3]);
+            const uint32_t off = (uint32_t)(i / 32) * kChunk + sw_off(row, i % 32);
+            *reinterpret_cast<float4 *>(hi + off) = v;
+            *reinterpret_cast<float4 *>(lo + off) =
+                make_float4(tf32_lo(v.x), tf32_lo(v.y), tf32_lo(v.z), tf32_lo(v.w));
+        }
+        fence_async_smem();
+        tc_before_sync();
+        __syncthreads();
+    };
+    // one thread: the 3xTF32 chains of buffer `buf` into accumulator `buf`
+    auto issue = [&](int buf) {
+        tc_after_sync();
+        const uint32_t ah = tc_smem_addr(base + buf * kBuf), al = ah + KC * kChunk;
+        const uint32_t wh = tc_smem_addr(base + kW), wl = tc_smem_addr(base + kWlo);
+        const uint32_t d = tmem + buf * n;
+#pragma unroll
+        for (int c = 0; c < KC; ++c) {
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint32_t ao = c * kChunk + s * 32, bo = c * wchunk + s * 32;
+                mma_tf32(d, desc_sw128(ah + ao), desc_sw128(wh + bo), idesc, (c | s) ? 1u : 0u);
+                mma_tf32(d, desc_sw128(ah + ao), desc_sw128(wl + bo), idesc, 1u);
+                mma_tf32(d, desc_sw128(al + ao), desc_sw128(wh + bo), idesc, 1u);
+            }
+        }
+        mma_commit(&bar[buf]);
+    };
+    int64_t tile = blockIdx.x;
+    if (tile < ntiles) {
+        load_split(tile, 0);
+        if (tid == 0) issue(0);
+    }
+    for (int k = 0; tile < ntiles; tile += gridDim.x, ++k) {
+        const int buf = k & 1;
+        const int64_t nxt = tile + gridDim.x;
+        if (nxt < ntiles) {
+            // buffer and accumulator buf ^ 1 were released at the end of tile k - 1
+            load_split(nxt, buf ^ 1);
+            if (tid == 0) issue(buf ^ 1);
+        }
+        const bool ok = mbar_wait(&bar[buf], (uint32_t)(k >> 1) & 1u, err);
+        tc_after_sync();
+        const int64_t b = tile / ptiles, p = (tile % ptiles) * kRows + row;
+        const bool pin = p < npix;
+        const uint32_t lane_addr = tmem + buf * n + ((uint32_t)(32 * (warp & 3)) << 16);
+        float hacc[kMaxCout];
+#pragma unroll
+        for (int q = 0; q < kMaxCout; ++q) hacc[q] = 0.f;
+#pragma unroll
+        for (int gg = 0; gg < kGroupsT; ++gg) {
+            const int g = quarter + kParts4 * gg;
+            if (g < NG) {
+                float v[16];
+                tmem_ld16(lane_addr + 16 * g, v);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const int o = 16 * g + q;
+                    const float h = gelu((ok ? v[q] : 0.f) + bias[o]);
+#pragma unroll
+                    for (int c = 0; c < kMaxCout; ++c)
+                        if (c < cout2) hacc[c] = fmaf(P2[(int64_t)c * n + o], h, hacc[c]);
+                }
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < kMaxCout; ++c)
+            if (c < cout2) s_head[(quarter * kMaxCout + c) * 128 + row] = hacc[c];
+        __syncthreads();
+        if (quarter == 0 && pin) {
+            for (int c = 0; c < cout2; ++c) {
+                float v = c2[c];
+#pragma unroll
+                for (int qq = 0; qq < kParts4; ++qq) v += s_head[(qq * kMaxCout + c) * 128 + row];
+                out[(b * cout2 + c) * npix + p] = v;
+            }
+        }
+        tc_before_sync();
+        __syncthreads();            // accumulator buf and s_head are reused
+    }
+    if (warp == 0) {
+        tc_after_sync();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(ncols));
+    }
+}
+
+inline TcFn head_kernel(int cin, int n) {
+    auto pick = [](auto kc, int nn) -> TcFn {
+        constexpr int KC = decltype(kc)::value;
+        switch (nn) {
+            case 32: return k_head_tc<KC, 2>;
+            case 48: return k_head_tc<KC, 3>;
+            case 64: return k_head_tc<KC, 4>;
+            default: return k_head_tc<KC, 8>;
+        }
+    };
+    return cin == 32 ? pick(std::integral_constant<int, 1>{}, n)
+                     : pick(std::integral_constant<int, 2>{}, n);
 }
 
 }  // namespace lintc
@@ -521,9 +666,9 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
     int sms = 0, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    auto setup_tc = [&](lintc::TcFn fn, int cin, int n, int *grid, size_t *smem_bytes) {
+    auto setup_tc = [&](lintc::TcFn fn, int cin, int n, size_t sb, int *grid,
+                        size_t *smem_bytes) {
         if (!lintc::eligible(cin, n)) return true;
-        const size_t sb = lintc::smem_map(cin, n).total;
         int per_sm = 0;
         if (raise_smem_limit(fn, (int)sb) !=
                 cudaSuccess ||
@@ -555,10 +700,12 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
     const bool f32 = d->dtype == FNO_F32;
     const bool tc_ok = f32 && lintc::eligible(d->width, d->width),
                th_ok = f32 && lintc::eligible(d->width, d->hidden);
-    if ((tc_ok && !setup_tc(lintc::kernel<false>(d->width, d->width), d->width, d->width,
-                            &m->layer_tc_grid, &m->layer_tc_smem)) ||
-        (th_ok && !setup_tc(lintc::kernel<true>(d->width, d->hidden), d->width, d->hidden,
-                            &m->head_tc_grid, &m->head_tc_smem))) {
+    if ((tc_ok && !setup_tc(lintc::kernel(d->width, d->width), d->width, d->width,
+                            lintc::smem_map(d->width, d->width).total, &m->layer_tc_grid,
+                            &m->layer_tc_smem)) ||
+        (th_ok && !setup_tc(lintc::head_kernel(d->width, d->hidden), d->width, d->hidden,
+                            lintc::head_smem(d->width, d->hidden), &m->head_tc_grid,
+                            &m->head_tc_smem))) {
         cudaGetLastError();
         fno_plan_destroy(m->spec);
         delete m;
@@ -628,7 +775,7 @@ fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_param
             bool done = false;
             if constexpr (std::is_same<T, float>::value) {
                 if (m.layer_tc_grid) {
-                    lintc::kernel<false>(d.width, d.width)<<<m.layer_tc_grid, lintc::kThreads,
+                    lintc::kernel(d.width, d.width)<<<m.layer_tc_grid, lintc::kThreads,
                                                              m.layer_tc_smem, s>>>(
                         A, p->pw_w + (size_t)l * d.width * d.width,
                         p->pw_b + (size_t)l * d.width, S, nullptr, nullptr, Tn, 0, m.npix,
@@ -648,8 +795,8 @@ fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_param
         bool done = false;
         if constexpr (std::is_same<T, float>::value) {
             if (m.head_tc_grid) {
-                lintc::kernel<true>(d.width, d.hidden)<<<m.head_tc_grid, lintc::kThreads,
-                                                         m.head_tc_smem, s>>>(
+                lintc::head_kernel(d.width, d.hidden)<<<m.head_tc_grid, lintc::kThreads,
+                                                        m.head_tc_smem, s>>>(
                     A, p->proj1_w, p->proj1_b, nullptr, p->proj2_w, p->proj2_b,
                     static_cast<float *>(out), d.cout, m.npix, ntiles, 1, err);
                 done = true;
