@@ -246,6 +246,13 @@ k_projection_tiled(const T *__restrict__ a, const float *__restrict__ P1,
 // k_linear_tc) or GELU and the second projection (head, k_head_tc, which
 // double-buffers the tile and the accumulator).  A CTA walks tiles grid-stride.
 // ---------------------------------------------------------------------------
+// one activation element as float: streaming load for float32 storage
+__device__ __forceinline__ float load_act(const float *p) { return __ldcs(p); }
+__device__ __forceinline__ float load_act(const __half *p) { return Storage<__half>::load(p); }
+__device__ __forceinline__ float load_act(const __nv_bfloat16 *p) {
+    return Storage<__nv_bfloat16>::load(p);
+}
+
 namespace lintc {
 
 constexpr int kThreads = 512;            // four threads per pixel row of a tile
@@ -271,11 +278,11 @@ __host__ __device__ inline Smem smem_map(int k, int n) {
 // out[b][o][p] = act(sum_i W[o][i] a[b][i][p] + bias[o] + add[b][o][p])
 // KC = input channels / 32, NG = output channels / 16 (fully unrolled, so that
 // every load of a tile is in flight before its first use)
-template <int KC, int NG>
+template <int KC, int NG, typename T>
 __global__ void __launch_bounds__(kThreads, 2)
-k_linear_tc(const float *__restrict__ a, const float *__restrict__ W,
-            const float *__restrict__ bias, const float *__restrict__ add,
-            const float *__restrict__ P2, const float *__restrict__ c2, float *__restrict__ out,
+k_linear_tc(const T *__restrict__ a, const float *__restrict__ W,
+            const float *__restrict__ bias, const T *__restrict__ add,
+            const float *__restrict__ P2, const float *__restrict__ c2, T *__restrict__ out,
             int cout2, int64_t npix, int64_t ntiles, int apply_gelu, int *err) {
     using namespace tcu;
     (void)P2;
@@ -328,9 +335,9 @@ k_linear_tc(const float *__restrict__ a, const float *__restrict__ W,
     auto load_tile = [&](int64_t t) {
         const int64_t tb = t / ptiles, tp = (t % ptiles) * kRows + row;
         const bool tin = t < ntiles && tp < npix;
-        const float *ab = a + (tb * cin + i0) * npix + tp;
+        const T *ab = a + (tb * cin + i0) * npix + tp;
 #pragma unroll
-        for (int i = 0; i < kCinT; ++i) av[i] = tin ? __ldcs(ab + (int64_t)i * npix) : 0.f;
+        for (int i = 0; i < kCinT; ++i) av[i] = tin ? load_act(ab + (int64_t)i * npix) : 0.f;
     };
     load_tile(blockIdx.x);
     uint32_t phase = 0;
@@ -378,7 +385,7 @@ k_linear_tc(const float *__restrict__ a, const float *__restrict__ W,
             for (int q = 0; q < 16; ++q) {
                 const int o = 16 * (quarter + kParts4 * gg) + q;
                 sv[16 * gg + q] = (add && pin && has_cols)
-                                      ? __ldcs(add + (b * n + o) * npix + p) : 0.f;
+                                      ? load_act(add + (b * n + o) * npix + p) : 0.f;
             }
         const bool ok = mbar_wait(&bar, phase++, err);
         tc_after_sync();
@@ -394,7 +401,7 @@ k_linear_tc(const float *__restrict__ a, const float *__restrict__ W,
                     const int o = 16 * g + q;
                     float r = (ok ? v[q] : 0.f) + bias[o] + sv[16 * gg + q];
                     if (apply_gelu) r = gelu(r);
-                    if (pin) out[(b * n + o) * npix + p] = r;
+                    if (pin) Storage<T>::store(out + (b * n + o) * npix + p, r);
                 }
             }
         }
@@ -413,19 +420,21 @@ inline bool eligible(int cin, int n) {
     return (cin == 32 || cin == 64) && (n == 32 || n == 48 || n == 64 || n == 128);
 }
 
-using TcFn = void (*)(const float *, const float *, const float *, const float *,
-                      const float *, const float *, float *, int, int64_t, int64_t, int, int *);
+template <typename T>
+using TcFn = void (*)(const T *, const float *, const float *, const T *, const float *,
+                      const float *, T *, int, int64_t, int64_t, int, int *);
 
-template <int KC>
-TcFn pick_n(int n) {
+template <int KC, typename T>
+TcFn<T> pick_n(int n) {
     switch (n) {
-        case 32: return k_linear_tc<KC, 2>;
-        case 48: return k_linear_tc<KC, 3>;
-        case 64: return k_linear_tc<KC, 4>;
-        default: return k_linear_tc<KC, 8>;
+        case 32: return k_linear_tc<KC, 2, T>;
+        case 48: return k_linear_tc<KC, 3, T>;
+        case 64: return k_linear_tc<KC, 4, T>;
+        default: return k_linear_tc<KC, 8, T>;
     }
 }
-inline TcFn kernel(int cin, int n) { return cin == 32 ? pick_n<1>(n) : pick_n<2>(n); }
+template <typename T>
+TcFn<T> kernel(int cin, int n) { return cin == 32 ? pick_n<1, T>(n) : pick_n<2, T>(n); }
 
 // The projection head, pipelined over its tiles: two activation-tile buffers
 // and two tensor-memory accumulators, so that while the threads run tile k's
@@ -438,11 +447,11 @@ __host__ __device__ inline uint32_t head_smem(int k, int n) {
     const uint32_t wchunk = ((uint32_t)n * 128 + 1023) / 1024 * 1024;
     return 2 * (2 * kc * kChunk) + 2 * kc * wchunk + 1024;
 }
-template <int KC, int NG>
+template <int KC, int NG, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
-k_head_tc(const float *__restrict__ a, const float *__restrict__ W,
-          const float *__restrict__ bias, const float *__restrict__ add,
-          const float *__restrict__ P2, const float *__restrict__ c2, float *__restrict__ out,
+k_head_tc(const T *__restrict__ a, const float *__restrict__ W,
+          const float *__restrict__ bias, const T *__restrict__ add,
+          const float *__restrict__ P2, const float *__restrict__ c2, T *__restrict__ out,
           int cout2, int64_t npix, int64_t ntiles, int apply_gelu, int *err) {
     using namespace tcu;
     (void)add;
@@ -492,10 +501,10 @@ k_head_tc(const float *__restrict__ a, const float *__restrict__ W,
     auto load_split = [&](int64_t t, int buf) {
         const int64_t tb = t / ptiles, tp = (t % ptiles) * kRows + row;
         const bool tin = tp < npix;
-        const float *ab = a + (tb * cin + i0) * npix + tp;
+        const T *ab = a + (tb * cin + i0) * npix + tp;
         float av[kCinT];
 #pragma unroll
-        for (int i = 0; i < kCinT; ++i) av[i] = tin ? __ldcs(ab + (int64_t)i * npix) : 0.f;
+        for (int i = 0; i < kCinT; ++i) av[i] = tin ? load_act(ab + (int64_t)i * npix) : 0.f;
         char *hi = base + buf * kBuf, *lo = hi + KC * kChunk;
 #pragma unroll
         for (int i4 = 0; i4 < kCinT / 4; ++i4) {
@@ -574,7 +583,7 @@ k_head_tc(const float *__restrict__ a, const float *__restrict__ W,
                 float v = c2[c];
 #pragma unroll
                 for (int qq = 0; qq < kParts4; ++qq) v += s_head[(qq * kMaxCout + c) * 128 + row];
-                out[(b * cout2 + c) * npix + p] = v;
+                Storage<T>::store(out + (b * cout2 + c) * npix + p, v);
             }
         }
         tc_before_sync();
@@ -587,14 +596,15 @@ k_head_tc(const float *__restrict__ a, const float *__restrict__ W,
     }
 }
 
-inline TcFn head_kernel(int cin, int n) {
-    auto pick = [](auto kc, int nn) -> TcFn {
+template <typename T>
+TcFn<T> head_kernel(int cin, int n) {
+    auto pick = [](auto kc, int nn) -> TcFn<T> {
         constexpr int KC = decltype(kc)::value;
         switch (nn) {
-            case 32: return k_head_tc<KC, 2>;
-            case 48: return k_head_tc<KC, 3>;
-            case 64: return k_head_tc<KC, 4>;
-            default: return k_head_tc<KC, 8>;
+            case 32: return k_head_tc<KC, 2, T>;
+            case 48: return k_head_tc<KC, 3, T>;
+            case 64: return k_head_tc<KC, 4, T>;
+            default: return k_head_tc<KC, 8, T>;
         }
     };
     return cin == 32 ? pick(std::integral_constant<int, 1>{}, n)
@@ -666,7 +676,7 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
     int sms = 0, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    auto setup_tc = [&](lintc::TcFn fn, int cin, int n, size_t sb, int *grid,
+    auto setup_tc = [&](const void *fn, int cin, int n, size_t sb, int *grid,
                         size_t *smem_bytes) {
         if (!lintc::eligible(cin, n)) return true;
         int per_sm = 0;
@@ -696,16 +706,20 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
         *smem_bytes = sb;
         return true;
     };
-    // (float32 activations only: the 16-bit stack runs the register-tiled linears)
+    // (16-bit activations convert on load and round once on store)
     const bool f32 = d->dtype == FNO_F32;
-    const bool tc_ok = f32 && lintc::eligible(d->width, d->width),
-               th_ok = f32 && lintc::eligible(d->width, d->hidden);
-    if ((tc_ok && !setup_tc(lintc::kernel(d->width, d->width), d->width, d->width,
-                            lintc::smem_map(d->width, d->width).total, &m->layer_tc_grid,
-                            &m->layer_tc_smem)) ||
-        (th_ok && !setup_tc(lintc::head_kernel(d->width, d->hidden), d->width, d->hidden,
-                            lintc::head_smem(d->width, d->hidden), &m->head_tc_grid,
-                            &m->head_tc_smem))) {
+    const bool tc_ok = lintc::eligible(d->width, d->width),
+               th_ok = lintc::eligible(d->width, d->hidden);
+    const bool tc_fail = with_storage(d->dtype, [&](auto t) {
+        using T = decltype(t);
+        return (tc_ok && !setup_tc((const void *)lintc::kernel<T>(d->width, d->width), d->width,
+                                   d->width, lintc::smem_map(d->width, d->width).total,
+                                   &m->layer_tc_grid, &m->layer_tc_smem)) ||
+               (th_ok && !setup_tc((const void *)lintc::head_kernel<T>(d->width, d->hidden),
+                                   d->width, d->hidden, lintc::head_smem(d->width, d->hidden),
+                                   &m->head_tc_grid, &m->head_tc_smem));
+    });
+    if (tc_fail) {
         cudaGetLastError();
         fno_plan_destroy(m->spec);
         delete m;
@@ -772,18 +786,12 @@ fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_param
                                                         stream);
             if (st != FNO_OK) return st;
             const int last = (l == d.nlayers - 1);
-            bool done = false;
-            if constexpr (std::is_same<T, float>::value) {
-                if (m.layer_tc_grid) {
-                    lintc::kernel(d.width, d.width)<<<m.layer_tc_grid, lintc::kThreads,
-                                                             m.layer_tc_smem, s>>>(
-                        A, p->pw_w + (size_t)l * d.width * d.width,
-                        p->pw_b + (size_t)l * d.width, S, nullptr, nullptr, Tn, 0, m.npix,
-                        ntiles, last ? 0 : 1, err);
-                    done = true;
-                }
-            }
-            if (!done)
+            if (m.layer_tc_grid)
+                lintc::kernel<T>(d.width, d.width)<<<m.layer_tc_grid, lintc::kThreads,
+                                                     m.layer_tc_smem, s>>>(
+                    A, p->pw_w + (size_t)l * d.width * d.width, p->pw_b + (size_t)l * d.width,
+                    S, nullptr, nullptr, Tn, 0, m.npix, ntiles, last ? 0 : 1, err);
+            else
                 k_linear_tiled<T><<<lin_grid, kTT, smem, s>>>(
                     A, p->pw_w + (size_t)l * d.width * d.width, p->pw_b + (size_t)l * d.width,
                     S, Tn, d.width, d.width, m.npix, last ? 0 : 1);
@@ -792,17 +800,12 @@ fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_param
             A = Tn;
             Tn = tmp;
         }
-        bool done = false;
-        if constexpr (std::is_same<T, float>::value) {
-            if (m.head_tc_grid) {
-                lintc::head_kernel(d.width, d.hidden)<<<m.head_tc_grid, lintc::kThreads,
-                                                        m.head_tc_smem, s>>>(
-                    A, p->proj1_w, p->proj1_b, nullptr, p->proj2_w, p->proj2_b,
-                    static_cast<float *>(out), d.cout, m.npix, ntiles, 1, err);
-                done = true;
-            }
-        }
-        if (!done)
+        if (m.head_tc_grid)
+            lintc::head_kernel<T>(d.width, d.hidden)<<<m.head_tc_grid, lintc::kThreads,
+                                                      m.head_tc_smem, s>>>(
+                A, p->proj1_w, p->proj1_b, nullptr, p->proj2_w, p->proj2_b,
+                static_cast<T *>(out), d.cout, m.npix, ntiles, 1, err);
+        else
             projection_kernel<T>(d.cout)<<<dim3(ptiles, (unsigned)d.batch), kTT, smem, s>>>(
                 A, p->proj1_w, p->proj1_b, p->proj2_w, p->proj2_b, static_cast<T *>(out),
                 d.width, d.hidden, d.cout, m.npix);
