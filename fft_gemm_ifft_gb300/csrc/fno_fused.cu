@@ -864,6 +864,11 @@ void make_table(std::vector<unsigned char> &img) {
 //   3. the 128 x 128 tile leaves through four swizzled 32-column staging boxes
 //      (over the operands, free once the MMAs completed) by TMA stores.
 // ---------------------------------------------------------------------------
+// kFused: the two column steps in one pass per thread (no U buffer in shared
+// memory, three CTAs per SM) -- for layers with many output images; the
+// two-pass form spreads the column inverse over more independent work per CTA
+// and is faster when there are at most two CTAs per SM anyway.
+template <bool kFused>
 struct GeoC32 {
     static constexpr int N0 = 128, N1 = 128, M0 = 16, M1 = 16, K0 = 32, NK = K0 * M1;
     static constexpr int G1 = 8, T1 = N0 / G1;          // g = g1 + 8 g2, t = t1 + 16 t2
@@ -871,8 +876,8 @@ struct GeoC32 {
     static constexpr uint32_t kT = 0;                   // T hi, T lo (B operands)
     static constexpr uint32_t kTBytes = 2 * kTile;
     static constexpr uint32_t kA = kT + kTBytes;        // Zo' hi, Zo' lo (A operands)
-    static constexpr uint32_t kS = kA + 2 * kTile;      // U[G1][T1][M1]
-    static constexpr uint32_t kY = kS + G1 * T1 * M1 * 8;
+    static constexpr uint32_t kS = kA + 2 * kTile;      // U[G1][T1][M1] (two-pass form)
+    static constexpr uint32_t kY = kS + (kFused ? 0 : G1 * T1 * M1 * 8);
     static constexpr uint32_t kTw = kY + NK * 8;
     static constexpr uint32_t kSmem = kTw + N0 * 8 + 1024;
     static constexpr uint32_t kStage = 0;               // 4 output boxes over T and A
@@ -880,9 +885,10 @@ struct GeoC32 {
     static_assert(kS >= 4 * kTile, "staging boxes fit over the operands");
 };
 
-__global__ void __launch_bounds__(NT, 2)
+template <bool kFused>
+__global__ void __launch_bounds__(NT, kFused ? 3 : 2)
 k_phase_c_tc32(const __grid_constant__ CUtensorMap ymap, Args a, const void *table) {
-    using Gm = GeoC32;
+    using Gm = GeoC32<kFused>;
     using namespace tcu;
     extern __shared__ __align__(1024) char smem_raw[];
     char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -893,7 +899,6 @@ k_phase_c_tc32(const __grid_constant__ CUtensorMap ymap, Args a, const void *tab
     const int tid = threadIdx.x, warp = tid >> 5;
     const int img = blockIdx.x;
     float2 *ys = reinterpret_cast<float2 *>(base + Gm::kY);
-    float2 *S = reinterpret_cast<float2 *>(base + Gm::kS);
     float2 *tw = reinterpret_cast<float2 *>(base + Gm::kTw);
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_t)));
@@ -922,49 +927,78 @@ k_phase_c_tc32(const __grid_constant__ CUtensorMap ymap, Args a, const void *tab
     cp_async_commit();
     cp_async_wait_all();
     __syncthreads();
-    // 1. U[g1][t1][k0..k0+3]: kept row j holds g = j (j < 16) or j - 32
-    for (int u = tid; u < Gm::G1 * Gm::T1 * (Gm::M1 / 4); u += NT) {
-        const int k0 = 4 * (u % (Gm::M1 / 4)), t1 = (u / (Gm::M1 / 4)) % Gm::T1;
-        const int g1 = u / (Gm::M1 / 4 * Gm::T1);
-        float2 acc[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int g2 = -2; g2 < 2; ++g2) {
-            const int g = g1 + 8 * g2, j = g < 0 ? g + Gm::K0 : g;
-            const float2 wv = tw[(g * t1) & (Gm::N0 - 1)];        // e^{-2 pi i g t1 / 128}
-            const float2 wc = make_float2(wv.x, -wv.y);
-            const float4 *y4 = reinterpret_cast<const float4 *>(ys + j * Gm::M1 + k0);
-            const float4 p0 = y4[0], p1 = y4[1];
-            cmac(acc[0], make_float2(p0.x, p0.y), wc);
-            cmac(acc[1], make_float2(p0.z, p0.w), wc);
-            cmac(acc[2], make_float2(p1.x, p1.y), wc);
-            cmac(acc[3], make_float2(p1.z, p1.w), wc);
-        }
-        float4 *d = reinterpret_cast<float4 *>(S + (g1 * Gm::T1 + t1) * Gm::M1 + k0);
-        d[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
-        d[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
-    }
-    __syncthreads();
-    // 2. Zo[t1 + 16 t2][k] = sum_g1 e^{+2 pi i g1 t2 / 8} U[g1][t1][k], split into the
-    //    tf32 head and remainder and written as the K-major operands: columns
-    //    0..15 the real parts, 16..31 the imaginary
     char *Ahi = base + Gm::kA, *Alo = Ahi + Gm::kTile;
-    for (int u = tid; u < Gm::T1 * Gm::M1; u += NT) {
-        const int k = u % Gm::M1, t1 = u / Gm::M1;
-        float2 z[Gm::G1];
+    // Zo[t][k] split into the tf32 head and remainder, written as the K-major
+    // operands: columns 0..15 the real parts, 16..31 the imaginary
+    auto put = [&](int t, int k, float2 v) {
+        const uint32_t ore = sw_off(t, k), oim = sw_off(t, Gm::M1 + k);
+        *reinterpret_cast<float *>(Ahi + ore) = v.x;
+        *reinterpret_cast<float *>(Ahi + oim) = v.y;
+        *reinterpret_cast<float *>(Alo + ore) = tf32_lo(v.x);
+        *reinterpret_cast<float *>(Alo + oim) = tf32_lo(v.y);
+    };
+    if constexpr (kFused) {
+        // thread (t1, k): the eight U[g1] (four-term sums, kept row j holds g = j
+        // for j < 16, j - 32 above), then the 8-point inverse FFT over g1
+        for (int u = tid; u < Gm::T1 * Gm::M1; u += NT) {
+            const int k = u % Gm::M1, t1 = u / Gm::M1;
+            float2 z[Gm::G1];
 #pragma unroll
-        for (int g1 = 0; g1 < Gm::G1; ++g1) z[g1] = S[(g1 * Gm::T1 + t1) * Gm::M1 + k];
-        fft::fft_dif<Gm::G1, 1>(z);
+            for (int g1 = 0; g1 < Gm::G1; ++g1) {
+                float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int t2 = 0; t2 < Gm::G1; ++t2) {
-            const float2 v = z[fft::bitrev(t2, fft::ilog2(Gm::G1))];
-            const int t = t1 + Gm::T1 * t2;
-            const uint32_t ore = sw_off(t, k), oim = sw_off(t, Gm::M1 + k);
-            *reinterpret_cast<float *>(Ahi + ore) = v.x;
-            *reinterpret_cast<float *>(Ahi + oim) = v.y;
-            *reinterpret_cast<float *>(Alo + ore) = tf32_lo(v.x);
-            *reinterpret_cast<float *>(Alo + oim) = tf32_lo(v.y);
+                for (int g2 = -2; g2 < 2; ++g2) {
+                    const int g = g1 + 8 * g2, j = g < 0 ? g + Gm::K0 : g;
+                    const float2 wv = tw[(g * t1) & (Gm::N0 - 1)];   // e^{-2 pi i g t1 / 128}
+                    cmac(acc, ys[j * Gm::M1 + k], make_float2(wv.x, -wv.y));
+                }
+                z[g1] = acc;
+            }
+            fft::fft_dif<Gm::G1, 1>(z);
+#pragma unroll
+            for (int t2 = 0; t2 < Gm::G1; ++t2)
+                put(t1 + Gm::T1 * t2, k, z[fft::bitrev(t2, fft::ilog2(Gm::G1))]);
+        }
+    } else {
+        float2 *S = reinterpret_cast<float2 *>(base + Gm::kS);
+        // 1. U[g1][t1][k0..k0+3]: kept row j holds g = j (j < 16) or j - 32
+        for (int u = tid; u < Gm::G1 * Gm::T1 * (Gm::M1 / 4); u += NT) {
+            const int k0 = 4 * (u % (Gm::M1 / 4)), t1 = (u / (Gm::M1 / 4)) % Gm::T1;
+            const int g1 = u / (Gm::M1 / 4 * Gm::T1);
+            float2 acc[4];
+    #pragma unroll
+            for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
+    #pragma unroll
+            for (int g2 = -2; g2 < 2; ++g2) {
+                const int g = g1 + 8 * g2, j = g < 0 ? g + Gm::K0 : g;
+                const float2 wv = tw[(g * t1) & (Gm::N0 - 1)];        // e^{-2 pi i g t1 / 128}
+                const float2 wc = make_float2(wv.x, -wv.y);
+                const float4 *y4 = reinterpret_cast<const float4 *>(ys + j * Gm::M1 + k0);
+                const float4 p0 = y4[0], p1 = y4[1];
+                cmac(acc[0], make_float2(p0.x, p0.y), wc);
+                cmac(acc[1], make_float2(p0.z, p0.w), wc);
+                cmac(acc[2], make_float2(p1.x, p1.y), wc);
+                cmac(acc[3], make_float2(p1.z, p1.w), wc);
+            }
+            float4 *d = reinterpret_cast<float4 *>(S + (g1 * Gm::T1 + t1) * Gm::M1 + k0);
+            d[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+            d[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+        }
+        __syncthreads();
+        // 2. Zo[t1 + 16 t2][k] = sum_g1 e^{+2 pi i g1 t2 / 8} U[g1][t1][k], split into the
+        //    tf32 head and remainder and written as the K-major operands: columns
+        //    0..15 the real parts, 16..31 the imaginary
+        for (int u = tid; u < Gm::T1 * Gm::M1; u += NT) {
+            const int k = u % Gm::M1, t1 = u / Gm::M1;
+            float2 z[Gm::G1];
+    #pragma unroll
+            for (int g1 = 0; g1 < Gm::G1; ++g1) z[g1] = S[(g1 * Gm::T1 + t1) * Gm::M1 + k];
+            fft::fft_dif<Gm::G1, 1>(z);
+    #pragma unroll
+            for (int t2 = 0; t2 < Gm::G1; ++t2) {
+                const float2 v = z[fft::bitrev(t2, fft::ilog2(Gm::G1))];
+                put(t1 + Gm::T1 * t2, k, v);
+            }
         }
     }
     fence_async_smem();
@@ -1026,7 +1060,7 @@ k_phase_c_tc32(const __grid_constant__ CUtensorMap ymap, Args a, const void *tab
 // Host: the fp32 inverse row-DFT operand, [hi, lo][n][k] (k < 16: cos, else
 // -sin), with c(k) and the output scale 1/128^2 folded in, computed in double.
 void make_table_c32(std::vector<unsigned char> &img) {
-    using Gm = GeoC32;
+    using Gm = GeoC32<false>;
     using tcu::sw_off;
     using tcu::tf32_lo;
     img.assign(Gm::kTBytes, 0);
@@ -1238,7 +1272,14 @@ struct Pdl {
             }
             if (e == cudaSuccess && p.fused_tcc) {
                 if constexpr (std::is_same<T, float>::value) {
-                    e = raise_smem_limit(tca::k_phase_c_tc32, (int)tca::GeoC32::kSmem);
+                    // the one-pass form where the output images fill more than
+                    // two CTAs per SM
+                    p.fused_c1pass = p.batch * p.cout > 2 * (int64_t)p.num_sms;
+                    e = p.fused_c1pass
+                            ? raise_smem_limit(tca::k_phase_c_tc32<true>,
+                                               (int)tca::GeoC32<true>::kSmem)
+                            : raise_smem_limit(tca::k_phase_c_tc32<false>,
+                                               (int)tca::GeoC32<false>::kSmem);
                     tca::make_table_c32(imgc);
                 } else {
                     e = raise_smem_limit(tca::k_phase_c_tc<T>, (int)tca::GeoC<T>::kSmem);
@@ -1388,15 +1429,20 @@ struct Pdl {
         cfg.blockDim = dim3(kNT);
         if constexpr (std::is_same<T, float>::value && CfC::N0 == 128) {
             if (p.fused_tcc) {
-                using Gc = tca::GeoC32;
+                using Gc = tca::GeoC32<false>;
                 CUtensorMap ymap;
                 if (!tcu::encode_rows_tiled(&ymap, a.y, (int64_t)p.batch * p.cout * Gc::N0,
                                             Gc::N1, sizeof(float), 32, tcu::tma_type<float>()))
                     return cudaErrorInvalidValue;
                 cfg.blockDim = dim3(tca::NT);
-                cfg.dynamicSmemBytes = Gc::kSmem;
                 const void *tab = static_cast<const char *>(p.fused_tables) + p.fused_table_c;
-                e = cudaLaunchKernelEx(&cfg, tca::k_phase_c_tc32, ymap, a, tab);
+                if (p.fused_c1pass) {
+                    cfg.dynamicSmemBytes = tca::GeoC32<true>::kSmem;
+                    e = cudaLaunchKernelEx(&cfg, tca::k_phase_c_tc32<true>, ymap, a, tab);
+                } else {
+                    cfg.dynamicSmemBytes = Gc::kSmem;
+                    e = cudaLaunchKernelEx(&cfg, tca::k_phase_c_tc32<false>, ymap, a, tab);
+                }
                 if (e != cudaSuccess) return e;
                 return cudaGetLastError();
             }

@@ -58,6 +58,7 @@ struct Plan {
     bool fused_mixtc;             // three-kernel path mixes on the tensor cores
     bool fused_tca;               // three-kernel path transforms (kernel A) on the tensor cores
     bool fused_tcc;               // ... and inverts (kernel C) on the tensor cores
+    bool fused_c1pass;            // fp32 kernel C: one-pass column inverse, 3 CTAs per SM
     size_t fused_table_c;         // byte offset of kernel C's operand in fused_tables
     fno_trace_record_t *trace;    // FNO_PLAN_TRACE: one record per work item (plan-owned)
     size_t trace_records;         // records one forward call produces

@@ -30,6 +30,7 @@ SMALL = [
     ((128, 128), (16, 16), 2, 64, 64, "f32"),
     ((128, 128), (16, 16), 1, 64, 37, "f32"),
     ((128, 128), (16, 16), 9, 3, 2, "f32"),
+    ((128, 128), (16, 16), 10, 3, 40, "f32"),    # > 2 output images per SM: one-pass kernel C
     ((16, 32), (3, 7), 3, 5, 3, "f32"),
     ((32, 16), (16, 9), 2, 2, 3, "f32"),
     ((64, 64), (16, 16), 2, 8, 8, "f32"),
