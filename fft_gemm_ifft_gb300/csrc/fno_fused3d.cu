@@ -84,12 +84,9 @@ struct Cfg3 {
     }
     template <typename T>
     static constexpr size_t smem_a() { return kSmemTw + ring_bytes<T>() + (size_t)N1 * Pl::ZS * 8; }
-    // kernel C: twiddles, the chunk's plane spectra [R0][NKP], the residue sums
-    // [A][B2][M2], and one region that holds a plane's residues [N1][M2] until
-    // the column pass has read them and its spectral rows [N1][ZS] after
-    static constexpr size_t kSmemC = kSmemTw + (size_t)R0 * NKP * 8 +
-                                     (size_t)Pl::A * Pl::B2 * M2 * 8 +
-                                     (size_t)N1 * (Pl::ZS > M2 ? Pl::ZS : M2) * 8;
+    // kernel C: twiddles, the chunk's plane spectra [R0][NKP] and one plane's
+    // spectral rows [N1][ZS]
+    static constexpr size_t kSmemC = kSmemTw + (size_t)R0 * NKP * 8 + (size_t)N1 * Pl::ZS * 8;
     static_assert(stage_bytes<float>() % 16 == 0 && stage_bytes<__half>() % 16 == 0, "align");
     static_assert((size_t)Pl::A * Pl::B2 * M2 * 8 <= stage_bytes<__half>(),
                   "the column pass works in the stage of its plane");
@@ -112,6 +109,38 @@ __device__ __forceinline__ Tw load_tw3(const Args &a, char *smem, const float2 *
     for (int e = threadIdx.x; e < C3::N0; e += kNT) ta[e] = a.tw0[e];
     *twa = ta;
     return Tw{t0, t1, t1i};
+}
+
+// Column inverse of one plane into its spectral rows.  Kept row j holds the
+// signed frequency g = j (j < M0) or j - 2 M0; with g = g1 + 8 g2 and, for a
+// 64-row plane, t = t1 + 8 t2,
+//   Zo[t][k] = sum_g1 e^{+2 pi i g1 t2 / 8} sum_g2 Y[g][k] e^{+2 pi i g t1 / N0},
+// 2 M0 / 8 terms in each inner sum and an 8-point inverse register FFT over g1;
+// thread (t1, k) owns the eight rows t1 + 8 t2 of bin k.
+template <class Pl>
+__device__ __forceinline__ void plane_col_inverse(const float2 *ys, float2 *zo, Tw tw) {
+    constexpr int N0 = Pl::N0, M0 = Pl::M0, M1 = Pl::M1, K0 = Pl::K0, ZS = Pl::ZS;
+    constexpr int G1 = 8, T1 = N0 / G1, G2 = M0 / G1;   // g2 = -G2 .. G2 - 1
+    static_assert(M0 % G1 == 0 && T1 == G1, "8 x 8 split of the plane's rows");
+    for (int u = threadIdx.x; u < T1 * M1; u += kNT) {
+        const int k = u % M1, t1 = u / M1;
+        float2 z[G1];
+#pragma unroll
+        for (int g1 = 0; g1 < G1; ++g1) {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int g2 = -G2; g2 < G2; ++g2) {
+                const int g = g1 + G1 * g2, j = g < 0 ? g + K0 : g;
+                const float2 wv = tw.t0[(g * t1) & (N0 - 1)];     // e^{-2 pi i g t1 / N0}
+                cmac(acc, ys[j * M1 + k], make_float2(wv.x, -wv.y));
+            }
+            z[g1] = acc;
+        }
+        fft::fft_dif<G1, 1>(z);
+#pragma unroll
+        for (int t2 = 0; t2 < G1; ++t2)
+            zo[(t1 + T1 * t2) * ZS + k] = z[fft::bitrev(t2, fft::ilog2(G1))];
+    }
 }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -236,9 +265,7 @@ __global__ void __launch_bounds__(kNT) k_phase_c3(Args a) {
     const float2 *twa;
     const Tw tw = load_tw3<C3>(a, smem, &twa);
     float2 *spec = reinterpret_cast<float2 *>(smem + C3::kSmemTw);   // [R0][NKP]
-    float2 *ss = spec + R0 * NKP;                                    // [A][B2][M2]
-    float2 *vs = ss + Pl::A * Pl::B2 * M2;                           // [N1][M2], then
-    float2 *zo = vs;                                                 // [N1][ZS]
+    float2 *zo = spec + R0 * NKP;                                    // [N1][ZS]
     __syncthreads();
     pdl_wait();                                  // kernel B's mixed modes are complete
     const unsigned long long t1 = a.trace ? trace_now() : 0;
@@ -274,14 +301,10 @@ __global__ void __launch_bounds__(kNT) k_phase_c3(Args a) {
     // 2. every plane of the chunk: column inverse, row inverse, store
     T *dst = static_cast<T *>(a.y) + (size_t)vol * N0 * N1 * N2;
     for (int t = 0; t < R0; ++t) {
-        c_residues<Pl>(spec + t * NKP, vs, 0, tw);
-        __syncthreads();
-        c_col_ifft<Pl>(vs, ss);
-        __syncthreads();
-        c_col_combine<Pl>(ss, zo, tw);
+        plane_col_inverse<Pl>(spec + t * NKP, zo, tw);
         __syncthreads();
         c_row_store<Pl, T>(zo, dst + (size_t)(c + C0 * t) * N1 * N2, 0, tw);
-        __syncthreads();                         // zo is the next plane's residue region
+        __syncthreads();                         // zo is rewritten for the next plane
     }
     cta_record(a, 2, a.trace_c, t0, t1);
 }
