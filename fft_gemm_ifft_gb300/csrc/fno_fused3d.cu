@@ -87,6 +87,11 @@ struct Cfg3 {
     // kernel C: twiddles, the chunk's plane spectra [R0][NKP] and one plane's
     // spectral rows [N1][ZS]
     static constexpr size_t kSmemC = kSmemTw + (size_t)R0 * NKP * 8 + (size_t)N1 * Pl::ZS * 8;
+    // kernel C reads the volume's mixed modes kYRows kept rows at a time, two
+    // stages over the spectra region
+    static constexpr int kYRows = 4;
+    static_assert(K0 % kYRows == 0 && 2 * kYRows <= R0 && (kYRows * NKP) % 2 == 0,
+                  "two stages of kept rows fit over the spectra");
     static_assert(stage_bytes<float>() % 16 == 0 && stage_bytes<__half>() % 16 == 0, "align");
     static_assert((size_t)Pl::A * Pl::B2 * M2 * 8 <= stage_bytes<__half>(),
                   "the column pass works in the stage of its plane");
@@ -273,21 +278,42 @@ __global__ void __launch_bounds__(kNT) k_phase_c3(Args a) {
     const float2 *Yv = a.Y + (size_t)vol * C3::NK;
 
     // 1. Z[r] = sum_m Y[r + R0 m] conj(W_N0^{f c}) for this thread's plane modes,
-    //    then the R0-point inverse DFT over r: spectra of planes c + C0 t
+    //    then the R0-point inverse DFT over r: spectra of planes c + C0 t.  The
+    //    volume's kept rows come through two cp.async stages of kRows rows over
+    //    the spectra region, so that the reads of a stage overlap the sums of
+    //    the one before.
+    constexpr int kRows = C3::kYRows, kNSt = C3::K0 / kRows;
+    auto issue_y = [&](int st) {
+        float2 *d = spec + (st & 1) * kRows * NKP;
+        const float2 *g = Yv + (size_t)st * kRows * NKP;
+        for (int e = threadIdx.x; e < kRows * NKP / 2; e += kNT) cp_async16(d + 2 * e, g + 2 * e);
+    };
+    issue_y(0);
+    cp_async_commit();
+    issue_y(1);
+    cp_async_commit();
     float2 z[QT][R0];
 #pragma unroll
-    for (int r = 0; r < R0; ++r) {
+    for (int r = 0; r < R0; ++r)
 #pragma unroll
         for (int q = 0; q < QT; ++q) z[q][r] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int m = 0; m < C3::KR; ++m) {
-            const int j0 = r + R0 * m;
+    for (int st = 0; st < kNSt; ++st) {
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+        __syncthreads();                         // stage st is in its buffer
+        const float2 *yb = spec + (st & 1) * kRows * NKP;
+#pragma unroll
+        for (int rr = 0; rr < kRows; ++rr) {
+            const int j0 = st * kRows + rr;
             const float2 w = twa[(freq0<C3>(j0) * c) & (N0 - 1)];
             const float2 wc = make_float2(w.x, -w.y);
 #pragma unroll
             for (int q = 0; q < QT; ++q)
-                cmac(z[q][r], __ldcg(Yv + (size_t)j0 * NKP + threadIdx.x + q * kNT), wc);
+                cmac(z[q][j0 % R0], yb[rr * NKP + threadIdx.x + q * kNT], wc);
         }
+        __syncthreads();                         // its buffer is free again
+        if (st + 2 < kNSt) issue_y(st + 2);
+        cp_async_commit();
     }
 #pragma unroll
     for (int q = 0; q < QT; ++q) {
