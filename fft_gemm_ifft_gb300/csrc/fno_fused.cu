@@ -615,30 +615,43 @@ void make_table32(std::vector<unsigned char> &img) {
 // ---------------------------------------------------------------------------
 // Kernel C on the tensor cores, for 16-bit 256 x 256 layers: one CTA inverts a
 // whole output image.  The column inverse over the kept rows runs on the SIMT
-// cores (32-point inverse register FFTs over the residues q = q1 + 8 q2, then
-// the twiddled sums over q1), giving Zo[t][k] for every row t; the row inverse
-// is then the GEMM y = s Zo' . Tinv^T with Zo' = [Re Zo | Im Zo] (K = 64) and
-// Tinv[n] = [c(k) cos(2 pi k n / N1) | -c(k) sin(...)], one kind::tf32 chain per
-// 128-row tile with N = 256 output samples in tensor memory (tf32 keeps the
-// float32 range of Zo; its 2^-11 precision is within the 16-bit tolerance
-// class).  The epilogue scales by s = 1/(N0 N1), converts to the storage type
-// and stores 64-column boxes by TMA through two swizzled staging tiles.
+// cores in one pass (two-term sums over the signed frequencies, then one
+// 32-point inverse register FFT per thread), giving Zo[t][k] for every row t;
+// the row inverse is then the GEMM y = Zo' . Tinv^T with Zo' = [Re Zo | Im Zo]
+// (K = 64) and Tinv[n] = s [c(k) cos(2 pi k n / N1) | -c(k) sin(...)],
+// s = 1/(N0 N1), one kind::tf32 chain per 128-row tile with N = 256 output
+// samples in tensor memory (tf32 keeps the float32 range of Zo; its 2^-11
+// precision is within the 16-bit tolerance class).  The epilogue converts to
+// the storage type and stores 64-column boxes by TMA through swizzled staging
+// tiles.
 // ---------------------------------------------------------------------------
+// Two floats rounded to the storage type, the first in the low half.
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    uint32_t u;
+    if constexpr (std::is_same<T, __half>::value) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        memcpy(&u, &h, 4);
+    } else {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        memcpy(&u, &h, 4);
+    }
+    return u;
+}
+
 template <typename T>
 struct GeoC {
     static constexpr int N0 = 256, N1 = 256, M0 = 32, M1 = 32, K0 = 64, NK = K0 * M1;
-    static constexpr int B2 = 32, A = N0 / B2;          // column inverse split
     static constexpr int MT = 2;                        // 128-row tiles
     static constexpr uint32_t kTile = 16384;            // 128 rows x 128 bytes
     static constexpr uint32_t kA = 0;                   // [MT][2 chunks] Zo operand, 64 KiB
     static constexpr uint32_t kB = kA + MT * 2 * kTile; // [2 chunks][256 rows] table, 64 KiB
     static constexpr uint32_t kTBytes = 2 * 256 * 128;
     static constexpr uint32_t kY = kB + kTBytes;        // kept modes, 16 KiB
-    static constexpr uint32_t kS = kY + NK * 8;         // [A][B2][M1] residue sums, 64 KiB
-    static constexpr uint32_t kTw = kS + A * B2 * M1 * 8;
+    static constexpr uint32_t kS = kY + NK * 8;         // staging of output rounds 0, 1
+    static constexpr uint32_t kTw = kS + 4 * kTile;
     static constexpr uint32_t kSmem = kTw + N0 * 8 + 1024;
-    static_assert(A * B2 * M1 * 8 >= 4 * kTile && MT * 2 * kTile >= 4 * kTile,
-                  "two rounds of output boxes fit over the sums and over the operand");
+    static_assert(MT * 2 * kTile >= 4 * kTile, "rounds 2, 3 stage over the operand");
     static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -656,7 +669,6 @@ k_phase_c_tc(const __grid_constant__ CUtensorMap ymap, Args a, const void *table
     const int tid = threadIdx.x, warp = tid >> 5;
     const int img = blockIdx.x;
     float2 *ys = reinterpret_cast<float2 *>(base + Gm::kY);
-    float2 *S = reinterpret_cast<float2 *>(base + Gm::kS);
     float2 *tw = reinterpret_cast<float2 *>(base + Gm::kTw);
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_t)));
@@ -685,50 +697,38 @@ k_phase_c_tc(const __grid_constant__ CUtensorMap ymap, Args a, const void *table
     cp_async_commit();
     cp_async_wait_all();
     __syncthreads();
-    // 1. S[q1][r][k] = inverse B2-point DFT over q2 of V[q1 + A q2][k], V the kept
-    //    modes placed at their frequency rows (zero elsewhere)
-    for (int u = tid; u < Gm::A * Gm::M1; u += NT) {
-        const int q1 = u / Gm::M1, k = u % Gm::M1;
-        float2 z[Gm::B2];
+    // 1. Column inverse over the kept rows in one pass.  Kept row j holds the
+    //    signed frequency g = j (j < M0) or j - K0; with g = g1 + M0 g2 (g2 = -1, 0)
+    //    and t = t1 + (N0 / M0) t2,
+    //      Zo[t][k] = sum_g1 e^{+2 pi i g1 t2 / M0} U[g1],
+    //      U[g1] = sum_g2 V[g][k] e^{+2 pi i g t1 / N0},
+    //    two terms per U[g1] and one M0-point inverse register FFT per (t1, k):
+    //    warp t1, lane k.  Zo goes into the K-major operand, chunk 0 the real
+    //    parts, chunk 1 the imaginary.
+    {
+        constexpr int G1 = Gm::M0, T1 = Gm::N0 / G1;
+        static_assert(T1 * Gm::M1 == NT && Gm::M1 == 32 && Gm::K0 == 2 * G1, "warp t1, lane k");
+        const int t1 = warp, k = tid & 31;
+        float2 z[G1];
 #pragma unroll
-        for (int q2 = 0; q2 < Gm::B2; ++q2) {
-            const int q = q1 + Gm::A * q2;
-            int j = -1;
-            if (q < Gm::M0) j = q;
-            else if (q >= Gm::N0 - Gm::M0) j = q - (Gm::N0 - Gm::K0);
-            z[q2] = j >= 0 ? ys[j * Gm::M1 + k] : make_float2(0.f, 0.f);
+        for (int g1 = 0; g1 < G1; ++g1) {
+            const float2 w0 = tw[(g1 * t1) & (Gm::N0 - 1)];          // e^{-2 pi i g t1 / N0}
+            const float2 w1 = tw[((g1 - G1) * t1) & (Gm::N0 - 1)];
+            float2 acc = make_float2(0.f, 0.f);
+            cmac(acc, ys[g1 * Gm::M1 + k], make_float2(w0.x, -w0.y));
+            cmac(acc, ys[(g1 + G1) * Gm::M1 + k], make_float2(w1.x, -w1.y));
+            z[g1] = acc;
         }
-        fft::fft_dif<Gm::B2, 1>(z);
+        fft::fft_dif<G1, 1>(z);
 #pragma unroll
-        for (int r = 0; r < Gm::B2; ++r)
-            S[(q1 * Gm::B2 + r) * Gm::M1 + k] = z[fft::bitrev(r, fft::ilog2(Gm::B2))];
-    }
-    __syncthreads();
-    // 2. Zo[t][k] = sum_q1 conj(W_N0^{q1 t}) S[q1][t mod B2][k], four bins per unit,
-    //    into the K-major operand: chunk 0 the real parts, chunk 1 the imaginary
-    for (int u = tid; u < Gm::N0 * (Gm::M1 / 4); u += NT) {
-        const int t = u / (Gm::M1 / 4), k0 = 4 * (u % (Gm::M1 / 4));
-        float2 acc[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int q1 = 0; q1 < Gm::A; ++q1) {
-            const float2 wv = tw[(q1 * t) & (Gm::N0 - 1)];
-            const float2 wc = make_float2(wv.x, -wv.y);
-            const float4 *s4 = reinterpret_cast<const float4 *>(
-                S + (q1 * Gm::B2 + (t % Gm::B2)) * Gm::M1 + k0);
-            const float4 p0 = s4[0], p1 = s4[1];
-            cmac(acc[0], make_float2(p0.x, p0.y), wc);
-            cmac(acc[1], make_float2(p0.z, p0.w), wc);
-            cmac(acc[2], make_float2(p1.x, p1.y), wc);
-            cmac(acc[3], make_float2(p1.z, p1.w), wc);
+        for (int t2 = 0; t2 < G1; ++t2) {
+            const int t = t1 + T1 * t2;
+            const float2 v = z[fft::bitrev(t2, fft::ilog2(G1))];
+            char *At = base + Gm::kA + (t / 128) * 2 * Gm::kTile;
+            const uint32_t off = sw_off(t % 128, k);
+            *reinterpret_cast<float *>(At + off) = v.x;
+            *reinterpret_cast<float *>(At + Gm::kTile + off) = v.y;
         }
-        char *At = base + Gm::kA + (t / 128) * 2 * Gm::kTile;
-        const uint32_t off = sw_off(t % 128, k0);
-        *reinterpret_cast<float4 *>(At + off) =
-            make_float4(acc[0].x, acc[1].x, acc[2].x, acc[3].x);
-        *reinterpret_cast<float4 *>(At + Gm::kTile + off) =
-            make_float4(acc[0].y, acc[1].y, acc[2].y, acc[3].y);
     }
     fence_async_smem();
     tc_before_sync();
@@ -751,9 +751,8 @@ k_phase_c_tc(const __grid_constant__ CUtensorMap ymap, Args a, const void *table
     // 3. rows out: warp w reads lanes 32 (w % 4).. of tensor memory; the two warp
     //    halves take column blocks 2h and 2h + 1 (64 outputs each) per tile.
     //    Round r = 2 t + step stages its two 64-column boxes in a region of its
-    //    own (rounds 0, 1 over the residue sums, 2, 3 over the Zo operand, both
-    //    free once the MMAs completed), so no round waits for an earlier store.
-    const float scale = 1.0f / ((float)Gm::N0 * (float)Gm::N1);
+    //    own (rounds 0, 1 in the staging region, 2, 3 over the Zo operand, free
+    //    once the MMAs completed), so no round waits for an earlier store.
     const int half = warp >> 2, lrow = 32 * (warp & 3) + (tid & 31);
     for (int t = 0; t < Gm::MT; ++t) {
         for (int step = 0; step < 2; ++step) {
@@ -768,21 +767,8 @@ k_phase_c_tc(const __grid_constant__ CUtensorMap ymap, Args a, const void *table
                 tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256 * t + 64 * cb + 16 * g, v);
                 uint32_t pk[8];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float lo = ok ? v[2 * q] * scale : 0.f, hi = ok ? v[2 * q + 1] * scale : 0.f;
-                    T tl, th;
-                    if constexpr (std::is_same<T, __half>::value) {
-                        tl = __float2half_rn(lo);
-                        th = __float2half_rn(hi);
-                    } else {
-                        tl = __float2bfloat16_rn(lo);
-                        th = __float2bfloat16_rn(hi);
-                    }
-                    uint16_t ul, uh;
-                    memcpy(&ul, &tl, 2);
-                    memcpy(&uh, &th, 2);
-                    pk[q] = (uint32_t)ul | ((uint32_t)uh << 16);
-                }
+                for (int q = 0; q < 8; ++q)
+                    pk[q] = pack2<T>(ok ? v[2 * q] : 0.f, ok ? v[2 * q + 1] : 0.f);
                 *reinterpret_cast<uint4 *>(stage + sw_off16(lrow, 16 * g)) =
                     make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 *reinterpret_cast<uint4 *>(stage + sw_off16(lrow, 16 * g + 8)) =
@@ -818,7 +804,10 @@ void make_table_c(std::vector<unsigned char> &img) {
     const double two_pi = 2.0 * M_PI;
     for (int n = 0; n < Gm::N1; ++n)
         for (int k = 0; k < Gm::M1; ++k) {
-            const double ck = (k == 0 || 2 * k == Gm::N1) ? 1.0 : 2.0;
+            // c(k) and the inverse's 1/(N0 N1) (a power of two: the rounding is
+            // that of the unscaled value)
+            const double ck = ((k == 0 || 2 * k == Gm::N1) ? 1.0 : 2.0) /
+                              ((double)Gm::N0 * (double)Gm::N1);
             const double ang = two_pi * (double)k * (double)n / (double)Gm::N1;
             const float c = (float)(ck * std::cos(ang)), sn = (float)(-ck * std::sin(ang));
             memcpy(&img[sw_off(n, k)], &c, 4);
