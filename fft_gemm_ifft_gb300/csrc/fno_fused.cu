@@ -250,24 +250,30 @@ __global__ void __launch_bounds__(kNT) k_phase_c(Args a) {
 
 
 // ---------------------------------------------------------------------------
-// Kernel A of the three-kernel path on the tensor cores: one CTA transforms a
-// whole input image, so the kept modes leave it complete (no partial copies).
+// Kernel A of the three-kernel path on the tensor cores for 16-bit 256 x 256
+// layers: a CTA transforms whole input images, so the kept modes leave it
+// complete (no partial copies).  One persistent CTA per SM takes the images
+// blockIdx.x, blockIdx.x + gridDim.x, ...: as soon as an image's MMAs have
+// read its tile, the next image's tile is requested into the same buffer and
+// lands while the current image's column work runs.
 //
-// TMA brings the image into shared memory as M tiles of 128 rows, K-major with
+// TMA brings an image into shared memory as M tiles of 128 rows, K-major with
 // the 128-byte swizzle.  The row DFT of bins 0..M1-1 is the GEMM
 // Z = X . T^T, T[j][n] = cos(2 pi j n / N1) (j < M1) and -sin(...) (j >= M1),
-// on tcgen05 with the accumulator in tensor memory, one kind::f16 pass for the
-// 16-bit images of this kernel (their tolerance class is 1e-2; fp32 images
-// have their own pipelined kernel below).  The column DFT over the N0 rows, kept rows
-// only, runs on the SIMT cores from the tensor-memory rows: r = r1 + R1 r2,
-// B2-point register FFTs over r2, then X[j][k] = sum_r1 W_N0^{f r1} S[r1][f mod B2][k].
+// on tcgen05 with the accumulator in tensor memory, one kind::f16 pass (the
+// 16-bit tolerance class is 1e-2; fp32 images have their own pipelined kernel
+// below).  The column DFT over the N0 rows, kept rows only, runs on the SIMT
+// cores in two steps: with rows t = t1 + T1 t2 and the signed frequencies
+// g = g1 + G1 g2 (G1 = M0, T1 = N0 / G1),
+//   F[t1][g1][k] = sum_t2 Z[t1 + T1 t2][k] e^{-2 pi i g1 t2 / G1}   (register FFTs)
+//   X[g][k]      = sum_t1 W_N0^{g t1} F[t1][g mod G1][k]             (T1 terms).
 // ---------------------------------------------------------------------------
 namespace tca {
 
 constexpr int NT = 256;
 template <typename T> struct Shape;
 template <> struct Shape<__half> {         // 256 x 256, 32 x 32 modes
-    static constexpr int N0 = 256, N1 = 256, M0 = 32, M1 = 32, kE = 64, B2 = 16;
+    static constexpr int N0 = 256, N1 = 256, M0 = 32, M1 = 32, kE = 64;
     static constexpr int kMinBlocks = 1;
 };
 template <> struct Shape<__nv_bfloat16> : Shape<__half> {};
@@ -280,26 +286,26 @@ struct Geo {
     static constexpr int MT = N0 / 128;                 // M tiles
     static constexpr int N = 2 * M1;                    // MMA N: bins, re then im
     static constexpr int K0 = 2 * M0, NK = K0 * M1;
-    static constexpr int B2 = S::B2, R1 = N0 / B2;
+    static constexpr int G1 = M0, T1 = N0 / G1;         // column DFT split
     static constexpr uint32_t kTile = 16384;            // 128 rows x 128 bytes
     static constexpr uint32_t kXBytes = (uint32_t)MT * KC * kTile;
     static constexpr uint32_t kTChunk = (uint32_t)N * 128;
     static constexpr uint32_t kTBytes = KC * kTChunk;
-    static constexpr int ZS = M1 + 1;                   // Z plane row stride (floats)
-    static constexpr uint32_t kZBytes = (uint32_t)N0 * ZS * 4 * 2;
-    static constexpr uint32_t kSBytes = (uint32_t)R1 * B2 * M1 * 8;
-    static constexpr uint32_t kRegion = kXBytes > kZBytes + kSBytes ? kXBytes : kZBytes + kSBytes;
-    static constexpr uint32_t kT = kRegion;              // offsets from a 1024-aligned base
-    static constexpr uint32_t kTw = kT + kTBytes;
-    static constexpr uint32_t kSmem = kTw + N0 * 8 + 1024;
+    // Z planes (re, im) [N0][M1], columns XOR-swizzled by the row; the column
+    // sums F [T1][G1][M1] go over them
+    static constexpr uint32_t kZBytes = (uint32_t)N0 * M1 * 4 * 2;
+    static constexpr uint32_t kFBytes = (uint32_t)T1 * G1 * M1 * 8;
+    static constexpr uint32_t kT = kXBytes;             // offsets from a 1024-aligned base
+    static constexpr uint32_t kZ = kT + kTBytes;
+    static constexpr uint32_t kSmem = kZ + (kZBytes > kFBytes ? kZBytes : kFBytes) + 1024;
     static constexpr uint32_t kTmemCols = MT * N <= 32 ? 32 : (MT * N <= 64 ? 64 : 128);
-    static_assert(R1 * M1 % NT == 0 || R1 * M1 < NT, "column units");
-    static_assert(NK % NT == 0, "kept modes per thread");
+    static_assert(T1 * 32 == NT && M1 == 32 && K0 == 2 * G1, "warp t1, lane k");
+    static_assert(kSmem + 1024 <= 232448, "image tile, table and Z planes fit one CTA");
 };
 
 template <typename T>
 __global__ void __launch_bounds__(NT, Shape<T>::kMinBlocks)
-k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *tables) {
+k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *tables, int nimg) {
     using Gm = Geo<T>;
     using namespace tcu;
     extern __shared__ __align__(1024) char smem_raw[];
@@ -307,10 +313,16 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
                                           ~static_cast<uintptr_t>(1023));
     __shared__ __align__(8) uint64_t bar_x, bar_t, bar_mma;
     __shared__ uint32_t s_tmem;
-    const unsigned long long t0 = a.trace ? trace_now() : 0;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int img = blockIdx.x;
-    float2 *tw = reinterpret_cast<float2 *>(base + Gm::kTw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the image: MT x KC boxes of 128 rows x 128 bytes (thread 0)
+    auto load_image = [&](int img) {
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     ::"r"(tc_smem_addr(&bar_x)), "r"(Gm::kXBytes) : "memory");
+        for (int t = 0; t < Gm::MT; ++t)
+            for (int kc = 0; kc < Gm::KC; ++kc)
+                tma_load_2d(tc_smem_addr(base + (t * Gm::KC + kc) * Gm::kTile), &xmap,
+                            kc * Gm::kE, img * Gm::N0 + 128 * t, &bar_x);
+    };
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_x)));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_t)));
@@ -322,96 +334,101 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
         asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                      ::"r"(tc_smem_addr(base + Gm::kT)), "l"(tables), "r"(Gm::kTBytes),
                      "r"(tc_smem_addr(&bar_t)) : "memory");
-        // the image: MT x KC boxes of 128 rows x 128 bytes
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                     ::"r"(tc_smem_addr(&bar_x)), "r"(Gm::kXBytes) : "memory");
-        for (int t = 0; t < Gm::MT; ++t)
-            for (int kc = 0; kc < Gm::KC; ++kc)
-                tma_load_2d(tc_smem_addr(base + (t * Gm::KC + kc) * Gm::kTile), &xmap,
-                                kc * Gm::kE, img * Gm::N0 + 128 * t, &bar_x);
+        if ((int)blockIdx.x < nimg) load_image(blockIdx.x);
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(tc_smem_addr(&s_tmem)), "r"(Gm::kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
-    for (int e = tid; e < Gm::N0; e += NT) tw[e] = a.tw0[e];
     tc_before_sync();
     __syncthreads();
     tc_after_sync();
     pdl_trigger();
     const uint32_t tmem = s_tmem;
     bool ok = mbar_wait(&bar_t, 0, a.err);
-    ok &= mbar_wait(&bar_x, 0, a.err);
-    const unsigned long long t_x = a.trace ? trace_now() : 0;     // the image has landed
     const uint32_t xs = tc_smem_addr(base), ts = tc_smem_addr(base + Gm::kT);
-    if (tid == 0) {
-        tc_after_sync();
-        for (int t = 0; t < Gm::MT; ++t) {
-            const uint32_t d = tmem + t * Gm::N;
-            for (int kc = 0; kc < Gm::KC; ++kc) {
+    float *zr = reinterpret_cast<float *>(base + Gm::kZ);
+    float *zi = zr + Gm::N0 * Gm::M1;
+    float2 *F = reinterpret_cast<float2 *>(base + Gm::kZ);
+    uint32_t it = 0;
+    for (int img = blockIdx.x; img < nimg; img += gridDim.x, ++it) {
+        const unsigned long long t0 = a.trace ? trace_now() : 0;
+        ok &= mbar_wait(&bar_x, it, a.err);
+        const unsigned long long t_x = a.trace ? trace_now() : 0;     // the image has landed
+        if (tid == 0 && ok) {
+            tc_after_sync();
+            for (int t = 0; t < Gm::MT; ++t) {
+                const uint32_t d = tmem + t * Gm::N;
+                for (int kc = 0; kc < Gm::KC; ++kc) {
 #pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint32_t ao = xs + (t * Gm::KC + kc) * Gm::kTile + s * 32;
-                    const uint32_t bo = ts + kc * Gm::kTChunk + s * 32;
-                    const uint32_t acc = (kc | s) ? 1u : 0u;
-                    constexpr uint32_t id = idesc_f16(Gm::N, std::is_same<T, __nv_bfloat16>::value);
-                    mma_f16(d, desc_sw128(ao), desc_sw128(bo), id, acc);
+                    for (int s = 0; s < 4; ++s) {
+                        const uint32_t ao = xs + (t * Gm::KC + kc) * Gm::kTile + s * 32;
+                        const uint32_t bo = ts + kc * Gm::kTChunk + s * 32;
+                        const uint32_t acc = (kc | s) ? 1u : 0u;
+                        constexpr uint32_t id =
+                            idesc_f16(Gm::N, std::is_same<T, __nv_bfloat16>::value);
+                        mma_f16(d, desc_sw128(ao), desc_sw128(bo), id, acc);
+                    }
+                }
+            }
+            mma_commit(&bar_mma);
+        }
+        ok &= mbar_wait(&bar_mma, it, a.err);
+        tc_after_sync();
+        // the MMAs have read the tile: the next image's tile lands under this
+        // image's column work
+        const int next = img + (int)gridDim.x;
+        if (tid == 0 && ok && next < nimg) load_image(next);
+        const unsigned long long t_z = a.trace ? trace_now() : 0;     // the row DFT is done
+        // Z planes from tensor memory: warps w and w + 4 read the same lanes, the
+        // first the re, the second the im half
+        {
+            const int half = warp >> 2;
+            float *dz = half ? zi : zr;
+            for (int t = 0; t < Gm::MT; ++t) {
+                const int row = 128 * t + 32 * (warp & 3) + lane;
+#pragma unroll
+                for (int g = 0; g < Gm::M1 / 16; ++g) {
+                    float v[16];
+                    tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + t * Gm::N +
+                                  half * Gm::M1 + 16 * g, v);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        dz[row * Gm::M1 + ((16 * g + q) ^ (row & 31))] = ok ? v[q] : 0.f;
                 }
             }
         }
-        mma_commit(&bar_mma);
-    }
-    ok &= mbar_wait(&bar_mma, 0, a.err);
-    tc_after_sync();
-    const unsigned long long t_z = a.trace ? trace_now() : 0;     // the row DFT is done
-    // Z planes (re, im) from tensor memory into the region the tile occupied:
-    // warps w and w + 4 read the same lanes, the first the re, the second the im half
-    float *zr = reinterpret_cast<float *>(base);
-    float *zi = zr + Gm::N0 * Gm::ZS;
-    float2 *S = reinterpret_cast<float2 *>(base + Gm::kZBytes);
-    {
-        const int half = warp >> 2;
-        float *dz = half ? zi : zr;
-        for (int t = 0; t < Gm::MT; ++t) {
-            const int row = 128 * t + 32 * (warp & 3) + (tid & 31);
+        tc_before_sync();
+        __syncthreads();
+        // F[t1][g1][k]: G1-point FFT over t2 of Z[t1 + T1 t2][k], warp t1, lane k
+        float2 z[Gm::G1];
 #pragma unroll
-            for (int g = 0; g < Gm::M1 / 16; ++g) {
-                float v[16];
-                tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + t * Gm::N + half * Gm::M1 +
-                              16 * g, v);
-#pragma unroll
-                for (int q = 0; q < 16; ++q) dz[row * Gm::ZS + 16 * g + q] = ok ? v[q] : 0.f;
-            }
+        for (int t2 = 0; t2 < Gm::G1; ++t2) {
+            const int r = warp + Gm::T1 * t2, c = r * Gm::M1 + (lane ^ (r & 31));
+            z[t2] = make_float2(zr[c], zi[c]);
         }
-    }
-    tc_before_sync();
-    __syncthreads();
-    // column DFT: S[r1][q][k] = B2-point DFT over r2 of Z[r1 + R1 r2][k]
-    for (int u = tid; u < Gm::R1 * Gm::M1; u += NT) {
-        const int r1 = u / Gm::M1, k = u % Gm::M1;
-        float2 z[Gm::B2];
+        fft::fft_dif<Gm::G1, -1>(z);
+        __syncthreads();                         // Z is read: F goes over it
 #pragma unroll
-        for (int r2 = 0; r2 < Gm::B2; ++r2) {
-            const int r = r1 + Gm::R1 * r2;
-            z[r2] = make_float2(zr[r * Gm::ZS + k], zi[r * Gm::ZS + k]);
+        for (int g1 = 0; g1 < Gm::G1; ++g1)
+            F[(warp * Gm::G1 + g1) * Gm::M1 + lane] = z[fft::bitrev(g1, fft::ilog2(Gm::G1))];
+        __syncthreads();
+        // kept modes: X[j][k] = sum_t1 W_N0^{g t1} F[t1][g mod G1][k], g the signed
+        // frequency of kept row j (j, or j - K0 for the high rows)
+        float2 *dst = a.part + (size_t)img * Gm::NK;
+        for (int o = tid; o < Gm::NK; o += NT) {
+            const int j = o / Gm::M1, k = o % Gm::M1;
+            const int g = j < Gm::M0 ? j : j - Gm::K0, g1 = j & (Gm::G1 - 1);
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int t1 = 0; t1 < Gm::T1; ++t1)
+                cmac(acc, F[(t1 * Gm::G1 + g1) * Gm::M1 + k],
+                     __ldg(a.tw0 + ((g * t1) & (Gm::N0 - 1))));
+            __stcg(dst + o, acc);
         }
-        fft::fft_dif<Gm::B2, -1>(z);
-#pragma unroll
-        for (int q = 0; q < Gm::B2; ++q)
-            S[(r1 * Gm::B2 + q) * Gm::M1 + k] = z[fft::bitrev(q, fft::ilog2(Gm::B2))];
-    }
-    __syncthreads();
-    // kept modes: X[j][k] = sum_r1 W_N0^{f r1} S[r1][f mod B2][k]
-    float2 *dst = a.part + (size_t)img * Gm::NK;
-    for (int o = tid; o < Gm::NK; o += NT) {
-        const int j = o / Gm::M1, k = o % Gm::M1;
-        const int f = j < Gm::M0 ? j : Gm::N0 - Gm::K0 + j;
-        float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int r1 = 0; r1 < Gm::R1; ++r1)
-            cmac(acc, S[(r1 * Gm::B2 + (f % Gm::B2)) * Gm::M1 + k], tw[(f * r1) & (Gm::N0 - 1)]);
-        __stcg(dst + o, acc);
+        __syncthreads();                         // F is read: the next Z goes over it
+        cta_record_at(a, 0, 0, img, t0, t_x, t_z);
     }
     tc_before_sync();
     __syncthreads();
@@ -420,7 +437,6 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(Gm::kTmemCols));
     }
-    cta_record(a, 0, 0, t0, t_x, t_z);
 }
 
 // ---------------------------------------------------------------------------
@@ -1357,7 +1373,10 @@ struct Pdl {
                     if (!tcu::encode_rows_tiled(&xmap, a.x, (int64_t)p.batch * p.cin * Gm::N0,
                                                 Gm::N1, sizeof(T), Gm::kE, tcu::tma_type<T>()))
                         return cudaErrorInvalidValue;
-                    tca::k_phase_a_tc<T><<<nA, tca::NT, Gm::kSmem, s>>>(xmap, a, p.fused_tables);
+                    // persistent: one CTA per SM walks the images
+                    const int grid = nA < p.num_sms ? nA : p.num_sms;
+                    tca::k_phase_a_tc<T><<<grid, tca::NT, Gm::kSmem, s>>>(xmap, a, p.fused_tables,
+                                                                         nA);
                 }
                 e = cudaGetLastError();
                 done_a = true;

@@ -772,23 +772,30 @@ __device__ __forceinline__ unsigned long long trace_now() {
 // Three-kernel variants: one trace record per CTA, written once every thread of
 // the CTA is done (t_start: entry, t_ready: the wait for the previous kernel
 // returned).  A no-op unless the plan traces.
-__device__ __forceinline__ void cta_record(const Args &a, int phase, int first,
-                                           unsigned long long t_start,
-                                           unsigned long long t_ready,
-                                           unsigned long long t_compute = 0) {
+// cta_record_at: the same for work item `idx` of a CTA that runs several.
+__device__ __forceinline__ void cta_record_at(const Args &a, int phase, int first, int idx,
+                                              unsigned long long t_start,
+                                              unsigned long long t_ready,
+                                              unsigned long long t_compute = 0) {
     if (!a.trace) return;
     __syncthreads();
     if (threadIdx.x != 0) return;
     unsigned smid;
     asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
     fno_trace_record_t r;
-    r.item = ((unsigned)phase << 24) | (blockIdx.x & 0xFFFFFFu);
+    r.item = ((unsigned)phase << 24) | ((unsigned)idx & 0xFFFFFFu);
     r.worker = smid;
     r.t_start = t_start;
     r.t_ready = t_ready;
     r.t_end = trace_now();
     r.t_compute = t_compute ? t_compute : r.t_end;
-    a.trace[first + blockIdx.x] = r;
+    a.trace[first + idx] = r;
+}
+__device__ __forceinline__ void cta_record(const Args &a, int phase, int first,
+                                           unsigned long long t_start,
+                                           unsigned long long t_ready,
+                                           unsigned long long t_compute = 0) {
+    cta_record_at(a, phase, first, (int)blockIdx.x, t_start, t_ready, t_compute);
 }
 
 // item = (pair * nob + output block) * batch blocks + batch block; a.bg = batch
