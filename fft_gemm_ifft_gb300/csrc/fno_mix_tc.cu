@@ -9,15 +9,16 @@
 //     [Yi] = [ Wi^T   Wr^T ] [Xi]      (M = 2 Cout rows, K = 2 Cin, N = batch)
 //
 // it is one tcgen05.mma chain (kind::f16, M = 128, K = 128 in 8 steps of 16)
-// per mode, accumulating in tensor memory.  A CTA takes a run of four
-// adjacent modes of one kept row (adjacent in the weight tensor too): it
-// builds the four 128 x 128 real-block weight operands in shared memory (128-
-// byte swizzle, K-major) from 16-byte loads of the weights -- before waiting
-// for the forward-transform kernel, since they do not depend on it -- then
-// the four operands [Xr; Xi]^T (N rows = batch) from the kept modes, issues
-// the four chains into four column ranges of tensor memory, and writes Y for
-// the four modes of every (b, o) as one 32-byte piece through a shared-memory
-// staging tile.  Channel counts up to 64 are zero-padded to the tile.
+// per mode, accumulating in tensor memory.  A CTA takes a run of kRun (two or
+// four) adjacent modes of one kept row (adjacent in the weight tensor too): it
+// builds the run's 128 x 128 real-block weight operands in shared memory (128-
+// byte swizzle, K-major) from 8- or 16-byte loads of the weights -- before
+// waiting for the forward-transform kernel, since they do not depend on it --
+// then the operands [Xr; Xi]^T (N rows = batch) from the kept modes, issues
+// one chain per mode into its own column range of tensor memory, and writes Y
+// for the run's modes of every (b, o) as one contiguous piece through a
+// shared-memory staging tile.  Channel counts up to 64 are zero-padded to the
+// tile.
 #include <type_traits>
 
 #include "fno_fused_dev.cuh"
@@ -28,9 +29,16 @@ namespace {
 
 using namespace tcu;
 
-constexpr int kMT = 256;                  // threads
+#ifndef FNO_MIX_THREADS
+#define FNO_MIX_THREADS 256
+#endif
+constexpr int kMT = FNO_MIX_THREADS;      // threads (256 or 512)
+// Runs of two modes fit two CTAs on an SM (97 KB of shared memory each against
+// 193 KB for four); behind the persistent 16-bit forward transform, which
+// leaves no SM to an early mixing CTA, that measured 275 -> 266 us on the
+// 32 x 64-channel 256^2 fp16 layer.
 #ifndef FNO_MIX_RUN
-#define FNO_MIX_RUN 4
+#define FNO_MIX_RUN 2
 #endif
 constexpr int kRun = FNO_MIX_RUN;         // modes per CTA (2 or 4)
 static_assert(kRun == 2 || kRun == 4, "modes per CTA");
@@ -206,8 +214,10 @@ __global__ void __launch_bounds__(kMT, kRun == 2 ? 2 : 1) k_mix_tc(MixTcArgs a) 
     {
         const int m = 32 * (warp & 3) + (tid & 31);          // D row: o (re) or 64 + o (im)
         const int o = m % kCh, part = m / kCh;
-        // warps 0-3 the first half of the run's modes, warps 4-7 the second
-        for (int r = (kRun / 2) * (warp >> 2); r < (kRun / 2) * (warp >> 2) + kRun / 2; ++r) {
+        // each group of four warps drains kPer of the run's modes
+        constexpr int kPer = kRun / (kMT / 128);
+        static_assert(kPer >= 1 && kPer * (kMT / 128) == kRun, "modes per warp group");
+        for (int r = kPer * (warp >> 2); r < kPer * (warp >> 2) + kPer; ++r) {
             for (int g = 0; g < nbp / 16; ++g) {
                 float v[16];
                 tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + r * nbp + 16 * g, v);
