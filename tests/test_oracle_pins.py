@@ -409,6 +409,57 @@ def test_fno_single_spectral_layer_against_numpy_fft(oracle_mod):
     assert np.max(np.abs(got - want)) < 1e-12
 
 
+def _numpy_spectral_conv(a, w, modes):
+    """The layer written independently with numpy.fft: rfft2, the two corner
+    blocks (low rows, then high rows) mixed by einsum, irfft2."""
+    h, wd = a.shape[-2:]
+    m0, m1 = modes
+    Xf = np.fft.rfft2(a)
+    rows = np.r_[0:m0, h - m0:h]
+    wk = np.concatenate([w[0], w[1]], axis=2)
+    half = np.zeros(a.shape[:1] + (w.shape[2], h, wd // 2 + 1), dtype=complex)
+    half[:, :, rows, :m1] = np.einsum("bikl,iokl->bokl", Xf[:, :, rows, :m1], wk)
+    return np.fft.irfft2(half, s=(h, wd))
+
+
+def _numpy_fno(x, p, modes):
+    """The whole stack with both branches live: a_{l+1} = GELU(S_l(a_l) + P_l a_l
+    + b_l), no GELU after the last layer, then the two-layer head."""
+    lin = lambda wt, b, v: np.einsum("ci,bihw->bchw", wt, v) + b[None, :, None, None]
+    a = lin(p["lift_w"], p["lift_b"], x)
+    L = p["pw_w"].shape[0]
+    for l in range(L):
+        t = _numpy_spectral_conv(a, p["spec_w"][l], modes) + lin(p["pw_w"][l], p["pw_b"][l], a)
+        a = t if l == L - 1 else gelu_ref(t)
+    return lin(p["proj2_w"], p["proj2_b"], gelu_ref(lin(p["proj1_w"], p["proj1_b"], a)))
+
+
+@pytest.mark.parametrize("nlayers", [2, 3])
+def test_fno_both_branches_against_numpy(oracle_mod, nlayers):
+    # Spectral and pointwise weights and all biases non-zero together: pins that
+    # the two branches are summed before the GELU (gelu(s) + gelu(t) agrees with
+    # both one-branch reductions above, because gelu(0) = 0), that the pointwise
+    # term reads the same layer's input as the spectral one, and that the last
+    # layer has no GELU.  Rectangular grid (8 x 16) so that a swapped axis fails.
+    r = rng(54 + nlayers)
+    modes = (2, 3)
+    p = small_fno_params(r, width=5, nlayers=nlayers, modes=modes)
+    x = r.standard_normal((2, 3, 8, 16))
+    got = oracle_mod.fno_forward(x, p, modes)
+    want = _numpy_fno(x, p, modes)
+    assert np.max(np.abs(want)) > 1.0
+    assert np.max(np.abs(got - want)) < 1e-12 * max(1.0, np.max(np.abs(want)))
+    # the plausible mistakes named above all move the result well past that bound
+    lin = lambda wt, b, v: np.einsum("ci,bihw->bchw", wt, v) + b[None, :, None, None]
+    a = lin(p["lift_w"], p["lift_b"], x)
+    for l in range(nlayers):
+        s = _numpy_spectral_conv(a, p["spec_w"][l], modes)
+        t = lin(p["pw_w"][l], p["pw_b"][l], a)
+        a = s + t if l == nlayers - 1 else gelu_ref(s) + gelu_ref(t)
+    wrong = lin(p["proj2_w"], p["proj2_b"], gelu_ref(lin(p["proj1_w"], p["proj1_b"], a)))
+    assert np.max(np.abs(got - wrong)) > 1e-3
+
+
 # ---------------------------------------------------------------------------
 # Backward pass: pinned to the (pinned) forward by the identities a gradient
 # of a real loss must satisfy.  The layer is linear in x and in w, so with
