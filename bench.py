@@ -1,17 +1,25 @@
 """Benchmark of the FNO spectral-convolution layer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--workload 2d_f32]
+                    [--workload 2d_f16] [--no-per-config]
 
 One step is one forward pass of the layer (truncated forward FFT, per-mode
-mixing, inverse FFT) over one batch of the workload, through the C ABI.
-Inputs are resident in device memory before the timed region; successive
-steps rotate through enough distinct (x, w, y) sets to exceed twice the L2
-size, so every step reads and writes HBM.  Steps are replayed from a CUDA
-graph (the forward call is capturable) so host launch overhead does not
-pace the GPU.  Under torchrun each rank runs its own batch (weak scaling,
-replicas: the layer has no exchange step), the timed region is bracketed by
-barriers and the slowest rank's time is reported.
+mixing, inverse FFT) over one batch of the workload, through the C ABI.  The
+headline workload is the largest single-GPU one: B=32, C=64, 256x256, 32x32
+modes per block, fp16 storage with float32 accumulation (570 MB of
+algorithmic traffic per forward).  Inputs are resident in device memory before
+the timed region; successive steps rotate through enough distinct (x, w, y)
+sets to exceed twice the L2 size, so every step reads and writes HBM.  Steps
+are replayed from a CUDA graph (the forward call is capturable) so host launch
+overhead does not pace the GPU.  Under torchrun each rank runs its own batch
+(weak scaling, replicas: the layer has no exchange step), the timed region is
+bracketed by barriers and the slowest rank's time is reported.
+
+The same JSON line carries ``per_config``: every workload (the 1-D, 2-D fp32,
+2-D fp16 and 3-D layers and the 2-D FNO stack, the last as one captured
+``fno_forward``) timed the same way for about ``--per-config-seconds`` of
+device time each, with its own roofline, clocks and the relative L2 error of
+one sample against the float64 oracle (checked after the timing, outside it).
 
 ``--impl reference`` times the float64 CPU oracle on the same workload (one
 sample of the batch per step, on all host cores); it is a deliberately slow
@@ -35,6 +43,13 @@ sys.path.insert(0, ROOT)
 
 METRIC = "spectral-conv samples/s & achieved HBM GB/s / roofline fraction on 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
+HEADLINE = "2d_f16"
+# every workload, in the order of the per-config record
+PER_CONFIG = ("1d_f32", "2d_f32", "2d_f16", "3d_f32", "fno2d_f32")
+# plan flags each workload runs with by default (FNO_PLAN_* bits)
+DEFAULT_FLAGS = {}
+# relative L2 bars against the float64 oracle
+REL_TOL = {"f32": 1e-5, "f16": 1e-2, "bf16": 1e-2}
 
 
 def parse_args(argv=None):
@@ -43,11 +58,17 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="2d_f32")
-    ap.add_argument("--flags", type=int, default=0, help="FNO_PLAN_* bits (ablations)")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--flags", type=int, default=-1,
+                    help="FNO_PLAN_* bits (ablations); default: the workload's own")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time the headline workload only")
+    ap.add_argument("--per-config-seconds", type=float, default=0.5)
+    ap.add_argument("--no-check", action="store_true",
+                    help="skip the oracle check of one sample per workload")
     return ap.parse_args(argv)
 
 
@@ -162,7 +183,7 @@ def whole_job_rate(batch_per_rank: int, world: int, steps: int, ms_max: float) -
     return world * batch_per_rank * steps / (ms_max / 1e3)
 
 
-def e2e_pipelined(torch, conv, case, x_np, ws, stream, steps, world, dev, dist):
+def e2e_pipelined(torch, conv, case, x_np, ws, stream, steps, world, dev):
     """Milliseconds for `steps` host-to-host forwards through the public API,
     pipelined over three slots (H2D, layer, D2H on their own streams)."""
     from fft_gemm_ifft_gb300 import workloads
@@ -197,6 +218,7 @@ def e2e_pipelined(torch, conv, case, x_np, ws, stream, steps, world, dev, dist):
     run(nslot)
     torch.cuda.synchronize(dev)
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s_in)
@@ -210,33 +232,25 @@ def e2e_pipelined(torch, conv, case, x_np, ws, stream, steps, world, dev, dist):
     return max_over_ranks(e0.elapsed_time(e1), world, dev)
 
 
-def bench_gpu(args, rank, world, local):
+def _rel_l2(got, ref):
     import numpy as np
-    import torch
-    import torch.distributed as dist
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    return float(np.linalg.norm(got - ref) / max(float(np.linalg.norm(ref)), 1e-300))
 
-    from fft_gemm_ifft_gb300 import SpectralConv, workloads
 
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    case = workloads.CASES[args.workload]
-    conv = SpectralConv(case.n, case.modes, case.batch, case.cin, case.cout, case.dtype,
-                        args.flags)
-    x_np, w_np = workloads.make_x(case), workloads.make_w(case)
-    set_bytes = (x_np.nbytes + w_np.nbytes + math.prod(case.y_shape) * case.elem_bytes)
+def _l2_bytes(torch, dev):
     props = torch.cuda.get_device_properties(dev)
-    l2 = int(getattr(props, "L2_cache_size", 0)) or (126 << 20)
-    nsets = max(2, math.ceil(2 * l2 / set_bytes))
-    xs = [workloads.to_torch_storage(x_np, case.dtype).to(dev) for _ in range(nsets)]
-    ws = [workloads.to_torch_storage(w_np, case.dtype).to(dev) for _ in range(nsets)]
-    from fft_gemm_ifft_gb300 import capi as _capi
-    if args.flags & _capi.FNO_PLAN_PACKED_WEIGHTS:
-        # weights are parameters: packed once per set, outside the timed region
-        ws = [conv.pack_weights(w) for w in ws]
-    ys = [torch.empty(case.y_shape, dtype=conv.torch_dtype, device=dev) for _ in range(nsets)]
+    return int(getattr(props, "L2_cache_size", 0)) or (126 << 20)
 
-    stream = torch.cuda.Stream(device=dev)
-    steps = max(1, args.steps)
+
+def graph_timing(torch, stream, step, steps, nsets, warmup, world, dev, sample_clocks=True):
+    """Time exactly `steps` calls of step(i) replayed from CUDA graphs on
+    `stream` (CUDA events on that stream, barriers and a synchronize on both
+    sides), after `warmup` eager calls and a 1.5 s pre-heat of the same graph
+    during which, and during the timed region, nvidia-smi samples the clocks.
+    Returns (ms for the whole timed region, max over ranks; clocks; layout)."""
+    steps = max(1, steps)
     per_graph = min(steps, nsets * max(1, 64 // nsets))
     reps, tail = divmod(steps, per_graph)
 
@@ -244,29 +258,28 @@ def bench_gpu(args, rank, world, local):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(count):
-                conv(xs[i % nsets], ws[i % nsets], ys[i % nsets], stream=stream)
+                step(i)
         return g
 
     with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, 3)):            # eager warm-up steps
-            conv(xs[i % nsets], ws[i % nsets], ys[i % nsets], stream=stream)
+        for i in range(max(warmup, 3)):
+            step(i)
         stream.synchronize()
-        assert conv.device_error(stream) == 0
         graph = capture(per_graph)
         graph_tail = capture(tail) if tail else None
         for _ in range(3):
             graph.replay()
         stream.synchronize()
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    # pre-heat of the same workload so the clock samples see a loaded GPU
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    if sample_clocks:
+        sampler.start()
     with torch.cuda.stream(stream):
         t_end = time.time() + 1.5
         while time.time() < t_end:
             graph.replay()
             stream.synchronize()
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -279,31 +292,204 @@ def bench_gpu(args, rank, world, local):
         end.record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
-    clocks = sampler.stop()
-    ms_max = max_over_ranks(start.elapsed_time(end), world, dev)
-    stream.synchronize()
-    assert conv.device_error(stream) == 0
+    clocks = sampler.stop() if sample_clocks else None
+    ms = max_over_ranks(start.elapsed_time(end), world, dev)
+    layout = f"CUDA-graph replay of {per_graph} forwards x {reps} (+{tail})"
+    return ms, clocks, layout
+
+
+def calibrated_steps(torch, stream, step, nsets, seconds):
+    """Forwards that fill about `seconds` of device time (one eager pass of
+    a few forwards measures the per-forward time first)."""
+    n = max(4, nsets)
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            step(i)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            step(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    per = max(e0.elapsed_time(e1) / n, 1e-3)          # ms
+    return int(min(200000, max(64, seconds * 1e3 / per)))
+
+
+class LayerSets:
+    """One plan, its rotating (x, w, y) sets on the device and the step."""
+
+    def __init__(self, torch, case, flags, dev):
+        from fft_gemm_ifft_gb300 import SpectralConv, capi, workloads
+        self.case, self.flags = case, flags
+        self.conv = SpectralConv(case.n, case.modes, case.batch, case.cin, case.cout,
+                                 case.dtype, flags)
+        self.x_np, self.w_np = workloads.make_x(case), workloads.make_w(case)
+        self.set_bytes = (self.x_np.nbytes + self.w_np.nbytes
+                          + math.prod(case.y_shape) * case.elem_bytes)
+        self.l2 = _l2_bytes(torch, dev)
+        self.nsets = max(2, math.ceil(2 * self.l2 / self.set_bytes))
+        self.xs = [workloads.to_torch_storage(self.x_np, case.dtype).to(dev)
+                   for _ in range(self.nsets)]
+        ws = [workloads.to_torch_storage(self.w_np, case.dtype).to(dev)
+              for _ in range(self.nsets)]
+        if flags & capi.FNO_PLAN_PACKED_WEIGHTS:
+            # weights are parameters: packed once per set, outside the timed region
+            ws = [self.conv.pack_weights(w) for w in ws]
+        self.ws = ws
+        self.ys = [torch.empty(case.y_shape, dtype=self.conv.torch_dtype, device=dev)
+                   for _ in range(self.nsets)]
+        self.stream = torch.cuda.Stream(device=dev)
+
+    def step(self, i):
+        k = i % self.nsets
+        self.conv(self.xs[k], self.ws[k], self.ys[k], stream=self.stream)
+
+    def l2_note(self):
+        return (f"rotating {self.nsets} distinct (x, w, y) sets = "
+                f"{self.nsets * self.set_bytes >> 20} MiB > 2 x L2 ({self.l2 >> 20} MiB)")
+
+    def sample_rel_l2(self, b=0):
+        """Parity check of one sample of set 0 (written by the timed replays)
+        against the float64 oracle; runs after the timing, outside it."""
+        import numpy as np
+
+        import oracle
+        from fft_gemm_ifft_gb300 import workloads
+        self.stream.synchronize()
+        got = self.ys[0][b:b + 1].float().cpu().numpy()
+        ref = oracle.spectral_conv(self.x_np[b:b + 1].astype(np.float64),
+                                   workloads.as_complex(self.w_np), self.case.modes)
+        return _rel_l2(got, ref)
+
+    def close(self):
+        self.conv.close()
+
+
+def roofline_obj(alg_bytes, ms_per_forward, kernel, kernels, traffic):
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / (ms_per_forward / 1e3) / 1e9
+    return {
+        "bound": "hbm",
+        "kernel": kernel,
+        "kernels_per_forward": kernels,
+        "achieved": round(achieved, 1),
+        "peak": peak,
+        "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s",
+        "unit": "GB/s",
+        "frac": round(achieved / peak, 4),
+        "algorithmic_bytes_per_launch": alg_bytes,
+        "traffic": traffic,
+    }
+
+
+def workload_text(case):
+    return (f"{case.name}: {case.ndim}-D spectral conv, B={case.batch}, Cin={case.cin}, "
+            f"Cout={case.cout}, N={'x'.join(map(str, case.n))}, "
+            f"modes={'x'.join(map(str, case.modes))} per block, {case.nblk} block(s), "
+            f"{case.dtype} storage")
+
+
+def layer_record(torch, case, flags, steps, warmup, world, dev, seconds=None):
+    """Time one spectral-conv workload; returns (record, LayerSets)."""
+    ls = LayerSets(torch, case, flags, dev)
+    if seconds is not None:
+        steps = calibrated_steps(torch, ls.stream, ls.step, ls.nsets, seconds)
+    ms, clocks, layout = graph_timing(torch, ls.stream, ls.step, steps, ls.nsets, warmup,
+                                      world, dev)
+    assert ls.conv.device_error(ls.stream) == 0
+    per = ms / steps
+    rec = {
+        "value": round(whole_job_rate(case.batch, world, steps, ms), 1),
+        "unit": "samples/s",
+        "ms_per_step": per,
+        "steps": steps,
+        "dtype": "f32" if case.dtype == "f32" else f"{case.dtype}-storage/f32-accumulate",
+        "workload": workload_text(case),
+        "plan_flags": flags,
+        "timing": layout + ", CUDA events on the launching stream",
+        "l2": ls.l2_note(),
+        "roofline": roofline_obj(case.algorithmic_bytes(), per, "fno_spectral_conv_forward",
+                                 ls.conv.kernel_count,
+                                 recorded_traffic(case.name) if flags == DEFAULT_FLAGS.get(
+                                     case.name, 0) else None),
+        "clocks": clocks,
+    }
+    return rec, ls
+
+
+def fno_record(torch, steps, warmup, world, dev, seconds=None, check=True):
+    """The FNO stack (fno_forward), replayed from a CUDA graph."""
+    import numpy as np
+
+    from fft_gemm_ifft_gb300 import FnoModel, workloads
+    case = workloads.FNO_CASE
+    m = FnoModel(case.batch, case.h, case.w, case.modes, case.cin_lift, case.width,
+                 case.nlayers, case.hidden, case.cout)
+    fx = workloads.make_fno_inputs(case)
+    fp = workloads.make_fno_params(case)
+    nsets = 2
+    xs = [torch.from_numpy(fx).to(dev) for _ in range(nsets)]
+    p = {k: torch.from_numpy(v).to(dev) for k, v in fp.items()}
+    ys = [torch.empty(m.y_shape, dtype=torch.float32, device=dev) for _ in range(nsets)]
+    stream = torch.cuda.Stream(device=dev)
+    step = lambda i: m(xs[i % nsets], p, ys[i % nsets], stream=stream)
+    if seconds is not None:
+        steps = calibrated_steps(torch, stream, step, nsets, seconds)
+    ms, clocks, layout = graph_timing(torch, stream, step, steps, nsets, warmup, world, dev)
+    assert m.device_error(stream) == 0
+    per = ms / steps
+    rec = {
+        "value": round(whole_job_rate(case.batch, world, steps, ms), 1),
+        "unit": "samples/s",
+        "ms_per_step": per,
+        "steps": steps,
+        "dtype": "f32",
+        "workload": (f"{case.name}: 2-D FNO forward, B={case.batch}, lift {case.cin_lift}->"
+                     f"{case.width}, {case.nlayers} layers (spectral conv modes "
+                     f"{case.modes[0]}x{case.modes[1]} x 2 blocks + 1x1 linear, GELU), head "
+                     f"{case.width}->{case.hidden}->{case.cout}, {case.h}x{case.w}"),
+        "timing": layout + " (fno_forward captured whole), CUDA events on the launching stream",
+        "l2": "each forward streams its 64-channel activations (64 MiB each) through HBM",
+        "roofline": roofline_obj(case.algorithmic_bytes(), per, "fno_forward", m.kernel_count,
+                                 None),
+        "clocks": clocks,
+    }
+    if check:
+        import oracle
+        stream.synchronize()
+        got = ys[0][0:1].cpu().numpy()
+        ref = oracle.fno_forward(fx[0:1], workloads.fno_params_for_oracle(fp), case.modes)
+        rec["rel_l2_sample"] = _rel_l2(got, ref)
+        rec["rel_l2_tol"] = 1e-5
+    m.close()
+    return rec
+
+
+def bench_gpu(args, rank, world, local):
+    import torch
+
+    from fft_gemm_ifft_gb300 import workloads
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    case = workloads.CASES[args.workload]
+    flags = DEFAULT_FLAGS.get(case.name, 0) if args.flags < 0 else args.flags
+    rec, ls = layer_record(torch, case, flags, args.steps, args.warmup, world, dev)
+    conv, stream = ls.conv, ls.stream
+    steps = max(1, args.steps)
 
     # L2-resident ("hot") figure for workloads whose set fits in L2: the same
-    # number of forwards on one (x, w, y) set, reported beside the rotated value
+    # forwards on one (x, w, y) set, reported beside the rotated value
     hot_ms = None
-    if set_bytes < l2:
-        with torch.cuda.stream(stream):
-            g_hot = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_hot, stream=stream):
-                for _ in range(per_graph):
-                    conv(xs[0], ws[0], ys[0], stream=stream)
-            for _ in range(3):
-                g_hot.replay()
-            h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            h0.record(stream)
-            for _ in range(reps):
-                g_hot.replay()
-            h1.record(stream)
-        torch.cuda.synchronize(dev)
-        hot_ms = max_over_ranks(h0.elapsed_time(h1), world, dev) / (reps * per_graph)
-        assert conv.device_error(stream) == 0
+    if ls.set_bytes < ls.l2:
+        hot = lambda i: conv(ls.xs[0], ls.ws[0], ls.ys[0], stream=stream)
+        ms_hot, _, _ = graph_timing(torch, stream, hot, steps, ls.nsets, 3, world, dev,
+                                    sample_clocks=False)
+        hot_ms = ms_hot / steps
 
     # end to end through the public API: every step copies its input from pinned
     # host memory, runs the layer and copies its output back to pinned host
@@ -311,57 +497,37 @@ def bench_gpu(args, rank, world, local):
     # streams (copy in, layer, copy out), as a serving loop would run them: the
     # input of step i+1 and the output of step i-1 move while step i computes.
     e2e_steps = max(3, args.e2e_steps)
-    e2e_ms = e2e_pipelined(torch, conv, case, x_np, ws, stream, e2e_steps, world, dev, dist)
-
-    value = whole_job_rate(case.batch, world, steps, ms_max)
-    kernel_ms = ms_max / steps          # back-to-back graph replay: per-forward duration
-    peak, peak_kind = measured_peaks()
-    alg_bytes = case.algorithmic_bytes()
-    achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
+    e2e_ms = e2e_pipelined(torch, conv, case, ls.x_np, ls.ws, stream, e2e_steps, world, dev)
+    parity = None
+    if rank == 0 and not args.no_check:
+        parity = {"rel_l2_sample": ls.sample_rel_l2(0), "rel_l2_tol": REL_TOL[case.dtype],
+                  "sample": "batch element 0 of set 0 against the float64 oracle"}
     result = {
         "metric": METRIC,
-        "value": round(value, 1),
+        "value": rec["value"],
         "unit": "samples/s",
         "n_gpus": world,
         "steps": steps,
         "warmup": max(args.warmup, 3),
-        "ms_per_step": ms_max / steps,
+        "ms_per_step": rec["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32" if case.dtype == "f32" else f"{case.dtype}-storage/f32-accumulate",
+        "dtype": rec["dtype"],
         "data": "synthetic (seeded N(0,1) fields, U[0,1)/(Cin*Cout) complex weights)",
         "config": {
-            "workload": f"{case.name}: {case.ndim}-D spectral conv, B={case.batch}, "
-                        f"Cin={case.cin}, Cout={case.cout}, N={'x'.join(map(str, case.n))}, "
-                        f"modes={'x'.join(map(str, case.modes))} per block, "
-                        f"{case.nblk} block(s)",
+            "workload": rec["workload"],
             "global_batch": world * case.batch,
             "parallelism": f"replicas x{world}",
-            "l2": f"rotating {nsets} distinct (x, w, y) sets = {nsets * set_bytes >> 20} MiB "
-                  f"> 2 x L2 ({l2 >> 20} MiB)",
-            "timing": f"CUDA-graph replay of {per_graph} forwards x {reps} (+{tail}), "
-                      "CUDA events on the launching stream",
-            "plan_flags": args.flags,
-            "weights": ("packed mode-major once per set, outside the timed region"
-                        if args.flags & 128 else "as given (nblk, Cin, Cout, modes)"),
+            "l2": rec["l2"],
+            "timing": rec["timing"],
+            "plan_flags": flags,
+            "weights": ("packed once per set into the mixing kernel's operand layout, "
+                        "outside the timed region (weights are parameters)"
+                        if flags & 128 else "as given (nblk, Cin, Cout, modes)"),
             "hot_l2_ms_per_step": hot_ms,
         },
-        "roofline": {
-            "bound": "hbm",
-            "kernel": "fno_spectral_conv_forward" if conv.kernel_count > 1
-                      else "fused spectral-conv kernel",
-            "kernels_per_forward": conv.kernel_count,
-            "achieved": round(achieved, 1),
-            "peak": peak,
-            "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                         else "fallback 6.8 TB/s",
-            "unit": "GB/s",
-            "frac": round(achieved / peak, 4),
-            "algorithmic_bytes_per_launch": alg_bytes,
-            # the committed capture covers the default kernels only
-            "traffic": recorded_traffic(case.name) if args.flags == 0 else None,
-        },
+        "roofline": rec["roofline"],
         "e2e": {
             "value": round(whole_job_rate(case.batch, world, e2e_steps, e2e_ms), 1),
             "unit": "samples/s",
@@ -370,8 +536,39 @@ def bench_gpu(args, rank, world, local):
             "d2h_bytes_per_step": int(math.prod(case.y_shape) * case.elem_bytes),
         },
         "gpu_launches": steps * conv.kernel_count,
-        "clocks": clocks,
+        "clocks": rec["clocks"],
     }
+    if parity is not None:
+        result["parity"] = parity
+    x_np, w_np = ls.x_np, ls.w_np
+    ls.close()
+    del ls
+    torch.cuda.empty_cache()
+
+    if not args.no_per_config:
+        per = {}
+        for name in PER_CONFIG:
+            if name == case.name:
+                r = dict(rec)
+                if parity is not None:
+                    r.update(parity)
+                per[name] = r
+                continue
+            if name == workloads.FNO_CASE.name:
+                per[name] = fno_record(torch, 0, 3, world, dev, args.per_config_seconds,
+                                       check=rank == 0 and not args.no_check)
+            else:
+                c = workloads.CASES[name]
+                r, lsc = layer_record(torch, c, DEFAULT_FLAGS.get(name, 0), 0, 3, world, dev,
+                                      args.per_config_seconds)
+                if rank == 0 and not args.no_check:
+                    r["rel_l2_sample"] = lsc.sample_rel_l2(0)
+                    r["rel_l2_tol"] = REL_TOL[c.dtype]
+                lsc.close()
+                del lsc
+                torch.cuda.empty_cache()
+                per[name] = r
+        result["per_config"] = per
     return result, case, x_np, w_np
 
 

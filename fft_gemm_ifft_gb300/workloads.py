@@ -111,6 +111,28 @@ class FnoCase:
         return SpectralConvCase(self.name + "/spectral", (self.h, self.w), self.modes,
                                 self.batch, self.width, self.width, "f32", self.index)
 
+    def algorithmic_bytes(self) -> int:
+        """Float32 bytes of the least traffic a forward of the stack can have
+        with two passes per layer: each layer reads its input twice (for the
+        forward transform, then for the pointwise term beside the inverse) and
+        writes its output once; the lift is recomputed from the 3-channel x
+        where the first layer reads, the head is taken where the last layer
+        writes (so only the 1-channel output is stored); every parameter is
+        read once."""
+        pix = self.batch * self.h * self.w
+        act = pix * self.width * 4
+        total = 0
+        for l in range(self.nlayers):
+            reads = pix * self.cin_lift * 4 if l == 0 else act
+            writes = pix * self.cout * 4 if l == self.nlayers - 1 else act
+            total += 2 * reads + writes
+        nblk = 2
+        spec = self.nlayers * nblk * self.width * self.width * math.prod(self.modes) * 8
+        lin = (self.width * (self.cin_lift + 1)
+               + self.nlayers * self.width * (self.width + 1)
+               + self.hidden * (self.width + 1) + self.cout * (self.hidden + 1)) * 4
+        return total + spec + lin
+
 
 CASES: Dict[str, SpectralConvCase] = {
     "1d_f32": SpectralConvCase("1d_f32", (256,), (16,), 4, 16, 16, "f32", 0),

@@ -101,3 +101,47 @@ def test_stack_16bit_storage(dt, shape):
     m.close()
     ref = oracle.fno_forward(x.astype(np.float64), workloads.fno_params_for_oracle(p), modes)
     assert_close(y.float().cpu().numpy(), ref, dt, f"16-bit FNO stack {shape}")
+
+
+@pytest.mark.parametrize("shape", [
+    # batch, width, nlayers, h, w, modes, hidden, cout
+    (2, 8, 2, 32, 32, (4, 4), 16, 2),             # register-tiled linears
+    (2, 64, 2, 128, 128, (16, 16), 128, 1),       # three-kernel 128^2 layers, tensor-core linears
+], ids=["small", "layer_128"])
+def test_fno_forward_graph_capture_replays(shape):
+    # One fno_forward captured in a CUDA graph, replayed twice on new inputs
+    # (and new parameters) copied into the captured buffers; each replay is
+    # compared with the oracle.  The call allocates nothing and syncs nothing,
+    # so the graph holds the whole stack.
+    b, width, nl, h, w, modes, hidden, cout = shape
+    case = workloads.FnoCase("graph", batch=b, width=width, nlayers=nl, h=h, w=w, modes=modes,
+                             hidden=hidden, cout=cout)
+    m = FnoModel(b, h, w, modes, case.cin_lift, width, nl, hidden, cout)
+    x0 = workloads.make_fno_inputs(case)
+    p0 = workloads.make_fno_params(case)
+    xd = to_dev(x0)
+    pd = {k: to_dev(v) for k, v in p0.items()}
+    yd = torch.empty(m.y_shape, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        m(xd, pd, yd, stream=s)                    # warm-up outside the capture
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            m(xd, pd, yd, stream=s)
+    r = np.random.default_rng(77)
+    for rep in range(2):
+        x = x0.copy()
+        x[:, 0] = r.standard_normal(x[:, 0].shape).astype(np.float32)
+        p = {k: (v * np.float32(1.0 + 0.25 * (rep + 1))).astype(np.float32)
+             if k in ("spec_w", "pw_w") else v for k, v in p0.items()}
+        xd.copy_(torch.from_numpy(x))
+        for k in ("spec_w", "pw_w"):
+            pd[k].copy_(torch.from_numpy(p[k]))
+        yd.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert m.device_error() == 0
+        ref = oracle.fno_forward(x, workloads.fno_params_for_oracle(p), modes)
+        assert_close(yd.cpu().numpy(), ref, "f32", f"graph replay {rep} {shape}")
+    m.close()
