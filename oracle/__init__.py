@@ -16,6 +16,8 @@ TurboFNO article (gsyq.cn/news/457482):
 * ``mix``            -- §2.2, per-mode complex contraction over input channels;
 * ``inverse_modes``  -- §2.3 / §3.3, zero-padded inverse real FFT;
 * ``spectral_conv``  -- the three in order;
+* ``spectral_conv_padded`` -- §2.3 / §3.3, the layer on a zero-padded domain
+  with the output cropped back to the input's extents;
 * ``spectral_conv_backward`` -- dL/dx and dL/dw of the layer for a real loss,
   the derivatives of the three steps above (the pages print no backward pass);
 * ``adjoint_modes``  -- the adjoint of ``forward_modes`` (used by the above);
@@ -194,6 +196,23 @@ def spectral_conv(x: np.ndarray, w: np.ndarray, modes) -> np.ndarray:
                                             m.ctypes.data_as(_i32p), B, cin, cout,
                                             _d(x), _d(ws), _d(y)), "spectral_conv")
     return y
+
+
+def spectral_conv_padded(x: np.ndarray, w: np.ndarray, modes, pad) -> np.ndarray:
+    """The layer on a non-periodic domain (TurboFNO §2.3, §3.3): every spatial
+    axis a of x (B, Cin, N...) is extended with pad[a] zeros after its last
+    sample, the layer runs at the extents L = N + pad (modes counted on L),
+    and the output is cropped back to its first N samples per axis."""
+    d = len(modes)
+    x = _f64(x)
+    n = x.shape[-d:]
+    pad = tuple(int(p) for p in pad)
+    if len(pad) != d or min(pad) < 0:
+        raise ValueError("pad needs one non-negative entry per spatial axis")
+    xp = np.zeros(x.shape[:2] + tuple(na + pa for na, pa in zip(n, pad)), dtype=np.float64)
+    xp[(slice(None), slice(None)) + tuple(slice(0, na) for na in n)] = x
+    yp = spectral_conv(xp, w, modes)
+    return np.ascontiguousarray(yp[(slice(None), slice(None)) + tuple(slice(0, na) for na in n)])
 
 
 def adjoint_modes(dX: np.ndarray, n, modes) -> np.ndarray:

@@ -560,3 +560,101 @@ def test_workload_generators_deterministic():
     fx = workloads.make_fno_inputs(batch=2)
     assert fx.shape == (2, 3, 128, 128)
     assert fx[0, 1, 0, 0] == 0.0 and fx[0, 1, -1, 0] == 1.0 and fx[0, 2, 0, -1] == 1.0
+
+
+# ---------------------------------------------------------------------------
+# Zero padding for non-periodic domains and output cropping (TurboFNO §2.3,
+# §3.3): x extended with zeros to L = N + pad per axis, the layer at L, the
+# output cropped to N.
+# ---------------------------------------------------------------------------
+
+def _numpy_padded_layer(x, w, modes, pad):
+    """pad -> rfftn -> per-block mixing -> irfftn -> crop, written with numpy."""
+    d = len(modes)
+    n = x.shape[-d:]
+    L = tuple(a + b for a, b in zip(n, pad))
+    xp = np.zeros(x.shape[:2] + L)
+    xp[(slice(None), slice(None)) + tuple(slice(0, a) for a in n)] = x
+    X = np.fft.rfftn(xp, axes=tuple(range(2, 2 + d)))
+    half = np.zeros(x.shape[:1] + (w.shape[2],) + X.shape[2:], dtype=complex)
+    for blk in range(w.shape[0]):
+        sl = []
+        for a in range(d - 1):
+            hi = (blk >> a) & 1
+            sl.append(slice(L[a] - modes[a], L[a]) if hi else slice(0, modes[a]))
+        sl.append(slice(0, modes[-1]))
+        idx = (slice(None), slice(None)) + tuple(sl)
+        half[idx] = np.einsum("bi...,io...->bo...", X[idx], w[blk])
+    y = np.fft.irfftn(half, s=L, axes=tuple(range(2, 2 + d)))
+    return y[(slice(None), slice(None)) + tuple(slice(0, a) for a in n)]
+
+
+PADDED_SHAPES = [
+    ((12,), (4,), (4,)),              # L = 16, power of two
+    ((10,), (6,), (5,)),              # L = 15: odd, the DFT fallback, no Nyquist bin
+    ((6,), (2,), (5,)),               # L = 8 with the Nyquist bin kept
+    ((6, 10), (2, 6), (2, 4)),        # 2-D, L = (8, 16)
+    ((5, 7), (3, 1), (2, 3)),         # 2-D, L = (8, 8)
+    ((3, 4, 6), (1, 4, 2), (2, 2, 3)),  # 3-D, L = (4, 8, 8)
+]
+
+
+@pytest.mark.parametrize("n,pad,modes", PADDED_SHAPES)
+def test_padded_layer_against_numpy(oracle_mod, n, pad, modes):
+    r = rng(600 + sum(n) + sum(pad))
+    nblk = 2 ** (len(n) - 1)
+    x = r.standard_normal((2, 3) + n)
+    w = (r.standard_normal((nblk, 3, 4) + modes) + 1j * r.standard_normal((nblk, 3, 4) + modes))
+    got = oracle_mod.spectral_conv_padded(x, w, modes, pad)
+    assert got.shape == (2, 4) + n
+    want = _numpy_padded_layer(x, w, modes, pad)
+    assert np.max(np.abs(got - want)) < 1e-12 * max(1.0, np.max(np.abs(want)))
+
+
+def test_padded_layer_brute_force_1d(oracle_mod):
+    # direct sums from the definition: X[k] = sum_{n<N} x[n] e^{-2 pi i k n / L}
+    # (the appended zeros add nothing), y[n] = (1/L) sum_k c(k) Re(Y[k] e^{+2 pi i k n / L})
+    # for n < N only
+    r = rng(610)
+    N, P, m = 7, 5, 4
+    L = N + P
+    x = r.standard_normal((1, 2, N))
+    w = r.standard_normal((1, 2, 3, m)) + 1j * r.standard_normal((1, 2, 3, m))
+    got = oracle_mod.spectral_conv_padded(x, w, (m,), (P,))
+    want = np.zeros((1, 3, N))
+    for o in range(3):
+        for t in range(N):
+            acc = 0.0
+            for k in range(m):
+                Xk = [sum(x[0, i, s] * np.exp(-2j * np.pi * k * s / L) for s in range(N))
+                      for i in range(2)]
+                Yk = sum(Xk[i] * w[0, i, o, k] for i in range(2))
+                c = 1.0 if (k == 0 or 2 * k == L) else 2.0
+                acc += c * (Yk * np.exp(2j * np.pi * k * t / L)).real
+            want[0, o, t] = acc / L
+    assert np.max(np.abs(got - want)) < 1e-12
+
+
+def test_padded_identity_all_modes_reproduces_input(oracle_mod):
+    # identity weights with every mode of the padded extents kept: the layer is
+    # the identity on the padded field, so the cropped output is x itself
+    r = rng(611)
+    n, pad = (6, 10), (2, 6)
+    L = (8, 16)
+    modes = (L[0] // 2, L[1] // 2 + 1)
+    x = r.standard_normal((2, 3) + n)
+    eye = np.eye(3)[None, :, :, None, None] * np.ones((2, 1, 1) + modes)
+    got = oracle_mod.spectral_conv_padded(x, eye.astype(complex), modes, pad)
+    assert np.max(np.abs(got - x)) < 1e-12
+
+
+def test_padded_zero_pad_is_the_periodic_layer(oracle_mod):
+    r = rng(612)
+    x = r.standard_normal((2, 3, 8, 16))
+    w = r.standard_normal((2, 3, 2, 2, 3)) + 1j * r.standard_normal((2, 3, 2, 2, 3))
+    a = oracle_mod.spectral_conv_padded(x, w, (2, 3), (0, 0))
+    b = oracle_mod.spectral_conv(x, w, (2, 3))
+    assert np.max(np.abs(a - b)) == 0.0
+    # and padding changes the result (the domain is no longer periodic)
+    c = oracle_mod.spectral_conv_padded(x, w, (2, 3), (8, 0))
+    assert np.max(np.abs(c - b)) > 1e-3
