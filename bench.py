@@ -46,8 +46,10 @@ FALLBACK_HBM_GBS = 6800.0
 HEADLINE = "2d_f16"
 # every workload, in the order of the per-config record
 PER_CONFIG = ("1d_f32", "2d_f32", "2d_f16", "3d_f32", "fno2d_f32")
-# plan flags each workload runs with by default (FNO_PLAN_* bits)
-DEFAULT_FLAGS = {}
+# plan flags each workload runs with by default (FNO_PLAN_* bits): the 16-bit
+# 256x256 layers take their weights packed once into the tensor-core mixing's
+# operand images (FNO_PLAN_PACKED_WEIGHTS; weights are parameters)
+DEFAULT_FLAGS = {"2d_f16": 128, "2d_bf16": 128}
 # relative L2 bars against the float64 oracle
 REL_TOL = {"f32": 1e-5, "f16": 1e-2, "bf16": 1e-2}
 

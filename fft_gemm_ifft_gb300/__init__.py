@@ -49,19 +49,27 @@ class SpectralConv:
     """One spectral-convolution plan and its workspace on the current device.
 
     ``w`` is passed as the real view of the interleaved complex weights,
-    shape (nblk, cin, cout, m..., 2), in the storage dtype.
+    shape (nblk, cin, cout, m..., 2), in the storage dtype.  ``pad`` (one
+    entry per axis) makes the layer non-periodic: x is read as if followed by
+    that many zeros per axis, the transform runs over n + pad points and y
+    keeps the first n (``fno_spectral_conv_plan_padded``).
     """
 
-    def __init__(self, n, modes, batch, cin, cout, dtype="f32", flags=0):
+    def __init__(self, n, modes, batch, cin, cout, dtype="f32", flags=0, pad=None):
         import torch
         self.n, self.modes = tuple(int(v) for v in n), tuple(int(v) for v in modes)
         self.batch, self.cin, self.cout = int(batch), int(cin), int(cout)
         self.dtype = dtype
+        self.pad = None if pad is None else tuple(int(v) for v in pad)
         self.torch_dtype = {"f32": torch.float32, "f16": torch.float16,
                             "bf16": torch.bfloat16}[dtype]
         code = capi.DTYPE_CODES[dtype]
-        st, self.handle = capi.fno_spectral_conv_plan(len(self.n), self.n, self.modes, batch,
-                                                      cin, cout, code, flags)
+        if self.pad is None:
+            st, self.handle = capi.fno_spectral_conv_plan(len(self.n), self.n, self.modes,
+                                                          batch, cin, cout, code, flags)
+        else:
+            st, self.handle = capi.fno_spectral_conv_plan_padded(
+                len(self.n), self.n, self.pad, self.modes, batch, cin, cout, code, flags)
         check(st, "fno_spectral_conv_plan")
         st, self.workspace_bytes = capi.fno_spectral_conv_workspace_size(self.handle)
         check(st)

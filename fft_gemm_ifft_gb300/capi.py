@@ -31,7 +31,6 @@ DTYPE_CODES = {"f32": FNO_F32, "f16": FNO_F16, "bf16": FNO_BF16}
 FNO_PLAN_DEFAULT = 0
 FNO_PLAN_UNFUSED = 1
 FNO_PLAN_TRACE = 2
-FNO_PLAN_TENSOR_CORES = 4
 FNO_PLAN_PERSISTENT = 8
 FNO_PLAN_BACKWARD = 16
 FNO_PLAN_SIMT_MIX = 32
@@ -42,6 +41,7 @@ FNO_PLAN_PACKED_WEIGHTS = 128
 EXPORTS = (
     "fno_status_string", "fno_version",
     "fno_spectral_conv_query", "fno_spectral_conv_plan",
+    "fno_spectral_conv_query_padded", "fno_spectral_conv_plan_padded",
     "fno_spectral_conv_workspace_size", "fno_spectral_conv_kernel_count",
     "fno_spectral_conv_forward", "fno_plan_get_device_error", "fno_plan_destroy",
     "fno_spectral_conv_forward_static", "fno_plan_get_trace", "fno_spectral_conv_backward",
@@ -105,6 +105,12 @@ def lib() -> ctypes.CDLL:
             L.fno_spectral_conv_plan.argtypes = [ctypes.POINTER(_vp), ctypes.c_int, pi64, pi32,
                                                  ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                                  _st, ctypes.c_uint32]
+            L.fno_spectral_conv_query_padded.argtypes = [
+                ctypes.c_int, pi64, pi64, pi32, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                _st, ctypes.c_uint32, psz, psz]
+            L.fno_spectral_conv_plan_padded.argtypes = [
+                ctypes.POINTER(_vp), ctypes.c_int, pi64, pi64, pi32, ctypes.c_int64,
+                ctypes.c_int32, ctypes.c_int32, _st, ctypes.c_uint32]
             L.fno_spectral_conv_workspace_size.argtypes = [_vp, psz]
             L.fno_spectral_conv_kernel_count.argtypes = [_vp, ctypes.POINTER(ctypes.c_int)]
             L.fno_spectral_conv_forward.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp]
@@ -157,6 +163,24 @@ def fno_spectral_conv_plan(ndim, n, modes, batch, cin, cout, dtype, flags=0):
     st = lib().fno_spectral_conv_plan(ctypes.byref(h), int(ndim), _arr(ctypes.c_int64, n),
                                       _arr(ctypes.c_int32, modes), int(batch), int(cin),
                                       int(cout), int(dtype), int(flags))
+    return st, h.value
+
+
+def fno_spectral_conv_query_padded(ndim, n, pad, modes, batch, cin, cout, dtype, flags=0):
+    ws, wb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    st = lib().fno_spectral_conv_query_padded(
+        int(ndim), _arr(ctypes.c_int64, n), None if pad is None else _arr(ctypes.c_int64, pad),
+        _arr(ctypes.c_int32, modes), int(batch), int(cin), int(cout), int(dtype), int(flags),
+        ctypes.byref(ws), ctypes.byref(wb))
+    return st, ws.value, wb.value
+
+
+def fno_spectral_conv_plan_padded(ndim, n, pad, modes, batch, cin, cout, dtype, flags=0):
+    h = _vp(0)
+    st = lib().fno_spectral_conv_plan_padded(
+        ctypes.byref(h), int(ndim), _arr(ctypes.c_int64, n),
+        None if pad is None else _arr(ctypes.c_int64, pad), _arr(ctypes.c_int32, modes),
+        int(batch), int(cin), int(cout), int(dtype), int(flags))
     return st, h.value
 
 

@@ -51,28 +51,38 @@ bool inject(const char *site) {
 }
 
 
-fno_status_t make_geom(Geom *g, int ndim, const int64_t *n, const int32_t *modes) {
+// pad == NULL: a periodic layer; else the transform of axis a runs over
+// n[a] + pad[a] points of which the last pad[a] are zeros (and are not stored).
+fno_status_t make_geom(Geom *g, int ndim, const int64_t *n, const int32_t *modes,
+                       const int64_t *pad = nullptr) {
     if (ndim < 1 || ndim > FNO_MAX_NDIM || !n || !modes) return FNO_ERR_INVALID_ARG;
     std::memset(g, 0, sizeof(*g));
     g->d = ndim;
-    g->nkept = g->npix = g->nblk = g->mblk = 1;
+    g->nkept = g->npix = g->ntr = g->nblk = g->mblk = 1;
     for (int a = 0; a < ndim; ++a) {
-        if (n[a] < 2) return FNO_ERR_INVALID_ARG;
-        if (n[a] > kMaxN) return FNO_ERR_UNSUPPORTED;
+        const int64_t p = pad ? pad[a] : 0;
+        if (p < 0 || n[a] < 1) return FNO_ERR_INVALID_ARG;
+        if (n[a] > kMaxN || p > kMaxN) return FNO_ERR_UNSUPPORTED;
+        g->ext[a] = n[a];
+        g->padded |= p > 0;
+        const int64_t len = n[a] + p;               // transform length
+        if (len < 2) return FNO_ERR_INVALID_ARG;
+        if (len > kMaxN) return FNO_ERR_UNSUPPORTED;
         const int64_t m = modes[a];
         if (m < 1) return FNO_ERR_INVALID_ARG;
         if (a < ndim - 1) {
-            if (2 * m > n[a]) return FNO_ERR_INVALID_ARG;   // corner blocks may not overlap
+            if (2 * m > len) return FNO_ERR_INVALID_ARG;    // corner blocks may not overlap
             g->kdim[a] = 2 * m;
             g->nblk *= 2;
         } else {
-            if (m > n[a] / 2 + 1) return FNO_ERR_INVALID_ARG;
+            if (m > len / 2 + 1) return FNO_ERR_INVALID_ARG;
             g->kdim[a] = m;
         }
-        g->n[a] = n[a];
+        g->n[a] = len;
         g->m[a] = (int32_t)m;
         g->nkept *= g->kdim[a];
         g->npix *= n[a];
+        g->ntr *= len;
         g->mblk *= m;
     }
     return FNO_OK;
@@ -99,12 +109,18 @@ struct Sizes {
 
 fno_status_t describe(int ndim, const int64_t *n, const int32_t *modes, int64_t batch,
                       int32_t cin, int32_t cout, fno_dtype_t dtype, uint32_t flags,
-                      Geom *g, Sizes *sz) {
-    fno_status_t st = make_geom(g, ndim, n, modes);
+                      Geom *g, Sizes *sz, const int64_t *pad = nullptr) {
+    fno_status_t st = make_geom(g, ndim, n, modes, pad);
     if (st != FNO_OK) return st;
+    // a padded layer runs on the separate per-axis kernels (the fused kernels
+    // are specialised to periodic power-of-two extents); it has no backward
+    if (g->padded) {
+        if (flags & FNO_PLAN_BACKWARD) return FNO_ERR_UNSUPPORTED;
+        flags |= FNO_PLAN_UNFUSED;
+    }
     if (batch < 1 || cin < 1 || cout < 1) return FNO_ERR_INVALID_ARG;
     if (dtype != FNO_F32 && dtype != FNO_F16 && dtype != FNO_BF16) return FNO_ERR_INVALID_ARG;
-    if (flags & ~(FNO_PLAN_UNFUSED | FNO_PLAN_TRACE | FNO_PLAN_TENSOR_CORES |
+    if (flags & ~(FNO_PLAN_UNFUSED | FNO_PLAN_TRACE |
                   FNO_PLAN_PERSISTENT | FNO_PLAN_BACKWARD | FNO_PLAN_SIMT_MIX |
                   FNO_PLAN_SIMT_TRANSFORM | FNO_PLAN_PACKED_WEIGHTS))
         return FNO_ERR_INVALID_ARG;
@@ -163,27 +179,43 @@ const char *fno_status_string(fno_status_t s) {
 
 int fno_version(void) { return kVersion; }
 
-fno_status_t fno_spectral_conv_query(int ndim, const int64_t *n, const int32_t *modes,
-                                     int64_t batch, int32_t cin, int32_t cout,
-                                     fno_dtype_t dtype, uint32_t flags,
-                                     size_t *workspace_bytes, size_t *weight_bytes) {
+fno_status_t fno_spectral_conv_query_padded(int ndim, const int64_t *n, const int64_t *pad,
+                                            const int32_t *modes, int64_t batch, int32_t cin,
+                                            int32_t cout, fno_dtype_t dtype, uint32_t flags,
+                                            size_t *workspace_bytes, size_t *weight_bytes) {
     Geom g;
     Sizes sz;
-    fno_status_t st = describe(ndim, n, modes, batch, cin, cout, dtype, flags, &g, &sz);
+    fno_status_t st = describe(ndim, n, modes, batch, cin, cout, dtype, flags, &g, &sz, pad);
     if (st != FNO_OK) return st;
     if (workspace_bytes) *workspace_bytes = sz.workspace;
     if (weight_bytes) *weight_bytes = sz.weight;
     return FNO_OK;
 }
 
+fno_status_t fno_spectral_conv_query(int ndim, const int64_t *n, const int32_t *modes,
+                                     int64_t batch, int32_t cin, int32_t cout,
+                                     fno_dtype_t dtype, uint32_t flags,
+                                     size_t *workspace_bytes, size_t *weight_bytes) {
+    return fno_spectral_conv_query_padded(ndim, n, nullptr, modes, batch, cin, cout, dtype,
+                                          flags, workspace_bytes, weight_bytes);
+}
+
 fno_status_t fno_spectral_conv_plan(fno_plan_t *out, int ndim, const int64_t *n,
                                     const int32_t *modes, int64_t batch, int32_t cin,
                                     int32_t cout, fno_dtype_t dtype, uint32_t flags) {
+    return fno_spectral_conv_plan_padded(out, ndim, n, nullptr, modes, batch, cin, cout, dtype,
+                                         flags);
+}
+
+fno_status_t fno_spectral_conv_plan_padded(fno_plan_t *out, int ndim, const int64_t *n,
+                                           const int64_t *pad, const int32_t *modes,
+                                           int64_t batch, int32_t cin, int32_t cout,
+                                           fno_dtype_t dtype, uint32_t flags) {
     if (!out) return FNO_ERR_INVALID_ARG;
     *out = nullptr;
     Geom g;
     Sizes sz;
-    fno_status_t st = describe(ndim, n, modes, batch, cin, cout, dtype, flags, &g, &sz);
+    fno_status_t st = describe(ndim, n, modes, batch, cin, cout, dtype, flags, &g, &sz, pad);
     if (st != FNO_OK) return st;
     if (inject("plan_alloc")) return FNO_ERR_OUT_OF_MEMORY;
 

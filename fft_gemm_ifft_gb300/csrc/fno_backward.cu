@@ -170,7 +170,7 @@ cudaError_t launch_grad_w(const Plan &p, const float2 *X, const float2 *G, int p
     mg.mblk = p.g.mblk;
     mg.nlast = p.g.n[p.g.d - 1];
     const int64_t total = p.g.nblk * p.cin * ((p.cout + kOB - 1) / kOB) * p.g.mblk;
-    const float inv_npix = (float)(1.0 / (double)p.g.npix);
+    const float inv_npix = (float)(1.0 / (double)p.g.ntr);
     with_storage(p.dtype, [&](auto t) {
         using T = decltype(t);
         k_grad_w<T><<<grid_for(total, p.num_sms), kThreads, 0, s>>>(

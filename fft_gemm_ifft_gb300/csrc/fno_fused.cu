@@ -303,42 +303,51 @@ struct Geo {
     static_assert(kSmem + 1024 <= 232448, "image tile, table and Z planes fit one CTA");
 };
 
+// The kernel is warp-specialised.  Warp 8 (one elected thread) is the
+// producer: it loads each image as two 128-row M tiles (64 KiB each, four TMA
+// boxes), issues a tile's row-DFT MMAs as soon as the tile has landed into one
+// of two tensor-memory accumulators, and requests the next image's tile into
+// the same buffer as soon as those MMAs have read it.  Warps 0-7 (the
+// consumers) take an accumulator once both tiles' MMAs are done, copy Z out of
+// tensor memory, release the accumulator, and run the column DFT.  So the next
+// image's loads and row DFT proceed under this image's column work.
+constexpr int kNTA = NT + 32;            // consumers + producer warp
+
+// named barrier of the 256 consumer threads (barrier 0 is the whole CTA's)
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"r"(NT) : "memory");
+}
+
 template <typename T>
-__global__ void __launch_bounds__(NT, Shape<T>::kMinBlocks)
+__global__ void __launch_bounds__(kNTA, Shape<T>::kMinBlocks)
 k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *tables, int nimg) {
     using Gm = Geo<T>;
     using namespace tcu;
     extern __shared__ __align__(1024) char smem_raw[];
     char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
-    __shared__ __align__(8) uint64_t bar_x, bar_t, bar_mma;
+    // full[t]: tile t landed; empty[t]: its MMAs are done (the buffer may be
+    // refilled); acc[b]: accumulator b holds an image's Z; free_[b]: the
+    // consumers have copied accumulator b out (256 arrivals)
+    __shared__ __align__(8) uint64_t bar_t, full[2], empty[2], acc[2], free_[2];
     __shared__ uint32_t s_tmem;
+    static_assert(Gm::MT == 2, "two M tiles");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // the image: MT x KC boxes of 128 rows x 128 bytes (thread 0)
-    auto load_image = [&](int img) {
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                     ::"r"(tc_smem_addr(&bar_x)), "r"(Gm::kXBytes) : "memory");
-        for (int t = 0; t < Gm::MT; ++t)
-            for (int kc = 0; kc < Gm::KC; ++kc)
-                tma_load_2d(tc_smem_addr(base + (t * Gm::KC + kc) * Gm::kTile), &xmap,
-                            kc * Gm::kE, img * Gm::N0 + 128 * t, &bar_x);
-    };
+    constexpr uint32_t kTileBytes = Gm::KC * Gm::kTile;        // one M tile of the image
     if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_x)));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_t)));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_mma)));
+        for (int i = 0; i < 2; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&full[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&empty[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&acc[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(tc_smem_addr(&free_[i])),
+                         "r"(NT));
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        // the twiddle operand (already in its swizzled image) in one bulk copy
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                     ::"r"(tc_smem_addr(&bar_t)), "r"(Gm::kTBytes) : "memory");
-        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                     ::"r"(tc_smem_addr(base + Gm::kT)), "l"(tables), "r"(Gm::kTBytes),
-                     "r"(tc_smem_addr(&bar_t)) : "memory");
-        if ((int)blockIdx.x < nimg) load_image(blockIdx.x);
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(tc_smem_addr(&s_tmem)), "r"(Gm::kTmemCols));
+                     ::"r"(tc_smem_addr(&s_tmem)), "r"(2 * Gm::kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     tc_before_sync();
@@ -346,96 +355,140 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
     tc_after_sync();
     pdl_trigger();
     const uint32_t tmem = s_tmem;
-    bool ok = mbar_wait(&bar_t, 0, a.err);
     const uint32_t xs = tc_smem_addr(base), ts = tc_smem_addr(base + Gm::kT);
-    float *zr = reinterpret_cast<float *>(base + Gm::kZ);
-    float *zi = zr + Gm::N0 * Gm::M1;
-    float2 *F = reinterpret_cast<float2 *>(base + Gm::kZ);
-    uint32_t it = 0;
-    for (int img = blockIdx.x; img < nimg; img += gridDim.x, ++it) {
-        const unsigned long long t0 = a.trace ? trace_now() : 0;
-        ok &= mbar_wait(&bar_x, it, a.err);
-        const unsigned long long t_x = a.trace ? trace_now() : 0;     // the image has landed
-        if (tid == 0 && ok) {
-            tc_after_sync();
-            for (int t = 0; t < Gm::MT; ++t) {
-                const uint32_t d = tmem + t * Gm::N;
-                for (int kc = 0; kc < Gm::KC; ++kc) {
+
+    if (warp == NT / 32) {
+        // ----- producer -----
+        if (lane == 0) {
+            // the input is read once: its lines leave L2 first, so the kept modes
+            // this kernel writes (and the mixing reads next) stay resident
+            const uint64_t pol = l2_evict_first_policy();
+            auto load_tile = [&](int img, int t) {
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                             ::"r"(tc_smem_addr(&full[t])), "r"(kTileBytes) : "memory");
+                for (int kc = 0; kc < Gm::KC; ++kc)
+                    tma_load_2d_hint(xs + (t * Gm::KC + kc) * Gm::kTile, &xmap, kc * Gm::kE,
+                                     img * Gm::N0 + 128 * t, &full[t], pol);
+            };
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                         ::"r"(tc_smem_addr(&bar_t)), "r"(Gm::kTBytes) : "memory");
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                         ::"r"(ts), "l"(tables), "r"(Gm::kTBytes), "r"(tc_smem_addr(&bar_t))
+                         : "memory");
+            if ((int)blockIdx.x < nimg) {
+                load_tile(blockIdx.x, 0);
+                load_tile(blockIdx.x, 1);
+            }
+            bool ok = mbar_wait(&bar_t, 0, a.err);
+            constexpr uint32_t id = idesc_f16(Gm::N, std::is_same<T, __nv_bfloat16>::value);
+            uint32_t it = 0;
+            for (int img = blockIdx.x; img < nimg; img += gridDim.x, ++it) {
+                const uint32_t b = it & 1;
+                if (it >= 2) ok &= mbar_wait(&free_[b], ((it - 2) >> 1) & 1, a.err);
+                tc_after_sync();
+                for (int t = 0; t < Gm::MT; ++t) {
+                    ok &= mbar_wait(&full[t], it & 1, a.err);
+                    tc_after_sync();
+                    const uint32_t d = tmem + b * Gm::kTmemCols + t * Gm::N;
+                    for (int kc = 0; kc < Gm::KC && ok; ++kc)
 #pragma unroll
-                    for (int s = 0; s < 4; ++s) {
-                        const uint32_t ao = xs + (t * Gm::KC + kc) * Gm::kTile + s * 32;
-                        const uint32_t bo = ts + kc * Gm::kTChunk + s * 32;
-                        const uint32_t acc = (kc | s) ? 1u : 0u;
-                        constexpr uint32_t id =
-                            idesc_f16(Gm::N, std::is_same<T, __nv_bfloat16>::value);
-                        mma_f16(d, desc_sw128(ao), desc_sw128(bo), id, acc);
+                        for (int s4 = 0; s4 < 4; ++s4)
+                            mma_f16(d, desc_sw128(xs + (t * Gm::KC + kc) * Gm::kTile + s4 * 32),
+                                    desc_sw128(ts + kc * Gm::kTChunk + s4 * 32), id,
+                                    (kc | s4) ? 1u : 0u);
+                    mma_commit(&empty[t]);
+                }
+                mma_commit(&acc[b]);
+                const int next = img + (int)gridDim.x;
+                for (int t = 0; t < Gm::MT; ++t) {
+                    ok &= mbar_wait(&empty[t], it & 1, a.err);
+                    if (next < nimg) load_tile(next, t);
+                }
+            }
+        }
+    } else {
+        // ----- consumers: warp t1, lane k of the column DFT -----
+        float *zr = reinterpret_cast<float *>(base + Gm::kZ);
+        float *zi = zr + Gm::N0 * Gm::M1;
+        float2 *F = reinterpret_cast<float2 *>(base + Gm::kZ);
+        bool ok = true;
+        uint32_t it = 0;
+        for (int img = blockIdx.x; img < nimg; img += gridDim.x, ++it) {
+            const unsigned long long t0 = a.trace ? trace_now() : 0;
+            const uint32_t b = it & 1;
+            ok &= mbar_wait(&acc[b], (it >> 1) & 1, a.err);
+            tc_after_sync();
+            const unsigned long long t_z = a.trace ? trace_now() : 0;   // the row DFT is done
+            // Z planes from tensor memory: warps w and w + 4 read the same lanes,
+            // the first the re, the second the im half
+            {
+                const int half = warp >> 2;
+                float *dz = half ? zi : zr;
+                for (int t = 0; t < Gm::MT; ++t) {
+                    const int row = 128 * t + 32 * (warp & 3) + lane;
+#pragma unroll
+                    for (int g = 0; g < Gm::M1 / 16; ++g) {
+                        float v[16];
+                        tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) +
+                                      b * Gm::kTmemCols + t * Gm::N + half * Gm::M1 + 16 * g,
+                                  v);
+#pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            dz[row * Gm::M1 + ((16 * g + q) ^ (row & 31))] = ok ? v[q] : 0.f;
                     }
                 }
             }
-            mma_commit(&bar_mma);
-        }
-        ok &= mbar_wait(&bar_mma, it, a.err);
-        tc_after_sync();
-        // the MMAs have read the tile: the next image's tile lands under this
-        // image's column work
-        const int next = img + (int)gridDim.x;
-        if (tid == 0 && ok && next < nimg) load_image(next);
-        const unsigned long long t_z = a.trace ? trace_now() : 0;     // the row DFT is done
-        // Z planes from tensor memory: warps w and w + 4 read the same lanes, the
-        // first the re, the second the im half
-        {
-            const int half = warp >> 2;
-            float *dz = half ? zi : zr;
-            for (int t = 0; t < Gm::MT; ++t) {
-                const int row = 128 * t + 32 * (warp & 3) + lane;
+            tc_before_sync();
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc_smem_addr(&free_[b]))
+                         : "memory");
+            consumer_sync();
+            // F[t1][g1][k]: G1-point FFT over t2 of Z[t1 + T1 t2][k], warp t1, lane k
+            float2 z[Gm::G1];
 #pragma unroll
-                for (int g = 0; g < Gm::M1 / 16; ++g) {
-                    float v[16];
-                    tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + t * Gm::N +
-                                  half * Gm::M1 + 16 * g, v);
+            for (int t2 = 0; t2 < Gm::G1; ++t2) {
+                const int r = warp + Gm::T1 * t2, c = r * Gm::M1 + (lane ^ (r & 31));
+                z[t2] = make_float2(zr[c], zi[c]);
+            }
+            fft::fft_dif<Gm::G1, -1>(z);
+            consumer_sync();                     // Z is read: F goes over it
 #pragma unroll
-                    for (int q = 0; q < 16; ++q)
-                        dz[row * Gm::M1 + ((16 * g + q) ^ (row & 31))] = ok ? v[q] : 0.f;
-                }
+            for (int g1 = 0; g1 < Gm::G1; ++g1)
+                F[(warp * Gm::G1 + g1) * Gm::M1 + lane] = z[fft::bitrev(g1, fft::ilog2(Gm::G1))];
+            consumer_sync();
+            // kept modes: X[j][k] = sum_t1 W_N0^{g t1} F[t1][g mod G1][k], g the signed
+            // frequency of kept row j (j, or j - K0 for the high rows)
+            float2 *dst = a.part + (size_t)img * Gm::NK;
+            for (int o = tid; o < Gm::NK; o += NT) {
+                const int j = o / Gm::M1, k = o % Gm::M1;
+                const int g = j < Gm::M0 ? j : j - Gm::K0, g1 = j & (Gm::G1 - 1);
+                float2 accv = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int t1 = 0; t1 < Gm::T1; ++t1)
+                    cmac(accv, F[(t1 * Gm::G1 + g1) * Gm::M1 + k],
+                         __ldg(a.tw0 + ((g * t1) & (Gm::N0 - 1))));
+                __stcg(dst + o, accv);
+            }
+            consumer_sync();                     // F is read: the next Z goes over it
+            if (a.trace && tid == 0) {
+                unsigned smid;
+                asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+                fno_trace_record_t r;
+                r.item = (0u << 24) | ((unsigned)img & 0xFFFFFFu);
+                r.worker = smid;
+                r.t_start = t0;
+                r.t_ready = t_z;
+                r.t_compute = t_z;
+                r.t_end = trace_now();
+                a.trace[img] = r;
             }
         }
-        tc_before_sync();
-        __syncthreads();
-        // F[t1][g1][k]: G1-point FFT over t2 of Z[t1 + T1 t2][k], warp t1, lane k
-        float2 z[Gm::G1];
-#pragma unroll
-        for (int t2 = 0; t2 < Gm::G1; ++t2) {
-            const int r = warp + Gm::T1 * t2, c = r * Gm::M1 + (lane ^ (r & 31));
-            z[t2] = make_float2(zr[c], zi[c]);
-        }
-        fft::fft_dif<Gm::G1, -1>(z);
-        __syncthreads();                         // Z is read: F goes over it
-#pragma unroll
-        for (int g1 = 0; g1 < Gm::G1; ++g1)
-            F[(warp * Gm::G1 + g1) * Gm::M1 + lane] = z[fft::bitrev(g1, fft::ilog2(Gm::G1))];
-        __syncthreads();
-        // kept modes: X[j][k] = sum_t1 W_N0^{g t1} F[t1][g mod G1][k], g the signed
-        // frequency of kept row j (j, or j - K0 for the high rows)
-        float2 *dst = a.part + (size_t)img * Gm::NK;
-        for (int o = tid; o < Gm::NK; o += NT) {
-            const int j = o / Gm::M1, k = o % Gm::M1;
-            const int g = j < Gm::M0 ? j : j - Gm::K0, g1 = j & (Gm::G1 - 1);
-            float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int t1 = 0; t1 < Gm::T1; ++t1)
-                cmac(acc, F[(t1 * Gm::G1 + g1) * Gm::M1 + k],
-                     __ldg(a.tw0 + ((g * t1) & (Gm::N0 - 1))));
-            __stcg(dst + o, acc);
-        }
-        __syncthreads();                         // F is read: the next Z goes over it
-        cta_record_at(a, 0, 0, img, t0, t_x, t_z);
     }
     tc_before_sync();
     __syncthreads();
     if (warp == 0) {
         tc_after_sync();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(Gm::kTmemCols));
+                     "r"(2 * Gm::kTmemCols));
     }
 }
 
@@ -625,209 +678,6 @@ void make_table32(std::vector<unsigned char> &img) {
             const uint32_t chunk = (uint32_t)(n / 32) * Gm::kTChunk;
             memcpy(&img[chunk + sw_off(j, n % 32)], &hi, 4);
             memcpy(&img[chunk + sw_off(2 * Gm::M1 + j, n % 32)], &lo, 4);
-        }
-}
-
-// ---------------------------------------------------------------------------
-// Kernel C on the tensor cores, for 16-bit 256 x 256 layers: one CTA inverts a
-// whole output image.  The column inverse over the kept rows runs on the SIMT
-// cores in one pass (two-term sums over the signed frequencies, then one
-// 32-point inverse register FFT per thread), giving Zo[t][k] for every row t;
-// the row inverse is then the GEMM y = Zo' . Tinv^T with Zo' = [Re Zo | Im Zo]
-// (K = 64) and Tinv[n] = s [c(k) cos(2 pi k n / N1) | -c(k) sin(...)],
-// s = 1/(N0 N1), one kind::tf32 chain per 128-row tile with N = 256 output
-// samples in tensor memory (tf32 keeps the float32 range of Zo; its 2^-11
-// precision is within the 16-bit tolerance class).  The epilogue converts to
-// the storage type and stores 64-column boxes by TMA through swizzled staging
-// tiles.
-// ---------------------------------------------------------------------------
-// Two floats rounded to the storage type, the first in the low half.
-template <typename T>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    uint32_t u;
-    if constexpr (std::is_same<T, __half>::value) {
-        const __half2 h = __floats2half2_rn(lo, hi);
-        memcpy(&u, &h, 4);
-    } else {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-        memcpy(&u, &h, 4);
-    }
-    return u;
-}
-
-template <typename T>
-struct GeoC {
-    static constexpr int N0 = 256, N1 = 256, M0 = 32, M1 = 32, K0 = 64, NK = K0 * M1;
-    static constexpr int MT = 2;                        // 128-row tiles
-    static constexpr uint32_t kTile = 16384;            // 128 rows x 128 bytes
-    static constexpr uint32_t kA = 0;                   // [MT][2 chunks] Zo operand, 64 KiB
-    static constexpr uint32_t kB = kA + MT * 2 * kTile; // [2 chunks][256 rows] table, 64 KiB
-    static constexpr uint32_t kTBytes = 2 * 256 * 128;
-    static constexpr uint32_t kY = kB + kTBytes;        // kept modes, 16 KiB
-    static constexpr uint32_t kS = kY + NK * 8;         // staging of output rounds 0, 1
-    static constexpr uint32_t kTw = kS + 4 * kTile;
-    static constexpr uint32_t kSmem = kTw + N0 * 8 + 1024;
-    static_assert(MT * 2 * kTile >= 4 * kTile, "rounds 2, 3 stage over the operand");
-    static constexpr uint32_t kTmemCols = 512;
-};
-
-template <typename T>
-__global__ void __launch_bounds__(NT, 1)
-k_phase_c_tc(const __grid_constant__ CUtensorMap ymap, Args a, const void *table) {
-    using Gm = GeoC<T>;
-    using namespace tcu;
-    extern __shared__ __align__(1024) char smem_raw[];
-    char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                          ~static_cast<uintptr_t>(1023));
-    __shared__ __align__(8) uint64_t bar_t, bar_mma;
-    __shared__ uint32_t s_tmem;
-    const unsigned long long t0 = a.trace ? trace_now() : 0;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int img = blockIdx.x;
-    float2 *ys = reinterpret_cast<float2 *>(base + Gm::kY);
-    float2 *tw = reinterpret_cast<float2 *>(base + Gm::kTw);
-    if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_t)));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_mma)));
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                     ::"r"(tc_smem_addr(&bar_t)), "r"(Gm::kTBytes) : "memory");
-        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                     ::"r"(tc_smem_addr(base + Gm::kB)), "l"(table), "r"(Gm::kTBytes),
-                     "r"(tc_smem_addr(&bar_t)) : "memory");
-    }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(tc_smem_addr(&s_tmem)), "r"(Gm::kTmemCols));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-    }
-    for (int e = tid; e < Gm::N0; e += NT) tw[e] = a.tw0[e];
-    tc_before_sync();
-    __syncthreads();
-    tc_after_sync();
-    const uint32_t tmem = s_tmem;
-    pdl_wait();                                  // kernel B's mixed modes are complete
-    const unsigned long long t1 = a.trace ? trace_now() : 0;
-    const float2 *src = a.Y + (size_t)img * Gm::NK;
-    for (int e = tid; e < Gm::NK / 2; e += NT) cp_async16(ys + 2 * e, src + 2 * e);
-    cp_async_commit();
-    cp_async_wait_all();
-    __syncthreads();
-    // 1. Column inverse over the kept rows in one pass.  Kept row j holds the
-    //    signed frequency g = j (j < M0) or j - K0; with g = g1 + M0 g2 (g2 = -1, 0)
-    //    and t = t1 + (N0 / M0) t2,
-    //      Zo[t][k] = sum_g1 e^{+2 pi i g1 t2 / M0} U[g1],
-    //      U[g1] = sum_g2 V[g][k] e^{+2 pi i g t1 / N0},
-    //    two terms per U[g1] and one M0-point inverse register FFT per (t1, k):
-    //    warp t1, lane k.  Zo goes into the K-major operand, chunk 0 the real
-    //    parts, chunk 1 the imaginary.
-    {
-        constexpr int G1 = Gm::M0, T1 = Gm::N0 / G1;
-        static_assert(T1 * Gm::M1 == NT && Gm::M1 == 32 && Gm::K0 == 2 * G1, "warp t1, lane k");
-        const int t1 = warp, k = tid & 31;
-        float2 z[G1];
-#pragma unroll
-        for (int g1 = 0; g1 < G1; ++g1) {
-            const float2 w0 = tw[(g1 * t1) & (Gm::N0 - 1)];          // e^{-2 pi i g t1 / N0}
-            const float2 w1 = tw[((g1 - G1) * t1) & (Gm::N0 - 1)];
-            float2 acc = make_float2(0.f, 0.f);
-            cmac(acc, ys[g1 * Gm::M1 + k], make_float2(w0.x, -w0.y));
-            cmac(acc, ys[(g1 + G1) * Gm::M1 + k], make_float2(w1.x, -w1.y));
-            z[g1] = acc;
-        }
-        fft::fft_dif<G1, 1>(z);
-#pragma unroll
-        for (int t2 = 0; t2 < G1; ++t2) {
-            const int t = t1 + T1 * t2;
-            const float2 v = z[fft::bitrev(t2, fft::ilog2(G1))];
-            char *At = base + Gm::kA + (t / 128) * 2 * Gm::kTile;
-            const uint32_t off = sw_off(t % 128, k);
-            *reinterpret_cast<float *>(At + off) = v.x;
-            *reinterpret_cast<float *>(At + Gm::kTile + off) = v.y;
-        }
-    }
-    fence_async_smem();
-    tc_before_sync();
-    __syncthreads();
-    bool ok = mbar_wait(&bar_t, 0, a.err);
-    if (tid == 0) {
-        tc_after_sync();
-        constexpr uint32_t id = idesc_tf32(256);
-        const uint32_t as = tc_smem_addr(base + Gm::kA), bs = tc_smem_addr(base + Gm::kB);
-        for (int t = 0; t < Gm::MT; ++t)
-            for (int c = 0; c < 2; ++c)
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_tf32(tmem + 256 * t, desc_sw128(as + (t * 2 + c) * Gm::kTile + s * 32),
-                             desc_sw128(bs + c * 256 * 128 + s * 32), id, (c | s) ? 1u : 0u);
-        mma_commit(&bar_mma);
-    }
-    ok &= mbar_wait(&bar_mma, 0, a.err);
-    tc_after_sync();
-    // 3. rows out: warp w reads lanes 32 (w % 4).. of tensor memory; the two warp
-    //    halves take column blocks 2h and 2h + 1 (64 outputs each) per tile.
-    //    Round r = 2 t + step stages its two 64-column boxes in a region of its
-    //    own (rounds 0, 1 in the staging region, 2, 3 over the Zo operand, free
-    //    once the MMAs completed), so no round waits for an earlier store.
-    const int half = warp >> 2, lrow = 32 * (warp & 3) + (tid & 31);
-    for (int t = 0; t < Gm::MT; ++t) {
-        for (int step = 0; step < 2; ++step) {
-            const int cb = 2 * half + step;               // 64-column block of y
-            const int round = 2 * t + step;
-            char *region = base + (round < 2 ? Gm::kS + round * 2 * Gm::kTile
-                                             : Gm::kA + (round - 2) * 2 * Gm::kTile);
-            char *stage = region + half * Gm::kTile;
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                float v[16];
-                tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256 * t + 64 * cb + 16 * g, v);
-                uint32_t pk[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    pk[q] = pack2<T>(ok ? v[2 * q] : 0.f, ok ? v[2 * q + 1] : 0.f);
-                *reinterpret_cast<uint4 *>(stage + sw_off16(lrow, 16 * g)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                *reinterpret_cast<uint4 *>(stage + sw_off16(lrow, 16 * g + 8)) =
-                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            }
-            fence_async_smem();
-            __syncthreads();
-            if (tid == 0) {
-                for (int h = 0; h < 2; ++h)
-                    tma_store_2d(&ymap, 64 * (2 * h + step), img * Gm::N0 + 128 * t,
-                                 tc_smem_addr(region + h * Gm::kTile));
-                bulk_commit();
-            }
-        }
-    }
-    if (tid == 0) bulk_wait_read();              // the staging regions may be released
-    tc_before_sync();
-    __syncthreads();
-    if (warp == 0) {
-        tc_after_sync();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(Gm::kTmemCols));
-    }
-    cta_record(a, 2, a.trace_c, t0, t1);
-}
-
-// Host: the inverse row-DFT operand: [chunk: re, im][n][k] with c(k) folded in.
-template <typename T>
-void make_table_c(std::vector<unsigned char> &img) {
-    using Gm = GeoC<T>;
-    using tcu::sw_off;
-    img.assign(Gm::kTBytes, 0);
-    const double two_pi = 2.0 * M_PI;
-    for (int n = 0; n < Gm::N1; ++n)
-        for (int k = 0; k < Gm::M1; ++k) {
-            // c(k) and the inverse's 1/(N0 N1) (a power of two: the rounding is
-            // that of the unscaled value)
-            const double ck = ((k == 0 || 2 * k == Gm::N1) ? 1.0 : 2.0) /
-                              ((double)Gm::N0 * (double)Gm::N1);
-            const double ang = two_pi * (double)k * (double)n / (double)Gm::N1;
-            const float c = (float)(ck * std::cos(ang)), sn = (float)(-ck * std::sin(ang));
-            memcpy(&img[sw_off(n, k)], &c, 4);
-            memcpy(&img[256 * 128 + sw_off(n, k)], &sn, 4);
         }
 }
 
@@ -1287,8 +1137,9 @@ struct Pdl {
                                                (int)tca::GeoC32<false>::kSmem);
                     tca::make_table_c32(imgc);
                 } else {
-                    e = raise_smem_limit(tca::k_phase_c_tc<T>, (int)tca::GeoC<T>::kSmem);
-                    tca::make_table_c<T>(imgc);
+                    // the persistent two-GEMM inverse (fno_inv16.cu)
+                    e = inv16_init(p.dtype);
+                    inv16_make_tables(p.dtype, imgc);
                 }
             }
             if (e == cudaSuccess && (p.fused_tca || p.fused_tcc)) {
@@ -1312,6 +1163,8 @@ struct Pdl {
                         mixtc_supported(p.g.d, p.dtype, p.batch, p.cin, p.cout, Cf::M1,
                                         p.g.nkept);
         if (e == cudaSuccess && p.fused_mixtc) e = mixtc_init(p.dtype);
+        p.mix_image = p.fused_mixtc && (p.flags & FNO_PLAN_PACKED_WEIGHTS) &&
+                      mixtc_image_layout(p.cin, p.cout);
         p.fused_bstream = 0;
 
         if (e == cudaSuccess && (p.flags & FNO_PLAN_TRACE)) {
@@ -1375,8 +1228,8 @@ struct Pdl {
                         return cudaErrorInvalidValue;
                     // persistent: one CTA per SM walks the images
                     const int grid = nA < p.num_sms ? nA : p.num_sms;
-                    tca::k_phase_a_tc<T><<<grid, tca::NT, Gm::kSmem, s>>>(xmap, a, p.fused_tables,
-                                                                         nA);
+                    tca::k_phase_a_tc<T><<<grid, tca::kNTA, Gm::kSmem, s>>>(xmap, a, p.fused_tables,
+                                                                           nA);
                 }
                 e = cudaGetLastError();
                 done_a = true;
@@ -1421,7 +1274,7 @@ struct Pdl {
             m.m1 = Cf::M1;
             m.mblk = (int)Cf::MBLK;
             m.nk = Cf::NK;
-            m.packed = a.wpacked;
+            m.packed = p.mix_image ? 2 : a.wpacked;
             e = mixtc_launch(p.dtype, m, s);
         } else {
             cfg.gridDim = dim3(nB);
@@ -1457,17 +1310,14 @@ struct Pdl {
         }
         if constexpr (!std::is_same<T, float>::value) {
             if (p.fused_tcc) {
-                using Gc = tca::GeoC<T>;
-                CUtensorMap ymap;
-                if (!tcu::encode_rows_tiled(&ymap, a.y, (int64_t)p.batch * p.cout * Gc::N0,
-                                            Gc::N1, sizeof(T), 64, tcu::tma_type<T>()))
-                    return cudaErrorInvalidValue;
-                cfg.blockDim = dim3(tca::NT);
-                cfg.dynamicSmemBytes = Gc::kSmem;
+                Inv16Args ia;
+                ia.Y = a.Y;
+                ia.y = a.y;
+                ia.err = a.err;
+                ia.trace = a.trace;
+                ia.trace_first = a.trace_c;
                 const void *tab = static_cast<const char *>(p.fused_tables) + p.fused_table_c;
-                e = cudaLaunchKernelEx(&cfg, tca::k_phase_c_tc<T>, ymap, a, tab);
-                if (e != cudaSuccess) return e;
-                return cudaGetLastError();
+                return inv16_launch(p.dtype, ia, tab, p.batch * p.cout, p.num_sms, s);
             }
         }
         cfg.dynamicSmemBytes = CfC::kSmemTw + CfC::kSmemC;

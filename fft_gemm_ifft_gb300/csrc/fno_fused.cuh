@@ -1,6 +1,8 @@
 // fno_fused.cuh -- host-side entry points of the fused layer kernels.
 #pragma once
 
+#include <vector>
+
 #include "fno_internal.cuh"
 
 namespace fno {
@@ -40,13 +42,34 @@ struct MixTcArgs {
     fno_trace_record_t *trace;    // nullptr unless tracing
     int trace_first;
     int batch, cin, cout, m0, m1, mblk, nk;
-    int packed;                   // w is in the packed mode-major layout
+    int packed;                   // w packed: 1 mode-major groups of four, 2 operand images
 };
 bool mixtc_supported(int d, fno_dtype_t dtype, int64_t batch, int cin, int cout, int m1,
                      int64_t nkept);
 int mixtc_items(int64_t nkept);
 cudaError_t mixtc_init(fno_dtype_t dtype);
 cudaError_t mixtc_launch(fno_dtype_t dtype, const MixTcArgs &args, cudaStream_t s);
+// Packed weights as the mixing kernel's operand images (MixTcArgs.packed = 2):
+// offered for 64 input and 64 output channels, where the images take exactly
+// the bytes of the weights.
+bool mixtc_image_layout(int cin, int cout);
+cudaError_t mixtc_pack_image(fno_dtype_t dtype, const void *w, void *wp, int cin, int cout,
+                             int m0, int m1, int mblk, int nk, int num_sms, cudaStream_t s);
+
+// Kernel C of the 16-bit 256 x 256 layer (fno_inv16.cu): the column and row
+// inverse DFTs of each output image as two tcgen05 GEMMs, persistent.
+struct Inv16Args {
+    const float2 *Y;              // mixed modes [nimg][64 kept rows][32 bins]
+    void *y;                      // output images [nimg][256][256], storage type
+    int *err;
+    fno_trace_record_t *trace;    // nullptr unless tracing: one record per image
+    int trace_first;
+};
+size_t inv16_tables_bytes();
+void inv16_make_tables(fno_dtype_t dtype, std::vector<unsigned char> &img);
+cudaError_t inv16_init(fno_dtype_t dtype);
+cudaError_t inv16_launch(fno_dtype_t dtype, const Inv16Args &a, const void *tables,
+                         int64_t nimg, int num_sms, cudaStream_t s);
 
 // The 1-D layer's kernel (one cluster per sample).
 bool fused1d_supported(const Geom &g, fno_dtype_t dtype, int64_t batch, int cin, int cout);

@@ -18,15 +18,22 @@ namespace fno {
 // Device error word codes (plan-owned int, first error wins).
 enum : int { kDevOk = 0, kDevTimeout = 1, kDevBounds = 2 };
 
+// n[a] is the transform length of axis a and ext[a] the extent of x and y
+// along it.  They differ only for a zero-padded layer (a non-periodic domain,
+// TurboFNO §2.3 / §3.3): x is read as if extended with n - ext zeros per axis
+// and y keeps the first ext samples of the inverse; everywhere else ext == n.
 struct Geom {
     int d;
     int64_t n[FNO_MAX_NDIM];
     int32_t m[FNO_MAX_NDIM];
     int64_t kdim[FNO_MAX_NDIM];   // kept extent per axis
+    int64_t ext[FNO_MAX_NDIM];    // extent of x and y per axis (<= n)
     int64_t nkept;                // |K|
-    int64_t npix;                 // prod N
+    int64_t npix;                 // prod ext: elements of one x or y image
+    int64_t ntr;                  // prod n: points of the transform (scale 1/ntr)
     int64_t nblk;                 // weight blocks 2^(d-1)
     int64_t mblk;                 // modes per block prod m
+    bool padded;                  // ext != n on some axis
 };
 
 // Host-side plan state.
@@ -59,6 +66,7 @@ struct Plan {
     bool fused_tca;               // three-kernel path transforms (kernel A) on the tensor cores
     bool fused_tcc;               // ... and inverts (kernel C) on the tensor cores
     bool fused_c1pass;            // fp32 kernel C: one-pass column inverse, 3 CTAs per SM
+    bool mix_image;               // packed weights are the tensor-core mixing's operand images
     size_t fused_table_c;         // byte offset of kernel C's operand in fused_tables
     fno_trace_record_t *trace;    // FNO_PLAN_TRACE: one record per work item (plan-owned)
     size_t trace_records;         // records one forward call produces

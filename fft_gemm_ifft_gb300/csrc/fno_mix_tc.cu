@@ -19,6 +19,17 @@
 // for the run's modes of every (b, o) as one contiguous piece through a
 // shared-memory staging tile.  Channel counts up to 64 are zero-padded to the
 // tile.
+//
+// Weights packed as operand images (plans with FNO_PLAN_PACKED_WEIGHTS and 64
+// input and output channels): fno_spectral_conv_pack_weights writes, once per
+// weight update, each kept mode's [Wr^T; Wi^T] as two 64 x 64 tiles in the
+// swizzled K-major layout above (16 KiB a mode, the size of the mode's weights).
+// A CTA then fetches a mode with one bulk copy into the middle of a 24 KiB slot
+// [-Wi^T | Wr^T | Wi^T] and negates Wi^T into the first third: K chunk 0 of the
+// real-block operand is the slot from its second tile (rows Wr^T, then Wi^T),
+// chunk 1 the slot from its start (rows -Wi^T, then Wr^T).
+#include <algorithm>
+#include <cstring>
 #include <type_traits>
 
 #include "fno_fused_dev.cuh"
@@ -51,6 +62,15 @@ constexpr uint32_t kBMode = 2 * kBChunk;
 constexpr uint32_t kOffB = kRun * kAMode;                 // weight operands, 32 KiB a mode
 constexpr uint32_t kSmem = kOffB + kRun * kBMode + 1024;  // + X operands, 16 KiB a mode + align
 constexpr uint32_t kTmemCols = kRun * 64;                  // kRun x N (N <= 64)
+// operand-image weights: a 24 KiB slot per mode
+constexpr uint32_t kHalfTile = 64 * 128;                   // 64 rows x 128 bytes
+constexpr uint32_t kASlot = 3 * kHalfTile;
+constexpr uint32_t kOffBImg = kRun * kASlot;
+constexpr uint32_t kSmemImg = kOffBImg + kRun * kBMode + 1024;
+constexpr uint32_t kImgMode = 2 * kHalfTile;               // packed bytes per mode (16-bit)
+// the drain's staging tile (batch x 64 outputs x kRun modes, complex float) goes
+// over the weight and X operands once the MMAs are done
+static_assert((uint32_t)kMaxB * kCh * kRun * 8 <= kRun * kASlot + kRun * kBMode, "staging fits");
 
 template <typename T> struct Bits;
 template <> struct Bits<__half> {
@@ -66,12 +86,13 @@ template <> struct Bits<__nv_bfloat16> {
     }
 };
 
-template <typename T>
+template <typename T, bool kImg>
 __global__ void __launch_bounds__(kMT, kRun == 2 ? 2 : 1) k_mix_tc(MixTcArgs a) {
     extern __shared__ __align__(1024) char smem_raw[];
     char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
-    __shared__ __align__(8) uint64_t bar;
+    constexpr uint32_t kB0 = kImg ? kOffBImg : kOffB;        // X operands
+    __shared__ __align__(8) uint64_t bar, bar_w;
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5;
     const unsigned long long t0 = a.trace ? trace_now() : 0;
@@ -83,15 +104,48 @@ __global__ void __launch_bounds__(kMT, kRun == 2 ? 2 : 1) k_mix_tc(MixTcArgs a) 
     const int local0 = (j - blk * a.m0) * a.m1 + k;
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_w)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if constexpr (kImg) {
+            // the run's weight images: kRun contiguous 16 KiB pieces, each into the
+            // middle third of its slot (independent of kernel A); a run beyond the
+            // packed tensor is an error, recorded, and nothing is copied (the
+            // barrier is released without bytes)
+            const bool inside = mode0 >= 0 && mode0 + kRun <= a.nk;
+            if (!inside) raise_dev_error(a.err, kDevBounds);
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                         ::"r"(tc_smem_addr(&bar_w)), "r"(inside ? kRun * kImgMode : 0u)
+                         : "memory");
+            const char *src = static_cast<const char *>(a.w) + (size_t)mode0 * kImgMode;
+            for (int r = 0; r < kRun && inside; ++r)
+                asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+                             " [%0], [%1], %2, [%3];"
+                             ::"r"(tc_smem_addr(base + r * kASlot + kHalfTile)),
+                               "l"(src + (size_t)r * kImgMode), "r"(kImgMode),
+                               "r"(tc_smem_addr(&bar_w)) : "memory");
+        }
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(tc_smem_addr(&s_tmem)), "r"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
+    bool ok = true;
+    if constexpr (kImg) {
+        // every thread waits on bar_w: it must be initialised first
+        __syncthreads();
+        // -Wi^T into the first third of each slot (a sign flip of every 16-bit value)
+        ok = mbar_wait(&bar_w, 0, a.err);
+        for (int e = tid; e < (int)(kRun * kHalfTile / 16); e += kMT) {
+            const int r = e / (kHalfTile / 16), q = e % (kHalfTile / 16);
+            const uint4 v = reinterpret_cast<const uint4 *>(base + r * kASlot + 2 * kHalfTile)[q];
+            reinterpret_cast<uint4 *>(base + r * kASlot)[q] =
+                make_uint4(v.x ^ 0x80008000u, v.y ^ 0x80008000u, v.z ^ 0x80008000u,
+                           v.w ^ 0x80008000u);
+        }
+    }
     // 1. zero the operands where the channel counts leave padding
-    if (a.cin < kCh || a.cout < kCh) {
+    if (!kImg && (a.cin < kCh || a.cout < kCh)) {
         for (int e = tid; e < (int)(kRun * kAMode / 16); e += kMT)
             reinterpret_cast<uint4 *>(base)[e] = make_uint4(0, 0, 0, 0);
         __syncthreads();
@@ -102,7 +156,7 @@ __global__ void __launch_bounds__(kMT, kRun == 2 ? 2 : 1) k_mix_tc(MixTcArgs a) 
     // a unit = one output o and eight consecutive input channels: eight 16-byte
     // loads (four modes each), then per mode and quadrant one 16-byte store of
     // eight consecutive K elements (conflict-free under the swizzle)
-    for (int un = tid; un < kCh * (kCh / 8); un += kMT) {
+    for (int un = tid; !kImg && un < kCh * (kCh / 8); un += kMT) {
         const int o = un % kCh, i0 = 8 * (un / kCh);
         if (o >= a.cout || i0 >= a.cin) continue;
         // the run's kRun modes of one (i, o): kRun x 4 bytes, contiguous in both layouts
@@ -180,7 +234,7 @@ __global__ void __launch_bounds__(kMT, kRun == 2 ? 2 : 1) k_mix_tc(MixTcArgs a) 
                 pr[t2] = (uint32_t)Bits<T>::from(xr[0]) | ((uint32_t)Bits<T>::from(xr[1]) << 16);
                 pi[t2] = (uint32_t)Bits<T>::from(xi[0]) | ((uint32_t)Bits<T>::from(xi[1]) << 16);
             }
-            char *B = base + kOffB + r * kBMode;
+            char *B = base + kB0 + r * kBMode;
             *reinterpret_cast<uint4 *>(B + sw_off16(bb, i0)) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
             *reinterpret_cast<uint4 *>(B + kBChunk + sw_off16(bb, i0)) =
                 make_uint4(pi[0], pi[1], pi[2], pi[3]);
@@ -194,19 +248,23 @@ __global__ void __launch_bounds__(kMT, kRun == 2 ? 2 : 1) k_mix_tc(MixTcArgs a) 
     if (tid == 0) {
         const uint32_t idesc = idesc_f16(nbp, Bits<T>::kBf16);
 #pragma unroll
-        for (int r = 0; r < kRun; ++r) {
-            const uint32_t am = tc_smem_addr(base + r * kAMode);
-            const uint32_t bm = tc_smem_addr(base + kOffB + r * kBMode);
+        for (int r = 0; r < kRun && ok; ++r) {
+            const uint32_t bm = tc_smem_addr(base + kB0 + r * kBMode);
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < 2; ++c) {
+                // K chunk c of the real-block weight operand
+                const uint32_t am =
+                    kImg ? tc_smem_addr(base + r * kASlot + (c == 0 ? kHalfTile : 0u))
+                         : tc_smem_addr(base + r * kAMode + c * kAChunk);
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    mma_f16(tmem + r * nbp, desc_sw128(am + c * kAChunk + s * 32),
+                    mma_f16(tmem + r * nbp, desc_sw128(am + s * 32),
                             desc_sw128(bm + c * kBChunk + s * 32), idesc, (c | s) ? 1u : 0u);
+            }
         }
         mma_commit(&bar);
     }
-    const bool ok = mbar_wait(&bar, 0, a.err);
+    ok &= mbar_wait(&bar, 0, a.err);
     tc_after_sync();
     // 4. tensor memory -> staging [b][o][4 modes] complex (over the weight operands,
     //    which the finished MMAs no longer read)
@@ -279,7 +337,8 @@ cudaError_t mixtc_init(fno_dtype_t dtype) {
         if constexpr (std::is_same<T, float>::value) {
             return cudaErrorInvalidValue;
         } else {
-            return raise_smem_limit(k_mix_tc<T>, (int)kSmem);
+            cudaError_t e = raise_smem_limit(k_mix_tc<T, false>, (int)kSmem);
+            return e != cudaSuccess ? e : raise_smem_limit(k_mix_tc<T, true>, (int)kSmemImg);
         }
     });
 }
@@ -291,7 +350,7 @@ cudaError_t mixtc_launch(fno_dtype_t dtype, const MixTcArgs &args, cudaStream_t 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(args.nk / kRun));
     cfg.blockDim = dim3(kMT);
-    cfg.dynamicSmemBytes = kSmem;
+    cfg.dynamicSmemBytes = args.packed == 2 ? kSmemImg : kSmem;
     cfg.stream = s;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
@@ -300,8 +359,69 @@ cudaError_t mixtc_launch(fno_dtype_t dtype, const MixTcArgs &args, cudaStream_t 
         if constexpr (std::is_same<T, float>::value) {
             return cudaErrorInvalidValue;
         } else {
-            cudaError_t e = cudaLaunchKernelEx(&cfg, k_mix_tc<T>, args);
+            cudaError_t e = args.packed == 2 ? cudaLaunchKernelEx(&cfg, k_mix_tc<T, true>, args)
+                                             : cudaLaunchKernelEx(&cfg, k_mix_tc<T, false>, args);
             return e != cudaSuccess ? e : cudaGetLastError();
+        }
+    });
+}
+
+namespace {
+
+// One thread per 16-byte piece of the packed images: mode kk, tile (0: Wr^T,
+// 1: Wi^T), row o, physical piece p of the swizzled row (logical columns
+// i = 8 ((p ^ o) & 7) .. + 7).  Zero outside cin x cout.
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_pack_image(const T *__restrict__ w, uint4 *__restrict__ wp, int cin, int cout, int m0, int m1,
+             int mblk, int nk) {
+    const int64_t total = (int64_t)nk * 2 * kCh * 8;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int p = (int)(idx & 7);
+        const int o = (int)((idx >> 3) % kCh);
+        const int tile = (int)((idx >> 3) / kCh % 2);
+        const int kk = (int)(idx / (16 * kCh));
+        const int jr = kk / m1, k = kk % m1;
+        const int blk = jr >= m0 ? 1 : 0;
+        const int local = (jr - blk * m0) * m1 + k;
+        const int i0 = 8 * ((p ^ o) & 7);
+        unsigned short v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u;
+            v[u] = 0;
+            if (i < cin && o < cout) {
+                const T val = w[((((size_t)blk * cin + i) * cout + o) * mblk + local) * 2 + tile];
+                memcpy(&v[u], &val, 2);
+            }
+        }
+        uint4 q;
+        q.x = (uint32_t)v[0] | ((uint32_t)v[1] << 16);
+        q.y = (uint32_t)v[2] | ((uint32_t)v[3] << 16);
+        q.z = (uint32_t)v[4] | ((uint32_t)v[5] << 16);
+        q.w = (uint32_t)v[6] | ((uint32_t)v[7] << 16);
+        wp[idx] = q;
+    }
+}
+
+}  // namespace
+
+bool mixtc_image_layout(int cin, int cout) { return cin == kCh && cout == kCh; }
+
+cudaError_t mixtc_pack_image(fno_dtype_t dtype, const void *w, void *wp, int cin, int cout,
+                             int m0, int m1, int mblk, int nk, int num_sms, cudaStream_t s) {
+    const int64_t pieces = (int64_t)nk * 2 * kCh * 8;
+    const int grid = (int)std::min<int64_t>((pieces + 255) / 256, (int64_t)num_sms * 16);
+    return with_storage(dtype, [&](auto t) {
+        using T = decltype(t);
+        if constexpr (std::is_same<T, float>::value) {
+            return cudaErrorInvalidValue;
+        } else {
+            k_pack_image<T><<<grid, 256, 0, s>>>(static_cast<const T *>(w),
+                                                 static_cast<uint4 *>(wp), cin, cout, m0, m1,
+                                                 mblk, nk);
+            return cudaGetLastError();
         }
     });
 }

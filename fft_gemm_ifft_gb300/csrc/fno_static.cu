@@ -15,7 +15,10 @@
 // addresses.  The first call on a device therefore looks up their device
 // addresses with cudaGetSymbolAddress (with that device current) and fills the
 // twiddle tables with a synchronous copy; later calls on that device reuse the
-// addresses.  That first call should come before any stream capture.
+// addresses.  That first call should come before any stream capture.  The
+// cached state assumes the device's context lives as long as the process: a
+// caller that runs cudaDeviceReset reloads the module (new, zeroed arrays) and
+// must not call this entry point on that device afterwards.
 #include <cmath>
 #include <mutex>
 #include <vector>
@@ -107,9 +110,10 @@ extern "C" fno_status_t fno_spectral_conv_forward_static(
     Plan p{};
     Geom &g = p.g;
     g.d = ndim;
-    g.nkept = g.npix = g.nblk = g.mblk = 1;
+    g.nkept = g.npix = g.ntr = g.nblk = g.mblk = 1;
     for (int a = 0; a < ndim; ++a) {
-        g.n[a] = n[a];
+        g.n[a] = g.ext[a] = n[a];
+        g.ntr *= n[a];
         g.m[a] = modes[a];
         g.kdim[a] = a < ndim - 1 ? 2 * (int64_t)modes[a] : modes[a];
         if (a < ndim - 1) g.nblk *= 2;
@@ -133,6 +137,11 @@ extern "C" fno_status_t fno_spectral_conv_forward_static(
     DeviceState *ds = nullptr;
     st = setup(dev, &ds);
     if (st != FNO_OK) return st;
+    // no operand may lie inside the library's own scratch array
+    if (overlaps(y, yb, ds->scratch, kStaticScratchBytes) ||
+        overlaps(x, xb, ds->scratch, kStaticScratchBytes) ||
+        overlaps(w, weight_bytes, ds->scratch, kStaticScratchBytes))
+        return FNO_ERR_ALIASING;
 
     p.batch = batch;
     p.cin = cin;

@@ -10,6 +10,7 @@
 // the fused kernels are not specialised for.
 #include <algorithm>
 
+#include "fno_fused.cuh"
 #include "fno_internal.cuh"
 
 namespace fno {
@@ -37,19 +38,21 @@ __device__ __forceinline__ int kept_freq(int r, int m, int n) {
     return r < m ? r : n - 2 * m + r;
 }
 
-// Step a1, last axis: out[line][k] = sum_n x[line][n] e^{-2 pi i k n / N}, k < M.
+// Step a1, last axis: out[line][k] = sum_n x[line][n] e^{-2 pi i k n / N}, k < M,
+// over the E <= N stored samples of a line (a padded line's other N - E
+// samples are zeros and add nothing).
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
-k_fwd_last(const T *__restrict__ x, float2 *__restrict__ out, int64_t nlines, int N,
+k_fwd_last(const T *__restrict__ x, float2 *__restrict__ out, int64_t nlines, int N, int E,
            int M, const float2 *__restrict__ tw) {
     const int64_t total = nlines * M;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
         const int64_t line = idx / M;
         const int k = (int)(idx - line * M);
-        const T *src = x + line * N;
+        const T *src = x + line * E;
         float2 acc = make_float2(0.f, 0.f);
-        for (int n = 0; n < N; ++n) {
+        for (int n = 0; n < E; ++n) {
             const float v = Storage<T>::load(src + n);
             const float2 w = tw[tw_idx(k * n, N)];
             acc.x = fmaf(v, w.x, acc.x);
@@ -59,10 +62,11 @@ k_fwd_last(const T *__restrict__ x, float2 *__restrict__ out, int64_t nlines, in
     }
 }
 
-// Step a1, one full axis: out[o][r][q] = sum_n in[o][n][q] e^{-2 pi i f(r) n / N}.
+// Step a1, one full axis: out[o][r][q] = sum_n in[o][n][q] e^{-2 pi i f(r) n / N},
+// over the E <= N stored rows n (the others are zero padding).
 __global__ void __launch_bounds__(kThreads)
 k_fwd_full(const float2 *__restrict__ in, float2 *__restrict__ out, int64_t outer, int N,
-           int64_t inner, int m, const float2 *__restrict__ tw) {
+           int E, int64_t inner, int m, const float2 *__restrict__ tw) {
     const int K = 2 * m;
     const int64_t total = outer * K * inner;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
@@ -72,9 +76,9 @@ k_fwd_full(const float2 *__restrict__ in, float2 *__restrict__ out, int64_t oute
         const int r = (int)(t % K);
         const int64_t o = t / K;
         const int f = kept_freq(r, m, N);
-        const float2 *src = in + o * N * inner + q;
+        const float2 *src = in + o * E * inner + q;
         float2 acc = make_float2(0.f, 0.f);
-        for (int n = 0; n < N; ++n) cfma(acc, src[n * inner], tw[tw_idx(f * n, N)]);
+        for (int n = 0; n < E; ++n) cfma(acc, src[n * inner], tw[tw_idx(f * n, N)]);
         out[idx] = acc;
     }
 }
@@ -115,18 +119,19 @@ k_mix(const float2 *__restrict__ X, const T *__restrict__ w, float2 *__restrict_
     }
 }
 
-// Step a3, one full axis: out[o][n][q] = sum_r in[o][r][q] e^{+2 pi i f(r) n / N}.
+// Step a3, one full axis: out[o][n][q] = sum_r in[o][r][q] e^{+2 pi i f(r) n / N},
+// for the first E <= N rows n only (the output crop of a padded axis).
 __global__ void __launch_bounds__(kThreads)
 k_inv_full(const float2 *__restrict__ in, float2 *__restrict__ out, int64_t outer, int N,
-           int64_t inner, int m, const float2 *__restrict__ tw) {
+           int E, int64_t inner, int m, const float2 *__restrict__ tw) {
     const int K = 2 * m;
-    const int64_t total = outer * N * inner;
+    const int64_t total = outer * E * inner;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
         const int64_t q = idx % inner;
         const int64_t t = idx / inner;
-        const int n = (int)(t % N);
-        const int64_t o = t / N;
+        const int n = (int)(t % E);
+        const int64_t o = t / E;
         const float2 *src = in + o * K * inner + q;
         float2 acc = make_float2(0.f, 0.f);
         for (int r = 0; r < K; ++r) {
@@ -138,16 +143,17 @@ k_inv_full(const float2 *__restrict__ in, float2 *__restrict__ out, int64_t oute
 }
 
 // Step a3, last axis: y[line][n] = scale * sum_{k<M} c(k) Re(Y[k] e^{+2 pi i k n/N}),
-// c(0) = c(N/2) = 1, c = 2 otherwise.
+// c(0) = c(N/2) = 1, c = 2 otherwise, for the first E <= N samples n of a line:
+// the crop of a padded axis is this guarded store (TurboFNO §3.3), not a copy.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
-k_inv_last(const float2 *__restrict__ in, T *__restrict__ y, int64_t nlines, int N, int M,
-           const float2 *__restrict__ tw, float scale) {
-    const int64_t total = nlines * N;
+k_inv_last(const float2 *__restrict__ in, T *__restrict__ y, int64_t nlines, int N, int E,
+           int M, const float2 *__restrict__ tw, float scale) {
+    const int64_t total = nlines * E;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t line = idx / N;
-        const int n = (int)(idx - line * N);
+        const int64_t line = idx / E;
+        const int n = (int)(idx - line * E);
         const float2 *src = in + line * M;
         float acc = 0.f;
         for (int k = 0; k < M; ++k) {
@@ -173,11 +179,11 @@ void stage_sizes(const Geom &g, int64_t batch, int cin, int cout, int64_t *max_e
     int64_t best = 0;
     // forward: after the last axis, then after each full axis from d-2 down to 0
     int64_t s0 = batch * cin * ml;
-    for (int j = 0; j < d - 1; ++j) s0 *= g.n[j];
+    for (int j = 0; j < d - 1; ++j) s0 *= g.ext[j];
     best = std::max(best, s0);
     for (int a = d - 2; a >= 0; --a) {
         int64_t s = batch * cin * ml;
-        for (int j = 0; j < d - 1; ++j) s *= (j < a) ? g.n[j] : g.kdim[j];
+        for (int j = 0; j < d - 1; ++j) s *= (j < a) ? g.ext[j] : g.kdim[j];
         best = std::max(best, s);
     }
     best = std::max(best, batch * cin * g.nkept);
@@ -185,7 +191,7 @@ void stage_sizes(const Geom &g, int64_t batch, int cin, int cout, int64_t *max_e
     // inverse: after expanding full axis a = 0..d-2
     for (int a = 0; a < d - 1; ++a) {
         int64_t s = batch * cout * ml;
-        for (int j = 0; j < d - 1; ++j) s *= (j <= a) ? g.n[j] : g.kdim[j];
+        for (int j = 0; j < d - 1; ++j) s *= (j <= a) ? g.ext[j] : g.kdim[j];
         best = std::max(best, s);
     }
     *max_elems = best;
@@ -217,17 +223,18 @@ static cudaError_t unfused_forward_t(const Plan &p, const Buffers &bf, cudaStrea
 
     // a1, last axis (real -> half spectrum, truncated)
     int64_t lines = p.batch * p.cin;
-    for (int j = 0; j < d - 1; ++j) lines *= g.n[j];
+    for (int j = 0; j < d - 1; ++j) lines *= g.ext[j];
     k_fwd_last<T><<<grid_for(lines * ml, sms), kThreads, 0, s>>>(
-        reinterpret_cast<const T *>(bf.x), bufA, lines, (int)g.n[d - 1], (int)ml, p.tw[d - 1]);
+        reinterpret_cast<const T *>(bf.x), bufA, lines, (int)g.n[d - 1], (int)g.ext[d - 1],
+        (int)ml, p.tw[d - 1]);
     float2 *cur = bufA, *nxt = bufB;
     // a1, full axes from d-2 down to 0
     for (int a = d - 2; a >= 0; --a) {
         int64_t outer = p.batch * p.cin, inner = ml;
-        for (int j = 0; j < a; ++j) outer *= g.n[j];
+        for (int j = 0; j < a; ++j) outer *= g.ext[j];
         for (int j = a + 1; j < d - 1; ++j) inner *= g.kdim[j];
         k_fwd_full<<<grid_for(outer * g.kdim[a] * inner, sms), kThreads, 0, s>>>(
-            cur, nxt, outer, (int)g.n[a], inner, g.m[a], p.tw[a]);
+            cur, nxt, outer, (int)g.n[a], (int)g.ext[a], inner, g.m[a], p.tw[a]);
         std::swap(cur, nxt);
     }
     // a2, mixing
@@ -246,18 +253,18 @@ static cudaError_t unfused_forward_t(const Plan &p, const Buffers &bf, cudaStrea
     // a3, full axes 0..d-2
     for (int a = 0; a < d - 1; ++a) {
         int64_t outer = p.batch * p.cout, inner = ml;
-        for (int j = 0; j < a; ++j) outer *= g.n[j];
+        for (int j = 0; j < a; ++j) outer *= g.ext[j];
         for (int j = a + 1; j < d - 1; ++j) inner *= g.kdim[j];
-        k_inv_full<<<grid_for(outer * g.n[a] * inner, sms), kThreads, 0, s>>>(
-            cur, nxt, outer, (int)g.n[a], inner, g.m[a], p.tw[a]);
+        k_inv_full<<<grid_for(outer * g.ext[a] * inner, sms), kThreads, 0, s>>>(
+            cur, nxt, outer, (int)g.n[a], (int)g.ext[a], inner, g.m[a], p.tw[a]);
         std::swap(cur, nxt);
     }
-    // a3, last axis (half spectrum -> real), scale 1/prod(N)
+    // a3, last axis (half spectrum -> real), scale 1/prod(N) over the transform
     lines = p.batch * p.cout;
-    for (int j = 0; j < d - 1; ++j) lines *= g.n[j];
-    k_inv_last<T><<<grid_for(lines * g.n[d - 1], sms), kThreads, 0, s>>>(
-        cur, reinterpret_cast<T *>(bf.y), lines, (int)g.n[d - 1], (int)ml, p.tw[d - 1],
-        (float)(1.0 / (double)g.npix));
+    for (int j = 0; j < d - 1; ++j) lines *= g.ext[j];
+    k_inv_last<T><<<grid_for(lines * g.ext[d - 1], sms), kThreads, 0, s>>>(
+        cur, reinterpret_cast<T *>(bf.y), lines, (int)g.n[d - 1], (int)g.ext[d - 1], (int)ml,
+        p.tw[d - 1], (float)(1.0 / (double)g.ntr));
     return cudaGetLastError();
 }
 
@@ -267,13 +274,13 @@ int64_t unfused_modes_scratch_elems(const Geom &g, int64_t nch) {
     int64_t best = 0;
     if (d > 1) {
         int64_t s0 = nch * ml;
-        for (int j = 0; j < d - 1; ++j) s0 *= g.n[j];
+        for (int j = 0; j < d - 1; ++j) s0 *= g.ext[j];
         best = s0;
     }
     // outputs of the full-axis passes a = d-2 .. 1 (the pass a = 0 writes out)
     for (int a = d - 2; a >= 1; --a) {
         int64_t s = nch * ml;
-        for (int j = 0; j < d - 1; ++j) s *= (j < a) ? g.n[j] : g.kdim[j];
+        for (int j = 0; j < d - 1; ++j) s *= (j < a) ? g.ext[j] : g.kdim[j];
         best = std::max(best, s);
     }
     return best;
@@ -286,17 +293,17 @@ static cudaError_t forward_modes_t(const Plan &p, const T *x, int64_t nch, float
     const int d = g.d;
     const int64_t ml = g.m[d - 1];
     int64_t lines = nch;
-    for (int j = 0; j < d - 1; ++j) lines *= g.n[j];
+    for (int j = 0; j < d - 1; ++j) lines *= g.ext[j];
     float2 *cur = d == 1 ? out : sa;
     k_fwd_last<T><<<grid_for(lines * ml, p.num_sms), kThreads, 0, s>>>(
-        x, cur, lines, (int)g.n[d - 1], (int)ml, p.tw[d - 1]);
+        x, cur, lines, (int)g.n[d - 1], (int)g.ext[d - 1], (int)ml, p.tw[d - 1]);
     for (int a = d - 2; a >= 0; --a) {
         float2 *dst = a == 0 ? out : (cur == sa ? sb : sa);
         int64_t outer = nch, inner = ml;
-        for (int j = 0; j < a; ++j) outer *= g.n[j];
+        for (int j = 0; j < a; ++j) outer *= g.ext[j];
         for (int j = a + 1; j < d - 1; ++j) inner *= g.kdim[j];
         k_fwd_full<<<grid_for(outer * g.kdim[a] * inner, p.num_sms), kThreads, 0, s>>>(
-            cur, dst, outer, (int)g.n[a], inner, g.m[a], p.tw[a]);
+            cur, dst, outer, (int)g.n[a], (int)g.ext[a], inner, g.m[a], p.tw[a]);
         cur = dst;
     }
     return cudaGetLastError();
@@ -345,6 +352,9 @@ k_pack_weights(const T *__restrict__ w, T *__restrict__ wp, int cin, int cout, K
 
 cudaError_t launch_pack_weights(const Plan &p, const void *w, void *wp, cudaStream_t s) {
     const Geom &g = p.g;
+    if (p.mix_image)      // the tensor-core mixing's operand images
+        return mixtc_pack_image(p.dtype, w, wp, p.cin, p.cout, g.m[0], g.m[1], (int)g.mblk,
+                                (int)g.nkept, p.num_sms, s);
     KeptGeom kg;
     kg.d = g.d;
     for (int a = 0; a < FNO_MAX_NDIM; ++a) {
@@ -366,14 +376,14 @@ cudaError_t launch_pack_weights(const Plan &p, const void *w, void *wp, cudaStre
 cudaError_t launch_axis_forward(const float2 *in, float2 *out, int64_t outer, int n, int64_t inner,
                                 int m, const float2 *tw, int num_sms, cudaStream_t s) {
     k_fwd_full<<<grid_for(outer * 2 * m * inner, num_sms), kThreads, 0, s>>>(in, out, outer, n,
-                                                                           inner, m, tw);
+                                                                           n, inner, m, tw);
     return cudaGetLastError();
 }
 
 cudaError_t launch_axis_inverse(const float2 *in, float2 *out, int64_t outer, int n, int64_t inner,
                                 int m, const float2 *tw, int num_sms, cudaStream_t s) {
-    k_inv_full<<<grid_for(outer * n * inner, num_sms), kThreads, 0, s>>>(in, out, outer, n, inner,
-                                                                       m, tw);
+    k_inv_full<<<grid_for(outer * n * inner, num_sms), kThreads, 0, s>>>(in, out, outer, n, n,
+                                                                       inner, m, tw);
     return cudaGetLastError();
 }
 

@@ -82,11 +82,9 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * CTA of each kernel of the three-kernel variants (2-D and 3-D layers).
  * Costs a few timer reads, a barrier and a store per item.                  */
 #define FNO_PLAN_TRACE 2u
-/* Accepted for compatibility and without effect: the forward transform of
- * the float32 128x128 layer (16x16 modes) runs on the tensor cores by default
- * (each image's row DFT as a pipelined tcgen05 3xTF32 GEMM over TMA-staged
- * K chunks); FNO_PLAN_SIMT_TRANSFORM selects the register-FFT kernels.       */
-#define FNO_PLAN_TENSOR_CORES 4u
+/* Bit 4u is unused; a plan with it set is rejected (FNO_ERR_INVALID_ARG).
+ * The tensor-core kernels are the default wherever they exist, and
+ * FNO_PLAN_SIMT_TRANSFORM / FNO_PLAN_SIMT_MIX select the SIMT kernels.       */
 /* Run the float32 / fp16 128x128 layer as ONE persistent kernel with a work
  * queue instead of three kernels chained by programmatic dependent launch
  * (the default).  FNO_PLAN_TRACE records only this variant.               */
@@ -106,12 +104,13 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * 128x128 layer (16x16 modes) the forward transform and the inverse (3xTF32
  * GEMMs per image, TMA loads and stores).  An ablation switch.              */
 #define FNO_PLAN_SIMT_TRANSFORM 64u
-/* The weights passed to fno_spectral_conv_forward are in the packed
- * mode-major layout written by fno_spectral_conv_pack_weights (weights are
- * parameters: pack once per update, use many times).  Packed, every mixing
- * kernel reads a mode group's Cin x Cout weights as one contiguous run instead
- * of 16-byte pieces strided by the mode count.  Requires |K| % 4 == 0; not
- * combinable with FNO_PLAN_BACKWARD.                                        */
+/* The weights passed to fno_spectral_conv_forward are in the packed layout
+ * written by fno_spectral_conv_pack_weights (weights are parameters: pack once
+ * per update, use many times).  Packed, every mixing kernel reads a mode's (or
+ * a group of four modes') Cin x Cout weights as one contiguous run instead of
+ * pieces strided by the mode count; the tensor-core mixing of the 64-channel
+ * 16-bit 2-D layers reads them as ready operand images.  Requires
+ * |K| % 4 == 0; not combinable with FNO_PLAN_BACKWARD.                      */
 #define FNO_PLAN_PACKED_WEIGHTS 128u
 
 /* One work item of the fused kernel, as recorded under FNO_PLAN_TRACE.
@@ -138,7 +137,10 @@ int fno_version(void);
  * ------------------------------------------------------------------------- */
 
 /* Validate a layer description and report its memory needs without touching
- * the GPU (no CUDA call is made).
+ * the GPU (no CUDA call is made).  The layer is the one of the TurboFNO
+ * article §2.1-§2.3 (forward real FFT, kept modes, per-mode mixing, inverse
+ * real FFT); its sizes are fixed here, ahead of any call, as §2.3 and §3.3
+ * ask of the fused module (compile-time output size).
  *   ndim          1, 2 or 3
  *   n[ndim]       spatial extents, 2 <= N <= 4096 (any length: extents
  *                 that are not powers of two, and shapes without a fused
@@ -157,7 +159,9 @@ fno_status_t fno_spectral_conv_query(int ndim, const int64_t *n, const int32_t *
                                      fno_dtype_t dtype, uint32_t flags,
                                      size_t *workspace_bytes, size_t *weight_bytes);
 
-/* Create a plan on the current CUDA device.  Arguments as in
+/* Create a plan on the current CUDA device (TurboFNO §2.3, §3.3: every size
+ * and table fixed before the first forward, so the forward is a fixed launch
+ * sequence that a CUDA graph can hold).  Arguments as in
  * fno_spectral_conv_query.  The plan computes its twiddle tables on the host
  * in double precision, rounds them once to float and copies them to
  * plan-owned device memory; it synchronises the device once, here, and is
@@ -167,13 +171,48 @@ fno_status_t fno_spectral_conv_plan(fno_plan_t *plan, int ndim, const int64_t *n
                                     const int32_t *modes, int64_t batch, int32_t cin,
                                     int32_t cout, fno_dtype_t dtype, uint32_t flags);
 
-/* Bytes of device workspace fno_spectral_conv_forward needs for this plan. */
+/* The layer on a non-periodic domain (TurboFNO §2.3: the input is zero-padded
+ * so that the transform sees no wrap-around, and the output is cropped back
+ * to the original size; §3.3: the crop is a guarded store in the inverse's
+ * final stage, not an extra copy or kernel).
+ *   n[ndim]    extents of x and y (1 <= n[a] <= 4096)
+ *   pad[ndim]  zeros appended after the last sample of each axis (>= 0);
+ *              the transform of axis a runs over L_a = n[a] + pad[a] <= 4096
+ *              points and `modes` are counted on L (2 m_a <= L_a on full
+ *              axes, m_{d-1} <= L_{d-1}/2 + 1); NULL or all zeros is the
+ *              periodic layer of fno_spectral_conv_plan
+ * x stays (batch, cin, n...) and y (batch, cout, n...): the forward reads x
+ * as if extended with zeros and writes only the first n[a] samples of the
+ * inverse along each axis (scale 1/prod(L)).  A padded plan runs on the
+ * separate per-axis kernels (FNO_PLAN_UNFUSED is implied) and takes the
+ * weights of the L-sized layer; FNO_PLAN_BACKWARD is not supported with
+ * padding (FNO_ERR_UNSUPPORTED).  Other arguments, ownership and errors as in
+ * fno_spectral_conv_query / fno_spectral_conv_plan; the plan is used with
+ * fno_spectral_conv_workspace_size, _kernel_count, _forward,
+ * _pack_weights and fno_plan_destroy like any other.                       */
+fno_status_t fno_spectral_conv_query_padded(int ndim, const int64_t *n, const int64_t *pad,
+                                            const int32_t *modes, int64_t batch, int32_t cin,
+                                            int32_t cout, fno_dtype_t dtype, uint32_t flags,
+                                            size_t *workspace_bytes, size_t *weight_bytes);
+fno_status_t fno_spectral_conv_plan_padded(fno_plan_t *plan, int ndim, const int64_t *n,
+                                           const int64_t *pad, const int32_t *modes,
+                                           int64_t batch, int32_t cin, int32_t cout,
+                                           fno_dtype_t dtype, uint32_t flags);
+
+/* Bytes of device workspace fno_spectral_conv_forward needs for this plan:
+ * the kept modes handed between the fused kernel's phases (TurboFNO §3.4
+ * keeps them on chip; here they pass through an L2-resident buffer). */
 fno_status_t fno_spectral_conv_workspace_size(fno_plan_t plan, size_t *bytes);
 
-/* Number of kernels one forward call launches for this plan. */
+/* Number of kernels one forward call launches for this plan (TurboFNO §1
+ * and §3.4 speak of one fused kernel and of three kernels per forward; the
+ * §5.2 note times the separate-kernels arrangement). */
 fno_status_t fno_spectral_conv_kernel_count(fno_plan_t plan, int *count);
 
-/* y = SpectralConv(x; w), enqueued on `stream`.
+/* y = SpectralConv(x; w), enqueued on `stream`: TurboFNO §2.1 (forward real
+ * FFT, truncated), §2.2 (per-mode complex mixing), §2.3 / §3.3 (zero-padded
+ * inverse real FFT), fused as §3.4 describes, behind the raw-pointer C
+ * function of §4.3.
  *   x          device, (batch, cin, N_0..N_{d-1}) storage dtype
  *   w          device, (nblk, cin, cout, m_0..m_{d-1}) complex storage dtype,
  *              block order as described at the top of this header
@@ -214,19 +253,33 @@ fno_status_t fno_spectral_conv_forward(fno_plan_t plan, const void *x, const voi
  * stream capture.  Every call shares the one scratch array, which keeps the
  * last call's contents; none of it has to start at zero.  Calls that overlap
  * on the GPU (different streams) race on the scratch and give wrong results;
- * calls on one stream are safe.  Runs the separate-kernels path (the kernels of
- * FNO_PLAN_UNFUSED).  Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, ALIASING,
- * CUDA.                                                                     */
+ * calls on one stream are safe.  The looked-up addresses are kept for the life
+ * of the process: after a cudaDeviceReset of a device (which discards the
+ * arrays) this call must not be used on that device again.  Runs the
+ * separate-kernels path (the kernels of FNO_PLAN_UNFUSED).  Errors:
+ * INVALID_ARG, UNSUPPORTED, MISALIGNED, ALIASING (y overlaps x or w, or an
+ * operand lies inside the library's scratch array), CUDA.                   */
 fno_status_t fno_spectral_conv_forward_static(int ndim, const int64_t *n,
                                               const int32_t *modes, int64_t batch,
                                               int32_t cin, int32_t cout, fno_dtype_t dtype,
                                               const void *x, const void *w, void *y,
                                               fno_stream_t stream);
 
-/* Write w (nblk, Cin, Cout, m...) in the packed layout of the plan's storage
- * type: w_packed[(q * Cin + i) * Cout + o][r] = W of kept mode k = 4 q + r
- * (kept modes in the order of the layer's kept-mode index: axis by axis, low
- * rows then high rows on full axes), interleaved complex; same size as w.
+/* Re-lay the learned weights out once per weight update (TurboFNO §2.2: one
+ * complex Cin x Cout weight per mode; §3.2: the GEMM stage takes its weights
+ * in the tensor-core operand layout rather than the framework's).
+ * Write w (nblk, Cin, Cout, m...) in the packed layout of the plan; same size
+ * as w.  Kept modes are numbered in the order of the layer's kept-mode index:
+ * axis by axis, low rows then high rows on full axes.  Two layouts:
+ *  - the tensor-core mixing's operand images, for 2-D fp16 / bf16 layers with
+ *    Cin = Cout = 64 whose mixing runs on the tensor cores (the 256 x 256,
+ *    32 x 32-mode layer): per kept mode k, 16 KiB = two 64 x 64 tiles of the
+ *    storage type, Wr^T then Wi^T (row o, column i holds W[i][o]), each row
+ *    128 bytes whose eight 16-byte pieces are permuted by p -> p ^ (o % 8)
+ *    (the 128-byte swizzle of the tensor cores' shared-memory operands); a
+ *    mixing CTA reads a mode's weights with one bulk copy;
+ *  - otherwise mode-major groups of four: w_packed[(q * Cin + i) * Cout + o][r]
+ *    = W of kept mode k = 4 q + r, interleaved complex.
  * For plans made with FNO_PLAN_PACKED_WEIGHTS.  Asynchronous on `stream`.
  * Errors: INVALID_ARG (NULL, plan without the flag), MISALIGNED, ALIASING
  * (w and w_packed overlap), CUDA.                                           */
@@ -234,7 +287,8 @@ fno_status_t fno_spectral_conv_pack_weights(fno_plan_t plan, const void *w, void
                                             fno_stream_t stream);
 
 /* Gradients of the layer for a real loss L, given dy = dL/dy (B, Cout, N...)
- * in the storage dtype.  The pages define only the forward pass; this is its
+ * in the storage dtype: the backward of the autograd function that TurboFNO
+ * §4.3 wraps around the fused layer.  The pages define only the forward pass; this is its
  * derivative, with dz = dL/dRe(z) + i dL/dIm(z) for a complex z:
  *   dY = c(k_last) / prod(N) * (truncated forward DFT of dy),
  *   dx = the layer applied to dy with the weights W'[blk][o][i] =
@@ -254,7 +308,8 @@ fno_status_t fno_spectral_conv_backward(fno_plan_t plan, const void *x, const vo
                                         fno_stream_t stream);
 
 /* Copy the trace of the plan's last forward call (FNO_PLAN_TRACE) to host
- * memory: up to `capacity` records, ordered by ticket (three-kernel variants:
+ * memory (the per-phase timeline TurboFNO §1 reads from a kernel launch
+ * trace): up to `capacity` records, ordered by ticket (three-kernel variants:
  * kernel A's CTAs, then B's, then C's); *count receives the number of records
  * the call produced.  Synchronises the device.  Returns FNO_ERR_INVALID_ARG if
  * the plan was made without FNO_PLAN_TRACE or runs a path that records none
@@ -262,11 +317,14 @@ fno_status_t fno_spectral_conv_backward(fno_plan_t plan, const void *x, const vo
 fno_status_t fno_plan_get_trace(fno_plan_t plan, fno_trace_record_t *records, size_t capacity,
                                 size_t *count);
 
-/* Synchronise `stream`, then read and clear the plan's device error word.
+/* Synchronise `stream`, then read and clear the plan's device error word
+ * (TurboFNO §6.1 traces a crash to an unchecked device index; faults found on
+ * the device are reported here instead of trapping).
  * Returns FNO_OK, FNO_ERR_DEVICE_TIMEOUT, FNO_ERR_DEVICE_BOUNDS or CUDA.   */
 fno_status_t fno_plan_get_device_error(fno_plan_t plan, fno_stream_t stream);
 
-/* Self-test of the bounded device waits.  Launches one CTA on `stream` that
+/* Self-test of the bounded device waits (the waits of the fused kernels of
+ * TurboFNO §3.4 between their phases).  Launches one CTA on `stream` that
  * waits for something no one will do -- which = 0: a flag word in the plan's
  * memory that no kernel writes (the wait CTAs of one launch use for each
  * other's phases); which = 1: phase 0 of an mbarrier nothing arrives on (the
@@ -277,7 +335,7 @@ fno_status_t fno_plan_get_device_error(fno_plan_t plan, fno_stream_t stream);
  * (NULL plan, `which` not 0 or 1), CUDA (launch failed).                    */
 fno_status_t fno_plan_check_bounded_wait(fno_plan_t plan, int which, fno_stream_t stream);
 
-/* Release the plan and its device memory.  NULL is accepted (no-op).  The
+/* Release the plan and its device memory (the plan of TurboFNO §2.3).  NULL is accepted (no-op).  The
  * caller must make sure no work that uses the plan is still running.       */
 fno_status_t fno_plan_destroy(fno_plan_t plan);
 
@@ -319,20 +377,24 @@ typedef struct fno_model_params_s {
 } fno_model_params_t;
 
 /* Validate the description and create the stack's plan (one spectral plan
- * shared by the layers).  Errors as for fno_spectral_conv_plan; also
+ * shared by the layers; TurboFNO §2.1 runs the layer inside a multi-layer
+ * operator, §5 on 128 x 128 tasks).  Errors as for fno_spectral_conv_plan; also
  * INVALID_ARG for an unknown dtype, UNSUPPORTED for cout > 8,
  * batch > 65535, or h*w not a multiple of 4.  The 1x1 linears run on the
  * tensor cores (3xTF32) for float32 storage where the channel counts fit one
  * tile, else as register-tiled float32 GEMMs.                               */
 fno_status_t fno_model_plan(fno_model_t *model, const fno_model_desc_t *desc);
 
-/* Device workspace bytes fno_forward needs (activations + layer scratch).  */
+/* Device workspace bytes fno_forward needs (activations + layer scratch;
+ * TurboFNO §2.1). */
 fno_status_t fno_model_workspace_size(fno_model_t model, size_t *bytes);
 
-/* Number of kernels one fno_forward call launches. */
+/* Number of kernels one fno_forward call launches (TurboFNO §2.1 counts the
+ * launches of a multi-layer operator). */
 fno_status_t fno_model_kernel_count(fno_model_t model, int *count);
 
-/* out = FNO(x), enqueued on `stream`.
+/* out = FNO(x), enqueued on `stream` (TurboFNO §2.1: the spectral layer inside
+ * an FNO; §2.3: capturable as one CUDA graph).
  *   x    device, (batch, cin_lift, h, w) in the storage dtype
  *   p    host struct of device pointers (all 16-byte aligned)
  *   out  device, (batch, cout, h, w) in the storage dtype; must not overlap
@@ -342,10 +404,11 @@ fno_status_t fno_model_kernel_count(fno_model_t model, int *count);
 fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_params_t *p,
                          void *out, void *workspace, fno_stream_t stream);
 
-/* Synchronise `stream`, read and clear the device error word of the stack. */
+/* Synchronise `stream`, read and clear the device error word of the stack
+ * (as fno_plan_get_device_error, TurboFNO §6.1). */
 fno_status_t fno_model_get_device_error(fno_model_t model, fno_stream_t stream);
 
-/* Release the stack's plan; NULL is accepted. */
+/* Release the stack's plan; NULL is accepted (TurboFNO §2.1). */
 fno_status_t fno_model_destroy(fno_model_t model);
 
 #ifdef __cplusplus

@@ -89,6 +89,9 @@ def test_query_rejects(L, args, code):
 def test_query_rejects_unknown_flags_and_nulls(L):
     st, _, _ = Q(1, [16], [4], 1, 1, 1, F32, flags=0x1000)
     assert st == capi.FNO_ERR_INVALID_ARG
+    # bit 4 (a former tensor-core switch that did nothing) is not a flag
+    st, _, _ = Q(2, [128, 128], [16, 16], 8, 32, 32, F32, flags=4)
+    assert st == capi.FNO_ERR_INVALID_ARG
     import ctypes
     assert L.fno_spectral_conv_query(1, None, None, 1, 1, 1, 0, 0, None, None) == \
         capi.FNO_ERR_INVALID_ARG
@@ -166,3 +169,27 @@ def test_packed_weights_flag_validation(L):
     assert Q(2, [32, 32], [4, 4], 1, 3, 5, F32, flags=P)[2] == \
         Q(2, [32, 32], [4, 4], 1, 3, 5, F32)[2]
     assert capi.fno_spectral_conv_pack_weights(None, None, None, None) == capi.FNO_ERR_INVALID_ARG
+
+
+def test_padded_query_validation(L):
+    QP = capi.fno_spectral_conv_query_padded
+    # modes are counted on the padded transform length: 2 m <= n + pad
+    assert QP(1, [12], [4], [8], 1, 2, 2, F32)[0] == capi.FNO_OK          # m <= 16/2 + 1
+    assert QP(1, [12], [4], [10], 1, 2, 2, F32)[0] == capi.FNO_ERR_INVALID_ARG
+    assert QP(2, [6, 10], [2, 6], [4, 9], 1, 2, 2, F32)[0] == capi.FNO_OK
+    assert QP(2, [6, 10], [1, 6], [4, 9], 1, 2, 2, F32)[0] == capi.FNO_ERR_INVALID_ARG
+    assert QP(1, [12], [-1], [4], 1, 2, 2, F32)[0] == capi.FNO_ERR_INVALID_ARG
+    assert QP(1, [4000], [200], [4], 1, 2, 2, F32)[0] == capi.FNO_ERR_UNSUPPORTED
+    # an extent of one sample is fine once padded; the backward is not offered
+    assert QP(1, [1], [7], [3], 1, 2, 2, F32)[0] == capi.FNO_OK
+    assert QP(1, [12], [4], [4], 1, 2, 2, F32,
+              flags=capi.FNO_PLAN_BACKWARD)[0] == capi.FNO_ERR_UNSUPPORTED
+    # NULL or zero padding is the periodic layer, with the same sizes
+    a = QP(2, [128, 128], None, [16, 16], 8, 32, 32, F32)
+    b = QP(2, [128, 128], [0, 0], [16, 16], 8, 32, 32, F32)
+    c = Q(2, [128, 128], [16, 16], 8, 32, 32, F32)
+    assert a == b == c
+    # a padded layer runs on the separate kernels: its workspace is theirs
+    d = QP(2, [100, 120], [28, 8], [16, 16], 8, 32, 32, F32)
+    e = Q(2, [128, 128], [16, 16], 8, 32, 32, F32, flags=capi.FNO_PLAN_UNFUSED)
+    assert d[0] == capi.FNO_OK and d[1] <= e[1] and d[2] == e[2]

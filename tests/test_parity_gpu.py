@@ -67,10 +67,9 @@ def _lib(fno, oracle_mod):
     yield
 
 
-@pytest.mark.parametrize("flags", [0, FNO_PLAN_UNFUSED, capi.FNO_PLAN_TENSOR_CORES,
-                                   capi.FNO_PLAN_PERSISTENT, capi.FNO_PLAN_SIMT_MIX,
-                                   capi.FNO_PLAN_SIMT_TRANSFORM],
-                         ids=["default", "unfused", "tensor_cores", "persistent", "simt_mix",
+@pytest.mark.parametrize("flags", [0, FNO_PLAN_UNFUSED, capi.FNO_PLAN_PERSISTENT,
+                                   capi.FNO_PLAN_SIMT_MIX, capi.FNO_PLAN_SIMT_TRANSFORM],
+                         ids=["default", "unfused", "persistent", "simt_mix",
                               "simt_transform"])
 @pytest.mark.parametrize("spec", SMALL, ids=[case_id(c) for c in SMALL])
 def test_small_cases_match_oracle(spec, flags):
@@ -228,6 +227,8 @@ PACKED_CASES = [
     ((128, 128), (16, 16), 2, 6, 5, "f32"),        # three-kernel 128^2
     ((128, 128), (16, 16), 2, 6, 5, "f32", capi.FNO_PLAN_PERSISTENT),
     ((256, 256), (32, 32), 2, 3, 5, "f16"),        # tensor-core mixing
+    ((256, 256), (32, 32), 3, 64, 64, "f16"),      # ... weights as operand images
+    ((256, 256), (32, 32), 2, 64, 64, "bf16"),
     ((256, 256), (32, 32), 1, 4, 4, "bf16", capi.FNO_PLAN_SIMT_MIX),
     ((64, 64, 64), (16, 16, 16), 1, 3, 2, "f32"),  # 3-D
     ((16, 32), (3, 8), 2, 3, 5, "f32"),            # separate kernels
@@ -339,3 +340,48 @@ def test_trace_records_every_item():
     st, _ = capi.fno_plan_get_trace(SpectralConv((16,), (4,), 1, 1, 1).handle)
     assert st == capi.FNO_ERR_INVALID_ARG
     conv.close()
+
+
+PADDED = [
+    # (n, pad, modes, batch, cin, cout, dtype): the layer on a zero-padded,
+    # cropped domain against the oracle's plain pad -> layer -> crop
+    ((12,), (4,), (4,), 2, 3, 5, "f32"),
+    ((250,), (6,), (16,), 3, 4, 4, "f32"),            # padded to a power of two
+    ((10,), (5,), (5,), 2, 2, 3, "f32"),              # odd transform length, no Nyquist
+    ((6,), (2,), (5,), 1, 3, 2, "f32"),               # Nyquist bin kept
+    ((100, 120), (28, 8), (16, 16), 2, 8, 6, "f32"),  # 2-D, L = 128 x 128
+    ((6, 10), (2, 6), (2, 6), 2, 3, 2, "f16"),
+    ((5, 7), (3, 1), (3, 2), 2, 2, 3, "bf16"),
+    ((30, 20, 12), (2, 12, 4), (8, 8, 5), 1, 3, 4, "f32"),   # 3-D, L = 32^3 x 16
+]
+
+
+@pytest.mark.parametrize("spec", PADDED, ids=[f"{'x'.join(map(str, c[0]))}_p"
+                                               f"{'x'.join(map(str, c[1]))}_{c[6]}"
+                                              for c in PADDED])
+def test_padded_layer_matches_oracle(spec):
+    n, pad, modes, b, ci, co, dt = spec
+    L = tuple(a + p for a, p in zip(n, pad))
+    case = workloads.small_case(n, modes, b, ci, co, dt, index=9)
+    wcase = workloads.small_case(L, modes, b, ci, co, dt, index=9)
+    x = workloads.make_x(case, seed=300 + sum(n))
+    w = workloads.make_w(wcase, seed=400 + sum(pad))
+    conv = SpectralConv(n, modes, b, ci, co, dt, pad=pad)
+    assert conv.kernel_count == 2 * len(n) + 1              # the separate kernels
+    y = torch.full((b, co) + n, float("nan"), device="cuda").to(conv.torch_dtype)
+    conv(to_dev(x, dt), to_dev(w, dt), y)
+    torch.cuda.synchronize()
+    assert conv.device_error() == 0
+    conv.close()
+    ref = oracle.spectral_conv_padded(x.astype(np.float64), workloads.as_complex(w), modes, pad)
+    assert_close(y.float().cpu().numpy(), ref, dt, f"padded {spec}")
+
+
+def test_padded_zero_pad_equals_periodic_plan():
+    case = workloads.small_case((64, 64), (8, 8), 2, 4, 4, "f32", index=9)
+    x, w = workloads.make_x(case, seed=5), workloads.make_w(case, seed=6)
+    a, _ = run_gpu(case, x, w, FNO_PLAN_UNFUSED)
+    conv = SpectralConv(case.n, case.modes, 2, 4, 4, "f32", pad=(0, 0))
+    b = conv(to_dev(x), to_dev(w)).cpu().numpy()
+    conv.close()
+    assert np.array_equal(a, b)
