@@ -458,6 +458,11 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
             // kept modes: X[j][k] = sum_t1 W_N0^{g t1} F[t1][g mod G1][k], g the signed
             // frequency of kept row j (j, or j - K0 for the high rows)
             float2 *dst = a.part + (size_t)img * Gm::NK;
+            // with the tensor-core mixing, mode o leaves as a 16-bit (re, im) pair in
+            // group o / 8 of the mixing's input: [group][image][8 modes], so a
+            // warp's 32 modes fill four whole 32-byte pieces
+            uint32_t *xg = reinterpret_cast<uint32_t *>(a.part) + (size_t)img * 8;
+            const size_t gstride = (size_t)a.batch * a.cin * 8;     // words per group
             for (int o = tid; o < Gm::NK; o += NT) {
                 const int j = o / Gm::M1, k = o % Gm::M1;
                 const int g = j < Gm::M0 ? j : j - Gm::K0, g1 = j & (Gm::G1 - 1);
@@ -466,7 +471,19 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
                 for (int t1 = 0; t1 < Gm::T1; ++t1)
                     cmac(accv, F[(t1 * Gm::G1 + g1) * Gm::M1 + k],
                          __ldg(a.tw0 + ((g * t1) & (Gm::N0 - 1))));
-                __stcg(dst + o, accv);
+                if (a.mix16) {
+                    uint32_t u;             // re in the low half, im in the high half
+                    if constexpr (std::is_same<T, __half>::value) {
+                        const __half2 h = __floats2half2_rn(accv.x, accv.y);
+                        memcpy(&u, &h, 4);
+                    } else {
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(accv.x, accv.y);
+                        memcpy(&u, &h, 4);
+                    }
+                    xg[(o >> 3) * gstride + (o & 7)] = u;
+                } else {
+                    __stcg(dst + o, accv);
+                }
             }
             consumer_sync();                     // F is read: the next Z goes over it
             if (a.trace && tid == 0) {
@@ -1087,9 +1104,20 @@ struct Pdl {
         const size_t w2 = dt == FNO_F32 ? 16 : 8;
         return ((size_t)cin * ob * w2 + 15) / 16 * 16 + (size_t)np * bb * cin * 16;
     }
-    static size_t part_bytes(const Geom &g, int64_t batch, int cin, fno_dtype_t dt,
+    // the mixing runs on the tensor cores (kernel A then writes 16-bit operand
+    // images of the kept modes, kernel B 16-bit mixed modes)
+    static bool mix16(const Geom &g, fno_dtype_t dt, int64_t batch, int cin, int cout,
+                      uint32_t flags) {
+        return dt != FNO_F32 && use_tca(dt, flags) && parts(dt, flags) == 1 &&
+               !(flags & FNO_PLAN_SIMT_MIX) &&
+               mixtc_supported(g.d, dt, batch, cin, cout, Cf::M1, g.nkept);
+    }
+    static size_t part_bytes(const Geom &g, int64_t batch, int cin, int cout, fno_dtype_t dt,
                              uint32_t flags) {
-        return (size_t)parts(dt, flags) * batch * cin * g.nkept * sizeof(float2);
+        const size_t f32 = (size_t)parts(dt, flags) * batch * cin * g.nkept * sizeof(float2);
+        const size_t x16 = mix16(g, dt, batch, cin, cout, flags)
+                               ? mixtc_x_bytes(batch, cin, g.nkept) : 0;
+        return f32 > x16 ? f32 : x16;
     }
     template <typename T, int NP>
     static void *kernel_b() {
@@ -1112,7 +1140,10 @@ struct Pdl {
         if (e == cudaSuccess)
             e = raise_smem_limit(k_phase_c<CfC, T>, (int)sc);
         if constexpr (!std::is_same<T, float>::value || Cf::N0 == 128) {
-            p.fused_tcc = use_tcc(p.dtype, p.flags);
+            // the 16-bit inverse kernel reads the tensor-core mixing's 16-bit output
+            p.fused_tcc = use_tcc(p.dtype, p.flags) &&
+                          (p.dtype == FNO_F32 ||
+                           mix16(p.g, p.dtype, p.batch, p.cin, p.cout, p.flags));
             if (e == cudaSuccess && (p.fused_tca || p.fused_tcc) && !tcu::encoder())
                 e = cudaErrorNotSupported;
             std::vector<unsigned char> img, imgc;
@@ -1159,9 +1190,7 @@ struct Pdl {
         p.fused_smem = sb;             // kernel B's; A and C use their fixed sizes
         p.fused_grid = 0;
         // tensor-core mixing where the kept modes arrive reduced (one copy)
-        p.fused_mixtc = np == 1 && !(p.flags & FNO_PLAN_SIMT_MIX) &&
-                        mixtc_supported(p.g.d, p.dtype, p.batch, p.cin, p.cout, Cf::M1,
-                                        p.g.nkept);
+        p.fused_mixtc = mix16(p.g, p.dtype, p.batch, p.cin, p.cout, p.flags);
         if (e == cudaSuccess && p.fused_mixtc) e = mixtc_init(p.dtype);
         p.mix_image = p.fused_mixtc && (p.flags & FNO_PLAN_PACKED_WEIGHTS) &&
                       mixtc_image_layout(p.cin, p.cout);
@@ -1364,8 +1393,8 @@ size_t fused_workspace_bytes(const Geom &g, fno_dtype_t dtype, int64_t batch, in
     if (v == kVarPdl3d) return fused3d_workspace_bytes(g, batch, cin, cout);
     if (v == kVarOne1d) return 0;
     if (v == kVarPersistent128) return layout(g, batch, cin, cout).total;
-    const size_t part = v == kVarPdl256 ? Pdl<Cfg256>::part_bytes(g, batch, cin, dtype, flags)
-                                        : Pdl128::part_bytes(g, batch, cin, dtype, flags);
+    const size_t part = v == kVarPdl256 ? Pdl<Cfg256>::part_bytes(g, batch, cin, cout, dtype, flags)
+                                        : Pdl128::part_bytes(g, batch, cin, cout, dtype, flags);
     const size_t y = (size_t)batch * cout * g.nkept * sizeof(float2);
     return ((part + 255) & ~size_t(255)) + ((y + 255) & ~size_t(255));
 }
@@ -1450,13 +1479,14 @@ cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
 
     if (v == kVarPdl128 || v == kVarPdl256) {
         const size_t part = v == kVarPdl256
-                                ? Pdl<Cfg256>::part_bytes(p.g, p.batch, p.cin, p.dtype, p.flags)
-                                : Pdl128::part_bytes(p.g, p.batch, p.cin, p.dtype, p.flags);
+                                ? Pdl<Cfg256>::part_bytes(p.g, p.batch, p.cin, p.cout, p.dtype, p.flags)
+                                : Pdl128::part_bytes(p.g, p.batch, p.cin, p.cout, p.dtype, p.flags);
         Args a{};
         a.x = b.x;
         a.w = b.w;
         a.y = b.y;
         a.wpacked = (p.flags & FNO_PLAN_PACKED_WEIGHTS) ? 1 : 0;
+        a.mix16 = p.fused_mixtc ? 1 : 0;
         a.part = static_cast<float2 *>(b.ws);
         a.Y = reinterpret_cast<float2 *>(static_cast<char *>(b.ws) + ((part + 255) & ~size_t(255)));
         a.tw0 = p.tw[0];

@@ -35,9 +35,10 @@ cudaError_t fused3d_forward_modes(const Plan &p, const void *x, int64_t nimg, fl
 // Tensor-core mixing (kernel B of the three-kernel 2-D path) for 16-bit
 // storage: four adjacent modes per CTA, real-block complex GEMMs on tcgen05.
 struct MixTcArgs {
-    const float2 *X;              // kept modes [batch * cin][nk]
+    const void *X;                // kept modes: [group of 8 modes][batch * cin][8] 16-bit
+                                  // (re, im) pairs, as kernel A writes them (mixtc_x_bytes)
     const void *w;                // weights (2, cin, cout, m0, m1) interleaved complex
-    float2 *Y;                    // mixed modes [batch * cout][nk]
+    void *Y;                      // mixed modes [batch * cout][nk] as 16-bit (re, im) pairs
     int *err;
     fno_trace_record_t *trace;    // nullptr unless tracing
     int trace_first;
@@ -46,6 +47,10 @@ struct MixTcArgs {
 };
 bool mixtc_supported(int d, fno_dtype_t dtype, int64_t batch, int cin, int cout, int m1,
                      int64_t nkept);
+// Bytes of the kept modes in the tensor-core mixing's input layout: kept mode
+// kk of image img = b * cin + i is the 16-bit (re, im) pair at byte
+// ((kk / 8) * batch * cin + img) * 32 + (kk % 8) * 4.
+size_t mixtc_x_bytes(int64_t batch, int cin, int64_t nkept);
 int mixtc_items(int64_t nkept);
 cudaError_t mixtc_init(fno_dtype_t dtype);
 cudaError_t mixtc_launch(fno_dtype_t dtype, const MixTcArgs &args, cudaStream_t s);
@@ -59,7 +64,7 @@ cudaError_t mixtc_pack_image(fno_dtype_t dtype, const void *w, void *wp, int cin
 // Kernel C of the 16-bit 256 x 256 layer (fno_inv16.cu): the column and row
 // inverse DFTs of each output image as two tcgen05 GEMMs, persistent.
 struct Inv16Args {
-    const float2 *Y;              // mixed modes [nimg][64 kept rows][32 bins]
+    const void *Y;                // mixed modes [nimg][64 kept rows][32 bins], 16-bit (re, im)
     void *y;                      // output images [nimg][256][256], storage type
     int *err;
     fno_trace_record_t *trace;    // nullptr unless tracing: one record per image

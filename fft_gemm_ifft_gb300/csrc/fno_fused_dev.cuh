@@ -761,6 +761,9 @@ struct Args {
     int ob, nob;        // phase B: outputs per item, output blocks
     int trace_b, trace_c;   // three-kernel variants: first trace record of kernel B, C
     int wpacked;            // w is in the packed mode-major layout
+    int mix16;              // 16-bit layer mixing on the tensor cores: the kept modes
+                            // leave kernel A as per-mode 16-bit operand images (mix16_x)
+                            // and the mixed modes leave kernel B as 16-bit pairs
 };
 
 __device__ __forceinline__ unsigned long long trace_now() {

@@ -3,7 +3,8 @@
 // (gsyq.cn/news/457482) §2.3 / §3.3, as two tensor-core GEMMs per output image
 // in one persistent kernel.
 //
-// For an output image (b, o) the mixed modes V[j][k] (kept row j = 0..63 with
+// For an output image (b, o) the mixed modes V[j][k] (16-bit (re, im) pairs from
+// the tensor-core mixing; kept row j = 0..63 with
 // the signed frequency g = j for j < 32 and j - 64 otherwise, bin k = 0..31)
 // give
 //   column inverse  Zo[t][k] = sum_j V[j][k] e^{+2 pi i g t / 256}     (t = 0..255)
@@ -47,8 +48,9 @@ constexpr uint32_t kOffE = 0;                     // [tile 2][chunk 2] GEMM-1 A,
 constexpr uint32_t kOffT = kOffE + 4 * kTile;     // GEMM-2 B: 256 rows x 128 B, 32 KiB
 constexpr uint32_t kOffB1 = kOffT + 2 * kTile;    // GEMM-1 B: [chunk 2][64 rows], 16 KiB
 constexpr uint32_t kOffA2 = kOffB1 + kTile;       // GEMM-2 A: [tile 2], 32 KiB
-constexpr uint32_t kOffY = kOffA2 + 2 * kTile;    // mixed modes of one image (float2), 16 KiB
-constexpr uint32_t kOffS = kOffY + kNK * 8;       // staging ring: 4 boxes of 128 x 64, 64 KiB
+constexpr uint32_t kOffY = kOffA2 + 2 * kTile;    // mixed modes of one image, 16-bit pairs, 8 KiB
+constexpr uint32_t kYBytes = kNK * 4;
+constexpr uint32_t kOffS = kOffY + kYBytes;       // staging ring: 4 boxes of 128 x 64, 64 KiB
 constexpr uint32_t kSmem = kOffS + 4 * kTile + 1024;
 constexpr uint32_t kTablesBytes = 6 * kTile;      // E then T, as they sit in shared memory
 constexpr uint32_t kTmemCols = 512;
@@ -109,7 +111,7 @@ k_inv16(const __grid_constant__ CUtensorMap ymap, Inv16Args a, const void *table
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t sbase = tc_smem_addr(base);
-    const float2 *ys = reinterpret_cast<const float2 *>(base + kOffY);
+    const uint32_t *ys = reinterpret_cast<const uint32_t *>(base + kOffY);   // (re, im) pairs
     if (tid == 0) {
         uint64_t *bars[5] = {&bar_t, &bar_y, &bar_m1, &bar_m2a, &bar_m2b};
         for (int i = 0; i < 5; ++i)
@@ -130,7 +132,8 @@ k_inv16(const __grid_constant__ CUtensorMap ymap, Inv16Args a, const void *table
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");   // kernel B's mixed modes are complete
     if (tid == 0 && (int)blockIdx.x < nimg)
-        bulk_load(sbase + kOffY, a.Y + (size_t)blockIdx.x * kNK, kNK * 8, &bar_y);
+        bulk_load(sbase + kOffY, static_cast<const char *>(a.Y) + (size_t)blockIdx.x * kYBytes,
+                  kYBytes, &bar_y);
     bool ok = mbar_wait(&bar_t, 0, a.err);
     constexpr uint32_t id1 = idesc_f16(64, Kind<T>::kBf16);
     constexpr uint32_t id2 = idesc_f16(256, Kind<T>::kBf16);
@@ -145,14 +148,14 @@ k_inv16(const __grid_constant__ CUtensorMap ymap, Inv16Args a, const void *table
         // 1. GEMM-1 B operand from the mixed modes: thread (k, group of 8 kept rows)
         {
             const int k = lane, j0 = 8 * warp;
-            float2 v[8];
+            uint32_t v[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) v[u] = ys[(j0 + u) * kM + k];
             uint32_t re[4], nim[4], im[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                re[q] = pack_pair<T>(v[2 * q].x, v[2 * q + 1].x);
-                im[q] = pack_pair<T>(v[2 * q].y, v[2 * q + 1].y);
+                re[q] = __byte_perm(v[2 * q], v[2 * q + 1], 0x5410);   // low halves
+                im[q] = __byte_perm(v[2 * q], v[2 * q + 1], 0x7632);   // high halves
                 nim[q] = im[q] ^ 0x80008000u;        // sign flip of both halves (exact)
             }
             char *b1 = base + kOffB1;
@@ -172,7 +175,8 @@ k_inv16(const __grid_constant__ CUtensorMap ymap, Inv16Args a, const void *table
         if (tid == 0) {
             const int next = img + (int)gridDim.x;
             if (next < nimg)                     // the next image's modes land under this one
-                bulk_load(sbase + kOffY, a.Y + (size_t)next * kNK, kNK * 8, &bar_y);
+                bulk_load(sbase + kOffY, static_cast<const char *>(a.Y) + (size_t)next * kYBytes,
+                          kYBytes, &bar_y);
             if (ok) {
                 for (int t = 0; t < 2; ++t)
                     for (int c = 0; c < 2; ++c)
