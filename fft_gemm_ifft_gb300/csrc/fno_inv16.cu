@@ -4,7 +4,8 @@
 // in one persistent kernel.
 //
 // For an output image (b, o) the mixed modes V[j][k] (16-bit (re, im) pairs from
-// the tensor-core mixing; kept row j = 0..63 with
+// the tensor-core mixing, stored in groups of 8 modes [group][image][8] and
+// gathered by one TMA load per image; kept row j = 0..63 with
 // the signed frequency g = j for j < 32 and j - 64 otherwise, bin k = 0..31)
 // give
 //   column inverse  Zo[t][k] = sum_j V[j][k] e^{+2 pi i g t / 256}     (t = 0..255)
@@ -103,7 +104,8 @@ __device__ __forceinline__ void drain_row64(uint32_t taddr, float scale, bool ok
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
-k_inv16(const __grid_constant__ CUtensorMap ymap, Inv16Args a, const void *tables, int nimg) {
+k_inv16(const __grid_constant__ CUtensorMap ymap, const __grid_constant__ CUtensorMap gmap,
+        Inv16Args a, const void *tables, int nimg) {
     extern __shared__ __align__(1024) char smem_raw[];
     char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
@@ -131,9 +133,17 @@ k_inv16(const __grid_constant__ CUtensorMap ymap, Inv16Args a, const void *table
     const uint32_t tmem = s_tmem;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");   // kernel B's mixed modes are complete
-    if (tid == 0 && (int)blockIdx.x < nimg)
-        bulk_load(sbase + kOffY, static_cast<const char *>(a.Y) + (size_t)blockIdx.x * kYBytes,
-                  kYBytes, &bar_y);
+    // an image's mixed modes: its row of each of the 256 groups of 8 modes, one
+    // TMA load that lands them in kept-mode order
+    auto load_y = [&](int img) {
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     ::"r"(tc_smem_addr(&bar_y)), "r"(kYBytes) : "memory");
+        asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                     " [%0], [%1, {%2, %3, %4}], [%5];"
+                     ::"r"(sbase + kOffY), "l"(&gmap), "r"(0), "r"(img), "r"(0),
+                       "r"(tc_smem_addr(&bar_y)) : "memory");
+    };
+    if (tid == 0 && (int)blockIdx.x < nimg) load_y(blockIdx.x);
     bool ok = mbar_wait(&bar_t, 0, a.err);
     constexpr uint32_t id1 = idesc_f16(64, Kind<T>::kBf16);
     constexpr uint32_t id2 = idesc_f16(256, Kind<T>::kBf16);
@@ -174,9 +184,7 @@ k_inv16(const __grid_constant__ CUtensorMap ymap, Inv16Args a, const void *table
         tc_after_sync();
         if (tid == 0) {
             const int next = img + (int)gridDim.x;
-            if (next < nimg)                     // the next image's modes land under this one
-                bulk_load(sbase + kOffY, static_cast<const char *>(a.Y) + (size_t)next * kYBytes,
-                          kYBytes, &bar_y);
+            if (next < nimg) load_y(next);       // the next image's modes land under this one
             if (ok) {
                 for (int t = 0; t < 2; ++t)
                     for (int c = 0; c < 2; ++c)
@@ -310,11 +318,12 @@ cudaError_t inv16_init(fno_dtype_t dtype) {
 // (at most one per output image).
 cudaError_t inv16_launch(fno_dtype_t dtype, const Inv16Args &a, const void *tables,
                          int64_t nimg, int num_sms, cudaStream_t s) {
-    CUtensorMap ymap;
+    CUtensorMap ymap, gmap;
     const size_t eb = 2;
     if (!encode_rows_tiled(&ymap, a.y, nimg * kN, kN, eb, 64,
                            dtype == FNO_F16 ? tma_type<__half>() : tma_type<__nv_bfloat16>()))
         return cudaErrorInvalidValue;
+    if (!encode_group_gather(&gmap, a.Y, 8, nimg, kNK / 8)) return cudaErrorInvalidValue;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
@@ -327,9 +336,9 @@ cudaError_t inv16_launch(fno_dtype_t dtype, const Inv16Args &a, const void *tabl
     cfg.numAttrs = 1;
     cudaError_t e;
     if (dtype == FNO_F16)
-        e = cudaLaunchKernelEx(&cfg, k_inv16<__half>, ymap, a, tables, (int)nimg);
+        e = cudaLaunchKernelEx(&cfg, k_inv16<__half>, ymap, gmap, a, tables, (int)nimg);
     else
-        e = cudaLaunchKernelEx(&cfg, k_inv16<__nv_bfloat16>, ymap, a, tables, (int)nimg);
+        e = cudaLaunchKernelEx(&cfg, k_inv16<__nv_bfloat16>, ymap, gmap, a, tables, (int)nimg);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -19,14 +19,16 @@
 // pieces they cost one L2 request per piece):
 //   X: [group of 8 kept modes][image b * Cin + i][8 modes] of 16-bit (re, im)
 //      pairs -- a group is one contiguous block of B * Cin * 32 bytes;
-//   Y: [image b * Cout + o][kept mode] of 16-bit (re, im) pairs -- a group's 8
-//      modes are 32 contiguous bytes of every image.
-// A CTA takes one group: one bulk copy brings its X block, the threads
-// transpose it in shared memory into the 8 modes' operands [Xr | Xi] (rows =
-// batch, K = input channels, the 128-byte-swizzled K-major layout), the modes'
-// weight operands pass through a ring of three slots, one MMA chain per mode
-// accumulates into its own tensor-memory columns, and the results are staged
-// so that each image's 8 modes leave as one 32-byte piece.
+//   Y: [group of 8 kept modes][image b * Cout + o][8 modes] of 16-bit (re, im)
+//      pairs, the same layout; the inverse gathers an image's 256 group rows
+//      with one three-dimensional TMA load.
+// A CTA takes half a group (4 modes; two CTAs per SM): the threads read each
+// image's 16 bytes of the run with coalesced loads and transpose them in
+// shared memory into the 4 modes' operands [Xr | Xi] (rows = batch, K = input
+// channels, the 128-byte-swizzled K-major layout), the modes' weight operands
+// pass through a ring of three slots, one MMA chain per mode accumulates into
+// its own tensor-memory columns, and the results are staged so that each
+// image's 4 modes leave as one 16-byte piece.
 //
 // Weights.  With FNO_PLAN_PACKED_WEIGHTS and 64 input and output channels,
 // fno_spectral_conv_pack_weights has written each kept mode's [Wr^T; Wi^T] once
@@ -50,7 +52,8 @@ namespace {
 using namespace tcu;
 
 constexpr int kMT = 256;                  // threads
-constexpr int kGrp = 8;                   // kept modes per CTA (one group)
+constexpr int kGrp = 8;                   // kept modes per group of the X layout
+constexpr int kRun = 4;                   // kept modes per CTA: half a group
 constexpr int kCh = 64;                   // channel tile (Cin, Cout <= 64)
 constexpr int kMaxN = 32;                 // batch rows (N) per CTA
 constexpr int kSlots = 3;                 // weight ring
@@ -58,17 +61,15 @@ constexpr uint32_t kHalfTile = 64 * 128;  // 64 rows x 128 bytes
 constexpr uint32_t kASlot = 3 * kHalfTile;          // [-Wi^T | Wr^T | Wi^T]
 constexpr uint32_t kImgMode = 2 * kHalfTile;        // packed bytes per mode
 constexpr uint32_t kXMode = 2 * kMaxN * 128;        // a mode's X operand: [Re | Im] x 32 rows
-// shared memory: the raw X block (B * Cin images x 32 bytes), later the Y
-// staging (B * Cout images x 9 words: a padded row keeps the drain free of
-// bank conflicts); the 8 X operands; the weight ring
-constexpr uint32_t kStageRow = 9;                   // words per staged image
-constexpr uint32_t kRawBytes = kCh * kMaxN * kStageRow * 4;   // >= B * Cin * 32 as well
-constexpr uint32_t kOffXop = (kRawBytes + 1023) / 1024 * 1024;
-constexpr uint32_t kOffW = kOffXop + kGrp * kXMode;
+// shared memory: the run's 4 X operands, then the weight ring; after the MMAs
+// the Y staging goes over both (B * Cout images x 5 words: a padded row keeps
+// the drain free of bank conflicts).  Two CTAs per SM.
+constexpr uint32_t kStageRow = kRun + 1;            // words per staged image
+constexpr uint32_t kOffW = kRun * kXMode;
 constexpr uint32_t kSmem = kOffW + kSlots * kASlot + 1024;
-constexpr uint32_t kTmemCols = 256;                 // kGrp modes x N (<= 32)
-static_assert(kSmem <= 232448 - 512, "one CTA per SM");
-static_assert((uint32_t)kCh * kMaxN * 32 <= kRawBytes, "raw X block fits");
+constexpr uint32_t kTmemCols = 128;                 // kRun modes x N (<= 32)
+static_assert(2 * (kSmem + 256) <= 232448, "two CTAs per SM");
+static_assert((uint32_t)kMaxN * kCh * kStageRow * 4 <= kOffW + kSlots * kASlot, "staging fits");
 
 template <typename T> struct Bits;
 template <> struct Bits<__half> {
@@ -96,21 +97,21 @@ __device__ __forceinline__ void expect_tx(uint64_t *bar, uint32_t bytes) {
 }
 
 template <typename T, bool kImg>
-__global__ void __launch_bounds__(kMT, 1) k_mix_tc(MixTcArgs a) {
+__global__ void __launch_bounds__(kMT, 2) k_mix_tc(MixTcArgs a) {
     extern __shared__ __align__(1024) char smem_raw[];
     char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
-    __shared__ __align__(8) uint64_t bar_x, bar_w[kSlots], bar_m[kSlots];
+    __shared__ __align__(8) uint64_t bar_w[kSlots], bar_m[kSlots];
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const unsigned long long t0 = a.trace ? trace_now() : 0;
-    const int grp = blockIdx.x, mode0 = grp * kGrp;
+    const int grp = blockIdx.x / 2, half = blockIdx.x % 2;
+    const int mode0 = grp * kGrp + half * kRun;
     const int nbp = (a.batch + 15) / 16 * 16;                // N: batch padded to 16
     const int nimg_in = a.batch * a.cin, nimg_out = a.batch * a.cout;
     const uint32_t sb = tc_smem_addr(base);
-    const bool inside = mode0 >= 0 && mode0 + kGrp <= a.nk;    // the group lies in the tensors
+    const bool inside = mode0 >= 0 && mode0 + kRun <= a.nk;  // the run lies in the tensors
     if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_x)));
         for (int s = 0; s < kSlots; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_w[s])));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_m[s])));
@@ -125,20 +126,22 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_tc(MixTcArgs a) {
     }
     // every thread waits on the barriers: they must be initialised first
     __syncthreads();
-    // The packed weight image of mode r into the last two thirds of slot r % kSlots
-    // (thread 0; nothing is copied for a group outside the tensors).
+    // mode r of the run sits in slot r % kSlots
+    auto slot_at = [&](int r) -> char * { return base + kOffW + (r % kSlots) * kASlot; };
+    // The packed weight image of mode r into the last two thirds of its slot
+    // (thread 0; nothing is copied for a run outside the tensors).
     auto fetch_w = [&](int r) {
-        const int s = r % kSlots;
-        expect_tx(&bar_w[s], inside ? kImgMode : 0u);
+        const int sl = r % kSlots;
+        expect_tx(&bar_w[sl], inside ? kImgMode : 0u);
         if (inside)
-            bulk_g2s(sb + kOffW + s * kASlot + kHalfTile,
+            bulk_g2s(tc_smem_addr(slot_at(r) + kHalfTile),
                      static_cast<const char *>(a.w) + (size_t)(mode0 + r) * kImgMode, kImgMode,
-                     &bar_w[s]);
+                     &bar_w[sl]);
     };
-    // Slot r % kSlots = [-Wi^T | Wr^T | Wi^T] of mode r from the weight tensor
-    // (all threads; element (o, i) of each tile).
+    // The slot of mode r = [-Wi^T | Wr^T | Wi^T] from the weight tensor (all
+    // threads; element (o, i) of each tile).
     auto build_w = [&](int r) {
-        char *slot = base + kOffW + (r % kSlots) * kASlot;
+        char *slot = slot_at(r);
         const int kk = mode0 + r, j = kk / a.m1, k = kk % a.m1;
         const int blk = j >= a.m0 ? 1 : 0;
         const int local = (j - blk * a.m0) * a.m1 + k;
@@ -160,104 +163,123 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_tc(MixTcArgs a) {
             *reinterpret_cast<unsigned short *>(slot + 2 * kHalfTile + off) = im;
         }
     };
-    // 1. the first weight slots (independent of kernel A)
+    // 1. the weights of modes 0-2 (independent of kernel A)
     if constexpr (kImg) {
         if (tid == 0)
             for (int r = 0; r < kSlots; ++r) fetch_w(r);
     }
+    if (a.cin < kCh) {
+        // input columns beyond cin stay zero in every X operand
+        for (int e = tid; e < (int)(kRun * kXMode / 16); e += kMT)
+            reinterpret_cast<uint4 *>(base)[e] = make_uint4(0, 0, 0, 0);
+        __syncthreads();                         // zeroing before the transpose writes
+    }
     pdl_trigger();
     pdl_wait();                                  // kernel A's kept modes are complete
     const unsigned long long t1 = a.trace ? trace_now() : 0;
-    // 2. the group's X block: B * Cin images x 32 bytes, one bulk copy
-    const uint32_t xblock = (uint32_t)nimg_in * 32;
-    if (tid == 0) {
-        expect_tx(&bar_x, inside ? xblock : 0u);
-        if (inside)
-            bulk_g2s(sb, static_cast<const char *>(a.X) + (size_t)grp * xblock, xblock, &bar_x);
-    }
-    if (a.cin < kCh) {
-        // input columns beyond cin stay zero in every X operand
-        for (int e = tid; e < (int)(kGrp * kXMode / 16); e += kMT)
-            reinterpret_cast<uint4 *>(base + kOffXop)[e] = make_uint4(0, 0, 0, 0);
-        __syncthreads();                         // zeroing before the transpose writes
-    }
-    bool ok = mbar_wait(&bar_x, 0, a.err);
-    // 3. transpose: image (b, i) holds 8 modes (re, im); mode r's operand gets
-    //    Re in chunk 0 and Im in chunk 1 at row b, column i.  A warp takes 32
-    //    consecutive images, so each of its 2-byte stores fills 64 contiguous bytes.
-    for (int img = tid; img < nimg_in; img += kMT) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(base + (size_t)img * 32);
-        const uint4 p0 = src[0], p1 = src[1];
-        const uint32_t v[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-        const uint32_t off = sw_off16(img / a.cin, img % a.cin);
+    // 2. X: image (b, i) holds the run's 4 modes (re, im) as 16 contiguous bytes
+    //    of its group row; all of a thread's loads are in flight before the
+    //    transpose writes mode r's Re (chunk 0) and Im (chunk 1) at row b,
+    //    column i.  A warp takes 32 consecutive images: each of its 2-byte
+    //    stores fills 64 contiguous bytes.
+    if (inside) {
+        const char *xg = static_cast<const char *>(a.X) + (size_t)grp * nimg_in * 32 + half * 16;
+        constexpr int kPer = 8;                  // images per thread per round
+        for (int img0 = 0; img0 < nimg_in; img0 += kPer * kMT) {
+            uint4 v[kPer];
 #pragma unroll
-        for (int r = 0; r < kGrp; ++r) {
-            char *xo = base + kOffXop + r * kXMode;
-            *reinterpret_cast<unsigned short *>(xo + off) = (unsigned short)(v[r] & 0xFFFF);
-            *reinterpret_cast<unsigned short *>(xo + nbp * 128 + off) =
-                (unsigned short)(v[r] >> 16);
+            for (int u = 0; u < kPer; ++u) {
+                const int img = img0 + u * kMT + tid;
+                v[u] = img < nimg_in ? __ldcg(reinterpret_cast<const uint4 *>(xg + (size_t)img * 32))
+                                     : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int img = img0 + u * kMT + tid;
+                if (img >= nimg_in) break;
+                const uint32_t off = sw_off16(img / a.cin, img % a.cin);
+                const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int r = 0; r < kRun; ++r) {
+                    char *xo = base + r * kXMode;
+                    *reinterpret_cast<unsigned short *>(xo + off) = (unsigned short)(w4[r] & 0xFFFF);
+                    *reinterpret_cast<unsigned short *>(xo + nbp * 128 + off) =
+                        (unsigned short)(w4[r] >> 16);
+                }
+            }
         }
     }
+    bool ok = true;
     const uint32_t tmem = s_tmem;
     const uint32_t idesc = idesc_f16(nbp, Bits<T>::kBf16);
-    // 4. one chain per mode.  Packed images: slot r % kSlots is refilled with
-    //    mode r + kSlots by thread 0 as soon as mode r's MMAs have read it.
-    //    Built slots: every thread waits for the slot's previous MMAs first.
-    for (int r = 0; r < kGrp; ++r) {
-        const int s = r % kSlots;
-        char *slot = base + kOffW + s * kASlot;
-        if constexpr (kImg) {
-            ok &= mbar_wait(&bar_w[s], (r / kSlots) & 1, a.err);
-            for (int e = tid; e < (int)(kHalfTile / 16); e += kMT) {   // -Wi^T, exact
-                const uint4 v = reinterpret_cast<const uint4 *>(slot + 2 * kHalfTile)[e];
-                reinterpret_cast<uint4 *>(slot)[e] =
-                    make_uint4(v.x ^ 0x80008000u, v.y ^ 0x80008000u, v.z ^ 0x80008000u,
-                               v.w ^ 0x80008000u);
+    // 3. the modes in two batches (0-2, then 3 in the slot of mode 0): every
+    //    slot of a batch made ready (packed: wait for its image and negate
+    //    Wi^T; else built from the weights), one barrier, then thread 0 issues
+    //    one chain per mode
+    for (int r0 = 0; r0 < kRun; r0 += kSlots) {
+        const int r1 = r0 + kSlots < kRun ? r0 + kSlots : kRun;
+        for (int r = r0; r < r1; ++r) {
+            char *slot = slot_at(r);
+            const uint32_t use = (uint32_t)(r / kSlots);       // 0: first use of the slot
+            if constexpr (kImg) {
+                ok &= mbar_wait(&bar_w[r % kSlots], use & 1, a.err);
+                for (int e = tid; e < (int)(kHalfTile / 16); e += kMT) {   // -Wi^T, exact
+                    const uint4 v = reinterpret_cast<const uint4 *>(slot + 2 * kHalfTile)[e];
+                    reinterpret_cast<uint4 *>(slot)[e] =
+                        make_uint4(v.x ^ 0x80008000u, v.y ^ 0x80008000u, v.z ^ 0x80008000u,
+                                   v.w ^ 0x80008000u);
+                }
+            } else {
+                if (use) {                        // the slot's first mode has been read
+                    ok &= mbar_wait(&bar_m[r % kSlots], 0, a.err);
+                    tc_after_sync();
+                }
+                build_w(r);
             }
-        } else {
-            if (r >= kSlots) {
-                ok &= mbar_wait(&bar_m[s], ((r - kSlots) / kSlots) & 1, a.err);
-                tc_after_sync();
-            }
-            build_w(r);
         }
         fence_async_smem();
         tc_before_sync();
-        __syncthreads();                         // slot (and, at r = 0, the X operands) ready
+        __syncthreads();                         // slots (and, at r0 = 0, the X operands) ready
         if (tid == 0) {
             tc_after_sync();
-            if (ok) {
-                const uint32_t bm = sb + kOffXop + r * kXMode;
+            for (int r = r0; r < r1; ++r) {
+                if (ok) {
+                    const uint32_t am0 = tc_smem_addr(slot_at(r));
+                    const uint32_t bm = sb + r * kXMode;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const uint32_t am = sb + kOffW + s * kASlot + (c == 0 ? kHalfTile : 0u);
+                    for (int c = 0; c < 2; ++c) {
+                        const uint32_t am = am0 + (c == 0 ? kHalfTile : 0u);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        mma_f16(tmem + r * nbp, desc_sw128(am + q * 32),
-                                desc_sw128(bm + c * nbp * 128 + q * 32), idesc,
-                                (c | q) ? 1u : 0u);
+                        for (int q = 0; q < 4; ++q)
+                            mma_f16(tmem + r * nbp, desc_sw128(am + q * 32),
+                                    desc_sw128(bm + c * nbp * 128 + q * 32), idesc,
+                                    (c | q) ? 1u : 0u);
+                    }
                 }
+                mma_commit(&bar_m[r % kSlots]);
             }
-            mma_commit(&bar_m[s]);
             if constexpr (kImg) {
-                if (r + kSlots < kGrp) {
-                    ok &= mbar_wait(&bar_m[s], (r / kSlots) & 1, a.err);
-                    fetch_w(r + kSlots);
-                }
+                // the later modes into the slots of the first ones once read
+                if (r0 == 0)
+                    for (int r = kSlots; r < kRun; ++r) {
+                        ok &= mbar_wait(&bar_m[r % kSlots], 0, a.err);
+                        fetch_w(r);
+                    }
             }
         }
     }
     // every chain is done once the last commit of each slot has arrived
-    for (int r = kGrp - kSlots; r < kGrp; ++r)
-        ok &= mbar_wait(&bar_m[r % kSlots], (r / kSlots) & 1, a.err);
+    for (int sl = 0; sl < kSlots; ++sl)
+        ok &= mbar_wait(&bar_m[sl], (sl + kSlots < kRun) ? 1u : 0u, a.err);
     tc_after_sync();
-    // 5. tensor memory -> staging: D row m = o (re) or 64 + o (im), column b;
-    //    staged image row (b * Cout + o) of 9 words, word r = mode r (re, im)
+    const unsigned long long t2 = a.trace ? trace_now() : 0;
+    // 4. tensor memory -> staging: D row m = o (re) or 64 + o (im), column b;
+    //    staged image row (b * Cout + o) of 5 words, word r = mode r (re, im)
     uint32_t *stage = reinterpret_cast<uint32_t *>(base);
     {
         const int m = 32 * (warp & 3) + lane;
         const int o = m % kCh, part = m / kCh;
-        for (int r = warp >> 2; r < kGrp; r += 2) {              // warps 0-3 even modes, 4-7 odd
+        for (int r = warp >> 2; r < kRun; r += 2) {            // warps 0-3 even modes, 4-7 odd
             for (int g = 0; g < nbp / 16; ++g) {
                 float v[16];
                 tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + r * nbp + 16 * g, v);
@@ -276,13 +298,12 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_tc(MixTcArgs a) {
     }
     tc_before_sync();
     __syncthreads();
-    // 6. Y: each image's 8 modes as one 32-byte piece
+    // 5. Y in the group layout: each image's 4 modes as one 16-byte piece of its
+    //    32-byte group row, so a warp's 32 consecutive images fill 1 KiB
+    uint32_t *yg = static_cast<uint32_t *>(a.Y) + (size_t)grp * nimg_out * kGrp + half * kRun;
     for (int img = tid; img < nimg_out && inside; img += kMT) {
         const uint32_t *sv = stage + (size_t)img * kStageRow;
-        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint32_t *>(a.Y) +
-                                               (size_t)img * a.nk + mode0);
-        dst[0] = make_uint4(sv[0], sv[1], sv[2], sv[3]);
-        dst[1] = make_uint4(sv[4], sv[5], sv[6], sv[7]);
+        *reinterpret_cast<uint4 *>(yg + (size_t)img * kGrp) = make_uint4(sv[0], sv[1], sv[2], sv[3]);
     }
     if (warp == 0) {
         tc_after_sync();
@@ -299,7 +320,8 @@ __global__ void __launch_bounds__(kMT, 1) k_mix_tc(MixTcArgs a) {
             rec.worker = smid;
             rec.t_start = t0;
             rec.t_ready = t1;
-            rec.t_compute = rec.t_end = trace_now();
+            rec.t_compute = t2;
+            rec.t_end = trace_now();
             a.trace[a.trace_first + blockIdx.x] = rec;
         }
     }
@@ -350,7 +372,7 @@ bool mixtc_supported(int d, fno_dtype_t dtype, int64_t batch, int cin, int cout,
            batch >= 1 && batch <= kMaxN && m1 % kGrp == 0 && nkept % kGrp == 0;
 }
 
-int mixtc_items(int64_t nkept) { return (int)(nkept / kGrp); }
+int mixtc_items(int64_t nkept) { return (int)(nkept / kRun); }
 
 size_t mixtc_x_bytes(int64_t batch, int cin, int64_t nkept) {
     return (size_t)nkept * batch * cin * 4;
@@ -373,7 +395,7 @@ cudaError_t mixtc_launch(fno_dtype_t dtype, const MixTcArgs &args, cudaStream_t 
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(args.nk / kGrp));
+    cfg.gridDim = dim3((unsigned)(args.nk / kRun));
     cfg.blockDim = dim3(kMT);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = s;

@@ -199,5 +199,21 @@ inline bool encode_rows_tiled(CUtensorMap *map, const void *ptr, int64_t rows, i
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A gather map for groups of 32-bit words laid out [group][row][w words]: one
+// box = w words of one row from each of `groups` groups (TMA boxes hold at most
+// 256 entries per dimension).
+inline bool encode_group_gather(CUtensorMap *map, const void *ptr, int w, int64_t rows,
+                                int groups) {
+    EncodeTiled fn = encoder();
+    if (!fn || groups > 256 || w > 256) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)w, (cuuint64_t)rows, (cuuint64_t)groups};
+    const cuuint64_t strides[2] = {(cuuint64_t)w * 4, (cuuint64_t)rows * w * 4};
+    const cuuint32_t box[3] = {(cuuint32_t)w, 1, (cuuint32_t)groups};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace tcu
 }  // namespace fno
