@@ -408,8 +408,8 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
         }
     } else {
         // ----- consumers: warp t1, lane k of the column DFT -----
-        float *zr = reinterpret_cast<float *>(base + Gm::kZ);
-        float *zi = zr + Gm::N0 * Gm::M1;
+        // Z as complex rows [t][32 bins], the bin index XOR-swizzled by the row
+        float2 *Zc = reinterpret_cast<float2 *>(base + Gm::kZ);
         float2 *F = reinterpret_cast<float2 *>(base + Gm::kZ);
         bool ok = true;
         uint32_t it = 0;
@@ -419,22 +419,23 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
             ok &= mbar_wait(&acc[b], (it >> 1) & 1, a.err);
             tc_after_sync();
             const unsigned long long t_z = a.trace ? trace_now() : 0;   // the row DFT is done
-            // Z planes from tensor memory: warps w and w + 4 read the same lanes,
-            // the first the re, the second the im half
+            // Z from tensor memory: warp w reads the lanes 32 (w % 4).. of M tile w / 4,
+            // all 64 columns (bins re, then im) of its row
             {
-                const int half = warp >> 2;
-                float *dz = half ? zi : zr;
-                for (int t = 0; t < Gm::MT; ++t) {
-                    const int row = 128 * t + 32 * (warp & 3) + lane;
+                const int t = warp >> 2;
+                const int row = 128 * t + 32 * (warp & 3) + lane;
+                const uint32_t tbase = tmem + ((uint32_t)(32 * (warp & 3)) << 16) +
+                                       b * Gm::kTmemCols + t * Gm::N;
 #pragma unroll
-                    for (int g = 0; g < Gm::M1 / 16; ++g) {
-                        float v[16];
-                        tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) +
-                                      b * Gm::kTmemCols + t * Gm::N + half * Gm::M1 + 16 * g,
-                                  v);
+                for (int g = 0; g < Gm::M1 / 16; ++g) {
+                    float re[16], im[16];
+                    tmem_ld16(tbase + 16 * g, re);
+                    tmem_ld16(tbase + Gm::M1 + 16 * g, im);
 #pragma unroll
-                        for (int q = 0; q < 16; ++q)
-                            dz[row * Gm::M1 + ((16 * g + q) ^ (row & 31))] = ok ? v[q] : 0.f;
+                    for (int q = 0; q < 16; ++q) {
+                        const int k = 16 * g + q;
+                        Zc[row * Gm::M1 + (k ^ (row & 31))] =
+                            ok ? make_float2(re[q], im[q]) : make_float2(0.f, 0.f);
                     }
                 }
             }
@@ -446,8 +447,8 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
             float2 z[Gm::G1];
 #pragma unroll
             for (int t2 = 0; t2 < Gm::G1; ++t2) {
-                const int r = warp + Gm::T1 * t2, c = r * Gm::M1 + (lane ^ (r & 31));
-                z[t2] = make_float2(zr[c], zi[c]);
+                const int r = warp + Gm::T1 * t2;
+                z[t2] = Zc[r * Gm::M1 + (lane ^ (r & 31))];
             }
             fft::fft_dif<Gm::G1, -1>(z);
             consumer_sync();                     // Z is read: F goes over it
@@ -455,34 +456,46 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
             for (int g1 = 0; g1 < Gm::G1; ++g1)
                 F[(warp * Gm::G1 + g1) * Gm::M1 + lane] = z[fft::bitrev(g1, fft::ilog2(Gm::G1))];
             consumer_sync();
-            // kept modes: X[j][k] = sum_t1 W_N0^{g t1} F[t1][g mod G1][k], g the signed
-            // frequency of kept row j (j, or j - K0 for the high rows)
-            float2 *dst = a.part + (size_t)img * Gm::NK;
-            // with the tensor-core mixing, mode o leaves as a 16-bit (re, im) pair in
-            // group o / 8 of the mixing's input: [group][image][8 modes], so a
-            // warp's 32 modes fill four whole 32-byte pieces
+            // kept modes in pairs: low row j (g = j) and high row j + 32 (g = j - 32)
+            // share F[t1][j][k]; with P[t1] = W_N0^{j t1} F[t1][j][k],
+            //   X[j][k] = sum_t1 P[t1],  X[j + 32][k] = sum_t1 P[t1] e^{+2 pi i t1 / 8}
+            // (W_N0^{-32 t1} = e^{+2 pi i t1 / 8}, a compile-time constant)
+            static_assert(Gm::K0 == 2 * Gm::G1 && Gm::T1 == 8, "pairs of kept rows, 8 terms");
+            const size_t gstride = (size_t)a.batch * a.cin * 8;         // words per group
             uint32_t *xg = reinterpret_cast<uint32_t *>(a.part) + (size_t)img * 8;
-            const size_t gstride = (size_t)a.batch * a.cin * 8;     // words per group
-            for (int o = tid; o < Gm::NK; o += NT) {
-                const int j = o / Gm::M1, k = o % Gm::M1;
-                const int g = j < Gm::M0 ? j : j - Gm::K0, g1 = j & (Gm::G1 - 1);
-                float2 accv = make_float2(0.f, 0.f);
+            float2 *dst = a.part + (size_t)img * Gm::NK;
 #pragma unroll
-                for (int t1 = 0; t1 < Gm::T1; ++t1)
-                    cmac(accv, F[(t1 * Gm::G1 + g1) * Gm::M1 + k],
-                         __ldg(a.tw0 + ((g * t1) & (Gm::N0 - 1))));
+            for (int pq = 0; pq < Gm::G1 / 8; ++pq) {
+                const int j = warp + 8 * pq;
+                float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
+                fft::unroll<0, Gm::T1>([&](auto tt) {
+                    constexpr int t1 = decltype(tt)::value;
+                    const float2 f = F[(t1 * Gm::G1 + j) * Gm::M1 + lane];
+                    const float2 P = fft::cmul(f, __ldg(a.tw0 + ((j * t1) & (Gm::N0 - 1))));
+                    lo = fft::cadd(lo, P);
+                    hi = fft::cadd(hi, fft::twiddle<t1, Gm::T1, +1>(P));
+                });
+                const int o_lo = j * Gm::M1 + lane, o_hi = (j + Gm::G1) * Gm::M1 + lane;
                 if (a.mix16) {
-                    uint32_t u;             // re in the low half, im in the high half
+                    // 16-bit (re, im) pairs in group o / 8 of the mixing's input:
+                    // [group][image][8 modes], a warp's 32 modes fill four 32-byte pieces
+                    uint32_t ulo, uhi;
                     if constexpr (std::is_same<T, __half>::value) {
-                        const __half2 h = __floats2half2_rn(accv.x, accv.y);
-                        memcpy(&u, &h, 4);
+                        const __half2 h0 = __floats2half2_rn(lo.x, lo.y);
+                        const __half2 h1 = __floats2half2_rn(hi.x, hi.y);
+                        memcpy(&ulo, &h0, 4);
+                        memcpy(&uhi, &h1, 4);
                     } else {
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(accv.x, accv.y);
-                        memcpy(&u, &h, 4);
+                        const __nv_bfloat162 h0 = __floats2bfloat162_rn(lo.x, lo.y);
+                        const __nv_bfloat162 h1 = __floats2bfloat162_rn(hi.x, hi.y);
+                        memcpy(&ulo, &h0, 4);
+                        memcpy(&uhi, &h1, 4);
                     }
-                    xg[(o >> 3) * gstride + (o & 7)] = u;
+                    xg[(o_lo >> 3) * gstride + (o_lo & 7)] = ulo;
+                    xg[(o_hi >> 3) * gstride + (o_hi & 7)] = uhi;
                 } else {
-                    __stcg(dst + o, accv);
+                    __stcg(dst + o_lo, lo);
+                    __stcg(dst + o_hi, hi);
                 }
             }
             consumer_sync();                     // F is read: the next Z goes over it
