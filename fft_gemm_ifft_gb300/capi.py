@@ -80,7 +80,9 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    """libfno.so, or the index-checking build libfno_bounds.so when the
+    environment sets FNO_LIBRARY=bounds (read once, at the first load)."""
+    return _build.BOUNDS_LIB_PATH if os.environ.get("FNO_LIBRARY") == "bounds" else _build.LIB_PATH
 
 
 def lib() -> ctypes.CDLL:
@@ -88,7 +90,7 @@ def lib() -> ctypes.CDLL:
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.LIB_PATH
+            path = library_path()
             if not os.path.exists(path):
                 raise RuntimeError(
                     f"{path} is not built; run fft_gemm_ifft_gb300.build.build() "

@@ -491,8 +491,11 @@ k_phase_a_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table
                         memcpy(&ulo, &h0, 4);
                         memcpy(&uhi, &h1, 4);
                     }
-                    xg[(o_lo >> 3) * gstride + (o_lo & 7)] = ulo;
-                    xg[(o_hi >> 3) * gstride + (o_hi & 7)] = uhi;
+                    const int64_t xwords = (int64_t)Gm::NK * a.batch * a.cin;
+                    const int64_t ilo = (o_lo >> 3) * gstride + (o_lo & 7) + (int64_t)img * 8;
+                    const int64_t ihi = (o_hi >> 3) * gstride + (o_hi & 7) + (int64_t)img * 8;
+                    if (in_bounds(ilo, xwords, a.err)) xg[ilo - (int64_t)img * 8] = ulo;
+                    if (in_bounds(ihi, xwords, a.err)) xg[ihi - (int64_t)img * 8] = uhi;
                 } else {
                     __stcg(dst + o_lo, lo);
                     __stcg(dst + o_hi, hi);

@@ -176,6 +176,21 @@ __device__ __forceinline__ void raise_dev_error(int *err, int code) {
     if (err) atomicCAS(err, 0, code);
 }
 
+// Index checks of the debug build (compiled with FNO_DEBUG_BOUNDS, the library
+// libfno_bounds.so): a global-memory index outside [0, size) records kDevBounds
+// in the error word and the access is skipped, so a wrong index shows up as
+// FNO_ERR_DEVICE_BOUNDS from fno_plan_get_device_error instead of a fault.  In
+// the normal build every check is the constant true and compiles away.
+#ifdef FNO_DEBUG_BOUNDS
+__device__ __forceinline__ bool in_bounds(int64_t idx, int64_t size, int *err) {
+    if (idx >= 0 && idx < size) return true;
+    raise_dev_error(err, kDevBounds);
+    return false;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(int64_t, int64_t, int *) { return true; }
+#endif
+
 // --------------------------------------------------------------------------
 // Host-side entry points of the kernel translation units
 // --------------------------------------------------------------------------

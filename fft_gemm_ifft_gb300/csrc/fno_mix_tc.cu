@@ -190,8 +190,10 @@ __global__ void __launch_bounds__(kMT, 2) k_mix_tc(MixTcArgs a) {
 #pragma unroll
             for (int u = 0; u < kPer; ++u) {
                 const int img = img0 + u * kMT + tid;
-                v[u] = img < nimg_in ? __ldcg(reinterpret_cast<const uint4 *>(xg + (size_t)img * 32))
-                                     : make_uint4(0, 0, 0, 0);
+                const int64_t word = ((int64_t)grp * nimg_in + img) * kGrp + half * kRun + 3;
+                v[u] = img < nimg_in && in_bounds(word, (int64_t)a.nk * nimg_in, a.err)
+                           ? __ldcg(reinterpret_cast<const uint4 *>(xg + (size_t)img * 32))
+                           : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int u = 0; u < kPer; ++u) {
@@ -303,7 +305,10 @@ __global__ void __launch_bounds__(kMT, 2) k_mix_tc(MixTcArgs a) {
     uint32_t *yg = static_cast<uint32_t *>(a.Y) + (size_t)grp * nimg_out * kGrp + half * kRun;
     for (int img = tid; img < nimg_out && inside; img += kMT) {
         const uint32_t *sv = stage + (size_t)img * kStageRow;
-        *reinterpret_cast<uint4 *>(yg + (size_t)img * kGrp) = make_uint4(sv[0], sv[1], sv[2], sv[3]);
+        const int64_t word = ((int64_t)grp * nimg_out + img) * kGrp + half * kRun + 3;
+        if (in_bounds(word, (int64_t)a.nk * nimg_out, a.err))
+            *reinterpret_cast<uint4 *>(yg + (size_t)img * kGrp) =
+                make_uint4(sv[0], sv[1], sv[2], sv[3]);
     }
     if (warp == 0) {
         tc_after_sync();

@@ -44,7 +44,7 @@ __device__ __forceinline__ int kept_freq(int r, int m, int n) {
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 k_fwd_last(const T *__restrict__ x, float2 *__restrict__ out, int64_t nlines, int N, int E,
-           int M, const float2 *__restrict__ tw) {
+           int M, const float2 *__restrict__ tw, int *err) {
     const int64_t total = nlines * M;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -52,6 +52,7 @@ k_fwd_last(const T *__restrict__ x, float2 *__restrict__ out, int64_t nlines, in
         const int k = (int)(idx - line * M);
         const T *src = x + line * E;
         float2 acc = make_float2(0.f, 0.f);
+        if (!in_bounds(line * E + E - 1, nlines * E, err)) continue;
         for (int n = 0; n < E; ++n) {
             const float v = Storage<T>::load(src + n);
             const float2 w = tw[tw_idx(k * n, N)];
@@ -66,7 +67,7 @@ k_fwd_last(const T *__restrict__ x, float2 *__restrict__ out, int64_t nlines, in
 // over the E <= N stored rows n (the others are zero padding).
 __global__ void __launch_bounds__(kThreads)
 k_fwd_full(const float2 *__restrict__ in, float2 *__restrict__ out, int64_t outer, int N,
-           int E, int64_t inner, int m, const float2 *__restrict__ tw) {
+           int E, int64_t inner, int m, const float2 *__restrict__ tw, int *err) {
     const int K = 2 * m;
     const int64_t total = outer * K * inner;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
@@ -78,6 +79,8 @@ k_fwd_full(const float2 *__restrict__ in, float2 *__restrict__ out, int64_t oute
         const int f = kept_freq(r, m, N);
         const float2 *src = in + o * E * inner + q;
         float2 acc = make_float2(0.f, 0.f);
+        if (!in_bounds(o * E * inner + q + (int64_t)(E - 1) * inner, outer * E * inner, err))
+            continue;
         for (int n = 0; n < E; ++n) cfma(acc, src[n * inner], tw[tw_idx(f * n, N)]);
         out[idx] = acc;
     }
@@ -87,7 +90,7 @@ k_fwd_full(const float2 *__restrict__ in, float2 *__restrict__ out, int64_t oute
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 k_mix(const float2 *__restrict__ X, const T *__restrict__ w, float2 *__restrict__ Y,
-      int64_t batch, int cin, int cout, KeptGeom g, int packed) {
+      int64_t batch, int cin, int cout, KeptGeom g, int packed, int *err) {
     const int64_t total = batch * cout * g.nkept;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -113,6 +116,11 @@ k_mix(const float2 *__restrict__ X, const T *__restrict__ w, float2 *__restrict_
                              : w + ((((int64_t)blk * cin) * cout + o) * g.mblk + local) * 2;
         const int64_t wstride = packed ? (int64_t)cout * 4 * 2 : (int64_t)cout * g.mblk * 2;
         float2 acc = make_float2(0.f, 0.f);
+        const int64_t wl = (int64_t)g.nkept * cin * cout * 2;       // weight elements
+        if (!in_bounds(b * cin * g.nkept + kk + (int64_t)(cin - 1) * g.nkept, batch * cin * g.nkept,
+                       err) ||
+            !in_bounds((ws - w) + (int64_t)(cin - 1) * wstride + 1, wl, err))
+            continue;
         for (int i = 0; i < cin; ++i)
             cfma(acc, xs[(int64_t)i * g.nkept], Storage<T>::load2(ws + i * wstride));
         Y[idx] = acc;
@@ -123,7 +131,7 @@ k_mix(const float2 *__restrict__ X, const T *__restrict__ w, float2 *__restrict_
 // for the first E <= N rows n only (the output crop of a padded axis).
 __global__ void __launch_bounds__(kThreads)
 k_inv_full(const float2 *__restrict__ in, float2 *__restrict__ out, int64_t outer, int N,
-           int E, int64_t inner, int m, const float2 *__restrict__ tw) {
+           int E, int64_t inner, int m, const float2 *__restrict__ tw, int *err) {
     const int K = 2 * m;
     const int64_t total = outer * E * inner;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
@@ -134,6 +142,8 @@ k_inv_full(const float2 *__restrict__ in, float2 *__restrict__ out, int64_t oute
         const int64_t o = t / E;
         const float2 *src = in + o * K * inner + q;
         float2 acc = make_float2(0.f, 0.f);
+        if (!in_bounds(o * K * inner + q + (int64_t)(K - 1) * inner, outer * K * inner, err))
+            continue;
         for (int r = 0; r < K; ++r) {
             const float2 w = tw[tw_idx(kept_freq(r, m, N) * n, N)];
             cfma(acc, src[r * inner], make_float2(w.x, -w.y));   // conjugate twiddle
@@ -148,7 +158,7 @@ k_inv_full(const float2 *__restrict__ in, float2 *__restrict__ out, int64_t oute
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 k_inv_last(const float2 *__restrict__ in, T *__restrict__ y, int64_t nlines, int N, int E,
-           int M, const float2 *__restrict__ tw, float scale) {
+           int M, const float2 *__restrict__ tw, float scale, int *err) {
     const int64_t total = nlines * E;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -156,6 +166,7 @@ k_inv_last(const float2 *__restrict__ in, T *__restrict__ y, int64_t nlines, int
         const int n = (int)(idx - line * E);
         const float2 *src = in + line * M;
         float acc = 0.f;
+        if (!in_bounds(line * M + M - 1, nlines * M, err)) continue;
         for (int k = 0; k < M; ++k) {
             const float c = (k == 0 || 2 * k == N) ? 1.f : 2.f;
             const float2 v = src[k];
@@ -226,7 +237,7 @@ static cudaError_t unfused_forward_t(const Plan &p, const Buffers &bf, cudaStrea
     for (int j = 0; j < d - 1; ++j) lines *= g.ext[j];
     k_fwd_last<T><<<grid_for(lines * ml, sms), kThreads, 0, s>>>(
         reinterpret_cast<const T *>(bf.x), bufA, lines, (int)g.n[d - 1], (int)g.ext[d - 1],
-        (int)ml, p.tw[d - 1]);
+        (int)ml, p.tw[d - 1], p.dev_err);
     float2 *cur = bufA, *nxt = bufB;
     // a1, full axes from d-2 down to 0
     for (int a = d - 2; a >= 0; --a) {
@@ -234,7 +245,7 @@ static cudaError_t unfused_forward_t(const Plan &p, const Buffers &bf, cudaStrea
         for (int j = 0; j < a; ++j) outer *= g.ext[j];
         for (int j = a + 1; j < d - 1; ++j) inner *= g.kdim[j];
         k_fwd_full<<<grid_for(outer * g.kdim[a] * inner, sms), kThreads, 0, s>>>(
-            cur, nxt, outer, (int)g.n[a], (int)g.ext[a], inner, g.m[a], p.tw[a]);
+            cur, nxt, outer, (int)g.n[a], (int)g.ext[a], inner, g.m[a], p.tw[a], p.dev_err);
         std::swap(cur, nxt);
     }
     // a2, mixing
@@ -248,7 +259,7 @@ static cudaError_t unfused_forward_t(const Plan &p, const Buffers &bf, cudaStrea
     kg.mblk = g.mblk;
     k_mix<T><<<grid_for(p.batch * p.cout * g.nkept, sms), kThreads, 0, s>>>(
         cur, reinterpret_cast<const T *>(bf.w), nxt, p.batch, p.cin, p.cout, kg,
-        (p.flags & FNO_PLAN_PACKED_WEIGHTS) ? 1 : 0);
+        (p.flags & FNO_PLAN_PACKED_WEIGHTS) ? 1 : 0, p.dev_err);
     std::swap(cur, nxt);
     // a3, full axes 0..d-2
     for (int a = 0; a < d - 1; ++a) {
@@ -256,7 +267,7 @@ static cudaError_t unfused_forward_t(const Plan &p, const Buffers &bf, cudaStrea
         for (int j = 0; j < a; ++j) outer *= g.ext[j];
         for (int j = a + 1; j < d - 1; ++j) inner *= g.kdim[j];
         k_inv_full<<<grid_for(outer * g.ext[a] * inner, sms), kThreads, 0, s>>>(
-            cur, nxt, outer, (int)g.n[a], (int)g.ext[a], inner, g.m[a], p.tw[a]);
+            cur, nxt, outer, (int)g.n[a], (int)g.ext[a], inner, g.m[a], p.tw[a], p.dev_err);
         std::swap(cur, nxt);
     }
     // a3, last axis (half spectrum -> real), scale 1/prod(N) over the transform
@@ -264,7 +275,7 @@ static cudaError_t unfused_forward_t(const Plan &p, const Buffers &bf, cudaStrea
     for (int j = 0; j < d - 1; ++j) lines *= g.ext[j];
     k_inv_last<T><<<grid_for(lines * g.ext[d - 1], sms), kThreads, 0, s>>>(
         cur, reinterpret_cast<T *>(bf.y), lines, (int)g.n[d - 1], (int)g.ext[d - 1], (int)ml,
-        p.tw[d - 1], (float)(1.0 / (double)g.ntr));
+        p.tw[d - 1], (float)(1.0 / (double)g.ntr), p.dev_err);
     return cudaGetLastError();
 }
 
@@ -296,14 +307,14 @@ static cudaError_t forward_modes_t(const Plan &p, const T *x, int64_t nch, float
     for (int j = 0; j < d - 1; ++j) lines *= g.ext[j];
     float2 *cur = d == 1 ? out : sa;
     k_fwd_last<T><<<grid_for(lines * ml, p.num_sms), kThreads, 0, s>>>(
-        x, cur, lines, (int)g.n[d - 1], (int)g.ext[d - 1], (int)ml, p.tw[d - 1]);
+        x, cur, lines, (int)g.n[d - 1], (int)g.ext[d - 1], (int)ml, p.tw[d - 1], p.dev_err);
     for (int a = d - 2; a >= 0; --a) {
         float2 *dst = a == 0 ? out : (cur == sa ? sb : sa);
         int64_t outer = nch, inner = ml;
         for (int j = 0; j < a; ++j) outer *= g.ext[j];
         for (int j = a + 1; j < d - 1; ++j) inner *= g.kdim[j];
         k_fwd_full<<<grid_for(outer * g.kdim[a] * inner, p.num_sms), kThreads, 0, s>>>(
-            cur, dst, outer, (int)g.n[a], (int)g.ext[a], inner, g.m[a], p.tw[a]);
+            cur, dst, outer, (int)g.n[a], (int)g.ext[a], inner, g.m[a], p.tw[a], p.dev_err);
         cur = dst;
     }
     return cudaGetLastError();
@@ -376,14 +387,15 @@ cudaError_t launch_pack_weights(const Plan &p, const void *w, void *wp, cudaStre
 cudaError_t launch_axis_forward(const float2 *in, float2 *out, int64_t outer, int n, int64_t inner,
                                 int m, const float2 *tw, int num_sms, cudaStream_t s) {
     k_fwd_full<<<grid_for(outer * 2 * m * inner, num_sms), kThreads, 0, s>>>(in, out, outer, n,
-                                                                           n, inner, m, tw);
+                                                                           n, inner, m, tw,
+                                                                           nullptr);
     return cudaGetLastError();
 }
 
 cudaError_t launch_axis_inverse(const float2 *in, float2 *out, int64_t outer, int n, int64_t inner,
                                 int m, const float2 *tw, int num_sms, cudaStream_t s) {
     k_inv_full<<<grid_for(outer * n * inner, num_sms), kThreads, 0, s>>>(in, out, outer, n, n,
-                                                                       inner, m, tw);
+                                                                       inner, m, tw, nullptr);
     return cudaGetLastError();
 }
 
@@ -401,7 +413,8 @@ cudaError_t launch_mix(const Plan &p, const float2 *X, const void *w, float2 *Y,
     with_storage(p.dtype, [&](auto t) {
         using T = decltype(t);
         k_mix<T><<<grid, kThreads, 0, s>>>(X, static_cast<const T *>(w), Y, p.batch, p.cin,
-                                          p.cout, kg, (p.flags & FNO_PLAN_PACKED_WEIGHTS) ? 1 : 0);
+                                          p.cout, kg, (p.flags & FNO_PLAN_PACKED_WEIGHTS) ? 1 : 0,
+                                          p.dev_err);
         return 0;
     });
     return cudaGetLastError();

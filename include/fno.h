@@ -56,7 +56,7 @@ typedef enum fno_status_e {
     FNO_ERR_OUT_OF_MEMORY = 4,   /* plan-owned device or host memory could not be had    */
     FNO_ERR_CUDA = 5,            /* a CUDA runtime call or kernel launch failed          */
     FNO_ERR_DEVICE_TIMEOUT = 6,  /* a bounded device-side wait gave up                   */
-    FNO_ERR_DEVICE_BOUNDS = 7,   /* reserved: a device index check (none in this version) */
+    FNO_ERR_DEVICE_BOUNDS = 7,   /* a device index check failed (index-checking build)   */
     FNO_ERR_ALIASING = 8         /* the output overlaps an input or the workspace        */
 } fno_status_t;
 
@@ -319,7 +319,11 @@ fno_status_t fno_plan_get_trace(fno_plan_t plan, fno_trace_record_t *records, si
 
 /* Synchronise `stream`, then read and clear the plan's device error word
  * (TurboFNO §6.1 traces a crash to an unchecked device index; faults found on
- * the device are reported here instead of trapping).
+ * the device are reported here instead of trapping).  FNO_ERR_DEVICE_BOUNDS
+ * comes from the index-checking build of the library (libfno_bounds.so,
+ * compiled with FNO_DEBUG_BOUNDS), whose kernels check the global-memory
+ * indices of the separate-kernels path and of the 16-bit 256 x 256 fused
+ * path, record a failure here and skip the access.
  * Returns FNO_OK, FNO_ERR_DEVICE_TIMEOUT, FNO_ERR_DEVICE_BOUNDS or CUDA.   */
 fno_status_t fno_plan_get_device_error(fno_plan_t plan, fno_stream_t stream);
 

@@ -193,3 +193,15 @@ def test_padded_query_validation(L):
     d = QP(2, [100, 120], [28, 8], [16, 16], 8, 32, 32, F32)
     e = Q(2, [128, 128], [16, 16], 8, 32, 32, F32, flags=capi.FNO_PLAN_UNFUSED)
     assert d[0] == capi.FNO_OK and d[1] <= e[1] and d[2] == e[2]
+
+
+def test_index_checking_build_exports_the_same_symbols():
+    # the FNO_DEBUG_BOUNDS variant is the same library with index checks:
+    # built from the same sources, it exports every declared entry point
+    import ctypes
+    from fft_gemm_ifft_gb300 import build
+    path = build.build(debug_bounds=True)
+    assert path.endswith("libfno_bounds.so") and os.path.exists(path)
+    B = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(B, name), f"libfno_bounds.so does not export {name}"

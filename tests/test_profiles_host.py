@@ -32,6 +32,13 @@ def test_recorded_traffic_is_plausible_for_the_bench_layer():
     assert 0.5 * 37748736 < e["dram_bytes_per_launch"] < 2.0 * 37748736
 
 
+def test_recorded_traffic_is_plausible_for_the_headline_layer():
+    # 2-D fp16 layer: x, w, y once = 570 425 344 bytes
+    e = load()["2d_f16"]
+    assert 0.9 * 570425344 < e["dram_bytes_per_launch"] < 1.3 * 570425344
+    assert set(e["per_kernel"]) == {"k_phase_a_tc", "k_mix_tc", "k_inv16"}
+
+
 def test_stale_record_is_not_reported(tmp_path, monkeypatch):
     d = load()
     d["2d_f32"]["source_digest"] = "0" * 16
