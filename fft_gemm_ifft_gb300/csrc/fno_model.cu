@@ -11,6 +11,7 @@
 #include <type_traits>
 
 #include "fno_internal.cuh"
+#include "fno_gelu.cuh"
 #include "fno_tc.cuh"
 
 using namespace fno;
@@ -32,9 +33,9 @@ struct Model {
     size_t layer_tc_smem, head_tc_smem;
 };
 
-__device__ __forceinline__ float gelu(float v) {
-    return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
-}
+// GELU(v) = v/2 (1 + erf(v / sqrt 2)), erf by Abramowitz & Stegun 7.1.26
+// (fno_gelu.cuh; |error of erf| <= 1.5e-7)
+__device__ __forceinline__ float gelu(float v) { return gelu_erf(v); }
 
 // ---------------------------------------------------------------------------
 // Register-tiled 1x1 linears.  A CTA of kTT threads owns kTP pixels of one
@@ -340,11 +341,19 @@ k_linear_tc(const T *__restrict__ a, const float *__restrict__ W,
         for (int i = 0; i < kCinT; ++i) av[i] = tin ? load_act(ab + (int64_t)i * npix) : 0.f;
     };
     load_tile(blockIdx.x);
+    // this thread's output columns: groups quarter, quarter + 4, ...; the
+    // biases are read once into shared memory (broadcast reads per tile)
+    const bool has_cols = quarter < NG;
+    __shared__ float s_bias[16 * 8];
+    for (int o = tid; o < n; o += kThreads) s_bias[o] = bias[o];
+    __syncthreads();
     uint32_t phase = 0;
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int64_t b = tile / ptiles, p0 = (tile % ptiles) * kRows;
         const int64_t p = p0 + row;
         const bool pin = p < npix;
+        // pixel p of image b in channel 0; channel o is o * npix further
+        const int64_t pix0 = b * n * npix + p;
 #pragma unroll
         for (int i4 = 0; i4 < kCinT / 4; ++i4) {
             const int i = i0 + 4 * i4;
@@ -375,18 +384,17 @@ k_linear_tc(const T *__restrict__ a, const float *__restrict__ W,
             mma_commit(&bar);
         }
         load_tile(tile + gridDim.x);    // av is in shared memory: prefetch the next tile
-        // this thread's column groups (quarter q takes groups q, q + 4, ...)
-        const bool has_cols = quarter < NG;
         // the spectral sums of these outputs are fetched while the MMAs run
         float sv[16 * kGroupsT];
 #pragma unroll
-        for (int gg = 0; gg < kGroupsT; ++gg)
+        for (int gg = 0; gg < kGroupsT; ++gg) {
+            const T *ap = add + pix0 + (int64_t)(16 * (quarter + kParts4 * gg)) * npix;
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
-                const int o = 16 * (quarter + kParts4 * gg) + q;
-                sv[16 * gg + q] = (add && pin && has_cols)
-                                      ? load_act(add + (b * n + o) * npix + p) : 0.f;
+                sv[16 * gg + q] = (add && pin && has_cols) ? load_act(ap) : 0.f;
+                ap += npix;
             }
+        }
         const bool ok = mbar_wait(&bar, phase++, err);
         tc_after_sync();
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
@@ -396,12 +404,13 @@ k_linear_tc(const T *__restrict__ a, const float *__restrict__ W,
             if (g < NG) {
                 float v[16];
                 tmem_ld16(lane_addr + 16 * g, v);
+                T *op = out + pix0 + (int64_t)(16 * g) * npix;
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
-                    const int o = 16 * g + q;
-                    float r = (ok ? v[q] : 0.f) + bias[o] + sv[16 * gg + q];
+                    float r = (ok ? v[q] : 0.f) + s_bias[16 * g + q] + sv[16 * gg + q];
                     if (apply_gelu) r = gelu(r);
-                    if (pin) Storage<T>::store(out + (b * n + o) * npix + p, r);
+                    if (pin) Storage<T>::store(op, r);
+                    op += npix;
                 }
             }
         }
@@ -537,6 +546,11 @@ k_head_tc(const T *__restrict__ a, const float *__restrict__ W,
         }
         mma_commit(&bar[buf]);
     };
+    // the first layer's biases and the second layer's weights, read once
+    __shared__ float s_b1[16 * 8], s_p2[kMaxCout * 16 * 8];
+    for (int o = tid; o < n; o += kThreads) s_b1[o] = bias[o];
+    for (int e = tid; e < cout2 * n; e += kThreads) s_p2[e] = P2[e];
+    __syncthreads();
     int64_t tile = blockIdx.x;
     if (tile < ntiles) {
         load_split(tile, 0);
@@ -567,10 +581,10 @@ k_head_tc(const T *__restrict__ a, const float *__restrict__ W,
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
                     const int o = 16 * g + q;
-                    const float h = gelu((ok ? v[q] : 0.f) + bias[o]);
+                    const float h = gelu((ok ? v[q] : 0.f) + s_b1[o]);
 #pragma unroll
                     for (int c = 0; c < kMaxCout; ++c)
-                        if (c < cout2) hacc[c] = fmaf(P2[(int64_t)c * n + o], h, hacc[c]);
+                        if (c < cout2) hacc[c] = fmaf(s_p2[c * n + o], h, hacc[c]);
                 }
             }
         }

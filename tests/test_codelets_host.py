@@ -32,3 +32,21 @@ def test_codelets_match_brute_force(output):
 def test_constexpr_twiddles_are_double_accurate(output):
     tw = [r for r in output if r[0] == "twiddles"][0]
     assert float(tw[1]) < 1e-14
+
+
+def test_gelu_erf_within_its_published_bound():
+    # erf by Abramowitz & Stegun 7.1.26 (|error| <= 1.5e-7): the GELU error is at
+    # most |v|/2 of that plus float rounding, far inside the float32 tolerance
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    import tempfile
+    with tempfile.TemporaryDirectory() as d:
+        exe = os.path.join(d, "gelu")
+        src = os.path.join(ROOT, "tests", "host", "gelu_check.cu")
+        inc = os.path.join(ROOT, "fft_gemm_ifft_gb300", "csrc")
+        subprocess.run([nvcc, "-std=c++17", "-O2", "-I", inc, src, "-o", exe], check=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout.split()
+    worst, worst_rel, n = float(out[0]), float(out[1]), int(out[2])
+    assert n > 2000000
+    assert worst_rel <= 2.5e-7, (worst, worst_rel)
