@@ -1320,6 +1320,7 @@ struct Pdl {
             m.mblk = (int)Cf::MBLK;
             m.nk = Cf::NK;
             m.packed = p.mix_image ? 2 : a.wpacked;
+            m.num_sms = p.num_sms;
             e = mixtc_launch(p.dtype, m, s);
         } else {
             cfg.gridDim = dim3(nB);

@@ -38,12 +38,14 @@ struct MixTcArgs {
     const void *X;                // kept modes: [group of 8 modes][batch * cin][8] 16-bit
                                   // (re, im) pairs, as kernel A writes them (mixtc_x_bytes)
     const void *w;                // weights (2, cin, cout, m0, m1) interleaved complex
-    void *Y;                      // mixed modes [batch * cout][nk] as 16-bit (re, im) pairs
+    void *Y;                      // mixed modes: [group of 8 modes][batch * cout][8] 16-bit
+                                  // (re, im) pairs, as kernel C gathers them
     int *err;
-    fno_trace_record_t *trace;    // nullptr unless tracing
+    fno_trace_record_t *trace;    // nullptr unless tracing: one record per run of 4 modes
     int trace_first;
     int batch, cin, cout, m0, m1, mblk, nk;
     int packed;                   // w packed: 1 mode-major groups of four, 2 operand images
+    int num_sms;                  // persistent grid: at most one CTA per SM
 };
 bool mixtc_supported(int d, fno_dtype_t dtype, int64_t batch, int cin, int cout, int m1,
                      int64_t nkept);

@@ -51,25 +51,27 @@ namespace {
 
 using namespace tcu;
 
-constexpr int kMT = 256;                  // threads
-constexpr int kGrp = 8;                   // kept modes per group of the X layout
-constexpr int kRun = 4;                   // kept modes per CTA: half a group
+constexpr int kMT = 512;                  // threads
+constexpr int kGrp = 8;                   // kept modes per group of the X / Y layout
+constexpr int kRun = 4;                   // kept modes per work unit: half a group
 constexpr int kCh = 64;                   // channel tile (Cin, Cout <= 64)
-constexpr int kMaxN = 32;                 // batch rows (N) per CTA
-constexpr int kSlots = 3;                 // weight ring
+constexpr int kMaxN = 32;                 // batch rows (N)
 constexpr uint32_t kHalfTile = 64 * 128;  // 64 rows x 128 bytes
 constexpr uint32_t kASlot = 3 * kHalfTile;          // [-Wi^T | Wr^T | Wi^T]
 constexpr uint32_t kImgMode = 2 * kHalfTile;        // packed bytes per mode
 constexpr uint32_t kXMode = 2 * kMaxN * 128;        // a mode's X operand: [Re | Im] x 32 rows
-// shared memory: the run's 4 X operands, then the weight ring; after the MMAs
-// the Y staging goes over both (B * Cout images x 5 words: a padded row keeps
-// the drain free of bank conflicts).  Two CTAs per SM.
+constexpr uint32_t kXUnit = kRun * kXMode;          // a unit's X operands
+// shared memory (one persistent CTA per SM): two buffers of a unit's X
+// operands (the next unit's are transposed in while the current one's MMAs
+// run), the unit's four weight slots, and the Y staging (B * Cout images x 5
+// words: a padded row keeps the drain free of bank conflicts)
 constexpr uint32_t kStageRow = kRun + 1;            // words per staged image
-constexpr uint32_t kOffW = kRun * kXMode;
-constexpr uint32_t kSmem = kOffW + kSlots * kASlot + 1024;
-constexpr uint32_t kTmemCols = 128;                 // kRun modes x N (<= 32)
-static_assert(2 * (kSmem + 256) <= 232448, "two CTAs per SM");
-static_assert((uint32_t)kMaxN * kCh * kStageRow * 4 <= kOffW + kSlots * kASlot, "staging fits");
+constexpr uint32_t kOffW = 2 * kXUnit;
+constexpr uint32_t kOffStage = kOffW + kRun * kASlot;
+constexpr uint32_t kStageBytes = (uint32_t)kMaxN * kCh * kStageRow * 4;
+constexpr uint32_t kSmem = kOffStage + kStageBytes + 1024;
+constexpr uint32_t kTmemCols = 256;                 // two units x kRun modes x N (<= 32)
+static_assert(kSmem + 256 <= 232448, "one CTA per SM");
 
 template <typename T> struct Bits;
 template <> struct Bits<__half> {
@@ -97,59 +99,61 @@ __device__ __forceinline__ void expect_tx(uint64_t *bar, uint32_t bytes) {
 }
 
 template <typename T, bool kImg>
-__global__ void __launch_bounds__(kMT, 2) k_mix_tc(MixTcArgs a) {
+__global__ void __launch_bounds__(kMT, 1) k_mix_tc(MixTcArgs a) {
     extern __shared__ __align__(1024) char smem_raw[];
     char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
-    __shared__ __align__(8) uint64_t bar_w[kSlots], bar_m[kSlots];
+    __shared__ __align__(8) uint64_t bar_w[kRun], bar_m[2];
     __shared__ uint32_t s_tmem;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const unsigned long long t0 = a.trace ? trace_now() : 0;
-    const int grp = blockIdx.x / 2, half = blockIdx.x % 2;
-    const int mode0 = grp * kGrp + half * kRun;
     const int nbp = (a.batch + 15) / 16 * 16;                // N: batch padded to 16
     const int nimg_in = a.batch * a.cin, nimg_out = a.batch * a.cout;
+    const int nunits = a.nk / kRun;
     const uint32_t sb = tc_smem_addr(base);
-    const bool inside = mode0 >= 0 && mode0 + kRun <= a.nk;  // the run lies in the tensors
     if (tid == 0) {
-        for (int s = 0; s < kSlots; ++s) {
+        for (int s = 0; s < kRun; ++s)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_w[s])));
+        for (int s = 0; s < 2; ++s)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_m[s])));
-        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        if (!inside) raise_dev_error(a.err, kDevBounds);
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(tc_smem_addr(&s_tmem)), "r"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
+    // both X operand buffers start at zero: rows past the batch and columns past
+    // cin are never written and must not hold stale bits (NaN times zero)
+    for (int e = tid; e < (int)(2 * kXUnit / 16); e += kMT)
+        reinterpret_cast<uint4 *>(base)[e] = make_uint4(0, 0, 0, 0);
     // every thread waits on the barriers: they must be initialised first
     __syncthreads();
-    // mode r of the run sits in slot r % kSlots
-    auto slot_at = [&](int r) -> char * { return base + kOffW + (r % kSlots) * kASlot; };
-    // The packed weight image of mode r into the last two thirds of its slot
-    // (thread 0; nothing is copied for a run outside the tensors).
-    auto fetch_w = [&](int r) {
-        const int sl = r % kSlots;
-        expect_tx(&bar_w[sl], inside ? kImgMode : 0u);
-        if (inside)
-            bulk_g2s(tc_smem_addr(slot_at(r) + kHalfTile),
-                     static_cast<const char *>(a.w) + (size_t)(mode0 + r) * kImgMode, kImgMode,
-                     &bar_w[sl]);
+    auto slot_at = [&](int r) -> char * { return base + kOffW + r * kASlot; };
+    // the packed weight images of unit u's modes into the last two thirds of
+    // the four slots (thread 0)
+    auto fetch_w = [&](int u) {
+        const bool in = u >= 0 && (u + 1) * kRun <= a.nk;
+        if (!in) raise_dev_error(a.err, kDevBounds);
+        for (int r = 0; r < kRun; ++r) {
+            expect_tx(&bar_w[r], in ? kImgMode : 0u);
+            if (in)
+                bulk_g2s(tc_smem_addr(slot_at(r) + kHalfTile),
+                         static_cast<const char *>(a.w) + ((size_t)u * kRun + r) * kImgMode,
+                         kImgMode, &bar_w[r]);
+        }
     };
-    // The slot of mode r = [-Wi^T | Wr^T | Wi^T] from the weight tensor (all
-    // threads; element (o, i) of each tile).
-    auto build_w = [&](int r) {
+    // slot r = [-Wi^T | Wr^T | Wi^T] of kept mode kk from the weight tensor
+    // (all threads; element (o, i) of each tile)
+    auto build_w = [&](int r, int kk) {
         char *slot = slot_at(r);
-        const int kk = mode0 + r, j = kk / a.m1, k = kk % a.m1;
+        const int j = kk / a.m1, k = kk % a.m1;
         const int blk = j >= a.m0 ? 1 : 0;
         const int local = (j - blk * a.m0) * a.m1 + k;
         const T *w = static_cast<const T *>(a.w);
         for (int e = tid; e < kCh * kCh; e += kMT) {
             const int o = e % kCh, i = e / kCh;
             uint32_t word = 0;
-            if (inside && i < a.cin && o < a.cout) {
+            if (i < a.cin && o < a.cout) {
                 const T *p = a.packed ? w + packed_index(kk, i, o, a.cin, a.cout) * 2
                                       : w + ((((size_t)blk * a.cin + i) * a.cout + o) * a.mblk +
                                              local) * 2;
@@ -163,172 +167,175 @@ __global__ void __launch_bounds__(kMT, 2) k_mix_tc(MixTcArgs a) {
             *reinterpret_cast<unsigned short *>(slot + 2 * kHalfTile + off) = im;
         }
     };
-    // 1. the weights of modes 0-2 (independent of kernel A)
-    if constexpr (kImg) {
-        if (tid == 0)
-            for (int r = 0; r < kSlots; ++r) fetch_w(r);
-    }
-    if (a.cin < kCh) {
-        // input columns beyond cin stay zero in every X operand
-        for (int e = tid; e < (int)(kRun * kXMode / 16); e += kMT)
-            reinterpret_cast<uint4 *>(base)[e] = make_uint4(0, 0, 0, 0);
-        __syncthreads();                         // zeroing before the transpose writes
-    }
-    pdl_trigger();
-    pdl_wait();                                  // kernel A's kept modes are complete
-    const unsigned long long t1 = a.trace ? trace_now() : 0;
-    // 2. X: image (b, i) holds the run's 4 modes (re, im) as 16 contiguous bytes
-    //    of its group row; all of a thread's loads are in flight before the
-    //    transpose writes mode r's Re (chunk 0) and Im (chunk 1) at row b,
-    //    column i.  A warp takes 32 consecutive images: each of its 2-byte
-    //    stores fills 64 contiguous bytes.
-    if (inside) {
+    // unit u's kept modes: image (b, i) holds the unit's 4 modes (re, im) as 16
+    // contiguous bytes of its group row; all of a thread's loads are in flight
+    // before the transpose writes mode r's Re (chunk 0) and Im (chunk 1) at row
+    // b, column i of X operand buffer xo.  A warp takes 32 consecutive images:
+    // each of its 2-byte stores fills 64 contiguous bytes.
+    auto load_x = [&](int u, char *xo) {
+        const int grp = u / 2, half = u % 2;
         const char *xg = static_cast<const char *>(a.X) + (size_t)grp * nimg_in * 32 + half * 16;
-        constexpr int kPer = 8;                  // images per thread per round
+        constexpr int kPer = 4;
         for (int img0 = 0; img0 < nimg_in; img0 += kPer * kMT) {
             uint4 v[kPer];
 #pragma unroll
-            for (int u = 0; u < kPer; ++u) {
-                const int img = img0 + u * kMT + tid;
+            for (int q = 0; q < kPer; ++q) {
+                const int img = img0 + q * kMT + tid;
                 const int64_t word = ((int64_t)grp * nimg_in + img) * kGrp + half * kRun + 3;
-                v[u] = img < nimg_in && in_bounds(word, (int64_t)a.nk * nimg_in, a.err)
+                v[q] = img < nimg_in && in_bounds(word, (int64_t)a.nk * nimg_in, a.err)
                            ? __ldcg(reinterpret_cast<const uint4 *>(xg + (size_t)img * 32))
                            : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
-            for (int u = 0; u < kPer; ++u) {
-                const int img = img0 + u * kMT + tid;
+            for (int q = 0; q < kPer; ++q) {
+                const int img = img0 + q * kMT + tid;
                 if (img >= nimg_in) break;
                 const uint32_t off = sw_off16(img / a.cin, img % a.cin);
-                const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                const uint32_t w4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
 #pragma unroll
                 for (int r = 0; r < kRun; ++r) {
-                    char *xo = base + r * kXMode;
-                    *reinterpret_cast<unsigned short *>(xo + off) = (unsigned short)(w4[r] & 0xFFFF);
-                    *reinterpret_cast<unsigned short *>(xo + nbp * 128 + off) =
+                    char *m = xo + r * kXMode;
+                    *reinterpret_cast<unsigned short *>(m + off) = (unsigned short)(w4[r] & 0xFFFF);
+                    *reinterpret_cast<unsigned short *>(m + nbp * 128 + off) =
                         (unsigned short)(w4[r] >> 16);
                 }
             }
         }
-    }
-    bool ok = true;
+    };
     const uint32_t tmem = s_tmem;
     const uint32_t idesc = idesc_f16(nbp, Bits<T>::kBf16);
-    // 3. the modes in two batches (0-2, then 3 in the slot of mode 0): every
-    //    slot of a batch made ready (packed: wait for its image and negate
-    //    Wi^T; else built from the weights), one barrier, then thread 0 issues
-    //    one chain per mode
-    for (int r0 = 0; r0 < kRun; r0 += kSlots) {
-        const int r1 = r0 + kSlots < kRun ? r0 + kSlots : kRun;
-        for (int r = r0; r < r1; ++r) {
+    uint32_t *stage = reinterpret_cast<uint32_t *>(base + kOffStage);
+    bool ok = true;
+    // the first unit's weights (independent of kernel A), then its kept modes
+    const int u0 = blockIdx.x;
+    if constexpr (kImg) {
+        if (tid == 0 && u0 < nunits) fetch_w(u0);
+    }
+    pdl_trigger();
+    pdl_wait();                                  // kernel A's kept modes are complete
+    if (u0 < nunits) load_x(u0, base);
+    fence_async_smem();
+    uint32_t it = 0;
+    for (int u = u0; u < nunits; u += gridDim.x, ++it) {
+        const unsigned long long t0 = a.trace ? trace_now() : 0;
+        const int nxt = u + (int)gridDim.x;
+        char *xo = base + (it & 1) * kXUnit;
+        const uint32_t tb = tmem + (it & 1) * (kTmemCols / 2);
+        // a. the unit's weight slots: packed images arrive and Wi^T is negated
+        //    into each slot's first third, or the slots are built from the weights
+        for (int r = 0; r < kRun; ++r) {
             char *slot = slot_at(r);
-            const uint32_t use = (uint32_t)(r / kSlots);       // 0: first use of the slot
             if constexpr (kImg) {
-                ok &= mbar_wait(&bar_w[r % kSlots], use & 1, a.err);
-                for (int e = tid; e < (int)(kHalfTile / 16); e += kMT) {   // -Wi^T, exact
+                ok &= mbar_wait(&bar_w[r], it & 1, a.err);
+                for (int e = tid; e < (int)(kHalfTile / 16); e += kMT) {   // exact sign flip
                     const uint4 v = reinterpret_cast<const uint4 *>(slot + 2 * kHalfTile)[e];
                     reinterpret_cast<uint4 *>(slot)[e] =
                         make_uint4(v.x ^ 0x80008000u, v.y ^ 0x80008000u, v.z ^ 0x80008000u,
                                    v.w ^ 0x80008000u);
                 }
             } else {
-                if (use) {                        // the slot's first mode has been read
-                    ok &= mbar_wait(&bar_m[r % kSlots], 0, a.err);
-                    tc_after_sync();
-                }
-                build_w(r);
+                build_w(r, u * kRun + r);
             }
         }
         fence_async_smem();
         tc_before_sync();
-        __syncthreads();                         // slots (and, at r0 = 0, the X operands) ready
+        __syncthreads();                         // slots, X operands, staging reads done
+        const unsigned long long t1 = a.trace ? trace_now() : 0;
+        // b. one chain per mode into this unit's half of tensor memory; thread 0
+        //    then refills the slots with the next unit's images once they are read
         if (tid == 0) {
             tc_after_sync();
-            for (int r = r0; r < r1; ++r) {
-                if (ok) {
+            if (ok) {
+                for (int r = 0; r < kRun; ++r) {
                     const uint32_t am0 = tc_smem_addr(slot_at(r));
-                    const uint32_t bm = sb + r * kXMode;
+                    const uint32_t bm = tc_smem_addr(xo + r * kXMode);
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         const uint32_t am = am0 + (c == 0 ? kHalfTile : 0u);
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            mma_f16(tmem + r * nbp, desc_sw128(am + q * 32),
+                            mma_f16(tb + r * nbp, desc_sw128(am + q * 32),
                                     desc_sw128(bm + c * nbp * 128 + q * 32), idesc,
                                     (c | q) ? 1u : 0u);
                     }
                 }
-                mma_commit(&bar_m[r % kSlots]);
             }
+            mma_commit(&bar_m[it & 1]);
             if constexpr (kImg) {
-                // the later modes into the slots of the first ones once read
-                if (r0 == 0)
-                    for (int r = kSlots; r < kRun; ++r) {
-                        ok &= mbar_wait(&bar_m[r % kSlots], 0, a.err);
-                        fetch_w(r);
-                    }
+                if (nxt < nunits) {
+                    ok &= mbar_wait(&bar_m[it & 1], (it >> 1) & 1, a.err);
+                    fetch_w(nxt);
+                }
             }
         }
-    }
-    // every chain is done once the last commit of each slot has arrived
-    for (int sl = 0; sl < kSlots; ++sl)
-        ok &= mbar_wait(&bar_m[sl], (sl + kSlots < kRun) ? 1u : 0u, a.err);
-    tc_after_sync();
-    const unsigned long long t2 = a.trace ? trace_now() : 0;
-    // 4. tensor memory -> staging: D row m = o (re) or 64 + o (im), column b;
-    //    staged image row (b * Cout + o) of 5 words, word r = mode r (re, im)
-    uint32_t *stage = reinterpret_cast<uint32_t *>(base);
-    {
-        const int m = 32 * (warp & 3) + lane;
-        const int o = m % kCh, part = m / kCh;
-        for (int r = warp >> 2; r < kRun; r += 2) {            // warps 0-3 even modes, 4-7 odd
-            for (int g = 0; g < nbp / 16; ++g) {
-                float v[16];
-                tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + r * nbp + 16 * g, v);
-                if (o < a.cout) {
+        // c. the next unit's kept modes into the other X buffer (its previous
+        //    unit's MMAs were waited for in the previous iteration)
+        if (nxt < nunits) load_x(nxt, base + ((it + 1) & 1) * kXUnit);
+        fence_async_smem();
+        // d. tensor memory -> staging: D row m = o (re) or 64 + o (im), column b;
+        //    staged image row (b * Cout + o) of 5 words, word r = mode r (re, im)
+        ok &= mbar_wait(&bar_m[it & 1], (it >> 1) & 1, a.err);
+        tc_after_sync();
+        const unsigned long long t2 = a.trace ? trace_now() : 0;
+        {
+            const int m = 32 * (warp & 3) + lane;
+            const int o = m % kCh, part = m / kCh;
+            // warps w, w + 4, ... share tensor-memory lanes: each group of four warps
+            // drains its own modes
+            for (int r = warp >> 2; r < kRun; r += kMT / 128) {
+                for (int g = 0; g < nbp / 16; ++g) {
+                    float v[16];
+                    tmem_ld16(tb + ((uint32_t)(32 * (warp & 3)) << 16) + r * nbp + 16 * g, v);
+                    if (o < a.cout) {
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const int b = 16 * g + q;
-                        if (b < a.batch)
-                            reinterpret_cast<unsigned short *>(
-                                stage + ((size_t)b * a.cout + o) * kStageRow + r)[part] =
-                                Bits<T>::from(ok ? v[q] : 0.f);
+                        for (int q = 0; q < 16; ++q) {
+                            const int b = 16 * g + q;
+                            if (b < a.batch)
+                                reinterpret_cast<unsigned short *>(
+                                    stage + ((size_t)b * a.cout + o) * kStageRow + r)[part] =
+                                    Bits<T>::from(ok ? v[q] : 0.f);
+                        }
                     }
                 }
+            }
+        }
+        tc_before_sync();
+        __syncthreads();
+        // e. Y in the group layout: each image's 4 modes as one 16-byte piece of
+        //    its 32-byte group row, so a warp's 32 consecutive images fill 1 KiB
+        {
+            const int grp = u / 2, half = u % 2;
+            uint32_t *yg = static_cast<uint32_t *>(a.Y) + (size_t)grp * nimg_out * kGrp + half * kRun;
+            for (int img = tid; img < nimg_out; img += kMT) {
+                const uint32_t *sv = stage + (size_t)img * kStageRow;
+                const int64_t word = ((int64_t)grp * nimg_out + img) * kGrp + half * kRun + 3;
+                if (in_bounds(word, (int64_t)a.nk * nimg_out, a.err))
+                    *reinterpret_cast<uint4 *>(yg + (size_t)img * kGrp) =
+                        make_uint4(sv[0], sv[1], sv[2], sv[3]);
+            }
+        }
+        if (a.trace) {
+            __syncthreads();
+            if (tid == 0) {
+                unsigned smid;
+                asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+                fno_trace_record_t rec;
+                rec.item = (1u << 24) | ((unsigned)u & 0xFFFFFFu);
+                rec.worker = smid;
+                rec.t_start = t0;
+                rec.t_ready = t1;
+                rec.t_compute = t2;
+                rec.t_end = trace_now();
+                a.trace[a.trace_first + u] = rec;
             }
         }
     }
     tc_before_sync();
     __syncthreads();
-    // 5. Y in the group layout: each image's 4 modes as one 16-byte piece of its
-    //    32-byte group row, so a warp's 32 consecutive images fill 1 KiB
-    uint32_t *yg = static_cast<uint32_t *>(a.Y) + (size_t)grp * nimg_out * kGrp + half * kRun;
-    for (int img = tid; img < nimg_out && inside; img += kMT) {
-        const uint32_t *sv = stage + (size_t)img * kStageRow;
-        const int64_t word = ((int64_t)grp * nimg_out + img) * kGrp + half * kRun + 3;
-        if (in_bounds(word, (int64_t)a.nk * nimg_out, a.err))
-            *reinterpret_cast<uint4 *>(yg + (size_t)img * kGrp) =
-                make_uint4(sv[0], sv[1], sv[2], sv[3]);
-    }
     if (warp == 0) {
         tc_after_sync();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols));
-    }
-    if (a.trace) {
-        __syncthreads();
-        if (tid == 0) {
-            unsigned smid;
-            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-            fno_trace_record_t rec;
-            rec.item = (1u << 24) | (blockIdx.x & 0xFFFFFFu);
-            rec.worker = smid;
-            rec.t_start = t0;
-            rec.t_ready = t1;
-            rec.t_compute = t2;
-            rec.t_end = trace_now();
-            a.trace[a.trace_first + blockIdx.x] = rec;
-        }
     }
 }
 
@@ -400,7 +407,8 @@ cudaError_t mixtc_launch(fno_dtype_t dtype, const MixTcArgs &args, cudaStream_t 
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(args.nk / kRun));
+    const int nunits = args.nk / kRun;
+    cfg.gridDim = dim3((unsigned)(nunits < args.num_sms ? nunits : args.num_sms));
     cfg.blockDim = dim3(kMT);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = s;
