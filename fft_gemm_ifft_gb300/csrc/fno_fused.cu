@@ -242,6 +242,7 @@ __global__ void __launch_bounds__(kNT) k_phase_c(Args a) {
     const Tw tw = load_twiddles<Cf>(a, smem);
     __syncthreads();
     pdl_wait();                                  // kernel B's mixed modes are complete
+    pdl_trigger();                               // a dependent kernel may set itself up
     const unsigned long long t1 = a.trace ? trace_now() : 0;
     const int item = blockIdx.x;
     phase_c<Cf, T>(a.Y, static_cast<T *>(a.y), item / Cf::C, item % Cf::C, smem + Cf::kSmemTw, tw);
@@ -809,6 +810,7 @@ k_phase_c_tc32(const __grid_constant__ CUtensorMap ymap, Args a, const void *tab
     tc_after_sync();
     const uint32_t tmem = s_tmem;
     pdl_wait();                                  // kernel B's mixed modes are complete
+    pdl_trigger();                               // a dependent kernel may set itself up
     const unsigned long long t1 = a.trace ? trace_now() : 0;
     const float2 *src = a.Y + (size_t)img * Gm::NK;
     for (int e = tid; e < Gm::NK / 2; e += NT) cp_async16(ys + 2 * e, src + 2 * e);

@@ -4,8 +4,9 @@
 //   erf(x) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) e^{-x^2},
 //   t = 1 / (1 + p x),  x >= 0,  |error| <= 1.5e-7,
 // and erf(-x) = -erf(x).  With r = 1 - erf(|v| / sqrt 2) = poly(t) e^{-v^2/2},
-// GELU(v) = v (1 - r/2) for v >= 0 and v r / 2 for v < 0, so the small values
-// on the negative side keep their relative precision.  __host__ __device__ so
+// GELU(v) = v (1 - r/2) for v >= 0 and v r / 2 for v < 0, i.e. max(v, 0) -
+// |v| r / 2 (one fused multiply-add, no branch), so the small values on the
+// negative side keep their relative precision.  __host__ __device__ so
 // that the host check in tests/host can compare it with a double-precision
 // erf; on the device the exponential and the reciprocal are the fast
 // hardware approximations (a few ulp, far below the formula's own error).
@@ -29,7 +30,7 @@ __host__ __device__ __forceinline__ float gelu_erf(float v) {
 #endif
     const float q = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, a5, a4), a3), a2), a1);
     const float r = q * e;
-    return v >= 0.0f ? fmaf(-0.5f * v, r, v) : 0.5f * v * r;
+    return fmaf(-0.5f * fabsf(v), r, fmaxf(v, 0.0f));
 }
 
 }  // namespace fno

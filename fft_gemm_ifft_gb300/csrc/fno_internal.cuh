@@ -118,6 +118,9 @@ template <> struct Storage<float> {
     static __device__ __forceinline__ void store4(float *p, float4 v) {
         *reinterpret_cast<float4 *>(p) = v;
     }
+    // read or written once: streaming cache hints
+    static __device__ __forceinline__ float load_stream(const float *p) { return __ldcs(p); }
+    static __device__ __forceinline__ void store_stream(float *p, float v) { __stcs(p, v); }
 };
 template <> struct Storage<__half> {
     static __device__ __forceinline__ float load(const __half *p) { return __half2float(*p); }
@@ -132,6 +135,12 @@ template <> struct Storage<__half> {
     static __device__ __forceinline__ void store4(__half *p, float4 v) {
         reinterpret_cast<__half2 *>(p)[0] = __floats2half2_rn(v.x, v.y);
         reinterpret_cast<__half2 *>(p)[1] = __floats2half2_rn(v.z, v.w);
+    }
+    static __device__ __forceinline__ float load_stream(const __half *p) {
+        return __half2float(__ldcs(p));
+    }
+    static __device__ __forceinline__ void store_stream(__half *p, float v) {
+        __stcs(p, __float2half_rn(v));
     }
 };
 
@@ -152,6 +161,12 @@ template <> struct Storage<__nv_bfloat16> {
     static __device__ __forceinline__ void store4(__nv_bfloat16 *p, float4 v) {
         reinterpret_cast<__nv_bfloat162 *>(p)[0] = __floats2bfloat162_rn(v.x, v.y);
         reinterpret_cast<__nv_bfloat162 *>(p)[1] = __floats2bfloat162_rn(v.z, v.w);
+    }
+    static __device__ __forceinline__ float load_stream(const __nv_bfloat16 *p) {
+        return __bfloat162float(__ldcs(p));
+    }
+    static __device__ __forceinline__ void store_stream(__nv_bfloat16 *p, float v) {
+        __stcs(p, __float2bfloat16_rn(v));
     }
 };
 
