@@ -13,7 +13,8 @@
 // copy, so that no thread's synchronisation waits on its own loads or stores:
 // * a load warp brings the activations [cin][128 pixels] into a ring of
 //   two to four shared-memory stages, that many tiles ahead;
-// * 16 compute warps (thread = one pixel row and a quarter of the channels)
+// * 16 compute warps (thread = one pixel row and a quarter of the channels:
+//   kParts = 4 threads per pixel row; 8 compute warps measured slower)
 //   transpose and split a tile's activations into the K-major 128-byte-
 //   swizzled A operand, then run the previous tile's epilogue: a layer adds
 //   bias and spectral branch and applies the GELU in place in the branch
@@ -38,8 +39,9 @@ namespace {
 
 using namespace tcu;
 
-constexpr int kCompute = 512;            // compute threads: four per pixel row of a tile
+constexpr int kCompute = 512;            // compute threads: kParts per pixel row of a tile
 constexpr int kWarps = kCompute / 32;
+constexpr int kParts = kWarps / 4;       // compute warps sharing one tensor-memory lane quarter
 constexpr int kThreads = kCompute + 96;  // + the load, MMA and store warps
 constexpr int kRows = 128;               // M: pixels per tile
 constexpr uint32_t kChunk = 16384;       // 128 rows x 128 bytes = 32 fp32 of K
@@ -65,7 +67,7 @@ struct Lay {
     // sums, barriers), bounded from above; it comes in whole kilobytes ahead
     // of the 1024-aligned dynamic part
     static constexpr uint32_t kStatic =
-        align1k(4u * (kN + (HEAD ? C2 * kN + 2 * 3 * C2 * kRows : 1) + C2) + 512);
+        align1k(4u * (kN + (HEAD ? C2 * kN + 2 * (kParts - 1) * C2 * kRows : 1) + C2) + 512);
     // as many activation stages (at most four) as the shared memory holds
     // beside the operands and, for a layer, two branch tiles
     static constexpr uint32_t kFixed = kX + (HEAD ? 0u : 2 * kSBytes) + 1024 + kStatic;
@@ -118,7 +120,8 @@ k_pointwise_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
     __shared__ uint32_t s_tmem;
     __shared__ __align__(16) float s_bias[L::kN];        // read as float4
     __shared__ float s_p2[HEAD ? C2 * L::kN : 1], s_c2[C2];
-    __shared__ float s_red[HEAD ? 2 * 3 * C2 * kRows : 1];   // head: quarters 1-3, two tiles
+    // head: the partial second projections of parts 1.. of a pixel, two tiles
+    __shared__ float s_red[HEAD ? 2 * (kParts - 1) * C2 * kRows : 1];
     const int tid = threadIdx.x, warp = tid >> 5;
     const int cin = p.cin, n = p.n;
 
@@ -248,9 +251,9 @@ k_pointwise_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
             bulk_wait_all();                                // the stores have landed
         }
     } else {
-        // ---- compute warps: thread -> (pixel row, quarter); warps w, w+4, w+8,
+        // ---- compute warps: thread -> (pixel row, part); warps w, w+4, w+8,
         // w+12 share tensor-memory lanes
-        const int row = 32 * (warp & 3) + (tid & 31), quarter = warp >> 2;
+        const int row = 32 * (warp & 3) + (tid & 31), part = warp >> 2;
         // the weights, hi and lo, as the B operand (N rows = outputs, K =
         // inputs), zero past n outputs and cin inputs; every load in flight
         // before the first store (the activations are on their way meanwhile)
@@ -281,8 +284,8 @@ k_pointwise_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
             for (int c = tid; c < C2; c += kCompute) s_c2[c] = c < p.cout2 ? p.c2[c] : 0.f;
         }
         compute_sync();                               // biases and head weights are in place
-        constexpr int kPerT = L::kK / 4;                      // input channels per thread
-        const int i0 = quarter * kPerT;
+        constexpr int kPerT = L::kK / kParts;                 // input channels per thread
+        const int i0 = part * kPerT;
         for (int64_t j = 0; j <= nt; ++j) {
             if (j < nt) {
                 // tile j: activations into the A operand (free once tile j - 1's
@@ -318,26 +321,35 @@ k_pointwise_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
                     tmem + (uint32_t)buf * L::kN + ((uint32_t)(32 * (warp & 3)) << 16);
                 if constexpr (!HEAD) {
                     T *S = reinterpret_cast<T *>(s_tile(buf));
-                    const int g = quarter;                    // n <= 64: one group per thread
-                    float v[16];
-                    if (16 * g < n) tmem_ld16(lane_addr + 16 * g, v);
+                    // groups part, part + kParts, ... of 16 outputs
+                    constexpr int kG = (NG + kParts - 1) / kParts;
+                    float v[kG][16];
+#pragma unroll
+                    for (int gg = 0; gg < kG; ++gg) {
+                        const int g = part + kParts * gg;
+                        if (g < NG && 16 * g < n) tmem_ld16(lane_addr + 16 * g, v[gg]);
+                    }
                     tc_before_sync();
                     warp_arrive(&acc_empty[buf]);
                     mbar_wait(&s_full[buf], (uint32_t)(jj >> 1), p.err);
-                    if (16 * g < n) {
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const float4 b4 =
-                                *reinterpret_cast<const float4 *>(&s_bias[16 * g + 4 * q4]);
-                            const float bq[4] = {b4.x, b4.y, b4.z, b4.w};
+                    for (int gg = 0; gg < kG; ++gg) {
+                        const int g = part + kParts * gg;
+                        if (g < NG && 16 * g < n) {
 #pragma unroll
-                            for (int q1 = 0; q1 < 4; ++q1) {
-                                const int q = 4 * q4 + q1;
-                                T *sp = S + (16 * g + q) * kRows + row;
-                                float r = v[q] + bq[q1];
-                                if (has_add) r += Storage<T>::load(sp);
-                                if (p.gelu) r = gelu_erf(r);
-                                Storage<T>::store(sp, r);
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                const float4 b4 =
+                                    *reinterpret_cast<const float4 *>(&s_bias[16 * g + 4 * q4]);
+                                const float bq[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                                for (int q1 = 0; q1 < 4; ++q1) {
+                                    const int q = 4 * q4 + q1;
+                                    T *sp = S + (16 * g + q) * kRows + row;
+                                    float r = v[gg][q] + bq[q1];
+                                    if (has_add) r += Storage<T>::load(sp);
+                                    if (p.gelu) r = gelu_erf(r);
+                                    Storage<T>::store(sp, r);
+                                }
                             }
                         }
                     }
@@ -348,8 +360,8 @@ k_pointwise_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
 #pragma unroll
                     for (int c = 0; c < C2; ++c) hacc[c] = 0.f;
 #pragma unroll
-                    for (int gg = 0; gg < (NG + 3) / 4; ++gg) {
-                        const int g = quarter + 4 * gg;
+                    for (int gg = 0; gg < (NG + kParts - 1) / kParts; ++gg) {
+                        const int g = part + kParts * gg;
                         if (g < NG && 16 * g < n) {
                             float v[16];
                             tmem_ld16(lane_addr + 16 * g, v);
@@ -371,20 +383,20 @@ k_pointwise_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
                     }
                     tc_before_sync();
                     warp_arrive(&acc_empty[buf]);
-                    // the four threads of a pixel sum their partial second
+                    // the kParts threads of a pixel sum their partial second
                     // projections (a buffer per tile parity: a warp is at most
                     // one tile ahead of another)
-                    float *red = s_red + buf * 3 * C2 * kRows;
-                    if (quarter > 0) {
+                    float *red = s_red + buf * (kParts - 1) * C2 * kRows;
+                    if (part > 0) {
 #pragma unroll
                         for (int c = 0; c < C2; ++c)
-                            red[((quarter - 1) * C2 + c) * kRows + row] = hacc[c];
+                            red[((part - 1) * C2 + c) * kRows + row] = hacc[c];
                     }
                     compute_sync();
                     int c0, b;
                     tile_at(jj, c0, b);
                     const int64_t px = c0 + row;
-                    if (quarter == 0 && px < p.npix) {
+                    if (part == 0 && px < p.npix) {
                         // the head's only global stores: one value per pixel and output
                         T *op = static_cast<T *>(p.out) + (int64_t)b * p.cout2 * p.npix + px;
 #pragma unroll
@@ -392,7 +404,7 @@ k_pointwise_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
                             if (c < p.cout2) {
                                 float v = s_c2[c] + hacc[c];
 #pragma unroll
-                                for (int qq = 0; qq < 3; ++qq)
+                                for (int qq = 0; qq < kParts - 1; ++qq)
                                     v += red[(qq * C2 + c) * kRows + row];
                                 Storage<T>::store(op + (int64_t)c * p.npix, v);
                             }
