@@ -91,13 +91,15 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_digest() -> str:
-    """Digest of the CUDA sources: a traffic figure taken from an ncu capture
-    is reported only while the kernels are unchanged since that capture."""
+def kernel_source_digest(sources=None) -> str:
+    """Digest of the CUDA sources behind a workload's kernels (the listed
+    translation units and every header; all units when none are listed): a
+    traffic figure taken from an ncu capture is reported only while those
+    kernels are unchanged since that capture."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fft_gemm_ifft_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh")):
+        if fn.endswith(".cuh") or (fn.endswith(".cu") and (sources is None or fn in sources)):
             with open(os.path.join(csrc, fn), "rb") as f:
                 h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
@@ -111,7 +113,7 @@ def recorded_traffic(workload: str):
         with open(path) as f:
             d = json.load(f)
         e = d[workload]
-        if e.get("source_digest") != kernel_source_digest():
+        if e.get("source_digest") != kernel_source_digest(e.get("sources")):
             return None
         return int(e["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):

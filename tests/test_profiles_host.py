@@ -50,7 +50,31 @@ def test_stale_record_is_not_reported(tmp_path, monkeypatch):
     (csrc / "k.cu").write_text("// kernel")
     monkeypatch.setattr(bench, "ROOT", str(fake_root))
     assert bench.recorded_traffic("2d_f32") is None
-    d["2d_f32"]["source_digest"] = bench.kernel_source_digest()
+    d["2d_f32"]["source_digest"] = bench.kernel_source_digest(d["2d_f32"].get("sources"))
     (fake_root / "profiles" / "traffic.json").write_text(json.dumps(d))
     assert bench.recorded_traffic("2d_f32") == d["2d_f32"]["dram_bytes_per_launch"]
     assert bench.recorded_traffic("no_such_workload") is None
+
+
+def test_record_follows_only_its_own_sources(tmp_path, monkeypatch):
+    # a record names the translation units of its kernels: editing another
+    # unit keeps it, editing one of its own (or any header) retires it
+    csrc = tmp_path / "fft_gemm_ifft_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (csrc / "mine.cu").write_text("// a")
+    (csrc / "other.cu").write_text("// b")
+    (csrc / "shared.cuh").write_text("// c")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    rec = {"w": {"dram_bytes_per_launch": 5, "sources": ["mine.cu"],
+                 "source_digest": bench.kernel_source_digest(["mine.cu"])}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    assert bench.recorded_traffic("w") == 5
+    (csrc / "other.cu").write_text("// b changed")
+    assert bench.recorded_traffic("w") == 5
+    (csrc / "shared.cuh").write_text("// c changed")
+    assert bench.recorded_traffic("w") is None
+    rec["w"]["source_digest"] = bench.kernel_source_digest(["mine.cu"])
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    (csrc / "mine.cu").write_text("// a changed")
+    assert bench.recorded_traffic("w") is None
