@@ -1210,14 +1210,24 @@ struct Pdl {
         // tensor-core mixing where the kept modes arrive reduced (one copy)
         p.fused_mixtc = mix16(p.g, p.dtype, p.batch, p.cin, p.cout, p.flags);
         if (e == cudaSuccess && p.fused_mixtc) e = mixtc_init(p.dtype);
+        // fp32, on request: the 3xTF32 tensor-core mixing where kernel A writes
+        // one reduced copy of the kept modes and the weights are in the
+        // standard layout
+        p.fused_mixtf32 = false;
+        if constexpr (std::is_same<T, float>::value)
+            p.fused_mixtf32 = (p.flags & FNO_PLAN_TENSOR_MIX) && p.fused_tca &&
+                              !(p.flags & (FNO_PLAN_SIMT_MIX | FNO_PLAN_PACKED_WEIGHTS)) &&
+                              mixtf32_supported(p.batch, p.cin, p.cout, Cf::M1, p.g.nkept);
+        if (e == cudaSuccess && p.fused_mixtf32) e = mixtf32_init();
         p.mix_image = p.fused_mixtc && (p.flags & FNO_PLAN_PACKED_WEIGHTS) &&
                       mixtc_image_layout(p.cin, p.cout);
         p.fused_bstream = 0;
 
         if (e == cudaSuccess && (p.flags & FNO_PLAN_TRACE)) {
-            const size_t nB = p.fused_mixtc ? (size_t)mixtc_items(p.g.nkept)
-                                            : (size_t)(p.g.nkept / kG) * ((p.cout + ob - 1) / ob) *
-                                                  ((p.batch + bb - 1) / bb);
+            const size_t nB = p.fused_mixtc     ? (size_t)mixtc_items(p.g.nkept)
+                              : p.fused_mixtf32 ? (size_t)(p.g.nkept / 2)
+                                                : (size_t)(p.g.nkept / kG) * ((p.cout + ob - 1) / ob) *
+                                                      ((p.batch + bb - 1) / bb);
             const size_t nA = (size_t)p.batch * p.cin * (p.fused_tca ? 1 : Cf::C);
             const size_t nC = (size_t)p.batch * p.cout * (p.fused_tcc ? 1 : CfC::C);
             p.trace_records = nA + nC + nB;
@@ -1252,7 +1262,9 @@ struct Pdl {
         a.nob = (p.cout + a.ob - 1) / a.ob;
         a.npairs = (int)(p.g.nkept / kG);
         const int nA = (int)p.batch * p.cin * (p.fused_tca ? 1 : Cf::C);
-        const int nB = p.fused_mixtc ? mixtc_items(p.g.nkept) : a.npairs * a.nob * a.ng;
+        const int nB = p.fused_mixtc     ? mixtc_items(p.g.nkept)
+                       : p.fused_mixtf32 ? (int)(p.g.nkept / 2)
+                                         : a.npairs * a.nob * a.ng;
         const int nC = (int)p.batch * p.cout * (p.fused_tcc ? 1 : CfC::C);
         a.trace = p.trace;
         a.trace_b = nA;
@@ -1324,6 +1336,21 @@ struct Pdl {
             m.packed = p.mix_image ? 2 : a.wpacked;
             m.num_sms = p.num_sms;
             e = mixtc_launch(p.dtype, m, s);
+        } else if (p.fused_mixtf32) {
+            MixTf32Args m;
+            m.X = a.part;
+            m.w = static_cast<const float *>(a.w);
+            m.Y = a.Y;
+            m.err = a.err;
+            m.trace = a.trace;
+            m.trace_first = nA;
+            m.batch = (int)p.batch;
+            m.cin = p.cin;
+            m.cout = p.cout;
+            m.m0 = Cf::M0;
+            m.m1 = Cf::M1;
+            m.nk = Cf::NK;
+            e = mixtf32_launch(m, s);
         } else {
             cfg.gridDim = dim3(nB);
             cfg.blockDim = dim3(kBThreads);

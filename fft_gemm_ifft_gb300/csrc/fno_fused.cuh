@@ -63,6 +63,22 @@ bool mixtc_image_layout(int cin, int cout);
 cudaError_t mixtc_pack_image(fno_dtype_t dtype, const void *w, void *wp, int cin, int cout,
                              int m0, int m1, int mblk, int nk, int num_sms, cudaStream_t s);
 
+// Tensor-core mixing for float32 storage (kernel B of the fp32 128 x 128
+// three-kernel layer, fno_mix_tf32.cu): one CTA per pair of kept modes, the
+// complex products in 3xTF32 on tcgen05.
+struct MixTf32Args {
+    const float2 *X;              // kept modes [batch * cin][nk] (one reduced copy)
+    const float *w;               // weights (2, cin, cout, m0, m1) interleaved complex
+    float2 *Y;                    // mixed modes [batch * cout][nk]
+    int *err;
+    fno_trace_record_t *trace;    // nullptr unless tracing: one record per pair
+    int trace_first;
+    int batch, cin, cout, m0, m1, nk;
+};
+bool mixtf32_supported(int64_t batch, int cin, int cout, int m1, int64_t nkept);
+cudaError_t mixtf32_init();
+cudaError_t mixtf32_launch(const MixTf32Args &a, cudaStream_t s);
+
 // Kernel C of the 16-bit 256 x 256 layer (fno_inv16.cu): the column and row
 // inverse DFTs of each output image as two tcgen05 GEMMs, persistent.
 struct Inv16Args {

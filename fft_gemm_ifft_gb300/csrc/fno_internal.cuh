@@ -63,6 +63,7 @@ struct Plan {
     int fused_bstream;            // > 0: kernel B streams the weights, this many modes a CTA
     void *fused_tables;           // tensor-core path: twiddle operands (plan-owned)
     bool fused_mixtc;             // three-kernel path mixes on the tensor cores
+    bool fused_mixtf32;           // fp32 three-kernel path mixes on the tensor cores (3xTF32)
     bool fused_tca;               // three-kernel path transforms (kernel A) on the tensor cores
     bool fused_tcc;               // ... and inverts (kernel C) on the tensor cores
     bool fused_c1pass;            // fp32 kernel C: one-pass column inverse, 3 CTAs per SM

@@ -92,6 +92,11 @@ def test_query_rejects_unknown_flags_and_nulls(L):
     # bit 4 (a former tensor-core switch that did nothing) is not a flag
     st, _, _ = Q(2, [128, 128], [16, 16], 8, 32, 32, F32, flags=4)
     assert st == capi.FNO_ERR_INVALID_ARG
+    # the tensor-core mixing request is a flag (ignored where it does not apply)
+    for shape in (([128, 128], [16, 16]), ([64], [8])):
+        st, _, _ = Q(len(shape[0]), shape[0], shape[1], 8, 32, 32, F32,
+                     flags=capi.FNO_PLAN_TENSOR_MIX)
+        assert st == capi.FNO_OK
     import ctypes
     assert L.fno_spectral_conv_query(1, None, None, 1, 1, 1, 0, 0, None, None) == \
         capi.FNO_ERR_INVALID_ARG
@@ -155,7 +160,7 @@ def test_backward_flag_adds_workspace(L):
     assert st == capi.FNO_OK and wb1 == wb
     # the adjoint weights, the kept modes of x (8*32*512) and dy (8*16*512)
     assert ws1 >= wb + 8 * 32 * 512 * 8 + 8 * 16 * 512 * 8
-    st, _, _ = Q(1, [16], [4], 1, 1, 1, F32, flags=capi.FNO_PLAN_BACKWARD | 0x100)
+    st, _, _ = Q(1, [16], [4], 1, 1, 1, F32, flags=capi.FNO_PLAN_BACKWARD | 0x1000)
     assert st == capi.FNO_ERR_INVALID_ARG
 
 

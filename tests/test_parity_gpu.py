@@ -31,6 +31,12 @@ SMALL = [
     ((128, 128), (16, 16), 1, 64, 37, "f32"),
     ((128, 128), (16, 16), 9, 3, 2, "f32"),
     ((128, 128), (16, 16), 10, 3, 40, "f32"),    # > 2 output images per SM: one-pass kernel C
+    # fp32 tensor-core mixing: 64 outputs (one mode on M; 16 / 32 batch rows on
+    # N) and 32 outputs (two modes on M; 8 / 16 rows each), 32 or 64 inputs
+    ((128, 128), (16, 16), 16, 64, 64, "f32"),
+    ((128, 128), (16, 16), 20, 32, 64, "f32"),
+    ((128, 128), (16, 16), 5, 64, 32, "f32"),
+    ((128, 128), (16, 16), 12, 32, 32, "f32"),
     ((16, 32), (3, 7), 3, 5, 3, "f32"),
     ((32, 16), (16, 9), 2, 2, 3, "f32"),
     ((64, 64), (16, 16), 2, 8, 8, "f32"),
@@ -68,9 +74,10 @@ def _lib(fno, oracle_mod):
 
 
 @pytest.mark.parametrize("flags", [0, FNO_PLAN_UNFUSED, capi.FNO_PLAN_PERSISTENT,
-                                   capi.FNO_PLAN_SIMT_MIX, capi.FNO_PLAN_SIMT_TRANSFORM],
+                                   capi.FNO_PLAN_SIMT_MIX, capi.FNO_PLAN_SIMT_TRANSFORM,
+                                   capi.FNO_PLAN_TENSOR_MIX],
                          ids=["default", "unfused", "persistent", "simt_mix",
-                              "simt_transform"])
+                              "simt_transform", "tensor_mix"])
 @pytest.mark.parametrize("spec", SMALL, ids=[case_id(c) for c in SMALL])
 def test_small_cases_match_oracle(spec, flags):
     n, modes, b, ci, co, dt = spec
