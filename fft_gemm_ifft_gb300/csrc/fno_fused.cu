@@ -1215,7 +1215,7 @@ struct Pdl {
         // standard layout
         p.fused_mixtf32 = false;
         if constexpr (std::is_same<T, float>::value)
-            p.fused_mixtf32 = (p.flags & FNO_PLAN_TENSOR_MIX) && p.fused_tca &&
+            p.fused_mixtf32 = (p.flags & FNO_PLAN_TENSOR_EXTRA) && p.fused_tca &&
                               !(p.flags & (FNO_PLAN_SIMT_MIX | FNO_PLAN_PACKED_WEIGHTS)) &&
                               mixtf32_supported(p.batch, p.cin, p.cout, Cf::M1, p.g.nkept);
         if (e == cudaSuccess && p.fused_mixtf32) e = mixtf32_init();

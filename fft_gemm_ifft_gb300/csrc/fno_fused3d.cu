@@ -26,6 +26,7 @@
 //     then the half-spectrum row transform with c(0) = 1, c(k) = 2 and the
 //     1/(N0 N1 N2) scale) is stored.
 #include "fno_fused_dev.cuh"
+#include "fno_tc.cuh"
 
 namespace fno {
 namespace {
@@ -335,6 +336,247 @@ __global__ void __launch_bounds__(kNT) k_phase_c3(Args a) {
     cta_record(a, 2, a.trace_c, t0, t1);
 }
 
+// ---------------------------------------------------------------------------
+// Kernel A on the tensor cores (float32 storage): the row DFT of the planes
+// (64 samples -> the 16 kept bins) is a 3xTF32 GEMM per pair of planes,
+// D[(plane, t1)][j] = sum_n x[plane][t1][n] T[j][n] with T[j][n] = cos(2 pi k n
+// / 64) (j = k < 16) or -sin (j = 16 + k): M = 128 rows (two planes), K = 64,
+// in two passes as in the 2-D fp32 kernel, x [T_hi ; T_lo] (N = 64) then
+// x_lo T_hi (N = 32, x_lo written over x).  TMA brings each plane's rows into
+// the K-major 128-byte-swizzled operand directly (two stages of a plane pair);
+// the column DFT, the kept modes and the fold into the chunk's residues over t
+// stay on the SIMT cores as in k_phase_a3, and so does the cluster's axis-0
+// combine.
+struct Geo3A {
+    static constexpr int N = 64, M2 = 16;
+    static constexpr uint32_t kTile = 128u * 128u;      // one K chunk of a plane pair
+    static constexpr uint32_t kPair = 2 * kTile;        // a plane pair (K = 64)
+    static constexpr uint32_t kTChunk = 64u * 128u;     // [T_hi rows 0..31 | T_lo rows 0..31]
+    static constexpr uint32_t kTBytes = 2 * kTChunk;
+    static constexpr uint32_t kRing = 0;                // two plane-pair stages
+    static constexpr uint32_t kT = kRing + 2 * kPair;
+    static constexpr uint32_t kZ = kT + kTBytes;        // two planes' row spectra [N1][ZS]
+    static constexpr uint32_t kTmemCols = 64;
+};
+
+template <class C3>
+__global__ void __launch_bounds__(kNT, 2)
+k_phase_a3_tc(const __grid_constant__ CUtensorMap xmap, Args a, const void *table) {
+    using Pl = typename C3::Pl;
+    using Gm = Geo3A;
+    using namespace tcu;
+    constexpr int N0 = C3::N0, N1 = C3::N1, C0 = C3::C0, R0 = C3::R0, NKP = C3::NKP, QT = C3::QT;
+    constexpr int kPairs = R0 / 2;
+    static_assert(N1 == Gm::N && C3::N2 == Gm::N && C3::M2 == Gm::M2 && R0 % 2 == 0, "64^3");
+    static_assert(kNT == 128, "a warp per tensor-memory lane quarter");
+    constexpr uint32_t kZBytes = (uint32_t)N1 * Pl::ZS * 8;
+    constexpr uint32_t kSs = Gm::kZ + 2 * kZBytes;      // the column pass's sums
+    constexpr uint32_t kTw = kSs + (uint32_t)Pl::A * Pl::B2 * Pl::M1 * 8;
+    extern __shared__ __align__(1024) char smem_raw[];
+    char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+    __shared__ __align__(8) uint64_t bar_t, bar_x[2], bar_p1, bar_fin;
+    __shared__ uint32_t s_tmem;
+    const unsigned long long t0 = a.trace ? trace_now() : 0;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int vol = blockIdx.x / C0, c = blockIdx.x % C0;
+    const float2 *twa;
+    const Tw tw = load_tw3<C3>(a, base + kTw, &twa);
+    // plane pair q (planes c + C0 (2q + p), p = 0, 1) into stage st: rows
+    // p * 64 .. of each K chunk
+    auto issue = [&](int q, int st) {
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     ::"r"(tc_smem_addr(&bar_x[st])), "r"(Gm::kPair) : "memory");
+        for (int pl = 0; pl < 2; ++pl) {
+            const int i0 = c + C0 * (2 * q + pl);
+            const int row0 = (vol * N0 + i0) * N1;
+            for (int kc = 0; kc < 2; ++kc)
+                tma_load_2d(tc_smem_addr(base + Gm::kRing + st * Gm::kPair + kc * Gm::kTile +
+                                         pl * (Gm::kTile / 2)),
+                            &xmap, kc * 32, row0, &bar_x[st]);
+        }
+    };
+    if (tid == 0) {
+        const uint64_t *bars[5] = {&bar_t, &bar_x[0], &bar_x[1], &bar_p1, &bar_fin};
+        for (const uint64_t *b : bars)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(b)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     ::"r"(tc_smem_addr(&bar_t)), "r"(Gm::kTBytes) : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(tc_smem_addr(base + Gm::kT)), "l"(table), "r"(Gm::kTBytes),
+                     "r"(tc_smem_addr(&bar_t)) : "memory");
+        issue(0, 0);
+        if (kPairs > 1) issue(1, 1);
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(tc_smem_addr(&s_tmem)), "r"(Gm::kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_before_sync();
+    __syncthreads();
+    tc_after_sync();
+    pdl_trigger();                               // kernel B may start fetching weights
+    const uint32_t tmem = s_tmem;
+    const uint32_t ts = tc_smem_addr(base + Gm::kT);
+    float2 *ss = reinterpret_cast<float2 *>(base + kSs);
+    bool ok = true;
+    if (tid == 0) ok &= mbar_wait(&bar_t, 0, a.err);
+    float2 acc[R0][QT];
+#pragma unroll
+    for (int r = 0; r < R0; ++r)
+#pragma unroll
+        for (int q = 0; q < QT; ++q) acc[r][q] = make_float2(0.f, 0.f);
+
+    for (int q = 0; q < kPairs; ++q) {
+        const int st = q & 1;
+        char *stage = base + Gm::kRing + st * Gm::kPair;
+        const uint32_t xs = tc_smem_addr(stage);
+        // pass 1 (one thread): x [T_hi ; T_lo]^T into columns 0..63
+        if (tid == 0) {
+            ok &= mbar_wait(&bar_x[st], (uint32_t)(q >> 1), a.err);
+            tc_after_sync();
+            constexpr uint32_t id = idesc_tf32(64);
+#pragma unroll
+            for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_tf32(tmem, desc_sw128(xs + kc * Gm::kTile + s4 * 32),
+                             desc_sw128(ts + kc * Gm::kTChunk + s4 * 32), id, (kc | s4) ? 1u : 0u);
+            mma_commit(&bar_p1);
+        }
+        ok &= mbar_wait(&bar_p1, (uint32_t)q, a.err);   // pass 1 has read the pair
+        // x_lo over the pair (elementwise: the swizzled layout carries over)
+        {
+            float4 *xv = reinterpret_cast<float4 *>(stage);
+            for (int e = tid; e < (int)(Gm::kPair / 16); e += kNT) {
+                const float4 v = xv[e];
+                xv[e] = make_float4(tf32_lo(v.x), tf32_lo(v.y), tf32_lo(v.z), tf32_lo(v.w));
+            }
+        }
+        fence_async_smem();
+        tc_before_sync();
+        __syncthreads();
+        // pass 2: x_lo T_hi^T into columns 0..31
+        if (tid == 0) {
+            tc_after_sync();
+            constexpr uint32_t id = idesc_tf32(32);
+#pragma unroll
+            for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_tf32(tmem, desc_sw128(xs + kc * Gm::kTile + s4 * 32),
+                             desc_sw128(ts + kc * Gm::kTChunk + s4 * 32), id, 1u);
+            mma_commit(&bar_fin);
+        }
+        ok &= mbar_wait(&bar_fin, (uint32_t)q, a.err);
+        tc_after_sync();
+        // the two planes' row spectra: lane r = (plane r / 64, row r % 64), warp
+        // w reading lanes 32 w..; bins 8h .. 8h + 7 at a time (re = columns k
+        // and 32 + k, im = 16 + k and 48 + k: the T_hi and T_lo halves summed)
+        {
+            const int r = 32 * warp + (tid & 31);
+            const uint32_t la = tmem + ((uint32_t)(32 * warp) << 16);
+            float2 *zs = reinterpret_cast<float2 *>(base + Gm::kZ + (r / 64) * kZBytes) +
+                         (r % 64) * Pl::ZS;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float re0[8], re1[8], im0[8], im1[8];
+                tmem_ld8(la + 8 * h, re0);           // cos of bins 8h .., T_hi
+                tmem_ld8(la + 16 + 8 * h, im0);      // -sin, T_hi
+                tmem_ld8(la + 32 + 8 * h, re1);      // cos, T_lo
+                tmem_ld8(la + 48 + 8 * h, im1);      // -sin, T_lo
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    zs[8 * h + k] = ok ? make_float2(re0[k] + re1[k], im0[k] + im1[k])
+                                       : make_float2(0.f, 0.f);
+            }
+        }
+        tc_before_sync();
+        __syncthreads();                         // the stage and tensor memory are free
+        if (tid == 0 && q + 2 < kPairs) issue(q + 2, st);
+        // each plane of the pair: column DFT, kept modes, fold into the residues
+#pragma unroll
+        for (int pl = 0; pl < 2; ++pl) {
+            const int t = 2 * q + pl;
+            const float2 *zs = reinterpret_cast<const float2 *>(base + Gm::kZ + pl * kZBytes);
+            a_col_fft<Pl>(zs, ss);
+            __syncthreads();
+            float2 wr[R0];                       // W_R0^{r t} = W_N0^{C0 r t}
+#pragma unroll
+            for (int rr = 0; rr < R0; ++rr) wr[rr] = twa[(C0 * rr * t) & (N0 - 1)];
+#pragma unroll
+            for (int qq = 0; qq < QT; ++qq) {
+                const float2 v = a_kept_mode<Pl>(ss, threadIdx.x + qq * kNT, 0, tw);
+#pragma unroll
+                for (int rr = 0; rr < R0; ++rr) cmac(acc[rr][qq], v, wr[rr]);
+            }
+            __syncthreads();                     // ss is rewritten by the next plane
+        }
+    }
+    if (warp == 0) {
+        tc_after_sync();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(Gm::kTmemCols));
+    }
+    // residues to shared memory (over the ring), then the cluster's combine
+    float2 *pm = reinterpret_cast<float2 *>(base + Gm::kRing);   // [R0][NKP]
+#pragma unroll
+    for (int rr = 0; rr < R0; ++rr)
+#pragma unroll
+        for (int qq = 0; qq < QT; ++qq) pm[rr * NKP + threadIdx.x + qq * kNT] = acc[rr][qq];
+    cluster_sync();
+    const uint32_t local = smem_addr(pm);
+    float2 *X = a.part + (size_t)vol * C3::NK;
+    for (int u = threadIdx.x; u < R0 * C3::kCols; u += kNT) {
+        const int rr = u / C3::kCols, col = c * C3::kCols + u % C3::kCols;
+        float2 v[C0];
+#pragma unroll
+        for (int cc = 0; cc < C0; ++cc) v[cc] = ld_dsmem(local + (uint32_t)(rr * NKP + col) * 8, cc);
+#pragma unroll
+        for (int m = 0; m < C3::KR; ++m) {
+            const int j0 = rr + R0 * m, f0 = freq0<C3>(j0);
+            float2 sum = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int cc = 0; cc < C0; ++cc) cmac(sum, v[cc], twa[(f0 * cc) & (N0 - 1)]);
+            __stcg(X + (size_t)j0 * NKP + col, sum);
+        }
+    }
+    cluster_sync();                              // peers may still read this CTA's residues
+    cta_record(a, 0, 0, t0, t0);
+}
+
+// shared memory of the tensor-core kernel A
+template <class C3>
+constexpr size_t smem_a3_tc() {
+    using Pl = typename C3::Pl;
+    return Geo3A::kZ + 2 * (size_t)C3::N1 * Pl::ZS * 8 + (size_t)Pl::A * Pl::B2 * Pl::M1 * 8 +
+           C3::kSmemTw + 1024;
+}
+
+// Host: the row-DFT operand for 64 samples and 16 bins, per K chunk [T_hi |
+// T_lo] with T[j][n] = cos(2 pi k n / 64) (j = k < 16) or -sin (j = 16 + k),
+// split in double (T_hi as stored is read at tf32 precision; T_lo is the rest)
+void make_table_a3(std::vector<unsigned char> &img) {
+    using Gm = Geo3A;
+    using tcu::sw_off;
+    using tcu::tf32_lo;
+    img.assign(Gm::kTBytes, 0);
+    const double two_pi = 2.0 * M_PI;
+    for (int j = 0; j < 2 * Gm::M2; ++j)
+        for (int n = 0; n < Gm::N; ++n) {
+            const int k = j % Gm::M2;
+            const double ang = two_pi * (double)k * (double)n / (double)Gm::N;
+            const double v = j < Gm::M2 ? std::cos(ang) : -std::sin(ang);
+            const float hi = (float)v;
+            const float lo = (float)(v - (double)(hi - tf32_lo(hi)));
+            const uint32_t chunk = (uint32_t)(n / 32) * Gm::kTChunk;
+            memcpy(&img[chunk + sw_off(j, n % 32)], &hi, 4);
+            memcpy(&img[chunk + sw_off(2 * Gm::M2 + j, n % 32)], &lo, 4);
+        }
+}
+
 #ifndef FNO_MIX_STREAM
 #define FNO_MIX_STREAM 1
 #endif
@@ -369,6 +611,22 @@ struct Pdl3 {
     static cudaError_t init(Plan &p) {
         const int ob = out_block(p.dtype, p.cin, p.cout), bb = batch_block(p.batch, p.cin);
         cudaError_t e = raise_smem_limit(k_phase_a3<C3, T>, (int)C3::template smem_a<T>());
+        // float32, on request: the row DFT of kernel A on the tensor cores (TMA
+        // plane pairs; slower than the register FFTs on the 4 x 32-channel
+        // layer, 202 against 173 us a forward)
+        p.fused_tca = false;
+        if constexpr (std::is_same<T, float>::value) {
+            if (e == cudaSuccess && (p.flags & FNO_PLAN_TENSOR_EXTRA) &&
+                !(p.flags & FNO_PLAN_SIMT_TRANSFORM) && tcu::encoder()) {
+                p.fused_tca = true;
+                e = raise_smem_limit(k_phase_a3_tc<C3>, (int)smem_a3_tc<C3>());
+                std::vector<unsigned char> img;
+                make_table_a3(img);
+                if (e == cudaSuccess) e = cudaMalloc(&p.fused_tables, img.size());
+                if (e == cudaSuccess)
+                    e = cudaMemcpy(p.fused_tables, img.data(), img.size(), cudaMemcpyHostToDevice);
+            }
+        }
         if (e == cudaSuccess)
             e = raise_smem_limit(k_phase_b<C3, T, 1, kNT>, smem_b(p.dtype, p.cin, ob + 1, bb));
         if (e == cudaSuccess)
@@ -417,7 +675,23 @@ struct Pdl3 {
         ca.stream = s;
         ca.attrs = &cl;
         ca.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&ca, k_phase_a3<C3, T>, a);
+        cudaError_t e = cudaSuccess;
+        bool done_a = false;
+        if constexpr (std::is_same<T, float>::value) {
+            if (p.fused_tca) {
+                // the input as rows of N2 samples, boxes of 32 samples x one plane
+                CUtensorMap xmap;
+                if (!tcu::encode_rows_tiled(&xmap, a.x, (int64_t)p.batch * p.cin * C3::N0 * C3::N1,
+                                            C3::N2, sizeof(float), 32, tcu::tma_type<float>(),
+                                            C3::N1))
+                    return cudaErrorInvalidValue;
+                ca.dynamicSmemBytes = smem_a3_tc<C3>();
+                e = cudaLaunchKernelEx(&ca, k_phase_a3_tc<C3>, xmap, a,
+                                       static_cast<const void *>(p.fused_tables));
+                done_a = true;
+            }
+        }
+        if (!done_a) e = cudaLaunchKernelEx(&ca, k_phase_a3<C3, T>, a);
         if (e != cudaSuccess) return e;
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;

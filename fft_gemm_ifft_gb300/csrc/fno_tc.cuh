@@ -98,6 +98,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // byte offset of (row, col) in a chunk of rows x 64 16-bit elements stored
 // K-major with the 128-byte swizzle (same atoms as above, 8 elements per
 // 16-byte piece)
@@ -188,15 +199,16 @@ template <> inline CUtensorMapDataType tma_type<__nv_bfloat16>() {
     return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 }
 
-// A (rows x cols) row-major matrix read in boxes of box_cols (128 bytes) x 128
-// rows with the 128-byte swizzle.
+// A (rows x cols) row-major matrix read in boxes of box_cols (128 bytes) x
+// box_rows (128 unless given) rows with the 128-byte swizzle.
 inline bool encode_rows_tiled(CUtensorMap *map, const void *ptr, int64_t rows, int cols,
-                              size_t elem, int box_cols, CUtensorMapDataType type) {
+                              size_t elem, int box_cols, CUtensorMapDataType type,
+                              int box_rows = 128) {
     EncodeTiled fn = encoder();
-    if (!fn) return false;
+    if (!fn || box_rows < 1 || box_rows > 256) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)cols * elem};
-    const cuuint32_t box[2] = {(cuuint32_t)box_cols, 128};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, type, 2, const_cast<void *>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -112,15 +112,20 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * 16-bit 2-D layers reads them as ready operand images.  Requires
  * |K| % 4 == 0; not combinable with FNO_PLAN_BACKWARD.                      */
 #define FNO_PLAN_PACKED_WEIGHTS 128u
-/* Mix the float32 128x128 three-kernel layer on the tensor cores: per pair of
- * kept modes one CTA, the complex products in 3xTF32 on kind::tf32
- * tcgen05.mma, [Wr^T ; Wi^T] as the one weight operand (fno_mix_tf32.cu),
- * for 32 or 64 input and output channels, batch <= 32 (64 outputs) or <= 16
- * (32 outputs), weights in the standard layout.  Matches the oracle like the
- * default; the SIMT mixing stays the default because it measured faster on
- * these shapes (the products are small: the kernel is bound by the latency of
- * its loads, not by arithmetic).  Ignored where it does not apply.          */
-#define FNO_PLAN_TENSOR_MIX 256u
+/* Also run the tensor-core variants that are not the default because they
+ * measured slower on the workloads (each matches the oracle like the default;
+ * ignored where none applies):
+ *  - the mixing of the float32 128x128 three-kernel layer: per pair of kept
+ *    modes one CTA, the complex products in 3xTF32 on kind::tf32
+ *    tcgen05.mma, [Wr^T ; Wi^T] as the one weight operand (fno_mix_tf32.cu),
+ *    for 32 or 64 input and output channels, batch <= 32 (64 outputs) or
+ *    <= 16 (32 outputs), weights in the standard layout;
+ *  - the forward transform of the float32 64^3 layer: the row DFT of each
+ *    pair of planes as a 3xTF32 GEMM, the planes brought in by TMA
+ *    (k_phase_a3_tc in fno_fused3d.cu).
+ * The products involved are small; the kernels are bound by the latency of
+ * their loads and by their SIMT steps, not by arithmetic.                   */
+#define FNO_PLAN_TENSOR_EXTRA 256u
 
 /* One work item of the fused kernel, as recorded under FNO_PLAN_TRACE.
  * Times are the GPU's global nanosecond timer.                              */

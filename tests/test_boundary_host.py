@@ -95,7 +95,7 @@ def test_query_rejects_unknown_flags_and_nulls(L):
     # the tensor-core mixing request is a flag (ignored where it does not apply)
     for shape in (([128, 128], [16, 16]), ([64], [8])):
         st, _, _ = Q(len(shape[0]), shape[0], shape[1], 8, 32, 32, F32,
-                     flags=capi.FNO_PLAN_TENSOR_MIX)
+                     flags=capi.FNO_PLAN_TENSOR_EXTRA)
         assert st == capi.FNO_OK
     import ctypes
     assert L.fno_spectral_conv_query(1, None, None, 1, 1, 1, 0, 0, None, None) == \

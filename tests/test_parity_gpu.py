@@ -75,9 +75,9 @@ def _lib(fno, oracle_mod):
 
 @pytest.mark.parametrize("flags", [0, FNO_PLAN_UNFUSED, capi.FNO_PLAN_PERSISTENT,
                                    capi.FNO_PLAN_SIMT_MIX, capi.FNO_PLAN_SIMT_TRANSFORM,
-                                   capi.FNO_PLAN_TENSOR_MIX],
+                                   capi.FNO_PLAN_TENSOR_EXTRA],
                          ids=["default", "unfused", "persistent", "simt_mix",
-                              "simt_transform", "tensor_mix"])
+                              "simt_transform", "tensor_extra"])
 @pytest.mark.parametrize("spec", SMALL, ids=[case_id(c) for c in SMALL])
 def test_small_cases_match_oracle(spec, flags):
     n, modes, b, ci, co, dt = spec
