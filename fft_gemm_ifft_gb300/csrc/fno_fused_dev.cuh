@@ -825,11 +825,18 @@ __device__ __forceinline__ BItem b_item(const Args &a, int it) {
 // Each weight is read once and used for every batch row with no shared-memory
 // staging; for small batches this is the weight stream's own bound.
 constexpr int kMixThreads = 256;
+// CTAs of the streaming mixing resident per SM with up to 4 batch rows (its
+// register bound; two with more rows, whose accumulators need the registers):
+// a CTA is a short chain of dependent loads, so the more of them are in flight
+// the better the latency is hidden (its registers alone allowed three)
+#ifndef FNO_MIX_STREAM_MINB
+#define FNO_MIX_STREAM_MINB 4
+#endif
 #ifndef FNO_MIX_STREAM_DEPTH
 #define FNO_MIX_STREAM_DEPTH 8
 #endif
 template <class Cf, typename T, int kParts, int R, int kMaxB>
-__global__ void __launch_bounds__(kMixThreads) k_mix_stream(Args a) {
+__global__ void __launch_bounds__(kMixThreads, kMaxB <= 4 ? FNO_MIX_STREAM_MINB : 2) k_mix_stream(Args a) {
     extern __shared__ __align__(16) char smem[];
     float2 *xs = reinterpret_cast<float2 *>(smem);          // [batch][cin][R]
     static_assert(Cf::MR % R == 0, "a run stays on one line of the last axis");
