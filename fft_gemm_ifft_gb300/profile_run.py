@@ -24,6 +24,8 @@ def main(argv=None) -> int:
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--flags", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0, help="override the batch size")
+    ap.add_argument("--channels", type=int, default=0,
+                    help="override the input and output channel counts")
     ap.add_argument("--trace", default="", help="write the last call's work-item trace "
                     "(CSV) here and print a per-phase summary")
     ap.add_argument("--time", action="store_true", help="time each forward with CUDA events")
@@ -45,6 +47,9 @@ def main(argv=None) -> int:
     case = workloads.CASES[args.workload]
     if args.batch:
         case = case.with_batch(args.batch)
+    if args.channels:
+        import dataclasses
+        case = dataclasses.replace(case, cin=args.channels, cout=args.channels)
     from . import capi
     flags = args.flags | (capi.FNO_PLAN_TRACE if args.trace else 0)
     if args.backward:
