@@ -544,18 +544,27 @@ struct Geo32 {
     static constexpr uint32_t kXBytes = KC * kTile;
     static constexpr uint32_t kTChunk = 64 * 128;       // [T_hi rows 0..31 | T_lo rows 0..31]
     static constexpr uint32_t kTBytes = KC * kTChunk;
-    static constexpr int ZS = M1 + 1;                   // Z plane row stride (floats)
+    // Z planes (then the column sums over them) [N0][M1], bin k of row r at
+    // column k ^ (r % 16): conflict-free both for a warp of rows and for a warp
+    // of (row pair, bins); they go over the image's last K chunk
+    static constexpr int ZS = M1;
     static constexpr uint32_t kZBytes = (uint32_t)N0 * ZS * 4 * 2;
-    static constexpr uint32_t kSBytes = (uint32_t)R1 * B2 * M1 * 8;
-    static_assert(kZBytes + kSBytes <= kXBytes, "Z planes and sums fit over the image");
+    static constexpr uint32_t kZOff = 3 * kTile;
+    static_assert(M1 == 16 && kZOff + kZBytes <= kXBytes, "Z planes fit over chunk 3");
     static constexpr uint32_t kT = kXBytes;
     static constexpr uint32_t kTw = kT + kTBytes;
     static constexpr uint32_t kSmem = kTw + N0 * 8 + 1024;
     static constexpr uint32_t kTmemCols = 64;
 };
 
+// One persistent CTA (two per SM) walks images img = blockIdx.x + k gridDim.x.
+// An image's four K chunks arrive by TMA; the row spectra (Z, then the column
+// sums over them in place) go over chunk 3 once the second pass has read it,
+// so the next image's chunks 0..2 are requested as soon as the row DFT is done
+// and chunk 3 once the kept modes are written: the loads of one image land
+// under the column work of the one before.
 __global__ void __launch_bounds__(NT, 2)
-k_phase_a_tc32(const __grid_constant__ CUtensorMap xmap, Args a, const void *tables) {
+k_phase_a_tc32(const __grid_constant__ CUtensorMap xmap, Args a, const void *tables, int nimg) {
     using Gm = Geo32;
     using namespace tcu;
     extern __shared__ __align__(1024) char smem_raw[];
@@ -563,10 +572,14 @@ k_phase_a_tc32(const __grid_constant__ CUtensorMap xmap, Args a, const void *tab
                                           ~static_cast<uintptr_t>(1023));
     __shared__ __align__(8) uint64_t bar_t, bar_fin, bar_x[Gm::KC], bar_p1[Gm::KC];
     __shared__ uint32_t s_tmem;
-    const unsigned long long t0 = a.trace ? trace_now() : 0;
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int img = blockIdx.x;
     float2 *tw = reinterpret_cast<float2 *>(base + Gm::kTw);
+    auto issue = [&](int img, int kc) {          // chunk kc of image img (thread 0)
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     ::"r"(tc_smem_addr(&bar_x[kc])), "r"(Gm::kTile) : "memory");
+        tma_load_2d(tc_smem_addr(base + kc * Gm::kTile), &xmap, kc * 32, img * Gm::N0,
+                    &bar_x[kc]);
+    };
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_t)));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_fin)));
@@ -580,12 +593,8 @@ k_phase_a_tc32(const __grid_constant__ CUtensorMap xmap, Args a, const void *tab
         asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                      ::"r"(tc_smem_addr(base + Gm::kT)), "l"(tables), "r"(Gm::kTBytes),
                      "r"(tc_smem_addr(&bar_t)) : "memory");
-        for (int kc = 0; kc < Gm::KC; ++kc) {
-            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                         ::"r"(tc_smem_addr(&bar_x[kc])), "r"(Gm::kTile) : "memory");
-            tma_load_2d(tc_smem_addr(base + kc * Gm::kTile), &xmap, kc * 32, img * Gm::N0,
-                        &bar_x[kc]);
-        }
+        if ((int)blockIdx.x < nimg)
+            for (int kc = 0; kc < Gm::KC; ++kc) issue(blockIdx.x, kc);
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -600,89 +609,113 @@ k_phase_a_tc32(const __grid_constant__ CUtensorMap xmap, Args a, const void *tab
     const uint32_t tmem = s_tmem;
     const uint32_t xs = tc_smem_addr(base), ts = tc_smem_addr(base + Gm::kT);
     bool ok = true;
-    // pass 1 of chunk kc (one thread): x [T_hi; T_lo]^T into columns 0..63
-    auto pass1 = [&](int kc) {
-        ok &= mbar_wait(&bar_x[kc], 0, a.err);
-        tc_after_sync();
-        constexpr uint32_t id = idesc_tf32(64);
+    if (tid == 0) ok &= mbar_wait(&bar_t, 0, a.err);
+    uint32_t it = 0;
+    for (int img = blockIdx.x; img < nimg; img += gridDim.x, ++it) {
+        const unsigned long long t0 = a.trace ? trace_now() : 0;
+        const int nxt = img + (int)gridDim.x;
+        // pass 1 (one thread): x [T_hi; T_lo]^T into columns 0..63, each K chunk
+        // as it lands
+        if (tid == 0) {
+            constexpr uint32_t id = idesc_tf32(64);
+            for (int kc = 0; kc < Gm::KC; ++kc) {
+                ok &= mbar_wait(&bar_x[kc], it, a.err);
+                tc_after_sync();
 #pragma unroll
-        for (int s = 0; s < 4; ++s)
-            mma_tf32(tmem, desc_sw128(xs + kc * Gm::kTile + s * 32),
-                     desc_sw128(ts + kc * Gm::kTChunk + s * 32), id, (kc | s) ? 1u : 0u);
-        mma_commit(&bar_p1[kc]);
-    };
-    if (tid == 0) {
-        ok &= mbar_wait(&bar_t, 0, a.err);
-        pass1(0);
-    }
-    for (int kc = 0; kc < Gm::KC; ++kc) {
-        if (tid == 0 && kc + 1 < Gm::KC) pass1(kc + 1);
-        ok &= mbar_wait(&bar_p1[kc], 0, a.err);          // pass 1 has read chunk kc
-        // x_lo over chunk kc (elementwise: the swizzled layout carries over)
-        float4 *xv = reinterpret_cast<float4 *>(base + kc * Gm::kTile);
-        for (int e = tid; e < (int)(Gm::kTile / 16); e += NT) {
-            const float4 v = xv[e];
-            xv[e] = make_float4(tf32_lo(v.x), tf32_lo(v.y), tf32_lo(v.z), tf32_lo(v.w));
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_tf32(tmem, desc_sw128(xs + kc * Gm::kTile + s4 * 32),
+                             desc_sw128(ts + kc * Gm::kTChunk + s4 * 32), id,
+                             (kc | s4) ? 1u : 0u);
+            }
+            mma_commit(&bar_p1[0]);
+        }
+        ok &= mbar_wait(&bar_p1[0], it, a.err);                // pass 1 has read the image
+        // x_lo over the image (elementwise: the swizzled layout carries over)
+        {
+            float4 *xv = reinterpret_cast<float4 *>(base);
+            for (int e = tid; e < (int)(Gm::kXBytes / 16); e += NT) {
+                const float4 v = xv[e];
+                xv[e] = make_float4(tf32_lo(v.x), tf32_lo(v.y), tf32_lo(v.z), tf32_lo(v.w));
+            }
         }
         fence_async_smem();
         tc_before_sync();
         __syncthreads();
+        // pass 2: x_lo T_hi^T into columns 0..31
         if (tid == 0) {
             tc_after_sync();
             constexpr uint32_t id = idesc_tf32(32);
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_tf32(tmem, desc_sw128(xs + kc * Gm::kTile + s * 32),
-                         desc_sw128(ts + kc * Gm::kTChunk + s * 32), id, 1u);
+            for (int kc = 0; kc < Gm::KC; ++kc)
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4)
+                    mma_tf32(tmem, desc_sw128(xs + kc * Gm::kTile + s4 * 32),
+                             desc_sw128(ts + kc * Gm::kTChunk + s4 * 32), id, 1u);
         }
-    }
-    if (tid == 0) mma_commit(&bar_fin);
-    ok &= mbar_wait(&bar_fin, 0, a.err);
-    tc_after_sync();
-    const unsigned long long t_z = a.trace ? trace_now() : 0;     // the row DFT is done
-    // Z planes from tensor memory into the region the image occupied: warps w
-    // and w + 4 read the same lanes, the first the re, the second the im bins,
-    // each summing the T_hi and T_lo column halves
-    float *zr = reinterpret_cast<float *>(base);
-    float *zi = zr + Gm::N0 * Gm::ZS;
-    float2 *S = reinterpret_cast<float2 *>(base + Gm::kZBytes);
-    {
-        const int half = warp >> 2, row = 32 * (warp & 3) + (tid & 31);
-        const uint32_t lanes = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        float v[16], u[16];
-        tmem_ld16(lanes + half * Gm::M1, v);
-        tmem_ld16(lanes + 32 + half * Gm::M1, u);
-        float *dz = half ? zi : zr;
+        if (tid == 0) mma_commit(&bar_fin);
+        ok &= mbar_wait(&bar_fin, it, a.err);
+        tc_after_sync();
+        const unsigned long long t_z = a.trace ? trace_now() : 0;   // the row DFT is done
+        // Z planes from tensor memory over chunk 3: warps w and w + 4 read
+        // the same lanes, the first the re, the second the im bins, each summing
+        // the T_hi and T_lo column halves
+        float *zr = reinterpret_cast<float *>(base + Gm::kZOff);
+        float *zi = zr + Gm::N0 * Gm::ZS;
+        {
+            const int half = warp >> 2, row = 32 * (warp & 3) + (tid & 31);
+            const uint32_t lanes = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+            float v[16], u[16];
+            tmem_ld16(lanes + half * Gm::M1, v);
+            tmem_ld16(lanes + 32 + half * Gm::M1, u);
+            float *dz = half ? zi : zr;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) dz[row * Gm::ZS + q] = ok ? v[q] + u[q] : 0.f;
-    }
-    tc_before_sync();
-    __syncthreads();
-    // column DFT: S[r1][q][k] = B2-point DFT over r2 of Z[r1 + R1 r2][k]
-    for (int u = tid; u < Gm::R1 * Gm::M1; u += NT) {
-        const int r1 = u / Gm::M1, k = u % Gm::M1;
-        float2 z[Gm::B2];
-#pragma unroll
-        for (int r2 = 0; r2 < Gm::B2; ++r2) {
-            const int r = r1 + Gm::R1 * r2;
-            z[r2] = make_float2(zr[r * Gm::ZS + k], zi[r * Gm::ZS + k]);
+            for (int q = 0; q < 16; ++q) dz[row * Gm::ZS + (q ^ (row & 15))] = ok ? v[q] + u[q] : 0.f;
         }
-        fft::fft_dif<Gm::B2, -1>(z);
+        tc_before_sync();
+        __syncthreads();
+        // chunks 0..2 and tensor memory are free: most of the next image
+        if (tid == 0 && nxt < nimg)
+            for (int kc = 0; kc < Gm::KC - 1; ++kc) issue(nxt, kc);
+        // column DFT in place: thread (r1, k) replaces Z rows r1 + R1 r2 of bin
+        // k by S[r1][q][k] = the B2-point DFT over r2 (row r1 + R1 q)
+        for (int u = tid; u < Gm::R1 * Gm::M1; u += NT) {
+            const int r1 = u / Gm::M1, k = u % Gm::M1;
+            float2 z[Gm::B2];
 #pragma unroll
-        for (int q = 0; q < Gm::B2; ++q)
-            S[(r1 * Gm::B2 + q) * Gm::M1 + k] = z[fft::bitrev(q, fft::ilog2(Gm::B2))];
-    }
-    __syncthreads();
-    // kept modes: X[j][k] = sum_r1 W_N0^{f r1} S[r1][f mod B2][k]
-    float2 *dst = a.part + (size_t)img * Gm::NK;
-    for (int o = tid; o < Gm::NK; o += NT) {
-        const int j = o / Gm::M1, k = o % Gm::M1;
-        const int f = j < Gm::M0 ? j : Gm::N0 - Gm::K0 + j;
-        float2 acc = make_float2(0.f, 0.f);
+            const int kc = k ^ r1;                        // rows r1 + R1 r2: r % 16 = r1
+            for (int r2 = 0; r2 < Gm::B2; ++r2) {
+                const int r = r1 + Gm::R1 * r2;
+                z[r2] = make_float2(zr[r * Gm::ZS + kc], zi[r * Gm::ZS + kc]);
+            }
+            fft::fft_dif<Gm::B2, -1>(z);
 #pragma unroll
-        for (int r1 = 0; r1 < Gm::R1; ++r1)
-            cmac(acc, S[(r1 * Gm::B2 + (f % Gm::B2)) * Gm::M1 + k], tw[(f * r1) & (Gm::N0 - 1)]);
-        __stcg(dst + o, acc);
+            for (int q = 0; q < Gm::B2; ++q) {
+                const int r = r1 + Gm::R1 * q;
+                const float2 sv = z[fft::bitrev(q, fft::ilog2(Gm::B2))];
+                zr[r * Gm::ZS + kc] = sv.x;
+                zi[r * Gm::ZS + kc] = sv.y;
+            }
+        }
+        __syncthreads();
+        // kept modes: X[j][k] = sum_r1 W_N0^{f r1} S[r1][f mod B2][k]
+        float2 *dst = a.part + (size_t)img * Gm::NK;
+        for (int o = tid; o < Gm::NK; o += NT) {
+            const int j = o / Gm::M1, k = o % Gm::M1;
+            const int f = j < Gm::M0 ? j : Gm::N0 - Gm::K0 + j;
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int r1 = 0; r1 < Gm::R1; ++r1) {
+                const int r = r1 + Gm::R1 * (f % Gm::B2);
+                cmac(acc, make_float2(zr[r * Gm::ZS + (k ^ r1)], zi[r * Gm::ZS + (k ^ r1)]),
+                     tw[(f * r1) & (Gm::N0 - 1)]);
+            }
+            __stcg(dst + o, acc);
+        }
+        fence_async_smem();
+        __syncthreads();
+        // chunk 3 is free: the rest of the next image
+        if (tid == 0 && nxt < nimg) issue(nxt, Gm::KC - 1);
+        if (a.trace) cta_record_at(a, 0, 0, img, t0, t0, t_z);
     }
     tc_before_sync();
     __syncthreads();
@@ -691,7 +724,6 @@ k_phase_a_tc32(const __grid_constant__ CUtensorMap xmap, Args a, const void *tab
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(Gm::kTmemCols));
     }
-    cta_record(a, 0, 0, t0, t0, t_z);
 }
 
 // Host: kernel A's fp32 operand image, per K chunk [T_hi | T_lo] with T[j][n] =
@@ -1279,7 +1311,10 @@ struct Pdl {
                     if (!tcu::encode_rows_tiled(&xmap, a.x, (int64_t)p.batch * p.cin * Gm::N0,
                                                 Gm::N1, sizeof(T), 32, tcu::tma_type<T>()))
                         return cudaErrorInvalidValue;
-                    tca::k_phase_a_tc32<<<nA, tca::NT, Gm::kSmem, s>>>(xmap, a, p.fused_tables);
+                    // persistent: two CTAs per SM walk the images
+                    const int grid = nA < 2 * p.num_sms ? nA : 2 * p.num_sms;
+                    tca::k_phase_a_tc32<<<grid, tca::NT, Gm::kSmem, s>>>(xmap, a, p.fused_tables,
+                                                                         nA);
                 } else {
                     using Gm = tca::Geo<T>;
                     if (!tcu::encode_rows_tiled(&xmap, a.x, (int64_t)p.batch * p.cin * Gm::N0,
