@@ -30,7 +30,7 @@ struct Model {
     int kernels;
     // which 1x1 linears run on the tensor cores (fno_pointwise.cu; otherwise
     // the register-tiled SIMT kernels below)
-    bool lift_tc, layer_tc, head_tc;
+    bool lift_simt, lift_tc, layer_tc, head_tc;
     int num_sms;
 };
 
@@ -235,6 +235,46 @@ k_projection_tiled(const T *__restrict__ a, const float *__restrict__ P1,
 }
 
 
+// The lift of a few input channels (the field and its coordinates) to the
+// model width: a pure write stream (each output value costs cin FMAs), so a
+// thread takes 4 consecutive pixels of one image, reads them once per input
+// channel and writes its 4 pixels of every output channel (a warp: 512
+// contiguous bytes per channel).
+constexpr int kLiftMaxCin = 8;
+constexpr int kLiftThreads = 256;
+template <typename T>
+__global__ void __launch_bounds__(kLiftThreads)
+k_lift(const T *__restrict__ x, const float *__restrict__ W, const float *__restrict__ bias,
+       T *__restrict__ out, int cin, int cout, int64_t npix) {
+    extern __shared__ float s_wb[];                  // W [cout][cin], then bias [cout]
+    for (int e = threadIdx.x; e < cout * (cin + 1); e += kLiftThreads)
+        s_wb[e] = e < cout * cin ? W[e] : bias[e - cout * cin];
+    __syncthreads();
+    const int b = blockIdx.y;
+    const int64_t p = ((int64_t)blockIdx.x * kLiftThreads + threadIdx.x) * 4;
+    if (p >= npix) return;
+    float4 xv[kLiftMaxCin];
+#pragma unroll
+    for (int i = 0; i < kLiftMaxCin; ++i)
+        if (i < cin) xv[i] = Storage<T>::load4(x + ((int64_t)b * cin + i) * npix + p);
+    T *op = out + (int64_t)b * cout * npix + p;
+    for (int o = 0; o < cout; ++o) {
+        const float bo = s_wb[cout * cin + o];
+        float4 y = make_float4(bo, bo, bo, bo);
+#pragma unroll
+        for (int i = 0; i < kLiftMaxCin; ++i) {
+            if (i < cin) {
+                const float w = s_wb[o * cin + i];
+                y.x = fmaf(w, xv[i].x, y.x);
+                y.y = fmaf(w, xv[i].y, y.y);
+                y.z = fmaf(w, xv[i].z, y.z);
+                y.w = fmaf(w, xv[i].w, y.w);
+            }
+        }
+        Storage<T>::store4(op + (int64_t)o * npix, y);
+    }
+}
+
 template <typename T>
 using ProjFn = void (*)(const T *, const float *, const float *, const float *,
                         const float *, T *, int, int, int, int64_t);
@@ -298,7 +338,11 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
     m->num_sms = 0;
     cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t npix = d->h * d->w;
-    m->lift_tc = pointwise_supported(d->dtype, d->cin_lift, d->width, 0, false, npix);
+    // a lift of up to 8 channels is a write stream: its own kernel
+    m->lift_simt = d->cin_lift <= kLiftMaxCin &&
+                   (size_t)d->width * (d->cin_lift + 1) * sizeof(float) <= (48u << 10);
+    m->lift_tc = !m->lift_simt &&
+                 pointwise_supported(d->dtype, d->cin_lift, d->width, 0, false, npix);
     m->layer_tc = pointwise_supported(d->dtype, d->width, d->width, 0, false, npix);
     m->head_tc = pointwise_supported(d->dtype, d->width, d->hidden, d->cout, true, npix);
     if ((m->lift_tc && pointwise_init(d->dtype, d->cin_lift, d->width, 0, false) != cudaSuccess) ||
@@ -376,7 +420,13 @@ fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_param
             pa.err = err;
             return pointwise_launch(d.dtype, pa, m.num_sms, s);
         };
-        if (m.lift_tc) {
+        if (m.lift_simt) {
+            const dim3 grid((unsigned)((m.npix / 4 + kLiftThreads - 1) / kLiftThreads),
+                            (unsigned)d.batch);
+            k_lift<T><<<grid, kLiftThreads,
+                        (size_t)d.width * (d.cin_lift + 1) * sizeof(float), s>>>(
+                static_cast<const T *>(x), p->lift_w, p->lift_b, A, d.cin_lift, d.width, m.npix);
+        } else if (m.lift_tc) {
             if (linear_tc(x, d.cin_lift, p->lift_w, p->lift_b, nullptr, A, d.width, 0) !=
                 cudaSuccess)
                 return FNO_ERR_CUDA;
