@@ -1120,6 +1120,14 @@ bool tca_shape(fno_dtype_t dt) {
 #define FNO_PDL_XP_BUDGET (64u << 10)
 #endif
 constexpr size_t kPdlXpBudget = FNO_PDL_XP_BUDGET;   // kernel B's partial modes (bytes)
+// kernel B's weight slab in the three-kernel variants: a whole output block
+// per item where it fits (64 -> 64 channels in one item: 256 items of 80 KB on
+// the FNO layer, one wave, instead of 1024 items over the four output blocks;
+// FNO stack 468 -> 459 us)
+#ifndef FNO_PDL_WS_BUDGET
+#define FNO_PDL_WS_BUDGET (64u << 10)
+#endif
+constexpr size_t kPdlWsBudget = FNO_PDL_WS_BUDGET;
 
 template <class Cf, class CfC = Cf>
 struct Pdl {
@@ -1180,7 +1188,7 @@ struct Pdl {
         p.fused_tca = use_tca(p.dtype, p.flags);
         const int np = parts(p.dtype, p.flags);
         int ob = p.cout;
-        while (ob > 1 && (size_t)p.cin * ob * w2 > kWsBudget) ob = (ob + 1) / 2;
+        while (ob > 1 && (size_t)p.cin * ob * w2 > kPdlWsBudget) ob = (ob + 1) / 2;
         const int bb = batch_block(p.batch, p.cin, np);
         const size_t sa = Cf::kSmemTw + Cf::kSmemA, sc = CfC::kSmemTw + CfC::kSmemC;
         const size_t sb = smem_b(p.dtype, p.cin, ob + 1, bb, np);   // padded slab rows
