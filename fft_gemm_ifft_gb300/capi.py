@@ -37,6 +37,7 @@ FNO_PLAN_SIMT_MIX = 32
 FNO_PLAN_SIMT_TRANSFORM = 64
 FNO_PLAN_PACKED_WEIGHTS = 128
 FNO_PLAN_TENSOR_EXTRA = 256
+FNO_PLAN_SPLIT_LAYER = 512
 
 # Every symbol include/fno.h declares.
 EXPORTS = (

@@ -122,7 +122,8 @@ fno_status_t describe(int ndim, const int64_t *n, const int32_t *modes, int64_t 
     if (dtype != FNO_F32 && dtype != FNO_F16 && dtype != FNO_BF16) return FNO_ERR_INVALID_ARG;
     if (flags & ~(FNO_PLAN_UNFUSED | FNO_PLAN_TRACE |
                   FNO_PLAN_PERSISTENT | FNO_PLAN_BACKWARD | FNO_PLAN_SIMT_MIX |
-                  FNO_PLAN_SIMT_TRANSFORM | FNO_PLAN_PACKED_WEIGHTS | FNO_PLAN_TENSOR_EXTRA))
+                  FNO_PLAN_SIMT_TRANSFORM | FNO_PLAN_PACKED_WEIGHTS | FNO_PLAN_TENSOR_EXTRA |
+                  FNO_PLAN_SPLIT_LAYER))
         return FNO_ERR_INVALID_ARG;
     // packed weights: groups of four kept modes; the backward reads the standard layout
     if ((flags & FNO_PLAN_PACKED_WEIGHTS) &&

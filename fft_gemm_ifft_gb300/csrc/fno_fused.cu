@@ -1294,8 +1294,9 @@ struct Pdl {
         cudaError_t e = cudaLaunchKernelEx(&ca, k_phase_a<Cf, T, kCluster>, a);
         return e != cudaSuccess ? e : cudaGetLastError();
     }
+    // mixed_only: kernels A and B alone (the caller inverts the mixed modes)
     template <typename T>
-    static cudaError_t forward(const Plan &p, Args a, cudaStream_t s) {
+    static cudaError_t forward(const Plan &p, Args a, cudaStream_t s, bool mixed_only = false) {
         a.bg = p.fused_bb;
         a.ng = (int)((p.batch + a.bg - 1) / a.bg);
         a.ob = p.fused_ob;
@@ -1404,6 +1405,7 @@ struct Pdl {
                 e = cudaLaunchKernelEx(&cfg, k_phase_b<Cf, T, kParts, kBThreads>, a);
         }
         if (e != cudaSuccess) return e;
+        if (mixed_only) return cudaGetLastError();
         cfg.gridDim = dim3(nC);
         cfg.blockDim = dim3(kNT);
         if constexpr (std::is_same<T, float>::value && CfC::N0 == 128) {
@@ -1560,6 +1562,34 @@ void fused_plan_release(Plan &p) {
     p.fused_tables = nullptr;
     p.trace = nullptr;
 }
+
+bool fused_mixed_available(const Plan &p) {
+    return p.path == kPathFused && p.dtype == FNO_F32 &&
+           variant(p.g, p.dtype, p.flags) == kVarPdl128 && p.fused_tca && !p.trace;
+}
+
+cudaError_t fused_forward_mixed(const Plan &p, const Buffers &b, const float2 **Y,
+                                cudaStream_t s) {
+    if (!fused_mixed_available(p)) return cudaErrorInvalidValue;
+    const size_t part = Pdl128::part_bytes(p.g, p.batch, p.cin, p.cout, p.dtype, p.flags);
+    Args a{};
+    a.x = b.x;
+    a.w = b.w;
+    a.y = nullptr;
+    a.wpacked = (p.flags & FNO_PLAN_PACKED_WEIGHTS) ? 1 : 0;
+    a.part = static_cast<float2 *>(b.ws);
+    a.Y = reinterpret_cast<float2 *>(static_cast<char *>(b.ws) + ((part + 255) & ~size_t(255)));
+    a.tw0 = p.tw[0];
+    a.tw1 = p.tw[1];
+    a.err = p.dev_err;
+    a.batch = (int)p.batch;
+    a.cin = p.cin;
+    a.cout = p.cout;
+    *Y = a.Y;
+    return Pdl128::forward<float>(p, a, s, true);
+}
+
+void inverse_row_operand_tf32(std::vector<unsigned char> &img) { tca::make_table_c32(img); }
 
 cudaError_t fused_forward(const Plan &p, const Buffers &b, cudaStream_t s) {
     const Variant v = variant(p.g, p.dtype, p.flags);

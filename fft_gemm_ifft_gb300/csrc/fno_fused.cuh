@@ -32,6 +32,20 @@ cudaError_t fused_forward_modes(const Plan &p, const void *x, int64_t nimg, floa
 cudaError_t fused3d_forward_modes(const Plan &p, const void *x, int64_t nimg, float2 *out,
                                   cudaStream_t s);
 
+// The float32 128 x 128 layer (16 x 16 modes) up to its mixed modes: the
+// forward-transform and mixing kernels of the three-kernel path alone, for a
+// caller that runs its own inverse (the FNO layer's fused output, fno_layer.cu).
+// True when the plan runs that path with the tensor-core forward transform.
+bool fused_mixed_available(const Plan &p);
+// Launches the two kernels; *Y = the mixed modes in the workspace,
+// [batch * cout][32 kept rows][16 kept columns] complex float.
+cudaError_t fused_forward_mixed(const Plan &p, const Buffers &b, const float2 **Y,
+                                cudaStream_t s);
+// The inverse row-DFT operand of the float32 128-point inverse: 128 rows of
+// [s c(k) cos(2 pi k n / 128) | -s c(k) sin(...)], k < 16, s = 1/128^2, as the
+// 128-byte-swizzled K-major tf32 operand, hi then lo (2 x 16 KB).
+void inverse_row_operand_tf32(std::vector<unsigned char> &img);
+
 // Tensor-core mixing (kernel B of the three-kernel 2-D path) for 16-bit
 // storage: four adjacent modes per CTA, real-block complex GEMMs on tcgen05.
 struct MixTcArgs {

@@ -11,7 +11,9 @@
 #include <type_traits>
 
 #include "fno_internal.cuh"
+#include "fno_fused.cuh"
 #include "fno_gelu.cuh"
+#include "fno_layer.cuh"
 #include "fno_pointwise.cuh"
 
 using namespace fno;
@@ -31,6 +33,12 @@ struct Model {
     // which 1x1 linears run on the tensor cores (fno_pointwise.cu; otherwise
     // the register-tiled SIMT kernels below)
     bool lift_simt, lift_tc, layer_tc, head_tc;
+    // the float32 128 x 128 layers: the spectral plan's forward transform and
+    // mixing, then the column step and ONE GEMM for the inverse row DFT and the
+    // 1x1 linear (fno_layer.cu) instead of the inverse kernel and the linear
+    bool layer_fused;
+    size_t z_off;          // the column step's output in the workspace
+    void *row_table;       // the inverse row-DFT operand (model-owned)
     int num_sms;
 };
 
@@ -359,6 +367,28 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
     m->act_bytes = align256((size_t)d->batch * d->width * m->npix * (d->dtype == FNO_F32 ? 4 : 2));
     m->spec_ws_bytes = spec_ws;
     m->ws_bytes = 3 * m->act_bytes + align256(spec_ws);
+    m->layer_fused = !(d->flags & FNO_PLAN_SPLIT_LAYER) && d->h == 128 && d->w == 128 &&
+                     d->modes[0] == 16 && d->modes[1] == 16 &&
+                     fused_mixed_available(*reinterpret_cast<Plan *>(m->spec)) &&
+                     layer_out_supported(d->width, d->batch);
+    m->row_table = nullptr;
+    if (m->layer_fused) {
+        std::vector<unsigned char> img;
+        inverse_row_operand_tf32(img);
+        cudaError_t e = layer_out_init(d->width);
+        if (e == cudaSuccess) e = cudaMalloc(&m->row_table, img.size());
+        if (e == cudaSuccess)
+            e = cudaMemcpy(m->row_table, img.data(), img.size(), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            if (m->row_table) cudaFree(m->row_table);
+            fno_plan_destroy(m->spec);
+            delete m;
+            return FNO_ERR_CUDA;
+        }
+        m->z_off = m->ws_bytes;
+        m->ws_bytes += align256(layer_out_z_bytes(d->batch, d->width));
+    }
     m->kernels = 1 + d->nlayers * (spec_kernels + 1) + 1;
     *out = reinterpret_cast<fno_model_t>(m);
     return FNO_OK;
@@ -437,13 +467,37 @@ fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_param
         }
         if (cudaGetLastError() != cudaSuccess) return FNO_ERR_CUDA;
         for (int l = 0; l < d.nlayers; ++l) {
+            const int last = (l == d.nlayers - 1);
+            const float *W = p->pw_w + (size_t)l * d.width * d.width;
+            const float *bias = p->pw_b + (size_t)l * d.width;
+            if constexpr (std::is_same<T, float>::value) {
+                if (m.layer_fused) {
+                    const Plan &sp = *reinterpret_cast<const Plan *>(m.spec);
+                    const Buffers b{A, spec_w + l * spec_stride, nullptr, spec_ws};
+                    LayerOutArgs la{};
+                    if (fused_forward_mixed(sp, b, &la.Y, s) != cudaSuccess) return FNO_ERR_CUDA;
+                    la.tw = sp.tw[0];
+                    la.Z = reinterpret_cast<float *>(ws + m.z_off);
+                    la.x = A;
+                    la.W = W;
+                    la.bias = bias;
+                    la.out = Tn;
+                    la.table = m.row_table;
+                    la.batch = d.batch;
+                    la.width = d.width;
+                    la.gelu = last ? 0 : 1;
+                    la.err = err;
+                    if (layer_out_launch(la, m.num_sms, s) != cudaSuccess) return FNO_ERR_CUDA;
+                    T *tmp = A;
+                    A = Tn;
+                    Tn = tmp;
+                    continue;
+                }
+            }
             fno_status_t st = fno_spectral_conv_forward(m.spec, A, spec_w + l * spec_stride, S,
                                                         m.spec_ws_bytes ? spec_ws : nullptr,
                                                         stream);
             if (st != FNO_OK) return st;
-            const int last = (l == d.nlayers - 1);
-            const float *W = p->pw_w + (size_t)l * d.width * d.width;
-            const float *bias = p->pw_b + (size_t)l * d.width;
             if (m.layer_tc) {
                 if (linear_tc(A, d.width, W, bias, S, Tn, d.width, last ? 0 : 1) != cudaSuccess)
                     return FNO_ERR_CUDA;
@@ -492,6 +546,7 @@ fno_status_t fno_model_destroy(fno_model_t model) {
     if (!model) return FNO_OK;
     Model *m = reinterpret_cast<Model *>(model);
     fno_status_t st = fno_plan_destroy(m->spec);
+    if (m->row_table) cudaFree(m->row_table);
     delete m;
     return st;
 }

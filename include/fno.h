@@ -126,6 +126,16 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * The products involved are small; the kernels are bound by the latency of
  * their loads and by their SIMT steps, not by arithmetic.                   */
 #define FNO_PLAN_TENSOR_EXTRA 256u
+/* FNO stack (fno_model_plan) only: run each layer as the spectral
+ * convolution's three kernels, which write the spectral branch out, followed
+ * by the 1x1-linear kernel that adds it (bias, sum, GELU).  The default for
+ * float32 128x128 layers with 16x16 modes and 32 or 64 channels instead runs
+ * the forward transform and the mixing, a column-step kernel, and ONE
+ * tensor-core GEMM per image row whose K concatenates the inverse row DFT's
+ * coefficients and the input channels (3xTF32), so that the spectral branch
+ * never reaches global memory.  Both match the oracle; an ablation switch.
+ * fno_spectral_conv_plan accepts and ignores it.                             */
+#define FNO_PLAN_SPLIT_LAYER 512u
 
 /* One work item of the fused kernel, as recorded under FNO_PLAN_TRACE.
  * Times are the GPU's global nanosecond timer.                              */

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle
-from fft_gemm_ifft_gb300 import FnoModel, workloads
+from fft_gemm_ifft_gb300 import FnoModel, capi, workloads
 from parity_util import assert_close, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -15,9 +15,9 @@ def _lib(fno, oracle_mod):
     yield
 
 
-def run_model(case, x, params, batch):
+def run_model(case, x, params, batch, flags=0):
     m = FnoModel(batch, case.h, case.w, case.modes, case.cin_lift, case.width, case.nlayers,
-                 case.hidden, case.cout)
+                 case.hidden, case.cout, flags=flags)
     dev = {k: to_dev(v) for k, v in params.items()}
     y = m(to_dev(x), dev)
     torch.cuda.synchronize()
@@ -61,6 +61,43 @@ def test_stack_ragged_tiles(shape):
     got, _ = run_model(case, x, p, case.batch)
     ref = oracle.fno_forward(x, workloads.fno_params_for_oracle(p), case.modes)
     assert_close(got, ref, "f32", f"FNO stack {shape}")
+
+
+@pytest.mark.parametrize("shape", [
+    # batch, width, nlayers, hidden, cout on the 128 x 128 grid, 16 x 16 modes:
+    # the layers' output half as one GEMM per image row (default) or as the
+    # inverse kernel plus the 1x1-linear kernel (FNO_PLAN_SPLIT_LAYER); batch 3
+    # leaves the persistent CTAs unequal tile counts, the last layer has no GELU
+    (2, 64, 2, 128, 1),
+    (3, 32, 2, 48, 2),
+    (1, 64, 1, 16, 3),
+], ids=["w64", "w32_uneven_tiles", "single_layer"])
+@pytest.mark.parametrize("flags", [0, capi.FNO_PLAN_SPLIT_LAYER, capi.FNO_PLAN_TENSOR_EXTRA],
+                         ids=["fused_layer", "split_layer", "fused_layer_tc_mix"])
+def test_layer_output_paths_match_oracle(shape, flags):
+    b, width, nl, hidden, cout = shape
+    case = workloads.FnoCase("layer", batch=b, width=width, nlayers=nl, h=128, w=128,
+                             modes=(16, 16), hidden=hidden, cout=cout)
+    x = workloads.make_fno_inputs(case)
+    p = workloads.make_fno_params(case)
+    got, kernels = run_model(case, x, p, case.batch, flags)
+    # lift, four kernels a layer, head
+    assert kernels == 2 + 4 * nl
+    ref = oracle.fno_forward(x, workloads.fno_params_for_oracle(p), case.modes)
+    assert_close(got, ref, "f32", f"FNO stack {shape} flags={flags}")
+
+
+def test_fused_layer_output_is_a_different_path():
+    # the fused output half sums the inverse row DFT and the 1x1 linear in one
+    # accumulator: equal to the split path within rounding, not bit for bit
+    case = workloads.FnoCase("layer", batch=1, width=64, nlayers=1, h=128, w=128,
+                             modes=(16, 16), hidden=16, cout=1)
+    x = workloads.make_fno_inputs(case)
+    p = workloads.make_fno_params(case)
+    fused, _ = run_model(case, x, p, case.batch, 0)
+    split, _ = run_model(case, x, p, case.batch, capi.FNO_PLAN_SPLIT_LAYER)
+    assert not np.array_equal(fused, split)
+    assert_close(fused, split, "f32", "fused vs split layer output")
 
 
 def test_full_stack_sampled():
