@@ -19,8 +19,10 @@
 // Zr[o][k] = Re Z_o[t][k], Zr[o][16 + k] = Im Z_o[t][k].
 //
 // Kernel 1 (k_colinv) computes Z for every (batch, channel) image -- the
-// column step -- and stores it as rows [b][t][o][32], so that one image row's
-// coefficients for all channels are one contiguous 128-byte-wide box.
+// column step -- and stores it split for 3xTF32 as rows [b][t][hi, lo][o][32]
+// (hi = the value, lo = its remainder below tf32), so that one image row's
+// coefficients for all channels are one contiguous 128-byte-wide box: the
+// B operand [Zr_hi; Zr_lo] stacked along N.
 // Kernel 2 (k_layer_gemm) walks tiles (b, t) of 128 pixels persistently, one
 // CTA per SM, with specialised warps as the 1x1-linear kernel
 // (fno_pointwise.cu): a load warp brings the tile's activations [C][128] and
@@ -55,7 +57,8 @@ __device__ __forceinline__ void grid_trigger() {
 }
 
 // ---------------------------------------------------------------------------
-// Kernel 1: Z[b][t][o][k | 16 + k] = Re | Im sum_j Y[b][o][j][k] e^{+2 pi i g(j) t / 128}.
+// Kernel 1: Z[b][t][h][o][k | 16 + k] = Re | Im sum_j Y[b][o][j][k] e^{+2 pi i g(j) t / 128},
+// h = 0 the value, h = 1 its remainder below tf32.
 // One CTA per image; thread (t1, k), t1 < 16: the eight partial sums
 // U[g1] = sum_{g2 = -2..1} Y[g1 + 8 g2][k] e^{+2 pi i (g1 + 8 g2) t1 / 128}
 // (the kept frequencies g = g1 + 8 g2 run over -16..15), then the 8-point
@@ -93,20 +96,22 @@ __global__ void __launch_bounds__(kColThreads) k_colinv(const float2 *__restrict
 #pragma unroll
     for (int t2 = 0; t2 < 8; ++t2) {
         const float2 v = z[fft::bitrev(t2, 3)];
-        float *row = Z + (((size_t)b * kN0 + t1 + 16 * t2) * width + o) * kZW;
+        float *row = Z + (((size_t)b * kN0 + t1 + 16 * t2) * 2 * width + o) * kZW;
         row[k] = v.x;
         row[kM1 + k] = v.y;
+        row[(size_t)width * kZW + k] = tcu::tf32_lo(v.x);
+        row[(size_t)width * kZW + kM1 + k] = tcu::tf32_lo(v.y);
     }
 }
 
 // ---------------------------------------------------------------------------
 // Kernel 2: the GEMM per image row.
 // ---------------------------------------------------------------------------
-constexpr int kCompute = 512;             // compute threads
-constexpr int kWarps = kCompute / 32;
-constexpr int kTWarps = 8;                // warps 0..7 transpose the activations
-constexpr int kEWarps = kWarps - kTWarps; // warps 8..15 run the epilogue
-constexpr int kThreads = kCompute + 64;   // + load and MMA warps
+constexpr int kTWarps = 4;                // warps 0..3 move the activations into tensor memory
+constexpr int kEWarps = 16;               // warps 4..19 run the epilogue (GELU-bound)
+constexpr int kWarps = kTWarps + kEWarps;
+constexpr int kCompute = 32 * kWarps;
+constexpr int kThreads = kCompute + 96;   // + a load warp and two MMA warps
 constexpr int kRows = 128;                // M: the pixels of one image row
 constexpr uint32_t kTile = 16384;         // 128 rows x 128 bytes
 constexpr int kTmemCols = 512;
@@ -124,19 +129,22 @@ struct Lay {
     static constexpr uint32_t kX = 2 * kKC * kHalf;             // ring: activations [C][128]
     static constexpr uint32_t kXBytes = (uint32_t)C * kRows * 4;
     static constexpr int kNX = 4;
-    static constexpr uint32_t kZ = kX + kNX * kXBytes;           // ring: Zr [hi (TMA); lo]
+    static constexpr uint32_t kZ = kX + kNX * kXBytes;           // ring: Zr [hi; lo] (one box)
     static constexpr uint32_t kZBytes = 2 * kHalf;
     static constexpr int kNZ = 4;
     static constexpr uint32_t kAlloc = kZ + kNZ * kZBytes + 1024;
     static constexpr uint32_t kLimit = 227u * 1024u;
     static constexpr uint32_t kStatic = 1024;                   // barriers, biases (bound)
     // tensor memory: accumulator b at columns [b 2C, b 2C + 2C) (the hi half,
-    // then the lo half), T hi / lo, and the two A chunk buffers (hi, lo)
+    // then the lo half), T hi / lo, and three A chunk buffers (hi, lo): chunk
+    // q may be written once chunk q - 3's MMAs are done, so that a transpose
+    // has a whole tile's MMAs to hide under
     static constexpr uint32_t kTc = 4 * C;                      // T hi, T lo: 32 columns each
     static constexpr uint32_t kAc = kTc + 64;                   // A buffer a: kAc + 64 a (hi, lo)
+    static constexpr int kNA = 3;
     static_assert(C == 32 || C == 64, "32 or 64 channels");
     static_assert(kAlloc + kStatic <= kLimit, "shared memory");
-    static_assert(kAc + 128 <= kTmemCols, "tensor memory");
+    static_assert(kAc + 64 * kNA <= kTmemCols, "tensor memory");
 };
 
 struct GParams {
@@ -154,6 +162,15 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar) {
         asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc_smem_addr(bar))
                      : "memory");
 }
+// the same with relaxed semantics: orders no earlier memory accesses (an
+// epilogue warp hands its accumulator back after tcgen05.wait::ld, without
+// waiting for the global stores of the tile before)
+__device__ __forceinline__ void warp_arrive_relaxed(uint64_t *bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0)
+        asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];"
+                     ::"r"(tc_smem_addr(bar)) : "memory");
+}
 __device__ __forceinline__ void compute_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory");
 }
@@ -168,11 +185,11 @@ k_layer_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                                           ~static_cast<uintptr_t>(1023));
     // x_full / x_empty: the activation slots (loaded / transposed);
     // z_full / z_empty: the coefficient slots (loaded / read by the MMAs);
-    // a_full / a_empty: the two A chunk buffers in tensor memory (written /
+    // a_full / a_empty: the A chunk buffers in tensor memory (written /
     // consumed; chunk q of the CTA's sequence, q = j * kKC + c, uses buffer
-    // q % 2); acc_full / acc_empty: the two accumulators
+    // q % kNA); acc_full / acc_empty: the two accumulators
     __shared__ __align__(8) uint64_t x_full[L::kNX], x_empty[L::kNX], z_full[L::kNZ],
-        z_empty[L::kNZ], a_full[2], a_empty[2], acc_full[2], acc_empty[2];
+        z_empty[L::kNZ], a_full[L::kNA], a_empty[L::kNA], acc_full[2], acc_empty[2];
     __shared__ uint32_t s_tmem;
     __shared__ __align__(16) float s_bias[C];
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -190,9 +207,11 @@ k_layer_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             init(&z_full[k], 1);
             init(&z_empty[k], 1);
         }
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < L::kNA; ++k) {
             init(&a_full[k], kTWarps);
             init(&a_empty[k], 1);
+        }
+        for (int k = 0; k < 2; ++k) {
             init(&acc_full[k], 1);
             init(&acc_empty[k], kEWarps);
         }
@@ -213,7 +232,7 @@ k_layer_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
         p.ntiles > (int64_t)blockIdx.x ? (p.ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     auto xslot = [&](int64_t j) { return base + L::kX + (uint32_t)(j % L::kNX) * L::kXBytes; };
     auto zslot = [&](int64_t j) { return base + L::kZ + (uint32_t)(j % L::kNZ) * L::kZBytes; };
-    auto acol = [&](int64_t q) { return tmem + L::kAc + 64u * (uint32_t)(q & 1); };
+    auto acol = [&](int64_t q) { return tmem + L::kAc + 64u * (uint32_t)(q % L::kNA); };
 
     if (warp == kWarps) {
         // ---- load warp: tile j's activations and coefficients
@@ -228,19 +247,23 @@ k_layer_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 arrive_expect_tx(&x_full[sx], L::kXBytes);
                 tma_load_2d_hint(tc_smem_addr(xslot(j)), &xmap, t * kRows, b * C, &x_full[sx], pol);
                 if (j >= L::kNZ) mbar_wait(&z_empty[sz], (uint32_t)(j / L::kNZ - 1), p.err);
-                arrive_expect_tx(&z_full[sz], L::kHalf);
-                tma_load_2d_hint(tc_smem_addr(zslot(j)), &zmap, 0, (int)(tg * C), &z_full[sz], pol);
+                arrive_expect_tx(&z_full[sz], L::kZBytes);
+                tma_load_2d_hint(tc_smem_addr(zslot(j)), &zmap, 0, (int)(tg * 2 * C), &z_full[sz],
+                                 pol);
             }
         }
-    } else if (warp == kWarps + 1) {
-        // ---- MMA warp: per tile the spectral chunk (with channel chunk 0), then
-        // the other channel chunks, into accumulator j % 2; per K step
-        // A_hi [B_hi; B_lo] (N = 2C) and A_lo B_hi (N = C)
+    } else if (warp > kWarps) {
+        // ---- MMA warps: warp kWarps + 1 + (j % 2) takes tile j (accumulator
+        // j % 2), so that one warp's waits and commits overlap the other's
+        // issue (the tensor pipe queues few MMAs); per tile the spectral chunk
+        // (with channel chunk 0), then the other channel chunks; per K step
+        // A_hi [B_hi; B_lo] (N = 2C) and A_lo B_hi (N = C).  A commit tracks
+        // the MMAs of its own thread, and the two warps share no accumulator.
         if ((tid & 31) == 0) {
             constexpr uint32_t id2 = idesc_tf32(2 * C), id1 = idesc_tf32(C);
             const uint32_t w0 = tc_smem_addr(base + L::kW);
             const uint32_t t_hi = tmem + L::kTc, t_lo = t_hi + 32;
-            for (int64_t j = 0; j < nt; ++j) {
+            for (int64_t j = warp - (kWarps + 1); j < nt; j += 2) {
                 const int buf = (int)(j & 1), sz = (int)(j % L::kNZ);
                 const uint32_t zb = tc_smem_addr(zslot(j));
                 const uint32_t d = tmem + (uint32_t)buf * 2 * C;
@@ -248,8 +271,8 @@ k_layer_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 mbar_wait(&z_full[sz], (uint32_t)(j / L::kNZ), p.err);
                 for (int c = 0; c < L::kKC; ++c) {
                     const int64_t q = j * L::kKC + c;
-                    const int ab = (int)(q & 1);
-                    mbar_wait(&a_full[ab], (uint32_t)(q >> 1), p.err);
+                    const int ab = (int)(q % L::kNA);
+                    mbar_wait(&a_full[ab], (uint32_t)(q / L::kNA), p.err);
                     tc_after_sync();
                     if (c == 0) {
 #pragma unroll
@@ -275,87 +298,74 @@ k_layer_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     } else {
         // ---- compute warps, set-up: W as the K-major B operand, chunk c of 32
         // inputs = [hi; lo] (rows = outputs); the biases
-        {
-            constexpr int kPer = C * C / kCompute;
-            float w[kPer];
-#pragma unroll
-            for (int r = 0; r < kPer; ++r) w[r] = p.W[tid + r * kCompute];
-#pragma unroll
-            for (int r = 0; r < kPer; ++r) {
-                const int e = tid + r * kCompute, o = e / C, i = e % C;
-                char *ch = base + L::kW + (uint32_t)(i / 32) * 2 * L::kHalf;
-                *reinterpret_cast<float *>(ch + sw_off(o, i % 32)) = w[r];
-                *reinterpret_cast<float *>(ch + L::kHalf + sw_off(o, i % 32)) = tf32_lo(w[r]);
-            }
+        for (int e = tid; e < C * C; e += kCompute) {
+            const float w = p.W[e];
+            const int o = e / C, i = e % C;
+            char *ch = base + L::kW + (uint32_t)(i / 32) * 2 * L::kHalf;
+            *reinterpret_cast<float *>(ch + sw_off(o, i % 32)) = w;
+            *reinterpret_cast<float *>(ch + L::kHalf + sw_off(o, i % 32)) = tf32_lo(w);
         }
         for (int o = tid; o < C; o += kCompute) s_bias[o] = p.bias[o];
         fence_async_smem();
         compute_sync();
-        // thread -> pixel row = tensor-memory lane; warps w and w + 4 of a group
-        // share the lane quarter w % 4
+        // thread -> pixel row = tensor-memory lane: warp w works on the lane
+        // quarter w % 4
         const int row = 32 * (warp & 3) + (tid & 31);
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         if (warp < kTWarps) {
-            const int half = warp >> 2;
             // the constant A operand T (the inverse row DFT, hi and lo) into
-            // tensor memory: thread (row, half) writes 16 of its row's 32 columns
+            // tensor memory: thread = one row's 32 columns
             {
                 const char *tab = static_cast<const char *>(p.table);
-                float hi[16], lo[16];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const uint32_t off = sw_off(row, 16 * half + u);
-                    hi[u] = *reinterpret_cast<const float *>(tab + off);
-                    lo[u] = *reinterpret_cast<const float *>(tab + kTile + off);
+                for (int half = 0; half < 2; ++half) {
+                    float hi[16], lo[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const uint32_t off = sw_off(row, 16 * half + u);
+                        hi[u] = *reinterpret_cast<const float *>(tab + off);
+                        lo[u] = *reinterpret_cast<const float *>(tab + kTile + off);
+                    }
+                    tmem_st16(tmem + lane_base + L::kTc + 16 * half, hi);
+                    tmem_st16(tmem + lane_base + L::kTc + 32 + 16 * half, lo);
                 }
-                tmem_st16(tmem + lane_base + L::kTc + 16 * half, hi);
-                tmem_st16(tmem + lane_base + L::kTc + 32 + 16 * half, lo);
             }
-            // ---- transposer warps: chunk q of 32 channels into A buffer q % 2
-            // once chunk q - 2's MMAs are done; thread (row, half) takes 16
-            // channels of the chunk, i.e. 16 columns of its lane
+            // ---- transposer warps: chunk q of 32 channels into A buffer q % kNA
+            // once chunk q - kNA's MMAs are done; thread = the chunk's 32
+            // channels of its pixel, i.e. 32 columns of its lane
             for (int64_t j = 0; j < nt; ++j) {
                 mbar_wait(&x_full[j % L::kNX], (uint32_t)(j / L::kNX), p.err);
-                mbar_wait(&z_full[j % L::kNZ], (uint32_t)(j / L::kNZ), p.err);
                 const float *X = reinterpret_cast<const float *>(xslot(j));
                 for (int c = 0; c < L::kKC; ++c) {
                     const int64_t q = j * L::kKC + c;
-                    if (q >= 2) {
-                        mbar_wait(&a_empty[q & 1], (uint32_t)((q >> 1) - 1), p.err);
+                    if (q >= L::kNA) {
+                        mbar_wait(&a_empty[q % L::kNA], (uint32_t)(q / L::kNA - 1), p.err);
                         tc_after_sync();
                     }
-                    if (c == 0) {
-                        // Zr lo beside Zr hi, element by element in the box's layout
-                        const float4 *zh = reinterpret_cast<const float4 *>(zslot(j));
-                        float4 *zl = reinterpret_cast<float4 *>(zslot(j) + L::kHalf);
-                        for (int e = tid; e < (int)(L::kHalf / 16); e += 32 * kTWarps) {
-                            const float4 h = zh[e];
-                            zl[e] = make_float4(tf32_lo(h.x), tf32_lo(h.y), tf32_lo(h.z),
-                                                tf32_lo(h.w));
-                        }
-                        fence_async_smem();
-                    }
-                    const int i0 = 32 * c + 16 * half;
-                    float v[16], lo[16];
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        v[u] = X[(i0 + u) * kRows + row];
-                        lo[u] = tf32_lo(v[u]);
+                    for (int half = 0; half < 2; ++half) {
+                        const int i0 = 32 * c + 16 * half;
+                        float v[16], lo[16];
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            v[u] = X[(i0 + u) * kRows + row];
+                            lo[u] = tf32_lo(v[u]);
+                        }
+                        const uint32_t a = acol(q) + lane_base + 16 * half;
+                        tmem_st16(a, v);
+                        tmem_st16(a + 32, lo);
                     }
-                    const uint32_t a = acol(q) + lane_base + 16 * half;
-                    tmem_st16(a, v);
-                    tmem_st16(a + 32, lo);
                     tmem_st_wait();
                     tc_before_sync();
-                    warp_arrive(&a_full[q & 1]);
+                    warp_arrive(&a_full[q % L::kNA]);
                 }
                 warp_arrive(&x_empty[j % L::kNX]);               // the activations are read
             }
         } else {
             // ---- epilogue warps: hi half + lo half of accumulator j % 2, bias,
             // GELU, stored straight out (a warp writes 128 consecutive bytes of
-            // one output channel per store); thread (row, part) takes C / 2 outputs
-            constexpr int kOut = C / 2;
+            // one output channel per store); thread (row, part) takes C / 4 outputs
+            constexpr int kOut = C / 4;
             const int o0 = ((warp - kTWarps) >> 2) * kOut;
             for (int64_t j = 0; j < nt; ++j) {
                 const int buf = (int)(j & 1);
@@ -363,29 +373,35 @@ k_layer_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 mbar_wait(&acc_full[buf], (uint32_t)(j >> 1), p.err);
                 tc_after_sync();
                 const uint32_t ta = tmem + lane_base + (uint32_t)buf * 2 * C + (uint32_t)o0;
-#pragma unroll
-                for (int g = 0; g < kOut / 16; ++g) {
+                if constexpr (kOut == 16) {
                     float u[16], w[16];
-                    tmem_ld16(ta + 16 * g, u);
-                    tmem_ld16(ta + C + 16 * g, w);
+                    tmem_ld16(ta, u);
+                    tmem_ld16(ta + C, w);
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) v[16 * g + q] = u[q] + w[q];
+                    for (int q = 0; q < 16; ++q) v[q] = u[q] + w[q];
+                } else {
+                    float u[8], w[8];
+                    tmem_ld8(ta, u);
+                    tmem_ld8(ta + C, w);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v[q] = u[q] + w[q];
                 }
                 tc_before_sync();
-                warp_arrive(&acc_empty[buf]);
+                warp_arrive_relaxed(&acc_empty[buf]);
                 const int64_t tg = blockIdx.x + j * gridDim.x;
                 const int64_t b = tg / kN0, t = tg % kN0;
                 float *op = p.out + (b * C + o0) * (int64_t)(kN0 * kN0) + t * kRows + row;
 #pragma unroll
                 for (int q4 = 0; q4 < kOut / 4; ++q4) {
                     const float4 b4 = *reinterpret_cast<const float4 *>(&s_bias[o0 + 4 * q4]);
-                    const float bq[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float r = v[4 * q4 + q] + bq[q];
-                        if (p.gelu) r = gelu_erf(r);
-                        op[(int64_t)(4 * q4 + q) * (kN0 * kN0)] = r;
+                    float r[4] = {v[4 * q4] + b4.x, v[4 * q4 + 1] + b4.y, v[4 * q4 + 2] + b4.z,
+                                  v[4 * q4 + 3] + b4.w};
+                    if (p.gelu) {
+                        gelu_erf2(r[0], r[1]);
+                        gelu_erf2(r[2], r[3]);
                     }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) op[(int64_t)(4 * q4 + q) * (kN0 * kN0)] = r[q];
                 }
             }
         }
@@ -406,8 +422,8 @@ cudaError_t launch_gemm(const LayerOutArgs &a, int num_sms, cudaStream_t s) {
     CUtensorMap xmap, zmap;
     if (!encode_rows_plain(&xmap, a.x, a.batch * C, npix, 4, kRows, C,
                            CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ||
-        !encode_rows_tiled(&zmap, a.Z, a.batch * kN0 * C, kZW, 4, kZW,
-                           CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C))
+        !encode_rows_tiled(&zmap, a.Z, a.batch * kN0 * 2 * C, kZW, 4, kZW,
+                           CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2 * C))
         return cudaErrorInvalidValue;
     GParams gp;
     gp.out = a.out;
@@ -435,11 +451,12 @@ cudaError_t launch_gemm(const LayerOutArgs &a, int num_sms, cudaStream_t s) {
 bool layer_out_supported(int width, int64_t batch) {
     if (!tcu::encoder()) return false;
     // Z's rows are addressed as one 32-bit TMA coordinate
-    return (width == 32 || width == 64) && batch >= 1 && batch * kN0 * width < ((int64_t)1 << 31);
+    return (width == 32 || width == 64) && batch >= 1 &&
+           batch * kN0 * 2 * width < ((int64_t)1 << 31);
 }
 
 size_t layer_out_z_bytes(int64_t batch, int width) {
-    return (size_t)batch * kN0 * width * kZW * sizeof(float);
+    return (size_t)batch * kN0 * 2 * width * kZW * sizeof(float);
 }
 
 cudaError_t layer_out_init(int width) {

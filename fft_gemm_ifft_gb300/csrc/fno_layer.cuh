@@ -11,7 +11,7 @@ namespace fno {
 struct LayerOutArgs {
     const float2 *Y;       // mixed modes, [batch * width][32 kept rows][16 kept columns]
     const float2 *tw;      // tw[j] = exp(-2 pi i j / 128), j < 128
-    float *Z;              // workspace: [batch][128 rows][width][32] (layer_out_z_bytes)
+    float *Z;              // workspace: [batch][128 rows][hi, lo][width][32] (layer_out_z_bytes)
     const float *x;        // the layer's input, [batch][width][128 * 128]
     const float *W;        // 1x1 linear, [width][width] (out, in)
     const float *bias;     // [width]
