@@ -13,6 +13,7 @@
 #include "fno_internal.cuh"
 #include "fno_fused.cuh"
 #include "fno_gelu.cuh"
+#include "fno_head.cuh"
 #include "fno_layer.cuh"
 #include "fno_pointwise.cuh"
 
@@ -33,6 +34,8 @@ struct Model {
     // which 1x1 linears run on the tensor cores (fno_pointwise.cu; otherwise
     // the register-tiled SIMT kernels below)
     bool lift_simt, lift_tc, layer_tc, head_tc;
+    // float32 heads whose shape fits it: the persistent head kernel (fno_head.cu)
+    bool head_fast;
     // the float32 128 x 128 layers: the spectral plan's forward transform and
     // mixing, then the column step and ONE GEMM for the inverse row DFT and the
     // 1x1 linear (fno_layer.cu) instead of the inverse kernel and the linear
@@ -352,10 +355,13 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
     m->lift_tc = !m->lift_simt &&
                  pointwise_supported(d->dtype, d->cin_lift, d->width, 0, false, npix);
     m->layer_tc = pointwise_supported(d->dtype, d->width, d->width, 0, false, npix);
-    m->head_tc = pointwise_supported(d->dtype, d->width, d->hidden, d->cout, true, npix);
+    m->head_fast = head_supported(d->dtype, d->width, d->hidden, d->cout, npix);
+    m->head_tc = !m->head_fast &&
+                 pointwise_supported(d->dtype, d->width, d->hidden, d->cout, true, npix);
     if ((m->lift_tc && pointwise_init(d->dtype, d->cin_lift, d->width, 0, false) != cudaSuccess) ||
         (m->layer_tc && pointwise_init(d->dtype, d->width, d->width, 0, false) != cudaSuccess) ||
-        (m->head_tc && pointwise_init(d->dtype, d->width, d->hidden, d->cout, true) != cudaSuccess)) {
+        (m->head_tc && pointwise_init(d->dtype, d->width, d->hidden, d->cout, true) != cudaSuccess) ||
+        (m->head_fast && head_init(d->width, d->hidden, d->cout) != cudaSuccess)) {
         cudaGetLastError();
         fno_plan_destroy(m->spec);
         delete m;
@@ -510,7 +516,28 @@ fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_param
             A = Tn;
             Tn = tmp;
         }
-        if (m.head_tc) {
+        bool head_done = false;
+        if constexpr (std::is_same<T, float>::value) {
+            if (m.head_fast) {
+                HeadArgs ha{};
+                ha.a = A;
+                ha.W = p->proj1_w;
+                ha.bias = p->proj1_b;
+                ha.P2 = p->proj2_w;
+                ha.c2 = p->proj2_b;
+                ha.out = static_cast<float *>(out);
+                ha.cin = d.width;
+                ha.hidden = d.hidden;
+                ha.cout2 = d.cout;
+                ha.batch = d.batch;
+                ha.npix = m.npix;
+                ha.err = err;
+                if (head_launch(ha, m.num_sms, s) != cudaSuccess) return FNO_ERR_CUDA;
+                head_done = true;
+            }
+        }
+        if (head_done) {
+        } else if (m.head_tc) {
             PointwiseArgs pa{};
             pa.a = A;
             pa.W = p->proj1_w;

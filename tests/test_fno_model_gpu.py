@@ -87,6 +87,27 @@ def test_layer_output_paths_match_oracle(shape, flags):
     assert_close(got, ref, "f32", f"FNO stack {shape} flags={flags}")
 
 
+@pytest.mark.parametrize("shape", [
+    # batch, width, nlayers, h, w, hidden, cout: the persistent head kernel's
+    # variants (32 / 64 inputs, 64 / 128 hidden units, one or several outputs),
+    # pixel counts that are whole 128-pixel tiles, tile counts that leave the
+    # CTAs unequal shares
+    (3, 64, 1, 16, 32, 128, 1),
+    (2, 32, 1, 32, 16, 64, 3),
+    (1, 64, 1, 8, 48, 64, 8),
+    (5, 32, 1, 16, 16, 128, 2),
+], ids=["c64_h128_o1", "c32_h64_o3", "c64_h64_o8", "c32_h128_o2"])
+def test_head_kernel_shapes(shape):
+    b, width, nl, h, w, hidden, cout = shape
+    case = workloads.FnoCase("head", batch=b, width=width, nlayers=nl, h=h, w=w, modes=(2, 2),
+                             hidden=hidden, cout=cout)
+    x = workloads.make_fno_inputs(case)
+    p = workloads.make_fno_params(case)
+    got, _ = run_model(case, x, p, case.batch)
+    ref = oracle.fno_forward(x, workloads.fno_params_for_oracle(p), case.modes)
+    assert_close(got, ref, "f32", f"FNO head {shape}")
+
+
 def test_fused_layer_output_is_a_different_path():
     # the fused output half sums the inverse row DFT and the 1x1 linear in one
     # accumulator: equal to the split path within rounding, not bit for bit
