@@ -45,7 +45,10 @@ constexpr int kTmemCols = 512;
 constexpr int kNA = 3;                    // A chunk buffers in tensor memory
 
 // Shared memory (offsets from a 1024-aligned base): W chunk c (32 inputs) =
-// [hi: H rows x 128 B][lo: H rows x 128 B]; the activation ring; the partial
+// [hi: H rows x 128 B][lo: H rows x 128 B]; the bias as one more K chunk
+// (row o: bias_hi, bias_lo, then zeros), multiplied by a constant A of ones
+// in tensor memory so that the accumulator starts at the bias; the
+// activation ring; the partial
 // second projections of parts 1..3 per tile parity; the output staging tiles
 // [2][C2][128]; bias, P2, c2.
 template <int C, int H, int C2>
@@ -53,7 +56,8 @@ struct Lay {
     static constexpr int kKC = C / 32;
     static constexpr uint32_t kWHalf = (uint32_t)H * 128;
     static constexpr uint32_t kW = 0;
-    static constexpr uint32_t kX = 2 * kKC * kWHalf;
+    static constexpr uint32_t kBias = 2 * kKC * kWHalf;
+    static constexpr uint32_t kX = kBias + kWHalf;
     static constexpr uint32_t kXBytes = (uint32_t)C * kRows * 4;
     static constexpr uint32_t kRedBytes = 2u * 3u * C2 * kRows * 4;
     static constexpr uint32_t kOutBytes = 2u * C2 * kRows * 4;
@@ -68,11 +72,12 @@ struct Lay {
     static constexpr uint32_t kPar = kOut + kOutBytes;
     static constexpr uint32_t kAlloc = kPar + kParBytes + 1024;
     static constexpr uint32_t kAc = 2 * H;          // A buffer a at columns kAc + 64 a
+    static constexpr uint32_t kOnes = kAc + 64 * kNA;   // 16 columns: 1, 1, 0 ...
     static_assert(C == 32 || C == 64, "32 or 64 inputs");
     static_assert(H == 64 || H == 128, "64 or 128 hidden units");
     static_assert(kNX >= 2, "two activation slots");
     static_assert(kAlloc + kStatic <= kLimit, "shared memory");
-    static_assert(kAc + 64 * kNA <= kTmemCols, "tensor memory");
+    static_assert(kOnes + 16 <= kTmemCols, "tensor memory");
 };
 
 struct KParams {
@@ -195,10 +200,12 @@ k_head(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtenso
         }
     } else if (warp > kWarps) {
         // ---- MMA warps: warp kWarps + 1 + (j % 2) takes tile j into
-        // accumulator j % 2; per K step a_hi W_hi, a_hi W_lo, a_lo W_hi (N = H)
+        // accumulator j % 2: first ones x [bias_hi, bias_lo] (the bias in every
+        // row), then per K step a_hi W_hi, a_hi W_lo, a_lo W_hi (N = H)
         if ((tid & 31) == 0) {
             constexpr uint32_t idesc = idesc_tf32(H);
             const uint32_t w0 = tc_smem_addr(base + L::kW);
+            const uint64_t bias_desc = desc_sw128(tc_smem_addr(base + L::kBias));
             for (int64_t j = warp - (kWarps + 1); j < nt; j += 2) {
                 const int buf = (int)(j & 1);
                 const uint32_t d = tmem + (uint32_t)buf * H;
@@ -210,10 +217,10 @@ k_head(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtenso
                     tc_after_sync();
                     const uint32_t a_hi = acol(q), a_lo = a_hi + 32;
                     const uint32_t wh = w0 + (uint32_t)c * 2 * L::kWHalf, wl = wh + L::kWHalf;
+                    if (c == 0) mma_tf32_ts(d, tmem + L::kOnes, bias_desc, idesc, 0u);
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
-                        mma_tf32_ts(d, a_hi + 8 * s, desc_sw128(wh + 32 * s), idesc,
-                                    (c | s) ? 1u : 0u);
+                        mma_tf32_ts(d, a_hi + 8 * s, desc_sw128(wh + 32 * s), idesc, 1u);
                         mma_tf32_ts(d, a_hi + 8 * s, desc_sw128(wl + 32 * s), idesc, 1u);
                         mma_tf32_ts(d, a_lo + 8 * s, desc_sw128(wh + 32 * s), idesc, 1u);
                     }
@@ -232,7 +239,12 @@ k_head(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtenso
             *reinterpret_cast<float *>(ch + sw_off(o, i % 32)) = w;
             *reinterpret_cast<float *>(ch + L::kWHalf + sw_off(o, i % 32)) = tf32_lo(w);
         }
-        for (int o = tid; o < H; o += kCompute) s_bias[o] = p.bias[o];
+        for (int e = tid; e < H * 32; e += kCompute) {
+            const int o = e / 32, k = e % 32;
+            const float b = p.bias[o];
+            *reinterpret_cast<float *>(base + L::kBias + sw_off(o, k)) =
+                k == 0 ? b : (k == 1 ? tf32_lo(b) : 0.f);
+        }
         for (int e = tid; e < C2 * H; e += kCompute) {
             const int c = e / H;
             s_p2[e] = c < p.cout2 ? p.P2[e] : 0.f;
@@ -243,6 +255,13 @@ k_head(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtenso
         const int quarter = warp & 3, row = 32 * quarter + (tid & 31);
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
         if (warp < kTWarps) {
+            // the constant ones operand (columns kOnes, kOnes + 1 = 1, the rest 0)
+            {
+                float one[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) one[u] = u < 2 ? 1.f : 0.f;
+                tmem_st16(tmem + lane_base + L::kOnes, one);
+            }
             // ---- transposer warps: chunk q into A buffer q % kNA once chunk
             // q - kNA's MMAs are done; thread = its pixel's 32 channels of the chunk
             for (int64_t j = 0; j < nt; ++j) {
@@ -283,9 +302,11 @@ k_head(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtenso
                 mbar_wait(&acc_full[buf], (uint32_t)(j >> 1), p.err);
                 tc_after_sync();
                 const uint32_t ta = tmem + lane_base + (uint32_t)buf * H + (uint32_t)o0;
-                float acc[C2];
+                // the second projection as pairs (two partial sums per output,
+                // packed f32x2 fused multiply-adds)
+                unsigned long long acc2[C2];
 #pragma unroll
-                for (int c = 0; c < C2; ++c) acc[c] = 0.f;
+                for (int c = 0; c < C2; ++c) acc2[c] = gelu2_detail::splat(0.f);
                 // 16 columns at a time; the accumulator goes back after the last load
 #pragma unroll
                 for (int g = 0; g < kOut / 16; ++g) {
@@ -297,14 +318,25 @@ k_head(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtenso
                     }
                     const int ob = o0 + 16 * g;
 #pragma unroll
-                    for (int q = 0; q < 16; q += 2) {
-                        float h0 = v[q] + s_bias[ob + q], h1 = v[q + 1] + s_bias[ob + q + 1];
-                        gelu_erf2(h0, h1);
+                    for (int q = 0; q < 16; q += 4) {
+                        gelu_erf2(v[q], v[q + 1]);
+                        gelu_erf2(v[q + 2], v[q + 3]);
+                        const unsigned long long h01 = gelu2_detail::pk(v[q], v[q + 1]);
+                        const unsigned long long h23 = gelu2_detail::pk(v[q + 2], v[q + 3]);
 #pragma unroll
-                        for (int c = 0; c < C2; ++c)
-                            acc[c] = fmaf(s_p2[c * H + ob + q + 1], h1,
-                                          fmaf(s_p2[c * H + ob + q], h0, acc[c]));
+                        for (int c = 0; c < C2; ++c) {
+                            const float4 w4 = *reinterpret_cast<const float4 *>(s_p2 + c * H + ob + q);
+                            acc2[c] = gelu2_detail::fma2(gelu2_detail::pk(w4.x, w4.y), h01, acc2[c]);
+                            acc2[c] = gelu2_detail::fma2(gelu2_detail::pk(w4.z, w4.w), h23, acc2[c]);
+                        }
                     }
+                }
+                float acc[C2];
+#pragma unroll
+                for (int c = 0; c < C2; ++c) {
+                    float a0, a1;
+                    gelu2_detail::upk(acc2[c], a0, a1);
+                    acc[c] = a0 + a1;
                 }
                 // the four parts of a pixel: parts 1..3 leave their sums, part 0
                 // adds them (a buffer per tile parity: a warp runs at most one
