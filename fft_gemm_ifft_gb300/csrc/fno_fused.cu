@@ -1564,8 +1564,10 @@ void fused_plan_release(Plan &p) {
 }
 
 bool fused_mixed_available(const Plan &p) {
-    return p.path == kPathFused && p.dtype == FNO_F32 &&
-           variant(p.g, p.dtype, p.flags) == kVarPdl128 && p.fused_tca && !p.trace;
+    // the mixed modes in float32 (the 16-bit tensor-core mixing writes its own
+    // 16-bit layout for the inverse kernel that reads it)
+    return p.path == kPathFused && variant(p.g, p.dtype, p.flags) == kVarPdl128 &&
+           !p.fused_mixtc && !p.trace;
 }
 
 cudaError_t fused_forward_mixed(const Plan &p, const Buffers &b, const float2 **Y,
@@ -1586,7 +1588,9 @@ cudaError_t fused_forward_mixed(const Plan &p, const Buffers &b, const float2 **
     a.cin = p.cin;
     a.cout = p.cout;
     *Y = a.Y;
-    return Pdl128::forward<float>(p, a, s, true);
+    return with_storage(p.dtype, [&](auto t) {
+        return Pdl128::forward<decltype(t)>(p, a, s, true);
+    });
 }
 
 void inverse_row_operand_tf32(std::vector<unsigned char> &img) { tca::make_table_c32(img); }

@@ -32,10 +32,10 @@ cudaError_t fused_forward_modes(const Plan &p, const void *x, int64_t nimg, floa
 cudaError_t fused3d_forward_modes(const Plan &p, const void *x, int64_t nimg, float2 *out,
                                   cudaStream_t s);
 
-// The float32 128 x 128 layer (16 x 16 modes) up to its mixed modes: the
+// The 128 x 128 layer (16 x 16 modes) up to its mixed modes: the
 // forward-transform and mixing kernels of the three-kernel path alone, for a
 // caller that runs its own inverse (the FNO layer's fused output, fno_layer.cu).
-// True when the plan runs that path with the tensor-core forward transform.
+// True when the plan runs that path and leaves the mixed modes in float32.
 bool fused_mixed_available(const Plan &p);
 // Launches the two kernels; *Y = the mixed modes in the workspace,
 // [batch * cout][32 kept rows][16 kept columns] complex float.

@@ -1,7 +1,8 @@
-// fno_layer.cu -- the output half of a float32 FNO layer (128 x 128 grid,
-// 16 x 16 kept modes per block): the inverse transform of the mixed modes,
-// the 1x1 linear of the layer's input, bias and GELU, without writing the
-// spectral branch out.
+// fno_layer.cu -- the output half of an FNO layer (128 x 128 grid, 16 x 16
+// kept modes per block; activations in float32 or a 16-bit storage type,
+// arithmetic in float32): the inverse transform of the mixed modes, the 1x1
+// linear of the layer's input, bias and GELU, without writing the spectral
+// branch out.
 //
 // The layer is the one of the TurboFNO article (gsyq.cn/news/457482, §5):
 // out = GELU(K(x) + W x + b), K(x) the spectral convolution (truncated forward
@@ -36,6 +37,8 @@
 // finished accumulator and store it, under the next tiles' transposes and
 // MMAs.  The spectral branch never reaches global memory.
 #include "fno_layer.cuh"
+
+#include <type_traits>
 
 #include "fno_fft.cuh"
 #include "fno_gelu.cuh"
@@ -121,13 +124,13 @@ constexpr int kTmemCols = 512;
 // N (rows 0..C-1 hi, C..2C-1 lo), so that x_hi [B_hi; B_lo] is one MMA of
 // N = 2C and x_lo B_hi one of N = C: an MMA of N <= 128 costs about the same
 // on these tensor cores whatever N is, and 3xTF32 then takes two per K step.
-template <int C>
+template <int C, typename T>
 struct Lay {
     static constexpr int kKC = C / 32;                          // K chunks of the 1x1 linear
     static constexpr uint32_t kHalf = (uint32_t)C * 128;        // C rows x 128 bytes
     static constexpr uint32_t kW = 0;                           // W chunk c: [hi; lo] at c * 2 kHalf
     static constexpr uint32_t kX = 2 * kKC * kHalf;             // ring: activations [C][128]
-    static constexpr uint32_t kXBytes = (uint32_t)C * kRows * 4;
+    static constexpr uint32_t kXBytes = (uint32_t)(C * kRows * sizeof(T));
     static constexpr int kNX = 4;
     static constexpr uint32_t kZ = kX + kNX * kXBytes;           // ring: Zr [hi; lo] (one box)
     static constexpr uint32_t kZBytes = 2 * kHalf;
@@ -150,7 +153,7 @@ struct Lay {
 struct GParams {
     const float *W, *bias;
     const void *table;
-    float *out;                // [batch][C][128 * 128]
+    void *out;                 // [batch][C][128 * 128], storage type
     int64_t ntiles;            // batch x 128 image rows
     int gelu;
     int *err;
@@ -175,11 +178,14 @@ __device__ __forceinline__ void compute_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory");
 }
 
-template <int C>
+template <int C, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 k_layer_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap zmap,
              const GParams p) {
-    using L = Lay<C>;
+    using L = Lay<C, T>;
+    // 16-bit activations are exact in tf32: no remainder operand, and the
+    // channel part needs only a_hi [W_hi; W_lo]
+    constexpr bool kLo = std::is_same<T, float>::value;
     extern __shared__ __align__(1024) char smem_raw[];
     char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
@@ -287,7 +293,7 @@ k_layer_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                     for (int s = 0; s < 4; ++s) {
                         const uint64_t wd = desc_sw128(w0 + (uint32_t)c * 2 * L::kHalf + 32 * s);
                         mma_tf32_ts(d, a_hi + 8 * s, wd, id2, 1u);
-                        mma_tf32_ts(d, a_lo + 8 * s, wd, id1, 1u);
+                        if constexpr (kLo) mma_tf32_ts(d, a_lo + 8 * s, wd, id1, 1u);
                     }
                     if (c == 0) mma_commit(&z_empty[sz]);           // Zr has been read
                     if (c == L::kKC - 1) mma_commit(&acc_full[buf]);
@@ -335,7 +341,7 @@ k_layer_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
             // channels of its pixel, i.e. 32 columns of its lane
             for (int64_t j = 0; j < nt; ++j) {
                 mbar_wait(&x_full[j % L::kNX], (uint32_t)(j / L::kNX), p.err);
-                const float *X = reinterpret_cast<const float *>(xslot(j));
+                const T *X = reinterpret_cast<const T *>(xslot(j));
                 for (int c = 0; c < L::kKC; ++c) {
                     const int64_t q = j * L::kKC + c;
                     if (q >= L::kNA) {
@@ -345,15 +351,17 @@ k_layer_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const int i0 = 32 * c + 16 * half;
-                        float v[16], lo[16];
+                        float v[16];
 #pragma unroll
-                        for (int u = 0; u < 16; ++u) {
-                            v[u] = X[(i0 + u) * kRows + row];
-                            lo[u] = tf32_lo(v[u]);
-                        }
+                        for (int u = 0; u < 16; ++u) v[u] = Storage<T>::load(X + (i0 + u) * kRows + row);
                         const uint32_t a = acol(q) + lane_base + 16 * half;
                         tmem_st16(a, v);
-                        tmem_st16(a + 32, lo);
+                        if constexpr (kLo) {
+                            float lo[16];
+#pragma unroll
+                            for (int u = 0; u < 16; ++u) lo[u] = tf32_lo(v[u]);
+                            tmem_st16(a + 32, lo);
+                        }
                     }
                     tmem_st_wait();
                     tc_before_sync();
@@ -390,7 +398,7 @@ k_layer_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                 warp_arrive_relaxed(&acc_empty[buf]);
                 const int64_t tg = blockIdx.x + j * gridDim.x;
                 const int64_t b = tg / kN0, t = tg % kN0;
-                float *op = p.out + (b * C + o0) * (int64_t)(kN0 * kN0) + t * kRows + row;
+                T *op = static_cast<T *>(p.out) + (b * C + o0) * (int64_t)(kN0 * kN0) + t * kRows + row;
 #pragma unroll
                 for (int q4 = 0; q4 < kOut / 4; ++q4) {
                     const float4 b4 = *reinterpret_cast<const float4 *>(&s_bias[o0 + 4 * q4]);
@@ -401,7 +409,8 @@ k_layer_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
                         gelu_erf2(r[2], r[3]);
                     }
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) op[(int64_t)(4 * q4 + q) * (kN0 * kN0)] = r[q];
+                    for (int q = 0; q < 4; ++q)
+                        Storage<T>::store(op + (int64_t)(4 * q4 + q) * (kN0 * kN0), r[q]);
                 }
             }
         }
@@ -415,13 +424,12 @@ k_layer_gemm(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ C
     }
 }
 
-template <int C>
+template <int C, typename T>
 cudaError_t launch_gemm(const LayerOutArgs &a, int num_sms, cudaStream_t s) {
-    using L = Lay<C>;
+    using L = Lay<C, T>;
     const int64_t npix = (int64_t)kN0 * kN0;
     CUtensorMap xmap, zmap;
-    if (!encode_rows_plain(&xmap, a.x, a.batch * C, npix, 4, kRows, C,
-                           CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ||
+    if (!encode_rows_plain(&xmap, a.x, a.batch * C, npix, sizeof(T), kRows, C, tma_type<T>()) ||
         !encode_rows_tiled(&zmap, a.Z, a.batch * kN0 * 2 * C, kZW, 4, kZW,
                            CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2 * C))
         return cudaErrorInvalidValue;
@@ -443,7 +451,7 @@ cudaError_t launch_gemm(const LayerOutArgs &a, int num_sms, cudaStream_t s) {
     cfg.stream = s;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_layer_gemm<C>, xmap, zmap, gp);
+    return cudaLaunchKernelEx(&cfg, k_layer_gemm<C, T>, xmap, zmap, gp);
 }
 
 }  // namespace
@@ -459,9 +467,12 @@ size_t layer_out_z_bytes(int64_t batch, int width) {
     return (size_t)batch * kN0 * 2 * width * kZW * sizeof(float);
 }
 
-cudaError_t layer_out_init(int width) {
-    return width == 32 ? raise_smem_limit(k_layer_gemm<32>, Lay<32>::kAlloc)
-                       : raise_smem_limit(k_layer_gemm<64>, Lay<64>::kAlloc);
+cudaError_t layer_out_init(fno_dtype_t dt, int width) {
+    return with_storage(dt, [&](auto t) {
+        using T = decltype(t);
+        return width == 32 ? raise_smem_limit(k_layer_gemm<32, T>, Lay<32, T>::kAlloc)
+                           : raise_smem_limit(k_layer_gemm<64, T>, Lay<64, T>::kAlloc);
+    });
 }
 
 cudaError_t layer_out_launch(const LayerOutArgs &a, int num_sms, cudaStream_t s) {
@@ -477,7 +488,10 @@ cudaError_t layer_out_launch(const LayerOutArgs &a, int num_sms, cudaStream_t s)
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, k_colinv, a.Y, a.tw, a.Z, a.width);
     if (e != cudaSuccess) return e;
-    e = a.width == 32 ? launch_gemm<32>(a, num_sms, s) : launch_gemm<64>(a, num_sms, s);
+    e = with_storage(a.dtype, [&](auto t) {
+        using T = decltype(t);
+        return a.width == 32 ? launch_gemm<32, T>(a, num_sms, s) : launch_gemm<64, T>(a, num_sms, s);
+    });
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

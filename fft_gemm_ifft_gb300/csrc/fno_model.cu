@@ -381,7 +381,7 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
     if (m->layer_fused) {
         std::vector<unsigned char> img;
         inverse_row_operand_tf32(img);
-        cudaError_t e = layer_out_init(d->width);
+        cudaError_t e = layer_out_init(d->dtype, d->width);
         if (e == cudaSuccess) e = cudaMalloc(&m->row_table, img.size());
         if (e == cudaSuccess)
             e = cudaMemcpy(m->row_table, img.data(), img.size(), cudaMemcpyHostToDevice);
@@ -476,7 +476,7 @@ fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_param
             const int last = (l == d.nlayers - 1);
             const float *W = p->pw_w + (size_t)l * d.width * d.width;
             const float *bias = p->pw_b + (size_t)l * d.width;
-            if constexpr (std::is_same<T, float>::value) {
+            {
                 if (m.layer_fused) {
                     const Plan &sp = *reinterpret_cast<const Plan *>(m.spec);
                     const Buffers b{A, spec_w + l * spec_stride, nullptr, spec_ws};
@@ -490,6 +490,7 @@ fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_param
                     la.out = Tn;
                     la.table = m.row_table;
                     la.batch = d.batch;
+                    la.dtype = d.dtype;
                     la.width = d.width;
                     la.gelu = last ? 0 : 1;
                     la.err = err;

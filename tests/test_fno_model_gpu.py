@@ -134,23 +134,27 @@ def test_full_stack_sampled():
 
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
 @pytest.mark.parametrize("shape", [
-    # batch, width, nlayers, h, w, modes, hidden, cout
-    (2, 8, 2, 32, 32, (4, 4), 16, 2),
-    (3, 70, 1, 16, 16, (4, 4), 70, 3),           # ragged channel tiles
-    (2, 64, 2, 128, 128, (16, 16), 128, 1),      # the three-kernel 128^2 layer, 16-bit
-], ids=["small", "ragged_channels", "layer_128"])
+    # batch, width, nlayers, h, w, modes, hidden, cout, flags
+    (2, 8, 2, 32, 32, (4, 4), 16, 2, 0),
+    (3, 70, 1, 16, 16, (4, 4), 70, 3, 0),           # ragged channel tiles
+    # the 128^2 layers: the one-GEMM output half (16-bit activations, no
+    # remainder operand) and the split form
+    (2, 64, 2, 128, 128, (16, 16), 128, 1, 0),
+    (3, 32, 2, 128, 128, (16, 16), 48, 2, 0),
+    (2, 64, 2, 128, 128, (16, 16), 128, 1, 512),
+], ids=["small", "ragged_channels", "layer_128", "layer_128_w32", "layer_128_split"])
 def test_stack_16bit_storage(dt, shape):
     # x, the activations, spec_w and out stored in fp16 / bf16, arithmetic in
     # float32; the oracle runs in float64 on the same rounded x and spec_w, so
     # the difference is the rounding of the stored activations (the 16-bit
     # tolerance class)
-    b, width, nl, h, w, modes, hidden, cout = shape
+    b, width, nl, h, w, modes, hidden, cout, flags = shape
     case = workloads.FnoCase("half", batch=b, width=width, nlayers=nl, h=h, w=w, modes=modes,
                              hidden=hidden, cout=cout)
     x = workloads.to_storage(workloads.make_fno_inputs(case), dt)
     p = workloads.make_fno_params(case)
     p["spec_w"] = workloads.to_storage(p["spec_w"], dt)
-    m = FnoModel(b, h, w, modes, case.cin_lift, width, nl, hidden, cout, dtype=dt)
+    m = FnoModel(b, h, w, modes, case.cin_lift, width, nl, hidden, cout, flags=flags, dtype=dt)
     dev = {k: to_dev(v, dt) if k == "spec_w" else to_dev(v) for k, v in p.items()}
     y = m(to_dev(x, dt), dev)
     torch.cuda.synchronize()
