@@ -1,5 +1,6 @@
 // fno_head.cu -- the projection head of the FNO stack as one persistent
-// tensor-core kernel.
+// tensor-core kernel (activations and output in float32 or a 16-bit storage
+// type, arithmetic in float32).
 //
 // The head is the two-layer 1x1 projection of the TurboFNO article's model
 // (gsyq.cn/news/457482, §5): out = P2 GELU(W a + b) + c2 per pixel, W of
@@ -26,6 +27,7 @@
 #include "fno_head.cuh"
 
 #include <algorithm>
+#include <type_traits>
 
 #include "fno_gelu.cuh"
 #include "fno_tc.cuh"
@@ -51,16 +53,17 @@ constexpr int kNA = 3;                    // A chunk buffers in tensor memory
 // activation ring; the partial
 // second projections of parts 1..3 per tile parity; the output staging tiles
 // [2][C2][128]; bias, P2, c2.
-template <int C, int H, int C2>
+template <int C, int H, int C2, typename T>
 struct Lay {
     static constexpr int kKC = C / 32;
     static constexpr uint32_t kWHalf = (uint32_t)H * 128;
     static constexpr uint32_t kW = 0;
     static constexpr uint32_t kBias = 2 * kKC * kWHalf;
     static constexpr uint32_t kX = kBias + kWHalf;
-    static constexpr uint32_t kXBytes = (uint32_t)C * kRows * 4;
+    static constexpr uint32_t kXBytes = (uint32_t)(C * kRows * sizeof(T));
     static constexpr uint32_t kRedBytes = 2u * 3u * C2 * kRows * 4;
-    static constexpr uint32_t kOutBytes = 2u * C2 * kRows * 4;
+    static constexpr uint32_t kOutBytes =
+        ((uint32_t)(2 * C2 * kRows * sizeof(T)) + 1023u) & ~1023u;   // staging, storage type
     static constexpr uint32_t kParBytes = ((uint32_t)(H + C2 * H + C2) * 4 + 15) & ~15u;
     static constexpr uint32_t kLimit = 227u * 1024u;
     static constexpr uint32_t kStatic = 1024;
@@ -82,7 +85,7 @@ struct Lay {
 
 struct KParams {
     const float *W, *bias, *P2, *c2;
-    float *out;
+    void *out;
     int cout2;
     int64_t npix, ptiles, ntiles;
     int *err;
@@ -110,11 +113,13 @@ __device__ __forceinline__ void quarter_sync(int quarter) {
     asm volatile("bar.sync %0, 128;" ::"r"(2 + quarter) : "memory");
 }
 
-template <int C, int H, int C2>
+template <int C, int H, int C2, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 k_head(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap omap,
        const KParams p) {
-    using L = Lay<C, H, C2>;
+    using L = Lay<C, H, C2, T>;
+    // 16-bit activations are exact in tf32: no remainder operand or product
+    constexpr bool kLo = std::is_same<T, float>::value;
     extern __shared__ __align__(1024) char smem_raw[];
     char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
@@ -190,7 +195,7 @@ k_head(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtenso
                 const int64_t tg = blockIdx.x + j * gridDim.x;
                 const int b = (int)(tg / p.ptiles), p0 = (int)((tg % p.ptiles) * kRows);
                 tma_store_2d(&omap, p0, b * p.cout2,
-                             tc_smem_addr(base + L::kOut + (uint32_t)buf * C2 * kRows * 4));
+                             tc_smem_addr(base + L::kOut + (uint32_t)(buf * C2 * kRows * sizeof(T))));
                 bulk_commit();
                 bulk_wait_read();
                 asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];"
@@ -222,7 +227,8 @@ k_head(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtenso
                     for (int s = 0; s < 4; ++s) {
                         mma_tf32_ts(d, a_hi + 8 * s, desc_sw128(wh + 32 * s), idesc, 1u);
                         mma_tf32_ts(d, a_hi + 8 * s, desc_sw128(wl + 32 * s), idesc, 1u);
-                        mma_tf32_ts(d, a_lo + 8 * s, desc_sw128(wh + 32 * s), idesc, 1u);
+                        if constexpr (kLo)
+                            mma_tf32_ts(d, a_lo + 8 * s, desc_sw128(wh + 32 * s), idesc, 1u);
                     }
                     if (c == L::kKC - 1) mma_commit(&acc_full[buf]);
                     mma_commit(&a_empty[ab]);
@@ -266,7 +272,7 @@ k_head(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtenso
             // q - kNA's MMAs are done; thread = its pixel's 32 channels of the chunk
             for (int64_t j = 0; j < nt; ++j) {
                 mbar_wait(&x_full[j % L::kNX], (uint32_t)(j / L::kNX), p.err);
-                const float *X = reinterpret_cast<const float *>(xslot(j));
+                const T *X = reinterpret_cast<const T *>(xslot(j));
                 for (int c = 0; c < L::kKC; ++c) {
                     const int64_t q = j * L::kKC + c;
                     if (q >= kNA) {
@@ -276,15 +282,17 @@ k_head(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtenso
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const int i0 = 32 * c + 16 * half;
-                        float v[16], lo[16];
+                        float v[16];
 #pragma unroll
-                        for (int u = 0; u < 16; ++u) {
-                            v[u] = X[(i0 + u) * kRows + row];
-                            lo[u] = tf32_lo(v[u]);
-                        }
+                        for (int u = 0; u < 16; ++u) v[u] = Storage<T>::load(X + (i0 + u) * kRows + row);
                         const uint32_t a = acol(q) + lane_base + 16 * half;
                         tmem_st16(a, v);
-                        tmem_st16(a + 32, lo);
+                        if constexpr (kLo) {
+                            float lo[16];
+#pragma unroll
+                            for (int u = 0; u < 16; ++u) lo[u] = tf32_lo(v[u]);
+                            tmem_st16(a + 32, lo);
+                        }
                     }
                     tmem_st_wait();
                     tc_before_sync();
@@ -351,14 +359,14 @@ k_head(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtenso
                     // the staging tile [cout2][128] of this parity is free once
                     // tile j - 2 has been read out
                     if (j >= 2) mbar_wait(&o_empty[buf], (uint32_t)((j - 2) >> 1), p.err);
-                    float *ob = reinterpret_cast<float *>(base + L::kOut) + buf * C2 * kRows;
+                    T *ob = reinterpret_cast<T *>(base + L::kOut) + buf * C2 * kRows;
 #pragma unroll
                     for (int c = 0; c < C2; ++c) {
                         if (c < p.cout2) {
                             float r = s_c2[c] + acc[c];
 #pragma unroll
                             for (int k = 0; k < 3; ++k) r += rb[(k * C2 + c) * kRows + row];
-                            ob[c * kRows + row] = r;
+                            Storage<T>::store(ob + c * kRows + row, r);
                         }
                     }
                     fence_async_smem();
@@ -381,40 +389,47 @@ struct Pick {
     uint32_t smem;
     int cin;
 };
-template <int C, int H, int C2>
+template <int C, int H, int C2, typename T>
 Pick make_pick() {
-    return {(const void *)k_head<C, H, C2>, Lay<C, H, C2>::kAlloc, C};
+    return {(const void *)k_head<C, H, C2, T>, Lay<C, H, C2, T>::kAlloc, C};
 }
-Pick pick(int cin, int hidden, int cout2) {
+template <typename T>
+Pick pick_t(int cin, int hidden, int cout2) {
     const bool c1 = cout2 <= 1;
     if (cin <= 32) {
-        if (hidden <= 64) return c1 ? make_pick<32, 64, 1>() : make_pick<32, 64, 8>();
-        return c1 ? make_pick<32, 128, 1>() : make_pick<32, 128, 8>();
+        if (hidden <= 64) return c1 ? make_pick<32, 64, 1, T>() : make_pick<32, 64, 8, T>();
+        return c1 ? make_pick<32, 128, 1, T>() : make_pick<32, 128, 8, T>();
     }
-    if (hidden <= 64) return c1 ? make_pick<64, 64, 1>() : make_pick<64, 64, 8>();
-    return c1 ? make_pick<64, 128, 1>() : make_pick<64, 128, 8>();
+    if (hidden <= 64) return c1 ? make_pick<64, 64, 1, T>() : make_pick<64, 64, 8, T>();
+    return c1 ? make_pick<64, 128, 1, T>() : make_pick<64, 128, 8, T>();
+}
+Pick pick(fno_dtype_t dt, int cin, int hidden, int cout2) {
+    return with_storage(dt, [&](auto t) { return pick_t<decltype(t)>(cin, hidden, cout2); });
 }
 
 }  // namespace
 
 bool head_supported(fno_dtype_t dt, int cin, int hidden, int cout2, int64_t npix) {
-    if (dt != FNO_F32 || !tcu::encoder()) return false;
+    if ((dt != FNO_F32 && dt != FNO_F16 && dt != FNO_BF16) || !tcu::encoder()) return false;
     return (cin == 32 || cin == 64) && (hidden == 64 || hidden == 128) && cout2 >= 1 &&
            cout2 <= 8 && npix > 0 && npix % kRows == 0 && npix < ((int64_t)1 << 31);
 }
 
-cudaError_t head_init(int cin, int hidden, int cout2) {
-    const Pick k = pick(cin, hidden, cout2);
+cudaError_t head_init(fno_dtype_t dt, int cin, int hidden, int cout2) {
+    const Pick k = pick(dt, cin, hidden, cout2);
     return raise_smem_limit(k.fn, k.smem);
 }
 
 cudaError_t head_launch(const HeadArgs &a, int num_sms, cudaStream_t s) {
-    const Pick k = pick(a.cin, a.hidden, a.cout2);
+    const Pick k = pick(a.dtype, a.cin, a.hidden, a.cout2);
+    const size_t eb = a.dtype == FNO_F32 ? 4 : 2;
+    const CUtensorMapDataType ty =
+        a.dtype == FNO_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                           : (a.dtype == FNO_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
     CUtensorMap xmap, omap;
-    if (!tcu::encode_rows_plain(&xmap, a.a, a.batch * a.cin, a.npix, 4, kRows, a.cin,
-                                CU_TENSOR_MAP_DATA_TYPE_FLOAT32) ||
-        !tcu::encode_rows_plain(&omap, a.out, a.batch * a.cout2, a.npix, 4, kRows, a.cout2,
-                                CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+    if (!tcu::encode_rows_plain(&xmap, a.a, a.batch * a.cin, a.npix, eb, kRows, a.cin, ty) ||
+        !tcu::encode_rows_plain(&omap, a.out, a.batch * a.cout2, a.npix, eb, kRows, a.cout2, ty))
         return cudaErrorInvalidValue;
     KParams kp;
     kp.W = a.W;

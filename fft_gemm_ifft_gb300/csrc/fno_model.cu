@@ -34,7 +34,7 @@ struct Model {
     // which 1x1 linears run on the tensor cores (fno_pointwise.cu; otherwise
     // the register-tiled SIMT kernels below)
     bool lift_simt, lift_tc, layer_tc, head_tc;
-    // float32 heads whose shape fits it: the persistent head kernel (fno_head.cu)
+    // heads whose shape fits it: the persistent head kernel (fno_head.cu)
     bool head_fast;
     // the float32 128 x 128 layers: the spectral plan's forward transform and
     // mixing, then the column step and ONE GEMM for the inverse row DFT and the
@@ -361,7 +361,7 @@ fno_status_t fno_model_plan(fno_model_t *out, const fno_model_desc_t *d) {
     if ((m->lift_tc && pointwise_init(d->dtype, d->cin_lift, d->width, 0, false) != cudaSuccess) ||
         (m->layer_tc && pointwise_init(d->dtype, d->width, d->width, 0, false) != cudaSuccess) ||
         (m->head_tc && pointwise_init(d->dtype, d->width, d->hidden, d->cout, true) != cudaSuccess) ||
-        (m->head_fast && head_init(d->width, d->hidden, d->cout) != cudaSuccess)) {
+        (m->head_fast && head_init(d->dtype, d->width, d->hidden, d->cout) != cudaSuccess)) {
         cudaGetLastError();
         fno_plan_destroy(m->spec);
         delete m;
@@ -518,7 +518,7 @@ fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_param
             Tn = tmp;
         }
         bool head_done = false;
-        if constexpr (std::is_same<T, float>::value) {
+        {
             if (m.head_fast) {
                 HeadArgs ha{};
                 ha.a = A;
@@ -526,12 +526,13 @@ fno_status_t fno_forward(fno_model_t model, const void *x, const fno_model_param
                 ha.bias = p->proj1_b;
                 ha.P2 = p->proj2_w;
                 ha.c2 = p->proj2_b;
-                ha.out = static_cast<float *>(out);
+                ha.out = out;
                 ha.cin = d.width;
                 ha.hidden = d.hidden;
                 ha.cout2 = d.cout;
                 ha.batch = d.batch;
                 ha.npix = m.npix;
+                ha.dtype = d.dtype;
                 ha.err = err;
                 if (head_launch(ha, m.num_sms, s) != cudaSuccess) return FNO_ERR_CUDA;
                 head_done = true;

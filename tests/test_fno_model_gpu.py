@@ -142,7 +142,11 @@ def test_full_stack_sampled():
     (2, 64, 2, 128, 128, (16, 16), 128, 1, 0),
     (3, 32, 2, 128, 128, (16, 16), 48, 2, 0),
     (2, 64, 2, 128, 128, (16, 16), 128, 1, 512),
-], ids=["small", "ragged_channels", "layer_128", "layer_128_w32", "layer_128_split"])
+    # the persistent head kernel with 16-bit activations and output, 8-output
+    # variant (32 -> 64 -> 3) on whole 128-pixel tiles
+    (2, 32, 1, 16, 32, (2, 2), 64, 3, 0),
+], ids=["small", "ragged_channels", "layer_128", "layer_128_w32", "layer_128_split",
+        "head_c32_h64_o3"])
 def test_stack_16bit_storage(dt, shape):
     # x, the activations, spec_w and out stored in fp16 / bf16, arithmetic in
     # float32; the oracle runs in float64 on the same rounded x and spec_w, so
