@@ -555,6 +555,228 @@ constexpr size_t smem_a3_tc() {
            C3::kSmemTw + 1024;
 }
 
+// ---------------------------------------------------------------------------
+// Kernel C on the tensor cores (64^3 volumes, 16^3 modes per block): the row
+// inverse of every plane, 16 kept bins -> 64 samples, is a 3xTF32 GEMM per
+// plane computed transposed, y^T = T Zo'^T with Zo' = [Re Zo | Im Zo] (K = 32
+// per row) and T[n] = s [c(k) cos(2 pi k n / 64) | -c(k) sin(...)], s =
+// 1 / 64^3: M = 64 output samples, N = 64 rows, the three products
+// concatenated along K, [T_hi | T_hi | T_lo] against [Zo'_hi | Zo'_lo | Zo'_hi]
+// (K = 96).  Tensor-memory lane n then holds sample n of every row, so the 16
+// lanes of a warp that carry data store 64 contiguous bytes of a row at a
+// time.  Z_c (the sums over the volume's kept rows) and the 8-point inverse
+// DFT over the residues stay in registers as in k_phase_c3; each plane's
+// spectrum goes to shared memory just before its column inverse (SIMT), whose
+// rows are written as the GEMM's operand.  Four CTAs of four warps per SM as
+// for k_phase_c3: one operand buffer, two 64-column accumulators, a plane's
+// MMAs running while the threads store the plane before and compute the next
+// plane's column inverse.
+struct Geo3C {
+    static constexpr int N = 64, M1 = 16, K0 = 32;
+    static constexpr uint32_t kRows64 = 64u * 128u;     // 64 rows x 32 fp32, swizzled
+    static constexpr uint32_t kT = 0;                   // T_hi, T_lo
+    static constexpr uint32_t kZ = kT + 2 * kRows64;    // Zo'_hi, Zo'_lo of a plane
+    static constexpr uint32_t kSpec = kZ + 2 * kRows64; // one plane's spectrum [32][16]
+    static constexpr uint32_t kTmemCols = 128;          // two plane accumulators
+};
+
+template <class C3>
+constexpr size_t smem_c3_tc() {
+    return Geo3C::kSpec + (size_t)C3::NKP * 8 + (size_t)(C3::N0 + C3::N1) * 8 + 1024;
+}
+
+// grid: volumes x C0 CTAs
+template <class C3, typename T>
+__global__ void __launch_bounds__(kNT, 4)
+k_phase_c3_tc(Args a, const void *table) {
+    using Gm = Geo3C;
+    using namespace tcu;
+    constexpr int NT = kNT;
+    constexpr int N0 = C3::N0, N1 = C3::N1, N2 = C3::N2, C0 = C3::C0, R0 = C3::R0;
+    constexpr int NKP = C3::NKP, M1 = C3::M2, QT = NKP / NT;   // M1: bins per kept row
+    constexpr int G1 = 8, T1 = N1 / G1, G2 = C3::M1 / G1;      // column inverse: g = g1 + 8 g2
+    static_assert(N1 == Gm::N && N2 == Gm::N && M1 == Gm::M1 && C3::M1 == Gm::M1 &&
+                  2 * M1 == Gm::K0, "64^3 volumes, 16^3 modes per block");
+    static_assert(NKP % NT == 0 && T1 * M1 == NT, "one column-inverse unit per thread");
+    static_assert(2 * Gm::kRows64 >= (uint32_t)C3::kYRows * NKP * 8,
+                  "a stage of kept rows fits over each pair of 64-row tiles");
+    extern __shared__ __align__(1024) char smem_raw[];
+    char *base = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+    __shared__ __align__(8) uint64_t bar_t, bar_mma[2];
+    __shared__ uint32_t s_tmem;
+    const unsigned long long t0 = a.trace ? trace_now() : 0;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int vol = blockIdx.x / C0, c = blockIdx.x % C0;
+    float2 *ysp = reinterpret_cast<float2 *>(base + Gm::kSpec);            // [32][16]
+    float2 *twa = ysp + NKP;                                                 // W_N0
+    float2 *tw1 = twa + N0;                                                  // W_N1
+    if (tid == 0) {
+        const uint64_t *bars[3] = {&bar_t, &bar_mma[0], &bar_mma[1]};
+        for (const uint64_t *b : bars)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(b)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(tc_smem_addr(&s_tmem)), "r"(Gm::kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    for (int e = tid; e < N0; e += NT) twa[e] = a.tw0[e];
+    for (int e = tid; e < N1; e += NT) tw1[e] = a.tw1[e];
+    tc_before_sync();
+    __syncthreads();
+    tc_after_sync();
+    const uint32_t tmem = s_tmem;
+    pdl_wait();                                  // kernel B's mixed modes are complete
+    const unsigned long long t_ready = a.trace ? trace_now() : 0;
+    const float2 *Yv = a.Y + (size_t)vol * C3::NK;
+
+    // 1. Z[r] = sum_m Y[r + R0 m] conj(W_N0^{f c}) for this thread's plane modes,
+    //    then the R0-point inverse DFT over r: spectra of planes c + C0 t, kept
+    //    in registers.  The volume's kept rows come through two cp.async stages
+    //    over the operand tiles (the T operand is fetched afterwards).
+    constexpr int kRows = C3::kYRows, kNSt = C3::K0 / kRows;
+    auto issue_y = [&](int st) {
+        float2 *d = reinterpret_cast<float2 *>(base + (st & 1) * 2 * Gm::kRows64);
+        const float2 *g = Yv + (size_t)st * kRows * NKP;
+        for (int e = tid; e < kRows * NKP / 2; e += NT) cp_async16(d + 2 * e, g + 2 * e);
+    };
+    issue_y(0);
+    cp_async_commit();
+    issue_y(1);
+    cp_async_commit();
+    float2 z[QT][R0];
+#pragma unroll
+    for (int r = 0; r < R0; ++r)
+#pragma unroll
+        for (int q = 0; q < QT; ++q) z[q][r] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int st = 0; st < kNSt; ++st) {
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+        __syncthreads();                         // stage st is in its buffer
+        const float2 *yb = reinterpret_cast<const float2 *>(base + (st & 1) * 2 * Gm::kRows64);
+#pragma unroll
+        for (int rr = 0; rr < kRows; ++rr) {
+            const int j0 = st * kRows + rr;
+            const float2 w = twa[(freq0<C3>(j0) * c) & (N0 - 1)];
+            const float2 wc = make_float2(w.x, -w.y);
+#pragma unroll
+            for (int q = 0; q < QT; ++q) cmac(z[q][j0 % R0], yb[rr * NKP + tid + q * NT], wc);
+        }
+        __syncthreads();                         // its buffer is free again
+        if (st + 2 < kNSt) issue_y(st + 2);
+        cp_async_commit();
+    }
+#pragma unroll
+    for (int q = 0; q < QT; ++q) fft::fft_dif<R0, 1>(z[q]);   // plane t at z[q][bitrev(t)]
+    if (tid == 0) {                              // the T operand over the first stage
+        fence_async_smem();
+        arrive_expect_tx(&bar_t, 2 * Gm::kRows64);
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     ::"r"(tc_smem_addr(base + Gm::kT)), "l"(table), "r"(2 * Gm::kRows64),
+                     "r"(tc_smem_addr(&bar_t)) : "memory");
+    }
+    const unsigned long long t_spec = a.trace ? trace_now() : 0;
+    bool ok = mbar_wait(&bar_t, 0, a.err);
+
+    // 2. planes: spectrum -> column inverse (SIMT) -> Zo' operands -> MMAs -> rows out
+    char *Zhi = base + Gm::kZ, *Zlo = Zhi + Gm::kRows64;
+    const int k = tid % M1, t1 = tid / M1;       // this thread's column-inverse unit
+    T *dst = static_cast<T *>(a.y) + (size_t)vol * N0 * N1 * N2;
+    // plane t's rows from accumulator t & 1: with M = 64, sample n sits in lane
+    // 32 (n / 16) + n % 16, so warp w reads samples 16 w .., lanes 0..15
+    // carrying data
+    auto drain = [&](int t) {
+        const int i0 = c + C0 * t, n = 16 * warp + (lane & 15);
+        T *out = dst + (size_t)i0 * N1 * N2 + n;
+        const uint32_t acc = tmem + (uint32_t)(64 * (t & 1)) + ((uint32_t)(32 * warp) << 16);
+#pragma unroll
+        for (int g = 0; g < N1 / 16; ++g) {
+            float v[16];
+            tmem_ld16(acc + 16 * g, v);          // rows 16 g .. 16 g + 15
+            if (!ok) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            }
+            if (lane < 16) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) Io<T>::store(out + (size_t)(16 * g + i) * N2, v[i]);
+            }
+        }
+    };
+#pragma unroll 1
+    for (int t = 0; t < R0; ++t) {
+        // the plane's spectrum from the registers (the buffer's previous plane
+        // was read before the barrier that ended the last iteration)
+        fft::unroll<0, R0>([&](auto ri) {
+            constexpr int r = decltype(ri)::value;
+            if (fft::bitrev(t, fft::ilog2(R0)) == r) {
+#pragma unroll
+                for (int q = 0; q < QT; ++q) ysp[tid + q * NT] = z[q][r];
+            }
+        });
+        __syncthreads();
+        // Zo[t1 + 8 t2][k] = sum_g1 e^{+2 pi i g1 t2 / 8} sum_g2 Y[g][k] e^{+2 pi i g t1 / 64}
+        float2 zc[G1];
+#pragma unroll
+        for (int g1 = 0; g1 < G1; ++g1) {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int g2 = -G2; g2 < G2; ++g2) {
+                const int g = g1 + G1 * g2, j = g < 0 ? g + 2 * C3::M1 : g;   // kept row of g
+                const float2 wv = tw1[(g * t1) & (N1 - 1)];   // e^{-2 pi i g t1 / 64}
+                cmac(acc, ysp[j * M1 + k], make_float2(wv.x, -wv.y));
+            }
+            zc[g1] = acc;
+        }
+        fft::fft_dif<G1, 1>(zc);
+        if (t > 0) ok &= mbar_wait(&bar_mma[(t - 1) & 1], (uint32_t)((t - 1) >> 1), a.err);
+        tc_after_sync();
+#pragma unroll
+        for (int t2 = 0; t2 < G1; ++t2) {
+            const float2 v = zc[fft::bitrev(t2, fft::ilog2(G1))];
+            const int row = t1 + T1 * t2;
+            const uint32_t ore = sw_off(row, k), oim = sw_off(row, M1 + k);
+            *reinterpret_cast<float *>(Zhi + ore) = v.x;
+            *reinterpret_cast<float *>(Zhi + oim) = v.y;
+            *reinterpret_cast<float *>(Zlo + ore) = tf32_lo(v.x);
+            *reinterpret_cast<float *>(Zlo + oim) = tf32_lo(v.y);
+        }
+        fence_async_smem();
+        tc_before_sync();
+        __syncthreads();                         // the operands are written, the spectrum
+                                                 // read; plane t - 2's accumulator drained
+        if (tid == 0) {
+            tc_after_sync();
+            const uint32_t d = tmem + (uint32_t)(64 * (t & 1));
+            const uint32_t zh = tc_smem_addr(Zhi), zl = tc_smem_addr(Zlo);
+            const uint32_t th = tc_smem_addr(base + Gm::kT), tl = th + Gm::kRows64;
+            constexpr uint32_t id = idesc_tf32(64, 64);    // M = 64 samples, N = 64 rows
+#pragma unroll
+            for (int s = 0; s < Gm::K0 / 8; ++s) {
+                mma_tf32(d, desc_sw128(th + s * 32), desc_sw128(zh + s * 32), id, s ? 1u : 0u);
+                mma_tf32(d, desc_sw128(th + s * 32), desc_sw128(zl + s * 32), id, 1u);
+                mma_tf32(d, desc_sw128(tl + s * 32), desc_sw128(zh + s * 32), id, 1u);
+            }
+            mma_commit(&bar_mma[t & 1]);
+        }
+        if (t > 0) drain(t - 1);
+        tc_before_sync();
+    }
+    ok &= mbar_wait(&bar_mma[(R0 - 1) & 1], (uint32_t)((R0 - 1) >> 1), a.err);
+    tc_after_sync();
+    drain(R0 - 1);
+    tc_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc_after_sync();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(Gm::kTmemCols));
+    }
+    cta_record(a, 2, a.trace_c, t0, t_ready, t_spec);  // compute: the planes' spectra, tail: the planes
+}
+
 // Host: the row-DFT operand for 64 samples and 16 bins, per K chunk [T_hi |
 // T_lo] with T[j][n] = cos(2 pi k n / 64) (j = k < 16) or -sin (j = 16 + k),
 // split in double (T_hi as stored is read at tf32 precision; T_lo is the rest)
@@ -574,6 +796,28 @@ void make_table_a3(std::vector<unsigned char> &img) {
             const uint32_t chunk = (uint32_t)(n / 32) * Gm::kTChunk;
             memcpy(&img[chunk + sw_off(j, n % 32)], &hi, 4);
             memcpy(&img[chunk + sw_off(2 * Gm::M2 + j, n % 32)], &lo, 4);
+        }
+}
+
+// Host: kernel C's row-inverse operands T_hi and T_lo, two 64-row tiles (k < 16: s c(k) cos(2 pi k n / 64), 16 + k: -s c(k) sin(...), s =
+// 1 / 64^3), split in double
+void make_table_c3(std::vector<unsigned char> &img) {
+    using Gm = Geo3C;
+    using tcu::sw_off;
+    using tcu::tf32_lo;
+    img.assign(2 * Gm::kRows64, 0);
+    const double two_pi = 2.0 * M_PI, s = 1.0 / ((double)Gm::N * Gm::N * Gm::N);
+    for (int n = 0; n < Gm::N; ++n)
+        for (int k = 0; k < Gm::M1; ++k) {
+            const double ck = (k == 0 || 2 * k == Gm::N) ? 1.0 : 2.0;
+            const double ang = two_pi * (double)k * (double)n / (double)Gm::N;
+            const double v[2] = {s * ck * std::cos(ang), -s * ck * std::sin(ang)};
+            for (int h = 0; h < 2; ++h) {
+                const float hi = (float)v[h];
+                const float lo = (float)(v[h] - (double)(hi - tf32_lo(hi)));
+                memcpy(&img[sw_off(n, h * Gm::M1 + k)], &hi, 4);
+                memcpy(&img[sw_off(Gm::N + n, h * Gm::M1 + k)], &lo, 4);
+            }
         }
 }
 
@@ -615,17 +859,29 @@ struct Pdl3 {
         // plane pairs; slower than the register FFTs on the 4 x 32-channel
         // layer, 202 against 173 us a forward)
         p.fused_tca = false;
+        std::vector<unsigned char> img;          // the tensor-core kernels' operands
         if constexpr (std::is_same<T, float>::value) {
             if (e == cudaSuccess && (p.flags & FNO_PLAN_TENSOR_EXTRA) &&
                 !(p.flags & FNO_PLAN_SIMT_TRANSFORM) && tcu::encoder()) {
                 p.fused_tca = true;
                 e = raise_smem_limit(k_phase_a3_tc<C3>, (int)smem_a3_tc<C3>());
-                std::vector<unsigned char> img;
                 make_table_a3(img);
-                if (e == cudaSuccess) e = cudaMalloc(&p.fused_tables, img.size());
-                if (e == cudaSuccess)
-                    e = cudaMemcpy(p.fused_tables, img.data(), img.size(), cudaMemcpyHostToDevice);
             }
+        }
+        // kernel C's row inverse on the tensor cores unless the SIMT transforms
+        // are asked for
+        p.fused_tcc = !(p.flags & FNO_PLAN_SIMT_TRANSFORM);
+        if (e == cudaSuccess && p.fused_tcc) {
+            e = raise_smem_limit(k_phase_c3_tc<C3, T>, (int)smem_c3_tc<C3>());
+            std::vector<unsigned char> imc;
+            make_table_c3(imc);
+            p.fused_table_c = img.size();
+            img.insert(img.end(), imc.begin(), imc.end());
+        }
+        if (e == cudaSuccess && !img.empty()) {
+            e = cudaMalloc(&p.fused_tables, img.size());
+            if (e == cudaSuccess)
+                e = cudaMemcpy(p.fused_tables, img.data(), img.size(), cudaMemcpyHostToDevice);
         }
         if (e == cudaSuccess)
             e = raise_smem_limit(k_phase_b<C3, T, 1, kNT>, smem_b(p.dtype, p.cin, ob + 1, bb));
@@ -719,9 +975,16 @@ struct Pdl3 {
         }
         if (e != cudaSuccess) return e;
         cfg.gridDim = dim3((unsigned)(p.batch * p.cout * C3::C0));
-        cfg.blockDim = dim3(kNT);
-        cfg.dynamicSmemBytes = C3::kSmemC;
-        e = cudaLaunchKernelEx(&cfg, k_phase_c3<C3, T>, a);
+        if (p.fused_tcc) {
+            cfg.blockDim = dim3(kNT);
+            cfg.dynamicSmemBytes = smem_c3_tc<C3>();
+            const void *tab = static_cast<const char *>(p.fused_tables) + p.fused_table_c;
+            e = cudaLaunchKernelEx(&cfg, k_phase_c3_tc<C3, T>, a, tab);
+        } else {
+            cfg.blockDim = dim3(kNT);
+            cfg.dynamicSmemBytes = C3::kSmemC;
+            e = cudaLaunchKernelEx(&cfg, k_phase_c3<C3, T>, a);
+        }
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }

@@ -102,7 +102,9 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
  * layer (32x32 modes) the forward transform (a kind::f16 tcgen05 GEMM per
  * image) and the inverse (a kind::tf32 GEMM per image); for the float32
  * 128x128 layer (16x16 modes) the forward transform and the inverse (3xTF32
- * GEMMs per image, TMA loads and stores).  An ablation switch.              */
+ * GEMMs per image, TMA loads and stores); for the 64x64x64 layer (16x16x16
+ * modes per block) the inverse's row transform (a 3xTF32 GEMM per pair of
+ * planes).  An ablation switch.                                             */
 #define FNO_PLAN_SIMT_TRANSFORM 64u
 /* The weights passed to fno_spectral_conv_forward are in the packed layout
  * written by fno_spectral_conv_pack_weights (weights are parameters: pack once
