@@ -821,8 +821,195 @@ void make_table_c3(std::vector<unsigned char> &img) {
         }
 }
 
+// ---------------------------------------------------------------------------
+// Kernel B of the float32 3-D layer with the weights streamed by TMA (batch up
+// to 4, up to 32 channels each way, weights in the standard layout).  One
+// persistent CTA per SM walks the runs of kR = 16 kept modes along the last
+// axis, run it = blockIdx.x, blockIdx.x + gridDim.x, ...  A producer warp
+// brings a run's weights W[blk][i][o][local .. local + 15] through a ring of
+// stages as boxes of 16 input channels x Cout x 16 modes (one 4-D TMA load,
+// 64 KB for 32 outputs), starting before kernel A has finished: the weights
+// do not depend on it.  The 8 compute warps, thread (o, mode pair), fetch the
+// run's kept modes of every batch row from L2 (cp.async, the next run's
+// during the current run's products), accumulate from shared memory and
+// store the mixed modes.
+namespace mixtma {
+#ifndef FNO_MIX_TMA_I
+#define FNO_MIX_TMA_I 16
+#endif
+#ifndef FNO_MIX_TMA_STAGES
+#define FNO_MIX_TMA_STAGES 3
+#endif
+constexpr int kR = 16;                           // kept modes a run
+constexpr int kI = FNO_MIX_TMA_I;                // input channels a stage
+constexpr int kStages = FNO_MIX_TMA_STAGES;
+constexpr int kCompute = 256;                    // threads of the 8 compute warps
+constexpr int kThreads = kCompute + 32;          // and the producer warp
+constexpr int kMaxC = 32, kMaxB = 4;
+constexpr uint32_t kStageBytes = (uint32_t)kR * 8 * kMaxC * kI;        // 64 KB
+constexpr uint32_t kXsBytes = (uint32_t)kMaxB * kMaxC * kR * 8;        // one run's kept modes
+constexpr size_t kSmem = (size_t)kStages * kStageBytes + 2 * kXsBytes + 1024;   // + alignment
+static_assert(kCompute == kMaxC * kR / 2, "one thread per (output, mode pair)");
+}  // namespace mixtma
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, int c3, uint64_t *bar) {
+    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+                 ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+                   "r"(tcu::tc_smem_addr(bar)) : "memory");
+}
+
+template <class C3>
+__global__ void __launch_bounds__(mixtma::kThreads, 1)
+k_mix_tma(const __grid_constant__ CUtensorMap wmap, Args a) {
+    using namespace mixtma;
+    using tcu::tc_smem_addr;
+    constexpr int NK = C3::NK, kRuns = NK / kR;
+    static_assert(NK % kR == 0 && C3::MR % kR == 0, "a run stays on one line of the last axis");
+    extern __shared__ __align__(1024) char smem_raw[];
+    // the stages start on a 1024-byte boundary (TMA destinations)
+    char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+    float2 *xs = reinterpret_cast<float2 *>(smem + kStages * kStageBytes);   // [2][batch][cin][kR]
+    __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const unsigned long long t0 = a.trace ? trace_now() : 0;
+    const int cin = a.cin, cout = a.cout, nb = a.batch;
+    const int ib = cin < kI ? cin : kI;          // input channels of a box
+    const int nst = (cin + kI - 1) / kI;         // stages a run
+    const uint32_t box = (uint32_t)kR * 8 * cout * ib;
+    if (tid == 0) {
+        for (int st = 0; st < kStages; ++st) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&full[st])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;"
+                         ::"r"(tc_smem_addr(&empty[st])), "r"(kCompute));
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    pdl_trigger();                               // kernel C may set itself up
+    if (warp == kCompute / 32) {                 // the producer
+        if ((tid & 31) == 0) {
+            // a TMA destination must be aligned: check rather than issue a bad copy
+            bool ok = (tc_smem_addr(smem) & 1023u) == 0;
+            if (!ok) raise_dev_error(a.err, kDevBounds);
+            int k = 0;
+            for (int it = blockIdx.x; it < kRuns && ok; it += gridDim.x) {
+                int blk, local;
+                C3::wmap(it * kR, blk, local);
+                for (int st = 0; st < nst && ok; ++st, ++k) {
+                    const int sl = k % kStages;
+                    if (k >= kStages) ok &= tcu::mbar_wait(&empty[sl], (uint32_t)(k / kStages - 1), a.err);
+                    if (!ok) break;
+                    tcu::arrive_expect_tx(&full[sl], box);
+                    tma_load_4d(tc_smem_addr(smem + sl * kStageBytes), &wmap, 2 * local, 0, st * kI,
+                                blk, &full[sl]);
+                }
+            }
+        }
+        return;
+    }
+    // thread (o, mode pair r, r + 1)
+    const int o = tid / (kR / 2), r = 2 * (tid % (kR / 2));
+    const bool act = o < cout;
+    auto load_x = [&](int it, int buf) {
+        float2 *d = xs + buf * (kXsBytes / 8);
+        for (int e = tid; e < nb * cin * (kR / 2); e += kCompute) {
+            const int row = e / (kR / 2), pr = e % (kR / 2);   // row = b * cin + i
+            cp_async16(d + row * kR + 2 * pr, a.part + (size_t)row * NK + (size_t)it * kR + 2 * pr);
+        }
+    };
+    pdl_wait();                                  // kernel A's kept modes are complete
+    const unsigned long long t1 = a.trace ? trace_now() : 0;
+    if ((int)blockIdx.x < kRuns) load_x(blockIdx.x, 0);
+    cp_async_commit();
+    bool ok = true;
+    int k = 0, n = 0;
+    for (int it = blockIdx.x; it < kRuns; it += gridDim.x, ++n) {
+        if (it + (int)gridDim.x < kRuns) load_x(it + gridDim.x, (n + 1) & 1);
+        cp_async_commit();
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory");   // this run's kept modes
+        const float2 *x = xs + (n & 1) * (kXsBytes / 8);
+        float2 acc0[kMaxB], acc1[kMaxB];
+#pragma unroll
+        for (int b = 0; b < kMaxB; ++b) acc0[b] = acc1[b] = make_float2(0.f, 0.f);
+        for (int st = 0; st < nst; ++st, ++k) {
+            const int sl = k % kStages;
+            ok &= tcu::mbar_wait(&full[sl], (uint32_t)(k / kStages), a.err);
+            if (act) {
+                const float *ws = reinterpret_cast<const float *>(smem + sl * kStageBytes);
+                const int i1 = cin - st * kI < kI ? cin - st * kI : kI;
+                for (int ii = 0; ii < i1; ++ii) {
+                    const int i = st * kI + ii;
+                    const float4 w = *reinterpret_cast<const float4 *>(
+                        ws + ((size_t)(ii * cout + o) * kR + r) * 2);
+                    const float2 w0 = make_float2(w.x, w.y), w1 = make_float2(w.z, w.w);
+#pragma unroll
+                    for (int b = 0; b < kMaxB; ++b) {
+                        if (b < nb) {
+                            const float4 x2 = *reinterpret_cast<const float4 *>(&x[(b * cin + i) * kR + r]);
+                            cmac(acc0[b], make_float2(x2.x, x2.y), w0);
+                            cmac(acc1[b], make_float2(x2.z, x2.w), w1);
+                        }
+                    }
+                }
+            }
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc_smem_addr(&empty[sl]))
+                         : "memory");
+        }
+        if (act) {
+#pragma unroll
+            for (int b = 0; b < kMaxB; ++b)
+                if (b < nb)
+                    __stcg(reinterpret_cast<float4 *>(a.Y + ((size_t)b * cout + o) * NK +
+                                                      (size_t)it * kR + r),
+                           make_float4(acc0[b].x, acc0[b].y, acc1[b].x, acc1[b].y));
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory");   // xs[n & 1] is read
+    }
+    (void)ok;
+    if (a.trace) {
+        asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory");
+        if (tid == 0) {
+            unsigned smid;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+            fno_trace_record_t rec;
+            rec.item = (1u << 24) | ((unsigned)blockIdx.x & 0xFFFFFFu);
+            rec.worker = smid;
+            rec.t_start = t0;
+            rec.t_ready = t1;
+            rec.t_end = trace_now();
+            rec.t_compute = rec.t_end;
+            a.trace[a.trace_b + blockIdx.x] = rec;
+        }
+    }
+}
+
+// Host: the weights of a 3-D float32 layer as a 4-D tensor map, [blk][i][o][mode
+// (re, im)], boxes of 16 modes x Cout x min(16, Cin) x 1 block
+template <class C3>
+bool encode_wmap(CUtensorMap *map, const void *w, int cin, int cout) {
+    using namespace mixtma;
+    tcu::EncodeTiled fn = tcu::encoder();
+    if (!fn) return false;
+    const cuuint64_t e = 4, run = (cuuint64_t)C3::MBLK * 2;   // floats of one (blk, i, o)
+    const cuuint64_t dims[4] = {run, (cuuint64_t)cout, (cuuint64_t)cin, 4};
+    const cuuint64_t strides[3] = {run * e, run * e * cout, run * e * cout * cin};
+    const cuuint32_t boxd[4] = {(cuuint32_t)kR * 2, (cuuint32_t)cout,
+                                (cuuint32_t)(cin < kI ? cin : kI), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(w), dims, strides, boxd,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 #ifndef FNO_MIX_STREAM
 #define FNO_MIX_STREAM 1
+#endif
+#ifndef FNO_MIX_TMA
+#define FNO_MIX_TMA 1
 #endif
 #ifndef FNO_STREAM_R
 #define FNO_STREAM_R 16
@@ -899,10 +1086,22 @@ struct Pdl3 {
             p.fused_bstream = kStreamR;
             if (e == cudaSuccess) e = raise_smem_limit(stream_kernel<T>(p.batch), xs);
         }
+        // float32, batch <= 4, <= 32 channels, standard weight layout: the
+        // weights streamed by TMA into one persistent CTA per SM (fused_grid CTAs)
+        if constexpr (std::is_same<T, float>::value) {
+            if (FNO_MIX_TMA && e == cudaSuccess && p.fused_bstream && p.batch <= mixtma::kMaxB &&
+                p.cin <= mixtma::kMaxC && p.cout <= mixtma::kMaxC &&
+                !(p.flags & FNO_PLAN_PACKED_WEIGHTS) && !(p.flags & FNO_PLAN_SIMT_MIX) &&
+                tcu::encoder()) {
+                p.fused_grid = std::min(p.num_sms, (int)(C3::NK / mixtma::kR));
+                e = raise_smem_limit(k_mix_tma<C3>, mixtma::kSmem);
+            }
+        }
         if (e == cudaSuccess && (p.flags & FNO_PLAN_TRACE)) {
-            const size_t nB = p.fused_bstream ? (size_t)(C3::NK / p.fused_bstream)
-                                              : (size_t)(C3::NK / kG) * ((p.cout + ob - 1) / ob) *
-                                                    ((p.batch + bb - 1) / bb);
+            const size_t nB = p.fused_grid      ? (size_t)p.fused_grid
+                              : p.fused_bstream ? (size_t)(C3::NK / p.fused_bstream)
+                                                : (size_t)(C3::NK / kG) * ((p.cout + ob - 1) / ob) *
+                                                      ((p.batch + bb - 1) / bb);
             p.trace_records = (size_t)p.batch * (p.cin + p.cout) * C3::C0 + nB;
             e = cudaMalloc(&p.trace, p.trace_records * sizeof(fno_trace_record_t));
         }
@@ -917,8 +1116,9 @@ struct Pdl3 {
         a.npairs = C3::NK / kG;
         a.trace = p.trace;
         a.trace_b = (int)(p.batch * p.cin * C3::C0);
-        a.trace_c = a.trace_b + (p.fused_bstream ? C3::NK / p.fused_bstream
-                                                 : a.npairs * a.nob * a.ng);
+        a.trace_c = a.trace_b + (p.fused_grid      ? p.fused_grid
+                                 : p.fused_bstream ? C3::NK / p.fused_bstream
+                                                   : a.npairs * a.nob * a.ng);
         cudaLaunchAttribute cl;
         cl.id = cudaLaunchAttributeClusterDimension;
         cl.val.clusterDim.x = C3::C0;
@@ -957,7 +1157,20 @@ struct Pdl3 {
         cfg.stream = s;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
-        if (p.fused_bstream) {
+        bool done_b = false;
+        if constexpr (std::is_same<T, float>::value) {
+            if (p.fused_grid) {
+                CUtensorMap wmap;
+                if (!encode_wmap<C3>(&wmap, a.w, p.cin, p.cout)) return cudaErrorInvalidValue;
+                cfg.gridDim = dim3((unsigned)p.fused_grid);
+                cfg.blockDim = dim3(mixtma::kThreads);
+                cfg.dynamicSmemBytes = mixtma::kSmem;
+                e = cudaLaunchKernelEx(&cfg, k_mix_tma<C3>, wmap, a);
+                done_b = true;
+            }
+        }
+        if (done_b) {
+        } else if (p.fused_bstream) {
             cfg.gridDim = dim3((unsigned)(C3::NK / p.fused_bstream));
             cfg.blockDim = dim3(kMixThreads);
             cfg.dynamicSmemBytes = (size_t)p.batch * p.cin * p.fused_bstream * 8;
