@@ -1129,6 +1129,134 @@ constexpr size_t kPdlXpBudget = FNO_PDL_XP_BUDGET;   // kernel B's partial modes
 #endif
 constexpr size_t kPdlWsBudget = FNO_PDL_WS_BUDGET;
 
+// ---------------------------------------------------------------------------
+// Kernel B of the float32 128 x 128 layer with the weights brought in by TMA
+// (up to 64 channels each way, up to 16 samples, weights in the standard
+// layout, kernel A leaving one copy of the kept modes): one CTA per run of
+// kR = 4 kept modes of a kept row.  Thread 0 requests the run's whole weight
+// block W[blk][i][o][local .. local + 3] (Cin x Cout x 4 modes, up to 128 KB)
+// as 4-D TMA boxes of 16 input channels before the CTA waits for kernel A --
+// the weights do not depend on it -- and the kept modes of every batch row
+// follow from L2 once kernel A is complete; thread (batch group, o, mode
+// pair) accumulates its rows from shared memory.
+namespace mix2d {
+constexpr int kR = 4;                            // kept modes a CTA
+constexpr int kI = 16;                           // input channels a box
+constexpr int kThreads = 512;
+constexpr int kMaxC = 64, kMaxB = 16, kRows = 4; // batch rows a thread
+constexpr uint32_t kWBytes = (uint32_t)kMaxC * kMaxC * kR * 8;   // 128 KB
+constexpr uint32_t kXBytes = (uint32_t)kMaxB * kMaxC * kR * 8;   // 32 KB
+constexpr size_t kSmem = (size_t)kWBytes + kXBytes + 1024;       // + alignment
+// batch groups for cout outputs: kNT / (2 cout) >= 4, so kMaxB rows need at
+// most kRows rows a thread
+static_assert(kThreads / (2 * kMaxC) * kRows >= kMaxB, "rows per thread");
+}  // namespace mix2d
+
+template <class Cf>
+__global__ void __launch_bounds__(mix2d::kThreads, 1)
+k_mix_tma2d(const __grid_constant__ CUtensorMap wmap, Args a) {
+    using namespace mix2d;
+    using tcu::tc_smem_addr;
+    constexpr int NK = Cf::NK;
+    static_assert(NK % kR == 0 && Cf::M1 % kR == 0, "a run stays on one kept row");
+    extern __shared__ __align__(1024) char smem_raw[];
+    // the boxes start on a 1024-byte boundary (TMA destinations)
+    char *smem = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+    const float *ws = reinterpret_cast<const float *>(smem);            // [i][o][kR] complex
+    float2 *xs = reinterpret_cast<float2 *>(smem + kWBytes);            // [b][i][kR]
+    __shared__ __align__(8) uint64_t bar_w;
+    const int tid = threadIdx.x;
+    const unsigned long long t0 = a.trace ? trace_now() : 0;
+    const int cin = a.cin, cout = a.cout, nb = a.batch;
+    const int mode0 = blockIdx.x * kR;
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tc_smem_addr(&bar_w)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        // a TMA destination must be aligned: check rather than issue a bad copy
+        if ((tc_smem_addr(smem) & 1023u) != 0) {
+            raise_dev_error(a.err, kDevBounds);
+        } else {
+            int blk, local;
+            Cf::wmap(mode0, blk, local);
+            const int ib = cin < kI ? cin : kI, nbox = (cin + kI - 1) / kI;
+            const uint32_t boxb = (uint32_t)kR * 8 * cout * ib;
+            tcu::arrive_expect_tx(&bar_w, boxb * nbox);
+            for (int k = 0; k < nbox; ++k)
+                asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::"
+                             "complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+                             ::"r"(tc_smem_addr(smem + k * boxb)), "l"(&wmap), "r"(2 * local),
+                               "r"(0), "r"(k * kI), "r"(blk), "r"(tc_smem_addr(&bar_w))
+                             : "memory");
+        }
+    }
+    __syncthreads();
+    pdl_trigger();                               // kernel C may set itself up
+    pdl_wait();                                  // kernel A's kept modes are complete
+    const unsigned long long t1 = a.trace ? trace_now() : 0;
+    for (int e = tid; e < nb * cin * (kR / 2); e += kThreads) {
+        const int row = e / (kR / 2), h = e % (kR / 2);   // row = b * cin + i
+        cp_async16(xs + row * kR + 2 * h, a.part + (size_t)row * NK + mode0 + 2 * h);
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+    const bool ok = tcu::mbar_wait(&bar_w, 0, a.err);
+    __syncthreads();
+    // thread (bg, o, mp): mode pair mp fastest, then the output, then the batch
+    // group; rows b = bg, bg + nbg, ...
+    const int nbg = kThreads / (2 * cout);
+    const int mp = tid & 1, o = (tid >> 1) % cout, bg = (tid >> 1) / cout;
+    if (ok && bg < nbg) {
+        float2 acc0[kRows], acc1[kRows];
+#pragma unroll
+        for (int q = 0; q < kRows; ++q) acc0[q] = acc1[q] = make_float2(0.f, 0.f);
+        for (int i = 0; i < cin; ++i) {
+            const float4 w = *reinterpret_cast<const float4 *>(ws + ((size_t)i * cout + o) * 8 + 4 * mp);
+            const float2 w0 = make_float2(w.x, w.y), w1 = make_float2(w.z, w.w);
+#pragma unroll
+            for (int q = 0; q < kRows; ++q) {
+                const int b = bg + nbg * q;
+                if (b < nb) {
+                    const float4 x2 =
+                        *reinterpret_cast<const float4 *>(&xs[((size_t)b * cin + i) * kR + 2 * mp]);
+                    cmac(acc0[q], make_float2(x2.x, x2.y), w0);
+                    cmac(acc1[q], make_float2(x2.z, x2.w), w1);
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kRows; ++q) {
+            const int b = bg + nbg * q;
+            if (b < nb)
+                __stcg(reinterpret_cast<float4 *>(a.Y + ((size_t)b * cout + o) * NK + mode0 + 2 * mp),
+                       make_float4(acc0[q].x, acc0[q].y, acc1[q].x, acc1[q].y));
+        }
+    }
+    cta_record(a, 1, a.trace_b, t0, t1);
+}
+
+// Host: the weights of a float32 2-D layer as a 4-D tensor map, [blk][i][o][mode
+// (re, im)], boxes of kR modes x Cout x min(16, Cin) x 1 block
+template <class Cf>
+bool encode_wmap2d(CUtensorMap *map, const void *w, int cin, int cout) {
+    using namespace mix2d;
+    tcu::EncodeTiled fn = tcu::encoder();
+    if (!fn) return false;
+    const cuuint64_t e = 4, run = (cuuint64_t)Cf::MBLK * 2;   // floats of one (blk, i, o)
+    const cuuint64_t dims[4] = {run, (cuuint64_t)cout, (cuuint64_t)cin, 2};
+    const cuuint64_t strides[3] = {run * e, run * e * cout, run * e * cout * cin};
+    const cuuint32_t boxd[4] = {(cuuint32_t)kR * 2, (cuuint32_t)cout,
+                                (cuuint32_t)(cin < kI ? cin : kI), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(w), dims, strides, boxd,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+#ifndef FNO_MIX_TMA2D
+#define FNO_MIX_TMA2D 1
+#endif
+
 template <class Cf, class CfC = Cf>
 struct Pdl {
     static constexpr bool kCluster = Cf::N0 >= 256;
@@ -1259,6 +1387,17 @@ struct Pdl {
                               !(p.flags & (FNO_PLAN_SIMT_MIX | FNO_PLAN_PACKED_WEIGHTS)) &&
                               mixtf32_supported(p.batch, p.cin, p.cout, Cf::M1, p.g.nkept);
         if (e == cudaSuccess && p.fused_mixtf32) e = mixtf32_init();
+        // fp32 128 x 128 with one copy of the kept modes: the mixing fed by TMA
+        // (fused_grid CTAs, one per run of kept modes)
+        if constexpr (std::is_same<T, float>::value && Cf::N0 == 128) {
+            if (FNO_MIX_TMA2D && e == cudaSuccess && p.fused_tca && !p.fused_mixtf32 &&
+                !(p.flags & (FNO_PLAN_SIMT_MIX | FNO_PLAN_PACKED_WEIGHTS)) &&
+                p.batch <= mix2d::kMaxB && p.cin <= mix2d::kMaxC && p.cout <= mix2d::kMaxC &&
+                tcu::encoder()) {
+                p.fused_grid = Cf::NK / mix2d::kR;
+                e = raise_smem_limit(k_mix_tma2d<Cf>, mix2d::kSmem);
+            }
+        }
         p.mix_image = p.fused_mixtc && (p.flags & FNO_PLAN_PACKED_WEIGHTS) &&
                       mixtc_image_layout(p.cin, p.cout);
         p.fused_bstream = 0;
@@ -1266,6 +1405,7 @@ struct Pdl {
         if (e == cudaSuccess && (p.flags & FNO_PLAN_TRACE)) {
             const size_t nB = p.fused_mixtc     ? (size_t)mixtc_items(p.g.nkept)
                               : p.fused_mixtf32 ? (size_t)(p.g.nkept / 2)
+                              : p.fused_grid    ? (size_t)p.fused_grid
                                                 : (size_t)(p.g.nkept / kG) * ((p.cout + ob - 1) / ob) *
                                                       ((p.batch + bb - 1) / bb);
             const size_t nA = (size_t)p.batch * p.cin * (p.fused_tca ? 1 : Cf::C);
@@ -1305,6 +1445,7 @@ struct Pdl {
         const int nA = (int)p.batch * p.cin * (p.fused_tca ? 1 : Cf::C);
         const int nB = p.fused_mixtc     ? mixtc_items(p.g.nkept)
                        : p.fused_mixtf32 ? (int)(p.g.nkept / 2)
+                       : p.fused_grid    ? p.fused_grid
                                          : a.npairs * a.nob * a.ng;
         const int nC = (int)p.batch * p.cout * (p.fused_tcc ? 1 : CfC::C);
         a.trace = p.trace;
@@ -1395,6 +1536,15 @@ struct Pdl {
             m.m1 = Cf::M1;
             m.nk = Cf::NK;
             e = mixtf32_launch(m, s);
+        } else if (p.fused_grid) {
+            if constexpr (std::is_same<T, float>::value && Cf::N0 == 128) {
+                CUtensorMap wmap;
+                if (!encode_wmap2d<Cf>(&wmap, a.w, p.cin, p.cout)) return cudaErrorInvalidValue;
+                cfg.gridDim = dim3((unsigned)p.fused_grid);
+                cfg.blockDim = dim3(mix2d::kThreads);
+                cfg.dynamicSmemBytes = mix2d::kSmem;
+                e = cudaLaunchKernelEx(&cfg, k_mix_tma2d<Cf>, wmap, a);
+            }
         } else {
             cfg.gridDim = dim3(nB);
             cfg.blockDim = dim3(kBThreads);

@@ -96,9 +96,10 @@ typedef struct fno_model_s *fno_model_t;    /* opaque FNO-stack plan            
 /* Mix with the SIMT kernel where the tensor-core mixing kernel would run
  * (2-D fp16 / bf16 layers with at most 64 channels and 64 samples; the
  * tensor-core kernel is the default there), and, for the float32 64x64x64
- * layer with at most 4 samples and 32 channels, with the weight-streaming
- * kernel that loads W itself instead of the persistent kernel fed by TMA
- * boxes.  An ablation switch.                                               */
+ * layer with at most 4 samples and 32 channels and the float32 128x128 layer
+ * with at most 16 samples and 64 channels, with the SIMT kernels that load W
+ * themselves instead of the kernels fed by TMA boxes of weights.  An
+ * ablation switch.                                                          */
 #define FNO_PLAN_SIMT_MIX 32u
 /* Run the transforms on the register-FFT kernels instead of the tensor-core
  * kernels that are the default for these shapes: for the 16-bit 256x256
