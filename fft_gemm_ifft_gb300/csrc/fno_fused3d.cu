@@ -232,6 +232,7 @@ __global__ void __launch_bounds__(kNT, FNO_A3_MIN_BLOCKS) k_phase_a3(Args a) {
         }
         __syncthreads();
     }
+    const unsigned long long t_planes = a.trace ? trace_now() : 0;
 
     // residues to shared memory (over the ring), then the cluster's combine
     float2 *pm = reinterpret_cast<float2 *>(ring);   // [R0][NKP]
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(kNT, FNO_A3_MIN_BLOCKS) k_phase_a3(Args a) {
         }
     }
     cluster_sync();                              // peers may still read this CTA's residues
-    cta_record(a, 0, 0, t0, t0);
+    cta_record(a, 0, 0, t0, t0, t_planes);       // compute: the planes, tail: the combine
 }
 
 // grid: volumes x C0 CTAs
