@@ -1388,12 +1388,14 @@ struct Pdl {
                               mixtf32_supported(p.batch, p.cin, p.cout, Cf::M1, p.g.nkept);
         if (e == cudaSuccess && p.fused_mixtf32) e = mixtf32_init();
         // fp32 128 x 128 with one copy of the kept modes: the mixing fed by TMA
-        // (fused_grid CTAs, one per run of kept modes)
+        // (fused_grid CTAs, one per run of kept modes) where a run's weights are
+        // at least 64 KB; with smaller blocks (the 8 x 32-channel layer) the slab
+        // kernel measured as fast or faster (7.1 against 8.3 us a launch)
         if constexpr (std::is_same<T, float>::value && Cf::N0 == 128) {
             if (FNO_MIX_TMA2D && e == cudaSuccess && p.fused_tca && !p.fused_mixtf32 &&
                 !(p.flags & (FNO_PLAN_SIMT_MIX | FNO_PLAN_PACKED_WEIGHTS)) &&
                 p.batch <= mix2d::kMaxB && p.cin <= mix2d::kMaxC && p.cout <= mix2d::kMaxC &&
-                tcu::encoder()) {
+                p.cin * p.cout >= 2048 && tcu::encoder()) {
                 p.fused_grid = Cf::NK / mix2d::kR;
                 e = raise_smem_limit(k_mix_tma2d<Cf>, mix2d::kSmem);
             }
