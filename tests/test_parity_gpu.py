@@ -57,6 +57,10 @@ SMALL = [
     ((64, 64, 64), (16, 16, 16), 2, 5, 3, "f32"),
     ((64, 64, 64), (16, 16, 16), 3, 3, 5, "f16"),
     ((64, 64, 64), (16, 16, 16), 1, 3, 2, "bf16"),
+    # weights by TMA with a partial last box of input channels (3-D: 16 per box;
+    # 128^2: 16 per box, Cin x Cout >= 2048)
+    ((64, 64, 64), (16, 16, 16), 3, 20, 24, "f32"),
+    ((128, 128), (16, 16), 3, 40, 60, "f32"),
     ((8, 8, 8), (2, 3, 4), 2, 3, 2, "f32"),
     ((4, 8, 16), (2, 4, 9), 2, 2, 2, "f32"),
     ((32, 32, 32), (8, 8, 8), 2, 3, 4, "f16"),
