@@ -1139,6 +1139,9 @@ constexpr size_t kPdlWsBudget = FNO_PDL_WS_BUDGET;
 // the weights do not depend on it -- and the kept modes of every batch row
 // follow from L2 once kernel A is complete; thread (batch group, o, mode
 // pair) accumulates its rows from shared memory.
+#ifndef FNO_MIX_TMA_EVICT_FIRST
+#define FNO_MIX_TMA_EVICT_FIRST 1
+#endif
 namespace mix2d {
 constexpr int kR = 4;                            // kept modes a CTA
 constexpr int kI = 16;                           // input channels a box
@@ -1182,12 +1185,23 @@ k_mix_tma2d(const __grid_constant__ CUtensorMap wmap, Args a) {
             const int ib = cin < kI ? cin : kI, nbox = (cin + kI - 1) / kI;
             const uint32_t boxb = (uint32_t)kR * 8 * cout * ib;
             tcu::arrive_expect_tx(&bar_w, boxb * nbox);
+#if FNO_MIX_TMA_EVICT_FIRST
+            // the weights are read once a forward: their lines go first from L2
+            const uint64_t pol = tcu::l2_evict_first_policy();
+            for (int k = 0; k < nbox; ++k)
+                asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::"
+                             "complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+                             ::"r"(tc_smem_addr(smem + k * boxb)), "l"(&wmap), "r"(2 * local),
+                               "r"(0), "r"(k * kI), "r"(blk), "r"(tc_smem_addr(&bar_w)), "l"(pol)
+                             : "memory");
+#else
             for (int k = 0; k < nbox; ++k)
                 asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::"
                              "complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
                              ::"r"(tc_smem_addr(smem + k * boxb)), "l"(&wmap), "r"(2 * local),
                                "r"(0), "r"(k * kI), "r"(blk), "r"(tc_smem_addr(&bar_w))
                              : "memory");
+#endif
         }
     }
     __syncthreads();

@@ -853,12 +853,26 @@ constexpr size_t kSmem = (size_t)kStages * kStageBytes + 2 * kXsBytes + 1024;   
 static_assert(kCompute == kMaxC * kR / 2, "one thread per (output, mode pair)");
 }  // namespace mixtma
 
+// A 4-D tile load; the weights are a stream read once a forward, so with
+// FNO_MIX_TMA_EVICT_FIRST their lines are marked first to go from L2 (the kept
+// and mixed modes that the other kernels read back stay)
+#ifndef FNO_MIX_TMA_EVICT_FIRST
+#define FNO_MIX_TMA_EVICT_FIRST 1
+#endif
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
                                             int c2, int c3, uint64_t *bar) {
+#if FNO_MIX_TMA_EVICT_FIRST
+    const uint64_t pol = tcu::l2_evict_first_policy();
+    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+                 ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+                   "r"(tcu::tc_smem_addr(bar)), "l"(pol) : "memory");
+#else
     asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
                  " [%0], [%1, {%2, %3, %4, %5}], [%6];"
                  ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
                    "r"(tcu::tc_smem_addr(bar)) : "memory");
+#endif
 }
 
 template <class C3>
