@@ -149,6 +149,34 @@ __device__ __forceinline__ void plane_col_inverse(const float2 *ys, float2 *zo, 
     }
 }
 
+// The kept modes of a 64-row plane from the column pass's 8-point sums
+// S[t1][q][k] = sum_t2 Z[t1 + 8 t2][k] W_8^{q t2} (ss, a_col_fft's output):
+// with the frequency f = q + 8 f2,
+//   X[f][k] = sum_t1 W_8^{f2 t1} (W_64^{q t1} S[t1][q][k]),
+// an 8-point FFT over t1 per (q, k) after the twiddle, of whose outputs the
+// kept rows need f2 = 0, 1 (f = q, q + 8) and 6, 7 (f = q - 16, q - 8).
+// Thread (q, k) = (tid / 16, tid % 16) so leaves exactly the modes
+// o = tid + 128 m (kept row j = q + 8 m) that it folds: m = 0..3 <-> f2 = 0,
+// 1, 6, 7 -- the same sums as a_kept_mode for these four modes, in
+// 8 + 8 loads and one FFT instead of 4 x 16 loads and 32 products.
+template <class Pl>
+__device__ __forceinline__ void plane_kept_modes(const float2 *ss, Tw tw, float2 (&v)[4]) {
+    constexpr int N = Pl::N0, M1 = Pl::M1, A = Pl::A, B2 = Pl::B2;
+    static_assert(N == 64 && A == 8 && B2 == 8 && Pl::K0 == 32 && Pl::M0 == 16 && M1 * A == kNT,
+                  "64-row plane, 32 kept rows, one (q, k) unit per thread");
+    const int q = threadIdx.x / M1, k = threadIdx.x % M1;
+    float2 u[A];
+#pragma unroll
+    for (int t1 = 0; t1 < A; ++t1)
+        u[t1] = cmul(ss[(t1 * B2 + q) * M1 + k], tw.t0[(q * t1) & (N - 1)]);   // W_64^{q t1}
+    fft::fft_dif<A, -1>(u);                      // output f2 at u[bitrev(f2)]
+    constexpr int lg = fft::ilog2(A);
+    v[0] = u[fft::bitrev(0, lg)];
+    v[1] = u[fft::bitrev(1, lg)];
+    v[2] = u[fft::bitrev(6, lg)];
+    v[3] = u[fft::bitrev(7, lg)];
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -224,11 +252,12 @@ __global__ void __launch_bounds__(kNT, FNO_A3_MIN_BLOCKS) k_phase_a3(Args a) {
         float2 wr[R0];                           // W_R0^{r t} = W_N0^{C0 r t}
 #pragma unroll
         for (int r = 0; r < R0; ++r) wr[r] = twa[(C0 * r * t) & (N0 - 1)];
+        float2 v[QT];
+        plane_kept_modes<Pl>(ss, tw, v);
 #pragma unroll
         for (int q = 0; q < QT; ++q) {
-            const float2 v = a_kept_mode<Pl>(ss, threadIdx.x + q * kNT, 0, tw);
 #pragma unroll
-            for (int r = 0; r < R0; ++r) cmac(acc[r][q], v, wr[r]);
+            for (int r = 0; r < R0; ++r) cmac(acc[r][q], v[q], wr[r]);
         }
         __syncthreads();
     }
