@@ -177,6 +177,35 @@ __device__ __forceinline__ void plane_kept_modes(const float2 *ss, Tw tw, float2
     v[3] = u[fft::bitrev(7, lg)];
 }
 
+// acc += v W_8^m, W_8 = e^{-2 pi i / 8}, for a compile-time m: the even
+// powers are 1, -i, -1, +i (adds and swaps); the odd ones (+-1 +- i) / sqrt 2
+// share s = (v.x + v.y) / sqrt 2 and d = (v.y - v.x) / sqrt 2
+template <int M>
+__device__ __forceinline__ void cmac_w8(float2 &acc, float2 v, float s, float d) {
+    constexpr int m = M & 7;
+    if constexpr (m == 0) { acc.x += v.x; acc.y += v.y; }
+    else if constexpr (m == 2) { acc.x += v.y; acc.y -= v.x; }
+    else if constexpr (m == 4) { acc.x -= v.x; acc.y -= v.y; }
+    else if constexpr (m == 6) { acc.x -= v.y; acc.y += v.x; }
+    else if constexpr (m == 1) { acc.x += s; acc.y += d; }
+    else if constexpr (m == 3) { acc.x += d; acc.y -= s; }
+    else if constexpr (m == 5) { acc.x -= s; acc.y -= d; }
+    else { acc.x -= d; acc.y += s; }
+}
+// the fold of plane t's kept modes into the eight residues, P[r] += v W_8^{r t}
+template <int T, int QT>
+__device__ __forceinline__ void fold_w8(float2 (&acc)[8][QT], const float2 (&v)[QT]) {
+    constexpr float c = 0.70710678118654752f;
+#pragma unroll
+    for (int q = 0; q < QT; ++q) {
+        const float s = c * (v[q].x + v[q].y), d = c * (v[q].y - v[q].x);
+        fft::unroll<0, 8>([&](auto ri) {
+            constexpr int r = decltype(ri)::value;
+            cmac_w8<r * T>(acc[r][q], v[q], s, d);
+        });
+    }
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -249,15 +278,20 @@ __global__ void __launch_bounds__(kNT, FNO_A3_MIN_BLOCKS) k_phase_a3(Args a) {
         float2 *ss = reinterpret_cast<float2 *>(ring + (t % S) * kStage);   // plane t consumed
         a_col_fft<Pl>(zs, ss);
         __syncthreads();
-        float2 wr[R0];                           // W_R0^{r t} = W_N0^{C0 r t}
-#pragma unroll
-        for (int r = 0; r < R0; ++r) wr[r] = twa[(C0 * r * t) & (N0 - 1)];
         float2 v[QT];
         plane_kept_modes<Pl>(ss, tw, v);
-#pragma unroll
-        for (int q = 0; q < QT; ++q) {
-#pragma unroll
-            for (int r = 0; r < R0; ++r) cmac(acc[r][q], v[q], wr[r]);
+        // P_c[r] += v W_R0^{r t}: with t known at compile time in each case the
+        // multipliers are the eighth roots of unity, applied as adds
+        static_assert(R0 == 8, "the fold's cases are the planes t < 8");
+        switch (t) {
+            case 0: fold_w8<0>(acc, v); break;
+            case 1: fold_w8<1>(acc, v); break;
+            case 2: fold_w8<2>(acc, v); break;
+            case 3: fold_w8<3>(acc, v); break;
+            case 4: fold_w8<4>(acc, v); break;
+            case 5: fold_w8<5>(acc, v); break;
+            case 6: fold_w8<6>(acc, v); break;
+            default: fold_w8<7>(acc, v); break;
         }
         __syncthreads();
     }
