@@ -644,6 +644,23 @@ struct Geo3C {
     static constexpr uint32_t kTmemCols = 128;          // two plane accumulators
 };
 
+// tensor memory -> registers, shape .16x32bx2: threads 0..15 read lanes
+// base .. base + 15 at columns col .. col + 15, threads 16..31 the same lanes
+// at columns col + kOff ..
+template <int kOff>
+__device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,"
+                 "%11,%12,%13,%14,%15}, [%16], %17;"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr), "n"(kOff));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 template <class C3>
 constexpr size_t smem_c3_tc() {
     return Geo3C::kSpec + (size_t)C3::NKP * 8 + (size_t)(C3::N0 + C3::N1) * 8 + 1024;
@@ -751,22 +768,23 @@ k_phase_c3_tc(Args a, const void *table) {
     // plane t's rows from accumulator t & 1: with M = 64, sample n sits in lane
     // 32 (n / 16) + n % 16, so warp w reads samples 16 w .., lanes 0..15
     // carrying data
+    // (the .16x32bx2 load: lanes 0..15 of the warp read the 16 data lanes at
+    // rows 16 g .., lanes 16..31 the same lanes 32 rows further on, so every
+    // lane stores and a warp's store covers two rows)
     auto drain = [&](int t) {
-        const int i0 = c + C0 * t, n = 16 * warp + (lane & 15);
-        T *out = dst + (size_t)i0 * N1 * N2 + n;
+        const int i0 = c + C0 * t, n = 16 * warp + (lane & 15), h = lane >> 4;
+        T *out = dst + (size_t)i0 * N1 * N2 + (size_t)(32 * h) * N2 + n;
         const uint32_t acc = tmem + (uint32_t)(64 * (t & 1)) + ((uint32_t)(32 * warp) << 16);
 #pragma unroll
-        for (int g = 0; g < N1 / 16; ++g) {
+        for (int g = 0; g < N1 / 32; ++g) {
             float v[16];
-            tmem_ld16(acc + 16 * g, v);          // rows 16 g .. 16 g + 15
+            tmem_ld16x2<32>(acc + 16 * g, v);    // rows 16 g + 32 h + i
             if (!ok) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] = 0.f;
             }
-            if (lane < 16) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) Io<T>::store(out + (size_t)(16 * g + i) * N2, v[i]);
-            }
+            for (int i = 0; i < 16; ++i) Io<T>::store(out + (size_t)(16 * g + i) * N2, v[i]);
         }
     };
 #pragma unroll 1
