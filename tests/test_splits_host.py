@@ -83,3 +83,38 @@ def test_a_wrong_split_fails():
     got = split_inverse(v, n, m, g1n)
     wrong = got.reshape(n // g1n, g1n, -1).transpose(1, 0, 2).reshape(n, -1)
     assert np.max(np.abs(wrong - ref)) > 1e-3 * np.max(np.abs(ref))
+
+
+def test_plane_kept_modes_by_two_8_point_ffts():
+    # the 64-row plane of the 3-D forward transform: S[t1][q] = sum_t2 Z[t1 + 8 t2]
+    # W_8^{q t2}, then per (q, k) one more 8-point FFT over t1 after the twiddle
+    # W_64^{q t1}; output f2 is frequency f = q + 8 f2, and the kept rows
+    # j = q + 8 m (m = 0..3) are f2 = 0, 1, 6, 7
+    n, m = 64, 16
+    rng = np.random.default_rng(11)
+    z = rng.standard_normal((n, 4)) + 1j * rng.standard_normal((n, 4))
+    ref = direct_forward(z, n, m)                               # [32 kept rows][4]
+    s = np.stack([np.fft.fft(z[t1::8], axis=0) for t1 in range(8)])   # [t1][q][k]
+    got = np.zeros_like(ref)
+    for q in range(8):
+        u = s[:, q, :] * np.exp(-2j * np.pi * q * np.arange(8) / n)[:, None]
+        x = np.fft.fft(u, axis=0)                               # [f2][k]
+        for mm, f2 in enumerate((0, 1, 6, 7)):
+            j = q + 8 * mm
+            assert (q + 8 * f2) % n == kept_freq(j, m) % n
+            got[j] = x[f2]
+    assert np.max(np.abs(got - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+def test_eighth_roots_as_adds():
+    # acc += v W_8^m for the eight m, W_8 = exp(-2 pi i / 8): the even powers
+    # as swaps and signs, the odd ones from s = (re + im)/sqrt 2 and
+    # d = (im - re)/sqrt 2, as the fold of the 3-D forward transform applies them
+    rng = np.random.default_rng(3)
+    v = complex(rng.standard_normal(), rng.standard_normal())
+    s, d = (v.real + v.imag) / np.sqrt(2), (v.imag - v.real) / np.sqrt(2)
+    table = {0: (v.real, v.imag), 1: (s, d), 2: (v.imag, -v.real), 3: (d, -s),
+             4: (-v.real, -v.imag), 5: (-s, -d), 6: (-v.imag, v.real), 7: (-d, s)}
+    for mm in range(8):
+        ref = v * np.exp(-2j * np.pi * mm / 8)
+        assert abs(complex(*table[mm]) - ref) <= 1e-12 * abs(v)
