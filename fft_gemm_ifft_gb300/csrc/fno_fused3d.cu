@@ -306,19 +306,24 @@ __global__ void __launch_bounds__(kNT, FNO_A3_MIN_BLOCKS) k_phase_a3(Args a) {
     cluster_sync();
     const uint32_t local = smem_addr(pm);
     float2 *X = a.part + (size_t)vol * C3::NK;
+    // X[f] = sum_cc W_64^{f cc} P_cc[r] for the kept rows of residue r: with
+    // f = r + 8 f2 an 8-point FFT over cc after the twiddle W_64^{r cc}, whose
+    // outputs f2 = 0, 1, 6, 7 are the kept rows r, r + 8, r + 16, r + 24
+    static_assert(C0 == 8 && R0 == 8 && C3::KR == 4 && N0 == 64 && C3::M0 == 16,
+                  "64 planes, 8 chunks, 32 kept rows");
     for (int u = threadIdx.x; u < R0 * C3::kCols; u += kNT) {
         const int r = u / C3::kCols, col = c * C3::kCols + u % C3::kCols;
         float2 v[C0];
 #pragma unroll
-        for (int cc = 0; cc < C0; ++cc) v[cc] = ld_dsmem(local + (uint32_t)(r * NKP + col) * 8, cc);
+        for (int cc = 0; cc < C0; ++cc)
+            v[cc] = cmul(ld_dsmem(local + (uint32_t)(r * NKP + col) * 8, cc),
+                         twa[(r * cc) & (N0 - 1)]);
+        fft::fft_dif<C0, -1>(v);                 // output f2 at v[bitrev(f2)]
+        constexpr int lg = fft::ilog2(C0);
+        constexpr int kF2[4] = {0, 1, 6, 7};
 #pragma unroll
-        for (int m = 0; m < C3::KR; ++m) {
-            const int j0 = r + R0 * m, f0 = freq0<C3>(j0);
-            float2 s = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int cc = 0; cc < C0; ++cc) cmac(s, v[cc], twa[(f0 * cc) & (N0 - 1)]);
-            __stcg(X + (size_t)j0 * NKP + col, s);
-        }
+        for (int m = 0; m < C3::KR; ++m)
+            __stcg(X + (size_t)(r + R0 * m) * NKP + col, v[fft::bitrev(kF2[m], lg)]);
     }
     cluster_sync();                              // peers may still read this CTA's residues
     cta_record(a, 0, 0, t0, t0, t_planes);       // compute: the planes, tail: the combine
